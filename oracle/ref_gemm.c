@@ -1,0 +1,144 @@
+/*
+ * CPU oracle for the tiled fp32 matrix multiply.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the library's product path may
+ * include, link, load or call this file; only the tests, the smoke check and
+ * the benchmark's CPU-baseline leg use it.  It shares no code, header or
+ * constant with the CUDA kernels.
+ *
+ * What it computes is the plain definition of the product the pages' tiled
+ * kernels compute ("My Triton From Scratch, Part 14: Shared Memory Tiles",
+ * section "Shared buffers are physical storage": dot(block<BMxBK>,
+ * block<BKxBN>) -> block<BMxBN>, accumulated over the runtime K loop of
+ * section "Staging inside a runtime K loop").  Masked, zero-filled edge
+ * tiles contribute nothing ("Matching the safety mask": an out-of-bounds
+ * element must contribute nothing), so the tiled result is, up to rounding
+ * order, the untiled textbook product:
+ *
+ *     C[i][j] = fp32( sum_{k=0}^{K-1} (double)A[i][k] * (double)B[k][j] )
+ *
+ * with A row-major M x K (row stride K), B row-major K x N (row stride N)
+ * and C row-major M x N (row stride N), as in the canonical A and B loads of
+ * section "The canonical source pattern" (a + rows*K + cols, b + rows*N +
+ * cols).  The sum runs in increasing k in double precision and is rounded
+ * once to fp32 (round to nearest even, the C cast).  Each product of two
+ * floats is exact in double.  The accumulator starts at zero
+ * (tl.zeros in "Staging inside a runtime K loop"), so K == 0 gives C = 0.
+ *
+ * Alongside C it can return W[i][j] = sum_k |A[i][k]| * |B[k][j]| in double,
+ * the scale the elementwise tolerance of the parity tests is measured in.
+ *
+ * No blocking, no reordering of the k sum: the loops are i, then k, then j,
+ * which keeps each C[i][j]'s sum in increasing k while streaming rows of B.
+ * Rows are independent and split over OpenMP threads.
+ *
+ * Build: gcc -O2 -fno-fast-math -ffp-contract=off -fopenmp -fPIC -shared
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* One output row i: acc[j] = sum_k A[i][k]*B[k][j] (and wacc for W). */
+static void oracle_row(const float *A, const float *B, int64_t N, int64_t K,
+                       int64_t i, double *acc, double *wacc,
+                       float *c_row, double *w_row)
+{
+    for (int64_t j = 0; j < N; ++j) {
+        acc[j] = 0.0;
+        if (wacc) wacc[j] = 0.0;
+    }
+    for (int64_t k = 0; k < K; ++k) {
+        const double a = (double)A[i * K + k];
+        const float *b_row = B + k * N;
+        for (int64_t j = 0; j < N; ++j)
+            acc[j] += a * (double)b_row[j];
+        if (wacc) {
+            const double aa = fabs(a);
+            for (int64_t j = 0; j < N; ++j)
+                wacc[j] += aa * fabs((double)b_row[j]);
+        }
+    }
+    for (int64_t j = 0; j < N; ++j) {
+        c_row[j] = (float)acc[j];
+        if (w_row) w_row[j] = wacc[j];
+    }
+}
+
+/* Every row listed in rows[0..nrows): C_out[r][*] is row rows[r] of A*B.
+ * rows == NULL means rows 0..nrows-1 (the full product when nrows == M).
+ * W_out may be NULL.  nthreads <= 0 uses the OpenMP default.
+ * Returns 0, or -1 on a bad argument or allocation failure. */
+int oracle_sgemm_rows(const float *A, const float *B, float *C_out,
+                      double *W_out, int64_t M, int64_t N, int64_t K,
+                      const int64_t *rows, int64_t nrows, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || nrows < 0) return -1;
+    if (nrows == 0 || N == 0) return 0;
+    int failed = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads) reduction(|:failed)
+#endif
+    {
+        double *acc = (double *)malloc((size_t)N * sizeof(double));
+        double *wacc = W_out ? (double *)malloc((size_t)N * sizeof(double)) : NULL;
+        if (!acc || (W_out && !wacc)) {
+            failed = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+            for (int64_t r = 0; r < nrows; ++r) {
+                const int64_t i = rows ? rows[r] : r;
+                if (i < 0 || i >= M) { failed = 1; continue; }
+                oracle_row(A, B, N, K, i, acc, wacc, C_out + r * N,
+                           W_out ? W_out + r * N : NULL);
+            }
+        }
+        free(acc);
+        free(wacc);
+    }
+    return failed ? -1 : 0;
+}
+
+/* The full product: C (M x N) and optionally W (M x N). */
+int oracle_sgemm(const float *A, const float *B, float *C, double *W,
+                 int64_t M, int64_t N, int64_t K, int nthreads)
+{
+    return oracle_sgemm_rows(A, B, C, W, M, N, K, NULL, M, nthreads);
+}
+
+/* Single elements: out[t] = C[ii[t]][jj[t]], wout[t] = W[ii[t]][jj[t]]
+ * (wout may be NULL).  Same per-element sum as oracle_sgemm. */
+int oracle_sgemm_elements(const float *A, const float *B, float *out,
+                          double *wout, int64_t M, int64_t N, int64_t K,
+                          const int64_t *ii, const int64_t *jj, int64_t count)
+{
+    if (M < 0 || N < 0 || K < 0 || count < 0) return -1;
+    for (int64_t t = 0; t < count; ++t) {
+        const int64_t i = ii[t], j = jj[t];
+        if (i < 0 || i >= M || j < 0 || j >= N) return -1;
+        double acc = 0.0, w = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double a = (double)A[i * K + k];
+            const double b = (double)B[k * N + j];
+            acc += a * b;
+            w += fabs(a) * fabs(b);
+        }
+        out[t] = (float)acc;
+        if (wout) wout[t] = w;
+    }
+    return 0;
+}
+
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,79 @@
+"""Plants plausible mistakes in a copy of the oracle and checks the pins catch them.
+
+Each mutant is a one-line edit of a private copy of ``oracle/ref_gemm.c``
+(the committed oracle is untouched), built with the oracle's own flags and
+run against ``test_oracle_pins.py`` in a child process, so a mutant that
+reads out of bounds cannot take the test run down with it.  Every mutant
+must make the pins fail.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "ref_gemm.c")
+
+MUTANTS = {
+    "dropped_last_k_term": (
+        "for (int64_t k = 0; k < K; ++k) {\n        const double a = (double)A[i * K + k];",
+        "for (int64_t k = 0; k + 1 < K; ++k) {\n        const double a = (double)A[i * K + k];"),
+    "wrong_sign": ("acc[j] += a * (double)b_row[j];",
+                   "acc[j] -= a * (double)b_row[j];"),
+    "wrong_leading_dim_b": ("const float *b_row = B + k * N;",
+                            "const float *b_row = B + k * K;"),
+    "transposed_a_index": ("const double a = (double)A[i * K + k];\n        const float *b_row",
+                           "const double a = (double)A[k * M_ + i];\n        const float *b_row"),
+    "fp32_accumulation": ("acc[j] += a * (double)b_row[j];",
+                          "acc[j] = (float)((float)acc[j] + (float)(a * (double)b_row[j]));"),
+    "shifted_output_column": ("c_row[j] = (float)acc[j];",
+                              "c_row[j] = (float)acc[j > 0 ? j - 1 : 0];"),
+    "w_without_abs": ("wacc[j] += aa * fabs((double)b_row[j]);",
+                      "wacc[j] += aa * (double)b_row[j];"),
+    "elements_transposed_b": ("const double b = (double)B[k * N + j];",
+                              "const double b = (double)B[j * K + k];"),
+}
+
+
+def _mutate(name, tmp_path):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"mutation site for {name} not unique"
+    text = text.replace(old, new)
+    if "M_" in new:  # the transposed index needs M inside oracle_row
+        text = text.replace("static void oracle_row(const float *A, const float *B, int64_t N, int64_t K,",
+                            "static int64_t M_ = 1;\nstatic void oracle_row(const float *A, const float *B, int64_t N, int64_t K,")
+        text = text.replace("if (nrows == 0 || N == 0) return 0;",
+                            "if (nrows == 0 || N == 0) return 0;\n    M_ = M;")
+    src = tmp_path / f"{name}.c"
+    src.write_text(text)
+    return oracle.build(force=True, src=str(src), out=str(tmp_path / f"lib{name}.so"))
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    lib = _mutate(name, tmp_path)
+    env = dict(os.environ, MT_ORACLE_LIB=lib, OMP_NUM_THREADS="2")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p",
+                        "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
+
+
+def test_unmutated_copy_passes(tmp_path):
+    # Control: the same procedure without an edit must pass.
+    src = tmp_path / "same.c"
+    src.write_text(open(SRC).read())
+    lib = oracle.build(force=True, src=str(src), out=str(tmp_path / "libsame.so"))
+    env = dict(os.environ, MT_ORACLE_LIB=lib, OMP_NUM_THREADS="2")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p",
+                        "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:]

@@ -1,0 +1,266 @@
+"""Pins the CPU oracle to facts that do not come from the oracle itself.
+
+Each check is chosen so that a plausible slip in the oracle (a dropped term,
+a wrong sign, a wrong index or leading dimension, a transposed operand,
+fp32 instead of fp64 accumulation) fails at least one of them;
+``test_oracle_mutants.py`` plants such slips and confirms it.
+
+Setting MT_ORACLE_LIB runs these pins against another build of the oracle
+(the mutant test uses that).
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import smem_rules as R
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+LIB = oracle.load(os.environ.get("MT_ORACLE_LIB") or None)
+
+
+def gemm(A, B, **kw):
+    return oracle.sgemm(A, B, lib=LIB, **kw)
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def rng(seed):
+    return np.random.default_rng(seed)
+
+
+# --- exact special cases ------------------------------------------------------
+@pytest.mark.parametrize("M,K", [(37, 29), (5, 64), (64, 3)])
+def test_identity_right_and_left(M, K):
+    A = rng(1).standard_normal((M, K)).astype(np.float32)
+    assert np.array_equal(gemm(A, np.eye(K, dtype=np.float32)), A)
+    assert np.array_equal(gemm(np.eye(M, dtype=np.float32), A), A)
+
+
+@pytest.mark.parametrize("M,N,K", [(23, 17, 11), (8, 40, 8)])
+def test_permutation_rows_and_columns(M, N, K):
+    g = rng(2)
+    B = g.standard_normal((K, N)).astype(np.float32)
+    perm = g.permutation(K)
+    P = np.zeros((K, K), np.float32)
+    P[np.arange(K), perm] = 1.0          # (P @ B)[r] = B[perm[r]]
+    assert np.array_equal(gemm(P, B), B[perm])
+    A = g.standard_normal((M, K)).astype(np.float32)
+    Q = np.zeros((K, K), np.float32)
+    Q[perm, np.arange(K)] = 1.0          # (A @ Q)[:, c] = A[:, perm[c]]
+    assert np.array_equal(gemm(A, Q), A[:, perm])
+
+
+@pytest.mark.parametrize("M,N,K", [(13, 7, 5), (33, 65, 17), (64, 48, 200),
+                                   (1, 9, 31), (9, 1, 2)])
+def test_small_integers_exact(M, N, K):
+    # Entries in [-8, 8]: every partial sum is an integer far below 2**24,
+    # so the exact integer product (numpy int64 matmul) is the answer.
+    g = rng(3)
+    Ai = g.integers(-8, 9, (M, K))
+    Bi = g.integers(-8, 9, (K, N))
+    C = gemm(Ai.astype(np.float32), Bi.astype(np.float32))
+    assert np.array_equal(C.astype(np.int64), Ai @ Bi)
+
+
+def test_rank_one_closed_form():
+    # A[i,k] = x_i, B[k,j] = y_j  ->  C[i,j] = K * x_i * y_j exactly.
+    M, N, K = 6, 5, 12
+    x = np.array([1, -2, 3, 0.5, -0.25, 7], np.float32)
+    y = np.array([2, -1, 0.5, 4, -8], np.float32)
+    A = np.repeat(x[:, None], K, axis=1)
+    B = np.repeat(y[None, :], K, axis=0)
+    assert np.array_equal(gemm(A, B), (K * x[:, None] * y[None, :]).astype(np.float32))
+
+
+def test_k_zero_gives_zeros():
+    # The accumulator starts at zero (tl.zeros) and the K loop runs no trip.
+    C = gemm(np.zeros((4, 0), np.float32), np.zeros((0, 3), np.float32))
+    assert C.shape == (4, 3) and np.all(C == 0) and not np.signbit(C).any()
+
+
+def test_w_is_abs_product():
+    # W = |A|*|B| with |entries| = 1 and random signs -> W = K everywhere,
+    # while C is the signed sum.
+    g = rng(4)
+    M, N, K = 9, 10, 21
+    A = g.choice([-1.0, 1.0], (M, K)).astype(np.float32)
+    B = g.choice([-1.0, 1.0], (K, N)).astype(np.float32)
+    C, W = gemm(A, B, with_w=True)
+    assert np.all(W == K)
+    assert np.array_equal(C.astype(np.int64),
+                          A.astype(np.int64) @ B.astype(np.int64))
+
+
+def test_fp64_accumulation():
+    # 2**24 + 1 - 2**24 summed left to right: fp32 accumulation gives 0,
+    # the double accumulation the oracle uses gives 1.
+    A = np.array([[2.0 ** 24, 1.0, -(2.0 ** 24)]], np.float32)
+    B = np.ones((3, 1), np.float32)
+    assert gemm(A, B)[0, 0] == 1.0
+
+
+# --- brute force on tiny ragged shapes -----------------------------------------
+SHAPES = [(1, 1, 1), (3, 5, 7), (9, 2, 16), (15, 17, 16), (16, 16, 17),
+          (17, 15, 33), (31, 33, 9), (33, 31, 32), (2, 65, 5), (63, 3, 8)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_brute_force_tiny(M, N, K):
+    """Exact rational sum, rounded once, versus the oracle.
+
+    The oracle's double sum differs from the exact sum by at most
+    K * 2**-53 * W; after one rounding to fp32 the result is within one
+    fp32 half-ulp of the exact value plus that amount.
+    """
+    g = rng(5 + M * 1000 + N * 10 + K)
+    A = g.uniform(-1, 1, (M, K)).astype(np.float32)
+    B = g.uniform(-1, 1, (K, N)).astype(np.float32)
+    C, W = gemm(A, B, with_w=True)
+    for i in range(M):
+        for j in range(N):
+            exact = sum((Fraction(float(A[i, k])) * Fraction(float(B[k, j]))
+                         for k in range(K)), Fraction(0))
+            e = float(exact)
+            bound = (abs(e) * 2.0 ** -24 + K * 2.0 ** -52 * W[i, j]
+                     + 2.0 ** -149)
+            assert abs(float(C[i, j]) - e) <= bound, (i, j)
+            assert math.isclose(W[i, j], sum(abs(float(A[i, k])) *
+                                             abs(float(B[k, j]))
+                                             for k in range(K)),
+                                rel_tol=1e-12, abs_tol=0.0)
+
+
+def test_second_opinion_float64_library_matmul():
+    # A library routine as a second opinion: float64 matmul then one rounding.
+    g = rng(6)
+    A = g.standard_normal((70, 130)).astype(np.float32)
+    B = g.standard_normal((130, 90)).astype(np.float32)
+    C, W = gemm(A, B, with_w=True)
+    ref = (A.astype(np.float64) @ B.astype(np.float64))
+    assert np.all(np.abs(C - ref) <= np.abs(ref) * 2.0 ** -24 + 1e-12 * W)
+
+
+# --- zero-fill invariant ("Matching the safety mask") ------------------------
+def test_zero_padding_changes_nothing():
+    # Padding K (and M, N) with zeros up to tile multiples leaves every real
+    # output bit-identical: the zero-filled elements contribute nothing.
+    g = rng(7)
+    M, N, K = 13, 10, 21
+    A = g.standard_normal((M, K)).astype(np.float32)
+    B = g.standard_normal((K, N)).astype(np.float32)
+    Ap = np.zeros((16, 32), np.float32)
+    Ap[:M, :K] = A
+    Bp = np.zeros((32, 16), np.float32)
+    Bp[:K, :N] = B
+    Cp = gemm(Ap, Bp)
+    assert np.array_equal(Cp[:M, :N], gemm(A, B))
+    assert np.all(Cp[M:, :] == 0) and np.all(Cp[:, N:] == 0)
+
+
+def test_rows_and_elements_agree_with_full():
+    g = rng(8)
+    A = g.standard_normal((40, 33)).astype(np.float32)
+    B = g.standard_normal((33, 27)).astype(np.float32)
+    C, W = gemm(A, B, with_w=True)
+    rows = [39, 0, 17]
+    Cr, Wr = oracle.sgemm_rows(A, B, rows, with_w=True, lib=LIB)
+    assert np.array_equal(Cr, C[rows]) and np.array_equal(Wr, W[rows])
+    ii, jj = np.array([0, 39, 5]), np.array([26, 0, 13])
+    e, w = oracle.sgemm_elements(A, B, ii, jj, lib=LIB)
+    assert np.array_equal(e, C[ii, jj]) and np.allclose(w, W[ii, jj], rtol=1e-15)
+
+
+# --- the pages' rules (smem_rules) -------------------------------------------
+def test_padding_rule_worked_examples():
+    data = golden("padding_rule_examples.json")
+    for c in data["cases"]:
+        assert R.row_padding(c["columns"], c["simultaneous_rows"]) == c["padding"], c
+
+
+def test_bank_mapping_example():
+    data = golden("bank_mapping.json")
+    for key in ("unpadded", "padded"):
+        got = R.column_banks(data[key]["row_stride"], data["rows"], data["column"])
+        assert list(got) == data[key]["banks"]
+
+
+def test_bank_simulator_matches_example_and_textbook_cases():
+    data = golden("bank_mapping.json")
+    # Four rows read column 0; lanes 8r..8r+7 share row r (a broadcast).
+    for key, expect in (("unpadded", 2), ("padded", 1)):
+        stride = data[key]["row_stride"]
+        addrs = [4 * ((lane // 8) * stride) for lane in range(32)]
+        assert R.conflict_degree(addrs, 4) == expect
+    # 32 lanes down one column of a 32-wide row-major tile: 32-way conflict;
+    # one padding word per row removes it (skills page, step 4).
+    assert R.conflict_degree([4 * 32 * t for t in range(32)], 4) == 32
+    assert R.conflict_degree([4 * 33 * t for t in range(32)], 4) == 1
+    # All lanes on one word: broadcast, one transaction.
+    assert R.wavefronts([128] * 32, 4) == 1
+    # Consecutive float4 per lane: 4 phases of 8 lanes, none conflicted.
+    addrs = [16 * t for t in range(32)]
+    assert R.wavefronts(addrs, 16) == R.ideal_wavefronts(addrs, 16) == 4
+
+
+def test_layout_examples():
+    data = golden("layout_examples.json")
+    sm = data["stage_mapping"]
+    assert [R.dot_stage(k, sm["bk"]) for k in sm["k_base"]] == sm["stage"]
+    for b in data["buffers"]:
+        buf = R.SharedBuffer(b["rows"], b["columns"])
+        assert buf.size == b["floats"]
+        counts = [len(R.cooperative_indices(t, b["rows"], b["columns"], b["threads"]))
+                  for t in range(b["threads"])]
+        assert set(counts) == {b["per_thread"]}
+        seen = sorted(p for t in range(b["threads"])
+                      for p in R.cooperative_indices(t, b["rows"], b["columns"],
+                                                     b["threads"]))
+        assert seen == [(r, c) for r in range(b["rows"]) for c in range(b["columns"])]
+    pa = data["padded_a"]
+    buf = R.SharedBuffer(pa["rows"], pa["columns"], pa["row_padding"], 2)
+    assert buf.row_stride == pa["row_stride"]
+    assert buf.stage_size == pa["rows"] * pa["row_stride"]
+    assert buf.size == 2 * buf.stage_size and buf.nbytes == 4 * buf.size
+    assert buf.element(1, 2, 3) == buf.stage_size + 2 * pa["row_stride"] + 3
+
+
+def test_layout_rejects_invalid():
+    for bad in [(0, 4), (4, 0), (-1, 4)]:
+        with pytest.raises(ValueError):
+            R.SharedBuffer(*bad)
+    with pytest.raises(ValueError):
+        R.SharedBuffer(4, 16, row_padding=-1)
+    with pytest.raises(ValueError):
+        R.SharedBuffer(4, 16, stage_count=0)
+    buf = R.SharedBuffer(4, 16, 1, 2)
+    for coord in [(2, 0, 0), (0, 4, 0), (0, 0, 16), (-1, 0, 0)]:
+        with pytest.raises(ValueError):
+            buf.element(*coord)
+
+
+def test_budget_formula():
+    limit = golden("layout_examples.json")["budget_limit_bytes"]
+    # The pages' own example tile (BM=4, BK=16, BN=8, one padding word).
+    assert R.two_stage_pair_bytes(4, 16, 8, 1) == 2 * (4 * 17 + 16 * 8) * 4
+    assert R.fits_budget(R.two_stage_pair_bytes(4, 16, 8, 1), limit)
+    # A 128x128 tile with BK=32 does not fit 48 KiB with two stages.
+    assert not R.fits_budget(R.two_stage_pair_bytes(128, 32, 128, 1), limit)
+    # Equality is allowed: the check is required <= limit.
+    assert R.fits_budget(limit, limit) and not R.fits_budget(limit + 1, limit)
+
+
+def test_vector_rule_reduces_to_scalar_rule_on_slots():
+    # Our float4 reading counts 16-byte slots: a row of 4*c words is c slots,
+    # 8 slots in all; it must agree with the scalar rule on a 8-bank machine.
+    for cols in (4, 8, 12, 16, 20, 32, 36, 64):
+        for rows in (1, 2, 4, 8):
+            slots = 8 // math.gcd(cols // 4, 8)
+            assert R.vector_row_padding(cols, rows) == 4 * int(rows > slots)
