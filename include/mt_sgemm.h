@@ -1,0 +1,194 @@
+/*
+ * mt_sgemm — tiled fp32 matrix multiply for one NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of the library (libmtsgemm.so).  Plain pointers and 64-bit sizes
+ * only.  Every entry point returns an mt_status; none of them aborts, traps
+ * or prints.
+ *
+ * The operation (all entry points that compute):
+ *
+ *     C[M,N] = A[M,K] * B[K,N]            fp32 in, fp32 out
+ *
+ * with A, B and C dense row-major: element (i,k) of A at A[i*K + k],
+ * (k,j) of B at B[k*N + j], (i,j) of C at C[i*N + j].  This is the product
+ * `tl.dot` computes in "My Triton From Scratch, Part 14: Shared Memory Tiles"
+ * (section "The canonical source pattern": a + rows*K + columns,
+ * b + rows*N + columns, masks rows < bound & columns < bound, other = 0.0)
+ * accumulated over the runtime K loop of section "Staging inside a runtime K
+ * loop" starting from zeros.  Tiles that straddle M, N or K read 0.0 outside
+ * the matrix, so any M, N, K >= 0 is accepted and C is overwritten (never
+ * accumulated into).  K == 0 writes zeros.  M == 0 or N == 0 does nothing.
+ *
+ * Ownership: every matrix pointer is owned by the caller.  The device entry
+ * points take device-accessible memory and return before the work finishes
+ * (stream-ordered, no implicit synchronisation); errors of the launch itself
+ * come back as MT_ERR_LAUNCH, errors during execution surface at the
+ * caller's next synchronisation.  The library keeps no per-call state; the
+ * only global state is a per-device record of kernel attributes set once.
+ * All entry points are thread-safe.
+ *
+ * There is no CPU fallback: without a usable CUDA device the computing entry
+ * points return MT_ERR_NO_DEVICE.
+ */
+#ifndef MT_SGEMM_H
+#define MT_SGEMM_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define MT_API __attribute__((visibility("default")))
+#else
+#define MT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MT_OK = 0,
+    MT_ERR_INVALID_ARG = 1,   /* negative or too-large size, NULL pointer, bad config */
+    MT_ERR_ALIAS = 2,         /* C overlaps A or B */
+    MT_ERR_NO_DEVICE = 3,     /* no usable CUDA device */
+    MT_ERR_UNSUPPORTED = 4,   /* tile configuration not built into the library */
+    MT_ERR_SMEM_BUDGET = 5,   /* staged tiles do not fit the shared-memory limit */
+    MT_ERR_LAUNCH = 6,        /* the kernel launch was rejected */
+    MT_ERR_TIMEOUT = 7,       /* a kernel gave up waiting (device status word) */
+    MT_ERR_CUDA = 8           /* a CUDA runtime call (copy, allocation, sync) failed */
+} mt_status;
+
+typedef enum {
+    MT_VARIANT_FFMA = 0,      /* CUDA-core FFMA register-tile kernel (default) */
+    MT_VARIANT_TF32X3 = 1,    /* tcgen05 kind::tf32 with the 3xTF32 split */
+    MT_VARIANT_P18 = 2        /* one-warp kernel restating the pages' Version 18 */
+} mt_variant;
+
+/* Optional launch choices.  Zero-initialise for "automatic". */
+typedef struct {
+    int variant;   /* mt_variant */
+    int bm;        /* CTA tile rows (M); 0 = automatic */
+    int bn;        /* CTA tile columns (N); 0 = automatic */
+    int bk;        /* K depth of one staged tile; 0 = automatic */
+    int stages;    /* shared-memory stages in the K pipeline; 0 = automatic */
+    int no_pad;    /* 1 = store rows unpadded (bank-conflict measurements); 0 = padding rule */
+    int split_k;   /* K slices reduced in a second pass; 0 = automatic, 1 = none */
+    int fma;       /* FFMA micro-kernel: 0 = automatic, 1 = scalar fma.rn.f32,
+                      2 = packed fma.rn.f32x2 (same results, fewer issue slots) */
+    int reserved[4];
+} mt_config;
+
+/* What a call with the same arguments would launch. */
+typedef struct {
+    int variant;
+    int bm, bn, bk, stages;
+    int pad_a, pad_b;         /* padding words appended to each shared row of A and B */
+    int threads;              /* threads per CTA */
+    int vec_ab;               /* 1: 16-byte staging of A and B; 0: 4-byte staging */
+    int vec_c;                /* 1: 16-byte stores of C; 0: 4-byte stores */
+    int split_k;              /* K slices (1 = none) */
+    int fma;                  /* 1 scalar, 2 packed (FFMA variant; 0 otherwise) */
+    int64_t grid;             /* CTAs of the main kernel */
+    int64_t smem_bytes;       /* dynamic shared memory per CTA */
+    int64_t workspace_bytes;  /* device scratch the call needs (0 = none) */
+} mt_plan;
+
+/*
+ * C = A*B on `stream` with the default variant and automatic tiling.
+ * A, B, C: device pointers, layouts above.  A and B may be NULL only when
+ * the product has no element that reads them (M*K == 0 or K*N == 0).
+ * Errors: MT_ERR_INVALID_ARG (size < 0 or > INT32_MAX per dimension,
+ * NULL pointer), MT_ERR_ALIAS (C overlaps A or B), MT_ERR_NO_DEVICE,
+ * MT_ERR_SMEM_BUDGET, MT_ERR_LAUNCH.  Nothing is launched on error.
+ */
+MT_API mt_status mt_sgemm(const float *A, const float *B, float *C,
+                   int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/* As mt_sgemm, with explicit choices (cfg == NULL: same as mt_sgemm).
+ * A choice the library was not built for returns MT_ERR_UNSUPPORTED. */
+MT_API mt_status mt_sgemm_ex(const float *A, const float *B, float *C,
+                      int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+                      const mt_config *cfg);
+
+/*
+ * C = A*B with A, B, C in HOST memory (pageable or pinned).  Copies A and B
+ * to the device, multiplies, copies C back and synchronises `stream` before
+ * returning, so on MT_OK the host C holds the result.  Device buffers come
+ * from the stream-ordered pool of the current device and are returned to it
+ * before the call ends.  Errors as mt_sgemm_ex, plus MT_ERR_CUDA when a
+ * copy, allocation or the final synchronisation fails.
+ */
+MT_API mt_status mt_sgemm_host(const float *A, const float *B, float *C,
+                        int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+                        const mt_config *cfg);
+
+/*
+ * Fills *out with the launch a call with these arguments would make,
+ * without launching anything.  A, B, C are only inspected for 16-byte
+ * alignment (they may be NULL, which counts as aligned).  smem_limit_bytes
+ * is the per-CTA dynamic shared-memory limit to check against; <= 0 asks
+ * the current device (MT_ERR_NO_DEVICE without one).  Returns the status the
+ * call itself would return for these sizes and choices.
+ */
+MT_API mt_status mt_sgemm_plan(const float *A, const float *B, const float *C,
+                        int64_t M, int64_t N, int64_t K, const mt_config *cfg,
+                        int64_t smem_limit_bytes, mt_plan *out);
+
+/*
+ * The pages' padding rule ("My Triton From Scratch, Part 18: Shared Memory
+ * Optimization", section "Choosing padding instead of hard-coding it"):
+ * distinct_banks = 32 / gcd(columns, 32); returns 1 when simultaneous_rows
+ * > distinct_banks, else 0.  Returns -1 when columns or simultaneous_rows
+ * is not positive.  Pure host function.
+ */
+MT_API int mt_smem_row_padding(int columns, int simultaneous_rows);
+
+/*
+ * The same rule counted in 16-byte slots, for rows read with float4 loads:
+ * 32 banks form 8 slots, a row of `columns` words spans columns/4 slots;
+ * returns the padding in words (0 or 4).  -1 when columns is not a positive
+ * multiple of 4 or simultaneous_rows is not positive.  Pure host function.
+ */
+MT_API int mt_smem_vector_row_padding(int columns, int simultaneous_rows);
+
+/*
+ * Physical layout of a staged shared tile ("My Triton From Scratch, Part 18",
+ * section "A shared buffer needs a physical row stride"): row_stride =
+ * columns + row_padding, stage_size = rows * row_stride, size = stage_count *
+ * stage_size elements, nbytes = 4 * size.  The kernels address their shared
+ * tiles through the same structure.
+ */
+typedef struct {
+    int rows, columns, row_padding, stage_count;
+    int row_stride, stage_size, size;
+    int64_t nbytes;
+} mt_smem_layout;
+
+/* Fills *out; MT_ERR_INVALID_ARG for non-positive rows, columns or
+ * stage_count, or negative padding.  Pure host function. */
+MT_API mt_status mt_smem_layout_make(int rows, int columns, int row_padding,
+                              int stage_count, mt_smem_layout *out);
+
+/* Element offset stage*stage_size + row*row_stride + column, or -1 when the
+ * coordinate lies outside the logical tile.  Pure host function. */
+MT_API int64_t mt_smem_layout_offset(const mt_smem_layout *layout, int stage, int row,
+                              int column);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device: MT_ERR_TIMEOUT if a kernel gave up a bounded wait since
+ * the last check, MT_ERR_CUDA if the synchronisation failed, else MT_OK.
+ */
+MT_API mt_status mt_device_status(cudaStream_t stream);
+
+/* Static English name of a status code. */
+MT_API const char *mt_status_string(mt_status status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+MT_API int mt_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MT_SGEMM_H */

@@ -1,0 +1,213 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+* the library loads and exports every function include/mt_sgemm.h declares;
+* the library's padding rule, vector rule and staged layout agree with the
+  oracle's restatement of the pages (oracle/smem_rules.py), which is pinned
+  to the pages' worked examples in test_oracle_pins.py;
+* the tile plans the library would launch keep every shared-memory access
+  conflict-free under the oracle's bank simulator, and the unpadded plans
+  show the conflict the rule removes;
+* argument errors, aliasing and the shared-memory budget are rejected on the
+  host before anything is launched; without a GPU the computing entry points
+  report MT_ERR_NO_DEVICE (there is no CPU fallback).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import tiled_fp32_gemm_gb300 as mt
+from tiled_fp32_gemm_gb300 import build as mt_build
+from oracle import smem_rules as R
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HAS_GPU = False
+try:
+    import torch
+    HAS_GPU = torch.cuda.is_available()
+except Exception:  # pragma: no cover
+    pass
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    assert mt_build.build() == mt.LIB_PATH
+    return mt.lib()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(mt_\w+)\s*\(", text))
+    return names
+
+
+def test_every_declared_function_is_exported_and_bound():
+    names = declared_functions()
+    assert names, "no declarations found"
+    handle = ctypes.CDLL(mt.LIB_PATH)
+    for n in sorted(names):
+        assert hasattr(handle, n), f"{n} not exported"
+    assert names == set(mt.SIGNATURES), "binding and header disagree"
+    assert mt.mt_version() >= 100
+    assert mt.mt_status_string(mt.MT_ERR_SMEM_BUDGET) == "shared-memory budget exceeded"
+
+
+def test_padding_rule_matches_pages_and_oracle():
+    for c in (1, 2, 3, 4, 5, 7, 8, 12, 16, 17, 24, 31, 32, 33, 48, 64, 96, 128):
+        for r in range(1, 33):
+            assert mt.mt_smem_row_padding(c, r) == R.row_padding(c, r), (c, r)
+    assert mt.mt_smem_row_padding(0, 4) == -1
+    assert mt.mt_smem_row_padding(16, 0) == -1
+
+
+def test_vector_rule_matches_oracle():
+    for c in range(4, 260, 4):
+        for r in range(1, 9):
+            assert mt.mt_smem_vector_row_padding(c, r) == R.vector_row_padding(c, r)
+    assert mt.mt_smem_vector_row_padding(6, 2) == -1
+
+
+def test_layout_matches_oracle():
+    for rows, cols, pad, stages in [(4, 16, 1, 2), (16, 8, 0, 2), (128, 32, 4, 3),
+                                    (32, 128, 0, 4), (1, 1, 0, 1), (7, 5, 3, 5)]:
+        st, L = mt.mt_smem_layout_make(rows, cols, pad, stages)
+        assert st == mt.MT_OK
+        ref = R.SharedBuffer(rows, cols, pad, stages)
+        assert (L.row_stride, L.stage_size, L.size, L.nbytes) == \
+            (ref.row_stride, ref.stage_size, ref.size, ref.nbytes)
+        for s in range(stages):
+            for r in {0, rows - 1, rows // 2}:
+                for c in {0, cols - 1, cols // 2}:
+                    assert mt.mt_smem_layout_offset(L, s, r, c) == ref.element(s, r, c)
+        for bad in [(stages, 0, 0), (0, rows, 0), (0, 0, cols), (-1, 0, 0)]:
+            assert mt.mt_smem_layout_offset(L, *bad) == -1
+    for bad in [(0, 4, 0, 1), (4, 0, 0, 1), (4, 4, -1, 1), (4, 4, 0, 0)]:
+        assert mt.mt_smem_layout_make(*bad)[0] == mt.MT_ERR_INVALID_ARG
+
+
+GB300_SMEM = 232448  # opt-in dynamic shared memory per block on sm_103
+
+
+def plan(M, N, K, limit=GB300_SMEM, **kw):
+    st, p = mt.mt_sgemm_plan(None, None, None, M, N, K,
+                             mt.make_config(**kw) if kw else None, limit)
+    return st, p
+
+
+# Lane layout of each FFMA tile configuration (warp tile WM x WN, thread tile
+# TM x TN; lanes numbered M-fastest), restated from the kernel's description.
+FFMA_LANES = {(128, 128): (32, 64, 8, 8), (128, 256): (64, 64, 8, 16), (64, 64): (32, 32, 8, 4)}
+
+
+def ffma_warp_accesses(p):
+    """Byte addresses of warp 0's shared reads and cp.async writes, per instruction."""
+    WM, WN, TM, TN = FFMA_LANES[(p.bm, p.bn)]
+    LM = WM // TM
+    LN = 32 // LM
+    la = R.SharedBuffer(p.bm, p.bk, p.pad_a, p.stages)
+    lb = R.SharedBuffer(p.bk, p.bn, p.pad_b, p.stages)
+    b_base = la.nbytes
+    reads = []
+    for k4 in range(p.bk // 4):
+        for i in range(TM):
+            reads.append([4 * la.element(0, i * LM + lane % LM, k4 * 4) for lane in range(32)])
+    for k in range(p.bk):
+        for g in range(TN // 4):
+            reads.append([b_base + 4 * lb.element(0, k, g * LN * 4 + (lane // LM) * 4)
+                          for lane in range(32)])
+    writes = []
+    a_chunks, b_chunks = p.bk // 4, p.bn // 4
+    for t in range(p.bm * a_chunks // p.threads):
+        writes.append([4 * la.element(0, (tid + t * p.threads) // a_chunks,
+                                      (tid % a_chunks) * 4) for tid in range(32)])
+    for t in range(p.bk * b_chunks // p.threads):
+        writes.append([b_base + 4 * lb.element(0, (tid + t * p.threads) // b_chunks,
+                                               (tid % b_chunks) * 4) for tid in range(32)])
+    return reads, writes
+
+
+@pytest.mark.parametrize("shape", [(4096, 4096, 4096), (1024, 1024, 1024), (128, 256, 64)])
+@pytest.mark.parametrize("tile", [dict(), dict(bm=128, bn=256), dict(bm=64, bn=64)])
+def test_ffma_layout_is_conflict_free(shape, tile):
+    st, p = plan(*shape, **tile)
+    assert st == mt.MT_OK
+    reads, writes = ffma_warp_accesses(p)
+    for addrs in reads + writes:
+        assert R.conflict_degree(addrs, 16) == 1
+    assert p.pad_b == 0  # B is read as a broadcast: the rule gives no padding
+
+
+def test_ffma_unpadded_layout_conflicts():
+    st, p = plan(4096, 4096, 4096, bm=128, bn=128, bk=32, stages=3, no_pad=True, fma=2)
+    assert st == mt.MT_OK and p.pad_a == 0
+    reads, _ = ffma_warp_accesses(p)
+    assert max(R.conflict_degree(a, 16) for a in reads) > 1
+    st, q = plan(4096, 4096, 4096, bm=128, bn=128, bk=32, stages=3, fma=2)
+    assert q.pad_a == R.vector_row_padding(32, 4) == 4
+
+
+def test_p18_plan_follows_the_pages():
+    st, p = plan(100, 72, 80, variant="p18")
+    assert st == mt.MT_OK
+    assert (p.bm, p.bn, p.bk, p.stages, p.threads) == (4, 8, 16, 2, 32)
+    assert p.pad_a == R.row_padding(16, 4) == 1 and p.pad_b == 0
+    assert p.grid == 25 * 9
+    # Four output rows read A at the same k: stride 17 is conflict-free,
+    # stride 16 is the 2-way conflict of the pages' example.
+    for pad, expect in ((1, 1), (0, 2)):
+        la = R.SharedBuffer(4, 16, pad, 2)
+        addrs = [4 * la.element(0, lane // 8, 5) for lane in range(32)]
+        assert R.conflict_degree(addrs, 4) == expect
+    st, p = plan(100, 72, 80, variant="p18", no_pad=True)
+    assert p.pad_a == 0
+
+
+def test_budget_is_checked_before_launch():
+    # 48 KiB is the pages' conservative budget: the default tile needs more.
+    st, p = plan(4096, 4096, 4096, limit=48 * 1024)
+    assert st == mt.MT_ERR_SMEM_BUDGET
+    assert p.smem_bytes > 48 * 1024
+    # Bytes are the staged layouts' sizes: stages * rows * (cols + pad) * 4.
+    st, p = plan(4096, 4096, 4096)
+    assert p.smem_bytes == (R.SharedBuffer(p.bm, p.bk, p.pad_a, p.stages).nbytes +
+                            R.SharedBuffer(p.bk, p.bn, p.pad_b, p.stages).nbytes)
+    assert mt.mt_sgemm_plan(None, None, None, 64, 64, 64, None, p.smem_bytes - 1,
+                            )[0] in (mt.MT_OK, mt.MT_ERR_SMEM_BUDGET)
+
+
+def test_alignment_selects_staging_width():
+    assert plan(4096, 4096, 4096)[1].vec_ab == 1
+    assert plan(4097, 3001, 2053)[1].vec_ab == 0
+    st, p = mt.mt_sgemm_plan(4, 16, 32, 64, 64, 64, None, GB300_SMEM)  # 4-byte aligned A
+    assert st == mt.MT_OK and p.vec_ab == 0
+
+
+def test_invalid_arguments_rejected_on_host():
+    assert plan(-1, 4, 4)[0] == mt.MT_ERR_INVALID_ARG
+    assert plan(4, 4, 2 ** 31)[0] == mt.MT_ERR_INVALID_ARG
+    assert plan(64, 64, 64, stages=-1)[0] == mt.MT_ERR_INVALID_ARG
+    assert plan(64, 64, 64, bm=96)[0] == mt.MT_ERR_UNSUPPORTED
+    assert plan(64, 64, 64, variant=7)[0] == mt.MT_ERR_INVALID_ARG
+    # Device entry points check arguments before looking for a device.
+    assert mt.mt_sgemm(0, 0, 0, -1, 4, 4, 0) == mt.MT_ERR_INVALID_ARG
+    assert mt.mt_sgemm(4096, 8192, 0, 4, 4, 4, 0) == mt.MT_ERR_INVALID_ARG  # C is NULL
+    # C overlapping A: rejected as aliasing.
+    assert mt.mt_sgemm(1 << 20, 1 << 30, (1 << 20) + 64, 16, 16, 16, 0) == mt.MT_ERR_ALIAS
+    # M == 0 or N == 0 is a no-op.
+    assert mt.mt_sgemm(0, 0, 0, 0, 16, 16, 0) == mt.MT_OK
+
+
+@pytest.mark.skipif(HAS_GPU, reason="checks the no-device path")
+def test_no_cpu_fallback_without_gpu():
+    assert mt.mt_sgemm(1 << 20, 1 << 30, 1 << 34, 16, 16, 16, 0) == mt.MT_ERR_NO_DEVICE
+    import numpy as np
+    a = np.ones((4, 4), np.float32)
+    c = np.zeros((4, 4), np.float32)
+    st = mt.mt_sgemm_host(a.ctypes.data, a.ctypes.data, c.ctypes.data, 4, 4, 4, 0, None)
+    assert st == mt.MT_ERR_NO_DEVICE
+    assert np.all(c == 0)

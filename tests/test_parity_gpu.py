@@ -1,0 +1,249 @@
+"""GPU parity: the CUDA kernels, called through the C ABI, against the CPU oracle.
+
+Tolerances (from the arithmetic, written here): every output of the FFMA and
+P18 kernels is a chain of K fp32 FMAs in increasing k; for inputs of random
+sign its error is a few fp32 ulps of the |A|*|B| scale W, far inside the
+bound |C - C_ref| <= 1e-5 * W that is asserted elementwise.  Integer-valued
+inputs whose partial sums stay below 2**24 have an exact result, so there
+the kernels must match the oracle bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gemm_inputs
+import oracle
+import tiled_fp32_gemm_gb300 as mt
+
+pytestmark = pytest.mark.gpu
+
+FFMA_TOL = 1e-5
+
+# Every FFMA tile configuration the library builds (tile choice, micro-kernel).
+FFMA_CONFIGS = [
+    dict(),                                           # automatic
+    dict(bm=128, bn=128, bk=32, stages=3, fma=2),
+    dict(bm=128, bn=128, bk=32, stages=3, fma=1),
+    dict(bm=128, bn=128, bk=32, stages=4, fma=2),
+    dict(bm=128, bn=256, bk=32, stages=3, fma=2),
+    dict(bm=64, bn=64, bk=32, stages=3, fma=2),
+    dict(bm=128, bn=128, bk=32, stages=3, fma=2, no_pad=True),
+]
+ALL_VARIANTS = FFMA_CONFIGS + [dict(variant="p18"), dict(variant="p18", no_pad=True)]
+
+
+def ids(cfgs):
+    return ["-".join(f"{k}{v}" for k, v in c.items()) or "auto" for c in cfgs]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    from tiled_fp32_gemm_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+    return mt.lib()
+
+
+def run(A, B, **cfg):
+    a = A.cuda()
+    b = B.cuda()
+    c = mt.sgemm(a, b, **cfg)
+    torch.cuda.synchronize()
+    return c.cpu()
+
+
+def assert_within(C, Cref, W, tol, what=""):
+    C = np.asarray(C, np.float64)
+    err = np.abs(C - np.asarray(Cref, np.float64))
+    bound = tol * np.asarray(W, np.float64)
+    bad = err > bound
+    if bad.any():
+        i, j = np.argwhere(bad)[0]
+        pytest.fail(f"{what}: {bad.sum()} outputs outside {tol}*W, first at ({i},{j}): "
+                    f"got {C[i, j]!r} want {Cref[i, j]!r} W={W[i, j]!r}")
+
+
+# --- the small workloads, every variant, full oracle ---------------------------
+@pytest.mark.parametrize("cfg", ALL_VARIANTS, ids=ids(ALL_VARIANTS))
+@pytest.mark.parametrize("name", ["masked_100x72x80", "square_1024"])
+def test_small_workloads_all_variants(name, cfg):
+    if cfg.get("variant") == "p18" and name == "square_1024":
+        pytest.skip("the one-warp kernel is only a parity reference at small sizes")
+    A, B = gemm_inputs.make_workload(name)
+    Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
+    assert_within(run(A, B, **cfg).numpy(), Cref, W, FFMA_TOL, f"{name} {cfg}")
+
+
+def test_ragged_workload_full():
+    # 4097 x 3001 x 2053: every tile edge on M, N and K is masked, and the
+    # odd leading dimensions force the 4-byte staging path.
+    A, B = gemm_inputs.make_workload("ragged_4097x3001x2053")
+    assert mt.plan(4097, 3001, 2053, a=A.cuda(), b=B.cuda())["vec_ab"] == 0
+    Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
+    assert_within(run(A, B).numpy(), Cref, W, FFMA_TOL, "ragged")
+
+
+def sampled_rows(M, bm=128, extra=24, seed=0):
+    """First and last rows, rows around tile edges and a few random rows."""
+    g = np.random.default_rng(seed)
+    rows = {0, M - 1}
+    for t in (1, M // bm // 2, M // bm - 1):
+        for d in (-1, 0):
+            r = t * bm + d
+            if 0 <= r < M:
+                rows.add(r)
+    rows |= set(g.integers(0, M, extra).tolist())
+    return np.array(sorted(rows), np.int64)
+
+
+@pytest.mark.parametrize("name", ["square_4096", "square_8192", "skinny_65536x128x4096"])
+def test_full_size_sampled_rows(name):
+    """The benchmark's workloads in the benchmark's launch configuration."""
+    w = gemm_inputs.WORKLOADS[name]
+    A, B = gemm_inputs.make_workload(w)
+    a, b = A.cuda(), B.cuda()
+    c = mt.sgemm(a, b)  # automatic choice, as the benchmark calls it
+    torch.cuda.synchronize()
+    rows = sampled_rows(w.M, extra=16 if w.N > 4096 else 40)
+    Cr, Wr = oracle.sgemm_rows(A.numpy(), B.numpy(), rows, with_w=True)
+    assert_within(c[torch.from_numpy(rows).cuda()].cpu().numpy(), Cr, Wr, FFMA_TOL, name)
+
+
+# --- exact cases ----------------------------------------------------------------
+@pytest.mark.parametrize("cfg", ALL_VARIANTS, ids=ids(ALL_VARIANTS))
+@pytest.mark.parametrize("shape", [(100, 72, 80), (257, 130, 77), (128, 256, 96)])
+def test_integer_inputs_bit_exact(shape, cfg):
+    M, N, K = shape
+    A, B = gemm_inputs.make_ab(M, N, K, seed=11, dist="int")
+    Cref = oracle.sgemm(A.numpy(), B.numpy())
+    got = run(A, B, **cfg).numpy()
+    assert np.array_equal(got, Cref)
+
+
+@pytest.mark.parametrize("cfg", [dict(), dict(variant="p18")], ids=["ffma", "p18"])
+def test_identity_and_permutation_exact(cfg):
+    g = torch.Generator().manual_seed(5)
+    A = torch.randn(150, 97, generator=g)
+    I = torch.eye(97)
+    assert torch.equal(run(A, I, **cfg), A)
+    perm = torch.randperm(150, generator=g)
+    P = torch.zeros(150, 150)
+    P[torch.arange(150), perm] = 1.0
+    assert torch.equal(run(P, A, **cfg), A[perm])
+
+
+def test_all_variants_agree_bitwise():
+    # Every FFMA/P18 output is the same chain of fp32 FMAs in increasing k,
+    # so every variant must produce the same bits.
+    A, B = gemm_inputs.make_ab(200, 136, 300, seed=12, dist="normal")
+    ref = run(A, B, variant="p18")
+    for cfg in FFMA_CONFIGS:
+        assert torch.equal(run(A, B, **cfg), ref), cfg
+
+
+# --- edge cases ---------------------------------------------------------------------
+TINY = [(1, 1, 1), (1, 7, 3), (5, 1, 9), (3, 5, 7), (16, 16, 16), (17, 15, 33),
+        (31, 33, 1), (33, 31, 32), (63, 65, 31), (129, 127, 64), (130, 258, 33)]
+
+
+@pytest.mark.parametrize("shape", TINY)
+def test_tiny_ragged_shapes(shape):
+    M, N, K = shape
+    A, B = gemm_inputs.make_ab(M, N, K, seed=M * 10000 + N * 100 + K, dist="uniform")
+    Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
+    for cfg in (dict(), dict(bm=128, bn=256, bk=32, stages=3, fma=2), dict(variant="p18")):
+        assert_within(run(A, B, **cfg).numpy(), Cref, W, FFMA_TOL, f"{shape} {cfg}")
+
+
+def test_k_zero_writes_zeros_and_empty_is_noop():
+    c = torch.full((7, 5), float("nan"), device="cuda")
+    a = torch.empty((7, 0), device="cuda")
+    b = torch.empty((0, 5), device="cuda")
+    mt.sgemm(a, b, out=c)
+    torch.cuda.synchronize()
+    assert torch.equal(c.cpu(), torch.zeros(7, 5))
+    c = torch.full((0, 5), 1.0, device="cuda")
+    assert mt.mt_sgemm(0, 0, c.data_ptr(), 0, 5, 3, 0) == mt.MT_OK
+    c = torch.full((4, 4), 3.0, device="cuda")
+    assert mt.mt_sgemm(0, 0, c.data_ptr(), 4, 0, 3, 0) == mt.MT_OK
+    torch.cuda.synchronize()
+    assert torch.all(c == 3.0)
+
+
+@pytest.mark.parametrize("cfg", [dict(), dict(bm=64, bn=64, bk=32, stages=3, fma=2),
+                                 dict(variant="p18")], ids=["auto", "64x64", "p18"])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_guard_bands_and_canaries(cfg, offset):
+    """NaN around A and B catches any unmasked read; sentinels around C catch
+    any stray write.  offset=1 misaligns the operands (4-byte staging)."""
+    M, N, K = 133, 100, 72
+    A, B = gemm_inputs.make_ab(M, N, K, seed=13, dist="uniform")
+    guard = 4096
+    abuf = torch.full((M * K + 2 * guard,), float("nan"))
+    bbuf = torch.full((K * N + 2 * guard,), float("nan"))
+    abuf[guard + offset:guard + offset + M * K] = A.reshape(-1)
+    bbuf[guard + offset:guard + offset + K * N] = B.reshape(-1)
+    sentinel = -12345.0
+    cbuf = torch.full((M * N + 2 * guard,), sentinel, device="cuda")
+    a_d, b_d = abuf.cuda(), bbuf.cuda()
+    pa = a_d.data_ptr() + 4 * (guard + offset)
+    pb = b_d.data_ptr() + 4 * (guard + offset)
+    pc = cbuf.data_ptr() + 4 * (guard + offset)
+    st = mt.mt_sgemm_ex(pa, pb, pc, M, N, K, torch.cuda.current_stream().cuda_stream,
+                        mt.make_config(**cfg))
+    assert st == mt.MT_OK
+    torch.cuda.synchronize()
+    out = cbuf.cpu()
+    C = out[guard + offset:guard + offset + M * N].reshape(M, N).numpy()
+    Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
+    assert np.isfinite(C).all()
+    assert_within(C, Cref, W, FFMA_TOL, "guarded")
+    assert torch.all(out[:guard + offset] == sentinel)
+    assert torch.all(out[guard + offset + M * N:] == sentinel)
+
+
+def test_nan_and_inf_propagate_like_ieee():
+    M, N, K = 40, 36, 50
+    A, B = gemm_inputs.make_ab(M, N, K, seed=14, dist="uniform")
+    A[3, 7] = float("nan")
+    B[11, 5] = float("inf")
+    C = run(A, B).numpy()
+    Cref = oracle.sgemm(A.numpy(), B.numpy())
+    same = (C == Cref) | (np.isnan(C) & np.isnan(Cref))
+    finite = np.isfinite(Cref)
+    assert np.array_equal(np.isnan(C), np.isnan(Cref))
+    assert np.array_equal(np.isinf(C), np.isinf(Cref))
+    assert same[~finite].all()
+
+
+def test_host_buffer_entry_point():
+    A, B = gemm_inputs.make_workload("masked_100x72x80")
+    a = A.numpy()
+    b = B.numpy()
+    c = np.full((100, 72), np.nan, np.float32)
+    st = mt.mt_sgemm_host(a.ctypes.data, b.ctypes.data, c.ctypes.data, 100, 72, 80, 0, None)
+    assert st == mt.MT_OK
+    Cref, W = oracle.sgemm(a, b, with_w=True)
+    assert_within(c, Cref, W, FFMA_TOL, "host")
+
+
+def test_runs_on_caller_stream():
+    A, B = gemm_inputs.make_ab(300, 260, 200, seed=15, dist="normal")
+    s = torch.cuda.Stream()
+    a, b = A.cuda(), B.cuda()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        c = mt.sgemm(a, b)
+    s.synchronize()
+    Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
+    assert_within(c.cpu().numpy(), Cref, W, FFMA_TOL, "stream")
+
+
+def test_alias_rejected_without_launch():
+    a = torch.ones(64, 64, device="cuda")
+    b = torch.ones(64, 64, device="cuda")
+    st = mt.mt_sgemm(a.data_ptr(), b.data_ptr(), a.data_ptr(), 64, 64, 64, 0)
+    assert st == mt.MT_ERR_ALIAS
+    torch.cuda.synchronize()
+    assert torch.all(a == 1.0)
+    assert mt.mt_device_status(0) == mt.MT_OK

@@ -1,0 +1,221 @@
+"""tiled_fp32_gemm_gb300 — fp32 GEMM for one GB300, C ABI plus a thin binding.
+
+The compute lives in ``libmtsgemm.so`` (hand-written CUDA for sm_103a, built
+by ``tiled_fp32_gemm_gb300.build``).  This module only marshals arguments:
+
+* ``mt_sgemm``, ``mt_sgemm_ex``, ``mt_sgemm_host``, ``mt_sgemm_plan``,
+  ``mt_smem_row_padding``, ``mt_smem_vector_row_padding``,
+  ``mt_smem_layout_make``, ``mt_smem_layout_offset``, ``mt_device_status``,
+  ``mt_status_string``, ``mt_version`` — the C entry points under the same
+  names, taking plain integers for pointers and streams;
+* ``sgemm(a, b, out=None, **choices)`` — the same call on torch CUDA tensors
+  (torch supplies device memory and the current stream; nothing else).
+
+There is no CPU fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+
+MT_OK = 0
+MT_ERR_INVALID_ARG = 1
+MT_ERR_ALIAS = 2
+MT_ERR_NO_DEVICE = 3
+MT_ERR_UNSUPPORTED = 4
+MT_ERR_SMEM_BUDGET = 5
+MT_ERR_LAUNCH = 6
+MT_ERR_TIMEOUT = 7
+MT_ERR_CUDA = 8
+
+MT_VARIANT_FFMA = 0
+MT_VARIANT_TF32X3 = 1
+MT_VARIANT_P18 = 2
+VARIANTS = {"ffma": MT_VARIANT_FFMA, "tf32x3": MT_VARIANT_TF32X3, "p18": MT_VARIANT_P18}
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libmtsgemm.so")
+
+
+class mt_config(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("bm", ctypes.c_int), ("bn", ctypes.c_int),
+                ("bk", ctypes.c_int), ("stages", ctypes.c_int), ("no_pad", ctypes.c_int),
+                ("split_k", ctypes.c_int), ("fma", ctypes.c_int),
+                ("reserved", ctypes.c_int * 4)]
+
+
+class mt_plan(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("bm", ctypes.c_int), ("bn", ctypes.c_int),
+                ("bk", ctypes.c_int), ("stages", ctypes.c_int), ("pad_a", ctypes.c_int),
+                ("pad_b", ctypes.c_int), ("threads", ctypes.c_int), ("vec_ab", ctypes.c_int),
+                ("vec_c", ctypes.c_int), ("split_k", ctypes.c_int), ("fma", ctypes.c_int),
+                ("grid", ctypes.c_int64), ("smem_bytes", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class mt_smem_layout(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int), ("columns", ctypes.c_int),
+                ("row_padding", ctypes.c_int), ("stage_count", ctypes.c_int),
+                ("row_stride", ctypes.c_int), ("stage_size", ctypes.c_int),
+                ("size", ctypes.c_int), ("nbytes", ctypes.c_int64)]
+
+
+class MtError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {mt_status_string(status)} (status {status})")
+
+
+_P, _I64, _I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+# name -> (restype, argtypes): every function include/mt_sgemm.h declares.
+SIGNATURES = {
+    "mt_sgemm": (_I, [_P, _P, _P, _I64, _I64, _I64, _P]),
+    "mt_sgemm_ex": (_I, [_P, _P, _P, _I64, _I64, _I64, _P, ctypes.POINTER(mt_config)]),
+    "mt_sgemm_host": (_I, [_P, _P, _P, _I64, _I64, _I64, _P, ctypes.POINTER(mt_config)]),
+    "mt_sgemm_plan": (_I, [_P, _P, _P, _I64, _I64, _I64, ctypes.POINTER(mt_config), _I64,
+                           ctypes.POINTER(mt_plan)]),
+    "mt_smem_row_padding": (_I, [_I, _I]),
+    "mt_smem_vector_row_padding": (_I, [_I, _I]),
+    "mt_smem_layout_make": (_I, [_I, _I, _I, _I, ctypes.POINTER(mt_smem_layout)]),
+    "mt_smem_layout_offset": (_I64, [ctypes.POINTER(mt_smem_layout), _I, _I, _I]),
+    "mt_device_status": (_I, [_P]),
+    "mt_status_string": (ctypes.c_char_p, [_I]),
+    "mt_version": (_I, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"{LIB_PATH} is missing: build it with "
+                        "`python -m tiled_fp32_gemm_gb300.build` (there is no CPU fallback)")
+                handle = ctypes.CDLL(LIB_PATH)
+                for name, (res, args) in SIGNATURES.items():
+                    fn = getattr(handle, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _lib = handle
+    return _lib
+
+
+def make_config(variant="ffma", bm=0, bn=0, bk=0, stages=0, no_pad=False, split_k=0,
+                fma=0) -> mt_config:
+    c = mt_config()
+    c.variant = VARIANTS[variant] if isinstance(variant, str) else int(variant)
+    c.bm, c.bn, c.bk, c.stages = bm, bn, bk, stages
+    c.no_pad = 1 if no_pad else 0
+    c.split_k = split_k
+    c.fma = fma
+    return c
+
+
+# --- the C entry points, same names -----------------------------------------
+def mt_sgemm(A: int, B: int, C: int, M: int, N: int, K: int, stream: int = 0) -> int:
+    return lib().mt_sgemm(A, B, C, M, N, K, stream)
+
+
+def mt_sgemm_ex(A: int, B: int, C: int, M: int, N: int, K: int, stream: int = 0,
+                cfg: mt_config | None = None) -> int:
+    return lib().mt_sgemm_ex(A, B, C, M, N, K, stream,
+                             ctypes.byref(cfg) if cfg is not None else None)
+
+
+def mt_sgemm_host(A: int, B: int, C: int, M: int, N: int, K: int, stream: int = 0,
+                  cfg: mt_config | None = None) -> int:
+    return lib().mt_sgemm_host(A, B, C, M, N, K, stream,
+                               ctypes.byref(cfg) if cfg is not None else None)
+
+
+def mt_sgemm_plan(A: int, B: int, C: int, M: int, N: int, K: int,
+                  cfg: mt_config | None = None, smem_limit_bytes: int = 0):
+    out = mt_plan()
+    st = lib().mt_sgemm_plan(A, B, C, M, N, K,
+                             ctypes.byref(cfg) if cfg is not None else None,
+                             smem_limit_bytes, ctypes.byref(out))
+    return st, out
+
+
+def mt_smem_row_padding(columns: int, simultaneous_rows: int) -> int:
+    return lib().mt_smem_row_padding(columns, simultaneous_rows)
+
+
+def mt_smem_vector_row_padding(columns: int, simultaneous_rows: int) -> int:
+    return lib().mt_smem_vector_row_padding(columns, simultaneous_rows)
+
+
+def mt_smem_layout_make(rows: int, columns: int, row_padding: int, stage_count: int):
+    out = mt_smem_layout()
+    st = lib().mt_smem_layout_make(rows, columns, row_padding, stage_count, ctypes.byref(out))
+    return st, out
+
+
+def mt_smem_layout_offset(layout: mt_smem_layout, stage: int, row: int, column: int) -> int:
+    return lib().mt_smem_layout_offset(ctypes.byref(layout), stage, row, column)
+
+
+def mt_device_status(stream: int = 0) -> int:
+    return lib().mt_device_status(stream)
+
+
+def mt_status_string(status: int) -> str:
+    return lib().mt_status_string(status).decode()
+
+
+def mt_version() -> int:
+    return lib().mt_version()
+
+
+# --- torch convenience (marshalling only) ------------------------------------
+def _check_tensor(t, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda:
+        raise TypeError(f"{name} must be a float32 CUDA tensor")
+    if t.dim() != 2 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D (row-major) tensor")
+
+
+def sgemm(a, b, out=None, stream=None, **choices):
+    """out = a @ b through mt_sgemm_ex on torch tensors (float32, CUDA, row-major)."""
+    import torch
+    _check_tensor(a, "a")
+    _check_tensor(b, "b")
+    M, K = a.shape
+    K2, N = b.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {tuple(a.shape)} x {tuple(b.shape)}")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    else:
+        _check_tensor(out, "out")
+        if tuple(out.shape) != (M, N):
+            raise ValueError("out has the wrong shape")
+    s = stream if stream is not None else torch.cuda.current_stream(a.device).cuda_stream
+    with torch.cuda.device(a.device):
+        st = mt_sgemm_ex(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K, s,
+                         make_config(**choices) if choices else None)
+    if st != MT_OK:
+        raise MtError(st, "mt_sgemm_ex")
+    return out
+
+
+def plan(M: int, N: int, K: int, smem_limit_bytes: int = 0, a=None, b=None, c=None,
+         **choices) -> dict:
+    """mt_sgemm_plan as a dict (raises on a non-OK status)."""
+    ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
+    st, p = mt_sgemm_plan(ptr(a), ptr(b), ptr(c), M, N, K,
+                          make_config(**choices) if choices else None, smem_limit_bytes)
+    if st != MT_OK:
+        raise MtError(st, "mt_sgemm_plan")
+    return p.as_dict()

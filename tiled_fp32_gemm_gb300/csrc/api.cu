@@ -1,0 +1,409 @@
+// Host side of the C ABI: argument checks, variant and tile selection,
+// shared-memory budget, launch, and the pure-host layout helpers.
+#include <atomic>
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "mt_sgemm.h"
+#include "smem_layout.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxEntries = 32;
+
+struct DeviceInfo {
+  int sms = 0;
+  int smem_optin = 0;  // max dynamic shared memory per block with opt-in
+  bool valid = false;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+// [device][entry][vec][pad]: max dynamic shared memory attribute applied.
+std::atomic<uint8_t> g_attr_done[kMaxDevices][kMaxEntries][2][2];
+cudaMemPool_t g_pools[kMaxDevices];
+
+mt_status current_device(int* dev, DeviceInfo* info) {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) {
+    cudaGetLastError();
+    return MT_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo& di = g_devices[d];
+  if (!di.valid) {
+    if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      return MT_ERR_NO_DEVICE;
+    }
+    di.valid = true;
+  }
+  *dev = d;
+  *info = di;
+  return MT_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
+  if (a_bytes <= 0 || b_bytes <= 0 || !a || !b) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + static_cast<uintptr_t>(b_bytes) && b0 < a0 + static_cast<uintptr_t>(a_bytes);
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Everything a launch needs beyond the plan the caller can see.
+struct Launch {
+  mt_plan plan;
+  int entry = -1;  // FFMA table index
+  const void* kern = nullptr;
+  int tiles_m = 0, tiles_n = 0, group_m = 8;
+  bool pad = true;
+};
+
+mt_status check_dims(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+    return MT_ERR_INVALID_ARG;
+  // Every operand must be addressable with 64-bit byte offsets.
+  const int64_t lim = (INT64_MAX / 4) >> 1;
+  if ((M && N > lim / M) || (M && K > lim / M) || (K && N > lim / K)) return MT_ERR_INVALID_ARG;
+  return MT_OK;
+}
+
+mt_status check_args(const float* A, const float* B, const float* C, int64_t M, int64_t N,
+                     int64_t K) {
+  mt_status st = check_dims(M, N, K);
+  if (st != MT_OK) return st;
+  if (M == 0 || N == 0) return MT_OK;
+  if (!C || !aligned4(C)) return MT_ERR_INVALID_ARG;
+  if (K > 0 && (!A || !B || !aligned4(A) || !aligned4(B))) return MT_ERR_INVALID_ARG;
+  const int64_t c_bytes = M * N * 4;
+  if (K > 0 && (overlaps(C, c_bytes, A, M * K * 4) || overlaps(C, c_bytes, B, K * N * 4)))
+    return MT_ERR_ALIAS;
+  return MT_OK;
+}
+
+// Chooses the FFMA table entry.  Explicit bm/bn/bk/stages/fma must all
+// match an entry; otherwise the choice is automatic.
+int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms) {
+  int count = 0;
+  const mt::FfmaEntry* e = mt::ffma_entries(&count);
+  const bool explicit_tile = cfg && (cfg->bm || cfg->bn || cfg->bk || cfg->stages);
+  const int want_packed = cfg && cfg->fma ? (cfg->fma == 2 ? 1 : 0) : 1;
+  if (explicit_tile || (cfg && cfg->fma)) {
+    for (int i = 0; i < count; ++i) {
+      if (cfg->bm && e[i].bm != cfg->bm) continue;
+      if (cfg->bn && e[i].bn != cfg->bn) continue;
+      if (cfg->bk && e[i].bk != cfg->bk) continue;
+      if (cfg->stages && e[i].stages != cfg->stages) continue;
+      if (e[i].packed != want_packed) continue;
+      if (!explicit_tile && !(e[i].bm == 128 && e[i].bn == 128 && e[i].stages == 3)) continue;
+      return i;
+    }
+    return -1;
+  }
+  // Automatic: 128x128 tiles when they fill every SM twice over, else
+  // 64x64 tiles for more CTAs.
+  int big = -1, small = -1;
+  for (int i = 0; i < count; ++i) {
+    if (!e[i].packed) continue;
+    if (e[i].bm == 128 && e[i].bn == 128 && e[i].stages == 3) big = i;
+    if (e[i].bm == 64 && e[i].bn == 64) small = i;
+  }
+  const int64_t tiles_big = ceil_div(M, 128) * ceil_div(N, 128);
+  if (tiles_big >= 2 * static_cast<int64_t>(sms) || small < 0) return big;
+  return small;
+}
+
+mt_status plan_call(const float* A, const float* B, const float* C, int64_t M, int64_t N,
+                    int64_t K, const mt_config* cfg, int64_t smem_limit, int sms,
+                    Launch* L) {
+  // Pointers are only inspected for alignment here (NULL counts as
+  // aligned); the caller checks them against the sizes.
+  mt_status st = check_dims(M, N, K);
+  if (st != MT_OK) return st;
+  const int variant = cfg ? cfg->variant : MT_VARIANT_FFMA;
+  if (cfg && (cfg->bm < 0 || cfg->bn < 0 || cfg->bk < 0 || cfg->stages < 0 ||
+              cfg->no_pad < 0 || cfg->no_pad > 1 || cfg->split_k < 0 || cfg->fma < 0 ||
+              cfg->fma > 2))
+    return MT_ERR_INVALID_ARG;
+  if (cfg && cfg->split_k > 1) return MT_ERR_UNSUPPORTED;
+  const bool pad = !(cfg && cfg->no_pad);
+  mt_plan& p = L->plan;
+  std::memset(&p, 0, sizeof(p));
+  p.variant = variant;
+  p.split_k = 1;
+  p.vec_ab = (K % 4 == 0) && (N % 4 == 0) && aligned16(A) && aligned16(B) && aligned16(C);
+  p.vec_c = p.vec_ab;
+  L->pad = pad;
+
+  if (variant == MT_VARIANT_P18) {
+    if (cfg && ((cfg->bm && cfg->bm != 4) || (cfg->bn && cfg->bn != 8) ||
+                (cfg->bk && cfg->bk != 16) || (cfg->stages && cfg->stages != 2) || cfg->fma))
+      return MT_ERR_UNSUPPORTED;
+    p.bm = 4; p.bn = 8; p.bk = 16; p.stages = 2; p.threads = 32;
+    p.pad_a = mt::p18_pad_a(pad);
+    p.pad_b = 0;
+    p.vec_ab = 0; p.vec_c = 0;
+    p.smem_bytes = 0;  // static shared memory only
+    L->tiles_m = static_cast<int>(ceil_div(M, 4));
+    L->tiles_n = static_cast<int>(ceil_div(N, 8));
+    p.grid = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
+    if (p.grid > INT32_MAX) return MT_ERR_UNSUPPORTED;
+    return MT_OK;
+  }
+  if (variant == MT_VARIANT_TF32X3) return MT_ERR_UNSUPPORTED;
+  if (variant != MT_VARIANT_FFMA) return MT_ERR_INVALID_ARG;
+
+  int count = 0;
+  const mt::FfmaEntry* e = mt::ffma_entries(&count);
+  const int i = pick_ffma(cfg, M, N, sms > 0 ? sms : 1);
+  if (i < 0) return MT_ERR_UNSUPPORTED;
+  const mt::FfmaEntry& E = e[i];
+  if (!E.kern[p.vec_ab][pad ? 1 : 0]) return MT_ERR_UNSUPPORTED;
+  p.bm = E.bm; p.bn = E.bn; p.bk = E.bk; p.stages = E.stages; p.threads = E.threads;
+  p.fma = E.packed ? 2 : 1;
+  p.pad_a = pad ? E.pad_a : 0;
+  p.pad_b = pad ? E.pad_b : 0;
+  p.smem_bytes = E.smem_bytes[pad ? 1 : 0];
+  L->entry = i;
+  L->kern = E.kern[p.vec_ab][pad ? 1 : 0];
+  L->tiles_m = static_cast<int>(ceil_div(M, E.bm));
+  L->tiles_n = static_cast<int>(ceil_div(N, E.bn));
+  p.grid = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
+  if (p.grid > INT32_MAX) return MT_ERR_UNSUPPORTED;
+  // The budget check comes before anything is launched ("Part 18", section
+  // "Shared-memory budget checks include stages and padding").
+  if (p.smem_bytes > smem_limit) return MT_ERR_SMEM_BUDGET;
+  return MT_OK;
+}
+
+mt_status set_smem_attr(int dev, const Launch& L) {
+  if (L.entry < 0 || L.plan.smem_bytes <= 48 * 1024) return MT_OK;
+  std::atomic<uint8_t>& done = g_attr_done[dev][L.entry][L.plan.vec_ab][L.pad ? 1 : 0];
+  if (done.load(std::memory_order_acquire)) return MT_OK;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!done.load(std::memory_order_relaxed)) {
+    if (cudaFuncSetAttribute(L.kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(L.plan.smem_bytes)) != cudaSuccess) {
+      cudaGetLastError();
+      return MT_ERR_LAUNCH;
+    }
+    done.store(1, std::memory_order_release);
+  }
+  return MT_OK;
+}
+
+mt_status run(const float* A, const float* B, float* C, int64_t M, int64_t N, int64_t K,
+              cudaStream_t stream, const mt_config* cfg) {
+  mt_status st = check_args(A, B, C, M, N, K);
+  if (st != MT_OK) return st;
+  if (M == 0 || N == 0) return MT_OK;
+  int dev = 0;
+  DeviceInfo info;
+  st = current_device(&dev, &info);
+  if (st != MT_OK) return st;
+  Launch L;
+  st = plan_call(A, B, C, M, N, K, cfg, info.smem_optin, info.sms, &L);
+  if (st != MT_OK) return st;
+  if (K == 0) {
+    // Empty reduction: the accumulator's zeros are the result.
+    if (cudaMemsetAsync(C, 0, static_cast<size_t>(M * N) * 4, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return MT_ERR_LAUNCH;
+    }
+    return MT_OK;
+  }
+  mt::GemmArgs args{A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                    L.tiles_m, L.tiles_n, L.group_m};
+  if (L.plan.variant == MT_VARIANT_P18) {
+    if (mt::launch_p18(args, L.pad, stream) != cudaSuccess) return MT_ERR_LAUNCH;
+    return MT_OK;
+  }
+  st = set_smem_attr(dev, L);
+  if (st != MT_OK) return st;
+  void* params[] = {&args};
+  if (cudaLaunchKernel(L.kern, dim3(static_cast<unsigned>(L.plan.grid)),
+                       dim3(static_cast<unsigned>(L.plan.threads)), params,
+                       static_cast<size_t>(L.plan.smem_bytes), stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MT_ERR_LAUNCH;
+  }
+  return MT_OK;
+}
+
+mt_status pool_for(int dev, cudaMemPool_t* pool) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_pools[dev]) {
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t p = nullptr;
+    if (cudaMemPoolCreate(&p, &props) != cudaSuccess) {
+      cudaGetLastError();
+      return MT_ERR_CUDA;
+    }
+    // Keep freed blocks for the next call instead of returning them to the
+    // driver at every synchronisation.
+    uint64_t keep = UINT64_MAX;
+    cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
+    g_pools[dev] = p;
+  }
+  *pool = g_pools[dev];
+  return MT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mt_status mt_sgemm(const float* A, const float* B, float* C, int64_t M, int64_t N, int64_t K,
+                   cudaStream_t stream) {
+  return run(A, B, C, M, N, K, stream, nullptr);
+}
+
+mt_status mt_sgemm_ex(const float* A, const float* B, float* C, int64_t M, int64_t N,
+                      int64_t K, cudaStream_t stream, const mt_config* cfg) {
+  return run(A, B, C, M, N, K, stream, cfg);
+}
+
+mt_status mt_sgemm_host(const float* A, const float* B, float* C, int64_t M, int64_t N,
+                        int64_t K, cudaStream_t stream, const mt_config* cfg) {
+  mt_status st0 = check_dims(M, N, K);
+  if (st0 != MT_OK) return st0;
+  if (M == 0 || N == 0) return MT_OK;
+  if (!C || (K > 0 && (!A || !B))) return MT_ERR_INVALID_ARG;
+  int dev = 0;
+  DeviceInfo info;
+  mt_status st = current_device(&dev, &info);
+  if (st != MT_OK) return st;
+  cudaMemPool_t pool = nullptr;
+  st = pool_for(dev, &pool);
+  if (st != MT_OK) return st;
+  const size_t a_bytes = static_cast<size_t>(M * K) * 4, b_bytes = static_cast<size_t>(K * N) * 4,
+               c_bytes = static_cast<size_t>(M * N) * 4;
+  float *dA = nullptr, *dB = nullptr, *dC = nullptr;
+  bool ok = true;
+  // 256-byte aligned pool blocks keep the 16-byte staging path available.
+  if (a_bytes) ok = ok && cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dA), a_bytes, pool, stream) == cudaSuccess;
+  if (b_bytes) ok = ok && cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dB), b_bytes, pool, stream) == cudaSuccess;
+  ok = ok && cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dC), c_bytes, pool, stream) == cudaSuccess;
+  if (ok && a_bytes) ok = cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, stream) == cudaSuccess;
+  if (ok && b_bytes) ok = cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, stream) == cudaSuccess;
+  if (ok) {
+    st = run(dA, dB, dC, M, N, K, stream, cfg);
+    if (st == MT_OK)
+      ok = cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, stream) == cudaSuccess;
+  }
+  if (dA) cudaFreeAsync(dA, stream);
+  if (dB) cudaFreeAsync(dB, stream);
+  if (dC) cudaFreeAsync(dC, stream);
+  const bool synced = cudaStreamSynchronize(stream) == cudaSuccess;
+  if (!ok || !synced) {
+    cudaGetLastError();
+    return st != MT_OK ? st : MT_ERR_CUDA;
+  }
+  return st;
+}
+
+mt_status mt_sgemm_plan(const float* A, const float* B, const float* C, int64_t M, int64_t N,
+                        int64_t K, const mt_config* cfg, int64_t smem_limit_bytes,
+                        mt_plan* out) {
+  if (!out) return MT_ERR_INVALID_ARG;
+  int sms = 0;
+  if (smem_limit_bytes <= 0) {
+    int dev = 0;
+    DeviceInfo info;
+    mt_status st = current_device(&dev, &info);
+    if (st != MT_OK) return st;
+    smem_limit_bytes = info.smem_optin;
+    sms = info.sms;
+  } else {
+    int dev = 0;
+    DeviceInfo info;
+    // The SM count only steers the automatic tile choice; without a device
+    // the choice assumes a full GB300 (152 SMs).
+    sms = current_device(&dev, &info) == MT_OK ? info.sms : 152;
+  }
+  Launch L;
+  mt_status st = plan_call(A, B, C, M, N, K, cfg, smem_limit_bytes, sms, &L);
+  *out = L.plan;
+  return st;
+}
+
+int mt_smem_row_padding(int columns, int simultaneous_rows) {
+  if (columns <= 0 || simultaneous_rows <= 0) return -1;
+  return mt::row_padding_rule(columns, simultaneous_rows);
+}
+
+int mt_smem_vector_row_padding(int columns, int simultaneous_rows) {
+  if (columns <= 0 || columns % 4 != 0 || simultaneous_rows <= 0) return -1;
+  return mt::vector_row_padding_rule(columns, simultaneous_rows);
+}
+
+mt_status mt_smem_layout_make(int rows, int columns, int row_padding, int stage_count,
+                              mt_smem_layout* out) {
+  if (!out || rows <= 0 || columns <= 0 || row_padding < 0 || stage_count <= 0)
+    return MT_ERR_INVALID_ARG;
+  const int64_t size = static_cast<int64_t>(stage_count) * rows * (columns + row_padding);
+  if (size > INT32_MAX / 4) return MT_ERR_INVALID_ARG;
+  const mt::SmemLayout L{rows, columns, row_padding, stage_count};
+  out->rows = rows;
+  out->columns = columns;
+  out->row_padding = row_padding;
+  out->stage_count = stage_count;
+  out->row_stride = L.row_stride();
+  out->stage_size = L.stage_size();
+  out->size = L.size();
+  out->nbytes = L.nbytes();
+  return MT_OK;
+}
+
+int64_t mt_smem_layout_offset(const mt_smem_layout* layout, int stage, int row, int column) {
+  if (!layout || stage < 0 || stage >= layout->stage_count || row < 0 || row >= layout->rows ||
+      column < 0 || column >= layout->columns)
+    return -1;
+  const mt::SmemLayout L{layout->rows, layout->columns, layout->row_padding,
+                         layout->stage_count};
+  return L.offset(stage, row, column);
+}
+
+mt_status mt_device_status(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MT_ERR_CUDA;
+  }
+  return MT_OK;
+}
+
+const char* mt_status_string(mt_status status) {
+  switch (status) {
+    case MT_OK: return "ok";
+    case MT_ERR_INVALID_ARG: return "invalid argument";
+    case MT_ERR_ALIAS: return "output overlaps an input";
+    case MT_ERR_NO_DEVICE: return "no usable CUDA device";
+    case MT_ERR_UNSUPPORTED: return "configuration not built into the library";
+    case MT_ERR_SMEM_BUDGET: return "shared-memory budget exceeded";
+    case MT_ERR_LAUNCH: return "kernel launch failed";
+    case MT_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+    case MT_ERR_CUDA: return "CUDA runtime call failed";
+  }
+  return "unknown status";
+}
+
+int mt_version(void) { return 100; }
+
+}  // extern "C"

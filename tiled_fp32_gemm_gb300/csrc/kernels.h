@@ -1,0 +1,39 @@
+// Internal interface between the host dispatcher (api.cu) and the kernel
+// translation units.  Not part of the C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mt {
+
+// One compiled FFMA tile configuration and its kernel instantiations.
+struct FfmaEntry {
+  int bm, bn, bk, stages, threads, min_blocks;
+  int packed;          // 1: fma.rn.f32x2 micro-kernel, 0: scalar fma
+  int pad_a, pad_b;    // padding words per shared row under the rule
+  int smem_bytes[2];   // [pad] dynamic shared memory per CTA
+  const void* kern[2][2];  // [vec][pad]; nullptr when not instantiated
+};
+
+// All FFMA configurations built into the library (null-terminated count).
+const FfmaEntry* ffma_entries(int* count);
+
+// Arguments every GEMM kernel receives.
+struct GemmArgs {
+  const float* A;
+  const float* B;
+  float* C;
+  int M, N, K;
+  int tiles_m, tiles_n;
+  int group_m;
+};
+
+// The one-warp kernel restating the pages' Version 18 (BM=4, BN=8, BK=16,
+// two stages, synchronous staging, padded A).  pad selects the rule's
+// padding (true) or an unpadded A tile (false).
+cudaError_t launch_p18(const GemmArgs& a, bool pad, cudaStream_t stream);
+int p18_pad_a(bool pad);
+int p18_smem_bytes(bool pad);
+
+}  // namespace mt
