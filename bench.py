@@ -58,8 +58,8 @@ def ffma_peak_tflops(sms: int, mhz: float) -> float:
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -72,7 +72,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -82,7 +82,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, name):
+        setattr(self, name, time.time())
 
     def __exit__(self, *exc):
         if self.proc:
@@ -94,9 +97,13 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self):
+        """Median SM clock and active throttle reasons of the samples taken
+        inside the timed window (between mark('t0') and mark('t1'))."""
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        t0, t1 = getattr(self, "t0", 0.0), getattr(self, "t1", float("inf"))
+        inside = [l for (t, l) in self.lines if t0 <= t <= t1 + 0.1]
+        for line in inside:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -143,21 +150,28 @@ def oracle_sample(steps: int, budget_s: float):
         oracle.sgemm_rows(A, B, rows)
         dt = time.perf_counter() - t0
         rate[name] = len(rows) / max(dt, 1e-6)  # rows per second
-    # Split the budget evenly between the shapes, in whole multiples of the
-    # thread count, at least one row per thread.
+    # Split the budget evenly between the shapes: a row sample of at most M
+    # rows (a whole multiple of the thread count, spread evenly over the
+    # matrix), repeated if the budget allows more.
     per_shape = budget_s / max(steps, 1) / len(mats)
-    nrows = {name: max(cores, int(rate[name] * per_shape) // cores * cores)
-             for name in mats}
+    plan = {}
+    for name in mats:
+        M = gemm_inputs.WORKLOADS[name].M
+        want = max(cores, int(rate[name] * per_shape) // cores * cores)
+        nrows = min(want, M)
+        plan[name] = (nrows, max(1, want // nrows))
     total_flops, total_t = 0.0, 0.0
     for _ in range(max(steps, 1)):
         for name, (A, B) in mats.items():
             w = gemm_inputs.WORKLOADS[name]
-            rows = np.linspace(0, w.M - 1, nrows[name]).astype(np.int64)
-            t0 = time.perf_counter()
-            oracle.sgemm_rows(A, B, rows)
-            total_t += time.perf_counter() - t0
-            total_flops += 2.0 * len(rows) * w.N * w.K
-    desc = ", ".join(f"{nrows[n]} of {gemm_inputs.WORKLOADS[n].M} rows of {n}"
+            nrows, reps = plan[name]
+            rows = np.linspace(0, w.M - 1, nrows).astype(np.int64)
+            for _r in range(reps):
+                t0 = time.perf_counter()
+                oracle.sgemm_rows(A, B, rows)
+                total_t += time.perf_counter() - t0
+                total_flops += 2.0 * len(rows) * w.N * w.K
+    desc = ", ".join(f"{plan[n][0]} of {gemm_inputs.WORKLOADS[n].M} rows of {n} x{plan[n][1]}"
                      for n in mats) + f" per step x {max(steps, 1)} steps"
     return total_flops / total_t / 1e12, total_t, cores, desc
 
@@ -242,6 +256,7 @@ def run_gpu(args):
                              **(json.loads(args.config) if args.config else {}))
              for (w, a, b, c, _, _) in bufs}
 
+    clocks = ClockSampler(dev).__enter__()
     for _ in range(args.warmup):
         for (w, a, b, c, _, _) in bufs:
             launch(w, a, b, c)
@@ -254,17 +269,19 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(dev) as clocks:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for s in range(args.steps):
-            for i, (w, a, b, c, _, _) in enumerate(bufs):
-                ev[s][i][0].record(stream)
-                launch(w, a, b, c)
-                ev[s][i][1].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize()
+    clocks.mark("t0")
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        for i, (w, a, b, c, _, _) in enumerate(bufs):
+            ev[s][i][0].record(stream)
+            launch(w, a, b, c)
+            ev[s][i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("t1")
+    clocks.__exit__(None, None, None)
     total_ms = t_start.elapsed_time(t_end)
     per_launch = {w.name: [ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps)]
                   for i, (w, *_r) in enumerate(bufs)}
@@ -378,7 +395,7 @@ def run_gpu(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["mt", "reference"], default="mt")
     ap.add_argument("--workloads", nargs="*", help="override the step's workloads (by name)")
