@@ -75,7 +75,11 @@ typedef struct {
     int split_k;   /* K slices reduced in a second pass; 0 = automatic, 1 = none */
     int fma;       /* FFMA micro-kernel: 0 = automatic, 1 = scalar fma.rn.f32,
                       2 = packed fma.rn.f32x2 (same results, fewer issue slots) */
-    int reserved[4];
+    int fault_inject; /* test hook, 0 = off.  1 (MT_VARIANT_TF32X3 only): the
+                         copy thread issues nothing, so every wait on its data
+                         runs out; the call then leaves C unwritten and the
+                         next mt_device_status returns MT_ERR_TIMEOUT. */
+    int reserved[3];
 } mt_config;
 
 /* What a call with the same arguments would launch. */

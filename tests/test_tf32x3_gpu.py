@@ -1,0 +1,157 @@
+"""GPU parity of the tcgen05 3xTF32 variant against the CPU oracle.
+
+Tolerance |C - C_ref| <= 5e-5 * W (W = |A|*|B|), elementwise.  Derivation:
+each input is split exactly into big (tf32) + small; the dropped
+small*small product and the tf32 conversion of the small parts each cost at
+most about 2^-21 of |a||b| per product, and fp32 accumulation of random-sign
+terms adds a few ulps of W — far inside 5e-5 * W.  Integer inputs in [-8, 8]
+are exact in tf32 (small = 0) with integer partial sums below 2^24, so there
+the result must be bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gemm_inputs
+import oracle
+import tiled_fp32_gemm_gb300 as mt
+
+pytestmark = pytest.mark.gpu
+
+TOL = 5e-5
+TF32 = dict(variant="tf32x3")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    from tiled_fp32_gemm_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+    return mt.lib()
+
+
+def run(A, B, **cfg):
+    c = mt.sgemm(A.cuda(), B.cuda(), **cfg)
+    torch.cuda.synchronize()
+    return c.cpu()
+
+
+def assert_within(C, Cref, W, tol, what=""):
+    C = np.asarray(C, np.float64)
+    err = np.abs(C - np.asarray(Cref, np.float64))
+    bad = err > tol * np.asarray(W, np.float64)
+    if bad.any():
+        i, j = np.argwhere(bad)[0]
+        pytest.fail(f"{what}: {bad.sum()} outputs outside {tol}*W, first at ({i},{j}): "
+                    f"got {C[i, j]!r} want {Cref[i, j]!r} W={W[i, j]!r}, "
+                    f"max err/W {(err / np.maximum(W, 1e-300)).max():.3g}")
+
+
+def test_plan_reports_tile_and_workspace():
+    p = mt.plan(4096, 4096, 4096, variant="tf32x3")
+    assert (p["bm"], p["bn"], p["bk"], p["stages"], p["threads"]) == (128, 256, 32, 2, 192)
+    # Packed copies of A (128-row blocks) and B (256-row blocks), 32 k each.
+    assert p["workspace_bytes"] == 4096 * 4096 * 4 * 2
+    assert p["grid"] == 32 * 16
+
+
+@pytest.mark.parametrize("name", ["masked_100x72x80", "square_1024", "ragged_4097x3001x2053"])
+def test_workloads_full_oracle(name):
+    A, B = gemm_inputs.make_workload(name)
+    Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
+    assert_within(run(A, B, **TF32).numpy(), Cref, W, TOL, name)
+
+
+@pytest.mark.parametrize("name", ["square_4096", "square_8192", "skinny_65536x128x4096"])
+def test_full_size_sampled_rows(name):
+    w = gemm_inputs.WORKLOADS[name]
+    A, B = gemm_inputs.make_workload(w)
+    c = mt.sgemm(A.cuda(), B.cuda(), **TF32)
+    torch.cuda.synchronize()
+    g = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([[0, w.M - 1, 127, 128, 255, 256],
+                                     g.integers(0, w.M, 24)]))
+    Cr, Wr = oracle.sgemm_rows(A.numpy(), B.numpy(), rows, with_w=True)
+    assert_within(c[torch.from_numpy(rows).cuda()].cpu().numpy(), Cr, Wr, TOL, name)
+
+
+@pytest.mark.parametrize("shape", [(100, 72, 80), (257, 130, 77), (128, 256, 96),
+                                   (300, 520, 1000)])
+def test_integer_inputs_bit_exact(shape):
+    M, N, K = shape
+    A, B = gemm_inputs.make_ab(M, N, K, seed=21, dist="int")
+    assert np.array_equal(run(A, B, **TF32).numpy(), oracle.sgemm(A.numpy(), B.numpy()))
+
+
+TINY = [(1, 1, 1), (1, 7, 3), (5, 1, 9), (3, 5, 7), (17, 15, 33), (31, 33, 1),
+        (129, 257, 31), (130, 258, 65)]
+
+
+@pytest.mark.parametrize("shape", TINY)
+def test_tiny_ragged(shape):
+    M, N, K = shape
+    A, B = gemm_inputs.make_ab(M, N, K, seed=M * 7 + N * 3 + K, dist="normal")
+    Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
+    assert_within(run(A, B, **TF32).numpy(), Cref, W, TOL, str(shape))
+
+
+def test_identity_within_tolerance():
+    A = torch.randn(150, 97, generator=torch.Generator().manual_seed(3))
+    C = run(A, torch.eye(97), **TF32).numpy()
+    assert np.all(np.abs(C - A.numpy()) <= TOL * np.abs(A.numpy()))
+
+
+@pytest.mark.parametrize("offset", [0, 1])
+def test_guard_bands_and_canaries(offset):
+    M, N, K = 133, 260, 72
+    A, B = gemm_inputs.make_ab(M, N, K, seed=22, dist="uniform")
+    guard = 4096
+    abuf = torch.full((M * K + 2 * guard,), float("nan"))
+    bbuf = torch.full((K * N + 2 * guard,), float("nan"))
+    abuf[guard + offset:guard + offset + M * K] = A.reshape(-1)
+    bbuf[guard + offset:guard + offset + K * N] = B.reshape(-1)
+    sentinel = -12345.0
+    cbuf = torch.full((M * N + 2 * guard,), sentinel, device="cuda")
+    a_d, b_d = abuf.cuda(), bbuf.cuda()
+    st = mt.mt_sgemm_ex(a_d.data_ptr() + 4 * (guard + offset), b_d.data_ptr() + 4 * (guard + offset),
+                        cbuf.data_ptr() + 4 * (guard + offset), M, N, K,
+                        torch.cuda.current_stream().cuda_stream, mt.make_config(**TF32))
+    assert st == mt.MT_OK
+    torch.cuda.synchronize()
+    out = cbuf.cpu()
+    C = out[guard + offset:guard + offset + M * N].reshape(M, N).numpy()
+    Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
+    assert np.isfinite(C).all()
+    assert_within(C, Cref, W, TOL, "guarded")
+    assert torch.all(out[:guard + offset] == sentinel)
+    assert torch.all(out[guard + offset + M * N:] == sentinel)
+
+
+def test_nan_propagates():
+    A, B = gemm_inputs.make_ab(40, 36, 50, seed=23, dist="uniform")
+    A[3, 7] = float("nan")
+    C = run(A, B, **TF32).numpy()
+    assert np.isnan(C[3]).all()
+    assert np.isfinite(np.delete(C, 3, axis=0)).all()
+
+
+def test_device_status_clean_after_runs():
+    A, B = gemm_inputs.make_workload("masked_100x72x80")
+    run(A, B, **TF32)
+    assert mt.mt_device_status(0) == mt.MT_OK
+
+
+def test_timeout_path_reports_and_context_survives():
+    """The copy thread issues nothing: every bounded wait runs out (about a
+    second), the kernel records the timeout and returns; the context stays
+    usable for the next call."""
+    A, B = gemm_inputs.make_workload("masked_100x72x80")
+    a, b = A.cuda(), B.cuda()
+    c = torch.full((100, 72), 7.0, device="cuda")
+    mt.sgemm(a, b, out=c, variant="tf32x3", fault_inject=1)
+    assert mt.mt_device_status(0) == mt.MT_ERR_TIMEOUT
+    assert torch.all(c == 7.0)  # nothing written
+    assert mt.mt_device_status(0) == mt.MT_OK  # the status word was cleared
+    Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
+    assert_within(run(A, B, **TF32).numpy(), Cref, W, TOL, "after timeout")
+    assert mt.mt_device_status(0) == mt.MT_OK

@@ -42,7 +42,7 @@ class mt_config(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("bm", ctypes.c_int), ("bn", ctypes.c_int),
                 ("bk", ctypes.c_int), ("stages", ctypes.c_int), ("no_pad", ctypes.c_int),
                 ("split_k", ctypes.c_int), ("fma", ctypes.c_int),
-                ("reserved", ctypes.c_int * 4)]
+                ("fault_inject", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
 
 
 class mt_plan(ctypes.Structure):
@@ -111,13 +111,14 @@ def lib():
 
 
 def make_config(variant="ffma", bm=0, bn=0, bk=0, stages=0, no_pad=False, split_k=0,
-                fma=0) -> mt_config:
+                fma=0, fault_inject=0) -> mt_config:
     c = mt_config()
     c.variant = VARIANTS[variant] if isinstance(variant, str) else int(variant)
     c.bm, c.bn, c.bk, c.stages = bm, bn, bk, stages
     c.no_pad = 1 if no_pad else 0
     c.split_k = split_k
     c.fma = fma
+    c.fault_inject = fault_inject
     return c
 
 

@@ -69,6 +69,7 @@ struct Launch {
   const void* kern = nullptr;
   int tiles_m = 0, tiles_n = 0, group_m = 8;
   bool pad = true;
+  int fault_inject = 0;
 };
 
 mt_status check_dims(int64_t M, int64_t N, int64_t K) {
@@ -135,10 +136,12 @@ mt_status plan_call(const float* A, const float* B, const float* C, int64_t M, i
   const int variant = cfg ? cfg->variant : MT_VARIANT_FFMA;
   if (cfg && (cfg->bm < 0 || cfg->bn < 0 || cfg->bk < 0 || cfg->stages < 0 ||
               cfg->no_pad < 0 || cfg->no_pad > 1 || cfg->split_k < 0 || cfg->fma < 0 ||
-              cfg->fma > 2))
+              cfg->fma > 2 || cfg->fault_inject < 0 || cfg->fault_inject > 1))
     return MT_ERR_INVALID_ARG;
+  if (cfg && cfg->fault_inject && variant != MT_VARIANT_TF32X3) return MT_ERR_UNSUPPORTED;
   if (cfg && cfg->split_k > 1) return MT_ERR_UNSUPPORTED;
   const bool pad = !(cfg && cfg->no_pad);
+  L->fault_inject = cfg ? cfg->fault_inject : 0;
   mt_plan& p = L->plan;
   std::memset(&p, 0, sizeof(p));
   p.variant = variant;
@@ -162,7 +165,29 @@ mt_status plan_call(const float* A, const float* B, const float* C, int64_t M, i
     if (p.grid > INT32_MAX) return MT_ERR_UNSUPPORTED;
     return MT_OK;
   }
-  if (variant == MT_VARIANT_TF32X3) return MT_ERR_UNSUPPORTED;
+  if (variant == MT_VARIANT_TF32X3) {
+    int bm, bn, bk, stages;
+    mt::tf32x3_tile(&bm, &bn, &bk, &stages);
+    if (cfg && ((cfg->bm && cfg->bm != bm) || (cfg->bn && cfg->bn != bn) ||
+                (cfg->bk && cfg->bk != bk) || (cfg->stages && cfg->stages != stages) ||
+                cfg->fma || cfg->no_pad))
+      return MT_ERR_UNSUPPORTED;
+    p.bm = bm; p.bn = bn; p.bk = bk; p.stages = stages;
+    p.threads = mt::tf32x3_threads();
+    p.pad_a = 0; p.pad_b = 0;  // swizzled tiles: the tensor core's layout, no padding
+    // The pack kernel reads A in float4 when K % 4 == 0 and A is 16-byte aligned.
+    p.vec_ab = (K % 4 == 0) && aligned16(A);
+    p.vec_c = (N % 4 == 0) && aligned16(C);
+    p.smem_bytes = mt::tf32x3_smem_bytes();
+    L->tiles_m = static_cast<int>(ceil_div(M, bm));
+    L->tiles_n = static_cast<int>(ceil_div(N, bn));
+    if (L->tiles_m > 65535 || L->tiles_n > 65535) return MT_ERR_UNSUPPORTED;
+    p.grid = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
+    p.workspace_bytes = mt::tf32x3_workspace_bytes(static_cast<int>(M), static_cast<int>(N),
+                                                   static_cast<int>(K));
+    if (p.smem_bytes > smem_limit) return MT_ERR_SMEM_BUDGET;
+    return MT_OK;
+  }
   if (variant != MT_VARIANT_FFMA) return MT_ERR_INVALID_ARG;
 
   int count = 0;
@@ -204,6 +229,8 @@ mt_status set_smem_attr(int dev, const Launch& L) {
   return MT_OK;
 }
 
+mt_status run_tf32x3(int dev, const mt::GemmArgs& args, const Launch& L, cudaStream_t stream);
+
 mt_status run(const float* A, const float* B, float* C, int64_t M, int64_t N, int64_t K,
               cudaStream_t stream, const mt_config* cfg) {
   mt_status st = check_args(A, B, C, M, N, K);
@@ -226,6 +253,7 @@ mt_status run(const float* A, const float* B, float* C, int64_t M, int64_t N, in
   }
   mt::GemmArgs args{A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                     L.tiles_m, L.tiles_n, L.group_m};
+  if (L.plan.variant == MT_VARIANT_TF32X3) return run_tf32x3(dev, args, L, stream);
   if (L.plan.variant == MT_VARIANT_P18) {
     if (mt::launch_p18(args, L.pad, stream) != cudaSuccess) return MT_ERR_LAUNCH;
     return MT_OK;
@@ -263,6 +291,38 @@ mt_status pool_for(int dev, cudaMemPool_t* pool) {
     g_pools[dev] = p;
   }
   *pool = g_pools[dev];
+  return MT_OK;
+}
+
+std::atomic<uint8_t> g_tf32x3_ready[kMaxDevices];
+
+mt_status run_tf32x3(int dev, const mt::GemmArgs& args, const Launch& L, cudaStream_t stream) {
+  if (!g_tf32x3_ready[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_tf32x3_ready[dev].load(std::memory_order_relaxed)) {
+      if (mt::tf32x3_prepare(dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MT_ERR_LAUNCH;
+      }
+      g_tf32x3_ready[dev].store(1, std::memory_order_release);
+    }
+  }
+  cudaMemPool_t pool = nullptr;
+  mt_status st = pool_for(dev, &pool);
+  if (st != MT_OK) return st;
+  void* ws = nullptr;
+  if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(L.plan.workspace_bytes), pool, stream) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return MT_ERR_CUDA;
+  }
+  const cudaError_t e =
+      mt::launch_tf32x3(args, ws, L.plan.vec_ab != 0, L.plan.vec_c != 0, L.fault_inject, stream);
+  cudaFreeAsync(ws, stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MT_ERR_LAUNCH;
+  }
   return MT_OK;
 }
 
@@ -386,7 +446,12 @@ mt_status mt_device_status(cudaStream_t stream) {
     cudaGetLastError();
     return MT_ERR_CUDA;
   }
-  return MT_OK;
+  unsigned int flags = 0;
+  if (mt::tf32x3_read_and_clear_status(&flags) != cudaSuccess) {
+    cudaGetLastError();
+    return MT_ERR_CUDA;
+  }
+  return flags ? MT_ERR_TIMEOUT : MT_OK;
 }
 
 const char* mt_status_string(mt_status status) {

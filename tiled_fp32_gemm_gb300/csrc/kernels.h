@@ -36,4 +36,19 @@ cudaError_t launch_p18(const GemmArgs& a, bool pad, cudaStream_t stream);
 int p18_pad_a(bool pad);
 int p18_smem_bytes(bool pad);
 
+// tcgen05 3xTF32 variant (sgemm_tf32x3.cu).  The call needs a device
+// workspace of tf32x3_workspace_bytes(M, N, K) bytes (the packed, swizzled
+// copies of A and B); launch_tf32x3 runs the two pack kernels and the GEMM.
+int64_t tf32x3_workspace_bytes(int M, int N, int K);
+int tf32x3_smem_bytes();
+int tf32x3_threads();
+void tf32x3_tile(int* bm, int* bn, int* bk, int* stages);
+cudaError_t tf32x3_prepare(int device);
+// fault_inject = 1: the copy thread issues nothing (tests the bounded waits).
+cudaError_t launch_tf32x3(const GemmArgs& a, void* workspace, bool vec_ab, bool vec_c,
+                          int fault_inject, cudaStream_t stream);
+// Reads and zeroes the device status word of the tf32x3 kernels
+// (bit 0: a bounded wait expired).  Synchronous.
+cudaError_t tf32x3_read_and_clear_status(unsigned int* status);
+
 }  // namespace mt

@@ -1,0 +1,489 @@
+// fp32 GEMM on the 5th-generation tensor cores: tcgen05.mma kind::tf32 with
+// the 3xTF32 split, accumulator in tensor memory (TMEM).
+//
+// The product is the same C = A*B as every other variant (row-major, masked
+// edges reading 0.0, "My Triton From Scratch, Part 14: Shared Memory Tiles",
+// sections "The canonical source pattern" and "Zero-filled boundary tiles").
+// The pages stop at CUDA cores ("Part 18", section "What Version 18 does not
+// do": no tensor-core instructions); this variant keeps their structure —
+// staged, zero-filled shared tiles and a multi-stage K pipeline — and moves
+// the dot onto tcgen05.
+//
+// 3xTF32: a tf32 operand keeps 10 of fp32's 23 mantissa bits.  Each input x
+// is split into big = x with the low 13 mantissa bits cleared (exactly
+// representable in tf32) and small = x - big (exact in fp32, and its own
+// top 11 bits survive the tensor core's tf32 conversion).  Then
+//     A*B ~= A_big*B_small + A_small*B_big + A_big*B_big
+// (A_small*B_small, about 2^-22 relative, is dropped), accumulated in fp32.
+//
+// Pipeline of one CTA (one 128 x 256 tile of C, 192 threads):
+//   pack kernels (before): A and B are copied once into zero-padded,
+//     K-major blocks of 128 (A) or 256 (B) rows x 32 k, already in the
+//     tensor core's 128-byte-swizzled shared-memory order, so the main loop
+//     moves each block with one cp.async.bulk and needs no alignment of the
+//     caller's leading dimensions;
+//   warp 0, one thread: bulk copies of the A and B blocks of K tile kt into
+//     stage kt % 2, completion counted on full[s];
+//   warps 2-5 (128 threads): wait full[s], split every fp32 in place into
+//     big and a separate small buffer, fence to the async proxy, arrive on
+//     conv[s];
+//   warp 1, one thread: wait conv[s], issue 4 k-steps x 3 tcgen05.mma
+//     (128x256x8 each) into the TMEM accumulator, tcgen05.commit -> empty[s]
+//     (frees the stage for the producer), and after the last tile -> done;
+//   warps 2-5: wait done, tcgen05.ld their 32 TMEM lanes (rows), masked
+//     stores to C.
+// Every wait is bounded (%globaltimer); on expiry the CTA records
+// MT_ERR_TIMEOUT in a device status word, stops issuing, drains what it
+// issued (again bounded), frees TMEM and returns.
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "device_util.cuh"
+#include "kernels.h"
+
+namespace mt {
+namespace tf32x3 {
+
+constexpr int BM = 128, BN = 256, BK = 32, STAGES = 2;
+constexpr int A_BLOCK_BYTES = BM * BK * 4;  // 16 KB
+constexpr int B_BLOCK_BYTES = BN * BK * 4;  // 32 KB
+// Stage: A big | A small | B big | B small.
+constexpr int STAGE_BYTES = 2 * A_BLOCK_BYTES + 2 * B_BLOCK_BYTES;  // 96 KB
+constexpr int THREADS = 192;
+constexpr int CONVERT_THREADS = 128;
+constexpr uint32_t TMEM_COLS = 256;  // fp32 accumulator: 128 lanes x 256 columns
+constexpr uint64_t TIMEOUT_NS = 1000000000ull;  // 1 s per wait
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment*/ + 256 /*barriers*/;
+
+__device__ unsigned int g_status;  // bit 0: a bounded wait expired
+
+// Byte offset of element (r, k), k < 32, inside a K-major block whose rows
+// are 32 fp32 (128 bytes) long, in the 128-byte swizzle the tensor core
+// reads: rows grouped by 8 into 1024-byte atoms, and the 16-byte chunk index
+// XOR-ed with the row's position inside its atom.
+__host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t k) {
+  const uint32_t r8 = r & 7u;
+  return (r >> 3) * 1024u + r8 * 128u + ((((k >> 2) ^ r8) & 7u) << 4) + (k & 3u) * 4u;
+}
+
+// ---------------------------------------------------------------------------
+// Pack kernels: caller's row-major A, B -> swizzled K-major blocks (zero fill).
+
+// grid (Kt, Mt), 256 threads: block (tm, kt) = A[tm*128 + r][kt*32 + k].
+__global__ void __launch_bounds__(256) pack_a_kernel(const float* __restrict__ A,
+                                                     float* __restrict__ Ap, int M, int K,
+                                                     int Kt, int vec) {
+  const int kt = blockIdx.x, tm = blockIdx.y;
+  char* dst = reinterpret_cast<char*>(Ap) +
+              (static_cast<int64_t>(tm) * Kt + kt) * static_cast<int64_t>(A_BLOCK_BYTES);
+  for (int c = threadIdx.x; c < BM * (BK / 4); c += 256) {
+    const int r = c >> 3, ch = c & 7;
+    const int m = tm * BM + r, k = kt * BK + ch * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (m < M) {
+      const float* src = A + static_cast<int64_t>(m) * K + k;
+      if (vec) {
+        if (k < K) v = *reinterpret_cast<const float4*>(src);
+      } else {
+        if (k + 0 < K) v.x = src[0];
+        if (k + 1 < K) v.y = src[1];
+        if (k + 2 < K) v.z = src[2];
+        if (k + 3 < K) v.w = src[3];
+      }
+    }
+    *reinterpret_cast<float4*>(dst + sw128_offset(r, ch * 4)) = v;
+  }
+}
+
+// grid (Kt, Nt), 256 threads: block (tn, kt) row n = B[kt*32 + k][tn*256 + n].
+// Thread t owns row n = t: it reads one column of the B tile (coalesced
+// across the warp) and writes its 128-byte row.
+__global__ void __launch_bounds__(256) pack_b_kernel(const float* __restrict__ B,
+                                                     float* __restrict__ Bp, int K, int N,
+                                                     int Kt) {
+  const int kt = blockIdx.x, tn = blockIdx.y, t = threadIdx.x;
+  const int n = tn * BN + t;
+  char* dst = reinterpret_cast<char*>(Bp) +
+              (static_cast<int64_t>(tn) * Kt + kt) * static_cast<int64_t>(B_BLOCK_BYTES);
+  float v[BK];
+#pragma unroll
+  for (int j = 0; j < BK; ++j) {
+    const int k = kt * BK + j;
+    v[j] = (n < N && k < K) ? B[static_cast<int64_t>(k) * N + n] : 0.f;
+  }
+#pragma unroll
+  for (int ch = 0; ch < BK / 4; ++ch)
+    *reinterpret_cast<float4*>(dst + sw128_offset(t, ch * 4)) =
+        make_float4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers.
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.b32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand in 128-byte swizzle,
+// 8-row atoms 1024 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);  // start address, 16-byte units
+  d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused here)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset: 1024 bytes
+  d |= static_cast<uint64_t>(1) << 46;                  // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: D fp32, A and B tf32, both K-major, M x N.
+__host__ __device__ constexpr uint32_t instr_desc_tf32(int m, int n) {
+  return (1u << 4)                                 // D format: f32
+         | (2u << 7)                               // A format: tf32
+         | (2u << 10)                              // B format: tf32
+         | (static_cast<uint32_t>(n >> 3) << 17)   // N / 8
+         | (static_cast<uint32_t>(m >> 4) << 24);  // M / 16
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_addr, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   slot_addr),
+               "r"(cols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Bounded wait on an mbarrier phase.  Returns false when the CTA is
+// aborting (another role gave up) or this wait itself ran out of time, in
+// which case it raises the abort flag and the device status word.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
+                                           volatile int* abort_flag, bool honour_abort = true) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15u) == 15u) {
+      if (honour_abort && *abort_flag) return false;
+      if (globaltimer() - t0 > TIMEOUT_NS) {
+        *abort_flag = 1;
+        atomicOr(&g_status, 1u);
+        return false;
+      }
+    }
+  }
+}
+
+// big = x with the low 13 mantissa bits cleared; small = x - big (exact).
+// Infinities and NaNs keep their bits in big and contribute 0 through small.
+__device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
+  const uint32_t u = __float_as_uint(x);
+  const bool special = (u & 0x7F800000u) == 0x7F800000u;
+  big = special ? x : __uint_as_float(u & 0xFFFFE000u);
+  small = special ? 0.0f : x - big;
+}
+
+__device__ __forceinline__ void split4(uint8_t* big_buf, uint8_t* small_buf, uint32_t off) {
+  float4 x = *reinterpret_cast<float4*>(big_buf + off);
+  float4 b, s;
+  split_tf32(x.x, b.x, s.x);
+  split_tf32(x.y, b.y, s.y);
+  split_tf32(x.z, b.z, s.z);
+  split_tf32(x.w, b.w, s.w);
+  *reinterpret_cast<float4*>(big_buf + off) = b;
+  *reinterpret_cast<float4*>(small_buf + off) = s;
+}
+
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(THREADS, 1)
+    tf32x3_gemm_kernel(const float* __restrict__ Ap, const float* __restrict__ Bp,
+                       float* __restrict__ C, int M, int N, int Kt, int tiles_m, int tiles_n,
+                       int group_m, int vec_c, int fault_inject) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars[0..S): full, [S..2S): conv, [2S..3S): empty, [3S]: done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  int tm, tn;
+  grouped_tile(blockIdx.x, tiles_m, tiles_n, group_m, tm, tn);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(s), 1);                          // full: producer + tx bytes
+      mbar_init(bar(STAGES + s), CONVERT_THREADS);   // conv: every converter
+      mbar_init(bar(2 * STAGES + s), 1);             // empty: MMA commit
+    }
+    mbar_init(bar(3 * STAGES), 1);  // done: final MMA commit
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const char* a_src = reinterpret_cast<const char*>(Ap) +
+                      static_cast<int64_t>(tm) * Kt * static_cast<int64_t>(A_BLOCK_BYTES);
+  const char* b_src = reinterpret_cast<const char*>(Bp) +
+                      static_cast<int64_t>(tn) * Kt * static_cast<int64_t>(B_BLOCK_BYTES);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // Producer.  With fault_inject set it issues nothing, so every wait
+      // on its data runs out (the test of the timeout path).
+      int issued = 0;
+      for (int kt = 0; kt < (fault_inject ? 0 : Kt); ++kt) {
+        const int s = kt % STAGES;
+        const uint32_t round = static_cast<uint32_t>(kt / STAGES);
+        if (kt >= STAGES && !wait_phase(bar(2 * STAGES + s), (round + 1) & 1u, abort_flag)) break;
+        uint8_t* st = smem + s * STAGE_BYTES;
+        mbar_arrive_expect_tx(bar(s), A_BLOCK_BYTES + B_BLOCK_BYTES);
+        bulk_copy_g2s(smem_u32(st), a_src + static_cast<int64_t>(kt) * A_BLOCK_BYTES,
+                      A_BLOCK_BYTES, bar(s));
+        bulk_copy_g2s(smem_u32(st + 2 * A_BLOCK_BYTES),
+                      b_src + static_cast<int64_t>(kt) * B_BLOCK_BYTES, B_BLOCK_BYTES, bar(s));
+        issued = kt + 1;
+      }
+      if (*abort_flag) {
+        // Let the copies this thread issued land before the CTA exits.
+        for (int kt = issued - STAGES < 0 ? 0 : issued - STAGES; kt < issued; ++kt)
+          wait_phase(bar(kt % STAGES), static_cast<uint32_t>(kt / STAGES) & 1u, abort_flag,
+                     false);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // MMA issuer.
+      constexpr uint32_t idesc = instr_desc_tf32(BM, BN);
+      uint32_t acc = 0;
+      for (int kt = 0; kt < Kt; ++kt) {
+        const int s = kt % STAGES;
+        const uint32_t round = static_cast<uint32_t>(kt / STAGES);
+        if (!wait_phase(bar(STAGES + s), round & 1u, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t a_big = smem_u32(smem + s * STAGE_BYTES);
+        const uint32_t a_small = a_big + A_BLOCK_BYTES;
+        const uint32_t b_big = a_big + 2 * A_BLOCK_BYTES;
+        const uint32_t b_small = b_big + B_BLOCK_BYTES;
+#pragma unroll
+        for (int j = 0; j < BK / 8; ++j) {
+          const uint32_t koff = j * 32;  // 8 tf32 = 32 bytes along K
+          mma_tf32(tmem, smem_desc_sw128(a_big + koff), smem_desc_sw128(b_small + koff), idesc,
+                   acc);
+          acc = 1;
+          mma_tf32(tmem, smem_desc_sw128(a_small + koff), smem_desc_sw128(b_big + koff), idesc, 1);
+          mma_tf32(tmem, smem_desc_sw128(a_big + koff), smem_desc_sw128(b_big + koff), idesc, 1);
+        }
+        mma_commit(bar(2 * STAGES + s));
+      }
+      // After the last MMA (or on abort, after whatever was issued).
+      mma_commit(bar(3 * STAGES));
+    }
+  } else {
+    // Converters, then the epilogue (warps 2..5 cover TMEM lane quarters
+    // 2, 3, 0, 1).
+    const int ct = threadIdx.x - 64;
+    bool ok = true;
+    for (int kt = 0; kt < Kt && ok; ++kt) {
+      const int s = kt % STAGES;
+      const uint32_t round = static_cast<uint32_t>(kt / STAGES);
+      if (!wait_phase(bar(s), round & 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      uint8_t* st = smem + s * STAGE_BYTES;
+      uint8_t* a_big = st;
+      uint8_t* a_small = st + A_BLOCK_BYTES;
+      uint8_t* b_big = st + 2 * A_BLOCK_BYTES;
+      uint8_t* b_small = b_big + B_BLOCK_BYTES;
+#pragma unroll 4
+      for (int c = ct; c < A_BLOCK_BYTES / 16; c += CONVERT_THREADS) split4(a_big, a_small, c * 16);
+#pragma unroll 4
+      for (int c = ct; c < B_BLOCK_BYTES / 16; c += CONVERT_THREADS) split4(b_big, b_small, c * 16);
+      fence_proxy_async_smem();
+      mbar_arrive(bar(STAGES + s));
+    }
+    // Wait for the accumulator even after an abort, so no MMA is in flight
+    // when TMEM is released.
+    const bool done = wait_phase(bar(3 * STAGES), 0, abort_flag, false);
+    tc_fence_after();
+    __syncwarp();
+    if (ok && done && !*abort_flag) {
+      const int q = warp & 3;  // TMEM lane quarter this warp may access
+      const int row = tm * BM + q * 32 + lane;
+      const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
+      float* c_row = C + static_cast<int64_t>(row) * N;
+#pragma unroll 1
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        float v[32];
+        tmem_ld32(t_row + ch * 32, v);
+        const int col0 = tn * BN + ch * 32;
+        if (row < M) {
+          if (vec_c) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              if (col0 + 4 * g < N)
+                *reinterpret_cast<float4*>(c_row + col0 + 4 * g) =
+                    make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (col0 + i < N) c_row[col0 + i] = v[i];
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace tf32x3
+
+// ---------------------------------------------------------------------------
+int64_t tf32x3_workspace_bytes(int M, int N, int K) {
+  const int64_t mt = (M + tf32x3::BM - 1) / tf32x3::BM;
+  const int64_t nt = (N + tf32x3::BN - 1) / tf32x3::BN;
+  const int64_t kt = (K + tf32x3::BK - 1) / tf32x3::BK;
+  return mt * kt * tf32x3::A_BLOCK_BYTES + nt * kt * tf32x3::B_BLOCK_BYTES;
+}
+
+int tf32x3_smem_bytes() { return tf32x3::SMEM_BYTES; }
+int tf32x3_threads() { return tf32x3::THREADS; }
+void tf32x3_tile(int* bm, int* bn, int* bk, int* stages) {
+  *bm = tf32x3::BM;
+  *bn = tf32x3::BN;
+  *bk = tf32x3::BK;
+  *stages = tf32x3::STAGES;
+}
+
+cudaError_t tf32x3_prepare(int device) {
+  (void)device;
+  return cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, tf32x3::SMEM_BYTES);
+}
+
+cudaError_t launch_tf32x3(const GemmArgs& a, void* workspace, bool vec_ab, bool vec_c,
+                          int fault_inject, cudaStream_t stream) {
+  using namespace tf32x3;
+  const int mt = (a.M + BM - 1) / BM, nt = (a.N + BN - 1) / BN, kt = (a.K + BK - 1) / BK;
+  if (mt > 65535 || nt > 65535) return cudaErrorInvalidValue;
+  float* Ap = static_cast<float*>(workspace);
+  float* Bp = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                       static_cast<int64_t>(mt) * kt * A_BLOCK_BYTES);
+  pack_a_kernel<<<dim3(kt, mt), 256, 0, stream>>>(a.A, Ap, a.M, a.K, kt, vec_ab ? 1 : 0);
+  pack_b_kernel<<<dim3(kt, nt), 256, 0, stream>>>(a.B, Bp, a.K, a.N, kt);
+  tf32x3_gemm_kernel<<<static_cast<unsigned>(mt * nt), THREADS, SMEM_BYTES, stream>>>(
+      Ap, Bp, a.C, a.M, a.N, kt, mt, nt, a.group_m, vec_c ? 1 : 0, fault_inject);
+  return cudaGetLastError();
+}
+
+cudaError_t tf32x3_read_and_clear_status(unsigned int* status) {
+  cudaError_t e = cudaMemcpyFromSymbol(status, tf32x3::g_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(tf32x3::g_status, &zero, sizeof(unsigned int));
+}
+
+}  // namespace mt
