@@ -55,7 +55,8 @@ typedef enum {
     MT_ERR_SMEM_BUDGET = 5,   /* staged tiles do not fit the shared-memory limit */
     MT_ERR_LAUNCH = 6,        /* the kernel launch was rejected */
     MT_ERR_TIMEOUT = 7,       /* a kernel gave up waiting (device status word) */
-    MT_ERR_CUDA = 8           /* a CUDA runtime call (copy, allocation, sync) failed */
+    MT_ERR_CUDA = 8,          /* a CUDA runtime call (copy, allocation, sync) failed */
+    MT_ERR_SCRATCH_LIMIT = 9  /* problem too large for mt_sgemm_tf32x3_noalloc's scratch */
 } mt_status;
 
 typedef enum {
@@ -125,6 +126,40 @@ MT_API mt_status mt_sgemm_ex(const float *A, const float *B, float *C,
 MT_API mt_status mt_sgemm_host(const float *A, const float *B, float *C,
                         int64_t M, int64_t N, int64_t K, cudaStream_t stream,
                         const mt_config *cfg);
+
+/*
+ * Allocation-free form of the MT_VARIANT_TF32X3 call, for callers that must
+ * not allocate device memory while they run: code whose device memory is
+ * owned by someone else (a host application or framework that hands it a
+ * fixed budget, or a caching allocator it must not bypass) and real-time
+ * loops that reserve everything at start-up, because cudaMalloc and
+ * cudaFree can synchronise the device, take unbounded time or fail under
+ * memory pressure in the middle of a step.  The paper has no counterpart:
+ * its kernels need no scratch memory.
+ *
+ * Same arguments, layouts and result as mt_sgemm_ex with
+ * cfg->variant = MT_VARIANT_TF32X3 (device pointers, stream-ordered).  The
+ * packed copies of A and B that variant builds go to a static device array
+ * of MT_NOALLOC_SCRATCH_BYTES (32 MiB) instead of memory allocated per call;
+ * this call allocates nothing.  A problem needs
+ * 16384*ceil(M/128)*ceil(K/32) + 32768*ceil(N/256)*ceil(K/32) bytes of it
+ * (about 4*(M + N)*K; up to about 2048 x 2048 x 2048); a larger one returns
+ * MT_ERR_SCRATCH_LIMIT and launches nothing (mt_sgemm_plan reports the
+ * bytes as workspace_bytes).  Other errors as mt_sgemm_ex.
+ *
+ * The array is shared by every call in the process: calls that overlap on
+ * the GPU (different streams, or host threads) race on it and must be
+ * serialised by the caller.  Each call rewrites all of the scratch it reads,
+ * so nothing needs clearing between calls.  Every device that loads the
+ * library holds the array until the process exits.  The first call on a
+ * device looks up the array's device address and sets the kernel's
+ * shared-memory limit (no allocation); make that first call before any
+ * stream capture.
+ */
+#define MT_NOALLOC_SCRATCH_BYTES (32ll << 20)
+MT_API mt_status mt_sgemm_tf32x3_noalloc(const float *A, const float *B, float *C,
+                                         int64_t M, int64_t N, int64_t K,
+                                         cudaStream_t stream);
 
 /*
  * Fills *out with the launch a call with these arguments would make,

@@ -3,7 +3,8 @@
 The compute lives in ``libmtsgemm.so`` (hand-written CUDA for sm_103a, built
 by ``tiled_fp32_gemm_gb300.build``).  This module only marshals arguments:
 
-* ``mt_sgemm``, ``mt_sgemm_ex``, ``mt_sgemm_host``, ``mt_sgemm_plan``,
+* ``mt_sgemm``, ``mt_sgemm_ex``, ``mt_sgemm_host``, ``mt_sgemm_tf32x3_noalloc``,
+  ``mt_sgemm_plan``,
   ``mt_smem_row_padding``, ``mt_smem_vector_row_padding``,
   ``mt_smem_layout_make``, ``mt_smem_layout_offset``, ``mt_device_status``,
   ``mt_status_string``, ``mt_version`` — the C entry points under the same
@@ -29,6 +30,8 @@ MT_ERR_SMEM_BUDGET = 5
 MT_ERR_LAUNCH = 6
 MT_ERR_TIMEOUT = 7
 MT_ERR_CUDA = 8
+MT_ERR_SCRATCH_LIMIT = 9
+MT_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 MT_VARIANT_FFMA = 0
 MT_VARIANT_TF32X3 = 1
@@ -76,6 +79,7 @@ SIGNATURES = {
     "mt_sgemm": (_I, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "mt_sgemm_ex": (_I, [_P, _P, _P, _I64, _I64, _I64, _P, ctypes.POINTER(mt_config)]),
     "mt_sgemm_host": (_I, [_P, _P, _P, _I64, _I64, _I64, _P, ctypes.POINTER(mt_config)]),
+    "mt_sgemm_tf32x3_noalloc": (_I, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "mt_sgemm_plan": (_I, [_P, _P, _P, _I64, _I64, _I64, ctypes.POINTER(mt_config), _I64,
                            ctypes.POINTER(mt_plan)]),
     "mt_smem_row_padding": (_I, [_I, _I]),
@@ -137,6 +141,13 @@ def mt_sgemm_host(A: int, B: int, C: int, M: int, N: int, K: int, stream: int = 
                   cfg: mt_config | None = None) -> int:
     return lib().mt_sgemm_host(A, B, C, M, N, K, stream,
                                ctypes.byref(cfg) if cfg is not None else None)
+
+
+def mt_sgemm_tf32x3_noalloc(A: int, B: int, C: int, M: int, N: int, K: int,
+                            stream: int = 0) -> int:
+    """The 3xTF32 product with its scratch in the library's static device
+    array: allocates nothing (see include/mt_sgemm.h for who needs that)."""
+    return lib().mt_sgemm_tf32x3_noalloc(A, B, C, M, N, K, stream)
 
 
 def mt_sgemm_plan(A: int, B: int, C: int, M: int, N: int, K: int,

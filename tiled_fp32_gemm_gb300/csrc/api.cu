@@ -379,6 +379,57 @@ mt_status mt_sgemm_host(const float* A, const float* B, float* C, int64_t M, int
   return st;
 }
 
+mt_status mt_sgemm_tf32x3_noalloc(const float* A, const float* B, float* C, int64_t M,
+                                  int64_t N, int64_t K, cudaStream_t stream) {
+  static_assert(MT_NOALLOC_SCRATCH_BYTES == mt::kNoAllocScratchBytes, "scratch size");
+  static std::atomic<uint8_t> prepared[kMaxDevices];
+  mt_status st = check_args(A, B, C, M, N, K);
+  if (st != MT_OK) return st;
+  if (M == 0 || N == 0) return MT_OK;
+  int dev = 0;
+  DeviceInfo info;
+  st = current_device(&dev, &info);
+  if (st != MT_OK) return st;
+  mt_config cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.variant = MT_VARIANT_TF32X3;
+  Launch L;
+  st = plan_call(A, B, C, M, N, K, &cfg, info.smem_optin, info.sms, &L);
+  if (st != MT_OK) return st;
+  if (K == 0) {
+    // Empty reduction: zeros, written without any scratch.
+    if (cudaMemsetAsync(C, 0, static_cast<size_t>(M * N) * 4, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return MT_ERR_LAUNCH;
+    }
+    return MT_OK;
+  }
+  if (L.plan.workspace_bytes > MT_NOALLOC_SCRATCH_BYTES) return MT_ERR_SCRATCH_LIMIT;
+  if (!prepared[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!prepared[dev].load(std::memory_order_relaxed)) {
+      if (mt::tf32x3_prepare(dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MT_ERR_LAUNCH;
+      }
+      prepared[dev].store(1, std::memory_order_release);
+    }
+  }
+  void* scratch = nullptr;
+  if (mt::tf32x3_noalloc_scratch(dev, &scratch) != cudaSuccess || !scratch) {
+    cudaGetLastError();
+    return MT_ERR_CUDA;
+  }
+  mt::GemmArgs args{A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                    L.tiles_m, L.tiles_n, L.group_m};
+  if (mt::launch_tf32x3(args, scratch, L.plan.vec_ab != 0, L.plan.vec_c != 0, 0, stream) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return MT_ERR_LAUNCH;
+  }
+  return MT_OK;
+}
+
 mt_status mt_sgemm_plan(const float* A, const float* B, const float* C, int64_t M, int64_t N,
                         int64_t K, const mt_config* cfg, int64_t smem_limit_bytes,
                         mt_plan* out) {
@@ -465,6 +516,8 @@ const char* mt_status_string(mt_status status) {
     case MT_ERR_LAUNCH: return "kernel launch failed";
     case MT_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
     case MT_ERR_CUDA: return "CUDA runtime call failed";
+    case MT_ERR_SCRATCH_LIMIT:
+      return "problem exceeds the static scratch of the allocation-free entry point";
   }
   return "unknown status";
 }

@@ -47,6 +47,11 @@ cudaError_t tf32x3_prepare(int device);
 // fault_inject = 1: the copy thread issues nothing (tests the bounded waits).
 cudaError_t launch_tf32x3(const GemmArgs& a, void* workspace, bool vec_ab, bool vec_c,
                           int fault_inject, cudaStream_t stream);
+// Size of the static scratch the allocation-free tf32x3 entry point uses,
+// and its device address on `device` (looked up once per device; the device
+// must be current).
+constexpr int64_t kNoAllocScratchBytes = int64_t(32) << 20;  // 32 MiB
+cudaError_t tf32x3_noalloc_scratch(int device, void** ptr);
 // Reads and zeroes the device status word of the tf32x3 kernels
 // (bit 0: a bounded wait expired).  Synchronous.
 cudaError_t tf32x3_read_and_clear_status(unsigned int* status);

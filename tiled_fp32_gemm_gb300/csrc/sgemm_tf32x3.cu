@@ -36,6 +36,7 @@
 // MT_ERR_TIMEOUT in a device status word, stops issuing, drains what it
 // issued (again bounded), frees TMEM and returns.
 #include <cstdint>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -477,6 +478,36 @@ cudaError_t launch_tf32x3(const GemmArgs& a, void* workspace, bool vec_ab, bool 
   tf32x3_gemm_kernel<<<static_cast<unsigned>(mt * nt), THREADS, SMEM_BYTES, stream>>>(
       Ap, Bp, a.C, a.M, a.N, kt, mt, nt, a.group_m, vec_c ? 1 : 0, fault_inject);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Static scratch of the allocation-free entry point (mt_sgemm_tf32x3_noalloc):
+// the packed copies of A and B live here instead of in memory allocated per
+// call.  Every device that loads the library holds this array until the
+// process exits.  Calls share it, so calls that overlap on the GPU race on
+// it; each call's pack kernels rewrite every byte the call then reads
+// (padding included), so nothing has to be cleared between calls.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[64];
+}  // namespace
+
+cudaError_t tf32x3_noalloc_scratch(int device, void** ptr) {
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[device]) {
+    // In host code the array's name is only a stand-in; the device address
+    // comes from the runtime, looked up once per device with that device
+    // current (the caller's current device).
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[device] = p;
+  }
+  *ptr = g_noalloc_ptr[device];
+  return cudaSuccess;
 }
 
 cudaError_t tf32x3_read_and_clear_status(unsigned int* status) {
