@@ -13,6 +13,9 @@ follows an 8192^3 one, so no launch starts with its inputs in L2.
 host->device copies of A and B, the GEMM and the device->host copy of C are
 all inside its timed region.
 
+`variants` holds the other fp32 variant (3xTF32 on tcgen05, or FFMA when
+--config selects 3xTF32) measured the same way in the same run.
+
 `--impl reference` times the reference arm instead: the CPU oracle (fp64
 accumulation, all host cores) on a bounded sample of rows of the same two
 GEMMs, reported in the same metric.
@@ -220,6 +223,16 @@ def load_traffic(kernel_key: str):
     return entry.get("bytes_per_launch")
 
 
+# Nominal dense tensor rates (PFLOP/s) of the recipe's table: the TF32 peak
+# is the measured bf16 peak scaled by their ratio.
+NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25
+LAUNCHES_PER_CALL = {"ffma": 1, "p18": 1, "tf32x3": 3}  # tf32x3: pack A, pack B, GEMM
+
+
+def variant_of(cfg_json):
+    return (cfg_json or {}).get("variant", "ffma")
+
+
 def run_gpu(args):
     import torch
     import tiled_fp32_gemm_gb300 as mt
@@ -236,8 +249,21 @@ def run_gpu(args):
     mt_build.build()
     mt.lib()
 
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
     shapes = [gemm_inputs.WORKLOADS[n] for n in (args.workloads or STEP_WORKLOADS)]
-    cfg = mt.make_config(**json.loads(args.config)) if args.config else None
+    main_cfg = json.loads(args.config) if args.config else {}
     bufs = []
     for w in shapes:
         A, B = gemm_inputs.make_workload(w)
@@ -246,107 +272,143 @@ def run_gpu(args):
         bufs.append((w, a, b, c, A, B))
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
+    flops_step = sum(w.flops for (w, *_r) in bufs)
 
-    def launch(w, a, b, c):
-        st = mt.mt_sgemm_ex(a.data_ptr(), b.data_ptr(), c.data_ptr(), w.M, w.N, w.K, sptr, cfg)
-        if st != mt.MT_OK:
-            raise mt.MtError(st, f"mt_sgemm_ex {w.name}")
+    def measure(cfg_json, steps, warmup, clocks=None):
+        """Per-launch CUDA-event times (ms) of every GEMM of `steps` steps."""
+        cfg = mt.make_config(**cfg_json) if cfg_json else None
 
-    plans = {w.name: mt.plan(w.M, w.N, w.K, a=a, b=b, c=c,
-                             **(json.loads(args.config) if args.config else {}))
-             for (w, a, b, c, _, _) in bufs}
+        def launch(w, a, b, c):
+            st = mt.mt_sgemm_ex(a.data_ptr(), b.data_ptr(), c.data_ptr(), w.M, w.N, w.K, sptr,
+                                cfg)
+            if st != mt.MT_OK:
+                raise mt.MtError(st, f"mt_sgemm_ex {w.name}")
+
+        for _ in range(warmup):
+            for (w, a, b, c, _, _) in bufs:
+                launch(w, a, b, c)
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in bufs] for _ in range(steps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        if clocks:
+            clocks.mark("t0")
+        t0.record(stream)
+        for s_ in range(steps):
+            for i, (w, a, b, c, _, _) in enumerate(bufs):
+                ev[s_][i][0].record(stream)
+                launch(w, a, b, c)
+                ev[s_][i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if clocks:
+            clocks.mark("t1")
+        total = max_over_ranks(t0.elapsed_time(t1))
+        per = {w.name: [ev[s_][i][0].elapsed_time(ev[s_][i][1]) for s_ in range(steps)]
+               for i, (w, *_r) in enumerate(bufs)}
+        if mt.mt_device_status(sptr) != mt.MT_OK:
+            raise RuntimeError("device status reported a kernel timeout")
+        return total, per
+
+    def plans_for(cfg_json):
+        return {w.name: mt.plan(w.M, w.N, w.K, a=a, b=b, c=c, **cfg_json)
+                for (w, a, b, c, _, _) in bufs}
 
     clocks = ClockSampler(dev).__enter__()
-    for _ in range(args.warmup):
-        for (w, a, b, c, _, _) in bufs:
-            launch(w, a, b, c)
-    torch.cuda.synchronize()
-
-    # Timed region: events around every launch on the launching stream.
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in bufs] for _ in range(args.steps)]
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.mark("t0")
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for s in range(args.steps):
-        for i, (w, a, b, c, _, _) in enumerate(bufs):
-            ev[s][i][0].record(stream)
-            launch(w, a, b, c)
-            ev[s][i][1].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    clocks.mark("t1")
+    total_ms, per_launch = measure(main_cfg, args.steps, args.warmup, clocks)
     clocks.__exit__(None, None, None)
-    total_ms = t_start.elapsed_time(t_end)
-    per_launch = {w.name: [ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps)]
-                  for i, (w, *_r) in enumerate(bufs)}
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-        dist.barrier()
-    flops_step = sum(w.flops for (w, *_r) in bufs)
     value = world * flops_step * args.steps / (total_ms / 1e3) / 1e12
+    plans = plans_for(main_cfg)
 
     clk = clocks.summary()
     peaks = measured_peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     sm_max = clk["sm_max_mhz"] or peaks.get("sm_max_mhz") or SM_MAX_MHZ_FALLBACK
-    peak_max = ffma_peak_tflops(sms, sm_max)
-    peak_live = ffma_peak_tflops(sms, clk["sm_mhz"]) if clk["sm_mhz"] else None
-    per_shape = {}
-    for (w, *_r) in bufs:
-        ms = statistics.median(per_launch[w.name])
-        tf = w.flops / (ms / 1e3) / 1e12
-        per_shape[w.name] = {"ms_median": ms, "tflops": tf,
-                             "frac_of_ffma_peak_at_max_clock": tf / peak_max,
-                             "frac_of_ffma_peak_at_run_clock":
-                                 tf / peak_live if peak_live else None,
-                             "plan": plans[w.name]}
-    # Dominant kernel: the launch with the most device time per step.
+    ffma_peak = ffma_peak_tflops(sms, sm_max)
+    ffma_live = ffma_peak_tflops(sms, clk["sm_mhz"]) if clk["sm_mhz"] else None
+    bf16 = peaks.get("bf16_tflops")
+    tf32_peak = (bf16 if bf16 else 1900.0) * NOMINAL_TF32_OVER_BF16
+    tf32_basis = ("measured bf16 %.0f TFLOP/s (MEASURED_PEAKS.json) x nominal tf32/bf16 "
+                  "1.1/2.25" % bf16) if bf16 else "fallback 1.9 PFLOP/s bf16 x 1.1/2.25"
+
+    def shape_summary(per, plans_):
+        out = {}
+        for (w, *_r) in bufs:
+            ms = statistics.median(per[w.name])
+            tf = w.flops / (ms / 1e3) / 1e12
+            out[w.name] = {"ms_median": ms, "tflops": tf,
+                           "frac_of_ffma_peak_at_max_clock": tf / ffma_peak,
+                           "frac_of_ffma_peak_at_run_clock": tf / ffma_live if ffma_live else None,
+                           "plan": plans_[w.name]}
+        return out
+
+    per_shape = shape_summary(per_launch, plans)
+    variant = variant_of(main_cfg)
     dom = max(bufs, key=lambda x: statistics.mean(per_launch[x[0].name]))[0]
     dom_ms = statistics.mean(per_launch[dom.name])
-    achieved = dom.flops / (dom_ms / 1e3) / 1e12
-    dom_plan = plans[dom.name]
-    kernel_key = (f"ffma_{dom_plan['bm']}x{dom_plan['bn']}x{dom_plan['bk']}_s{dom_plan['stages']}"
-                  f"_{dom.name}")
+    dp = plans[dom.name]
+    kernel_key = f"{variant}_{dp['bm']}x{dp['bn']}x{dp['bk']}_s{dp['stages']}_{dom.name}"
+    if variant == "tf32x3":
+        # Three tf32 MMAs per output product; the call's time includes the
+        # two pack kernels, so this understates the GEMM kernel's own rate.
+        achieved = 3 * dom.flops / (dom_ms / 1e3) / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": tf32_peak,
+                    "unit": "TFLOP/s", "frac": achieved / tf32_peak,
+                    "traffic": load_traffic(kernel_key), "kernel": kernel_key,
+                    "peak_basis": tf32_basis,
+                    "note": "achieved = 3 x 2MNK tf32 flops / time of the whole call "
+                            "(pack kernels included)"}
+    else:
+        achieved = dom.flops / (dom_ms / 1e3) / 1e12
+        roofline = {"bound": "alu", "achieved": achieved, "peak": ffma_peak, "unit": "TFLOP/s",
+                    "frac": achieved / ffma_peak, "traffic": load_traffic(kernel_key),
+                    "kernel": kernel_key,
+                    "peak_basis": f"{sms} SMs x 128 FP32 lanes x 2 flop x {sm_max:.0f} MHz "
+                                  "(max SM clock)",
+                    "frac_at_run_clock": achieved / ffma_live if ffma_live else None}
+
+    # The other fp32 variant, measured in the same run for comparison.
+    variants = {}
+    if not args.no_variants:
+        other = {"variant": "tf32x3"} if variant == "ffma" else {"variant": "ffma"}
+        o_steps = max(1, min(args.steps, 10))
+        o_total, o_per = measure(other, o_steps, max(1, min(args.warmup, 3)))
+        o_val = world * flops_step * o_steps / (o_total / 1e3) / 1e12
+        variants[other["variant"]] = {
+            "value": o_val, "unit": "TFLOP/s", "steps": o_steps,
+            "per_shape": shape_summary(o_per, plans_for(other)),
+            "tolerance": "5e-5*|A||B|" if other["variant"] == "tf32x3" else "1e-5*|A||B|"}
+        if other["variant"] == "tf32x3":
+            o_dom = max(bufs, key=lambda x: statistics.mean(o_per[x[0].name]))[0]
+            o_ach = 3 * o_dom.flops / (statistics.mean(o_per[o_dom.name]) / 1e3) / 1e12
+            variants["tf32x3"]["roofline"] = {
+                "bound": "tensor", "achieved": o_ach, "peak": tf32_peak, "unit": "TFLOP/s",
+                "frac": o_ach / tf32_peak, "peak_basis": tf32_basis,
+                "note": "3 tf32 MMAs per product; call time includes the pack kernels"}
 
     # End to end through the host-buffer entry point (pinned host memory).
     e2e = None
     if not args.no_e2e:
+        cfg = mt.make_config(**main_cfg) if main_cfg else None
         hbufs = []
         for (w, _a, _b, _c, A, B) in bufs:
-            hA = A.pin_memory()
-            hB = B.pin_memory()
-            hC = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
-            hbufs.append((w, hA, hB, hC))
+            hbufs.append((w, A.pin_memory(), B.pin_memory(),
+                          torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()))
 
         def host_step():
             for (w, hA, hB, hC) in hbufs:
-                st = mt.mt_sgemm_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), w.M, w.N, w.K,
-                                      sptr, cfg)
+                st = mt.mt_sgemm_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), w.M, w.N,
+                                      w.K, sptr, cfg)
                 if st != mt.MT_OK:
                     raise mt.MtError(st, "mt_sgemm_host")
         host_step()  # warm the stream-ordered pool
         e2e_steps = max(1, min(args.steps, 5))
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
+        barrier()
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
             host_step()
-        e2e_s = time.perf_counter() - t0
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e2e_s], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
+        e2e_s = max_over_ranks(time.perf_counter() - t0)
         e2e = {"value": world * flops_step * e2e_steps / e2e_s / 1e12, "unit": "TFLOP/s",
                "steps": e2e_steps,
                "h2d_bytes_per_step": sum(4 * (w.M * w.K + w.K * w.N) for (w, *_r) in hbufs),
@@ -368,21 +430,16 @@ def run_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": " + ".join(f"sgemm {w.M}x{w.N}x{w.K} ({w.dist}, seed {w.seed})"
                                               for (w, *_r) in bufs),
-                       "variant": "ffma" if not args.config else args.config,
+                       "variant": variant, "choices": main_cfg,
                        "l2": "inputs larger than L2 (192 MB and 768 MB per GEMM vs 129 MB); "
                              "the 8192^3 GEMM between 4096^3 GEMMs evicts their operands",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "per_shape": per_shape,
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_max,
-                         "unit": "TFLOP/s", "frac": achieved / peak_max,
-                         "traffic": load_traffic(kernel_key),
-                         "kernel": kernel_key,
-                         "peak_basis": f"{sms} SMs x 128 FP32 lanes x 2 flop x {sm_max:.0f} MHz "
-                                       "(max SM clock)",
-                         "frac_at_run_clock": achieved / peak_live if peak_live else None},
+            "roofline": roofline,
             "clocks": clk,
             "e2e": e2e,
-            "gpu_launches": len(bufs) * args.steps,
+            "gpu_launches": LAUNCHES_PER_CALL[variant] * len(bufs) * args.steps,
+            "variants": variants,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -402,6 +459,8 @@ def main():
     ap.add_argument("--config", help="JSON of mt_config choices, e.g. '{\"bm\":128}'")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip measuring the other fp32 variant")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "mt":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)

@@ -69,10 +69,16 @@ __global__ void __launch_bounds__(P18_THREADS) sgemm_p18_kernel(GemmArgs args) {
               : 0.0f;
     }
     __syncthreads();
+    // One 4-byte shared load per operand and k, as the page's generated loop
+    // reads them (volatile keeps the compiler from merging the A reads of a
+    // row into wider loads, which would change the access pattern the
+    // padding rule is about).
+    const volatile float* lhs = dot_lhs;
+    const volatile float* rhs = dot_rhs;
 #pragma unroll
     for (int dot_k = 0; dot_k < P18_BK; ++dot_k)
-      accumulator = fmaf(dot_lhs[LA.offset(dot_stage, tile_i, dot_k)],
-                         dot_rhs[LB.offset(dot_stage, dot_k, tile_j)], accumulator);
+      accumulator = fmaf(lhs[LA.offset(dot_stage, tile_i, dot_k)],
+                         rhs[LB.offset(dot_stage, dot_k, tile_j)], accumulator);
   }
   const int out_row = block_m + tile_i, out_col = block_n + tile_j;
   if (out_row < M && out_col < N)
