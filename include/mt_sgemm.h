@@ -142,8 +142,8 @@ MT_API mt_status mt_sgemm_host(const float *A, const float *B, float *C,
  * packed copies of A and B that variant builds go to a static device array
  * of MT_NOALLOC_SCRATCH_BYTES (32 MiB) instead of memory allocated per call;
  * this call allocates nothing.  A problem needs
- * 16384*ceil(M/128)*ceil(K/32) + 32768*ceil(N/256)*ceil(K/32) bytes of it
- * (about 4*(M + N)*K; up to about 2048 x 2048 x 2048); a larger one returns
+ * 8192*ceil(M/128)*ceil(K/16) + 16384*ceil(N/256)*ceil(K/16) bytes of it
+ * (about 8*(M + N)*K; up to about 1448 x 1448 x 1448); a larger one returns
  * MT_ERR_SCRATCH_LIMIT and launches nothing (mt_sgemm_plan reports the
  * bytes as workspace_bytes).  Other errors as mt_sgemm_ex.
  *

@@ -47,19 +47,29 @@ def assert_within(C, Cref, W, tol, what=""):
                     f"max err/W {(err / np.maximum(W, 1e-300)).max():.3g}")
 
 
-def test_plan_reports_tile_and_workspace():
-    p = mt.plan(4096, 4096, 4096, variant="tf32x3")
-    assert (p["bm"], p["bn"], p["bk"], p["stages"], p["threads"]) == (128, 256, 32, 2, 192)
-    # Packed copies of A (128-row blocks) and B (256-row blocks), 32 k each.
-    assert p["workspace_bytes"] == 4096 * 4096 * 4 * 2
+# Both K depths the kernel is built for: 16 (64-byte swizzle, 4 stages) and
+# 32 (128-byte swizzle, 2 stages).
+DEPTHS = [dict(variant="tf32x3", bk=16), dict(variant="tf32x3", bk=32)]
+DEPTH_IDS = ["bk16", "bk32"]
+
+
+@pytest.mark.parametrize("bk,stages", [(16, 4), (32, 2)])
+def test_plan_reports_tile_and_workspace(bk, stages):
+    p = mt.plan(4096, 4096, 4096, variant="tf32x3", bk=bk)
+    assert (p["bm"], p["bn"], p["bk"], p["stages"], p["threads"]) == (128, 256, bk, stages, 192)
+    # Packed big and small copies of A (128-row blocks) and B (256-row
+    # blocks), bk k each.
+    assert p["workspace_bytes"] == 4096 * 4096 * 4 * 4
     assert p["grid"] == 32 * 16
+    assert mt.plan(4096, 4096, 4096, variant="tf32x3")["bk"] == 16  # the default depth
 
 
+@pytest.mark.parametrize("cfg", DEPTHS, ids=DEPTH_IDS)
 @pytest.mark.parametrize("name", ["masked_100x72x80", "square_1024", "ragged_4097x3001x2053"])
-def test_workloads_full_oracle(name):
+def test_workloads_full_oracle(name, cfg):
     A, B = gemm_inputs.make_workload(name)
     Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
-    assert_within(run(A, B, **TF32).numpy(), Cref, W, TOL, name)
+    assert_within(run(A, B, **cfg).numpy(), Cref, W, TOL, name)
 
 
 @pytest.mark.parametrize("name", ["square_4096", "square_8192", "skinny_65536x128x4096"])
@@ -75,12 +85,13 @@ def test_full_size_sampled_rows(name):
     assert_within(c[torch.from_numpy(rows).cuda()].cpu().numpy(), Cr, Wr, TOL, name)
 
 
+@pytest.mark.parametrize("cfg", DEPTHS, ids=DEPTH_IDS)
 @pytest.mark.parametrize("shape", [(100, 72, 80), (257, 130, 77), (128, 256, 96),
                                    (300, 520, 1000)])
-def test_integer_inputs_bit_exact(shape):
+def test_integer_inputs_bit_exact(shape, cfg):
     M, N, K = shape
     A, B = gemm_inputs.make_ab(M, N, K, seed=21, dist="int")
-    assert np.array_equal(run(A, B, **TF32).numpy(), oracle.sgemm(A.numpy(), B.numpy()))
+    assert np.array_equal(run(A, B, **cfg).numpy(), oracle.sgemm(A.numpy(), B.numpy()))
 
 
 TINY = [(1, 1, 1), (1, 7, 3), (5, 1, 9), (3, 5, 7), (17, 15, 33), (31, 33, 1),
@@ -92,7 +103,8 @@ def test_tiny_ragged(shape):
     M, N, K = shape
     A, B = gemm_inputs.make_ab(M, N, K, seed=M * 7 + N * 3 + K, dist="normal")
     Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
-    assert_within(run(A, B, **TF32).numpy(), Cref, W, TOL, str(shape))
+    for cfg in DEPTHS:
+        assert_within(run(A, B, **cfg).numpy(), Cref, W, TOL, f"{shape} {cfg}")
 
 
 def test_identity_within_tolerance():

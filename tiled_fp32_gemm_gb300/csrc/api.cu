@@ -16,6 +16,9 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxEntries = 32;
+// K depth of the 3xTF32 kernel when the caller does not choose: 16 (4-stage
+// ring, 64-byte swizzle).
+constexpr int kTf32x3DefaultBk = 16;
 
 struct DeviceInfo {
   int sms = 0;
@@ -166,11 +169,13 @@ mt_status plan_call(const float* A, const float* B, const float* C, int64_t M, i
     return MT_OK;
   }
   if (variant == MT_VARIANT_TF32X3) {
-    int bm, bn, bk, stages;
-    mt::tf32x3_tile(&bm, &bn, &bk, &stages);
+    int bm, bn;
+    mt::tf32x3_tile(&bm, &bn);
+    const int bk = cfg && cfg->bk ? cfg->bk : kTf32x3DefaultBk;
+    if (!mt::tf32x3_valid_bk(bk)) return MT_ERR_UNSUPPORTED;
+    const int stages = mt::tf32x3_stages(bk);
     if (cfg && ((cfg->bm && cfg->bm != bm) || (cfg->bn && cfg->bn != bn) ||
-                (cfg->bk && cfg->bk != bk) || (cfg->stages && cfg->stages != stages) ||
-                cfg->fma || cfg->no_pad))
+                (cfg->stages && cfg->stages != stages) || cfg->fma || cfg->no_pad))
       return MT_ERR_UNSUPPORTED;
     p.bm = bm; p.bn = bn; p.bk = bk; p.stages = stages;
     p.threads = mt::tf32x3_threads();
@@ -178,13 +183,13 @@ mt_status plan_call(const float* A, const float* B, const float* C, int64_t M, i
     // The pack kernel reads A in float4 when K % 4 == 0 and A is 16-byte aligned.
     p.vec_ab = (K % 4 == 0) && aligned16(A);
     p.vec_c = (N % 4 == 0) && aligned16(C);
-    p.smem_bytes = mt::tf32x3_smem_bytes();
+    p.smem_bytes = mt::tf32x3_smem_bytes(bk);
     L->tiles_m = static_cast<int>(ceil_div(M, bm));
     L->tiles_n = static_cast<int>(ceil_div(N, bn));
     if (L->tiles_m > 65535 || L->tiles_n > 65535) return MT_ERR_UNSUPPORTED;
     p.grid = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
     p.workspace_bytes = mt::tf32x3_workspace_bytes(static_cast<int>(M), static_cast<int>(N),
-                                                   static_cast<int>(K));
+                                                   static_cast<int>(K), bk);
     if (p.smem_bytes > smem_limit) return MT_ERR_SMEM_BUDGET;
     return MT_OK;
   }
@@ -294,19 +299,27 @@ mt_status pool_for(int dev, cudaMemPool_t* pool) {
   return MT_OK;
 }
 
-std::atomic<uint8_t> g_tf32x3_ready[kMaxDevices];
+// [device][bk == 32]: shared-memory attribute of the 3xTF32 kernel applied.
+std::atomic<uint8_t> g_tf32x3_ready[kMaxDevices][2];
 
-mt_status run_tf32x3(int dev, const mt::GemmArgs& args, const Launch& L, cudaStream_t stream) {
-  if (!g_tf32x3_ready[dev].load(std::memory_order_acquire)) {
+mt_status prepare_tf32x3(int dev, int bk) {
+  std::atomic<uint8_t>& ready = g_tf32x3_ready[dev][bk == 32 ? 1 : 0];
+  if (!ready.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_tf32x3_ready[dev].load(std::memory_order_relaxed)) {
-      if (mt::tf32x3_prepare(dev) != cudaSuccess) {
+    if (!ready.load(std::memory_order_relaxed)) {
+      if (mt::tf32x3_prepare(dev, bk) != cudaSuccess) {
         cudaGetLastError();
         return MT_ERR_LAUNCH;
       }
-      g_tf32x3_ready[dev].store(1, std::memory_order_release);
+      ready.store(1, std::memory_order_release);
     }
   }
+  return MT_OK;
+}
+
+mt_status run_tf32x3(int dev, const mt::GemmArgs& args, const Launch& L, cudaStream_t stream) {
+  mt_status st0 = prepare_tf32x3(dev, L.plan.bk);
+  if (st0 != MT_OK) return st0;
   cudaMemPool_t pool = nullptr;
   mt_status st = pool_for(dev, &pool);
   if (st != MT_OK) return st;
@@ -317,7 +330,8 @@ mt_status run_tf32x3(int dev, const mt::GemmArgs& args, const Launch& L, cudaStr
     return MT_ERR_CUDA;
   }
   const cudaError_t e =
-      mt::launch_tf32x3(args, ws, L.plan.vec_ab != 0, L.plan.vec_c != 0, L.fault_inject, stream);
+      mt::launch_tf32x3(args, ws, L.plan.vec_ab != 0, L.plan.vec_c != 0, L.plan.bk,
+                        L.fault_inject, stream);
   cudaFreeAsync(ws, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -382,7 +396,6 @@ mt_status mt_sgemm_host(const float* A, const float* B, float* C, int64_t M, int
 mt_status mt_sgemm_tf32x3_noalloc(const float* A, const float* B, float* C, int64_t M,
                                   int64_t N, int64_t K, cudaStream_t stream) {
   static_assert(MT_NOALLOC_SCRATCH_BYTES == mt::kNoAllocScratchBytes, "scratch size");
-  static std::atomic<uint8_t> prepared[kMaxDevices];
   mt_status st = check_args(A, B, C, M, N, K);
   if (st != MT_OK) return st;
   if (M == 0 || N == 0) return MT_OK;
@@ -405,16 +418,8 @@ mt_status mt_sgemm_tf32x3_noalloc(const float* A, const float* B, float* C, int6
     return MT_OK;
   }
   if (L.plan.workspace_bytes > MT_NOALLOC_SCRATCH_BYTES) return MT_ERR_SCRATCH_LIMIT;
-  if (!prepared[dev].load(std::memory_order_acquire)) {
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (!prepared[dev].load(std::memory_order_relaxed)) {
-      if (mt::tf32x3_prepare(dev) != cudaSuccess) {
-        cudaGetLastError();
-        return MT_ERR_LAUNCH;
-      }
-      prepared[dev].store(1, std::memory_order_release);
-    }
-  }
+  st = prepare_tf32x3(dev, L.plan.bk);
+  if (st != MT_OK) return st;
   void* scratch = nullptr;
   if (mt::tf32x3_noalloc_scratch(dev, &scratch) != cudaSuccess || !scratch) {
     cudaGetLastError();
@@ -422,7 +427,8 @@ mt_status mt_sgemm_tf32x3_noalloc(const float* A, const float* B, float* C, int6
   }
   mt::GemmArgs args{A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                     L.tiles_m, L.tiles_n, L.group_m};
-  if (mt::launch_tf32x3(args, scratch, L.plan.vec_ab != 0, L.plan.vec_c != 0, 0, stream) !=
+  if (mt::launch_tf32x3(args, scratch, L.plan.vec_ab != 0, L.plan.vec_c != 0, L.plan.bk, 0,
+                        stream) !=
       cudaSuccess) {
     cudaGetLastError();
     return MT_ERR_LAUNCH;

@@ -16,22 +16,22 @@
 //     A*B ~= A_big*B_small + A_small*B_big + A_big*B_big
 // (A_small*B_small, about 2^-22 relative, is dropped), accumulated in fp32.
 //
-// Pipeline of one CTA (one 128 x 256 tile of C, 192 threads):
-//   pack kernels (before): A and B are copied once into zero-padded,
-//     K-major blocks of 128 (A) or 256 (B) rows x 32 k, already in the
-//     tensor core's 128-byte-swizzled shared-memory order, so the main loop
-//     moves each block with one cp.async.bulk and needs no alignment of the
-//     caller's leading dimensions;
-//   warp 0, one thread: bulk copies of the A and B blocks of K tile kt into
-//     stage kt % 2, completion counted on full[s];
-//   warps 2-5 (128 threads): wait full[s], split every fp32 in place into
-//     big and a separate small buffer, fence to the async proxy, arrive on
-//     conv[s];
-//   warp 1, one thread: wait conv[s], issue 4 k-steps x 3 tcgen05.mma
+// Pipeline of one CTA (one 128 x 256 tile of C, 192 threads), for a K
+// depth BK of 32 (128-byte swizzle, 2 stages of 96 KB) or 16 (64-byte
+// swizzle, 4 stages of 48 KB):
+//   pack kernels (before): A and B are read once, every value is split into
+//     big and small, and both halves are written as zero-padded, K-major
+//     blocks of 128 (A) or 256 (B) rows x BK k, already in the tensor
+//     core's swizzled shared-memory order; so the main loop moves each
+//     operand pair with one cp.async.bulk, does no arithmetic on the
+//     operands and needs no alignment of the caller's leading dimensions;
+//   warp 0, one thread: bulk copies of the A and B block pairs of K tile kt
+//     into stage kt % STAGES, completion counted on full[s];
+//   warp 1, one thread: wait full[s], issue BK/8 k-steps x 3 tcgen05.mma
 //     (128x256x8 each) into the TMEM accumulator, tcgen05.commit -> empty[s]
 //     (frees the stage for the producer), and after the last tile -> done;
-//   warps 2-5: wait done, tcgen05.ld their 32 TMEM lanes (rows), masked
-//     stores to C.
+//   warps 2-5 (128 threads, TMEM lane quarters 2, 3, 0, 1): wait done,
+//     tcgen05.ld their 32 TMEM lanes (rows), masked stores to C.
 // Every wait is bounded (%globaltimer); on expiry the CTA records
 // MT_ERR_TIMEOUT in a device status word, stops issuing, drains what it
 // issued (again bounded), frees TMEM and returns.
@@ -46,40 +46,76 @@
 namespace mt {
 namespace tf32x3 {
 
-constexpr int BM = 128, BN = 256, BK = 32, STAGES = 2;
-constexpr int A_BLOCK_BYTES = BM * BK * 4;  // 16 KB
-constexpr int B_BLOCK_BYTES = BN * BK * 4;  // 32 KB
-// Stage: A big | A small | B big | B small.
-constexpr int STAGE_BYTES = 2 * A_BLOCK_BYTES + 2 * B_BLOCK_BYTES;  // 96 KB
+constexpr int BM = 128, BN = 256;
 constexpr int THREADS = 192;
-constexpr int CONVERT_THREADS = 128;
 constexpr uint32_t TMEM_COLS = 256;  // fp32 accumulator: 128 lanes x 256 columns
 constexpr uint64_t TIMEOUT_NS = 1000000000ull;  // 1 s per wait
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment*/ + 256 /*barriers*/;
 
 __device__ unsigned int g_status;  // bit 0: a bounded wait expired
 
-// Byte offset of element (r, k), k < 32, inside a K-major block whose rows
-// are 32 fp32 (128 bytes) long, in the 128-byte swizzle the tensor core
-// reads: rows grouped by 8 into 1024-byte atoms, and the 16-byte chunk index
-// XOR-ed with the row's position inside its atom.
-__host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t k) {
-  const uint32_t r8 = r & 7u;
-  return (r >> 3) * 1024u + r8 * 128u + ((((k >> 2) ^ r8) & 7u) << 4) + (k & 3u) * 4u;
-}
+// Shared-memory geometry for a K depth of BK fp32 per stage.  Blocks are
+// K-major: each of the 128 (A) or 256 (B) rows holds BK consecutive k
+// (ROW_BYTES), rows are grouped by 8 into swizzle atoms, and inside an atom
+// the 16-byte chunk index of a row is XOR-ed with the row's position —
+// all of it (BK = 32, 128-byte swizzle) or its upper two bits (BK = 16,
+// 64-byte swizzle) — the pattern the tensor core applies to the address
+// bits when it reads the operand.
+template <int BK_>
+struct Geometry {
+  static_assert(BK_ == 32 || BK_ == 16, "BK is 32 or 16");
+  static constexpr int BK = BK_;
+  static constexpr int ROW_BYTES = BK * 4;
+  static constexpr int ATOM_BYTES = 8 * ROW_BYTES;
+  static constexpr uint32_t CHUNK_MASK = ROW_BYTES / 16 - 1;
+  static constexpr uint64_t LAYOUT = BK == 32 ? 2 : 4;  // descriptor: 128-B / 64-B swizzle
+  static constexpr int STAGES = BK == 32 ? 2 : 4;
+  static constexpr int A_BLOCK_BYTES = BM * ROW_BYTES;
+  static constexpr int B_BLOCK_BYTES = BN * ROW_BYTES;
+  // Packed pairs in global memory and stages in shared memory alike:
+  // A big | A small and B big | B small.  Stage: A pair | B pair.
+  static constexpr int STAGE_BYTES = 2 * A_BLOCK_BYTES + 2 * B_BLOCK_BYTES;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment*/ + 256 /*barriers*/;
+
+  // Byte offset of element (r, k), k < BK, inside a block.
+  __host__ __device__ static __forceinline__ uint32_t offset(uint32_t r, uint32_t k) {
+    const uint32_t r8 = r & 7u;
+    const uint32_t x = BK == 32 ? r8 : (r8 >> 1);
+    return (r >> 3) * ATOM_BYTES + r8 * ROW_BYTES + ((((k >> 2) ^ x) & CHUNK_MASK) << 4) +
+           (k & 3u) * 4u;
+  }
+};
 
 // ---------------------------------------------------------------------------
-// Pack kernels: caller's row-major A, B -> swizzled K-major blocks (zero fill).
+// Pack kernels: caller's row-major A, B -> split, swizzled K-major block
+// pairs (zero fill).
 
-// grid (Kt, Mt), 256 threads: block (tm, kt) = A[tm*128 + r][kt*32 + k].
+// big = x with the low 13 mantissa bits cleared; small = x - big (exact).
+// Infinities and NaNs keep their bits in big and contribute 0 through small.
+__device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
+  const uint32_t u = __float_as_uint(x);
+  const bool special = (u & 0x7F800000u) == 0x7F800000u;
+  big = special ? x : __uint_as_float(u & 0xFFFFE000u);
+  small = special ? 0.0f : x - big;
+}
+
+__device__ __forceinline__ void split4(float4 x, float4& big, float4& small) {
+  split_tf32(x.x, big.x, small.x);
+  split_tf32(x.y, big.y, small.y);
+  split_tf32(x.z, big.z, small.z);
+  split_tf32(x.w, big.w, small.w);
+}
+
+// grid (Kt, Mt), 256 threads: block (tm, kt) = A[tm*128 + r][kt*BK + k].
+template <int BK>
 __global__ void __launch_bounds__(256) pack_a_kernel(const float* __restrict__ A,
                                                      float* __restrict__ Ap, int M, int K,
                                                      int Kt, int vec) {
+  using G = Geometry<BK>;
   const int kt = blockIdx.x, tm = blockIdx.y;
   char* dst = reinterpret_cast<char*>(Ap) +
-              (static_cast<int64_t>(tm) * Kt + kt) * static_cast<int64_t>(A_BLOCK_BYTES);
+              (static_cast<int64_t>(tm) * Kt + kt) * static_cast<int64_t>(2 * G::A_BLOCK_BYTES);
   for (int c = threadIdx.x; c < BM * (BK / 4); c += 256) {
-    const int r = c >> 3, ch = c & 7;
+    const int r = c / (BK / 4), ch = c % (BK / 4);
     const int m = tm * BM + r, k = kt * BK + ch * 4;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (m < M) {
@@ -93,20 +129,26 @@ __global__ void __launch_bounds__(256) pack_a_kernel(const float* __restrict__ A
         if (k + 3 < K) v.w = src[3];
       }
     }
-    *reinterpret_cast<float4*>(dst + sw128_offset(r, ch * 4)) = v;
+    float4 big, small;
+    split4(v, big, small);
+    const uint32_t off = G::offset(r, ch * 4);
+    *reinterpret_cast<float4*>(dst + off) = big;
+    *reinterpret_cast<float4*>(dst + G::A_BLOCK_BYTES + off) = small;
   }
 }
 
-// grid (Kt, Nt), 256 threads: block (tn, kt) row n = B[kt*32 + k][tn*256 + n].
+// grid (Kt, Nt), 256 threads: block (tn, kt) row n = B[kt*BK + k][tn*256 + n].
 // Thread t owns row n = t: it reads one column of the B tile (coalesced
-// across the warp) and writes its 128-byte row.
+// across the warp) and writes its row of BK values.
+template <int BK>
 __global__ void __launch_bounds__(256) pack_b_kernel(const float* __restrict__ B,
                                                      float* __restrict__ Bp, int K, int N,
                                                      int Kt) {
+  using G = Geometry<BK>;
   const int kt = blockIdx.x, tn = blockIdx.y, t = threadIdx.x;
   const int n = tn * BN + t;
   char* dst = reinterpret_cast<char*>(Bp) +
-              (static_cast<int64_t>(tn) * Kt + kt) * static_cast<int64_t>(B_BLOCK_BYTES);
+              (static_cast<int64_t>(tn) * Kt + kt) * static_cast<int64_t>(2 * G::B_BLOCK_BYTES);
   float v[BK];
 #pragma unroll
   for (int j = 0; j < BK; ++j) {
@@ -114,9 +156,13 @@ __global__ void __launch_bounds__(256) pack_b_kernel(const float* __restrict__ B
     v[j] = (n < N && k < K) ? B[static_cast<int64_t>(k) * N + n] : 0.f;
   }
 #pragma unroll
-  for (int ch = 0; ch < BK / 4; ++ch)
-    *reinterpret_cast<float4*>(dst + sw128_offset(t, ch * 4)) =
-        make_float4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
+  for (int ch = 0; ch < BK / 4; ++ch) {
+    float4 big, small;
+    split4(make_float4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]), big, small);
+    const uint32_t off = G::offset(t, ch * 4);
+    *reinterpret_cast<float4*>(dst + off) = big;
+    *reinterpret_cast<float4*>(dst + G::B_BLOCK_BYTES + off) = small;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -174,15 +220,18 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor: K-major operand in 128-byte swizzle,
-// 8-row atoms 1024 bytes apart (stride byte offset), descriptor version 1.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+// Shared-memory matrix descriptor of a K-major operand block: start address,
+// 8-row atoms `atom_bytes` apart (stride byte offset), swizzle `layout`
+// (2 = 128-byte, 4 = 64-byte), descriptor version 1.  The leading byte
+// offset is unused for swizzled K-major operands.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t atom_bytes,
+                                              uint64_t layout) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);  // start address, 16-byte units
-  d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused here)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset: 1024 bytes
+  d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused)
+  d |= static_cast<uint64_t>(atom_bytes >> 4) << 32;    // stride byte offset
   d |= static_cast<uint64_t>(1) << 46;                  // descriptor version
-  d |= static_cast<uint64_t>(2) << 61;                  // 128-byte swizzle
+  d |= layout << 61;                                    // swizzle mode
   return d;
 }
 
@@ -249,13 +298,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 // aborting (another role gave up) or this wait itself ran out of time, in
 // which case it raises the abort flag and the device status word.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
-                                           volatile int* abort_flag, bool honour_abort = true) {
+                                           volatile int* abort_flag, bool honour_abort = true,
+                                           uint64_t limit_ns = TIMEOUT_NS) {
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 15u) == 15u) {
       if (honour_abort && *abort_flag) return false;
-      if (globaltimer() - t0 > TIMEOUT_NS) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(&g_status, 1u);
         return false;
@@ -264,37 +314,23 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
   }
 }
 
-// big = x with the low 13 mantissa bits cleared; small = x - big (exact).
-// Infinities and NaNs keep their bits in big and contribute 0 through small.
-__device__ __forceinline__ void split_tf32(float x, float& big, float& small) {
-  const uint32_t u = __float_as_uint(x);
-  const bool special = (u & 0x7F800000u) == 0x7F800000u;
-  big = special ? x : __uint_as_float(u & 0xFFFFE000u);
-  small = special ? 0.0f : x - big;
-}
-
-__device__ __forceinline__ void split4(uint8_t* big_buf, uint8_t* small_buf, uint32_t off) {
-  float4 x = *reinterpret_cast<float4*>(big_buf + off);
-  float4 b, s;
-  split_tf32(x.x, b.x, s.x);
-  split_tf32(x.y, b.y, s.y);
-  split_tf32(x.z, b.z, s.z);
-  split_tf32(x.w, b.w, s.w);
-  *reinterpret_cast<float4*>(big_buf + off) = b;
-  *reinterpret_cast<float4*>(small_buf + off) = s;
-}
-
 // ---------------------------------------------------------------------------
+template <int BK>
 __global__ void __launch_bounds__(THREADS, 1)
     tf32x3_gemm_kernel(const float* __restrict__ Ap, const float* __restrict__ Bp,
                        float* __restrict__ C, int M, int N, int Kt, int tiles_m, int tiles_n,
                        int group_m, int vec_c, int fault_inject) {
+  using G = Geometry<BK>;
+  constexpr int STAGES = G::STAGES;
+  constexpr int STAGE_BYTES = G::STAGE_BYTES;
+  constexpr int A_BLOCK_BYTES = G::A_BLOCK_BYTES;
+  constexpr int B_BLOCK_BYTES = G::B_BLOCK_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  // bars[0..S): full, [S..2S): conv, [2S..3S): empty, [3S]: done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 1);
+  // bars[0..S): full, [S..2S): empty, [2S]: done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
@@ -304,11 +340,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar(s), 1);                          // full: producer + tx bytes
-      mbar_init(bar(STAGES + s), CONVERT_THREADS);   // conv: every converter
-      mbar_init(bar(2 * STAGES + s), 1);             // empty: MMA commit
+      mbar_init(bar(s), 1);           // full: producer + tx bytes
+      mbar_init(bar(STAGES + s), 1);  // empty: MMA commit
     }
-    mbar_init(bar(3 * STAGES), 1);  // done: final MMA commit
+    mbar_init(bar(2 * STAGES), 1);  // done: final MMA commit
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -319,9 +354,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   const char* a_src = reinterpret_cast<const char*>(Ap) +
-                      static_cast<int64_t>(tm) * Kt * static_cast<int64_t>(A_BLOCK_BYTES);
+                      static_cast<int64_t>(tm) * Kt * static_cast<int64_t>(2 * A_BLOCK_BYTES);
   const char* b_src = reinterpret_cast<const char*>(Bp) +
-                      static_cast<int64_t>(tn) * Kt * static_cast<int64_t>(B_BLOCK_BYTES);
+                      static_cast<int64_t>(tn) * Kt * static_cast<int64_t>(2 * B_BLOCK_BYTES);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -331,13 +366,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int kt = 0; kt < (fault_inject ? 0 : Kt); ++kt) {
         const int s = kt % STAGES;
         const uint32_t round = static_cast<uint32_t>(kt / STAGES);
-        if (kt >= STAGES && !wait_phase(bar(2 * STAGES + s), (round + 1) & 1u, abort_flag)) break;
+        if (kt >= STAGES && !wait_phase(bar(STAGES + s), (round + 1) & 1u, abort_flag)) break;
         uint8_t* st = smem + s * STAGE_BYTES;
-        mbar_arrive_expect_tx(bar(s), A_BLOCK_BYTES + B_BLOCK_BYTES);
-        bulk_copy_g2s(smem_u32(st), a_src + static_cast<int64_t>(kt) * A_BLOCK_BYTES,
-                      A_BLOCK_BYTES, bar(s));
+        mbar_arrive_expect_tx(bar(s), STAGE_BYTES);
+        bulk_copy_g2s(smem_u32(st), a_src + static_cast<int64_t>(kt) * (2 * A_BLOCK_BYTES),
+                      2 * A_BLOCK_BYTES, bar(s));
         bulk_copy_g2s(smem_u32(st + 2 * A_BLOCK_BYTES),
-                      b_src + static_cast<int64_t>(kt) * B_BLOCK_BYTES, B_BLOCK_BYTES, bar(s));
+                      b_src + static_cast<int64_t>(kt) * (2 * B_BLOCK_BYTES), 2 * B_BLOCK_BYTES,
+                      bar(s));
         issued = kt + 1;
       }
       if (*abort_flag) {
@@ -355,7 +391,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int kt = 0; kt < Kt; ++kt) {
         const int s = kt % STAGES;
         const uint32_t round = static_cast<uint32_t>(kt / STAGES);
-        if (!wait_phase(bar(STAGES + s), round & 1u, abort_flag)) break;
+        if (!wait_phase(bar(s), round & 1u, abort_flag)) break;
         tc_fence_after();
         const uint32_t a_big = smem_u32(smem + s * STAGE_BYTES);
         const uint32_t a_small = a_big + A_BLOCK_BYTES;
@@ -364,47 +400,31 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int j = 0; j < BK / 8; ++j) {
           const uint32_t koff = j * 32;  // 8 tf32 = 32 bytes along K
-          mma_tf32(tmem, smem_desc_sw128(a_big + koff), smem_desc_sw128(b_small + koff), idesc,
-                   acc);
+          const uint64_t ab = smem_desc(a_big + koff, G::ATOM_BYTES, G::LAYOUT);
+          const uint64_t as = smem_desc(a_small + koff, G::ATOM_BYTES, G::LAYOUT);
+          const uint64_t bb = smem_desc(b_big + koff, G::ATOM_BYTES, G::LAYOUT);
+          const uint64_t bs = smem_desc(b_small + koff, G::ATOM_BYTES, G::LAYOUT);
+          mma_tf32(tmem, ab, bs, idesc, acc);
           acc = 1;
-          mma_tf32(tmem, smem_desc_sw128(a_small + koff), smem_desc_sw128(b_big + koff), idesc, 1);
-          mma_tf32(tmem, smem_desc_sw128(a_big + koff), smem_desc_sw128(b_big + koff), idesc, 1);
+          mma_tf32(tmem, as, bb, idesc, 1);
+          mma_tf32(tmem, ab, bb, idesc, 1);
         }
-        mma_commit(bar(2 * STAGES + s));
+        mma_commit(bar(STAGES + s));
       }
       // After the last MMA (or on abort, after whatever was issued).
-      mma_commit(bar(3 * STAGES));
+      mma_commit(bar(2 * STAGES));
     }
   } else {
-    // Converters, then the epilogue (warps 2..5 cover TMEM lane quarters
-    // 2, 3, 0, 1).
-    const int ct = threadIdx.x - 64;
-    bool ok = true;
-    for (int kt = 0; kt < Kt && ok; ++kt) {
-      const int s = kt % STAGES;
-      const uint32_t round = static_cast<uint32_t>(kt / STAGES);
-      if (!wait_phase(bar(s), round & 1u, abort_flag)) {
-        ok = false;
-        break;
-      }
-      uint8_t* st = smem + s * STAGE_BYTES;
-      uint8_t* a_big = st;
-      uint8_t* a_small = st + A_BLOCK_BYTES;
-      uint8_t* b_big = st + 2 * A_BLOCK_BYTES;
-      uint8_t* b_small = b_big + B_BLOCK_BYTES;
-#pragma unroll 4
-      for (int c = ct; c < A_BLOCK_BYTES / 16; c += CONVERT_THREADS) split4(a_big, a_small, c * 16);
-#pragma unroll 4
-      for (int c = ct; c < B_BLOCK_BYTES / 16; c += CONVERT_THREADS) split4(b_big, b_small, c * 16);
-      fence_proxy_async_smem();
-      mbar_arrive(bar(STAGES + s));
-    }
-    // Wait for the accumulator even after an abort, so no MMA is in flight
-    // when TMEM is released.
-    const bool done = wait_phase(bar(3 * STAGES), 0, abort_flag, false);
+    // Epilogue warps (2..5 cover TMEM lane quarters 2, 3, 0, 1).  Wait for
+    // the accumulator even after an abort, so no MMA is in flight when TMEM
+    // is released.
+    // The accumulator is ready only after the whole K loop: allow 20 us per
+    // K tile on top of the usual limit.
+    const bool done = wait_phase(bar(2 * STAGES), 0, abort_flag, false,
+                                 TIMEOUT_NS + 20000ull * static_cast<uint64_t>(Kt));
     tc_fence_after();
     __syncwarp();
-    if (ok && done && !*abort_flag) {
+    if (done && !*abort_flag) {
       const int q = warp & 3;  // TMEM lane quarter this warp may access
       const int row = tm * BM + q * 32 + lane;
       const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
@@ -443,41 +463,65 @@ __global__ void __launch_bounds__(THREADS, 1)
 }  // namespace tf32x3
 
 // ---------------------------------------------------------------------------
-int64_t tf32x3_workspace_bytes(int M, int N, int K) {
+template <int BK>
+int64_t workspace_bytes_for(int M, int N, int K) {
+  using G = tf32x3::Geometry<BK>;
   const int64_t mt = (M + tf32x3::BM - 1) / tf32x3::BM;
   const int64_t nt = (N + tf32x3::BN - 1) / tf32x3::BN;
-  const int64_t kt = (K + tf32x3::BK - 1) / tf32x3::BK;
-  return mt * kt * tf32x3::A_BLOCK_BYTES + nt * kt * tf32x3::B_BLOCK_BYTES;
+  const int64_t kt = (K + BK - 1) / BK;
+  return 2 * (mt * kt * G::A_BLOCK_BYTES + nt * kt * G::B_BLOCK_BYTES);
 }
 
-int tf32x3_smem_bytes() { return tf32x3::SMEM_BYTES; }
+bool tf32x3_valid_bk(int bk) { return bk == 16 || bk == 32; }
+
+int64_t tf32x3_workspace_bytes(int M, int N, int K, int bk) {
+  return bk == 32 ? workspace_bytes_for<32>(M, N, K) : workspace_bytes_for<16>(M, N, K);
+}
+
+int tf32x3_smem_bytes(int bk) {
+  return bk == 32 ? tf32x3::Geometry<32>::SMEM_BYTES : tf32x3::Geometry<16>::SMEM_BYTES;
+}
+int tf32x3_stages(int bk) {
+  return bk == 32 ? tf32x3::Geometry<32>::STAGES : tf32x3::Geometry<16>::STAGES;
+}
 int tf32x3_threads() { return tf32x3::THREADS; }
-void tf32x3_tile(int* bm, int* bn, int* bk, int* stages) {
+void tf32x3_tile(int* bm, int* bn) {
   *bm = tf32x3::BM;
   *bn = tf32x3::BN;
-  *bk = tf32x3::BK;
-  *stages = tf32x3::STAGES;
 }
 
-cudaError_t tf32x3_prepare(int device) {
+cudaError_t tf32x3_prepare(int device, int bk) {
   (void)device;
-  return cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, tf32x3::SMEM_BYTES);
+  if (bk == 32)
+    return cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<32>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                tf32x3::Geometry<32>::SMEM_BYTES);
+  return cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<16>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              tf32x3::Geometry<16>::SMEM_BYTES);
 }
 
-cudaError_t launch_tf32x3(const GemmArgs& a, void* workspace, bool vec_ab, bool vec_c,
-                          int fault_inject, cudaStream_t stream) {
+template <int BK>
+cudaError_t launch_tf32x3_bk(const GemmArgs& a, void* workspace, bool vec_ab, bool vec_c,
+                             int fault_inject, cudaStream_t stream) {
   using namespace tf32x3;
+  using G = Geometry<BK>;
   const int mt = (a.M + BM - 1) / BM, nt = (a.N + BN - 1) / BN, kt = (a.K + BK - 1) / BK;
   if (mt > 65535 || nt > 65535) return cudaErrorInvalidValue;
   float* Ap = static_cast<float*>(workspace);
   float* Bp = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                       static_cast<int64_t>(mt) * kt * A_BLOCK_BYTES);
-  pack_a_kernel<<<dim3(kt, mt), 256, 0, stream>>>(a.A, Ap, a.M, a.K, kt, vec_ab ? 1 : 0);
-  pack_b_kernel<<<dim3(kt, nt), 256, 0, stream>>>(a.B, Bp, a.K, a.N, kt);
-  tf32x3_gemm_kernel<<<static_cast<unsigned>(mt * nt), THREADS, SMEM_BYTES, stream>>>(
+                                       static_cast<int64_t>(mt) * kt * 2 * G::A_BLOCK_BYTES);
+  pack_a_kernel<BK><<<dim3(kt, mt), 256, 0, stream>>>(a.A, Ap, a.M, a.K, kt, vec_ab ? 1 : 0);
+  pack_b_kernel<BK><<<dim3(kt, nt), 256, 0, stream>>>(a.B, Bp, a.K, a.N, kt);
+  tf32x3_gemm_kernel<BK><<<static_cast<unsigned>(mt * nt), THREADS, G::SMEM_BYTES, stream>>>(
       Ap, Bp, a.C, a.M, a.N, kt, mt, nt, a.group_m, vec_c ? 1 : 0, fault_inject);
   return cudaGetLastError();
+}
+
+cudaError_t launch_tf32x3(const GemmArgs& a, void* workspace, bool vec_ab, bool vec_c, int bk,
+                          int fault_inject, cudaStream_t stream) {
+  if (bk == 32) return launch_tf32x3_bk<32>(a, workspace, vec_ab, vec_c, fault_inject, stream);
+  return launch_tf32x3_bk<16>(a, workspace, vec_ab, vec_c, fault_inject, stream);
 }
 
 // ---------------------------------------------------------------------------
