@@ -47,21 +47,25 @@ def assert_within(C, Cref, W, tol, what=""):
                     f"max err/W {(err / np.maximum(W, 1e-300)).max():.3g}")
 
 
-# Both K depths the kernel is built for: 16 (64-byte swizzle, 4 stages) and
-# 32 (128-byte swizzle, 2 stages).
-DEPTHS = [dict(variant="tf32x3", bk=16), dict(variant="tf32x3", bk=32)]
-DEPTH_IDS = ["bk16", "bk32"]
+# Every configuration the kernel is built for: K depth 16 (64-byte swizzle)
+# or 32 (128-byte swizzle) x tile width 256, 128 or 64.
+DEPTHS = [dict(variant="tf32x3", bk=bk, bn=bn) for bk in (16, 32) for bn in (256, 128, 64)]
+DEPTH_IDS = [f"bk{c['bk']}-bn{c['bn']}" for c in DEPTHS]
 
 
-@pytest.mark.parametrize("bk,stages", [(16, 4), (32, 2)])
-def test_plan_reports_tile_and_workspace(bk, stages):
-    p = mt.plan(4096, 4096, 4096, variant="tf32x3", bk=bk)
-    assert (p["bm"], p["bn"], p["bk"], p["stages"], p["threads"]) == (128, 256, bk, stages, 192)
-    # Packed big and small copies of A (128-row blocks) and B (256-row
+@pytest.mark.parametrize("cfg", DEPTHS, ids=DEPTH_IDS)
+def test_plan_reports_tile_and_workspace(cfg):
+    bk, bn = cfg["bk"], cfg["bn"]
+    p = mt.plan(4096, 4096, 4096, **cfg)
+    assert (p["bm"], p["bn"], p["bk"], p["threads"]) == (128, bn, bk, 192)
+    assert p["stages"] >= 2
+    # Packed big and small copies of A (128-row blocks) and B (bn-row
     # blocks), bk k each.
     assert p["workspace_bytes"] == 4096 * 4096 * 4 * 4
-    assert p["grid"] == 32 * 16
-    assert mt.plan(4096, 4096, 4096, variant="tf32x3")["bk"] == 16  # the default depth
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert p["grid"] == min(32 * (4096 // bn), sms)  # persistent: one CTA per SM at most
+    auto = mt.plan(4096, 4096, 4096, variant="tf32x3")
+    assert (auto["bn"], auto["bk"]) == (256, 16)  # the automatic choice for large squares
 
 
 @pytest.mark.parametrize("cfg", DEPTHS, ids=DEPTH_IDS)

@@ -16,9 +16,10 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxEntries = 32;
-// K depth of the 3xTF32 kernel when the caller does not choose: 16 (4-stage
-// ring, 64-byte swizzle).
-constexpr int kTf32x3DefaultBk = 16;
+// K depth of the 3xTF32 kernel when the caller does not choose: 16 for
+// 256-wide tiles (a 4-stage ring instead of 2), 32 for narrower tiles (3 or
+// 4 stages, half the barrier round trips) — the faster of the two on GB300.
+int tf32x3_default_bk(int bn) { return bn == 256 ? 16 : 32; }
 
 struct DeviceInfo {
   int sms = 0;
@@ -73,6 +74,7 @@ struct Launch {
   int tiles_m = 0, tiles_n = 0, group_m = 8;
   bool pad = true;
   int fault_inject = 0;
+  int max_ctas = 0;  // persistent kernels: CTAs to launch at most
 };
 
 mt_status check_dims(int64_t M, int64_t N, int64_t K) {
@@ -129,6 +131,33 @@ int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms) {
   return small;
 }
 
+// Tile width of the 3xTF32 kernel: the widest tile wins unless padding N
+// up to it, or too few tiles for the SMs, costs more than its higher
+// per-tile efficiency (relative weights measured on GB300).
+int pick_tf32x3_bn(int64_t M, int64_t N, int sms) {
+  // Per-tile throughput relative to 256-wide tiles (8192^3 and 4096^3 on
+  // GB300: narrower tiles re-read A from shared memory for fewer columns).
+  static const int widths[3] = {256, 128, 64};
+  static const double weight[3] = {1.0, 0.7, 0.4};
+  int best = 256;
+  double best_score = -1.0;
+  for (int i = 0; i < 3; ++i) {
+    const int bn = widths[i];
+    const int64_t nt = ceil_div(N, bn);
+    const double used = static_cast<double>(N) / static_cast<double>(nt * bn);
+    const int64_t tiles = ceil_div(M, 128) * nt;
+    const double waves = static_cast<double>(tiles) / sms;
+    const double fill = waves >= 1.0 ? waves / static_cast<double>(ceil_div(tiles, sms))
+                                     : waves;
+    const double score = used * fill * weight[i];
+    if (score > best_score + 1e-9) {
+      best_score = score;
+      best = bn;
+    }
+  }
+  return best;
+}
+
 mt_status plan_call(const float* A, const float* B, const float* C, int64_t M, int64_t N,
                     int64_t K, const mt_config* cfg, int64_t smem_limit, int sms,
                     Launch* L) {
@@ -169,13 +198,13 @@ mt_status plan_call(const float* A, const float* B, const float* C, int64_t M, i
     return MT_OK;
   }
   if (variant == MT_VARIANT_TF32X3) {
-    int bm, bn;
-    mt::tf32x3_tile(&bm, &bn);
-    const int bk = cfg && cfg->bk ? cfg->bk : kTf32x3DefaultBk;
-    if (!mt::tf32x3_valid_bk(bk)) return MT_ERR_UNSUPPORTED;
-    const int stages = mt::tf32x3_stages(bk);
-    if (cfg && ((cfg->bm && cfg->bm != bm) || (cfg->bn && cfg->bn != bn) ||
-                (cfg->stages && cfg->stages != stages) || cfg->fma || cfg->no_pad))
+    const int bm = mt::tf32x3_bm();
+    const int bn = cfg && cfg->bn ? cfg->bn : pick_tf32x3_bn(M, N, sms > 0 ? sms : 1);
+    const int bk = cfg && cfg->bk ? cfg->bk : tf32x3_default_bk(bn);
+    if (!mt::tf32x3_valid(bk, bn)) return MT_ERR_UNSUPPORTED;
+    const int stages = mt::tf32x3_stages(bk, bn);
+    if (cfg && ((cfg->bm && cfg->bm != bm) || (cfg->stages && cfg->stages != stages) ||
+                cfg->fma || cfg->no_pad))
       return MT_ERR_UNSUPPORTED;
     p.bm = bm; p.bn = bn; p.bk = bk; p.stages = stages;
     p.threads = mt::tf32x3_threads();
@@ -183,13 +212,17 @@ mt_status plan_call(const float* A, const float* B, const float* C, int64_t M, i
     // The pack kernel reads A in float4 when K % 4 == 0 and A is 16-byte aligned.
     p.vec_ab = (K % 4 == 0) && aligned16(A);
     p.vec_c = (N % 4 == 0) && aligned16(C);
-    p.smem_bytes = mt::tf32x3_smem_bytes(bk);
+    p.smem_bytes = mt::tf32x3_smem_bytes(bk, bn);
     L->tiles_m = static_cast<int>(ceil_div(M, bm));
     L->tiles_n = static_cast<int>(ceil_div(N, bn));
-    if (L->tiles_m > 65535 || L->tiles_n > 65535) return MT_ERR_UNSUPPORTED;
-    p.grid = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
+    if (L->tiles_m > 65535 || ceil_div(static_cast<int64_t>(L->tiles_n) * bn, 256) > 65535)
+      return MT_ERR_UNSUPPORTED;
+    // Persistent: one CTA per SM at most.
+    const int64_t tiles = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
+    L->max_ctas = sms > 0 ? sms : 1;
+    p.grid = tiles < L->max_ctas ? tiles : L->max_ctas;
     p.workspace_bytes = mt::tf32x3_workspace_bytes(static_cast<int>(M), static_cast<int>(N),
-                                                   static_cast<int>(K), bk);
+                                                   static_cast<int>(K), bk, bn);
     if (p.smem_bytes > smem_limit) return MT_ERR_SMEM_BUDGET;
     return MT_OK;
   }
@@ -299,15 +332,19 @@ mt_status pool_for(int dev, cudaMemPool_t* pool) {
   return MT_OK;
 }
 
-// [device][bk == 32]: shared-memory attribute of the 3xTF32 kernel applied.
-std::atomic<uint8_t> g_tf32x3_ready[kMaxDevices][2];
+// [device][configuration]: shared-memory attribute of the 3xTF32 kernel applied.
+std::atomic<uint8_t> g_tf32x3_ready[kMaxDevices][8];
 
-mt_status prepare_tf32x3(int dev, int bk) {
-  std::atomic<uint8_t>& ready = g_tf32x3_ready[dev][bk == 32 ? 1 : 0];
+int tf32x3_cfg_index(int bk, int bn) {
+  return (bk == 32 ? 4 : 0) + (bn == 256 ? 0 : bn == 128 ? 1 : 2);
+}
+
+mt_status prepare_tf32x3(int dev, int bk, int bn) {
+  std::atomic<uint8_t>& ready = g_tf32x3_ready[dev][tf32x3_cfg_index(bk, bn)];
   if (!ready.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!ready.load(std::memory_order_relaxed)) {
-      if (mt::tf32x3_prepare(dev, bk) != cudaSuccess) {
+      if (mt::tf32x3_prepare(dev, bk, bn) != cudaSuccess) {
         cudaGetLastError();
         return MT_ERR_LAUNCH;
       }
@@ -318,7 +355,7 @@ mt_status prepare_tf32x3(int dev, int bk) {
 }
 
 mt_status run_tf32x3(int dev, const mt::GemmArgs& args, const Launch& L, cudaStream_t stream) {
-  mt_status st0 = prepare_tf32x3(dev, L.plan.bk);
+  mt_status st0 = prepare_tf32x3(dev, L.plan.bk, L.plan.bn);
   if (st0 != MT_OK) return st0;
   cudaMemPool_t pool = nullptr;
   mt_status st = pool_for(dev, &pool);
@@ -330,8 +367,8 @@ mt_status run_tf32x3(int dev, const mt::GemmArgs& args, const Launch& L, cudaStr
     return MT_ERR_CUDA;
   }
   const cudaError_t e =
-      mt::launch_tf32x3(args, ws, L.plan.vec_ab != 0, L.plan.vec_c != 0, L.plan.bk,
-                        L.fault_inject, stream);
+      mt::launch_tf32x3(args, ws, L.plan.vec_ab != 0, L.plan.vec_c != 0, L.plan.bk, L.plan.bn,
+                        L.max_ctas, L.fault_inject, stream);
   cudaFreeAsync(ws, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -418,7 +455,7 @@ mt_status mt_sgemm_tf32x3_noalloc(const float* A, const float* B, float* C, int6
     return MT_OK;
   }
   if (L.plan.workspace_bytes > MT_NOALLOC_SCRATCH_BYTES) return MT_ERR_SCRATCH_LIMIT;
-  st = prepare_tf32x3(dev, L.plan.bk);
+  st = prepare_tf32x3(dev, L.plan.bk, L.plan.bn);
   if (st != MT_OK) return st;
   void* scratch = nullptr;
   if (mt::tf32x3_noalloc_scratch(dev, &scratch) != cudaSuccess || !scratch) {
@@ -427,8 +464,8 @@ mt_status mt_sgemm_tf32x3_noalloc(const float* A, const float* B, float* C, int6
   }
   mt::GemmArgs args{A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                     L.tiles_m, L.tiles_n, L.group_m};
-  if (mt::launch_tf32x3(args, scratch, L.plan.vec_ab != 0, L.plan.vec_c != 0, L.plan.bk, 0,
-                        stream) !=
+  if (mt::launch_tf32x3(args, scratch, L.plan.vec_ab != 0, L.plan.vec_c != 0, L.plan.bk,
+                        L.plan.bn, L.max_ctas, 0, stream) !=
       cudaSuccess) {
     cudaGetLastError();
     return MT_ERR_LAUNCH;

@@ -36,20 +36,21 @@ cudaError_t launch_p18(const GemmArgs& a, bool pad, cudaStream_t stream);
 int p18_pad_a(bool pad);
 int p18_smem_bytes(bool pad);
 
-// tcgen05 3xTF32 variant (sgemm_tf32x3.cu), 128 x 256 tiles with a K depth
-// bk of 16 (4 stages) or 32 (2 stages).  A call needs a device workspace of
-// tf32x3_workspace_bytes(M, N, K, bk) bytes (the packed, swizzled copies of
-// A and B); launch_tf32x3 runs the two pack kernels and the GEMM.
-bool tf32x3_valid_bk(int bk);
-int64_t tf32x3_workspace_bytes(int M, int N, int K, int bk);
-int tf32x3_smem_bytes(int bk);
-int tf32x3_stages(int bk);
+// tcgen05 3xTF32 variant (sgemm_tf32x3.cu): persistent kernel over tiles of
+// 128 x bn (bn = 256, 128 or 64) with a K depth bk of 16 or 32 per stage.
+// A call needs a device workspace of tf32x3_workspace_bytes(M, N, K, bk, bn)
+// bytes (the packed, split, swizzled copies of A and B); launch_tf32x3 runs
+// the two pack kernels and the GEMM on at most max_ctas CTAs (one per SM).
+bool tf32x3_valid(int bk, int bn);
+int64_t tf32x3_workspace_bytes(int M, int N, int K, int bk, int bn);
+int tf32x3_smem_bytes(int bk, int bn);
+int tf32x3_stages(int bk, int bn);
 int tf32x3_threads();
-void tf32x3_tile(int* bm, int* bn);
-cudaError_t tf32x3_prepare(int device, int bk);
+int tf32x3_bm();
+cudaError_t tf32x3_prepare(int device, int bk, int bn);
 // fault_inject = 1: the copy thread issues nothing (tests the bounded waits).
 cudaError_t launch_tf32x3(const GemmArgs& a, void* workspace, bool vec_ab, bool vec_c, int bk,
-                          int fault_inject, cudaStream_t stream);
+                          int bn, int max_ctas, int fault_inject, cudaStream_t stream);
 // Size of the static scratch the allocation-free tf32x3 entry point uses,
 // and its device address on `device` (looked up once per device; the device
 // must be current).

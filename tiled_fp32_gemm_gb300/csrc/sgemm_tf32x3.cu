@@ -16,22 +16,26 @@
 //     A*B ~= A_big*B_small + A_small*B_big + A_big*B_big
 // (A_small*B_small, about 2^-22 relative, is dropped), accumulated in fp32.
 //
-// Pipeline of one CTA (one 128 x 256 tile of C, 192 threads), for a K
-// depth BK of 32 (128-byte swizzle, 2 stages of 96 KB) or 16 (64-byte
-// swizzle, 4 stages of 48 KB):
+// Tiles are 128 x BN (BN = 256, 128 or 64) with a K depth BK of 16 (64-byte
+// swizzle) or 32 (128-byte swizzle) per pipeline stage.
 //   pack kernels (before): A and B are read once, every value is split into
 //     big and small, and both halves are written as zero-padded, K-major
-//     blocks of 128 (A) or 256 (B) rows x BK k, already in the tensor
-//     core's swizzled shared-memory order; so the main loop moves each
-//     operand pair with one cp.async.bulk, does no arithmetic on the
-//     operands and needs no alignment of the caller's leading dimensions;
-//   warp 0, one thread: bulk copies of the A and B block pairs of K tile kt
-//     into stage kt % STAGES, completion counted on full[s];
-//   warp 1, one thread: wait full[s], issue BK/8 k-steps x 3 tcgen05.mma
-//     (128x256x8 each) into the TMEM accumulator, tcgen05.commit -> empty[s]
-//     (frees the stage for the producer), and after the last tile -> done;
-//   warps 2-5 (128 threads, TMEM lane quarters 2, 3, 0, 1): wait done,
-//     tcgen05.ld their 32 TMEM lanes (rows), masked stores to C.
+//     blocks of 128 (A) or BN (B) rows x BK k, already in the tensor core's
+//     swizzled shared-memory order; so the main loop moves each operand
+//     pair with one cp.async.bulk, does no arithmetic on the operands and
+//     needs no alignment of the caller's leading dimensions.
+//   GEMM kernel: persistent, one CTA per SM (192 threads) walking tiles
+//     blockIdx.x, blockIdx.x + gridDim.x, ... of a grouped raster;
+//     warp 0, one thread: bulk copies of the A and B block pairs of every
+//       K tile of every tile into a ring of STAGES stages (full[s]);
+//     warp 1, one thread: per K tile, BK/8 k-steps x 3 tcgen05.mma
+//       (128 x BN x 8) into one of two TMEM accumulators, tcgen05.commit ->
+//       empty[s] (frees the stage), and after a tile's last K tile ->
+//       acc_full[b];
+//     warps 2-5 (128 threads, TMEM lane quarters 2, 3, 0, 1): wait
+//       acc_full[b], tcgen05.ld their 32 lanes (rows), masked stores to C,
+//       arrive acc_empty[b] — while the MMAs of the next tile already run
+//       into the other accumulator.
 // Every wait is bounded (%globaltimer); on expiry the CTA records
 // MT_ERR_TIMEOUT in a device status word, stops issuing, drains what it
 // issued (again bounded), frees TMEM and returns.
@@ -46,34 +50,43 @@
 namespace mt {
 namespace tf32x3 {
 
-constexpr int BM = 128, BN = 256;
+constexpr int BM = 128;
 constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 256;  // fp32 accumulator: 128 lanes x 256 columns
+constexpr int EPILOGUE_THREADS = 128;
 constexpr uint64_t TIMEOUT_NS = 1000000000ull;  // 1 s per wait
+constexpr int SMEM_STAGE_BUDGET = 200 * 1024;   // shared memory for the operand ring
 
 __device__ unsigned int g_status;  // bit 0: a bounded wait expired
 
-// Shared-memory geometry for a K depth of BK fp32 per stage.  Blocks are
-// K-major: each of the 128 (A) or 256 (B) rows holds BK consecutive k
-// (ROW_BYTES), rows are grouped by 8 into swizzle atoms, and inside an atom
-// the 16-byte chunk index of a row is XOR-ed with the row's position —
-// all of it (BK = 32, 128-byte swizzle) or its upper two bits (BK = 16,
-// 64-byte swizzle) — the pattern the tensor core applies to the address
-// bits when it reads the operand.
-template <int BK_>
+// Shared-memory geometry for tiles of 128 x BN with a K depth of BK fp32
+// per stage.  Blocks are K-major: each of the 128 (A) or BN (B) rows holds
+// BK consecutive k (ROW_BYTES), rows are grouped by 8 into swizzle atoms,
+// and inside an atom the 16-byte chunk index of a row is XOR-ed with the
+// row's position — all of it (BK = 32, 128-byte swizzle) or its upper two
+// bits (BK = 16, 64-byte swizzle) — the pattern the tensor core applies to
+// the address bits when it reads the operand.
+template <int BK_, int BN_>
 struct Geometry {
   static_assert(BK_ == 32 || BK_ == 16, "BK is 32 or 16");
+  static_assert(BN_ == 256 || BN_ == 128 || BN_ == 64, "BN is 256, 128 or 64");
   static constexpr int BK = BK_;
+  static constexpr int BN = BN_;
   static constexpr int ROW_BYTES = BK * 4;
   static constexpr int ATOM_BYTES = 8 * ROW_BYTES;
   static constexpr uint32_t CHUNK_MASK = ROW_BYTES / 16 - 1;
   static constexpr uint64_t LAYOUT = BK == 32 ? 2 : 4;  // descriptor: 128-B / 64-B swizzle
-  static constexpr int STAGES = BK == 32 ? 2 : 4;
   static constexpr int A_BLOCK_BYTES = BM * ROW_BYTES;
   static constexpr int B_BLOCK_BYTES = BN * ROW_BYTES;
   // Packed pairs in global memory and stages in shared memory alike:
   // A big | A small and B big | B small.  Stage: A pair | B pair.
-  static constexpr int STAGE_BYTES = 2 * A_BLOCK_BYTES + 2 * B_BLOCK_BYTES;
+  static constexpr int A_PAIR_BYTES = 2 * A_BLOCK_BYTES;
+  static constexpr int B_PAIR_BYTES = 2 * B_BLOCK_BYTES;
+  static constexpr int STAGE_BYTES = A_PAIR_BYTES + B_PAIR_BYTES;
+  static constexpr int STAGES_FIT = SMEM_STAGE_BUDGET / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static_assert(STAGES >= 2, "at least two stages");
+  // Two fp32 accumulators of 128 lanes x BN columns.
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment*/ + 256 /*barriers*/;
 
   // Byte offset of element (r, k), k < BK, inside a block.
@@ -105,15 +118,16 @@ __device__ __forceinline__ void split4(float4 x, float4& big, float4& small) {
   split_tf32(x.w, big.w, small.w);
 }
 
-// grid (Kt, Mt), 256 threads: block (tm, kt) = A[tm*128 + r][kt*BK + k].
-template <int BK>
+
+// grid (Kt, Mt), 256 threads: pair (tm, kt) holds A[tm*128 + r][kt*BK + k].
+template <class G>
 __global__ void __launch_bounds__(256) pack_a_kernel(const float* __restrict__ A,
                                                      float* __restrict__ Ap, int M, int K,
                                                      int Kt, int vec) {
-  using G = Geometry<BK>;
+  constexpr int BK = G::BK;
   const int kt = blockIdx.x, tm = blockIdx.y;
   char* dst = reinterpret_cast<char*>(Ap) +
-              (static_cast<int64_t>(tm) * Kt + kt) * static_cast<int64_t>(2 * G::A_BLOCK_BYTES);
+              (static_cast<int64_t>(tm) * Kt + kt) * static_cast<int64_t>(G::A_PAIR_BYTES);
   for (int c = threadIdx.x; c < BM * (BK / 4); c += 256) {
     const int r = c / (BK / 4), ch = c % (BK / 4);
     const int m = tm * BM + r, k = kt * BK + ch * 4;
@@ -137,18 +151,21 @@ __global__ void __launch_bounds__(256) pack_a_kernel(const float* __restrict__ A
   }
 }
 
-// grid (Kt, Nt), 256 threads: block (tn, kt) row n = B[kt*BK + k][tn*256 + n].
-// Thread t owns row n = t: it reads one column of the B tile (coalesced
-// across the warp) and writes its row of BK values.
-template <int BK>
+// grid (Kt, ceil(Nt*BN/256)), 256 threads: thread t owns column
+// n = blockIdx.y*256 + t of B, i.e. row n % BN of pair (n / BN, kt).  It
+// reads its column of the K tile (coalesced across the warp) and writes its
+// row of BK values.
+template <class G>
 __global__ void __launch_bounds__(256) pack_b_kernel(const float* __restrict__ B,
                                                      float* __restrict__ Bp, int K, int N,
-                                                     int Kt) {
-  using G = Geometry<BK>;
-  const int kt = blockIdx.x, tn = blockIdx.y, t = threadIdx.x;
-  const int n = tn * BN + t;
+                                                     int Kt, int Nt) {
+  constexpr int BK = G::BK;
+  const int kt = blockIdx.x;
+  const int n = blockIdx.y * 256 + threadIdx.x;
+  const int tn = n / G::BN, r = n % G::BN;
+  if (tn >= Nt) return;
   char* dst = reinterpret_cast<char*>(Bp) +
-              (static_cast<int64_t>(tn) * Kt + kt) * static_cast<int64_t>(2 * G::B_BLOCK_BYTES);
+              (static_cast<int64_t>(tn) * Kt + kt) * static_cast<int64_t>(G::B_PAIR_BYTES);
   float v[BK];
 #pragma unroll
   for (int j = 0; j < BK; ++j) {
@@ -159,7 +176,7 @@ __global__ void __launch_bounds__(256) pack_b_kernel(const float* __restrict__ B
   for (int ch = 0; ch < BK / 4; ++ch) {
     float4 big, small;
     split4(make_float4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]), big, small);
-    const uint32_t off = G::offset(t, ch * 4);
+    const uint32_t off = G::offset(r, ch * 4);
     *reinterpret_cast<float4*>(dst + off) = big;
     *reinterpret_cast<float4*>(dst + G::B_BLOCK_BYTES + off) = small;
   }
@@ -315,119 +332,141 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
 }
 
 // ---------------------------------------------------------------------------
-template <int BK>
+template <class G>
 __global__ void __launch_bounds__(THREADS, 1)
     tf32x3_gemm_kernel(const float* __restrict__ Ap, const float* __restrict__ Bp,
                        float* __restrict__ C, int M, int N, int Kt, int tiles_m, int tiles_n,
                        int group_m, int vec_c, int fault_inject) {
-  using G = Geometry<BK>;
+  constexpr int BK = G::BK, BN = G::BN;
   constexpr int STAGES = G::STAGES;
   constexpr int STAGE_BYTES = G::STAGE_BYTES;
-  constexpr int A_BLOCK_BYTES = G::A_BLOCK_BYTES;
-  constexpr int B_BLOCK_BYTES = G::B_BLOCK_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  // bars[0..S): full, [S..2S): empty, [2S]: done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  // bars: [0, S) full, [S, 2S) empty, 2S + b acc_full[b], 2S + 2 + b
+  // acc_empty[b], 2S + 4 drain.
+  constexpr int FULL = 0, EMPTY = STAGES, ACC_FULL = 2 * STAGES, ACC_EMPTY = 2 * STAGES + 2,
+                DRAIN = 2 * STAGES + 4, NBARS = 2 * STAGES + 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  int tm, tn;
-  grouped_tile(blockIdx.x, tiles_m, tiles_n, group_m, tm, tn);
+  const int num_tiles = tiles_m * tiles_n;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar(s), 1);           // full: producer + tx bytes
-      mbar_init(bar(STAGES + s), 1);  // empty: MMA commit
+      mbar_init(bar(FULL + s), 1);   // producer arrival + tx bytes
+      mbar_init(bar(EMPTY + s), 1);  // MMA commit
     }
-    mbar_init(bar(2 * STAGES), 1);  // done: final MMA commit
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(ACC_FULL + b), 1);                  // MMA commit
+      mbar_init(bar(ACC_EMPTY + b), EPILOGUE_THREADS);  // every epilogue thread
+    }
+    mbar_init(bar(DRAIN), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), G::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const char* a_src = reinterpret_cast<const char*>(Ap) +
-                      static_cast<int64_t>(tm) * Kt * static_cast<int64_t>(2 * A_BLOCK_BYTES);
-  const char* b_src = reinterpret_cast<const char*>(Bp) +
-                      static_cast<int64_t>(tn) * Kt * static_cast<int64_t>(2 * B_BLOCK_BYTES);
-
+  uint32_t issued = 0;  // producer: K tiles issued by this CTA, across its tiles
   if (warp == 0) {
     if (lane == 0) {
       // Producer.  With fault_inject set it issues nothing, so every wait
       // on its data runs out (the test of the timeout path).
-      int issued = 0;
-      for (int kt = 0; kt < (fault_inject ? 0 : Kt); ++kt) {
-        const int s = kt % STAGES;
-        const uint32_t round = static_cast<uint32_t>(kt / STAGES);
-        if (kt >= STAGES && !wait_phase(bar(STAGES + s), (round + 1) & 1u, abort_flag)) break;
-        uint8_t* st = smem + s * STAGE_BYTES;
-        mbar_arrive_expect_tx(bar(s), STAGE_BYTES);
-        bulk_copy_g2s(smem_u32(st), a_src + static_cast<int64_t>(kt) * (2 * A_BLOCK_BYTES),
-                      2 * A_BLOCK_BYTES, bar(s));
-        bulk_copy_g2s(smem_u32(st + 2 * A_BLOCK_BYTES),
-                      b_src + static_cast<int64_t>(kt) * (2 * B_BLOCK_BYTES), 2 * B_BLOCK_BYTES,
-                      bar(s));
-        issued = kt + 1;
-      }
-      if (*abort_flag) {
-        // Let the copies this thread issued land before the CTA exits.
-        for (int kt = issued - STAGES < 0 ? 0 : issued - STAGES; kt < issued; ++kt)
-          wait_phase(bar(kt % STAGES), static_cast<uint32_t>(kt / STAGES) & 1u, abort_flag,
-                     false);
+      uint32_t& g = issued;
+      bool stop = fault_inject != 0;
+      for (int tile = blockIdx.x; tile < num_tiles && !stop; tile += gridDim.x) {
+        int tm, tn;
+        grouped_tile(tile, tiles_m, tiles_n, group_m, tm, tn);
+        const char* a_src = reinterpret_cast<const char*>(Ap) +
+                            static_cast<int64_t>(tm) * Kt * G::A_PAIR_BYTES;
+        const char* b_src = reinterpret_cast<const char*>(Bp) +
+                            static_cast<int64_t>(tn) * Kt * G::B_PAIR_BYTES;
+        for (int kt = 0; kt < Kt; ++kt, ++g) {
+          const uint32_t s = g % STAGES, round = g / STAGES;
+          if (g >= STAGES && !wait_phase(bar(EMPTY + s), (round + 1) & 1u, abort_flag)) {
+            stop = true;
+            break;
+          }
+          uint8_t* st = smem + s * STAGE_BYTES;
+          mbar_arrive_expect_tx(bar(FULL + s), STAGE_BYTES);
+          bulk_copy_g2s(smem_u32(st), a_src + static_cast<int64_t>(kt) * G::A_PAIR_BYTES,
+                        G::A_PAIR_BYTES, bar(FULL + s));
+          bulk_copy_g2s(smem_u32(st + G::A_PAIR_BYTES),
+                        b_src + static_cast<int64_t>(kt) * G::B_PAIR_BYTES, G::B_PAIR_BYTES,
+                        bar(FULL + s));
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // MMA issuer.
       constexpr uint32_t idesc = instr_desc_tf32(BM, BN);
-      uint32_t acc = 0;
-      for (int kt = 0; kt < Kt; ++kt) {
-        const int s = kt % STAGES;
-        const uint32_t round = static_cast<uint32_t>(kt / STAGES);
-        if (!wait_phase(bar(s), round & 1u, abort_flag)) break;
+      uint32_t g = 0;
+      bool stop = false;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && !stop; tile += gridDim.x, ++it) {
+        const int b = it & 1;
+        // The epilogue must have drained this accumulator (used by tile it-2).
+        if (it >= 2 && !wait_phase(bar(ACC_EMPTY + b), ((it >> 1) + 1) & 1u, abort_flag)) break;
         tc_fence_after();
-        const uint32_t a_big = smem_u32(smem + s * STAGE_BYTES);
-        const uint32_t a_small = a_big + A_BLOCK_BYTES;
-        const uint32_t b_big = a_big + 2 * A_BLOCK_BYTES;
-        const uint32_t b_small = b_big + B_BLOCK_BYTES;
+        const uint32_t acc_tmem = tmem + static_cast<uint32_t>(b * BN);
+        uint32_t acc = 0;
+        for (int kt = 0; kt < Kt; ++kt, ++g) {
+          const uint32_t s = g % STAGES, round = g / STAGES;
+          if (!wait_phase(bar(FULL + s), round & 1u, abort_flag)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_big = smem_u32(smem + s * STAGE_BYTES);
+          const uint32_t a_small = a_big + G::A_BLOCK_BYTES;
+          const uint32_t b_big = a_big + G::A_PAIR_BYTES;
+          const uint32_t b_small = b_big + G::B_BLOCK_BYTES;
 #pragma unroll
-        for (int j = 0; j < BK / 8; ++j) {
-          const uint32_t koff = j * 32;  // 8 tf32 = 32 bytes along K
-          const uint64_t ab = smem_desc(a_big + koff, G::ATOM_BYTES, G::LAYOUT);
-          const uint64_t as = smem_desc(a_small + koff, G::ATOM_BYTES, G::LAYOUT);
-          const uint64_t bb = smem_desc(b_big + koff, G::ATOM_BYTES, G::LAYOUT);
-          const uint64_t bs = smem_desc(b_small + koff, G::ATOM_BYTES, G::LAYOUT);
-          mma_tf32(tmem, ab, bs, idesc, acc);
-          acc = 1;
-          mma_tf32(tmem, as, bb, idesc, 1);
-          mma_tf32(tmem, ab, bb, idesc, 1);
+          for (int j = 0; j < BK / 8; ++j) {
+            const uint32_t koff = j * 32;  // 8 tf32 = 32 bytes along K
+            const uint64_t ab = smem_desc(a_big + koff, G::ATOM_BYTES, G::LAYOUT);
+            const uint64_t as = smem_desc(a_small + koff, G::ATOM_BYTES, G::LAYOUT);
+            const uint64_t bb = smem_desc(b_big + koff, G::ATOM_BYTES, G::LAYOUT);
+            const uint64_t bs = smem_desc(b_small + koff, G::ATOM_BYTES, G::LAYOUT);
+            mma_tf32(acc_tmem, ab, bs, idesc, acc);
+            acc = 1;
+            mma_tf32(acc_tmem, as, bb, idesc, 1);
+            mma_tf32(acc_tmem, ab, bb, idesc, 1);
+          }
+          mma_commit(bar(EMPTY + s));
         }
-        mma_commit(bar(STAGES + s));
+        if (!stop) mma_commit(bar(ACC_FULL + b));
       }
-      // After the last MMA (or on abort, after whatever was issued).
-      mma_commit(bar(2 * STAGES));
+      // Every MMA this thread issued has retired once DRAIN completes.
+      mma_commit(bar(DRAIN));
+      wait_phase(bar(DRAIN), 0, abort_flag, false);
     }
   } else {
-    // Epilogue warps (2..5 cover TMEM lane quarters 2, 3, 0, 1).  Wait for
-    // the accumulator even after an abort, so no MMA is in flight when TMEM
-    // is released.
-    // The accumulator is ready only after the whole K loop: allow 20 us per
-    // K tile on top of the usual limit.
-    const bool done = wait_phase(bar(2 * STAGES), 0, abort_flag, false,
-                                 TIMEOUT_NS + 20000ull * static_cast<uint64_t>(Kt));
-    tc_fence_after();
-    __syncwarp();
-    if (done && !*abort_flag) {
-      const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // Epilogue warps: warp w may access TMEM lanes 32*(w%4) .. +31.
+    const int q = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+      const int b = it & 1;
+      // A tile's accumulator is ready after its whole K loop.  The warp
+      // goes on only if every lane saw it (tcgen05.ld needs the whole warp).
+      const bool ready = wait_phase(bar(ACC_FULL + b), (it >> 1) & 1u, abort_flag, true,
+                                    TIMEOUT_NS + 20000ull * static_cast<uint64_t>(Kt));
+      if (!__all_sync(0xffffffffu, ready)) break;
+      tc_fence_after();
+      __syncwarp();
+      int tm, tn;
+      grouped_tile(tile, tiles_m, tiles_n, group_m, tm, tn);
       const int row = tm * BM + q * 32 + lane;
-      const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
+      const uint32_t t_row = tmem + lane_base + static_cast<uint32_t>(b * BN);
       float* c_row = C + static_cast<int64_t>(row) * N;
 #pragma unroll 1
       for (int ch = 0; ch < BN / 32; ++ch) {
@@ -437,10 +476,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (row < M) {
           if (vec_c) {
 #pragma unroll
-            for (int g = 0; g < 8; ++g)
-              if (col0 + 4 * g < N)
-                *reinterpret_cast<float4*>(c_row + col0 + 4 * g) =
-                    make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+            for (int g4 = 0; g4 < 8; ++g4)
+              if (col0 + 4 * g4 < N)
+                *reinterpret_cast<float4*>(c_row + col0 + 4 * g4) =
+                    make_float4(v[4 * g4], v[4 * g4 + 1], v[4 * g4 + 2], v[4 * g4 + 3]);
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -448,80 +487,118 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(bar(ACC_EMPTY + b));
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    // Let the copies the producer issued land before the CTA exits.
+    for (uint32_t q = issued > STAGES ? issued - STAGES : 0; q < issued; ++q)
+      wait_phase(bar(FULL + q % STAGES), (q / STAGES) & 1u, abort_flag, false);
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc(tmem, G::TMEM_COLS);
   }
 }
 
 }  // namespace tf32x3
 
 // ---------------------------------------------------------------------------
-template <int BK>
-int64_t workspace_bytes_for(int M, int N, int K) {
-  using G = tf32x3::Geometry<BK>;
-  const int64_t mt = (M + tf32x3::BM - 1) / tf32x3::BM;
-  const int64_t nt = (N + tf32x3::BN - 1) / tf32x3::BN;
-  const int64_t kt = (K + BK - 1) / BK;
-  return 2 * (mt * kt * G::A_BLOCK_BYTES + nt * kt * G::B_BLOCK_BYTES);
+// Host side.  Configurations: (BK, BN) in {16, 32} x {256, 128, 64}.
+
+namespace {
+
+template <int BK, int BN>
+struct Cfg {
+  using G = tf32x3::Geometry<BK, BN>;
+  static int64_t workspace(int M, int N, int K) {
+    const int64_t mt = (M + tf32x3::BM - 1) / tf32x3::BM;
+    const int64_t nt = (N + BN - 1) / BN;
+    const int64_t kt = (K + BK - 1) / BK;
+    return mt * kt * G::A_PAIR_BYTES + nt * kt * G::B_PAIR_BYTES;
+  }
+  static cudaError_t prepare() {
+    return cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<G>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
+  }
+  static cudaError_t launch(const GemmArgs& a, void* workspace, bool vec_ab, bool vec_c,
+                            int max_ctas, int fault_inject, cudaStream_t stream) {
+    using namespace tf32x3;
+    const int mt = (a.M + BM - 1) / BM, nt = (a.N + BN - 1) / BN, kt = (a.K + BK - 1) / BK;
+    if (mt > 65535 || (nt * BN + 255) / 256 > 65535) return cudaErrorInvalidValue;
+    float* Ap = static_cast<float*>(workspace);
+    float* Bp = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         static_cast<int64_t>(mt) * kt * G::A_PAIR_BYTES);
+    pack_a_kernel<G><<<dim3(kt, mt), 256, 0, stream>>>(a.A, Ap, a.M, a.K, kt, vec_ab ? 1 : 0);
+    pack_b_kernel<G><<<dim3(kt, (nt * BN + 255) / 256), 256, 0, stream>>>(a.B, Bp, a.K, a.N, kt,
+                                                                          nt);
+    const int tiles = mt * nt;
+    const int grid = tiles < max_ctas ? tiles : max_ctas;
+    tf32x3_gemm_kernel<G><<<grid, THREADS, G::SMEM_BYTES, stream>>>(
+        Ap, Bp, a.C, a.M, a.N, kt, mt, nt, a.group_m, vec_c ? 1 : 0, fault_inject);
+    return cudaGetLastError();
+  }
+};
+
+// Calls f.template operator()<BK, BN>() for the runtime choice; false when
+// the pair is not built.
+template <class F>
+bool dispatch(int bk, int bn, F&& f) {
+  if (bk == 16 && bn == 256) { f(Cfg<16, 256>{}); return true; }
+  if (bk == 16 && bn == 128) { f(Cfg<16, 128>{}); return true; }
+  if (bk == 16 && bn == 64) { f(Cfg<16, 64>{}); return true; }
+  if (bk == 32 && bn == 256) { f(Cfg<32, 256>{}); return true; }
+  if (bk == 32 && bn == 128) { f(Cfg<32, 128>{}); return true; }
+  if (bk == 32 && bn == 64) { f(Cfg<32, 64>{}); return true; }
+  return false;
 }
 
-bool tf32x3_valid_bk(int bk) { return bk == 16 || bk == 32; }
+}  // namespace
 
-int64_t tf32x3_workspace_bytes(int M, int N, int K, int bk) {
-  return bk == 32 ? workspace_bytes_for<32>(M, N, K) : workspace_bytes_for<16>(M, N, K);
+bool tf32x3_valid(int bk, int bn) {
+  return dispatch(bk, bn, [](auto) {});
 }
 
-int tf32x3_smem_bytes(int bk) {
-  return bk == 32 ? tf32x3::Geometry<32>::SMEM_BYTES : tf32x3::Geometry<16>::SMEM_BYTES;
+int64_t tf32x3_workspace_bytes(int M, int N, int K, int bk, int bn) {
+  int64_t r = -1;
+  dispatch(bk, bn, [&](auto c) { r = decltype(c)::workspace(M, N, K); });
+  return r;
 }
-int tf32x3_stages(int bk) {
-  return bk == 32 ? tf32x3::Geometry<32>::STAGES : tf32x3::Geometry<16>::STAGES;
+
+int tf32x3_smem_bytes(int bk, int bn) {
+  int r = -1;
+  dispatch(bk, bn, [&](auto c) { r = decltype(c)::G::SMEM_BYTES; });
+  return r;
 }
+
+int tf32x3_stages(int bk, int bn) {
+  int r = -1;
+  dispatch(bk, bn, [&](auto c) { r = decltype(c)::G::STAGES; });
+  return r;
+}
+
 int tf32x3_threads() { return tf32x3::THREADS; }
-void tf32x3_tile(int* bm, int* bn) {
-  *bm = tf32x3::BM;
-  *bn = tf32x3::BN;
-}
+int tf32x3_bm() { return tf32x3::BM; }
 
-cudaError_t tf32x3_prepare(int device, int bk) {
+cudaError_t tf32x3_prepare(int device, int bk, int bn) {
   (void)device;
-  if (bk == 32)
-    return cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<32>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                tf32x3::Geometry<32>::SMEM_BYTES);
-  return cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<16>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              tf32x3::Geometry<16>::SMEM_BYTES);
-}
-
-template <int BK>
-cudaError_t launch_tf32x3_bk(const GemmArgs& a, void* workspace, bool vec_ab, bool vec_c,
-                             int fault_inject, cudaStream_t stream) {
-  using namespace tf32x3;
-  using G = Geometry<BK>;
-  const int mt = (a.M + BM - 1) / BM, nt = (a.N + BN - 1) / BN, kt = (a.K + BK - 1) / BK;
-  if (mt > 65535 || nt > 65535) return cudaErrorInvalidValue;
-  float* Ap = static_cast<float*>(workspace);
-  float* Bp = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                       static_cast<int64_t>(mt) * kt * 2 * G::A_BLOCK_BYTES);
-  pack_a_kernel<BK><<<dim3(kt, mt), 256, 0, stream>>>(a.A, Ap, a.M, a.K, kt, vec_ab ? 1 : 0);
-  pack_b_kernel<BK><<<dim3(kt, nt), 256, 0, stream>>>(a.B, Bp, a.K, a.N, kt);
-  tf32x3_gemm_kernel<BK><<<static_cast<unsigned>(mt * nt), THREADS, G::SMEM_BYTES, stream>>>(
-      Ap, Bp, a.C, a.M, a.N, kt, mt, nt, a.group_m, vec_c ? 1 : 0, fault_inject);
-  return cudaGetLastError();
+  cudaError_t e = cudaErrorInvalidValue;
+  dispatch(bk, bn, [&](auto c) { e = decltype(c)::prepare(); });
+  return e;
 }
 
 cudaError_t launch_tf32x3(const GemmArgs& a, void* workspace, bool vec_ab, bool vec_c, int bk,
-                          int fault_inject, cudaStream_t stream) {
-  if (bk == 32) return launch_tf32x3_bk<32>(a, workspace, vec_ab, vec_c, fault_inject, stream);
-  return launch_tf32x3_bk<16>(a, workspace, vec_ab, vec_c, fault_inject, stream);
+                          int bn, int max_ctas, int fault_inject, cudaStream_t stream) {
+  cudaError_t e = cudaErrorInvalidValue;
+  dispatch(bk, bn, [&](auto c) {
+    e = decltype(c)::launch(a, workspace, vec_ab, vec_c, max_ctas, fault_inject, stream);
+  });
+  return e;
 }
 
 // ---------------------------------------------------------------------------
