@@ -80,7 +80,9 @@ typedef struct {
                          copy thread issues nothing, so every wait on its data
                          runs out; the call then leaves C unwritten and the
                          next mt_device_status returns MT_ERR_TIMEOUT. */
-    int reserved[3];
+    int wm;        /* FFMA warp tile rows; 0 = automatic */
+    int wn;        /* FFMA warp tile columns; 0 = automatic */
+    int reserved[1];
 } mt_config;
 
 /* What a call with the same arguments would launch. */
@@ -93,6 +95,8 @@ typedef struct {
     int vec_c;                /* 1: 16-byte stores of C; 0: 4-byte stores */
     int split_k;              /* K slices (1 = none) */
     int fma;                  /* 1 scalar, 2 packed (FFMA variant; 0 otherwise) */
+    int wm, wn;               /* warp tile (FFMA variant; 0 otherwise) */
+    int tm, tn;               /* outputs per thread (FFMA variant; 0 otherwise) */
     int64_t grid;             /* CTAs of the main kernel */
     int64_t smem_bytes;       /* dynamic shared memory per CTA */
     int64_t workspace_bytes;  /* device scratch the call needs (0 = none) */

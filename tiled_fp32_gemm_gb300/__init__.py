@@ -45,7 +45,8 @@ class mt_config(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("bm", ctypes.c_int), ("bn", ctypes.c_int),
                 ("bk", ctypes.c_int), ("stages", ctypes.c_int), ("no_pad", ctypes.c_int),
                 ("split_k", ctypes.c_int), ("fma", ctypes.c_int),
-                ("fault_inject", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
+                ("fault_inject", ctypes.c_int), ("wm", ctypes.c_int), ("wn", ctypes.c_int),
+                ("reserved", ctypes.c_int * 1)]
 
 
 class mt_plan(ctypes.Structure):
@@ -53,6 +54,8 @@ class mt_plan(ctypes.Structure):
                 ("bk", ctypes.c_int), ("stages", ctypes.c_int), ("pad_a", ctypes.c_int),
                 ("pad_b", ctypes.c_int), ("threads", ctypes.c_int), ("vec_ab", ctypes.c_int),
                 ("vec_c", ctypes.c_int), ("split_k", ctypes.c_int), ("fma", ctypes.c_int),
+                ("wm", ctypes.c_int), ("wn", ctypes.c_int), ("tm", ctypes.c_int),
+                ("tn", ctypes.c_int),
                 ("grid", ctypes.c_int64), ("smem_bytes", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_int64)]
 
@@ -115,7 +118,7 @@ def lib():
 
 
 def make_config(variant="ffma", bm=0, bn=0, bk=0, stages=0, no_pad=False, split_k=0,
-                fma=0, fault_inject=0) -> mt_config:
+                fma=0, fault_inject=0, wm=0, wn=0) -> mt_config:
     c = mt_config()
     c.variant = VARIANTS[variant] if isinstance(variant, str) else int(variant)
     c.bm, c.bn, c.bk, c.stages = bm, bn, bk, stages
@@ -123,6 +126,7 @@ def make_config(variant="ffma", bm=0, bn=0, bk=0, stages=0, no_pad=False, split_
     c.split_k = split_k
     c.fma = fma
     c.fault_inject = fault_inject
+    c.wm, c.wn = wm, wn
     return c
 
 

@@ -99,12 +99,15 @@ mt_status check_args(const float* A, const float* B, const float* C, int64_t M, 
   return MT_OK;
 }
 
-// Chooses the FFMA table entry.  Explicit bm/bn/bk/stages/fma must all
-// match an entry; otherwise the choice is automatic.
+// Chooses the FFMA table entry.  Explicit choices (tile, stages, warp tile,
+// micro-kernel form) must all match one entry; the first match in table
+// order wins, so each tile's default warp layout comes first.  Otherwise
+// the choice is automatic.
 int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms) {
   int count = 0;
   const mt::FfmaEntry* e = mt::ffma_entries(&count);
-  const bool explicit_tile = cfg && (cfg->bm || cfg->bn || cfg->bk || cfg->stages);
+  const bool explicit_tile =
+      cfg && (cfg->bm || cfg->bn || cfg->bk || cfg->stages || cfg->wm || cfg->wn);
   const int want_packed = cfg && cfg->fma ? (cfg->fma == 2 ? 1 : 0) : 1;
   if (explicit_tile || (cfg && cfg->fma)) {
     for (int i = 0; i < count; ++i) {
@@ -112,6 +115,8 @@ int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms) {
       if (cfg->bn && e[i].bn != cfg->bn) continue;
       if (cfg->bk && e[i].bk != cfg->bk) continue;
       if (cfg->stages && e[i].stages != cfg->stages) continue;
+      if (cfg->wm && e[i].wm != cfg->wm) continue;
+      if (cfg->wn && e[i].wn != cfg->wn) continue;
       if (e[i].packed != want_packed) continue;
       if (!explicit_tile && !(e[i].bm == 128 && e[i].bn == 128 && e[i].stages == 3)) continue;
       return i;
@@ -123,8 +128,9 @@ int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms) {
   int big = -1, small = -1;
   for (int i = 0; i < count; ++i) {
     if (!e[i].packed) continue;
-    if (e[i].bm == 128 && e[i].bn == 128 && e[i].stages == 3) big = i;
-    if (e[i].bm == 64 && e[i].bn == 64) small = i;
+    if (big < 0 && e[i].bm == 128 && e[i].bn == 128 && e[i].bk == 32 && e[i].stages == 3)
+      big = i;
+    if (small < 0 && e[i].bm == 64 && e[i].bn == 64) small = i;
   }
   const int64_t tiles_big = ceil_div(M, 128) * ceil_div(N, 128);
   if (tiles_big >= 2 * static_cast<int64_t>(sms) || small < 0) return big;
@@ -168,8 +174,10 @@ mt_status plan_call(const float* A, const float* B, const float* C, int64_t M, i
   const int variant = cfg ? cfg->variant : MT_VARIANT_FFMA;
   if (cfg && (cfg->bm < 0 || cfg->bn < 0 || cfg->bk < 0 || cfg->stages < 0 ||
               cfg->no_pad < 0 || cfg->no_pad > 1 || cfg->split_k < 0 || cfg->fma < 0 ||
-              cfg->fma > 2 || cfg->fault_inject < 0 || cfg->fault_inject > 1))
+              cfg->fma > 2 || cfg->fault_inject < 0 || cfg->fault_inject > 1 || cfg->wm < 0 ||
+              cfg->wn < 0))
     return MT_ERR_INVALID_ARG;
+  if (cfg && (cfg->wm || cfg->wn) && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
   if (cfg && cfg->fault_inject && variant != MT_VARIANT_TF32X3) return MT_ERR_UNSUPPORTED;
   if (cfg && cfg->split_k > 1) return MT_ERR_UNSUPPORTED;
   const bool pad = !(cfg && cfg->no_pad);
@@ -236,6 +244,7 @@ mt_status plan_call(const float* A, const float* B, const float* C, int64_t M, i
   if (!E.kern[p.vec_ab][pad ? 1 : 0]) return MT_ERR_UNSUPPORTED;
   p.bm = E.bm; p.bn = E.bn; p.bk = E.bk; p.stages = E.stages; p.threads = E.threads;
   p.fma = E.packed ? 2 : 1;
+  p.wm = E.wm; p.wn = E.wn; p.tm = E.tm; p.tn = E.tn;
   p.pad_a = pad ? E.pad_a : 0;
   p.pad_b = pad ? E.pad_b : 0;
   p.smem_bytes = E.smem_bytes[pad ? 1 : 0];
