@@ -131,6 +131,24 @@ def dist_setup():
     return world, rank, local
 
 
+def reduce_max(x: float, device: str = "cuda") -> float:
+    """Max of x over the ranks of the default process group (x itself when
+    there is none).  `device` holds the reduction tensor: "cuda" under NCCL,
+    "cpu" under gloo."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_step: float, steps: int, seconds: float) -> float:
+    """Whole-job throughput: the work of every rank over the slowest rank's time."""
+    return world * flops_per_step * steps / seconds / 1e12
+
+
 def oracle_sample(steps: int, budget_s: float):
     """Times the CPU oracle on row samples of the step's GEMMs.
 
@@ -255,12 +273,7 @@ def run_gpu(args):
             dist.barrier()
 
     def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, "cuda")
 
     shapes = [gemm_inputs.WORKLOADS[n] for n in (args.workloads or STEP_WORKLOADS)]
     main_cfg = json.loads(args.config) if args.config else {}
@@ -318,7 +331,7 @@ def run_gpu(args):
     clocks = ClockSampler(dev).__enter__()
     total_ms, per_launch = measure(main_cfg, args.steps, args.warmup, clocks)
     clocks.__exit__(None, None, None)
-    value = world * flops_step * args.steps / (total_ms / 1e3) / 1e12
+    value = job_tflops(world, flops_step, args.steps, total_ms / 1e3)
     plans = plans_for(main_cfg)
 
     clk = clocks.summary()
@@ -374,7 +387,7 @@ def run_gpu(args):
         other = {"variant": "tf32x3"} if variant == "ffma" else {"variant": "ffma"}
         o_steps = max(1, min(args.steps, 10))
         o_total, o_per = measure(other, o_steps, max(1, min(args.warmup, 3)))
-        o_val = world * flops_step * o_steps / (o_total / 1e3) / 1e12
+        o_val = job_tflops(world, flops_step, o_steps, o_total / 1e3)
         variants[other["variant"]] = {
             "value": o_val, "unit": "TFLOP/s", "steps": o_steps,
             "per_shape": shape_summary(o_per, plans_for(other)),
@@ -409,7 +422,7 @@ def run_gpu(args):
         for _ in range(e2e_steps):
             host_step()
         e2e_s = max_over_ranks(time.perf_counter() - t0)
-        e2e = {"value": world * flops_step * e2e_steps / e2e_s / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_tflops(world, flops_step, e2e_steps, e2e_s), "unit": "TFLOP/s",
                "steps": e2e_steps,
                "h2d_bytes_per_step": sum(4 * (w.M * w.K + w.K * w.N) for (w, *_r) in hbufs),
                "d2h_bytes_per_step": sum(4 * w.M * w.N for (w, *_r) in hbufs),

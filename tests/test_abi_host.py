@@ -99,14 +99,14 @@ def plan(M, N, K, limit=GB300_SMEM, **kw):
     return st, p
 
 
-# Lane layout of each FFMA tile configuration (warp tile WM x WN, thread tile
-# TM x TN; lanes numbered M-fastest), restated from the kernel's description.
-FFMA_LANES = {(128, 128): (32, 64, 8, 8), (128, 256): (64, 64, 8, 16), (64, 64): (32, 32, 8, 4)}
-
-
 def ffma_warp_accesses(p):
-    """Byte addresses of warp 0's shared reads and cp.async writes, per instruction."""
-    WM, WN, TM, TN = FFMA_LANES[(p.bm, p.bn)]
+    """Byte addresses of warp 0's shared reads and cp.async writes, per instruction.
+
+    Lane layout restated from the kernel's description: a warp tile of
+    WM x WN, TM x TN outputs per thread, lanes numbered M-fastest; thread
+    (lm, ln) reads A rows i*LM + lm and B columns g*LN*4 + ln*4.
+    """
+    WM, WN, TM, TN = p.wm, p.wn, p.tm, p.tn
     LM = WM // TM
     LN = 32 // LM
     la = R.SharedBuffer(p.bm, p.bk, p.pad_a, p.stages)
@@ -132,7 +132,9 @@ def ffma_warp_accesses(p):
 
 
 @pytest.mark.parametrize("shape", [(4096, 4096, 4096), (1024, 1024, 1024), (128, 256, 64)])
-@pytest.mark.parametrize("tile", [dict(), dict(bm=128, bn=256), dict(bm=64, bn=64)])
+@pytest.mark.parametrize("tile", [dict(), dict(bm=128, bn=256), dict(bm=64, bn=64),
+                                  dict(bm=256, bn=128), dict(bm=128, bn=128, wm=32, wn=64),
+                                  dict(bm=128, bn=128, wm=64, wn=32)])
 def test_ffma_layout_is_conflict_free(shape, tile):
     st, p = plan(*shape, **tile)
     assert st == mt.MT_OK
@@ -142,13 +144,15 @@ def test_ffma_layout_is_conflict_free(shape, tile):
     assert p.pad_b == 0  # B is read as a broadcast: the rule gives no padding
 
 
-def test_ffma_unpadded_layout_conflicts():
-    st, p = plan(4096, 4096, 4096, bm=128, bn=128, bk=32, stages=3, no_pad=True, fma=2)
+@pytest.mark.parametrize("warp", [dict(wm=64, wn=64), dict(wm=32, wn=64)])
+def test_ffma_unpadded_layout_conflicts(warp):
+    st, p = plan(4096, 4096, 4096, bm=128, bn=128, bk=32, stages=3, no_pad=True, fma=2, **warp)
     assert st == mt.MT_OK and p.pad_a == 0
     reads, _ = ffma_warp_accesses(p)
     assert max(R.conflict_degree(a, 16) for a in reads) > 1
-    st, q = plan(4096, 4096, 4096, bm=128, bn=128, bk=32, stages=3, fma=2)
-    assert q.pad_a == R.vector_row_padding(32, 4) == 4
+    st, q = plan(4096, 4096, 4096, bm=128, bn=128, bk=32, stages=3, fma=2, **warp)
+    rows_per_phase = min(q.wm // q.tm, 8)
+    assert q.pad_a == R.vector_row_padding(32, rows_per_phase) == 4
 
 
 def test_p18_plan_follows_the_pages():
@@ -211,3 +215,20 @@ def test_no_cpu_fallback_without_gpu():
     st = mt.mt_sgemm_host(a.ctypes.data, a.ctypes.data, c.ctypes.data, 4, 4, 4, 0, None)
     assert st == mt.MT_ERR_NO_DEVICE
     assert np.all(c == 0)
+
+
+def test_split_k_plan():
+    # No automatic split; an explicit split applies to every tile and needs
+    # one partial tile per slice; split_k = 1 is the same as none.
+    st, p = plan(4096, 4096, 4096)
+    assert st == mt.MT_OK and (p.bm, p.bn) == (128, 128)
+    assert p.split_k == 1 and p.workspace_bytes == 0
+    st, p = plan(4096, 4096, 4096, split_k=2)
+    assert p.grid == 1024 * 2 and p.workspace_bytes == 1024 * 2 * 128 * 128 * 4
+    st, p = plan(4096, 4096, 4096, split_k=3)
+    assert p.split_k == 3 and p.grid == 1024 * 3
+    st, p = plan(4096, 4096, 4096, split_k=1)
+    assert p.split_k == 1 and p.grid == 1024 and p.workspace_bytes == 0
+    # A split larger than the K tiles is clamped to one K tile per slice.
+    st, p = plan(64, 64, 64, split_k=4)
+    assert p.split_k == 2

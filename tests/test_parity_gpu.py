@@ -22,12 +22,17 @@ FFMA_TOL = 1e-5
 # Every FFMA tile configuration the library builds (tile choice, micro-kernel).
 FFMA_CONFIGS = [
     dict(),                                           # automatic
-    dict(bm=128, bn=128, bk=32, stages=3, fma=2),
+    dict(bm=128, bn=128, bk=32, stages=3, fma=2),     # 4 warps of 64 x 64
+    dict(bm=128, bn=128, bk=32, stages=3, fma=2, wm=32, wn=64),
+    dict(bm=128, bn=128, bk=32, stages=3, fma=2, wm=64, wn=32),
+    dict(bm=128, bn=128, bk=16, stages=4, fma=2),
+    dict(bm=256, bn=128, fma=2),
     dict(bm=128, bn=128, bk=32, stages=3, fma=1),
     dict(bm=128, bn=128, bk=32, stages=4, fma=2),
     dict(bm=128, bn=256, bk=32, stages=3, fma=2),
     dict(bm=64, bn=64, bk=32, stages=3, fma=2),
     dict(bm=128, bn=128, bk=32, stages=3, fma=2, no_pad=True),
+    dict(bm=128, bn=128, bk=32, stages=3, fma=2, wm=32, wn=64, no_pad=True),
 ]
 ALL_VARIANTS = FFMA_CONFIGS + [dict(variant="p18"), dict(variant="p18", no_pad=True)]
 
@@ -133,12 +138,33 @@ def test_identity_and_permutation_exact(cfg):
 
 
 def test_all_variants_agree_bitwise():
-    # Every FFMA/P18 output is the same chain of fp32 FMAs in increasing k,
-    # so every variant must produce the same bits.
+    # Without K splitting, every FFMA/P18 output is the same chain of fp32
+    # FMAs in increasing k, so every variant must produce the same bits.
     A, B = gemm_inputs.make_ab(200, 136, 300, seed=12, dist="normal")
     ref = run(A, B, variant="p18")
     for cfg in FFMA_CONFIGS:
-        assert torch.equal(run(A, B, **cfg), ref), cfg
+        assert torch.equal(run(A, B, split_k=1, **cfg), ref), cfg
+
+
+@pytest.mark.parametrize("split", [2, 3, 4])
+@pytest.mark.parametrize("shape", [(257, 130, 777), (1000, 1000, 1000), (64, 64, 4096)])
+def test_split_k_matches_oracle_and_is_deterministic(shape, split):
+    M, N, K = shape
+    A, B = gemm_inputs.make_ab(M, N, K, seed=16, dist="normal")
+    Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
+    first = run(A, B, split_k=split)
+    assert_within(first.numpy(), Cref, W, FFMA_TOL, f"split {split}")
+    assert torch.equal(run(A, B, split_k=split), first)  # slices add in a fixed order
+
+
+def test_split_k_integer_inputs_bit_exact():
+    A, B = gemm_inputs.make_ab(300, 200, 1024, seed=17, dist="int")
+    Cref = oracle.sgemm(A.numpy(), B.numpy())
+    for split in (2, 4):
+        assert np.array_equal(run(A, B, split_k=split).numpy(), Cref)
+
+
+
 
 
 # --- edge cases ---------------------------------------------------------------------

@@ -1,5 +1,6 @@
 // Host side of the C ABI: argument checks, variant and tile selection,
 // shared-memory budget, launch, and the pure-host layout helpers.
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cstdint>
@@ -75,6 +76,8 @@ struct Launch {
   bool pad = true;
   int fault_inject = 0;
   int max_ctas = 0;  // persistent kernels: CTAs to launch at most
+  // FFMA split-K tail (see GemmArgs).
+  int full_tiles = 0, split = 1, kt_per_slice = 0;
 };
 
 mt_status check_dims(int64_t M, int64_t N, int64_t K) {
@@ -179,7 +182,7 @@ mt_status plan_call(const float* A, const float* B, const float* C, int64_t M, i
     return MT_ERR_INVALID_ARG;
   if (cfg && (cfg->wm || cfg->wn) && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
   if (cfg && cfg->fault_inject && variant != MT_VARIANT_TF32X3) return MT_ERR_UNSUPPORTED;
-  if (cfg && cfg->split_k > 1) return MT_ERR_UNSUPPORTED;
+  if (cfg && cfg->split_k > 1 && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
   const bool pad = !(cfg && cfg->no_pad);
   L->fault_inject = cfg ? cfg->fault_inject : 0;
   mt_plan& p = L->plan;
@@ -252,8 +255,31 @@ mt_status plan_call(const float* A, const float* B, const float* C, int64_t M, i
   L->kern = E.kern[p.vec_ab][pad ? 1 : 0];
   L->tiles_m = static_cast<int>(ceil_div(M, E.bm));
   L->tiles_n = static_cast<int>(ceil_div(N, E.bn));
-  p.grid = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
-  if (p.grid > INT32_MAX) return MT_ERR_UNSUPPORTED;
+  const int64_t tiles = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
+  if (tiles > INT32_MAX / 4) return MT_ERR_UNSUPPORTED;
+  // Split-K: the tiles of the split part are cut along K into slices whose
+  // partial tiles add up in a second kernel (see GemmArgs).
+  const int64_t ktiles = ceil_div(K, E.bk);
+  const int64_t slots = static_cast<int64_t>(sms > 0 ? sms : 1) * E.min_blocks;
+  int64_t full = tiles, split = 1;
+  // Automatic splitting is off: on GB300 a partial last wave runs one CTA
+  // per SM at most of the two-CTA rate, and splitting it (or a small grid)
+  // measured no faster; an explicit split_k splits every tile.
+  (void)slots;
+  if (cfg && cfg->split_k > 1) {
+    full = 0;
+    split = std::min<int64_t>(cfg->split_k, ktiles > 0 ? ktiles : 1);
+  }
+  if (split <= 1) {
+    split = 1;
+    full = tiles;
+  }
+  L->full_tiles = static_cast<int>(full);
+  L->split = static_cast<int>(split);
+  L->kt_per_slice = static_cast<int>(ceil_div(ktiles, split));
+  p.split_k = L->split;
+  p.grid = full + (tiles - full) * split;
+  p.workspace_bytes = (tiles - full) * split * E.bm * E.bn * 4;
   // The budget check comes before anything is launched ("Part 18", section
   // "Shared-memory budget checks include stages and padding").
   if (p.smem_bytes > smem_limit) return MT_ERR_SMEM_BUDGET;
@@ -277,6 +303,7 @@ mt_status set_smem_attr(int dev, const Launch& L) {
 }
 
 mt_status run_tf32x3(int dev, const mt::GemmArgs& args, const Launch& L, cudaStream_t stream);
+mt_status pool_for(int dev, cudaMemPool_t* pool);
 
 mt_status run(const float* A, const float* B, float* C, int64_t M, int64_t N, int64_t K,
               cudaStream_t stream, const mt_config* cfg) {
@@ -299,7 +326,7 @@ mt_status run(const float* A, const float* B, float* C, int64_t M, int64_t N, in
     return MT_OK;
   }
   mt::GemmArgs args{A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                    L.tiles_m, L.tiles_n, L.group_m};
+                    L.tiles_m, L.tiles_n, L.group_m, L.tiles_m * L.tiles_n, 1, 0, nullptr};
   if (L.plan.variant == MT_VARIANT_TF32X3) return run_tf32x3(dev, args, L, stream);
   if (L.plan.variant == MT_VARIANT_P18) {
     if (mt::launch_p18(args, L.pad, stream) != cudaSuccess) return MT_ERR_LAUNCH;
@@ -307,10 +334,29 @@ mt_status run(const float* A, const float* B, float* C, int64_t M, int64_t N, in
   }
   st = set_smem_attr(dev, L);
   if (st != MT_OK) return st;
+  args.full_tiles = L.full_tiles;
+  args.split = L.split;
+  args.kt_per_slice = L.kt_per_slice;
+  void* ws = nullptr;
+  cudaMemPool_t pool = nullptr;
+  if (L.plan.workspace_bytes > 0) {
+    st = pool_for(dev, &pool);
+    if (st != MT_OK) return st;
+    if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(L.plan.workspace_bytes), pool,
+                                stream) != cudaSuccess) {
+      cudaGetLastError();
+      return MT_ERR_CUDA;
+    }
+    args.partial = static_cast<float*>(ws);
+  }
   void* params[] = {&args};
-  if (cudaLaunchKernel(L.kern, dim3(static_cast<unsigned>(L.plan.grid)),
-                       dim3(static_cast<unsigned>(L.plan.threads)), params,
-                       static_cast<size_t>(L.plan.smem_bytes), stream) != cudaSuccess) {
+  bool ok = cudaLaunchKernel(L.kern, dim3(static_cast<unsigned>(L.plan.grid)),
+                             dim3(static_cast<unsigned>(L.plan.threads)), params,
+                             static_cast<size_t>(L.plan.smem_bytes), stream) == cudaSuccess;
+  if (ok && ws) ok = mt::launch_splitk_reduce(args, L.plan.bm, L.plan.bn, L.plan.vec_c != 0,
+                                              stream) == cudaSuccess;
+  if (ws) cudaFreeAsync(ws, stream);
+  if (!ok) {
     cudaGetLastError();
     return MT_ERR_LAUNCH;
   }
@@ -472,7 +518,7 @@ mt_status mt_sgemm_tf32x3_noalloc(const float* A, const float* B, float* C, int6
     return MT_ERR_CUDA;
   }
   mt::GemmArgs args{A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                    L.tiles_m, L.tiles_n, L.group_m};
+                    L.tiles_m, L.tiles_n, L.group_m, L.tiles_m * L.tiles_n, 1, 0, nullptr};
   if (mt::launch_tf32x3(args, scratch, L.plan.vec_ab != 0, L.plan.vec_c != 0, L.plan.bk,
                         L.plan.bn, L.max_ctas, 0, stream) !=
       cudaSuccess) {

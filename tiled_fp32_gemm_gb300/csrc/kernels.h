@@ -28,7 +28,23 @@ struct GemmArgs {
   int M, N, K;
   int tiles_m, tiles_n;
   int group_m;
+  // Split-K tail (FFMA kernel): work units below full_tiles are whole tiles
+  // (tile = unit, in grouped raster order); the remaining tiles are cut
+  // into `split` K slices of kt_per_slice K tiles each, one unit per slice,
+  // and each slice writes its fp32 partial tile to `partial` (dense
+  // BM x BN blocks, slice-major per tile).  full_tiles = all tiles and
+  // split = 1 when nothing is split.
+  int full_tiles;
+  int split;
+  int kt_per_slice;
+  float* partial;
 };
+
+// Sums the K-slice partials of the split tiles (in slice order, so the
+// result does not depend on scheduling) and writes them to C with the
+// edge masks.  One CTA per split tile.
+cudaError_t launch_splitk_reduce(const GemmArgs& a, int bm, int bn, bool vec_c,
+                                 cudaStream_t stream);
 
 // The one-warp kernel restating the pages' Version 18 (BM=4, BN=8, BK=16,
 // two stages, synchronous staging, padded A).  pad selects the rule's

@@ -215,12 +215,25 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
   float* As = reinterpret_cast<float*>(smem_f4);
   float* Bs = As + LA.size();
 
-  int tm, tn;
-  grouped_tile(blockIdx.x, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
-  const int m0 = tm * T::BM, n0 = tn * T::BN;
   const int M = args.M, N = args.N, K = args.K;
   const int tid = threadIdx.x;
-  const int ktiles = (K + T::BK - 1) / T::BK;
+
+  // Work unit: a whole tile, or one K slice of a tile of the split tail,
+  // whose fp32 partial goes to the workspace instead of C.
+  const int ktiles_all = (K + T::BK - 1) / T::BK;
+  int tile = blockIdx.x, slice = 0, kt_begin = 0, kt_end = ktiles_all;
+  const bool partial = static_cast<int>(blockIdx.x) >= args.full_tiles;
+  if (partial) {
+    const int v = blockIdx.x - args.full_tiles;
+    tile = args.full_tiles + v / args.split;
+    slice = v % args.split;
+    kt_begin = min(ktiles_all, slice * args.kt_per_slice);
+    kt_end = min(ktiles_all, kt_begin + args.kt_per_slice);
+  }
+  const int ktiles = kt_end - kt_begin;
+  int tm, tn;
+  grouped_tile(tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
+  const int m0 = tm * T::BM, n0 = tn * T::BN;
 
   const Stager<T, VEC> stager(args.A, args.B, M, N, K, m0, n0, tid);
 
@@ -228,7 +241,7 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
   // groups keep the count uniform when K has fewer tiles).
 #pragma unroll
   for (int s = 0; s < T::STAGES - 1; ++s) {
-    if (s < ktiles) stager.load(As, Bs, LA, LB, s, s);
+    if (s < ktiles) stager.load(As, Bs, LA, LB, s, kt_begin + s);
     cp_async_commit();
   }
 
@@ -254,7 +267,8 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     // iteration kt-1) is no longer being read.
     cp_async_wait<T::STAGES - 2>();
     __syncthreads();
-    if (kt + T::STAGES - 1 < ktiles) stager.load(As, Bs, LA, LB, load_stage, kt + T::STAGES - 1);
+    if (kt + T::STAGES - 1 < ktiles)
+      stager.load(As, Bs, LA, LB, load_stage, kt_begin + kt + T::STAGES - 1);
     cp_async_commit();
 
     const float* a_ptr = As + stage * LA.stage_size() + a_off;
@@ -293,6 +307,26 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     }
     stage = stage + 1 == T::STAGES ? 0 : stage + 1;
     load_stage = load_stage + 1 == T::STAGES ? 0 : load_stage + 1;
+  }
+
+  if (partial) {
+    // The slice's partial tile, dense BM x BN (rows and columns past M or N
+    // hold zeros from the zero-filled staging and are never read back).
+    float* P = args.partial +
+               (static_cast<int64_t>(tile - args.full_tiles) * args.split + slice) *
+                   (T::BM * T::BN);
+#pragma unroll
+    for (int i = 0; i < T::TM; ++i) {
+      const int r = wm * T::WM + i * T::LM + lm;
+#pragma unroll
+      for (int g = 0; g < T::TN / 4; ++g) {
+        const int c = wn * T::WN + g * T::LN * 4 + ln * 4;
+        *reinterpret_cast<float4*>(P + r * T::BN + c) =
+            make_float4(acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
+                        acc[i][2 * g + 1].y);
+      }
+    }
+    return;
   }
 
   // Masked epilogue: C[row, col] for row < M, col < N.
