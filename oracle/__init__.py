@@ -7,7 +7,8 @@ library shares no code with it.
 * ``sgemm`` / ``sgemm_rows`` / ``sgemm_elements``: the plain definition of
   C = A*B (row-major, fp64 accumulation in increasing k, one rounding to
   fp32), from ``ref_gemm.c``; see that file's header for the passages it
-  follows.
+  follows.  ``sgemm_general``: alpha*op(A)*op(B) + beta*C with leading
+  dimensions and transposes, the same sum with one rounding.
 * ``smem_rules``: the pages' padding rule, bank mapping, staged layout,
   stage selection and budget formula, plus a bank-conflict simulator.
 
@@ -64,6 +65,10 @@ def load(path: str | None = None):
         lib.oracle_sgemm_elements.argtypes = [p, p, p, p, i64, i64, i64, p, p,
                                               i64]
         lib.oracle_sgemm_elements.restype = ctypes.c_int
+        lib.oracle_sgemm_general.argtypes = [p, i64, p, i64, p, i64, p, i64, i64, i64,
+                                             ctypes.c_double, ctypes.c_double, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int]
+        lib.oracle_sgemm_general.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         if path is None:
@@ -138,3 +143,21 @@ def sgemm_elements(A, B, ii, jj, lib=None):
     if rc:
         raise RuntimeError("oracle_sgemm_elements failed")
     return out, w
+
+
+def sgemm_general(A, B, C0, M, N, K, lda, ldb, ldc, alpha=1.0, beta=0.0,
+                  trans_a=False, trans_b=False, with_w=False, threads: int = 0, lib=None):
+    """alpha*op(A)*op(B) + beta*C on flat float32 buffers with leading
+    dimensions (see oracle_sgemm_general); returns the new C buffer (and W,
+    M x N, if asked).  C0 is copied, never modified."""
+    A = np.ascontiguousarray(np.asarray(A, np.float32).reshape(-1))
+    B = np.ascontiguousarray(np.asarray(B, np.float32).reshape(-1))
+    C = np.array(np.asarray(C0, np.float32).reshape(-1), copy=True)
+    W = np.empty((M, N), np.float64) if with_w else None
+    rc = (lib or load()).oracle_sgemm_general(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc,
+                                              _ptr(W) if with_w else None, M, N, K,
+                                              float(alpha), float(beta), int(trans_a),
+                                              int(trans_b), threads)
+    if rc:
+        raise RuntimeError("oracle_sgemm_general failed")
+    return (C, W) if with_w else C

@@ -134,6 +134,61 @@ int oracle_sgemm_elements(const float *A, const float *B, float *out,
     return 0;
 }
 
+/* The general form (BLAS-style):
+ *
+ *     C[i][j] = fp32( alpha * sum_k a(i,k) * b(k,j)  +  beta * C[i][j] )
+ *
+ * summed in increasing k in double, rounded once, with
+ *   a(i,k) = trans_a ? A[k*lda + i] : A[i*lda + k]
+ *   b(k,j) = trans_b ? B[j*ldb + k] : B[k*ldb + j]
+ * and C[i][j] at C[i*ldc + j].  beta == 0 means C is not read (a NaN in C
+ * is overwritten); alpha == 0 means A and B are not read.  With alpha = 1,
+ * beta = 0, no transposes and packed leading dimensions this is exactly
+ * oracle_sgemm (same sum, same rounding).  W (optional, M x N packed)
+ * receives |alpha| * sum_k |a(i,k)| |b(k,j)| + |beta| * |C[i][j]|, the
+ * scale of the general form's tolerance.  Returns 0, or -1 on a bad
+ * argument or allocation failure. */
+int oracle_sgemm_general(const float *A, int64_t lda, const float *B, int64_t ldb,
+                         float *C, int64_t ldc, double *W, int64_t M, int64_t N,
+                         int64_t K, double alpha, double beta, int trans_a, int trans_b,
+                         int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || ldc < N) return -1;
+    if (!trans_a && lda < K) return -1;
+    if (trans_a && lda < M) return -1;
+    if (!trans_b && ldb < N) return -1;
+    if (trans_b && ldb < K) return -1;
+    if (M == 0 || N == 0) return 0;
+    int failed = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(|:failed)
+#endif
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double acc = 0.0, w = 0.0;
+            if (alpha != 0.0) {
+                for (int64_t k = 0; k < K; ++k) {
+                    const double a = (double)(trans_a ? A[k * lda + i] : A[i * lda + k]);
+                    const double b = (double)(trans_b ? B[j * ldb + k] : B[k * ldb + j]);
+                    acc += a * b;
+                    w += fabs(a) * fabs(b);
+                }
+            }
+            double c = alpha * acc;
+            double wc = fabs(alpha) * w;
+            if (beta != 0.0) {
+                const double c0 = (double)C[i * ldc + j];
+                c += beta * c0;
+                wc += fabs(beta) * fabs(c0);
+            }
+            C[i * ldc + j] = (float)c;
+            if (W) W[i * N + j] = wc;
+        }
+    }
+    return failed ? -1 : 0;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP

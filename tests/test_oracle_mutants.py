@@ -35,6 +35,12 @@ MUTANTS = {
                       "wacc[j] += aa * (double)b_row[j];"),
     "elements_transposed_b": ("const double b = (double)B[k * N + j];",
                               "const double b = (double)B[j * K + k];"),
+    "general_beta_dropped": ("c += beta * c0;", "c += 0.0 * c0;"),
+    "general_alpha_sign": ("double c = alpha * acc;", "double c = -alpha * acc;"),
+    "general_trans_b_swapped": ("(trans_b ? B[j * ldb + k] : B[k * ldb + j])",
+                                "(trans_b ? B[k * ldb + j] : B[j * ldb + k])"),
+    "general_lda_ignored": ("(trans_a ? A[k * lda + i] : A[i * lda + k])",
+                            "(trans_a ? A[k * lda + i] : A[i * K + k])"),
 }
 
 

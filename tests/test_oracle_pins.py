@@ -264,3 +264,57 @@ def test_vector_rule_reduces_to_scalar_rule_on_slots():
         for rows in (1, 2, 4, 8):
             slots = 8 // math.gcd(cols // 4, 8)
             assert R.vector_row_padding(cols, rows) == 4 * int(rows > slots)
+
+
+# --- the general form: leading dimensions, transposes, alpha and beta --------
+def general(A, B, C0, M, N, K, lda, ldb, ldc, **kw):
+    return oracle.sgemm_general(A, B, C0, M, N, K, lda, ldb, ldc, lib=LIB, **kw)
+
+
+def test_general_reduces_to_plain_product():
+    g = rng(30)
+    M, N, K = 37, 29, 41
+    A = g.standard_normal((M, K)).astype(np.float32)
+    B = g.standard_normal((K, N)).astype(np.float32)
+    C = general(A, B, np.full(M * N, np.nan, np.float32), M, N, K, K, N, N)
+    assert np.array_equal(C.reshape(M, N), gemm(A, B))  # beta = 0 never reads C
+
+
+def test_general_leading_dimensions_and_transposes():
+    g = rng(31)
+    M, N, K = 13, 11, 17
+    A = g.standard_normal((M, K)).astype(np.float32)
+    B = g.standard_normal((K, N)).astype(np.float32)
+    ref = gemm(A, B)
+    lda, ldb, ldc = K + 5, N + 3, N + 7
+    Ab = np.full((M, lda), np.nan, np.float32)
+    Ab[:, :K] = A
+    Bb = np.full((K, ldb), np.nan, np.float32)
+    Bb[:, :N] = B
+    C = general(Ab, Bb, np.zeros(M * ldc, np.float32), M, N, K, lda, ldb, ldc)
+    assert np.array_equal(C.reshape(M, ldc)[:, :N], ref)
+    assert np.all(C.reshape(M, ldc)[:, N:] == 0)  # columns past N untouched
+    # Transposed storage: A as K x M (lda >= M), B as N x K (ldb >= K).
+    At = np.full((K, M + 2), np.nan, np.float32)
+    At[:, :M] = A.T
+    Bt = np.full((N, K + 1), np.nan, np.float32)
+    Bt[:, :K] = B.T
+    C = general(At, Bt, np.zeros(M * N, np.float32), M, N, K, M + 2, K + 1, N,
+                trans_a=True, trans_b=True)
+    assert np.array_equal(C.reshape(M, N), ref)
+
+
+def test_general_alpha_beta_exact_on_integers():
+    g = rng(32)
+    M, N, K = 9, 14, 23
+    Ai = g.integers(-8, 9, (M, K))
+    Bi = g.integers(-8, 9, (K, N))
+    Ci = g.integers(-50, 51, (M, N))
+    C, W = general(Ai.astype(np.float32), Bi.astype(np.float32), Ci.astype(np.float32),
+                   M, N, K, K, N, N, alpha=2.0, beta=-3.0, with_w=True)
+    assert np.array_equal(C.reshape(M, N).astype(np.int64), 2 * (Ai @ Bi) - 3 * Ci)
+    assert np.array_equal(W, 2 * (np.abs(Ai) @ np.abs(Bi)) + 3 * np.abs(Ci))
+    # alpha = 0: A and B are not read (NaN there does not propagate).
+    C = general(np.full(M * K, np.nan, np.float32), np.full(K * N, np.nan, np.float32),
+                Ci.astype(np.float32), M, N, K, K, N, N, alpha=0.0, beta=0.5)
+    assert np.array_equal(C.reshape(M, N), (0.5 * Ci).astype(np.float32))
