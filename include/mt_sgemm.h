@@ -120,6 +120,33 @@ MT_API mt_status mt_sgemm_ex(const float *A, const float *B, float *C,
                       const mt_config *cfg);
 
 /*
+ * The general form, BLAS-style:
+ *
+ *     C = alpha * op(A) * op(B) + beta * C
+ *
+ * op(A) is M x K: A[i*lda + k], or A[k*lda + i] when trans_a (A stored
+ * K x M); op(B) is K x N: B[k*ldb + j], or B[j*ldb + k] when trans_b (B
+ * stored N x K); C[i][j] is at C[i*ldc + j].  The pages' loads are the
+ * row-major case with packed rows ("My Triton From Scratch, Part 14: Shared
+ * Memory Tiles", section "Cooperative copy mapping": only row-major order
+ * (1, 0)); this entry point adds any leading dimension, transposed storage
+ * and the alpha/beta update.  trans_a, trans_b: 0 or 1.  Leading dimensions
+ * in elements: lda >= (trans_a ? M : K), ldb >= (trans_b ? K : N),
+ * ldc >= N, each at least 1.  beta == 0: C is only written (NaN or Inf in
+ * C do not propagate); alpha == 0 or K == 0: A and B are not read and
+ * C = beta * C.  mt_sgemm(A, B, C, M, N, K, s) is the same as
+ * mt_sgemm_general(0, 0, M, N, K, 1, A, K, B, N, 0, C, N, s, NULL).
+ * Every variant supports every form; FFMA stages transposed operands with
+ * 4-byte copies (the automatic tiles and 64 x 64 only — other explicit
+ * tiles return MT_ERR_UNSUPPORTED).  Errors as mt_sgemm_ex (MT_ERR_ALIAS
+ * compares the spans each view covers).
+ */
+MT_API mt_status mt_sgemm_general(int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
+                                  float alpha, const float *A, int64_t lda, const float *B,
+                                  int64_t ldb, float beta, float *C, int64_t ldc,
+                                  cudaStream_t stream, const mt_config *cfg);
+
+/*
  * C = A*B with A, B, C in HOST memory (pageable or pinned).  Copies A and B
  * to the device, multiplies, copies C back and synchronises `stream` before
  * returning, so on MT_OK the host C holds the result.  Device buffers come

@@ -232,3 +232,24 @@ def test_split_k_plan():
     # A split larger than the K tiles is clamped to one K tile per slice.
     st, p = plan(64, 64, 64, split_k=4)
     assert p.split_k == 2
+
+
+def test_general_form_argument_checks():
+    g = mt.mt_sgemm_general
+    # Leading dimensions below the row length are rejected before any device work.
+    assert g(0, 0, 8, 8, 8, 1.0, 1 << 20, 7, 1 << 30, 8, 0.0, 1 << 34, 8, 0, None) == \
+        mt.MT_ERR_INVALID_ARG                                   # lda < K
+    assert g(1, 0, 8, 8, 4, 1.0, 1 << 20, 7, 1 << 30, 8, 0.0, 1 << 34, 8, 0, None) == \
+        mt.MT_ERR_INVALID_ARG                                   # transposed A: lda < M
+    assert g(0, 1, 8, 8, 9, 1.0, 1 << 20, 9, 1 << 30, 8, 0.0, 1 << 34, 8, 0, None) == \
+        mt.MT_ERR_INVALID_ARG                                   # transposed B: ldb < K
+    assert g(0, 0, 8, 8, 8, 1.0, 1 << 20, 8, 1 << 30, 8, 0.0, 1 << 34, 7, 0, None) == \
+        mt.MT_ERR_INVALID_ARG                                   # ldc < N
+    assert g(2, 0, 8, 8, 8, 1.0, 1 << 20, 8, 1 << 30, 8, 0.0, 1 << 34, 8, 0, None) == \
+        mt.MT_ERR_INVALID_ARG                                   # trans flag not 0/1
+    # C's span (rows of ldc floats) overlapping A's span is aliasing ...
+    a, c = 1 << 20, (1 << 20) + 4 * 100
+    assert g(0, 0, 4, 4, 4, 1.0, a, 64, 1 << 30, 4, 0.0, c, 4, 0, None) == mt.MT_ERR_ALIAS
+    # ... but not when A is never read (alpha == 0).
+    st = g(0, 0, 4, 4, 4, 0.0, a, 64, 1 << 30, 4, 0.0, c, 4, 0, None)
+    assert st in (mt.MT_OK, mt.MT_ERR_NO_DEVICE)

@@ -1,0 +1,142 @@
+"""GPU parity of the general form C = alpha*op(A)*op(B) + beta*C.
+
+Leading dimensions, transposed storage and the alpha/beta update through
+mt_sgemm_general, for every variant, against the oracle's general form
+(oracle_sgemm_general: the same fp64 sum, one rounding).  Tolerance scale:
+W = |alpha| * |op(A)|*|op(B)| + |beta| * |C|; FFMA and P18 within 1e-5 * W,
+3xTF32 within 5e-5 * W, integer-valued inputs bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tiled_fp32_gemm_gb300 as mt
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = [(dict(), 1e-5), (dict(bm=128, bn=128), 1e-5), (dict(bm=64, bn=64), 1e-5),
+            (dict(variant="p18"), 1e-5), (dict(variant="tf32x3"), 5e-5),
+            (dict(variant="tf32x3", bn=64), 5e-5)]
+VIDS = ["ffma", "ffma128", "ffma64", "p18", "tf32x3", "tf32x3-bn64"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    from tiled_fp32_gemm_gb300 import build
+    build.build()
+    return mt.lib()
+
+
+def stored(g, rows, cols, ld, dist="normal"):
+    """A rows x cols matrix inside a rows x ld buffer whose extra columns are NaN."""
+    buf = np.full((rows, ld), np.nan, np.float32)
+    if dist == "int":
+        buf[:, :cols] = g.integers(-8, 9, (rows, cols))
+    else:
+        buf[:, :cols] = g.standard_normal((rows, cols))
+    return buf
+
+
+def run_general(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, **cfg):
+    a, b, c = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), torch.from_numpy(C0).cuda()
+    st = mt.mt_sgemm_general(ta, tb, M, N, K, alpha, a.data_ptr(), lda, b.data_ptr(), ldb, beta,
+                             c.data_ptr(), ldc, torch.cuda.current_stream().cuda_stream,
+                             mt.make_config(**cfg) if cfg else None)
+    assert st == mt.MT_OK, mt.mt_status_string(st)
+    torch.cuda.synchronize()
+    return c.cpu().numpy()
+
+
+@pytest.mark.parametrize("cfg,tol", VARIANTS, ids=VIDS)
+@pytest.mark.parametrize("ta,tb", [(0, 0), (1, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("shape,pads", [((133, 97, 71), (3, 5, 7)), ((260, 300, 96), (4, 8, 4)),
+                                        ((31, 17, 300), (0, 1, 2))])
+def test_general_matches_oracle(cfg, tol, ta, tb, shape, pads):
+    M, N, K = shape
+    g = np.random.default_rng(M + 7 * N + 13 * K + 2 * ta + tb)
+    lda = (M if ta else K) + pads[0]
+    ldb = (K if tb else N) + pads[1]
+    ldc = N + pads[2]
+    A = stored(g, K if ta else M, M if ta else K, lda)
+    B = stored(g, N if tb else K, K if tb else N, ldb)
+    C0 = stored(g, M, N, ldc)
+    alpha, beta = 1.75, -0.5
+    got = run_general(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, **cfg)
+    want, W = oracle.sgemm_general(A, B, C0, M, N, K, lda, ldb, ldc, alpha, beta, ta, tb,
+                                   with_w=True)
+    want = want.reshape(M, ldc)
+    err = np.abs(got[:, :N].astype(np.float64) - want[:, :N])
+    assert np.all(err <= tol * W), f"max err/W {(err / np.maximum(W, 1e-30)).max():.3g}"
+    assert np.isnan(got[:, N:]).all()  # C's padding columns untouched
+
+
+@pytest.mark.parametrize("cfg,tol", VARIANTS, ids=VIDS)
+def test_general_integers_exact(cfg, tol):
+    M, N, K = 70, 90, 130
+    g = np.random.default_rng(5)
+    for ta, tb in [(0, 0), (1, 1)]:
+        lda, ldb, ldc = (M if ta else K) + 2, (K if tb else N) + 3, N + 1
+        A = stored(g, K if ta else M, M if ta else K, lda, "int")
+        B = stored(g, N if tb else K, K if tb else N, ldb, "int")
+        C0 = stored(g, M, N, ldc, "int")
+        got = run_general(ta, tb, M, N, K, 2.0, A, lda, B, ldb, -3.0, C0, ldc, **cfg)
+        want = oracle.sgemm_general(A, B, C0, M, N, K, lda, ldb, ldc, 2.0, -3.0, ta, tb)
+        assert np.array_equal(got[:, :N], want.reshape(M, ldc)[:, :N])
+
+
+@pytest.mark.parametrize("cfg,tol", VARIANTS, ids=VIDS)
+def test_beta_zero_never_reads_c_and_alpha_zero_never_reads_ab(cfg, tol):
+    M, N, K = 40, 44, 36
+    g = np.random.default_rng(6)
+    A = stored(g, M, K, K)
+    B = stored(g, K, N, N)
+    C0 = np.full((M, N), np.nan, np.float32)
+    got = run_general(0, 0, M, N, K, 1.0, A, K, B, N, 0.0, C0, N, **cfg)
+    want, W = oracle.sgemm(A, B, with_w=True)
+    assert np.isfinite(got).all() and np.all(np.abs(got - want) <= tol * W)
+    # alpha == 0: C = beta * C, A and B (all NaN here) are not read.
+    Cb = stored(g, M, N, N)
+    nanA = np.full((M, K), np.nan, np.float32)
+    nanB = np.full((K, N), np.nan, np.float32)
+    got = run_general(0, 0, M, N, K, 0.0, nanA, K, nanB, N, 0.5, Cb, N, **cfg)
+    assert np.array_equal(got, (0.5 * Cb).astype(np.float32))
+    # K == 0 with beta: the same.
+    got = run_general(0, 0, M, N, 0, 1.0, A, 1, B, N, 2.0, Cb, N, **cfg)
+    assert np.array_equal(got, (2.0 * Cb).astype(np.float32))
+
+
+def test_packed_general_is_the_plain_call_bit_for_bit():
+    M, N, K = 300, 260, 200
+    g = np.random.default_rng(7)
+    A = g.standard_normal((M, K)).astype(np.float32)
+    B = g.standard_normal((K, N)).astype(np.float32)
+    a, b = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    plain = mt.sgemm(a, b)
+    general = mt.gemm(a, b)
+    torch.cuda.synchronize()
+    assert torch.equal(plain, general)
+
+
+def test_torch_views_and_transposes():
+    g = torch.Generator().manual_seed(8)
+    big = torch.randn(300, 400, generator=g).cuda()
+    a = big[10:110, 20:170]          # 100 x 150, row stride 400
+    b = torch.randn(150, 90, generator=g).cuda()
+    c = torch.zeros(100, 128).cuda()[:, :90]
+    mt.gemm(a, b, c)
+    at = a.t().contiguous()          # stored 150 x 100
+    c2 = mt.gemm(at, b, trans_a=True)
+    torch.cuda.synchronize()
+    A, B = a.cpu().numpy(), b.cpu().numpy()
+    want, W = oracle.sgemm(np.ascontiguousarray(A), np.ascontiguousarray(B), with_w=True)
+    assert np.all(np.abs(c.cpu().numpy() - want) <= 1e-5 * W)
+    assert np.all(np.abs(c2.cpu().numpy() - want) <= 1e-5 * W)
+
+
+def test_ffma_transposes_need_a_tile_built_for_them():
+    a = torch.zeros(64, 64, device="cuda")
+    c = torch.zeros(64, 64, device="cuda")
+    st = mt.mt_sgemm_general(1, 0, 64, 64, 64, 1.0, a.data_ptr(), 64, a.data_ptr(), 64, 0.0,
+                             c.data_ptr(), 64, 0, mt.make_config(bm=256, bn=128))
+    assert st == mt.MT_ERR_UNSUPPORTED

@@ -3,7 +3,8 @@
 The compute lives in ``libmtsgemm.so`` (hand-written CUDA for sm_103a, built
 by ``tiled_fp32_gemm_gb300.build``).  This module only marshals arguments:
 
-* ``mt_sgemm``, ``mt_sgemm_ex``, ``mt_sgemm_host``, ``mt_sgemm_tf32x3_noalloc``,
+* ``mt_sgemm``, ``mt_sgemm_ex``, ``mt_sgemm_general``, ``mt_sgemm_host``,
+  ``mt_sgemm_tf32x3_noalloc``,
   ``mt_sgemm_plan``,
   ``mt_smem_row_padding``, ``mt_smem_vector_row_padding``,
   ``mt_smem_layout_make``, ``mt_smem_layout_offset``, ``mt_device_status``,
@@ -83,6 +84,8 @@ SIGNATURES = {
     "mt_sgemm_ex": (_I, [_P, _P, _P, _I64, _I64, _I64, _P, ctypes.POINTER(mt_config)]),
     "mt_sgemm_host": (_I, [_P, _P, _P, _I64, _I64, _I64, _P, ctypes.POINTER(mt_config)]),
     "mt_sgemm_tf32x3_noalloc": (_I, [_P, _P, _P, _I64, _I64, _I64, _P]),
+    "mt_sgemm_general": (_I, [_I, _I, _I64, _I64, _I64, ctypes.c_float, _P, _I64, _P, _I64,
+                              ctypes.c_float, _P, _I64, _P, ctypes.POINTER(mt_config)]),
     "mt_sgemm_plan": (_I, [_P, _P, _P, _I64, _I64, _I64, ctypes.POINTER(mt_config), _I64,
                            ctypes.POINTER(mt_plan)]),
     "mt_smem_row_padding": (_I, [_I, _I]),
@@ -145,6 +148,13 @@ def mt_sgemm_host(A: int, B: int, C: int, M: int, N: int, K: int, stream: int = 
                   cfg: mt_config | None = None) -> int:
     return lib().mt_sgemm_host(A, B, C, M, N, K, stream,
                                ctypes.byref(cfg) if cfg is not None else None)
+
+
+def mt_sgemm_general(trans_a: int, trans_b: int, M: int, N: int, K: int, alpha: float,
+                     A: int, lda: int, B: int, ldb: int, beta: float, C: int, ldc: int,
+                     stream: int = 0, cfg: mt_config | None = None) -> int:
+    return lib().mt_sgemm_general(trans_a, trans_b, M, N, K, alpha, A, lda, B, ldb, beta, C,
+                                  ldc, stream, ctypes.byref(cfg) if cfg is not None else None)
 
 
 def mt_sgemm_tf32x3_noalloc(A: int, B: int, C: int, M: int, N: int, K: int,
@@ -235,3 +245,38 @@ def plan(M: int, N: int, K: int, smem_limit_bytes: int = 0, a=None, b=None, c=No
     if st != MT_OK:
         raise MtError(st, "mt_sgemm_plan")
     return p.as_dict()
+
+
+def gemm(a, b, c=None, alpha=1.0, beta=0.0, trans_a=False, trans_b=False, stream=None,
+         **choices):
+    """c = alpha * op(a) @ op(b) + beta * c on 2-D float32 CUDA tensors whose
+    rows may be strided (unit column stride); op transposes the stored
+    matrix when asked.  Returns c (allocated when not given; then beta must
+    be 0)."""
+    import torch
+    for t, name in ((a, "a"), (b, "b")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda:
+            raise TypeError(f"{name} must be a float32 CUDA tensor")
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError(f"{name} must be 2-D with unit column stride")
+    M, K = (a.shape[1], a.shape[0]) if trans_a else (a.shape[0], a.shape[1])
+    Kb, N = (b.shape[1], b.shape[0]) if trans_b else (b.shape[0], b.shape[1])
+    if K != Kb:
+        raise ValueError("inner dimensions differ")
+    if c is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs c")
+        c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    if c.dim() != 2 or c.stride(1) != 1 or tuple(c.shape) != (M, N):
+        raise ValueError("c must be M x N with unit column stride")
+    def ld(t):  # row stride; any value >= the row length works for one row
+        return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
+
+    s = stream if stream is not None else torch.cuda.current_stream(a.device).cuda_stream
+    with torch.cuda.device(a.device):
+        st = mt_sgemm_general(int(trans_a), int(trans_b), M, N, K, alpha, a.data_ptr(), ld(a),
+                              b.data_ptr(), ld(b), beta, c.data_ptr(), ld(c), s,
+                              make_config(**choices) if choices else None)
+    if st != MT_OK:
+        raise MtError(st, "mt_sgemm_general")
+    return c

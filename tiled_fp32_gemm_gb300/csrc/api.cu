@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <unordered_set>
 
 #include <cuda_runtime.h>
 
@@ -16,7 +17,6 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxEntries = 32;
 // K depth of the 3xTF32 kernel when the caller does not choose: 16 for
 // 256-wide tiles (a 4-stage ring instead of 2), 32 for narrower tiles (3 or
 // 4 stages, half the barrier round trips) — the faster of the two on GB300.
@@ -30,8 +30,8 @@ struct DeviceInfo {
 
 std::mutex g_mutex;
 DeviceInfo g_devices[kMaxDevices];
-// [device][entry][vec][pad]: max dynamic shared memory attribute applied.
-std::atomic<uint8_t> g_attr_done[kMaxDevices][kMaxEntries][2][2];
+// Kernels whose dynamic shared-memory limit was raised, per device.
+std::unordered_set<const void*> g_attr_done[kMaxDevices];
 cudaMemPool_t g_pools[kMaxDevices];
 
 mt_status current_device(int* dev, DeviceInfo* info) {
@@ -67,6 +67,25 @@ bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// One product: C = alpha * op(A) * op(B) + beta * C (see GemmArgs).
+struct Problem {
+  const float* A;
+  const float* B;
+  float* C;
+  int64_t M, N, K;
+  int64_t lda, ldb, ldc;
+  float alpha, beta;
+  int trans_a, trans_b;
+};
+
+// The packed row-major product C = A*B (a leading dimension of at least 1
+// keeps empty operands valid).
+Problem packed_problem(const float* A, const float* B, float* C, int64_t M, int64_t N,
+                       int64_t K) {
+  const int64_t lda = K > 0 ? K : 1, ldn = N > 0 ? N : 1;
+  return Problem{A, B, C, M, N, K, lda, ldn, ldn, 1.0f, 0.0f, 0, 0};
+}
+
 // Everything a launch needs beyond the plan the caller can see.
 struct Launch {
   mt_plan plan;
@@ -76,8 +95,10 @@ struct Launch {
   bool pad = true;
   int fault_inject = 0;
   int max_ctas = 0;  // persistent kernels: CTAs to launch at most
-  // FFMA split-K tail (see GemmArgs).
+  // FFMA split-K (see GemmArgs).
   int full_tiles = 0, split = 1, kt_per_slice = 0;
+  // 3xTF32: float4 reads of A / B by their packers.
+  bool vec_a = false, vec_b = false;
 };
 
 mt_status check_dims(int64_t M, int64_t N, int64_t K) {
@@ -89,17 +110,54 @@ mt_status check_dims(int64_t M, int64_t N, int64_t K) {
   return MT_OK;
 }
 
+// Bytes from the first to one past the last element of a rows x cols view
+// with row stride ld.
+int64_t extent_bytes(int64_t rows, int64_t cols, int64_t ld) {
+  return rows > 0 && cols > 0 ? ((rows - 1) * ld + cols) * 4 : 0;
+}
+
+// Leading dimensions: each stored row must hold its logical row.
+mt_status check_lds(const Problem& P) {
+  const int64_t lim = INT64_MAX / 16;
+  if (P.lda < std::max<int64_t>(1, P.trans_a ? P.M : P.K) ||
+      P.ldb < std::max<int64_t>(1, P.trans_b ? P.K : P.N) || P.ldc < std::max<int64_t>(1, P.N) ||
+      P.lda > lim || P.ldb > lim || P.ldc > lim)
+    return MT_ERR_INVALID_ARG;
+  if ((P.trans_a ? P.K : P.M) > 0 && P.lda > lim / std::max<int64_t>(1, P.trans_a ? P.K : P.M))
+    return MT_ERR_INVALID_ARG;
+  if ((P.trans_b ? P.N : P.K) > 0 && P.ldb > lim / std::max<int64_t>(1, P.trans_b ? P.N : P.K))
+    return MT_ERR_INVALID_ARG;
+  if (P.M > 0 && P.ldc > lim / P.M) return MT_ERR_INVALID_ARG;
+  return MT_OK;
+}
+
+// Whether A and B are read at all (BLAS: not when alpha == 0 or K == 0).
+bool reads_ab(const Problem& P) { return P.K > 0 && P.alpha != 0.0f; }
+
+mt_status check_problem(const Problem& P) {
+  mt_status st = check_dims(P.M, P.N, P.K);
+  if (st != MT_OK) return st;
+  if (P.trans_a < 0 || P.trans_a > 1 || P.trans_b < 0 || P.trans_b > 1) return MT_ERR_INVALID_ARG;
+  st = check_lds(P);
+  if (st != MT_OK) return st;
+  if (P.M == 0 || P.N == 0) return MT_OK;
+  if (!P.C || !aligned4(P.C)) return MT_ERR_INVALID_ARG;
+  if (reads_ab(P) && (!P.A || !P.B || !aligned4(P.A) || !aligned4(P.B))) return MT_ERR_INVALID_ARG;
+  const int64_t c_bytes = extent_bytes(P.M, P.N, P.ldc);
+  if (reads_ab(P)) {
+    const int64_t a_bytes = P.trans_a ? extent_bytes(P.K, P.M, P.lda)
+                                      : extent_bytes(P.M, P.K, P.lda);
+    const int64_t b_bytes = P.trans_b ? extent_bytes(P.N, P.K, P.ldb)
+                                      : extent_bytes(P.K, P.N, P.ldb);
+    if (overlaps(P.C, c_bytes, P.A, a_bytes) || overlaps(P.C, c_bytes, P.B, b_bytes))
+      return MT_ERR_ALIAS;
+  }
+  return MT_OK;
+}
+
 mt_status check_args(const float* A, const float* B, const float* C, int64_t M, int64_t N,
                      int64_t K) {
-  mt_status st = check_dims(M, N, K);
-  if (st != MT_OK) return st;
-  if (M == 0 || N == 0) return MT_OK;
-  if (!C || !aligned4(C)) return MT_ERR_INVALID_ARG;
-  if (K > 0 && (!A || !B || !aligned4(A) || !aligned4(B))) return MT_ERR_INVALID_ARG;
-  const int64_t c_bytes = M * N * 4;
-  if (K > 0 && (overlaps(C, c_bytes, A, M * K * 4) || overlaps(C, c_bytes, B, K * N * 4)))
-    return MT_ERR_ALIAS;
-  return MT_OK;
+  return check_problem(packed_problem(A, B, const_cast<float*>(C), M, N, K));
 }
 
 // Chooses the FFMA table entry.  Explicit choices (tile, stages, warp tile,
@@ -167,12 +225,14 @@ int pick_tf32x3_bn(int64_t M, int64_t N, int sms) {
   return best;
 }
 
-mt_status plan_call(const float* A, const float* B, const float* C, int64_t M, int64_t N,
-                    int64_t K, const mt_config* cfg, int64_t smem_limit, int sms,
+// Pointers are only inspected for alignment here (NULL counts as aligned);
+// check_problem checks them against the sizes.
+mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, int sms,
                     Launch* L) {
-  // Pointers are only inspected for alignment here (NULL counts as
-  // aligned); the caller checks them against the sizes.
+  const int64_t M = P.M, N = P.N, K = P.K;
   mt_status st = check_dims(M, N, K);
+  if (st != MT_OK) return st;
+  st = check_lds(P);
   if (st != MT_OK) return st;
   const int variant = cfg ? cfg->variant : MT_VARIANT_FFMA;
   if (cfg && (cfg->bm < 0 || cfg->bn < 0 || cfg->bk < 0 || cfg->stages < 0 ||
@@ -184,12 +244,17 @@ mt_status plan_call(const float* A, const float* B, const float* C, int64_t M, i
   if (cfg && cfg->fault_inject && variant != MT_VARIANT_TF32X3) return MT_ERR_UNSUPPORTED;
   if (cfg && cfg->split_k > 1 && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
   const bool pad = !(cfg && cfg->no_pad);
+  const bool trans = P.trans_a || P.trans_b;
   L->fault_inject = cfg ? cfg->fault_inject : 0;
   mt_plan& p = L->plan;
   std::memset(&p, 0, sizeof(p));
   p.variant = variant;
   p.split_k = 1;
-  p.vec_ab = (K % 4 == 0) && (N % 4 == 0) && aligned16(A) && aligned16(B) && aligned16(C);
+  // 16-byte staging of both operands and 16-byte stores of C: untransposed
+  // operands whose rows are whole float4s (K, N and every leading dimension
+  // multiples of 4) from 16-byte aligned bases.
+  p.vec_ab = !trans && K % 4 == 0 && N % 4 == 0 && P.lda % 4 == 0 && P.ldb % 4 == 0 &&
+             P.ldc % 4 == 0 && aligned16(P.A) && aligned16(P.B) && aligned16(P.C);
   p.vec_c = p.vec_ab;
   L->pad = pad;
 
@@ -220,13 +285,17 @@ mt_status plan_call(const float* A, const float* B, const float* C, int64_t M, i
     p.bm = bm; p.bn = bn; p.bk = bk; p.stages = stages;
     p.threads = mt::tf32x3_threads();
     p.pad_a = 0; p.pad_b = 0;  // swizzled tiles: the tensor core's layout, no padding
-    // The pack kernel reads A in float4 when K % 4 == 0 and A is 16-byte aligned.
-    p.vec_ab = (K % 4 == 0) && aligned16(A);
-    p.vec_c = (N % 4 == 0) && aligned16(C);
+    // A packer reads float4 when it walks k-contiguous rows (A as stored,
+    // B stored transposed) that are whole float4s from an aligned base.
+    L->vec_a = !P.trans_a && K % 4 == 0 && P.lda % 4 == 0 && aligned16(P.A);
+    L->vec_b = P.trans_b && K % 4 == 0 && P.ldb % 4 == 0 && aligned16(P.B);
+    p.vec_ab = L->vec_a;
+    p.vec_c = N % 4 == 0 && P.ldc % 4 == 0 && aligned16(P.C);
     p.smem_bytes = mt::tf32x3_smem_bytes(bk, bn);
     L->tiles_m = static_cast<int>(ceil_div(M, bm));
     L->tiles_n = static_cast<int>(ceil_div(N, bn));
-    if (L->tiles_m > 65535 || ceil_div(static_cast<int64_t>(L->tiles_n) * bn, 256) > 65535)
+    if (L->tiles_m > 65535 || ceil_div(static_cast<int64_t>(L->tiles_n) * bn, 256) > 65535 ||
+        ceil_div(static_cast<int64_t>(L->tiles_m) * bm, 256) > 65535)
       return MT_ERR_UNSUPPORTED;
     // Persistent: one CTA per SM at most.
     const int64_t tiles = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
@@ -244,28 +313,28 @@ mt_status plan_call(const float* A, const float* B, const float* C, int64_t M, i
   const int i = pick_ffma(cfg, M, N, sms > 0 ? sms : 1);
   if (i < 0) return MT_ERR_UNSUPPORTED;
   const mt::FfmaEntry& E = e[i];
-  if (!E.kern[p.vec_ab][pad ? 1 : 0]) return MT_ERR_UNSUPPORTED;
+  const void* kern = trans ? (pad ? E.kern_t[P.trans_a][P.trans_b] : nullptr)
+                           : E.kern[p.vec_ab][pad ? 1 : 0];
+  if (!kern) return MT_ERR_UNSUPPORTED;
   p.bm = E.bm; p.bn = E.bn; p.bk = E.bk; p.stages = E.stages; p.threads = E.threads;
   p.fma = E.packed ? 2 : 1;
   p.wm = E.wm; p.wn = E.wn; p.tm = E.tm; p.tn = E.tn;
   p.pad_a = pad ? E.pad_a : 0;
-  p.pad_b = pad ? E.pad_b : 0;
-  p.smem_bytes = E.smem_bytes[pad ? 1 : 0];
+  p.pad_b = P.trans_b ? E.pad_b_t : (pad ? E.pad_b : 0);
+  p.smem_bytes = P.trans_b ? E.smem_bytes_t : E.smem_bytes[pad ? 1 : 0];
   L->entry = i;
-  L->kern = E.kern[p.vec_ab][pad ? 1 : 0];
+  L->kern = kern;
   L->tiles_m = static_cast<int>(ceil_div(M, E.bm));
   L->tiles_n = static_cast<int>(ceil_div(N, E.bn));
   const int64_t tiles = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
   if (tiles > INT32_MAX / 4) return MT_ERR_UNSUPPORTED;
   // Split-K: the tiles of the split part are cut along K into slices whose
-  // partial tiles add up in a second kernel (see GemmArgs).
+  // partial tiles add up in a second kernel (see GemmArgs).  Automatic
+  // splitting is off: on GB300 a partial last wave runs one CTA per SM at
+  // most of the two-CTA rate, and splitting it (or a small grid) measured
+  // no faster; an explicit split_k splits every tile.
   const int64_t ktiles = ceil_div(K, E.bk);
-  const int64_t slots = static_cast<int64_t>(sms > 0 ? sms : 1) * E.min_blocks;
   int64_t full = tiles, split = 1;
-  // Automatic splitting is off: on GB300 a partial last wave runs one CTA
-  // per SM at most of the two-CTA rate, and splitting it (or a small grid)
-  // measured no faster; an explicit split_k splits every tile.
-  (void)slots;
   if (cfg && cfg->split_k > 1) {
     full = 0;
     split = std::min<int64_t>(cfg->split_k, ktiles > 0 ? ktiles : 1);
@@ -288,78 +357,14 @@ mt_status plan_call(const float* A, const float* B, const float* C, int64_t M, i
 
 mt_status set_smem_attr(int dev, const Launch& L) {
   if (L.entry < 0 || L.plan.smem_bytes <= 48 * 1024) return MT_OK;
-  std::atomic<uint8_t>& done = g_attr_done[dev][L.entry][L.plan.vec_ab][L.pad ? 1 : 0];
-  if (done.load(std::memory_order_acquire)) return MT_OK;
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (!done.load(std::memory_order_relaxed)) {
-    if (cudaFuncSetAttribute(L.kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(L.plan.smem_bytes)) != cudaSuccess) {
-      cudaGetLastError();
-      return MT_ERR_LAUNCH;
-    }
-    done.store(1, std::memory_order_release);
-  }
-  return MT_OK;
-}
-
-mt_status run_tf32x3(int dev, const mt::GemmArgs& args, const Launch& L, cudaStream_t stream);
-mt_status pool_for(int dev, cudaMemPool_t* pool);
-
-mt_status run(const float* A, const float* B, float* C, int64_t M, int64_t N, int64_t K,
-              cudaStream_t stream, const mt_config* cfg) {
-  mt_status st = check_args(A, B, C, M, N, K);
-  if (st != MT_OK) return st;
-  if (M == 0 || N == 0) return MT_OK;
-  int dev = 0;
-  DeviceInfo info;
-  st = current_device(&dev, &info);
-  if (st != MT_OK) return st;
-  Launch L;
-  st = plan_call(A, B, C, M, N, K, cfg, info.smem_optin, info.sms, &L);
-  if (st != MT_OK) return st;
-  if (K == 0) {
-    // Empty reduction: the accumulator's zeros are the result.
-    if (cudaMemsetAsync(C, 0, static_cast<size_t>(M * N) * 4, stream) != cudaSuccess) {
-      cudaGetLastError();
-      return MT_ERR_LAUNCH;
-    }
-    return MT_OK;
-  }
-  mt::GemmArgs args{A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                    L.tiles_m, L.tiles_n, L.group_m, L.tiles_m * L.tiles_n, 1, 0, nullptr};
-  if (L.plan.variant == MT_VARIANT_TF32X3) return run_tf32x3(dev, args, L, stream);
-  if (L.plan.variant == MT_VARIANT_P18) {
-    if (mt::launch_p18(args, L.pad, stream) != cudaSuccess) return MT_ERR_LAUNCH;
-    return MT_OK;
-  }
-  st = set_smem_attr(dev, L);
-  if (st != MT_OK) return st;
-  args.full_tiles = L.full_tiles;
-  args.split = L.split;
-  args.kt_per_slice = L.kt_per_slice;
-  void* ws = nullptr;
-  cudaMemPool_t pool = nullptr;
-  if (L.plan.workspace_bytes > 0) {
-    st = pool_for(dev, &pool);
-    if (st != MT_OK) return st;
-    if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(L.plan.workspace_bytes), pool,
-                                stream) != cudaSuccess) {
-      cudaGetLastError();
-      return MT_ERR_CUDA;
-    }
-    args.partial = static_cast<float*>(ws);
-  }
-  void* params[] = {&args};
-  bool ok = cudaLaunchKernel(L.kern, dim3(static_cast<unsigned>(L.plan.grid)),
-                             dim3(static_cast<unsigned>(L.plan.threads)), params,
-                             static_cast<size_t>(L.plan.smem_bytes), stream) == cudaSuccess;
-  if (ok && ws) ok = mt::launch_splitk_reduce(args, L.plan.bm, L.plan.bn, L.plan.vec_c != 0,
-                                              stream) == cudaSuccess;
-  if (ws) cudaFreeAsync(ws, stream);
-  if (!ok) {
+  if (g_attr_done[dev].count(L.kern)) return MT_OK;
+  if (cudaFuncSetAttribute(L.kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(L.plan.smem_bytes)) != cudaSuccess) {
     cudaGetLastError();
     return MT_ERR_LAUNCH;
   }
+  g_attr_done[dev].insert(L.kern);
   return MT_OK;
 }
 
@@ -409,6 +414,31 @@ mt_status prepare_tf32x3(int dev, int bk, int bn) {
   return MT_OK;
 }
 
+mt::GemmArgs make_args(const Problem& P, const Launch& L) {
+  mt::GemmArgs a{};
+  a.A = P.A;
+  a.B = P.B;
+  a.C = P.C;
+  a.M = static_cast<int>(P.M);
+  a.N = static_cast<int>(P.N);
+  a.K = static_cast<int>(P.K);
+  a.tiles_m = L.tiles_m;
+  a.tiles_n = L.tiles_n;
+  a.group_m = L.group_m;
+  a.lda = P.lda;
+  a.ldb = P.ldb;
+  a.ldc = P.ldc;
+  a.alpha = P.alpha;
+  a.beta = P.beta;
+  a.trans_a = P.trans_a;
+  a.trans_b = P.trans_b;
+  a.full_tiles = L.full_tiles;
+  a.split = L.split;
+  a.kt_per_slice = L.kt_per_slice;
+  a.partial = nullptr;
+  return a;
+}
+
 mt_status run_tf32x3(int dev, const mt::GemmArgs& args, const Launch& L, cudaStream_t stream) {
   mt_status st0 = prepare_tf32x3(dev, L.plan.bk, L.plan.bn);
   if (st0 != MT_OK) return st0;
@@ -422,10 +452,65 @@ mt_status run_tf32x3(int dev, const mt::GemmArgs& args, const Launch& L, cudaStr
     return MT_ERR_CUDA;
   }
   const cudaError_t e =
-      mt::launch_tf32x3(args, ws, L.plan.vec_ab != 0, L.plan.vec_c != 0, L.plan.bk, L.plan.bn,
+      mt::launch_tf32x3(args, ws, L.vec_a, L.vec_b, L.plan.vec_c != 0, L.plan.bk, L.plan.bn,
                         L.max_ctas, L.fault_inject, stream);
   cudaFreeAsync(ws, stream);
   if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MT_ERR_LAUNCH;
+  }
+  return MT_OK;
+}
+
+mt_status run(const Problem& P, cudaStream_t stream, const mt_config* cfg) {
+  mt_status st = check_problem(P);
+  if (st != MT_OK) return st;
+  if (P.M == 0 || P.N == 0) return MT_OK;
+  int dev = 0;
+  DeviceInfo info;
+  st = current_device(&dev, &info);
+  if (st != MT_OK) return st;
+  Launch L;
+  st = plan_call(P, cfg, info.smem_optin, info.sms, &L);
+  if (st != MT_OK) return st;
+  if (!reads_ab(P)) {
+    // No product to form (K == 0: the accumulator's zeros; alpha == 0):
+    // C = beta * C, A and B untouched.
+    if (mt::launch_scale_c(P.C, static_cast<int>(P.M), static_cast<int>(P.N), P.ldc, P.beta,
+                           stream) != cudaSuccess) {
+      cudaGetLastError();
+      return MT_ERR_LAUNCH;
+    }
+    return MT_OK;
+  }
+  mt::GemmArgs args = make_args(P, L);
+  if (L.plan.variant == MT_VARIANT_TF32X3) return run_tf32x3(dev, args, L, stream);
+  if (L.plan.variant == MT_VARIANT_P18) {
+    if (mt::launch_p18(args, L.pad, stream) != cudaSuccess) return MT_ERR_LAUNCH;
+    return MT_OK;
+  }
+  st = set_smem_attr(dev, L);
+  if (st != MT_OK) return st;
+  void* ws = nullptr;
+  cudaMemPool_t pool = nullptr;
+  if (L.plan.workspace_bytes > 0) {
+    st = pool_for(dev, &pool);
+    if (st != MT_OK) return st;
+    if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(L.plan.workspace_bytes), pool,
+                                stream) != cudaSuccess) {
+      cudaGetLastError();
+      return MT_ERR_CUDA;
+    }
+    args.partial = static_cast<float*>(ws);
+  }
+  void* params[] = {&args};
+  bool ok = cudaLaunchKernel(L.kern, dim3(static_cast<unsigned>(L.plan.grid)),
+                             dim3(static_cast<unsigned>(L.plan.threads)), params,
+                             static_cast<size_t>(L.plan.smem_bytes), stream) == cudaSuccess;
+  if (ok && ws) ok = mt::launch_splitk_reduce(args, L.plan.bm, L.plan.bn, L.plan.vec_c != 0,
+                                              stream) == cudaSuccess;
+  if (ws) cudaFreeAsync(ws, stream);
+  if (!ok) {
     cudaGetLastError();
     return MT_ERR_LAUNCH;
   }
@@ -438,12 +523,20 @@ extern "C" {
 
 mt_status mt_sgemm(const float* A, const float* B, float* C, int64_t M, int64_t N, int64_t K,
                    cudaStream_t stream) {
-  return run(A, B, C, M, N, K, stream, nullptr);
+  return run(packed_problem(A, B, C, M, N, K), stream, nullptr);
 }
 
 mt_status mt_sgemm_ex(const float* A, const float* B, float* C, int64_t M, int64_t N,
                       int64_t K, cudaStream_t stream, const mt_config* cfg) {
-  return run(A, B, C, M, N, K, stream, cfg);
+  return run(packed_problem(A, B, C, M, N, K), stream, cfg);
+}
+
+mt_status mt_sgemm_general(int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
+                           float alpha, const float* A, int64_t lda, const float* B,
+                           int64_t ldb, float beta, float* C, int64_t ldc, cudaStream_t stream,
+                           const mt_config* cfg) {
+  return run(Problem{A, B, C, M, N, K, lda, ldb, ldc, alpha, beta, trans_a, trans_b}, stream,
+             cfg);
 }
 
 mt_status mt_sgemm_host(const float* A, const float* B, float* C, int64_t M, int64_t N,
@@ -470,7 +563,7 @@ mt_status mt_sgemm_host(const float* A, const float* B, float* C, int64_t M, int
   if (ok && a_bytes) ok = cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, stream) == cudaSuccess;
   if (ok && b_bytes) ok = cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, stream) == cudaSuccess;
   if (ok) {
-    st = run(dA, dB, dC, M, N, K, stream, cfg);
+    st = run(packed_problem(dA, dB, dC, M, N, K), stream, cfg);
     if (st == MT_OK)
       ok = cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, stream) == cudaSuccess;
   }
@@ -488,7 +581,8 @@ mt_status mt_sgemm_host(const float* A, const float* B, float* C, int64_t M, int
 mt_status mt_sgemm_tf32x3_noalloc(const float* A, const float* B, float* C, int64_t M,
                                   int64_t N, int64_t K, cudaStream_t stream) {
   static_assert(MT_NOALLOC_SCRATCH_BYTES == mt::kNoAllocScratchBytes, "scratch size");
-  mt_status st = check_args(A, B, C, M, N, K);
+  const Problem P = packed_problem(A, B, C, M, N, K);
+  mt_status st = check_problem(P);
   if (st != MT_OK) return st;
   if (M == 0 || N == 0) return MT_OK;
   int dev = 0;
@@ -499,7 +593,7 @@ mt_status mt_sgemm_tf32x3_noalloc(const float* A, const float* B, float* C, int6
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.variant = MT_VARIANT_TF32X3;
   Launch L;
-  st = plan_call(A, B, C, M, N, K, &cfg, info.smem_optin, info.sms, &L);
+  st = plan_call(P, &cfg, info.smem_optin, info.sms, &L);
   if (st != MT_OK) return st;
   if (K == 0) {
     // Empty reduction: zeros, written without any scratch.
@@ -517,11 +611,9 @@ mt_status mt_sgemm_tf32x3_noalloc(const float* A, const float* B, float* C, int6
     cudaGetLastError();
     return MT_ERR_CUDA;
   }
-  mt::GemmArgs args{A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                    L.tiles_m, L.tiles_n, L.group_m, L.tiles_m * L.tiles_n, 1, 0, nullptr};
-  if (mt::launch_tf32x3(args, scratch, L.plan.vec_ab != 0, L.plan.vec_c != 0, L.plan.bk,
-                        L.plan.bn, L.max_ctas, 0, stream) !=
-      cudaSuccess) {
+  const mt::GemmArgs args = make_args(P, L);
+  if (mt::launch_tf32x3(args, scratch, L.vec_a, L.vec_b, L.plan.vec_c != 0, L.plan.bk,
+                        L.plan.bn, L.max_ctas, 0, stream) != cudaSuccess) {
     cudaGetLastError();
     return MT_ERR_LAUNCH;
   }
@@ -548,7 +640,8 @@ mt_status mt_sgemm_plan(const float* A, const float* B, const float* C, int64_t 
     sms = current_device(&dev, &info) == MT_OK ? info.sms : 152;
   }
   Launch L;
-  mt_status st = plan_call(A, B, C, M, N, K, cfg, smem_limit_bytes, sms, &L);
+  mt_status st = plan_call(packed_problem(A, B, const_cast<float*>(C), M, N, K), cfg,
+                           smem_limit_bytes, sms, &L);
   *out = L.plan;
   return st;
 }

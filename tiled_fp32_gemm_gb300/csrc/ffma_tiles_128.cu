@@ -19,7 +19,7 @@ int ffma_entries_128(FfmaEntry* out) {
   int n = 0;
   // Table order matters: the first entry that matches the caller's
   // choices wins, so each tile's preferred warp layout comes first.
-  out[n++] = make_entry<Tile128x128w64, true, true>();
+  out[n++] = make_entry<Tile128x128w64, true, true, true>();
   out[n++] = make_entry<Tile128x128, true, true>();
   out[n++] = make_entry<Tile128x128, false, false>();
   out[n++] = make_entry<Tile128x128s4, true, false>();

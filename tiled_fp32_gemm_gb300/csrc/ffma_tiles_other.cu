@@ -13,7 +13,7 @@ int ffma_entries_other(FfmaEntry* out) {
   int n = 0;
   out[n++] = make_entry<Tile128x256, true, false>();
   out[n++] = make_entry<Tile256x128, true, false>();
-  out[n++] = make_entry<Tile64x64, true, false>();
+  out[n++] = make_entry<Tile64x64, true, false, true>();
   return n;
 }
 

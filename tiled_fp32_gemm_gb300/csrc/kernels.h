@@ -14,13 +14,25 @@ struct FfmaEntry {
   int packed;          // 1: fma.rn.f32x2 micro-kernel, 0: scalar fma
   int pad_a, pad_b;    // padding words per shared row under the rule
   int smem_bytes[2];   // [pad] dynamic shared memory per CTA
-  const void* kern[2][2];  // [vec][pad]; nullptr when not instantiated
+  const void* kern[2][2];  // [vec][pad], untransposed operands; nullptr when not built
+  // Transposed operands (4-byte staging, padded rows): [trans_a][trans_b],
+  // [0][0] unused; nullptr when not built.
+  const void* kern_t[2][2];
+  int pad_b_t, smem_bytes_t;  // B padding and shared memory when B is transposed
 };
+
+// C = beta * C over an M x N view with row stride ldc (zeros when beta is
+// 0: C is not read).  The whole product when alpha == 0 or K == 0.
+cudaError_t launch_scale_c(float* C, int M, int N, int64_t ldc, float beta,
+                           cudaStream_t stream);
 
 // All FFMA configurations built into the library (null-terminated count).
 const FfmaEntry* ffma_entries(int* count);
 
-// Arguments every GEMM kernel receives.
+// Arguments every GEMM kernel receives:
+//   C = alpha * op(A) * op(B) + beta * C   (beta == 0: C is not read)
+// op(A)[i][k] = trans_a ? A[k*lda + i] : A[i*lda + k],
+// op(B)[k][j] = trans_b ? B[j*ldb + k] : B[k*ldb + j], C[i][j] at C[i*ldc + j].
 struct GemmArgs {
   const float* A;
   const float* B;
@@ -28,6 +40,9 @@ struct GemmArgs {
   int M, N, K;
   int tiles_m, tiles_n;
   int group_m;
+  int64_t lda, ldb, ldc;
+  float alpha, beta;
+  int trans_a, trans_b;
   // Split-K tail (FFMA kernel): work units below full_tiles are whole tiles
   // (tile = unit, in grouped raster order); the remaining tiles are cut
   // into `split` K slices of kt_per_slice K tiles each, one unit per slice,
@@ -65,9 +80,13 @@ int tf32x3_stages(int bk, int bn);
 int tf32x3_threads();
 int tf32x3_bm();
 cudaError_t tf32x3_prepare(int device, int bk, int bn);
-// fault_inject = 1: the copy thread issues nothing (tests the bounded waits).
-cudaError_t launch_tf32x3(const GemmArgs& a, void* workspace, bool vec_ab, bool vec_c, int bk,
-                          int bn, int max_ctas, int fault_inject, cudaStream_t stream);
+// vec_a / vec_b: that operand may be read with float4 by its packer (read
+// k-contiguous, leading dimension % 4 == 0, 16-byte aligned); vec_c: C may
+// be written with float4.  fault_inject = 1: the copy thread issues nothing
+// (tests the bounded waits).
+cudaError_t launch_tf32x3(const GemmArgs& a, void* workspace, bool vec_a, bool vec_b,
+                          bool vec_c, int bk, int bn, int max_ctas, int fault_inject,
+                          cudaStream_t stream);
 // Size of the static scratch the allocation-free tf32x3 entry point uses,
 // and its device address on `device` (looked up once per device; the device
 // must be current).

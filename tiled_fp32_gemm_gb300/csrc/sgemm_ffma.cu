@@ -27,16 +27,45 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(GemmArgs a, int bm, 
       s.z += v.z;
       s.w += v.w;
     }
-    float* c_row = a.C + static_cast<int64_t>(row) * a.N;
+    float* c_row = a.C + static_cast<int64_t>(row) * a.ldc;
+    const float v[4] = {a.alpha * s.x, a.alpha * s.y, a.alpha * s.z, a.alpha * s.w};
     if (vec_c) {
-      *reinterpret_cast<float4*>(c_row + col) = s;
+      float4* cp = reinterpret_cast<float4*>(c_row + col);
+      float4 o = make_float4(v[0], v[1], v[2], v[3]);
+      if (a.beta != 0.0f) {
+        const float4 c0 = *cp;
+        o = make_float4(fmaf(a.beta, c0.x, v[0]), fmaf(a.beta, c0.y, v[1]),
+                        fmaf(a.beta, c0.z, v[2]), fmaf(a.beta, c0.w, v[3]));
+      }
+      *cp = o;
     } else {
-      c_row[col] = s.x;
-      if (col + 1 < a.N) c_row[col + 1] = s.y;
-      if (col + 2 < a.N) c_row[col + 2] = s.z;
-      if (col + 3 < a.N) c_row[col + 3] = s.w;
+      for (int e = 0; e < 4; ++e)
+        if (col + e < a.N)
+          c_row[col + e] = a.beta != 0.0f ? fmaf(a.beta, c_row[col + e], v[e]) : v[e];
     }
   }
+}
+
+// C = beta * C on an M x N view (zeros when beta is 0, C not read).
+__global__ void __launch_bounds__(256) scale_c_kernel(float* C, int M, int N, int64_t ldc,
+                                                     float beta) {
+  const int64_t total = static_cast<int64_t>(M) * N;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t i = e / N, j = e % N;
+    float* c = C + i * ldc + j;
+    *c = beta != 0.0f ? beta * *c : 0.0f;
+  }
+}
+
+cudaError_t launch_scale_c(float* C, int M, int N, int64_t ldc, float beta,
+                           cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(M) * N;
+  if (total <= 0) return cudaSuccess;
+  const int64_t blocks = (total + 255) / 256;
+  scale_c_kernel<<<static_cast<unsigned>(blocks < 65536 ? blocks : 65536), 256, 0, stream>>>(
+      C, M, N, ldc, beta);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_splitk_reduce(const GemmArgs& a, int bm, int bn, bool vec_c,

@@ -63,140 +63,231 @@ struct FfmaTile {
                       STAGES};
   }
   // Every lane of a warp reads the same k row of B: one row at a time, so
-  // the rule gives no padding.
-  static constexpr SmemLayout b_layout(bool pad) {
-    return SmemLayout{BK, BN, pad ? vector_row_padding_rule(BN, 1) : 0, STAGES};
+  // the rule gives no padding.  A transposed B is written instead 8 k rows
+  // at a time at the same column (the staging's lane blocks): the scalar
+  // rule asks for one padding word there, rounded up to a float4 so rows
+  // stay 16-byte aligned for the reads.
+  static constexpr int B_TRANS_PAD = (row_padding_rule(BN, 8) + 3) / 4 * 4;
+  static constexpr SmemLayout b_layout(bool pad, bool trans = false) {
+    return SmemLayout{BK, BN,
+                      trans ? B_TRANS_PAD : (pad ? vector_row_padding_rule(BN, 1) : 0), STAGES};
   }
-  static constexpr int smem_bytes(bool pad) {
-    return a_layout(pad).nbytes() + b_layout(pad).nbytes();
+  static constexpr int smem_bytes(bool pad, bool trans_b = false) {
+    return a_layout(pad).nbytes() + b_layout(pad, trans_b).nbytes();
   }
 };
 
 // ---------------------------------------------------------------------------
-// Global -> shared staging of one K tile (A: BM x BK, B: BK x BN).
-// VEC: 16-byte chunks (needs K % 4 == 0, N % 4 == 0 and 16-byte aligned A, B);
-// otherwise 4-byte elements.  Out-of-bounds chunks are zero-filled.
-template <class T, bool VEC>
-struct Stager;
+// Global -> shared staging of one K tile: A (BM x BK) into As[r][c] and B
+// (BK x BN) into Bs[kk][n], 0.0 where the element lies outside M, N or K.
+//   STAGE_VEC    16-byte chunks along the contiguous dimension (operand not
+//                transposed, leading dimension % 4 == 0, 16-byte aligned);
+//   STAGE_SCALAR 4-byte elements, threads along the contiguous dimension;
+//   STAGE_TRANS  4-byte elements of a transposed operand (A stored K x M, B
+//                stored N x K); a warp copies 8 x 4 blocks, 8 lanes along
+//                the contiguous dimension, so global reads stay within
+//                32-byte sectors and the shared writes land in 32 distinct
+//                banks.
+enum StageMode { STAGE_VEC = 0, STAGE_SCALAR = 1, STAGE_TRANS = 2 };
+
+template <class T, int MODE>
+struct AStage;
+template <class T, int MODE>
+struct BStage;
 
 template <class T>
-struct Stager<T, true> {
-  static constexpr int A_CHUNKS_ROW = T::BK / 4;
-  static constexpr int B_CHUNKS_ROW = T::BN / 4;
-  static_assert(T::THREADS % A_CHUNKS_ROW == 0 && T::THREADS % B_CHUNKS_ROW == 0, "");
-  static constexpr int A_ROWS_STEP = T::THREADS / A_CHUNKS_ROW;
-  static constexpr int B_ROWS_STEP = T::THREADS / B_CHUNKS_ROW;
-  static constexpr int A_ITERS = T::BM / A_ROWS_STEP;
-  static constexpr int B_ITERS = T::BK / B_ROWS_STEP;
-  static_assert(A_ITERS * A_ROWS_STEP == T::BM && B_ITERS * B_ROWS_STEP == T::BK, "");
+struct AStage<T, STAGE_VEC> {
+  static constexpr int CHUNKS_ROW = T::BK / 4;
+  static_assert(T::THREADS % CHUNKS_ROW == 0, "");
+  static constexpr int ROWS_STEP = T::THREADS / CHUNKS_ROW;
+  static constexpr int ITERS = T::BM / ROWS_STEP;
+  static_assert(ITERS * ROWS_STEP == T::BM && ITERS <= 32, "");
+  const float* base;  // any valid address, read by nothing (masked chunks)
+  const float* src;   // A[(m0 + row) * lda + col]
+  int64_t row_step;   // ROWS_STEP * lda
+  int row, col, K;
+  uint32_t rows_ok;   // bit t: row t of this thread's chunks is inside M
 
-  const float* a_src;  // A[m0 + a_row, a_col]
-  const float* b_src;  // B[b_row, n0 + b_col]
-  const float* A;
-  const float* B;
-  int64_t a_row_step, b_row_step;  // elements between rows a thread copies
-  int a_row, a_col, b_row, b_col;
-  int M, N, K;
-  uint32_t a_rows_ok;  // bit t: row t of this thread's A chunks is inside M
-  bool b_col_ok;
-
-  __device__ Stager(const float* A_, const float* B_, int M_, int N_, int K_, int m0, int n0,
-                    int tid)
-      : A(A_), B(B_), M(M_), N(N_), K(K_) {
-    a_row = tid / A_CHUNKS_ROW;
-    a_col = (tid % A_CHUNKS_ROW) * 4;
-    b_row = tid / B_CHUNKS_ROW;
-    b_col = (tid % B_CHUNKS_ROW) * 4;
-    a_row_step = static_cast<int64_t>(A_ROWS_STEP) * K;
-    b_row_step = static_cast<int64_t>(B_ROWS_STEP) * N;
-    a_src = A + static_cast<int64_t>(m0 + a_row) * K + a_col;
-    b_src = B + static_cast<int64_t>(b_row) * N + n0 + b_col;
-    a_rows_ok = 0;
+  __device__ AStage(const GemmArgs& a, int m0, int tid) : base(a.A), K(a.K) {
+    row = tid / CHUNKS_ROW;
+    col = (tid % CHUNKS_ROW) * 4;
+    row_step = static_cast<int64_t>(ROWS_STEP) * a.lda;
+    src = a.A + static_cast<int64_t>(m0 + row) * a.lda + col;
+    rows_ok = 0;
 #pragma unroll
-    for (int t = 0; t < A_ITERS; ++t)
-      if (m0 + a_row + t * A_ROWS_STEP < M) a_rows_ok |= 1u << t;
-    b_col_ok = n0 + b_col < N;
+    for (int t = 0; t < ITERS; ++t)
+      if (m0 + row + t * ROWS_STEP < a.M) rows_ok |= 1u << t;
   }
-
-  template <class LA, class LB>
-  __device__ __forceinline__ void load(float* As, float* Bs, const LA& la, const LB& lb,
-                                       int stage, int kt) const {
+  template <class L>
+  __device__ __forceinline__ void load(float* As, const L& la, int stage, int kt) const {
     const int k0 = kt * T::BK;
-    const bool a_k_ok = k0 + a_col < K;
+    const bool k_ok = k0 + col < K;
 #pragma unroll
-    for (int t = 0; t < A_ITERS; ++t) {
-      const bool ok = a_k_ok && (a_rows_ok >> t & 1u);
-      const float* src = ok ? a_src + t * a_row_step + k0 : A;
-      cp_async_16(smem_u32(As + la.offset(stage, a_row + t * A_ROWS_STEP, a_col)), src,
-                  ok ? 16u : 0u);
-    }
-#pragma unroll
-    for (int t = 0; t < B_ITERS; ++t) {
-      const int kr = k0 + b_row + t * B_ROWS_STEP;
-      const bool ok = b_col_ok && kr < K;
-      const float* src = ok ? b_src + static_cast<int64_t>(k0) * N + t * b_row_step : B;
-      cp_async_16(smem_u32(Bs + lb.offset(stage, b_row + t * B_ROWS_STEP, b_col)), src,
-                  ok ? 16u : 0u);
+    for (int t = 0; t < ITERS; ++t) {
+      const bool ok = k_ok && (rows_ok >> t & 1u);
+      cp_async_16(smem_u32(As + la.offset(stage, row + t * ROWS_STEP, col)),
+                  ok ? src + t * row_step + k0 : base, ok ? 16u : 0u);
     }
   }
 };
 
 template <class T>
-struct Stager<T, false> {
-  static_assert(T::THREADS % T::BK == 0 && T::THREADS % T::BN == 0, "");
-  static constexpr int A_ROWS_STEP = T::THREADS / T::BK;
-  static constexpr int B_ROWS_STEP = T::THREADS / T::BN;
-  static constexpr int A_ITERS = T::BM / A_ROWS_STEP;
-  static constexpr int B_ITERS = T::BK / B_ROWS_STEP;
+struct AStage<T, STAGE_SCALAR> {
+  static_assert(T::THREADS % T::BK == 0, "");
+  static constexpr int ROWS_STEP = T::THREADS / T::BK;
+  static constexpr int ITERS = T::BM / ROWS_STEP;
+  static_assert(ITERS <= 32, "");
+  const float* base;
+  const float* src;
+  int64_t row_step;
+  int row, col, K;
+  uint32_t rows_ok;
 
-  const float* a_src;
-  const float* b_src;
-  const float* A;
-  const float* B;
-  int64_t a_row_step, b_row_step;
-  int a_row, a_col, b_row, b_col;
-  int M, N, K;
-  uint32_t a_rows_ok;
-  bool b_col_ok;
-
-  __device__ Stager(const float* A_, const float* B_, int M_, int N_, int K_, int m0, int n0,
-                    int tid)
-      : A(A_), B(B_), M(M_), N(N_), K(K_) {
-    a_row = tid / T::BK;
-    a_col = tid % T::BK;
-    b_row = tid / T::BN;
-    b_col = tid % T::BN;
-    a_row_step = static_cast<int64_t>(A_ROWS_STEP) * K;
-    b_row_step = static_cast<int64_t>(B_ROWS_STEP) * N;
-    a_src = A + static_cast<int64_t>(m0 + a_row) * K + a_col;
-    b_src = B + static_cast<int64_t>(b_row) * N + n0 + b_col;
-    a_rows_ok = 0;
-    static_assert(A_ITERS <= 32, "");
+  __device__ AStage(const GemmArgs& a, int m0, int tid) : base(a.A), K(a.K) {
+    row = tid / T::BK;
+    col = tid % T::BK;
+    row_step = static_cast<int64_t>(ROWS_STEP) * a.lda;
+    src = a.A + static_cast<int64_t>(m0 + row) * a.lda + col;
+    rows_ok = 0;
 #pragma unroll
-    for (int t = 0; t < A_ITERS; ++t)
-      if (m0 + a_row + t * A_ROWS_STEP < M) a_rows_ok |= 1u << t;
-    b_col_ok = n0 + b_col < N;
+    for (int t = 0; t < ITERS; ++t)
+      if (m0 + row + t * ROWS_STEP < a.M) rows_ok |= 1u << t;
   }
-
-  template <class LA, class LB>
-  __device__ __forceinline__ void load(float* As, float* Bs, const LA& la, const LB& lb,
-                                       int stage, int kt) const {
+  template <class L>
+  __device__ __forceinline__ void load(float* As, const L& la, int stage, int kt) const {
     const int k0 = kt * T::BK;
-    const bool a_k_ok = k0 + a_col < K;
+    const bool k_ok = k0 + col < K;
 #pragma unroll
-    for (int t = 0; t < A_ITERS; ++t) {
-      const bool ok = a_k_ok && (a_rows_ok >> t & 1u);
-      const float* src = ok ? a_src + t * a_row_step + k0 : A;
-      cp_async_4(smem_u32(As + la.offset(stage, a_row + t * A_ROWS_STEP, a_col)), src,
-                 ok ? 4u : 0u);
+    for (int t = 0; t < ITERS; ++t) {
+      const bool ok = k_ok && (rows_ok >> t & 1u);
+      cp_async_4(smem_u32(As + la.offset(stage, row + t * ROWS_STEP, col)),
+                 ok ? src + t * row_step + k0 : base, ok ? 4u : 0u);
     }
+  }
+};
+
+template <class T>
+struct AStage<T, STAGE_TRANS> {
+  // Lane l copies row 8*rb + l%8, column 4*cb + l/8 of block b = warp +
+  // t*NW (rb = b % RB, cb = b / RB) from At[(k0 + column) * lda + m0 + row].
+  static constexpr int RB = T::BM / 8, CB = T::BK / 4;
+  static constexpr int NW = T::THREADS / 32;
+  static constexpr int ITERS = RB * CB / NW;
+  static_assert(ITERS * NW == RB * CB, "");
+  const float* At;
+  int64_t lda;
+  int M, K, m0, lr, lc, warp;
+
+  __device__ AStage(const GemmArgs& a, int m0_, int tid)
+      : At(a.A), lda(a.lda), M(a.M), K(a.K), m0(m0_) {
+    lr = tid & 7;
+    lc = (tid & 31) >> 3;
+    warp = tid >> 5;
+  }
+  template <class L>
+  __device__ __forceinline__ void load(float* As, const L& la, int stage, int kt) const {
+    const int k0 = kt * T::BK;
 #pragma unroll
-    for (int t = 0; t < B_ITERS; ++t) {
-      const int kr = k0 + b_row + t * B_ROWS_STEP;
-      const bool ok = b_col_ok && kr < K;
-      const float* src = ok ? b_src + static_cast<int64_t>(k0) * N + t * b_row_step : B;
-      cp_async_4(smem_u32(Bs + lb.offset(stage, b_row + t * B_ROWS_STEP, b_col)), src,
-                 ok ? 4u : 0u);
+    for (int t = 0; t < ITERS; ++t) {
+      const int b = warp + t * NW;
+      const int r = (b % RB) * 8 + lr, c = (b / RB) * 4 + lc;
+      const bool ok = m0 + r < M && k0 + c < K;
+      cp_async_4(smem_u32(As + la.offset(stage, r, c)),
+                 ok ? At + static_cast<int64_t>(k0 + c) * lda + m0 + r : At, ok ? 4u : 0u);
+    }
+  }
+};
+
+template <class T>
+struct BStage<T, STAGE_VEC> {
+  static constexpr int CHUNKS_ROW = T::BN / 4;
+  static_assert(T::THREADS % CHUNKS_ROW == 0, "");
+  static constexpr int ROWS_STEP = T::THREADS / CHUNKS_ROW;
+  static constexpr int ITERS = T::BK / ROWS_STEP;
+  static_assert(ITERS * ROWS_STEP == T::BK, "");
+  const float* base;
+  const float* src;   // B[row * ldb + n0 + col]
+  int64_t ldb, row_step;
+  int row, col, K;
+  bool col_ok;
+
+  __device__ BStage(const GemmArgs& a, int n0, int tid) : base(a.B), ldb(a.ldb), K(a.K) {
+    row = tid / CHUNKS_ROW;
+    col = (tid % CHUNKS_ROW) * 4;
+    row_step = static_cast<int64_t>(ROWS_STEP) * a.ldb;
+    src = a.B + static_cast<int64_t>(row) * a.ldb + n0 + col;
+    col_ok = n0 + col < a.N;
+  }
+  template <class L>
+  __device__ __forceinline__ void load(float* Bs, const L& lb, int stage, int kt) const {
+    const int k0 = kt * T::BK;
+#pragma unroll
+    for (int t = 0; t < ITERS; ++t) {
+      const bool ok = col_ok && k0 + row + t * ROWS_STEP < K;
+      cp_async_16(smem_u32(Bs + lb.offset(stage, row + t * ROWS_STEP, col)),
+                  ok ? src + static_cast<int64_t>(k0) * ldb + t * row_step : base, ok ? 16u : 0u);
+    }
+  }
+};
+
+template <class T>
+struct BStage<T, STAGE_SCALAR> {
+  static_assert(T::THREADS % T::BN == 0, "");
+  static constexpr int ROWS_STEP = T::THREADS / T::BN;
+  static constexpr int ITERS = T::BK / ROWS_STEP;
+  const float* base;
+  const float* src;
+  int64_t ldb, row_step;
+  int row, col, K;
+  bool col_ok;
+
+  __device__ BStage(const GemmArgs& a, int n0, int tid) : base(a.B), ldb(a.ldb), K(a.K) {
+    row = tid / T::BN;
+    col = tid % T::BN;
+    row_step = static_cast<int64_t>(ROWS_STEP) * a.ldb;
+    src = a.B + static_cast<int64_t>(row) * a.ldb + n0 + col;
+    col_ok = n0 + col < a.N;
+  }
+  template <class L>
+  __device__ __forceinline__ void load(float* Bs, const L& lb, int stage, int kt) const {
+    const int k0 = kt * T::BK;
+#pragma unroll
+    for (int t = 0; t < ITERS; ++t) {
+      const bool ok = col_ok && k0 + row + t * ROWS_STEP < K;
+      cp_async_4(smem_u32(Bs + lb.offset(stage, row + t * ROWS_STEP, col)),
+                 ok ? src + static_cast<int64_t>(k0) * ldb + t * row_step : base, ok ? 4u : 0u);
+    }
+  }
+};
+
+template <class T>
+struct BStage<T, STAGE_TRANS> {
+  // Lane l copies k row 8*kb + l%8, column 4*nb + l/8 of block b = warp +
+  // t*NW (kb = b % KB, nb = b / KB) from Bt[(n0 + column) * ldb + k0 + row].
+  static constexpr int KB = T::BK / 8, NB = T::BN / 4;
+  static constexpr int NW = T::THREADS / 32;
+  static constexpr int ITERS = KB * NB / NW;
+  static_assert(ITERS * NW == KB * NB, "");
+  const float* Bt;
+  int64_t ldb;
+  int N, K, n0, lk, ln, warp;
+
+  __device__ BStage(const GemmArgs& a, int n0_, int tid)
+      : Bt(a.B), ldb(a.ldb), N(a.N), K(a.K), n0(n0_) {
+    lk = tid & 7;
+    ln = (tid & 31) >> 3;
+    warp = tid >> 5;
+  }
+  template <class L>
+  __device__ __forceinline__ void load(float* Bs, const L& lb, int stage, int kt) const {
+    const int k0 = kt * T::BK;
+#pragma unroll
+    for (int t = 0; t < ITERS; ++t) {
+      const int b = warp + t * NW;
+      const int kk = (b % KB) * 8 + lk, n = (b / KB) * 4 + ln;
+      const bool ok = n0 + n < N && k0 + kk < K;
+      cp_async_4(smem_u32(Bs + lb.offset(stage, kk, n)),
+                 ok ? Bt + static_cast<int64_t>(n0 + n) * ldb + k0 + kk : Bt, ok ? 4u : 0u);
     }
   }
 };
@@ -206,11 +297,15 @@ __device__ __forceinline__ float pick(const float4& v, int c) {
 }
 
 // ---------------------------------------------------------------------------
-template <class T, bool VEC, bool PAD, bool PACKED>
+// AMODE, BMODE: StageMode of each operand.  C is written with float4 stores
+// when A is staged in 16-byte chunks (the host picks that mode only when C is
+// 16-byte aligned with ldc % 4 == 0 too), else with scalar stores.
+template <class T, int AMODE, int BMODE, bool PAD, bool PACKED>
 __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     sgemm_ffma_kernel(GemmArgs args) {
+  constexpr bool VEC = AMODE == STAGE_VEC;
   constexpr SmemLayout LA = T::a_layout(PAD);
-  constexpr SmemLayout LB = T::b_layout(PAD);
+  constexpr SmemLayout LB = T::b_layout(PAD, BMODE == STAGE_TRANS);
   extern __shared__ float4 smem_f4[];
   float* As = reinterpret_cast<float*>(smem_f4);
   float* Bs = As + LA.size();
@@ -235,13 +330,17 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
   grouped_tile(tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
   const int m0 = tm * T::BM, n0 = tn * T::BN;
 
-  const Stager<T, VEC> stager(args.A, args.B, M, N, K, m0, n0, tid);
+  const AStage<T, AMODE> stage_a(args, m0, tid);
+  const BStage<T, BMODE> stage_b(args, n0, tid);
 
   // Prologue: STAGES-1 tiles in flight.  One commit group per tile (empty
   // groups keep the count uniform when K has fewer tiles).
 #pragma unroll
   for (int s = 0; s < T::STAGES - 1; ++s) {
-    if (s < ktiles) stager.load(As, Bs, LA, LB, s, kt_begin + s);
+    if (s < ktiles) {
+      stage_a.load(As, LA, s, kt_begin + s);
+      stage_b.load(Bs, LB, s, kt_begin + s);
+    }
     cp_async_commit();
   }
 
@@ -267,8 +366,10 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     // iteration kt-1) is no longer being read.
     cp_async_wait<T::STAGES - 2>();
     __syncthreads();
-    if (kt + T::STAGES - 1 < ktiles)
-      stager.load(As, Bs, LA, LB, load_stage, kt_begin + kt + T::STAGES - 1);
+    if (kt + T::STAGES - 1 < ktiles) {
+      stage_a.load(As, LA, load_stage, kt_begin + kt + T::STAGES - 1);
+      stage_b.load(Bs, LB, load_stage, kt_begin + kt + T::STAGES - 1);
+    }
     cp_async_commit();
 
     const float* a_ptr = As + stage * LA.stage_size() + a_off;
@@ -329,32 +430,44 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     return;
   }
 
-  // Masked epilogue: C[row, col] for row < M, col < N.
+  // Masked epilogue: C[row, col] = alpha * acc + beta * C[row, col] for
+  // row < M, col < N (C is not read when beta == 0; alpha == 1 and
+  // beta == 0 store acc unchanged).
   float* C = args.C;
+  const float alpha = args.alpha, beta = args.beta;
 #pragma unroll
   for (int i = 0; i < T::TM; ++i) {
     const int row = m0 + wm * T::WM + i * T::LM + lm;
     if (row >= M) continue;
-    float* c_row = C + static_cast<int64_t>(row) * N;
+    float* c_row = C + static_cast<int64_t>(row) * args.ldc;
 #pragma unroll
     for (int g = 0; g < T::TN / 4; ++g) {
       const int col = n0 + wn * T::WN + g * T::LN * 4 + ln * 4;
-      const float4 v = make_float4(acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
-                                   acc[i][2 * g + 1].y);
+      float4 v = make_float4(alpha * acc[i][2 * g].x, alpha * acc[i][2 * g].y,
+                             alpha * acc[i][2 * g + 1].x, alpha * acc[i][2 * g + 1].y);
       if constexpr (VEC) {
         // N % 4 == 0, so a float4 group is either wholly inside or outside.
-        if (col < N) *reinterpret_cast<float4*>(c_row + col) = v;
+        if (col < N) {
+          float4* cp = reinterpret_cast<float4*>(c_row + col);
+          if (beta != 0.0f) {
+            const float4 o = *cp;
+            v = make_float4(fmaf(beta, o.x, v.x), fmaf(beta, o.y, v.y), fmaf(beta, o.z, v.z),
+                            fmaf(beta, o.w, v.w));
+          }
+          *cp = v;
+        }
       } else {
-        if (col + 0 < N) c_row[col + 0] = v.x;
-        if (col + 1 < N) c_row[col + 1] = v.y;
-        if (col + 2 < N) c_row[col + 2] = v.z;
-        if (col + 3 < N) c_row[col + 3] = v.w;
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (col + e < N)
+            c_row[col + e] = beta != 0.0f ? fmaf(beta, c_row[col + e], vv[e]) : vv[e];
       }
     }
   }
 }
 
-template <class T, bool PACKED, bool WITH_UNPADDED>
+template <class T, bool PACKED, bool WITH_UNPADDED, bool WITH_TRANS = false>
 FfmaEntry make_entry() {
   FfmaEntry e{};
   e.bm = T::BM;
@@ -372,11 +485,25 @@ FfmaEntry make_entry() {
   e.pad_b = T::b_layout(true).row_padding;
   e.smem_bytes[0] = T::smem_bytes(false);
   e.smem_bytes[1] = T::smem_bytes(true);
-  e.kern[1][1] = reinterpret_cast<const void*>(&sgemm_ffma_kernel<T, true, true, PACKED>);
-  e.kern[0][1] = reinterpret_cast<const void*>(&sgemm_ffma_kernel<T, false, true, PACKED>);
+  e.kern[1][1] = reinterpret_cast<const void*>(
+      &sgemm_ffma_kernel<T, STAGE_VEC, STAGE_VEC, true, PACKED>);
+  e.kern[0][1] = reinterpret_cast<const void*>(
+      &sgemm_ffma_kernel<T, STAGE_SCALAR, STAGE_SCALAR, true, PACKED>);
   if (WITH_UNPADDED) {
-    e.kern[1][0] = reinterpret_cast<const void*>(&sgemm_ffma_kernel<T, true, false, PACKED>);
-    e.kern[0][0] = reinterpret_cast<const void*>(&sgemm_ffma_kernel<T, false, false, PACKED>);
+    e.kern[1][0] = reinterpret_cast<const void*>(
+        &sgemm_ffma_kernel<T, STAGE_VEC, STAGE_VEC, false, PACKED>);
+    e.kern[0][0] = reinterpret_cast<const void*>(
+        &sgemm_ffma_kernel<T, STAGE_SCALAR, STAGE_SCALAR, false, PACKED>);
+  }
+  e.pad_b_t = T::b_layout(true, true).row_padding;
+  e.smem_bytes_t = T::smem_bytes(true, true);
+  if (WITH_TRANS) {
+    e.kern_t[1][0] = reinterpret_cast<const void*>(
+        &sgemm_ffma_kernel<T, STAGE_TRANS, STAGE_SCALAR, true, PACKED>);
+    e.kern_t[0][1] = reinterpret_cast<const void*>(
+        &sgemm_ffma_kernel<T, STAGE_SCALAR, STAGE_TRANS, true, PACKED>);
+    e.kern_t[1][1] = reinterpret_cast<const void*>(
+        &sgemm_ffma_kernel<T, STAGE_TRANS, STAGE_TRANS, true, PACKED>);
   }
   return e;
 }

@@ -18,6 +18,8 @@
 // gets the rule's padding (16 columns, 4 rows -> one word, stride 17); B is
 // read as a broadcast and is not padded (section "Why shared-memory banks
 // matter").  pad=false keeps stride 16 to measure the conflict it removes.
+// Leading dimensions, transposed storage and alpha/beta only change how the
+// copies index A and B and how the result is written.
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -55,9 +57,11 @@ __global__ void __launch_bounds__(P18_THREADS) sgemm_p18_kernel(GemmArgs args) {
     for (int index = tid; index < P18_BM * P18_BK; index += P18_THREADS) {
       const int row = index / P18_BK, column = index % P18_BK;
       const int global_row = block_m + row, global_column = k_base + column;
+      // op(A)[global_row][global_column], stored row-major or transposed.
       dot_lhs[LA.offset(dot_stage, row, column)] =
           global_row < M && global_column < K
-              ? args.A[static_cast<int64_t>(global_row) * K + global_column]
+              ? args.A[args.trans_a ? static_cast<int64_t>(global_column) * args.lda + global_row
+                                    : static_cast<int64_t>(global_row) * args.lda + global_column]
               : 0.0f;
     }
     for (int index = tid; index < P18_BK * P18_BN; index += P18_THREADS) {
@@ -65,7 +69,8 @@ __global__ void __launch_bounds__(P18_THREADS) sgemm_p18_kernel(GemmArgs args) {
       const int global_row = k_base + row, global_column = block_n + column;
       dot_rhs[LB.offset(dot_stage, row, column)] =
           global_row < K && global_column < N
-              ? args.B[static_cast<int64_t>(global_row) * N + global_column]
+              ? args.B[args.trans_b ? static_cast<int64_t>(global_column) * args.ldb + global_row
+                                    : static_cast<int64_t>(global_row) * args.ldb + global_column]
               : 0.0f;
     }
     __syncthreads();
@@ -81,8 +86,11 @@ __global__ void __launch_bounds__(P18_THREADS) sgemm_p18_kernel(GemmArgs args) {
                          rhs[LB.offset(dot_stage, dot_k, tile_j)], accumulator);
   }
   const int out_row = block_m + tile_i, out_col = block_n + tile_j;
-  if (out_row < M && out_col < N)
-    args.C[static_cast<int64_t>(out_row) * N + out_col] = accumulator;
+  if (out_row < M && out_col < N) {
+    float* c = args.C + static_cast<int64_t>(out_row) * args.ldc + out_col;
+    const float v = args.alpha * accumulator;
+    *c = args.beta != 0.0f ? fmaf(args.beta, *c, v) : v;
+  }
 }
 
 cudaError_t launch_p18(const GemmArgs& a, bool pad, cudaStream_t stream) {

@@ -119,58 +119,69 @@ __device__ __forceinline__ void split4(float4 x, float4& big, float4& small) {
 }
 
 
-// grid (Kt, Mt), 256 threads: pair (tm, kt) holds A[tm*128 + r][kt*BK + k].
-template <class G>
-__global__ void __launch_bounds__(256) pack_a_kernel(const float* __restrict__ A,
-                                                     float* __restrict__ Ap, int M, int K,
-                                                     int Kt, int vec) {
+// Both operands are packed as blocks of ROWS rows (128 for A, BN for B) x BK
+// k, one block pair (big, small) per (row tile, K tile), block pairs of a
+// row tile consecutive in K.  Two readers cover the four ways an operand
+// can be stored:
+//   pack_kc: element (r, k) at src[r*ld + k] (k contiguous): A as stored
+//            row-major, or B stored transposed (N x K);
+//   pack_rc: element (r, k) at src[k*ld + r] (rows contiguous): B as stored
+//            row-major, or A stored transposed (K x M).
+
+// grid (Kt, Rt), 256 threads: each thread moves 16-byte chunks (4 k of a row).
+template <class G, int ROWS>
+__global__ void __launch_bounds__(256) pack_kc_kernel(const float* __restrict__ src, int64_t ld,
+                                                      float* __restrict__ dst_base, int R, int K,
+                                                      int Kt, int vec) {
   constexpr int BK = G::BK;
-  const int kt = blockIdx.x, tm = blockIdx.y;
-  char* dst = reinterpret_cast<char*>(Ap) +
-              (static_cast<int64_t>(tm) * Kt + kt) * static_cast<int64_t>(G::A_PAIR_BYTES);
-  for (int c = threadIdx.x; c < BM * (BK / 4); c += 256) {
+  constexpr int BLOCK = ROWS * G::ROW_BYTES;
+  const int kt = blockIdx.x, rt = blockIdx.y;
+  char* dst = reinterpret_cast<char*>(dst_base) +
+              (static_cast<int64_t>(rt) * Kt + kt) * static_cast<int64_t>(2 * BLOCK);
+  for (int c = threadIdx.x; c < ROWS * (BK / 4); c += 256) {
     const int r = c / (BK / 4), ch = c % (BK / 4);
-    const int m = tm * BM + r, k = kt * BK + ch * 4;
+    const int row = rt * ROWS + r, k = kt * BK + ch * 4;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (m < M) {
-      const float* src = A + static_cast<int64_t>(m) * K + k;
+    if (row < R) {
+      const float* p = src + static_cast<int64_t>(row) * ld + k;
       if (vec) {
-        if (k < K) v = *reinterpret_cast<const float4*>(src);
+        if (k < K) v = *reinterpret_cast<const float4*>(p);
       } else {
-        if (k + 0 < K) v.x = src[0];
-        if (k + 1 < K) v.y = src[1];
-        if (k + 2 < K) v.z = src[2];
-        if (k + 3 < K) v.w = src[3];
+        if (k + 0 < K) v.x = p[0];
+        if (k + 1 < K) v.y = p[1];
+        if (k + 2 < K) v.z = p[2];
+        if (k + 3 < K) v.w = p[3];
       }
     }
     float4 big, small;
     split4(v, big, small);
     const uint32_t off = G::offset(r, ch * 4);
     *reinterpret_cast<float4*>(dst + off) = big;
-    *reinterpret_cast<float4*>(dst + G::A_BLOCK_BYTES + off) = small;
+    *reinterpret_cast<float4*>(dst + BLOCK + off) = small;
   }
 }
 
-// grid (Kt, ceil(Nt*BN/256)), 256 threads: thread t owns column
-// n = blockIdx.y*256 + t of B, i.e. row n % BN of pair (n / BN, kt).  It
-// reads its column of the K tile (coalesced across the warp) and writes its
-// row of BK values.
-template <class G>
-__global__ void __launch_bounds__(256) pack_b_kernel(const float* __restrict__ B,
-                                                     float* __restrict__ Bp, int K, int N,
-                                                     int Kt, int Nt) {
+// grid (Kt, ceil(Rt*ROWS/256)), 256 threads: thread t owns row
+// n = blockIdx.y*256 + t, i.e. row n % ROWS of block pair (n / ROWS, kt).
+// It reads its row's BK values down the K tile (coalesced across the warp)
+// and writes them.
+template <class G, int ROWS>
+__global__ void __launch_bounds__(256) pack_rc_kernel(const float* __restrict__ src, int64_t ld,
+                                                      float* __restrict__ dst_base, int R, int K,
+                                                      int Kt, int Rt) {
   constexpr int BK = G::BK;
+  constexpr int BLOCK = ROWS * G::ROW_BYTES;
   const int kt = blockIdx.x;
   const int n = blockIdx.y * 256 + threadIdx.x;
-  const int tn = n / G::BN, r = n % G::BN;
-  if (tn >= Nt) return;
-  char* dst = reinterpret_cast<char*>(Bp) +
-              (static_cast<int64_t>(tn) * Kt + kt) * static_cast<int64_t>(G::B_PAIR_BYTES);
+  const int rt = n / ROWS, r = n % ROWS;
+  if (rt >= Rt) return;
+  char* dst = reinterpret_cast<char*>(dst_base) +
+              (static_cast<int64_t>(rt) * Kt + kt) * static_cast<int64_t>(2 * BLOCK);
   float v[BK];
 #pragma unroll
   for (int j = 0; j < BK; ++j) {
     const int k = kt * BK + j;
-    v[j] = (n < N && k < K) ? B[static_cast<int64_t>(k) * N + n] : 0.f;
+    v[j] = (n < R && k < K) ? src[static_cast<int64_t>(k) * ld + n] : 0.f;
   }
 #pragma unroll
   for (int ch = 0; ch < BK / 4; ++ch) {
@@ -178,7 +189,7 @@ __global__ void __launch_bounds__(256) pack_b_kernel(const float* __restrict__ B
     split4(make_float4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]), big, small);
     const uint32_t off = G::offset(r, ch * 4);
     *reinterpret_cast<float4*>(dst + off) = big;
-    *reinterpret_cast<float4*>(dst + G::B_BLOCK_BYTES + off) = small;
+    *reinterpret_cast<float4*>(dst + BLOCK + off) = small;
   }
 }
 
@@ -335,8 +346,9 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
 template <class G>
 __global__ void __launch_bounds__(THREADS, 1)
     tf32x3_gemm_kernel(const float* __restrict__ Ap, const float* __restrict__ Bp,
-                       float* __restrict__ C, int M, int N, int Kt, int tiles_m, int tiles_n,
-                       int group_m, int vec_c, int fault_inject) {
+                       float* __restrict__ C, int64_t ldc, float alpha, float beta, int M,
+                       int N, int Kt, int tiles_m, int tiles_n, int group_m, int vec_c,
+                       int fault_inject) {
   constexpr int BK = G::BK, BN = G::BN;
   constexpr int STAGES = G::STAGES;
   constexpr int STAGE_BYTES = G::STAGE_BYTES;
@@ -467,23 +479,34 @@ __global__ void __launch_bounds__(THREADS, 1)
       grouped_tile(tile, tiles_m, tiles_n, group_m, tm, tn);
       const int row = tm * BM + q * 32 + lane;
       const uint32_t t_row = tmem + lane_base + static_cast<uint32_t>(b * BN);
-      float* c_row = C + static_cast<int64_t>(row) * N;
+      float* c_row = C + static_cast<int64_t>(row) * ldc;
 #pragma unroll 1
       for (int ch = 0; ch < BN / 32; ++ch) {
         float v[32];
         tmem_ld32(t_row + ch * 32, v);
         const int col0 = tn * BN + ch * 32;
         if (row < M) {
+          // C = alpha * acc + beta * C (C not read when beta == 0).
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= alpha;
           if (vec_c) {
 #pragma unroll
             for (int g4 = 0; g4 < 8; ++g4)
-              if (col0 + 4 * g4 < N)
-                *reinterpret_cast<float4*>(c_row + col0 + 4 * g4) =
-                    make_float4(v[4 * g4], v[4 * g4 + 1], v[4 * g4 + 2], v[4 * g4 + 3]);
+              if (col0 + 4 * g4 < N) {
+                float4* cp = reinterpret_cast<float4*>(c_row + col0 + 4 * g4);
+                float4 o = make_float4(v[4 * g4], v[4 * g4 + 1], v[4 * g4 + 2], v[4 * g4 + 3]);
+                if (beta != 0.0f) {
+                  const float4 c0 = *cp;
+                  o = make_float4(fmaf(beta, c0.x, o.x), fmaf(beta, c0.y, o.y),
+                                  fmaf(beta, c0.z, o.z), fmaf(beta, c0.w, o.w));
+                }
+                *cp = o;
+              }
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (col0 + i < N) c_row[col0 + i] = v[i];
+              if (col0 + i < N)
+                c_row[col0 + i] = beta != 0.0f ? fmaf(beta, c_row[col0 + i], v[i]) : v[i];
           }
         }
       }
@@ -526,21 +549,38 @@ struct Cfg {
     return cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<G>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
   }
-  static cudaError_t launch(const GemmArgs& a, void* workspace, bool vec_ab, bool vec_c,
-                            int max_ctas, int fault_inject, cudaStream_t stream) {
+  // vec_a / vec_b: the operand is read k-contiguous (A as stored, B stored
+  // transposed) with a leading dimension % 4 == 0 from a 16-byte aligned
+  // base, so its packer may read float4.
+  static cudaError_t launch(const GemmArgs& a, void* workspace, bool vec_a, bool vec_b,
+                            bool vec_c, int max_ctas, int fault_inject, cudaStream_t stream) {
     using namespace tf32x3;
     const int mt = (a.M + BM - 1) / BM, nt = (a.N + BN - 1) / BN, kt = (a.K + BK - 1) / BK;
-    if (mt > 65535 || (nt * BN + 255) / 256 > 65535) return cudaErrorInvalidValue;
+    if (mt > 65535 || nt > 65535 || (mt * BM + 255) / 256 > 65535 ||
+        (nt * BN + 255) / 256 > 65535)
+      return cudaErrorInvalidValue;
     float* Ap = static_cast<float*>(workspace);
     float* Bp = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                          static_cast<int64_t>(mt) * kt * G::A_PAIR_BYTES);
-    pack_a_kernel<G><<<dim3(kt, mt), 256, 0, stream>>>(a.A, Ap, a.M, a.K, kt, vec_ab ? 1 : 0);
-    pack_b_kernel<G><<<dim3(kt, (nt * BN + 255) / 256), 256, 0, stream>>>(a.B, Bp, a.K, a.N, kt,
-                                                                          nt);
+    // A: rows m, k contiguous unless stored transposed.
+    if (a.trans_a)
+      pack_rc_kernel<G, BM><<<dim3(kt, (mt * BM + 255) / 256), 256, 0, stream>>>(
+          a.A, a.lda, Ap, a.M, a.K, kt, mt);
+    else
+      pack_kc_kernel<G, BM><<<dim3(kt, mt), 256, 0, stream>>>(a.A, a.lda, Ap, a.M, a.K, kt,
+                                                              vec_a ? 1 : 0);
+    // B: rows n, n contiguous (row-major K x N) unless stored transposed.
+    if (a.trans_b)
+      pack_kc_kernel<G, BN><<<dim3(kt, nt), 256, 0, stream>>>(a.B, a.ldb, Bp, a.N, a.K, kt,
+                                                              vec_b ? 1 : 0);
+    else
+      pack_rc_kernel<G, BN><<<dim3(kt, (nt * BN + 255) / 256), 256, 0, stream>>>(
+          a.B, a.ldb, Bp, a.N, a.K, kt, nt);
     const int tiles = mt * nt;
     const int grid = tiles < max_ctas ? tiles : max_ctas;
     tf32x3_gemm_kernel<G><<<grid, THREADS, G::SMEM_BYTES, stream>>>(
-        Ap, Bp, a.C, a.M, a.N, kt, mt, nt, a.group_m, vec_c ? 1 : 0, fault_inject);
+        Ap, Bp, a.C, a.ldc, a.alpha, a.beta, a.M, a.N, kt, mt, nt, a.group_m, vec_c ? 1 : 0,
+        fault_inject);
     return cudaGetLastError();
   }
 };
@@ -592,11 +632,12 @@ cudaError_t tf32x3_prepare(int device, int bk, int bn) {
   return e;
 }
 
-cudaError_t launch_tf32x3(const GemmArgs& a, void* workspace, bool vec_ab, bool vec_c, int bk,
-                          int bn, int max_ctas, int fault_inject, cudaStream_t stream) {
+cudaError_t launch_tf32x3(const GemmArgs& a, void* workspace, bool vec_a, bool vec_b,
+                          bool vec_c, int bk, int bn, int max_ctas, int fault_inject,
+                          cudaStream_t stream) {
   cudaError_t e = cudaErrorInvalidValue;
   dispatch(bk, bn, [&](auto c) {
-    e = decltype(c)::launch(a, workspace, vec_ab, vec_c, max_ctas, fault_inject, stream);
+    e = decltype(c)::launch(a, workspace, vec_a, vec_b, vec_c, max_ctas, fault_inject, stream);
   });
   return e;
 }
