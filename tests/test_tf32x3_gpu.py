@@ -61,9 +61,14 @@ def test_plan_reports_tile_and_workspace(cfg):
     assert p["stages"] >= 2
     # Packed big and small copies of A (128-row blocks) and B (bn-row
     # blocks), bk k each.
-    assert p["workspace_bytes"] == 4096 * 4096 * 4 * 4
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert p["grid"] == min(32 * (4096 // bn), sms)  # persistent: one CTA per SM at most
+    tiles = 32 * (4096 // bn)
+    ctas = min(tiles, sms)
+    rem = tiles % ctas
+    partial = rem * p["split_k"] * 128 * bn * 4 if p["split_k"] > 1 else 0
+    assert p["workspace_bytes"] == 4096 * 4096 * 4 * 4 + partial
+    units = tiles + (p["split_k"] - 1) * rem if p["split_k"] > 1 else tiles
+    assert p["grid"] == min(units, sms)  # persistent: one CTA per SM at most
     auto = mt.plan(4096, 4096, 4096, variant="tf32x3")
     assert (auto["bn"], auto["bk"]) == (256, 16)  # the automatic choice for large squares
 
@@ -76,11 +81,12 @@ def test_workloads_full_oracle(name, cfg):
     assert_within(run(A, B, **cfg).numpy(), Cref, W, TOL, name)
 
 
+@pytest.mark.parametrize("split", [0, 1], ids=["auto-split-tail", "no-split"])
 @pytest.mark.parametrize("name", ["square_4096", "square_8192", "skinny_65536x128x4096"])
-def test_full_size_sampled_rows(name):
+def test_full_size_sampled_rows(name, split):
     w = gemm_inputs.WORKLOADS[name]
     A, B = gemm_inputs.make_workload(w)
-    c = mt.sgemm(A.cuda(), B.cuda(), **TF32)
+    c = mt.sgemm(A.cuda(), B.cuda(), split_k=split, **TF32)
     torch.cuda.synchronize()
     g = np.random.default_rng(1)
     rows = np.unique(np.concatenate([[0, w.M - 1, 127, 128, 255, 256],
@@ -171,3 +177,24 @@ def test_timeout_path_reports_and_context_survives():
     Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
     assert_within(run(A, B, **TF32).numpy(), Cref, W, TOL, "after timeout")
     assert mt.mt_device_status(0) == mt.MT_OK
+
+
+def test_split_tail_plan_and_parity():
+    # 512 tiles of 128 x 256 on one CTA per SM leave a partial last round;
+    # its tiles are cut into K slices whose partials a second kernel adds.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = mt.plan(4096, 4096, 4096, variant="tf32x3")
+    rem = 512 % sms
+    if 0 < 2 * rem <= sms:
+        assert p["split_k"] == min(sms // rem, 4)
+    # 32 x 5 = 160 tiles: 152 in the first round, 8 split into 4 K slices.
+    M, N, K = 4096, 1280, 520
+    q = mt.plan(M, N, K, variant="tf32x3")
+    if sms == 152:
+        assert (q["bn"], q["split_k"]) == (256, 4)
+    A, B = gemm_inputs.make_ab(M, N, K, seed=24, dist="normal")
+    rows = np.array([0, 1, 127, 128, 2047, 3968, 4095])
+    Cr, Wr = oracle.sgemm_rows(A.numpy(), B.numpy(), rows, with_w=True)
+    got = run(A, B, **TF32).numpy()[rows]
+    assert_within(got, Cr, Wr, TOL, "split tail")
+    assert np.array_equal(run(A, B, **TF32).numpy()[rows], got)  # deterministic

@@ -242,6 +242,7 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
     return MT_ERR_INVALID_ARG;
   if (cfg && (cfg->wm || cfg->wn) && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
   if (cfg && cfg->fault_inject && variant != MT_VARIANT_TF32X3) return MT_ERR_UNSUPPORTED;
+  // 3xTF32 splits only its tail by itself (split_k = 1 turns that off).
   if (cfg && cfg->split_k > 1 && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
   const bool pad = !(cfg && cfg->no_pad);
   const bool trans = P.trans_a || P.trans_b;
@@ -300,9 +301,33 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
     // Persistent: one CTA per SM at most.
     const int64_t tiles = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
     L->max_ctas = sms > 0 ? sms : 1;
-    p.grid = tiles < L->max_ctas ? tiles : L->max_ctas;
+    // Split tail: when the tiles leave a last round on at most half of the
+    // CTAs, those tiles are cut into K slices that run on the idle ones and
+    // are added by a second kernel (split_k = 1 turns this off).
+    const int64_t ctas = std::min<int64_t>(tiles, L->max_ctas);
+    const int64_t ktiles = ceil_div(K, bk);
+    int64_t full = tiles, split = 1;
+    if (!(cfg && cfg->split_k == 1) && tiles > ctas) {
+      const int64_t rem = tiles % ctas;
+      if (rem > 0 && 2 * rem <= ctas) {
+        split = std::min<int64_t>(ctas / rem, 4);
+        // Every slice non-empty and at least 2 K tiles long.
+        while (split > 1 && ((split - 1) * ceil_div(ktiles, split) >= ktiles ||
+                             ktiles / split < 2))
+          --split;
+        if (split > 1) full = tiles - rem;
+        else split = 1;
+      }
+    }
+    L->full_tiles = static_cast<int>(full);
+    L->split = static_cast<int>(split);
+    L->kt_per_slice = static_cast<int>(ceil_div(ktiles, split));
+    p.split_k = L->split;
+    const int64_t units = full + (tiles - full) * split;
+    p.grid = std::min<int64_t>(units, L->max_ctas);
     p.workspace_bytes = mt::tf32x3_workspace_bytes(static_cast<int>(M), static_cast<int>(N),
-                                                   static_cast<int>(K), bk, bn);
+                                                   static_cast<int>(K), bk, bn) +
+                        (tiles - full) * split * bm * bn * 4;
     if (p.smem_bytes > smem_limit) return MT_ERR_SMEM_BUDGET;
     return MT_OK;
   }

@@ -343,12 +343,47 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
 }
 
 // ---------------------------------------------------------------------------
+// Work units of the persistent loop: below full_tiles a unit is a whole tile
+// (its index in the grouped raster); the tiles after those are split into
+// `split` K slices, one unit per slice, whose fp32 partial tiles (dense
+// 128 x BN, tail tile major, slice minor) are added by a second kernel.
+struct Sched {
+  int full_tiles;
+  int split;
+  int kt_per_slice;
+  float* partial;
+};
+
+struct Unit {
+  int tm, tn;    // tile coordinates
+  int kt0, kt1;  // K tiles [kt0, kt1)
+  int pidx;      // partial tile index, -1 for a whole tile
+};
+
+__device__ __forceinline__ Unit unit_of(int u, const Sched& sc, int tiles_m, int tiles_n,
+                                        int group_m, int Kt) {
+  Unit w;
+  int tile = u;
+  w.kt0 = 0;
+  w.kt1 = Kt;
+  w.pidx = -1;
+  if (u >= sc.full_tiles) {
+    const int v = u - sc.full_tiles;
+    tile = sc.full_tiles + v / sc.split;
+    w.kt0 = min(Kt, (v % sc.split) * sc.kt_per_slice);
+    w.kt1 = min(Kt, w.kt0 + sc.kt_per_slice);
+    w.pidx = v;
+  }
+  grouped_tile(tile, tiles_m, tiles_n, group_m, w.tm, w.tn);
+  return w;
+}
+
 template <class G>
 __global__ void __launch_bounds__(THREADS, 1)
     tf32x3_gemm_kernel(const float* __restrict__ Ap, const float* __restrict__ Bp,
                        float* __restrict__ C, int64_t ldc, float alpha, float beta, int M,
                        int N, int Kt, int tiles_m, int tiles_n, int group_m, int vec_c,
-                       int fault_inject) {
+                       Sched sched, int fault_inject) {
   constexpr int BK = G::BK, BN = G::BN;
   constexpr int STAGES = G::STAGES;
   constexpr int STAGE_BYTES = G::STAGE_BYTES;
@@ -366,6 +401,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int num_tiles = tiles_m * tiles_n;
+  const int num_units = sched.full_tiles + (num_tiles - sched.full_tiles) * sched.split;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -393,14 +429,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       // on its data runs out (the test of the timeout path).
       uint32_t& g = issued;
       bool stop = fault_inject != 0;
-      for (int tile = blockIdx.x; tile < num_tiles && !stop; tile += gridDim.x) {
-        int tm, tn;
-        grouped_tile(tile, tiles_m, tiles_n, group_m, tm, tn);
+      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
+        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
         const char* a_src = reinterpret_cast<const char*>(Ap) +
-                            static_cast<int64_t>(tm) * Kt * G::A_PAIR_BYTES;
+                            static_cast<int64_t>(w.tm) * Kt * G::A_PAIR_BYTES;
         const char* b_src = reinterpret_cast<const char*>(Bp) +
-                            static_cast<int64_t>(tn) * Kt * G::B_PAIR_BYTES;
-        for (int kt = 0; kt < Kt; ++kt, ++g) {
+                            static_cast<int64_t>(w.tn) * Kt * G::B_PAIR_BYTES;
+        for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
           const uint32_t s = g % STAGES, round = g / STAGES;
           if (g >= STAGES && !wait_phase(bar(EMPTY + s), (round + 1) & 1u, abort_flag)) {
             stop = true;
@@ -423,14 +458,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t g = 0;
       bool stop = false;
       int it = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && !stop; tile += gridDim.x, ++it) {
+      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x, ++it) {
+        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
         const int b = it & 1;
-        // The epilogue must have drained this accumulator (used by tile it-2).
+        // The epilogue must have drained this accumulator (used by unit it-2).
         if (it >= 2 && !wait_phase(bar(ACC_EMPTY + b), ((it >> 1) + 1) & 1u, abort_flag)) break;
         tc_fence_after();
         const uint32_t acc_tmem = tmem + static_cast<uint32_t>(b * BN);
         uint32_t acc = 0;
-        for (int kt = 0; kt < Kt; ++kt, ++g) {
+        for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
           const uint32_t s = g % STAGES, round = g / STAGES;
           if (!wait_phase(bar(FULL + s), round & 1u, abort_flag)) {
             stop = true;
@@ -466,7 +502,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int it = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++it) {
       const int b = it & 1;
       // A tile's accumulator is ready after its whole K loop.  The warp
       // goes on only if every lane saw it (tcgen05.ld needs the whole warp).
@@ -475,17 +511,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after();
       __syncwarp();
-      int tm, tn;
-      grouped_tile(tile, tiles_m, tiles_n, group_m, tm, tn);
-      const int row = tm * BM + q * 32 + lane;
+      const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      const int row = w.tm * BM + q * 32 + lane;
       const uint32_t t_row = tmem + lane_base + static_cast<uint32_t>(b * BN);
       float* c_row = C + static_cast<int64_t>(row) * ldc;
 #pragma unroll 1
       for (int ch = 0; ch < BN / 32; ++ch) {
         float v[32];
         tmem_ld32(t_row + ch * 32, v);
-        const int col0 = tn * BN + ch * 32;
-        if (row < M) {
+        const int col0 = w.tn * BN + ch * 32;
+        if (w.pidx >= 0) {
+          // A K slice: the raw partial tile, dense 128 x BN.
+          float* prow = sched.partial + static_cast<int64_t>(w.pidx) * (BM * BN) +
+                        (q * 32 + lane) * BN + ch * 32;
+#pragma unroll
+          for (int g4 = 0; g4 < 8; ++g4)
+            *reinterpret_cast<float4*>(prow + 4 * g4) =
+                make_float4(v[4 * g4], v[4 * g4 + 1], v[4 * g4 + 2], v[4 * g4 + 3]);
+        } else if (row < M) {
           // C = alpha * acc + beta * C (C not read when beta == 0).
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] *= alpha;
@@ -539,6 +582,7 @@ namespace {
 template <int BK, int BN>
 struct Cfg {
   using G = tf32x3::Geometry<BK, BN>;
+  static int64_t workspace_bytes_packed(int M, int N, int K) { return workspace(M, N, K); }
   static int64_t workspace(int M, int N, int K) {
     const int64_t mt = (M + tf32x3::BM - 1) / tf32x3::BM;
     const int64_t nt = (N + BN - 1) / BN;
@@ -577,11 +621,21 @@ struct Cfg {
       pack_rc_kernel<G, BN><<<dim3(kt, (nt * BN + 255) / 256), 256, 0, stream>>>(
           a.B, a.ldb, Bp, a.N, a.K, kt, nt);
     const int tiles = mt * nt;
-    const int grid = tiles < max_ctas ? tiles : max_ctas;
+    // Split tail: the partial tiles follow the packed operands.
+    Sched sched{a.full_tiles, a.split, a.kt_per_slice, nullptr};
+    if (a.split > 1)
+      sched.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                workspace_bytes_packed(a.M, a.N, a.K));
+    const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
+    const int grid = units < max_ctas ? units : max_ctas;
     tf32x3_gemm_kernel<G><<<grid, THREADS, G::SMEM_BYTES, stream>>>(
         Ap, Bp, a.C, a.ldc, a.alpha, a.beta, a.M, a.N, kt, mt, nt, a.group_m, vec_c ? 1 : 0,
-        fault_inject);
-    return cudaGetLastError();
+        sched, fault_inject);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || a.split <= 1) return e;
+    GemmArgs r = a;
+    r.partial = sched.partial;
+    return launch_splitk_reduce(r, BM, BN, vec_c, stream);
   }
 };
 
