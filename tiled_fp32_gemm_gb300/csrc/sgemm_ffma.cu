@@ -1,27 +1,35 @@
 // Registry of the FFMA tile configurations built into the library.  The
 // kernels themselves are in sgemm_ffma.cuh; each ffma_tiles_*.cu instantiates
 // a few configurations (separate translation units build in parallel).
+#include <algorithm>
+
 #include "device_util.cuh"
 #include "kernels.h"
 
 namespace mt {
 
-// One CTA per split tile: C[tile] = sum over slices s = 0, 1, ... of the
-// slice partials, added in that order.
+// C[tile] = alpha * (sum over slices s = 0, 1, ... of the slice partials,
+// added in that order) + beta * C[tile], masked to M x N.  Each split tile
+// is cut into `pieces` CTAs of up to 1024 float4 (4 per thread), so a
+// small tail still spreads over the GPU.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(GemmArgs a, int bm, int bn,
-                                                           int vec_c) {
+                                                           int pieces, int vec_c) {
+  const int t = blockIdx.x / pieces, piece = blockIdx.x % pieces;
   int tm, tn;
-  grouped_tile(a.full_tiles + blockIdx.x, a.tiles_m, a.tiles_n, a.group_m, tm, tn);
-  const int block = bm * bn;
-  const float4* P = reinterpret_cast<const float4*>(
-      a.partial + static_cast<int64_t>(blockIdx.x) * a.split * block);
-  for (int e4 = threadIdx.x; e4 < block / 4; e4 += blockDim.x) {
+  grouped_tile(a.full_tiles + t, a.tiles_m, a.tiles_n, a.group_m, tm, tn);
+  const int block4 = bm * bn / 4;
+  const int per_piece = (block4 + pieces - 1) / pieces;
+  const int e_begin = piece * per_piece;
+  const int e_end = min(block4, e_begin + per_piece);
+  const float4* P = reinterpret_cast<const float4*>(a.partial) +
+                    static_cast<int64_t>(t) * a.split * block4;
+  for (int e4 = e_begin + threadIdx.x; e4 < e_end; e4 += blockDim.x) {
     const int r = (e4 * 4) / bn, c = (e4 * 4) % bn;
     const int row = tm * bm + r, col = tn * bn + c;
     if (row >= a.M || col >= a.N) continue;
     float4 s = P[e4];
     for (int sl = 1; sl < a.split; ++sl) {
-      const float4 v = P[static_cast<int64_t>(sl) * (block / 4) + e4];
+      const float4 v = P[static_cast<int64_t>(sl) * block4 + e4];
       s.x += v.x;
       s.y += v.y;
       s.z += v.z;
@@ -46,6 +54,15 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(GemmArgs a, int bm, 
   }
 }
 
+cudaError_t launch_splitk_reduce(const GemmArgs& a, int bm, int bn, bool vec_c,
+                                 cudaStream_t stream) {
+  const int tail = a.tiles_m * a.tiles_n - a.full_tiles;
+  if (tail <= 0) return cudaSuccess;
+  const int pieces = std::max(1, bm * bn / 4096);
+  splitk_reduce_kernel<<<tail * pieces, 256, 0, stream>>>(a, bm, bn, pieces, vec_c ? 1 : 0);
+  return cudaGetLastError();
+}
+
 // C = beta * C on an M x N view (zeros when beta is 0, C not read).
 __global__ void __launch_bounds__(256) scale_c_kernel(float* C, int M, int N, int64_t ldc,
                                                      float beta) {
@@ -65,14 +82,6 @@ cudaError_t launch_scale_c(float* C, int M, int N, int64_t ldc, float beta,
   const int64_t blocks = (total + 255) / 256;
   scale_c_kernel<<<static_cast<unsigned>(blocks < 65536 ? blocks : 65536), 256, 0, stream>>>(
       C, M, N, ldc, beta);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_splitk_reduce(const GemmArgs& a, int bm, int bn, bool vec_c,
-                                 cudaStream_t stream) {
-  const int tail = a.tiles_m * a.tiles_n - a.full_tiles;
-  if (tail <= 0) return cudaSuccess;
-  splitk_reduce_kernel<<<tail, 256, 0, stream>>>(a, bm, bn, vec_c ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -161,33 +161,42 @@ __global__ void __launch_bounds__(256) pack_kc_kernel(const float* __restrict__ 
   }
 }
 
-// grid (Kt, ceil(Rt*ROWS/256)), 256 threads: thread t owns row
-// n = blockIdx.y*256 + t, i.e. row n % ROWS of block pair (n / ROWS, kt).
-// It reads its row's BK values down the K tile (coalesced across the warp)
-// and writes them.
+// grid (Kt, ceil(Rt*ROWS/256)), 256 threads: the CTA packs rows
+// n0 = blockIdx.y*256 .. n0+255 (ROWS divides 256, so they cover whole
+// blocks).  It reads the 256 x BK tile with coalesced row-of-k loads into
+// shared memory, then writes the blocks' 16-byte chunks in address order,
+// so a warp stores 512 contiguous bytes.
 template <class G, int ROWS>
 __global__ void __launch_bounds__(256) pack_rc_kernel(const float* __restrict__ src, int64_t ld,
                                                       float* __restrict__ dst_base, int R, int K,
                                                       int Kt, int Rt) {
+  static_assert(256 % ROWS == 0, "a CTA covers whole blocks");
   constexpr int BK = G::BK;
   constexpr int BLOCK = ROWS * G::ROW_BYTES;
+  constexpr int CPR = G::ROW_BYTES / 16;  // 16-byte chunks per packed row
+  constexpr int TS = 256 + 1;             // tile row stride (words): k rows, banks spread
+  __shared__ float tile[BK * TS];
   const int kt = blockIdx.x;
-  const int n = blockIdx.y * 256 + threadIdx.x;
-  const int rt = n / ROWS, r = n % ROWS;
-  if (rt >= Rt) return;
-  char* dst = reinterpret_cast<char*>(dst_base) +
-              (static_cast<int64_t>(rt) * Kt + kt) * static_cast<int64_t>(2 * BLOCK);
-  float v[BK];
-#pragma unroll
+  const int n0 = blockIdx.y * 256;
+#pragma unroll 4
   for (int j = 0; j < BK; ++j) {
-    const int k = kt * BK + j;
-    v[j] = (n < R && k < K) ? src[static_cast<int64_t>(k) * ld + n] : 0.f;
+    const int k = kt * BK + j, n = n0 + threadIdx.x;
+    tile[j * TS + threadIdx.x] = (n < R && k < K) ? src[static_cast<int64_t>(k) * ld + n] : 0.f;
   }
-#pragma unroll
-  for (int ch = 0; ch < BK / 4; ++ch) {
+  __syncthreads();
+  for (int p = threadIdx.x; p < 256 * CPR; p += 256) {
+    const int rr = p / CPR, pc = p % CPR;  // row within the CTA, physical chunk
+    const int rt = (n0 + rr) / ROWS, r = (n0 + rr) % ROWS;
+    if (rt >= Rt) break;
+    const int r8 = r & 7;
+    const int lc = (pc ^ (BK == 32 ? r8 : (r8 >> 1))) & (CPR - 1);  // logical chunk
+    float4 v = make_float4(tile[(lc * 4 + 0) * TS + rr], tile[(lc * 4 + 1) * TS + rr],
+                           tile[(lc * 4 + 2) * TS + rr], tile[(lc * 4 + 3) * TS + rr]);
     float4 big, small;
-    split4(make_float4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]), big, small);
-    const uint32_t off = G::offset(r, ch * 4);
+    split4(v, big, small);
+    char* dst = reinterpret_cast<char*>(dst_base) +
+                (static_cast<int64_t>(rt) * Kt + kt) * static_cast<int64_t>(2 * BLOCK);
+    const uint32_t off = (r >> 3) * G::ATOM_BYTES + r8 * G::ROW_BYTES + pc * 16;
     *reinterpret_cast<float4*>(dst + off) = big;
     *reinterpret_cast<float4*>(dst + BLOCK + off) = small;
   }
