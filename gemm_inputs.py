@@ -9,6 +9,10 @@ Recipe: a CPU ``torch.Generator`` seeded with the workload's seed draws A
 [-1, 1)), "normal" is ``randn`` (mean 0, variance 1), "int" draws integers
 in [-8, 8] (exact test inputs).  A workload that names two shapes reseeds the
 generator for each shape.
+
+16-bit inputs (``make_ab16``): the same float32 draws, rounded to the
+nearest float16 or bfloat16 by torch's CPU conversion.  The 16-bit values
+are the inputs; both sides read the same patterns.
 """
 from __future__ import annotations
 
@@ -67,3 +71,12 @@ def make_workload(w: Workload | str):
     if isinstance(w, str):
         w = WORKLOADS[w]
     return make_ab(w.M, w.N, w.K, w.seed, w.dist)
+
+
+def make_ab16(M: int, N: int, K: int, seed: int, dist: str = "uniform",
+              dtype: str = "bf16"):
+    """(A, B) as contiguous CPU tensors of torch.bfloat16 ("bf16") or
+    torch.float16 ("f16"): the float32 draws of make_ab, rounded."""
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16}[dtype]
+    A, B = make_ab(M, N, K, seed, dist)
+    return A.to(tdt).contiguous(), B.to(tdt).contiguous()

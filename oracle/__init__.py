@@ -9,6 +9,8 @@ library shares no code with it.
   fp32), from ``ref_gemm.c``; see that file's header for the passages it
   follows.  ``sgemm_general``: alpha*op(A)*op(B) + beta*C with leading
   dimensions and transposes, the same sum with one rounding.
+* ``gemm_mixed_general``: the same general form on 16-bit inputs (fp16 or
+  bf16 patterns, decoded from the formats' definitions), fp32 result.
 * ``smem_rules``: the pages' padding rule, bank mapping, staged layout,
   stage selection and budget formula, plus a bank-conflict simulator.
 
@@ -69,6 +71,14 @@ def load(path: str | None = None):
                                              ctypes.c_double, ctypes.c_double, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_int]
         lib.oracle_sgemm_general.restype = ctypes.c_int
+        lib.oracle_gemm_mixed_general.argtypes = [ctypes.c_int, p, i64, p, i64, p, i64, p, i64,
+                                                  i64, i64, ctypes.c_double, ctypes.c_double,
+                                                  ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.oracle_gemm_mixed_general.restype = ctypes.c_int
+        lib.oracle_f16_value.argtypes = [ctypes.c_uint16]
+        lib.oracle_f16_value.restype = ctypes.c_double
+        lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_value.restype = ctypes.c_double
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         if path is None:
@@ -160,4 +170,52 @@ def sgemm_general(A, B, C0, M, N, K, lda, ldb, ldc, alpha=1.0, beta=0.0,
                                               int(trans_b), threads)
     if rc:
         raise RuntimeError("oracle_sgemm_general failed")
+    return (C, W) if with_w else C
+
+
+F16, BF16 = 1, 2  # dtype codes of oracle_gemm_mixed_general
+
+
+def _u16(x) -> np.ndarray:
+    """16-bit patterns as a flat uint16 array (accepts uint16/int16 numpy
+    arrays or float16/bfloat16 torch tensors)."""
+    if hasattr(x, "view") and hasattr(x, "dtype") and str(x.dtype).startswith("torch."):
+        import torch
+        x = x.detach().contiguous().view(torch.int16).numpy()
+    x = np.asarray(x)
+    if x.dtype == np.float16:
+        x = x.view(np.uint16)
+    if x.dtype.kind in "iu" and x.dtype.itemsize > 2:
+        if x.size and (x.min() < 0 or x.max() > 0xFFFF):
+            raise ValueError("16-bit patterns lie in [0, 65535]")
+        x = x.astype(np.uint16)
+    if x.dtype not in (np.uint16, np.int16):
+        raise TypeError("16-bit inputs must be 16-bit patterns")
+    return np.ascontiguousarray(x.reshape(-1)).view(np.uint16)
+
+
+def value16(dtype: int, patterns) -> np.ndarray:
+    """The float64 value of each 16-bit pattern (oracle_f16_value /
+    oracle_bf16_value, one call per element)."""
+    lib = load()
+    fn = lib.oracle_f16_value if dtype == F16 else lib.oracle_bf16_value
+    pats = _u16(patterns)
+    return np.array([fn(int(h)) for h in pats], dtype=np.float64)
+
+
+def gemm_mixed_general(dtype, A, B, C0, M, N, K, lda, ldb, ldc, alpha=1.0, beta=0.0,
+                       trans_a=False, trans_b=False, with_w=False, threads: int = 0,
+                       lib=None):
+    """alpha*op(A)*op(B) + beta*C on flat 16-bit A and B (dtype F16 or BF16)
+    and a flat float32 C; returns the new C buffer (and W, M x N, if asked).
+    C0 is copied, never modified."""
+    A, B = _u16(A), _u16(B)
+    C = np.array(np.asarray(C0, np.float32).reshape(-1), copy=True)
+    W = np.empty((M, N), np.float64) if with_w else None
+    rc = (lib or load()).oracle_gemm_mixed_general(int(dtype), _ptr(A), lda, _ptr(B), ldb,
+                                                   _ptr(C), ldc, _ptr(W) if with_w else None,
+                                                   M, N, K, float(alpha), float(beta),
+                                                   int(trans_a), int(trans_b), threads)
+    if rc:
+        raise RuntimeError("oracle_gemm_mixed_general failed")
     return (C, W) if with_w else C

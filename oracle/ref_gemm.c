@@ -189,6 +189,93 @@ int oracle_sgemm_general(const float *A, int64_t lda, const float *B, int64_t ld
     return failed ? -1 : 0;
 }
 
+/* ------------------------------------------------------------------------
+ * 16-bit inputs, fp32 products and sums ("My Triton From Scratch, Part 18",
+ * section "Next" announces Part 19, mixed-precision types; the plainest
+ * reading, and the one tl.dot takes for 16-bit operands, is inputs stored in
+ * 16 bits and accumulation in fp32).  The result is the same definition as
+ * above on the values the 16-bit patterns encode:
+ *
+ *     C[i][j] = fp32( alpha * sum_k a(i,k) * b(k,j)  +  beta * C[i][j] )
+ *
+ * summed in increasing k in double and rounded once.  A product of two
+ * 16-bit values is exact in double (at most 22 significant bits).
+ *
+ * The patterns are decoded from the formats' definitions:
+ *   binary16 (IEEE 754): sign bit 15, exponent bits 14..10 (bias 15),
+ *     fraction bits 9..0; exponent 0 is zero or subnormal (f * 2^-24),
+ *     exponent 31 is infinity (f == 0) or NaN.
+ *   bfloat16: the upper half of a binary32 — sign bit 15, exponent bits
+ *     14..7 (bias 127), fraction bits 6..0; exponent 0 is zero or subnormal
+ *     (f * 2^-133), exponent 255 is infinity or NaN.
+ */
+enum { ORACLE_F16 = 1, ORACLE_BF16 = 2 };
+
+double oracle_f16_value(uint16_t h)
+{
+    const int s = (h >> 15) & 1, e = (h >> 10) & 0x1F, f = h & 0x3FF;
+    double v;
+    if (e == 0) v = ldexp((double)f, -24);
+    else if (e == 31) v = f ? NAN : INFINITY;
+    else v = ldexp((double)(1024 + f), e - 25);
+    return s ? -v : v;
+}
+
+double oracle_bf16_value(uint16_t h)
+{
+    const int s = (h >> 15) & 1, e = (h >> 7) & 0xFF, f = h & 0x7F;
+    double v;
+    if (e == 0) v = ldexp((double)f, -133);
+    else if (e == 255) v = f ? NAN : INFINITY;
+    else v = ldexp((double)(128 + f), e - 134);
+    return s ? -v : v;
+}
+
+/* The general form on 16-bit A and B (both of type `dtype`, ORACLE_F16 or
+ * ORACLE_BF16), fp32 C; layouts, W and the alpha/beta rules as in
+ * oracle_sgemm_general.  Returns 0, or -1 on a bad argument. */
+int oracle_gemm_mixed_general(int dtype, const uint16_t *A, int64_t lda, const uint16_t *B,
+                              int64_t ldb, float *C, int64_t ldc, double *W, int64_t M,
+                              int64_t N, int64_t K, double alpha, double beta, int trans_a,
+                              int trans_b, int nthreads)
+{
+    if (dtype != ORACLE_F16 && dtype != ORACLE_BF16) return -1;
+    if (M < 0 || N < 0 || K < 0 || ldc < N) return -1;
+    if (!trans_a && lda < K) return -1;
+    if (trans_a && lda < M) return -1;
+    if (!trans_b && ldb < N) return -1;
+    if (trans_b && ldb < K) return -1;
+    if (M == 0 || N == 0) return 0;
+    double (*value)(uint16_t) = dtype == ORACLE_F16 ? oracle_f16_value : oracle_bf16_value;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double acc = 0.0, w = 0.0;
+            if (alpha != 0.0) {
+                for (int64_t k = 0; k < K; ++k) {
+                    const double a = value(trans_a ? A[k * lda + i] : A[i * lda + k]);
+                    const double b = value(trans_b ? B[j * ldb + k] : B[k * ldb + j]);
+                    acc += a * b;
+                    w += fabs(a) * fabs(b);
+                }
+            }
+            double c = alpha * acc;
+            double wc = fabs(alpha) * w;
+            if (beta != 0.0) {
+                const double c0 = (double)C[i * ldc + j];
+                c += beta * c0;
+                wc += fabs(beta) * fabs(c0);
+            }
+            C[i * ldc + j] = (float)c;
+            if (W) W[i * N + j] = wc;
+        }
+    }
+    return 0;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP

@@ -35,20 +35,39 @@ MUTANTS = {
                       "wacc[j] += aa * (double)b_row[j];"),
     "elements_transposed_b": ("const double b = (double)B[k * N + j];",
                               "const double b = (double)B[j * K + k];"),
-    "general_beta_dropped": ("c += beta * c0;", "c += 0.0 * c0;"),
-    "general_alpha_sign": ("double c = alpha * acc;", "double c = -alpha * acc;"),
+    # (old, new, occurrence): the fp32 and the 16-bit general forms share
+    # these lines; the third field picks which copy is mutated.
+    "general_beta_dropped": ("c += beta * c0;", "c += 0.0 * c0;", 0),
+    "general_alpha_sign": ("double c = alpha * acc;", "double c = -alpha * acc;", 0),
+    "mixed_beta_dropped": ("c += beta * c0;", "c += 0.0 * c0;", 1),
+    "mixed_alpha_sign": ("double c = alpha * acc;", "double c = -alpha * acc;", 1),
     "general_trans_b_swapped": ("(trans_b ? B[j * ldb + k] : B[k * ldb + j])",
-                                "(trans_b ? B[k * ldb + j] : B[j * ldb + k])"),
+                                "(trans_b ? B[k * ldb + j] : B[j * ldb + k])", 0),
+    "f16_exponent_bias": ("ldexp((double)(1024 + f), e - 25)",
+                          "ldexp((double)(1024 + f), e - 24)"),
+    "f16_subnormal_as_normal": ("if (e == 0) v = ldexp((double)f, -24);",
+                                "if (e == 0) v = ldexp((double)(1024 + f), -25);"),
+    "bf16_exponent_bias": ("ldexp((double)(128 + f), e - 134)",
+                           "ldexp((double)(128 + f), e - 133)"),
+    "mixed_trans_a_ignored": ("value(trans_a ? A[k * lda + i] : A[i * lda + k])",
+                              "value(A[i * lda + k])"),
     "general_lda_ignored": ("(trans_a ? A[k * lda + i] : A[i * lda + k])",
-                            "(trans_a ? A[k * lda + i] : A[i * K + k])"),
+                            "(trans_a ? A[k * lda + i] : A[i * K + k])", 0),
 }
 
 
 def _mutate(name, tmp_path):
-    old, new = MUTANTS[name]
+    old, new, *which = MUTANTS[name]
     text = open(SRC).read()
-    assert text.count(old) == 1, f"mutation site for {name} not unique"
-    text = text.replace(old, new)
+    if which:
+        assert text.count(old) > which[0], f"mutation site for {name} missing"
+        at = -1
+        for _ in range(which[0] + 1):
+            at = text.index(old, at + 1)
+        text = text[:at] + new + text[at + len(old):]
+    else:
+        assert text.count(old) == 1, f"mutation site for {name} not unique"
+        text = text.replace(old, new)
     if "M_" in new:  # the transposed index needs M inside oracle_row
         text = text.replace("static void oracle_row(const float *A, const float *B, int64_t N, int64_t K,",
                             "static int64_t M_ = 1;\nstatic void oracle_row(const float *A, const float *B, int64_t N, int64_t K,")

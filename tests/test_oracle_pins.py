@@ -318,3 +318,99 @@ def test_general_alpha_beta_exact_on_integers():
     C = general(np.full(M * K, np.nan, np.float32), np.full(K * N, np.nan, np.float32),
                 Ci.astype(np.float32), M, N, K, K, N, N, alpha=0.0, beta=0.5)
     assert np.array_equal(C.reshape(M, N), (0.5 * Ci).astype(np.float32))
+
+
+# --- 16-bit inputs (fp16 / bf16 patterns, fp32 result) ------------------------
+ALL16 = np.arange(1 << 16, dtype=np.uint16)
+
+
+def same_or_both_nan(x, y):
+    x, y = np.asarray(x, np.float64), np.asarray(y, np.float64)
+    return np.array_equal(np.isnan(x), np.isnan(y)) and \
+        np.array_equal(x[~np.isnan(x)], y[~np.isnan(y)])
+
+
+def test_f16_decode_every_pattern_matches_numpy():
+    # numpy's float16 is an independent implementation of IEEE binary16.
+    assert same_or_both_nan(oracle.value16(oracle.F16, ALL16),
+                            ALL16.view(np.float16).astype(np.float64))
+
+
+def test_bf16_decode_every_pattern_matches_torch():
+    torch = pytest.importorskip("torch")
+    ref = torch.from_numpy(ALL16.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64)
+    assert same_or_both_nan(oracle.value16(oracle.BF16, ALL16), ref.numpy())
+
+
+@pytest.mark.parametrize("dtype,pattern,value", [
+    # binary16: one, smallest normal 2^-14, smallest subnormal 2^-24, largest
+    # finite (2 - 2^-10) * 2^15 = 65504, minus two.
+    (1, 0x3C00, Fraction(1)), (1, 0x0400, Fraction(1, 2 ** 14)),
+    (1, 0x0001, Fraction(1, 2 ** 24)), (1, 0x7BFF, Fraction(65504)), (1, 0xC000, Fraction(-2)),
+    # bfloat16: one, smallest normal 2^-126, smallest subnormal 2^-133,
+    # largest finite (2 - 2^-7) * 2^127, 0x4049 = 1.5703125 * 2.
+    (2, 0x3F80, Fraction(1)), (2, 0x0080, Fraction(1, 2 ** 126)),
+    (2, 0x0001, Fraction(1, 2 ** 133)), (2, 0x7F7F, (2 - Fraction(1, 2 ** 7)) * 2 ** 127),
+    (2, 0x4049, Fraction(201, 64)),
+])
+def test_16bit_closed_form_values(dtype, pattern, value):
+    assert Fraction(float(oracle.value16(dtype, [pattern])[0])) == value
+
+
+def _int16_operands(dtype, Ai, Bi):
+    """Integer matrices as 16-bit patterns (integers up to 8 are exact)."""
+    if dtype == oracle.F16:
+        return Ai.astype(np.float16).view(np.uint16), Bi.astype(np.float16).view(np.uint16)
+    torch = pytest.importorskip("torch")
+    cv = lambda x: torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+    return cv(Ai), cv(Bi)
+
+
+@pytest.mark.parametrize("dtype", [1, 2])
+@pytest.mark.parametrize("ta,tb", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_mixed_exact_on_integers_every_form(dtype, ta, tb):
+    g = rng(40 + 2 * ta + tb)
+    M, N, K = 11, 13, 19
+    Ai = g.integers(-8, 9, (M, K))
+    Bi = g.integers(-8, 9, (K, N))
+    Ci = g.integers(-50, 51, (M, N))
+    A16, B16 = _int16_operands(dtype, Ai, Bi)
+    # Stored with padded leading dimensions, transposed where asked.
+    As = A16.T if ta else A16
+    Bs = B16.T if tb else B16
+    lda, ldb, ldc = As.shape[1] + 3, Bs.shape[1] + 5, N + 2
+    Ab = np.zeros((As.shape[0], lda), np.uint16)
+    Ab[:, :As.shape[1]] = As
+    Bb = np.zeros((Bs.shape[0], ldb), np.uint16)
+    Bb[:, :Bs.shape[1]] = Bs
+    C0 = np.full((M, ldc), 7, np.float32)
+    C0[:, :N] = Ci
+    C, W = oracle.gemm_mixed_general(dtype, Ab, Bb, C0, M, N, K, lda, ldb, ldc, alpha=2.0,
+                                     beta=-3.0, trans_a=ta, trans_b=tb, with_w=True, lib=LIB)
+    C = C.reshape(M, ldc)
+    assert np.array_equal(C[:, :N].astype(np.int64), 2 * (Ai @ Bi) - 3 * Ci)
+    assert np.all(C[:, N:] == 7)
+    assert np.array_equal(W, 2 * (np.abs(Ai) @ np.abs(Bi)) + 3 * np.abs(Ci))
+
+
+@pytest.mark.parametrize("dtype", [1, 2])
+def test_mixed_reduces_to_fp32_oracle_on_widened_inputs(dtype):
+    # Widening a 16-bit value to fp32 is exact, so the fp32 oracle on the
+    # widened operands forms the same exact products in the same order.
+    torch = pytest.importorskip("torch")
+    M, N, K = 23, 17, 45
+    g = torch.Generator().manual_seed(50 + dtype)
+    tdt = torch.float16 if dtype == oracle.F16 else torch.bfloat16
+    A = (torch.randn((M, K), generator=g) * 3).to(tdt)
+    B = (torch.randn((K, N), generator=g) * 3).to(tdt)
+    C = oracle.gemm_mixed_general(dtype, A, B, np.zeros(M * N, np.float32), M, N, K, K, N, N,
+                                  lib=LIB)
+    ref = gemm(A.float().numpy(), B.float().numpy())
+    assert np.array_equal(C.reshape(M, N), ref)
+
+
+def test_mixed_rejects_unknown_dtype():
+    with pytest.raises(RuntimeError):
+        oracle.gemm_mixed_general(3, np.zeros(4, np.uint16), np.zeros(4, np.uint16),
+                                  np.zeros(4, np.float32), 2, 2, 2, 2, 2, 2, lib=LIB)
