@@ -62,8 +62,15 @@ typedef enum {
 typedef enum {
     MT_VARIANT_FFMA = 0,      /* CUDA-core FFMA register-tile kernel (default) */
     MT_VARIANT_TF32X3 = 1,    /* tcgen05 kind::tf32 with the 3xTF32 split */
-    MT_VARIANT_P18 = 2        /* one-warp kernel restating the pages' Version 18 */
+    MT_VARIANT_P18 = 2,       /* one-warp kernel restating the pages' Version 18 */
+    MT_VARIANT_TC16 = 3       /* tcgen05 kind::f16 on 16-bit inputs (mt_gemm_mixed* only) */
 } mt_variant;
+
+/* Storage type of A and B in the mt_gemm_mixed* entry points. */
+typedef enum {
+    MT_DTYPE_F16 = 1,         /* IEEE 754 binary16 */
+    MT_DTYPE_BF16 = 2         /* bfloat16: the upper 16 bits of a binary32 */
+} mt_dtype;
 
 /* Optional launch choices.  Zero-initialise for "automatic". */
 typedef struct {
@@ -76,10 +83,11 @@ typedef struct {
     int split_k;   /* K slices reduced in a second pass; 0 = automatic, 1 = none */
     int fma;       /* FFMA micro-kernel: 0 = automatic, 1 = scalar fma.rn.f32,
                       2 = packed fma.rn.f32x2 (same results, fewer issue slots) */
-    int fault_inject; /* test hook, 0 = off.  1 (MT_VARIANT_TF32X3 only): the
-                         copy thread issues nothing, so every wait on its data
-                         runs out; the call then leaves C unwritten and the
-                         next mt_device_status returns MT_ERR_TIMEOUT. */
+    int fault_inject; /* test hook, 0 = off.  1 (MT_VARIANT_TF32X3 and the
+                         mt_gemm_mixed* kernel only): the copy thread issues
+                         nothing, so every wait on its data runs out; the call
+                         then leaves C unwritten and the next mt_device_status
+                         returns MT_ERR_TIMEOUT. */
     int wm;        /* FFMA warp tile rows; 0 = automatic */
     int wn;        /* FFMA warp tile columns; 0 = automatic */
     int reserved[1];
@@ -191,6 +199,54 @@ MT_API mt_status mt_sgemm_host(const float *A, const float *B, float *C,
 MT_API mt_status mt_sgemm_tf32x3_noalloc(const float *A, const float *B, float *C,
                                          int64_t M, int64_t N, int64_t K,
                                          cudaStream_t stream);
+
+/*
+ * Mixed precision: A and B stored as 16-bit floating point (both fp16 or
+ * both bf16, `dtype`), C in fp32, products and sums in fp32:
+ *
+ *     C = alpha * op(A) * op(B) + beta * C
+ *
+ * with the layouts, leading dimensions (in elements), transposes and
+ * alpha/beta rules of mt_sgemm_general.  The pages announce mixed-precision
+ * types as their next part ("My Triton From Scratch, Part 18: Shared Memory
+ * Optimization", section "Next": Part 19, Mixed-Precision Types); this is
+ * their product with 16-bit storage and fp32 accumulation.  A product of two
+ * 16-bit values is exact in fp32; only the accumulation rounds.
+ *
+ * Runs on the tensor cores (tcgen05.mma kind::f16, MT_VARIANT_TC16) with
+ * the operands read by TMA straight from A and B.  TMA needs a 16-byte
+ * aligned base and a row pitch that is a multiple of 8 elements; an operand
+ * without them is first copied into a padded scratch matrix from the
+ * current device's stream-ordered pool (mt_gemm_mixed_plan reports the
+ * bytes as workspace_bytes, vec_ab = 1 when no copy is needed).
+ * A and B: 2-byte aligned device pointers.  cfg (NULL = automatic): variant
+ * 0 or MT_VARIANT_TC16; bn 0, 256 or 128; bm 0 or 128; bk 0 or 64; stages 0
+ * or the built count; split_k 0 (automatic tail split) or 1 (none);
+ * fault_inject as for MT_VARIANT_TF32X3; other fields 0, else
+ * MT_ERR_UNSUPPORTED.  dtype other than MT_DTYPE_F16 / MT_DTYPE_BF16:
+ * MT_ERR_INVALID_ARG.  MT_ERR_CUDA when the driver's tensor-map encoder
+ * cannot be found or scratch cannot be allocated.  Other errors as
+ * mt_sgemm_general.
+ */
+MT_API mt_status mt_gemm_mixed_general(int dtype, int trans_a, int trans_b, int64_t M,
+                                       int64_t N, int64_t K, float alpha, const void *A,
+                                       int64_t lda, const void *B, int64_t ldb, float beta,
+                                       float *C, int64_t ldc, cudaStream_t stream,
+                                       const mt_config *cfg);
+
+/* C = A*B with 16-bit A (M x K, row stride K) and B (K x N, row stride N),
+ * fp32 C (M x N): mt_gemm_mixed_general(dtype, 0, 0, M, N, K, 1, A, K, B, N,
+ * 0, C, N, stream, NULL). */
+MT_API mt_status mt_gemm_mixed(int dtype, const void *A, const void *B, float *C,
+                               int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/* The launch mt_gemm_mixed_general would make for these arguments, as
+ * mt_sgemm_plan (pointers inspected for alignment only, may be NULL). */
+MT_API mt_status mt_gemm_mixed_plan(int dtype, int trans_a, int trans_b, int64_t M,
+                                    int64_t N, int64_t K, const void *A, int64_t lda,
+                                    const void *B, int64_t ldb, const float *C, int64_t ldc,
+                                    const mt_config *cfg, int64_t smem_limit_bytes,
+                                    mt_plan *out);
 
 /*
  * Fills *out with the launch a call with these arguments would make,

@@ -253,3 +253,72 @@ def test_general_form_argument_checks():
     # ... but not when A is never read (alpha == 0).
     st = g(0, 0, 4, 4, 4, 0.0, a, 64, 1 << 30, 4, 0.0, c, 4, 0, None)
     assert st in (mt.MT_OK, mt.MT_ERR_NO_DEVICE)
+
+
+# --- 16-bit inputs (mt_gemm_mixed*) -------------------------------------------
+def plan16(M, N, K, dtype=mt.MT_DTYPE_BF16, ta=0, tb=0, lda=0, ldb=0, ldc=0, a=None, b=None,
+           c=None, **kw):
+    lda = lda or max(M if ta else K, 1)
+    ldb = ldb or max(K if tb else N, 1)
+    ldc = ldc or max(N, 1)
+    return mt.mt_gemm_mixed_plan(dtype, ta, tb, M, N, K, a, lda, b, ldb, c, ldc,
+                                 mt.make_config(**kw) if kw else None, GB300_SMEM)
+
+
+def test_mixed_plan_tiles_and_tail():
+    st, p = plan16(8192, 8192, 8192)
+    assert st == mt.MT_OK
+    assert (p.variant, p.bm, p.bn, p.bk) == (mt.MT_VARIANT_TC16, 128, 256, 64)
+    assert p.threads == 192 and p.grid == 152 and p.vec_ab == 1 and p.vec_c == 1
+    # 64 x 32 = 2048 tiles on 152 SMs leave 72 (at most half the CTAs):
+    # those 72 run as 2 K slices each.
+    assert p.split_k == 2 and p.workspace_bytes == 72 * 2 * 128 * 256 * 4
+    assert p.smem_bytes <= GB300_SMEM and p.stages * (128 + 256) * 64 * 2 <= p.smem_bytes
+    # 4096^3: 512 tiles leave 56 on 152 CTAs: those 56 split in 2 K slices.
+    st, p = plan16(4096, 4096, 4096)
+    assert p.split_k == 2 and p.workspace_bytes == 56 * 2 * 128 * 256 * 4
+    st, p = plan16(4096, 4096, 4096, split_k=1)
+    assert p.split_k == 1 and p.workspace_bytes == 0
+    # Explicit 128-wide tiles.
+    st, p = plan16(1024, 1024, 1024, bn=128)
+    assert st == mt.MT_OK and p.bn == 128 and p.stages >= 4
+
+
+def test_mixed_plan_repacks_what_tma_cannot_read():
+    # Row pitches that are not multiples of 8 elements (16 bytes): both
+    # operands get padded copies, sized rows x round_up(cols, 8) x 2 bytes.
+    st, p = plan16(4097, 3001, 2053)
+    assert st == mt.MT_OK and p.vec_ab == 0
+    rnd = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert p.workspace_bytes == rnd(4097 * 2056 * 2) + rnd(2053 * 3008 * 2)
+    # A 2-byte (not 16-byte) aligned base alone also needs the copy.
+    st, p = plan16(256, 256, 256, a=(1 << 20) + 2)
+    assert p.vec_ab == 0 and p.workspace_bytes == rnd(256 * 256 * 2)
+    st, p = plan16(256, 256, 256, a=1 << 20, b=1 << 24)
+    assert p.vec_ab == 1 and p.workspace_bytes == 0
+
+
+def test_mixed_argument_checks():
+    assert plan16(64, 64, 64, dtype=0)[0] == mt.MT_ERR_INVALID_ARG
+    assert plan16(64, 64, 64, dtype=3)[0] == mt.MT_ERR_INVALID_ARG
+    assert plan16(64, 64, 64, variant="tf32x3")[0] == mt.MT_ERR_UNSUPPORTED
+    assert plan16(64, 64, 64, bn=64)[0] == mt.MT_ERR_UNSUPPORTED
+    assert plan16(64, 64, 64, bk=32)[0] == mt.MT_ERR_UNSUPPORTED
+    assert plan16(64, 64, 64, split_k=2)[0] == mt.MT_ERR_UNSUPPORTED
+    assert plan16(64, 64, 64, wm=32)[0] == mt.MT_ERR_UNSUPPORTED
+    assert plan16(64, 64, 64, variant="tc16")[0] == mt.MT_OK
+    # MT_VARIANT_TC16 needs 16-bit inputs.
+    assert plan(64, 64, 64, variant="tc16")[0] == mt.MT_ERR_UNSUPPORTED
+    g = mt.mt_gemm_mixed_general
+    assert g(2, 0, 0, 8, 8, 8, 1.0, 1 << 20, 7, 1 << 30, 8, 0.0, 1 << 34, 8, 0, None) == \
+        mt.MT_ERR_INVALID_ARG                                   # lda < K
+    assert g(2, 0, 0, 8, 8, 8, 1.0, (1 << 20) + 1, 8, 1 << 30, 8, 0.0, 1 << 34, 8, 0,
+             None) == mt.MT_ERR_INVALID_ARG                     # A not 2-byte aligned
+    # Aliasing is judged on 2-byte elements: A spans 8 * 64 * 2 = 1024 bytes.
+    a = 1 << 20
+    assert g(2, 0, 0, 8, 8, 64, 1.0, a, 64, 1 << 30, 8, 0.0, a + 1020, 8, 0, None) == \
+        mt.MT_ERR_ALIAS
+    st = g(2, 0, 0, 8, 8, 64, 1.0, a, 64, 1 << 30, 8, 0.0, a + 1024, 8, 0, None)
+    assert st in (mt.MT_OK, mt.MT_ERR_NO_DEVICE)
+    assert mt.mt_gemm_mixed(5, 0, 0, 0, 4, 4, 4, 0) == mt.MT_ERR_INVALID_ARG
+    assert mt.mt_gemm_mixed(mt.MT_DTYPE_F16, 0, 0, 0, 0, 4, 4, 0) == mt.MT_OK  # M == 0

@@ -5,13 +5,15 @@ by ``tiled_fp32_gemm_gb300.build``).  This module only marshals arguments:
 
 * ``mt_sgemm``, ``mt_sgemm_ex``, ``mt_sgemm_general``, ``mt_sgemm_host``,
   ``mt_sgemm_tf32x3_noalloc``,
-  ``mt_sgemm_plan``,
+  ``mt_sgemm_plan``, ``mt_gemm_mixed``, ``mt_gemm_mixed_general``,
+  ``mt_gemm_mixed_plan``,
   ``mt_smem_row_padding``, ``mt_smem_vector_row_padding``,
   ``mt_smem_layout_make``, ``mt_smem_layout_offset``, ``mt_device_status``,
   ``mt_status_string``, ``mt_version`` — the C entry points under the same
   names, taking plain integers for pointers and streams;
 * ``sgemm(a, b, out=None, **choices)`` — the same call on torch CUDA tensors
-  (torch supplies device memory and the current stream; nothing else).
+  (torch supplies device memory and the current stream; nothing else);
+  ``gemm`` for the general form and ``gemm_mixed`` for 16-bit inputs.
 
 There is no CPU fallback: if the library is missing, every call raises.
 """
@@ -37,7 +39,12 @@ MT_NOALLOC_SCRATCH_BYTES = 32 << 20
 MT_VARIANT_FFMA = 0
 MT_VARIANT_TF32X3 = 1
 MT_VARIANT_P18 = 2
-VARIANTS = {"ffma": MT_VARIANT_FFMA, "tf32x3": MT_VARIANT_TF32X3, "p18": MT_VARIANT_P18}
+MT_VARIANT_TC16 = 3
+VARIANTS = {"ffma": MT_VARIANT_FFMA, "tf32x3": MT_VARIANT_TF32X3, "p18": MT_VARIANT_P18,
+            "tc16": MT_VARIANT_TC16}
+
+MT_DTYPE_F16 = 1
+MT_DTYPE_BF16 = 2
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libmtsgemm.so")
 
@@ -88,6 +95,12 @@ SIGNATURES = {
                               ctypes.c_float, _P, _I64, _P, ctypes.POINTER(mt_config)]),
     "mt_sgemm_plan": (_I, [_P, _P, _P, _I64, _I64, _I64, ctypes.POINTER(mt_config), _I64,
                            ctypes.POINTER(mt_plan)]),
+    "mt_gemm_mixed": (_I, [_I, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "mt_gemm_mixed_general": (_I, [_I, _I, _I, _I64, _I64, _I64, ctypes.c_float, _P, _I64,
+                                   _P, _I64, ctypes.c_float, _P, _I64, _P,
+                                   ctypes.POINTER(mt_config)]),
+    "mt_gemm_mixed_plan": (_I, [_I, _I, _I, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64,
+                                ctypes.POINTER(mt_config), _I64, ctypes.POINTER(mt_plan)]),
     "mt_smem_row_padding": (_I, [_I, _I]),
     "mt_smem_vector_row_padding": (_I, [_I, _I]),
     "mt_smem_layout_make": (_I, [_I, _I, _I, _I, ctypes.POINTER(mt_smem_layout)]),
@@ -170,6 +183,30 @@ def mt_sgemm_plan(A: int, B: int, C: int, M: int, N: int, K: int,
     st = lib().mt_sgemm_plan(A, B, C, M, N, K,
                              ctypes.byref(cfg) if cfg is not None else None,
                              smem_limit_bytes, ctypes.byref(out))
+    return st, out
+
+
+def mt_gemm_mixed(dtype: int, A: int, B: int, C: int, M: int, N: int, K: int,
+                  stream: int = 0) -> int:
+    return lib().mt_gemm_mixed(dtype, A, B, C, M, N, K, stream)
+
+
+def mt_gemm_mixed_general(dtype: int, trans_a: int, trans_b: int, M: int, N: int, K: int,
+                          alpha: float, A: int, lda: int, B: int, ldb: int, beta: float,
+                          C: int, ldc: int, stream: int = 0,
+                          cfg: mt_config | None = None) -> int:
+    return lib().mt_gemm_mixed_general(dtype, trans_a, trans_b, M, N, K, alpha, A, lda, B,
+                                       ldb, beta, C, ldc, stream,
+                                       ctypes.byref(cfg) if cfg is not None else None)
+
+
+def mt_gemm_mixed_plan(dtype: int, trans_a: int, trans_b: int, M: int, N: int, K: int,
+                       A: int | None, lda: int, B: int | None, ldb: int, C: int | None,
+                       ldc: int, cfg: mt_config | None = None, smem_limit_bytes: int = 0):
+    out = mt_plan()
+    st = lib().mt_gemm_mixed_plan(dtype, trans_a, trans_b, M, N, K, A, lda, B, ldb, C, ldc,
+                                  ctypes.byref(cfg) if cfg is not None else None,
+                                  smem_limit_bytes, ctypes.byref(out))
     return st, out
 
 
@@ -280,3 +317,69 @@ def gemm(a, b, c=None, alpha=1.0, beta=0.0, trans_a=False, trans_b=False, stream
     if st != MT_OK:
         raise MtError(st, "mt_sgemm_general")
     return c
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return MT_DTYPE_F16
+    if t.dtype == torch.bfloat16:
+        return MT_DTYPE_BF16
+    raise TypeError("16-bit inputs must be torch.float16 or torch.bfloat16")
+
+
+def gemm_mixed(a, b, c=None, alpha=1.0, beta=0.0, trans_a=False, trans_b=False, stream=None,
+               **choices):
+    """c (float32) = alpha * op(a) @ op(b) + beta * c with a and b 2-D CUDA
+    tensors of the same 16-bit dtype (float16 or bfloat16) whose rows may be
+    strided (unit column stride), through mt_gemm_mixed_general.  Returns c
+    (allocated when not given; then beta must be 0)."""
+    import torch
+    for t, name in ((a, "a"), (b, "b")):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError(f"{name} must be 2-D with unit column stride")
+    code = _dtype_code(a)
+    if b.dtype != a.dtype:
+        raise TypeError("a and b must have the same dtype")
+    M, K = (a.shape[1], a.shape[0]) if trans_a else (a.shape[0], a.shape[1])
+    Kb, N = (b.shape[1], b.shape[0]) if trans_b else (b.shape[0], b.shape[1])
+    if K != Kb:
+        raise ValueError("inner dimensions differ")
+    if c is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs c")
+        c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    if c.dtype != torch.float32 or c.dim() != 2 or c.stride(1) != 1 or tuple(c.shape) != (M, N):
+        raise ValueError("c must be float32, M x N, with unit column stride")
+
+    def ld(t):  # row stride; any value >= the row length works for one row
+        return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
+
+    s = stream if stream is not None else torch.cuda.current_stream(a.device).cuda_stream
+    with torch.cuda.device(a.device):
+        st = mt_gemm_mixed_general(code, int(trans_a), int(trans_b), M, N, K, alpha,
+                                   a.data_ptr(), ld(a), b.data_ptr(), ld(b), beta,
+                                   c.data_ptr(), ld(c), s,
+                                   make_config(**choices) if choices else None)
+    if st != MT_OK:
+        raise MtError(st, "mt_gemm_mixed_general")
+    return c
+
+
+def plan_mixed(dtype: int, M: int, N: int, K: int, trans_a=False, trans_b=False, lda=0,
+               ldb=0, ldc=0, a=None, b=None, c=None, smem_limit_bytes: int = 0,
+               **choices) -> dict:
+    """mt_gemm_mixed_plan as a dict (leading dimensions default to packed
+    rows; raises on a non-OK status)."""
+    ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
+    lda = lda or max(M if trans_a else K, 1)
+    ldb = ldb or max(K if trans_b else N, 1)
+    ldc = ldc or max(N, 1)
+    st, p = mt_gemm_mixed_plan(dtype, int(trans_a), int(trans_b), M, N, K, ptr(a), lda, ptr(b),
+                               ldb, ptr(c), ldc, make_config(**choices) if choices else None,
+                               smem_limit_bytes)
+    if st != MT_OK:
+        raise MtError(st, "mt_gemm_mixed_plan")
+    return p.as_dict()

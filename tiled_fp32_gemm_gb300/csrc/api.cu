@@ -67,23 +67,27 @@ bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// One product: C = alpha * op(A) * op(B) + beta * C (see GemmArgs).
+// One product: C = alpha * op(A) * op(B) + beta * C (see GemmArgs).  A and
+// B hold fp32 values (dtype 0) or 16-bit ones (MT_DTYPE_F16 / MT_DTYPE_BF16).
 struct Problem {
-  const float* A;
-  const float* B;
+  const void* A;
+  const void* B;
   float* C;
   int64_t M, N, K;
   int64_t lda, ldb, ldc;
   float alpha, beta;
   int trans_a, trans_b;
+  int dtype;
 };
+
+int ab_bytes(const Problem& P) { return P.dtype ? 2 : 4; }
 
 // The packed row-major product C = A*B (a leading dimension of at least 1
 // keeps empty operands valid).
-Problem packed_problem(const float* A, const float* B, float* C, int64_t M, int64_t N,
-                       int64_t K) {
+Problem packed_problem(const void* A, const void* B, float* C, int64_t M, int64_t N,
+                       int64_t K, int dtype = 0) {
   const int64_t lda = K > 0 ? K : 1, ldn = N > 0 ? N : 1;
-  return Problem{A, B, C, M, N, K, lda, ldn, ldn, 1.0f, 0.0f, 0, 0};
+  return Problem{A, B, C, M, N, K, lda, ldn, ldn, 1.0f, 0.0f, 0, 0, dtype};
 }
 
 // Everything a launch needs beyond the plan the caller can see.
@@ -111,9 +115,9 @@ mt_status check_dims(int64_t M, int64_t N, int64_t K) {
 }
 
 // Bytes from the first to one past the last element of a rows x cols view
-// with row stride ld.
-int64_t extent_bytes(int64_t rows, int64_t cols, int64_t ld) {
-  return rows > 0 && cols > 0 ? ((rows - 1) * ld + cols) * 4 : 0;
+// with row stride ld and elements of `elem` bytes.
+int64_t extent_bytes(int64_t rows, int64_t cols, int64_t ld, int elem = 4) {
+  return rows > 0 && cols > 0 ? ((rows - 1) * ld + cols) * elem : 0;
 }
 
 // Leading dimensions: each stored row must hold its logical row.
@@ -142,23 +146,23 @@ mt_status check_problem(const Problem& P) {
   if (st != MT_OK) return st;
   if (P.M == 0 || P.N == 0) return MT_OK;
   if (!P.C || !aligned4(P.C)) return MT_ERR_INVALID_ARG;
-  if (reads_ab(P) && (!P.A || !P.B || !aligned4(P.A) || !aligned4(P.B))) return MT_ERR_INVALID_ARG;
+  const int e = ab_bytes(P);
+  const uintptr_t amask = static_cast<uintptr_t>(e - 1);
+  if (reads_ab(P) && (!P.A || !P.B || (reinterpret_cast<uintptr_t>(P.A) & amask) ||
+                      (reinterpret_cast<uintptr_t>(P.B) & amask)))
+    return MT_ERR_INVALID_ARG;
   const int64_t c_bytes = extent_bytes(P.M, P.N, P.ldc);
   if (reads_ab(P)) {
-    const int64_t a_bytes = P.trans_a ? extent_bytes(P.K, P.M, P.lda)
-                                      : extent_bytes(P.M, P.K, P.lda);
-    const int64_t b_bytes = P.trans_b ? extent_bytes(P.N, P.K, P.ldb)
-                                      : extent_bytes(P.K, P.N, P.ldb);
+    const int64_t a_bytes = P.trans_a ? extent_bytes(P.K, P.M, P.lda, e)
+                                      : extent_bytes(P.M, P.K, P.lda, e);
+    const int64_t b_bytes = P.trans_b ? extent_bytes(P.N, P.K, P.ldb, e)
+                                      : extent_bytes(P.K, P.N, P.ldb, e);
     if (overlaps(P.C, c_bytes, P.A, a_bytes) || overlaps(P.C, c_bytes, P.B, b_bytes))
       return MT_ERR_ALIAS;
   }
   return MT_OK;
 }
 
-mt_status check_args(const float* A, const float* B, const float* C, int64_t M, int64_t N,
-                     int64_t K) {
-  return check_problem(packed_problem(A, B, const_cast<float*>(C), M, N, K));
-}
 
 // Chooses the FFMA table entry.  Explicit choices (tile, stages, warp tile,
 // micro-kernel form) must all match one entry; the first match in table
@@ -198,17 +202,14 @@ int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms) {
   return small;
 }
 
-// Tile width of the 3xTF32 kernel: the widest tile wins unless padding N
-// up to it, or too few tiles for the SMs, costs more than its higher
-// per-tile efficiency (relative weights measured on GB300).
-int pick_tf32x3_bn(int64_t M, int64_t N, int sms) {
-  // Per-tile throughput relative to 256-wide tiles (8192^3 and 4096^3 on
-  // GB300: narrower tiles re-read A from shared memory for fewer columns).
-  static const int widths[3] = {256, 128, 64};
-  static const double weight[3] = {1.0, 0.7, 0.4};
-  int best = 256;
+// Tile width of a persistent tensor-core kernel: the widest tile wins
+// unless padding N up to it, or too few tiles for the SMs, costs more than
+// its higher per-tile efficiency (`weight`, relative to the first width).
+int pick_tile_bn(int64_t M, int64_t N, int sms, const int* widths, const double* weight,
+                 int count) {
+  int best = widths[0];
   double best_score = -1.0;
-  for (int i = 0; i < 3; ++i) {
+  for (int i = 0; i < count; ++i) {
     const int bn = widths[i];
     const int64_t nt = ceil_div(N, bn);
     const double used = static_cast<double>(N) / static_cast<double>(nt * bn);
@@ -223,6 +224,91 @@ int pick_tf32x3_bn(int64_t M, int64_t N, int sms) {
     }
   }
   return best;
+}
+
+// 3xTF32: per-tile throughput relative to 256-wide tiles measured at 8192^3
+// and 4096^3 on GB300 (narrower tiles re-read A from shared memory for
+// fewer columns).
+int pick_tf32x3_bn(int64_t M, int64_t N, int sms) {
+  static const int widths[3] = {256, 128, 64};
+  static const double weight[3] = {1.0, 0.7, 0.4};
+  return pick_tile_bn(M, N, sms, widths, weight, 3);
+}
+
+// 16-bit kernel: 256- or 128-wide tiles.
+int pick_f16_bn(int64_t M, int64_t N, int sms) {
+  static const int widths[2] = {256, 128};
+  static const double weight[2] = {1.0, 0.8};
+  return pick_tile_bn(M, N, sms, widths, weight, 2);
+}
+
+// Split tail of a persistent kernel: when `tiles` leave a last round on at
+// most half of the `ctas` CTAs, those tiles are cut into K slices that run
+// on the idle ones (at most 4, every slice non-empty and at least 2 K tiles
+// long) and are added by a second kernel.  Outputs the whole tiles and the
+// slice count (1: no split).
+void split_tail(int64_t tiles, int64_t ctas, int64_t ktiles, bool allowed, int64_t* full,
+                int64_t* split) {
+  *full = tiles;
+  *split = 1;
+  if (!allowed || tiles <= ctas) return;
+  const int64_t rem = tiles % ctas;
+  if (rem == 0 || 2 * rem > ctas) return;
+  int64_t s = std::min<int64_t>(ctas / rem, 4);
+  while (s > 1 && ((s - 1) * ceil_div(ktiles, s) >= ktiles || ktiles / s < 2)) --s;
+  if (s > 1) {
+    *full = tiles - rem;
+    *split = s;
+  }
+}
+
+mt::GemmArgs make_args(const Problem& P, const Launch& L);
+
+// The 16-bit kernel (MT_VARIANT_TC16): 128 x BN tiles, BK = 64, persistent
+// with a split tail; operands TMA cannot read in place are copied first.
+mt_status plan_f16(const Problem& P, const mt_config* cfg, int64_t smem_limit, int sms,
+                   Launch* L) {
+  if (P.dtype != MT_DTYPE_F16 && P.dtype != MT_DTYPE_BF16) return MT_ERR_INVALID_ARG;
+  if (cfg && cfg->variant != MT_VARIANT_FFMA && cfg->variant != MT_VARIANT_TC16)
+    return MT_ERR_UNSUPPORTED;
+  if (cfg && (cfg->wm || cfg->wn || cfg->fma || cfg->no_pad || cfg->split_k > 1))
+    return MT_ERR_UNSUPPORTED;
+  const int64_t M = P.M, N = P.N, K = P.K;
+  const int bm = mt::f16tc_bm(), bk = mt::f16tc_bk();
+  const int bn = cfg && cfg->bn ? cfg->bn : pick_f16_bn(M, N, sms > 0 ? sms : 1);
+  if (!mt::f16tc_valid(bn)) return MT_ERR_UNSUPPORTED;
+  const int stages = mt::f16tc_stages(bn);
+  if (cfg && ((cfg->bm && cfg->bm != bm) || (cfg->bk && cfg->bk != bk) ||
+              (cfg->stages && cfg->stages != stages)))
+    return MT_ERR_UNSUPPORTED;
+  L->fault_inject = cfg ? cfg->fault_inject : 0;
+  mt_plan& p = L->plan;
+  std::memset(&p, 0, sizeof(p));
+  p.variant = MT_VARIANT_TC16;
+  p.bm = bm; p.bn = bn; p.bk = bk; p.stages = stages;
+  p.threads = mt::f16tc_threads();
+  p.vec_c = N % 4 == 0 && P.ldc % 4 == 0 && aligned16(P.C);
+  p.smem_bytes = mt::f16tc_smem_bytes(bn);
+  const int64_t tiles_m = ceil_div(M, bm), tiles_n = ceil_div(N, bn);
+  if (tiles_m * tiles_n > INT32_MAX / 8) return MT_ERR_UNSUPPORTED;
+  L->tiles_m = static_cast<int>(tiles_m);
+  L->tiles_n = static_cast<int>(tiles_n);
+  const int64_t tiles = tiles_m * tiles_n;
+  L->max_ctas = sms > 0 ? sms : 1;
+  int64_t full = tiles, split = 1;
+  split_tail(tiles, std::min<int64_t>(tiles, L->max_ctas), ceil_div(K, bk),
+             !(cfg && cfg->split_k == 1), &full, &split);
+  L->full_tiles = static_cast<int>(full);
+  L->split = static_cast<int>(split);
+  L->kt_per_slice = static_cast<int>(ceil_div(ceil_div(K, bk), split));
+  p.split_k = L->split;
+  p.grid = std::min<int64_t>(full + (tiles - full) * split, L->max_ctas);
+  const mt::F16Layout lay =
+      mt::f16tc_layout(make_args(P, *L), mt::F16Operands{P.A, P.B, P.dtype}, bn);
+  p.vec_ab = lay.repack_a_bytes == 0 && lay.repack_b_bytes == 0;
+  p.workspace_bytes = lay.workspace_bytes;
+  if (p.smem_bytes > smem_limit) return MT_ERR_SMEM_BUDGET;
+  return MT_OK;
 }
 
 // Pointers are only inspected for alignment here (NULL counts as aligned);
@@ -240,6 +326,8 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
               cfg->fma > 2 || cfg->fault_inject < 0 || cfg->fault_inject > 1 || cfg->wm < 0 ||
               cfg->wn < 0))
     return MT_ERR_INVALID_ARG;
+  if (P.dtype) return plan_f16(P, cfg, smem_limit, sms, L);
+  if (variant == MT_VARIANT_TC16) return MT_ERR_UNSUPPORTED;  // 16-bit inputs only
   if (cfg && (cfg->wm || cfg->wn) && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
   if (cfg && cfg->fault_inject && variant != MT_VARIANT_TF32X3) return MT_ERR_UNSUPPORTED;
   // 3xTF32 splits only its tail by itself (split_k = 1 turns that off).
@@ -301,24 +389,11 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
     // Persistent: one CTA per SM at most.
     const int64_t tiles = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
     L->max_ctas = sms > 0 ? sms : 1;
-    // Split tail: when the tiles leave a last round on at most half of the
-    // CTAs, those tiles are cut into K slices that run on the idle ones and
-    // are added by a second kernel (split_k = 1 turns this off).
+    // Split tail (split_k = 1 turns it off).
     const int64_t ctas = std::min<int64_t>(tiles, L->max_ctas);
     const int64_t ktiles = ceil_div(K, bk);
     int64_t full = tiles, split = 1;
-    if (!(cfg && cfg->split_k == 1) && tiles > ctas) {
-      const int64_t rem = tiles % ctas;
-      if (rem > 0 && 2 * rem <= ctas) {
-        split = std::min<int64_t>(ctas / rem, 4);
-        // Every slice non-empty and at least 2 K tiles long.
-        while (split > 1 && ((split - 1) * ceil_div(ktiles, split) >= ktiles ||
-                             ktiles / split < 2))
-          --split;
-        if (split > 1) full = tiles - rem;
-        else split = 1;
-      }
-    }
+    split_tail(tiles, ctas, ktiles, !(cfg && cfg->split_k == 1), &full, &split);
     L->full_tiles = static_cast<int>(full);
     L->split = static_cast<int>(split);
     L->kt_per_slice = static_cast<int>(ceil_div(ktiles, split));
@@ -441,8 +516,8 @@ mt_status prepare_tf32x3(int dev, int bk, int bn) {
 
 mt::GemmArgs make_args(const Problem& P, const Launch& L) {
   mt::GemmArgs a{};
-  a.A = P.A;
-  a.B = P.B;
+  a.A = P.dtype ? nullptr : static_cast<const float*>(P.A);
+  a.B = P.dtype ? nullptr : static_cast<const float*>(P.B);
   a.C = P.C;
   a.M = static_cast<int>(P.M);
   a.N = static_cast<int>(P.N);
@@ -487,6 +562,45 @@ mt_status run_tf32x3(int dev, const mt::GemmArgs& args, const Launch& L, cudaStr
   return MT_OK;
 }
 
+// [device][bn == 128]: shared-memory attribute of the 16-bit kernels applied.
+std::atomic<uint8_t> g_f16_ready[kMaxDevices][2];
+
+mt_status run_f16(int dev, const Problem& P, const mt::GemmArgs& args, const Launch& L,
+                  cudaStream_t stream) {
+  if (!mt::f16tc_encoder_available()) return MT_ERR_CUDA;
+  std::atomic<uint8_t>& ready = g_f16_ready[dev][L.plan.bn == 128 ? 1 : 0];
+  if (!ready.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!ready.load(std::memory_order_relaxed)) {
+      if (mt::f16tc_prepare(L.plan.bn) != cudaSuccess) {
+        cudaGetLastError();
+        return MT_ERR_LAUNCH;
+      }
+      ready.store(1, std::memory_order_release);
+    }
+  }
+  void* ws = nullptr;
+  if (L.plan.workspace_bytes > 0) {
+    cudaMemPool_t pool = nullptr;
+    mt_status st = pool_for(dev, &pool);
+    if (st != MT_OK) return st;
+    if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(L.plan.workspace_bytes), pool,
+                                stream) != cudaSuccess) {
+      cudaGetLastError();
+      return MT_ERR_CUDA;
+    }
+  }
+  const cudaError_t e =
+      mt::launch_f16tc(args, mt::F16Operands{P.A, P.B, P.dtype}, ws, L.plan.vec_c != 0,
+                       L.plan.bn, L.max_ctas, L.fault_inject, stream);
+  if (ws) cudaFreeAsync(ws, stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MT_ERR_LAUNCH;
+  }
+  return MT_OK;
+}
+
 mt_status run(const Problem& P, cudaStream_t stream, const mt_config* cfg) {
   mt_status st = check_problem(P);
   if (st != MT_OK) return st;
@@ -509,6 +623,7 @@ mt_status run(const Problem& P, cudaStream_t stream, const mt_config* cfg) {
     return MT_OK;
   }
   mt::GemmArgs args = make_args(P, L);
+  if (P.dtype) return run_f16(dev, P, args, L, stream);
   if (L.plan.variant == MT_VARIANT_TF32X3) return run_tf32x3(dev, args, L, stream);
   if (L.plan.variant == MT_VARIANT_P18) {
     if (mt::launch_p18(args, L.pad, stream) != cudaSuccess) return MT_ERR_LAUNCH;
@@ -671,6 +786,47 @@ mt_status mt_sgemm_plan(const float* A, const float* B, const float* C, int64_t 
   return st;
 }
 
+mt_status mt_gemm_mixed(int dtype, const void* A, const void* B, float* C, int64_t M, int64_t N,
+                        int64_t K, cudaStream_t stream) {
+  if (dtype != MT_DTYPE_F16 && dtype != MT_DTYPE_BF16) return MT_ERR_INVALID_ARG;
+  return run(packed_problem(A, B, C, M, N, K, dtype), stream, nullptr);
+}
+
+mt_status mt_gemm_mixed_general(int dtype, int trans_a, int trans_b, int64_t M, int64_t N,
+                                int64_t K, float alpha, const void* A, int64_t lda,
+                                const void* B, int64_t ldb, float beta, float* C, int64_t ldc,
+                                cudaStream_t stream, const mt_config* cfg) {
+  if (dtype != MT_DTYPE_F16 && dtype != MT_DTYPE_BF16) return MT_ERR_INVALID_ARG;
+  return run(Problem{A, B, C, M, N, K, lda, ldb, ldc, alpha, beta, trans_a, trans_b, dtype},
+             stream, cfg);
+}
+
+mt_status mt_gemm_mixed_plan(int dtype, int trans_a, int trans_b, int64_t M, int64_t N,
+                             int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                             const float* C, int64_t ldc, const mt_config* cfg,
+                             int64_t smem_limit_bytes, mt_plan* out) {
+  if (!out) return MT_ERR_INVALID_ARG;
+  if (dtype != MT_DTYPE_F16 && dtype != MT_DTYPE_BF16) return MT_ERR_INVALID_ARG;
+  const Problem P{A, B, const_cast<float*>(C), M, N, K, lda, ldb, ldc, 1.0f, 0.0f,
+                  trans_a, trans_b, dtype};
+  if (trans_a < 0 || trans_a > 1 || trans_b < 0 || trans_b > 1) return MT_ERR_INVALID_ARG;
+  int sms = 0;
+  int dev = 0;
+  DeviceInfo info;
+  if (smem_limit_bytes <= 0) {
+    mt_status st = current_device(&dev, &info);
+    if (st != MT_OK) return st;
+    smem_limit_bytes = info.smem_optin;
+    sms = info.sms;
+  } else {
+    sms = current_device(&dev, &info) == MT_OK ? info.sms : 152;
+  }
+  Launch L;
+  mt_status st = plan_call(P, cfg, smem_limit_bytes, sms, &L);
+  *out = L.plan;
+  return st;
+}
+
 int mt_smem_row_padding(int columns, int simultaneous_rows) {
   if (columns <= 0 || simultaneous_rows <= 0) return -1;
   return mt::row_padding_rule(columns, simultaneous_rows);
@@ -713,11 +869,13 @@ mt_status mt_device_status(cudaStream_t stream) {
     cudaGetLastError();
     return MT_ERR_CUDA;
   }
-  unsigned int flags = 0;
-  if (mt::tf32x3_read_and_clear_status(&flags) != cudaSuccess) {
+  unsigned int flags = 0, flags16 = 0;
+  if (mt::tf32x3_read_and_clear_status(&flags) != cudaSuccess ||
+      mt::f16tc_read_and_clear_status(&flags16) != cudaSuccess) {
     cudaGetLastError();
     return MT_ERR_CUDA;
   }
+  flags |= flags16;
   return flags ? MT_ERR_TIMEOUT : MT_OK;
 }
 

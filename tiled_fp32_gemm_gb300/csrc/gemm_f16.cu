@@ -1,0 +1,482 @@
+// fp32-accumulating GEMM on 16-bit inputs (fp16 or bf16) on the 5th-generation
+// tensor cores: tcgen05.mma kind::f16, accumulator in tensor memory (TMEM),
+// operands moved by the Tensor Memory Accelerator (TMA) straight from the
+// caller's matrices.
+//
+// The product is the general form of every other variant,
+//     C = alpha * op(A) * op(B) + beta * C      (C fp32, masked to M x N),
+// with A and B stored in 16 bits.  The pages announce mixed-precision types
+// as their next part ("My Triton From Scratch, Part 18: Shared Memory
+// Optimization", section "Next": Part 19, Mixed-Precision Types); the reading
+// taken here is 16-bit storage with products and sums in fp32.  A product of
+// two 16-bit values is exact in fp32, so only the fp32 accumulation rounds.
+//
+// Tiles are 128 x BN (BN = 256 or 128) with 64 values of K per stage: one
+// 128-byte swizzle row of 16-bit values, so every operand tile sits in
+// shared memory in the tensor core's 128-byte-swizzled layout and TMA writes
+// it there directly (no packing pass):
+//   K-major operand (A as stored, B stored transposed): one box of 64 k x
+//     128 (or BN) rows; row r at r * 128 bytes, 8-row atoms 1024 bytes apart.
+//   MN-major operand (B as stored, A stored transposed): boxes of 64 m/n x
+//     64 k, one per 64 columns of the tile, 8192 bytes apart; k-row r of a
+//     box at r * 128 bytes.  The MMA reads it MN-major (instruction
+//     descriptor bit), so neither layout is transposed on the way.
+// Zero fill: TMA returns 0 for every element outside the matrix, the masked
+// load of the pages ("Part 14: Shared Memory Tiles", section "Zero-filled
+// boundary tiles"), so ragged M, N and K need no special path.  A caller
+// stride TMA cannot take (row pitch not a multiple of 16 bytes, or a base
+// not 16-byte aligned) is first copied into a padded scratch matrix.
+//
+// The persistent kernel: one CTA per SM (192 threads) over units of a
+// grouped raster of tiles, with the last partial round split along K:
+//   warp 0, one thread: TMA loads of every K tile into a ring of STAGES
+//     stages (full[s], expect_tx of the stage's bytes);
+//   warp 1, one thread: per K tile 4 tcgen05.mma 128 x BN x 16 into one of
+//     two TMEM accumulators, tcgen05.commit -> empty[s]; after the unit's
+//     last K tile -> acc_full[b];
+//   warps 2-5: drain the other accumulator to C (alpha, beta, mask) while
+//     the next unit's MMAs run.
+// Every wait is bounded (%globaltimer); on expiry the CTA records
+// MT_ERR_TIMEOUT in this kernel's device status word, stops issuing, drains
+// what it issued, frees TMEM and returns.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "device_util.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace mt {
+namespace f16tc {
+
+using namespace tc;
+
+constexpr int BM = 128;
+constexpr int BK = 64;            // 16-bit values of K per stage: one 128-byte row
+constexpr int ROW_BYTES = BK * 2;
+constexpr int ATOM_BYTES = 8 * ROW_BYTES;
+constexpr int MN_BOX = 64;        // M/N values per box of an MN-major operand
+constexpr int MN_BOX_BYTES = BK * MN_BOX * 2;
+constexpr uint64_t SWIZZLE_128B = 2;  // descriptor layout code
+constexpr int THREADS = 192;
+constexpr int EPILOGUE_THREADS = 128;
+constexpr int SMEM_STAGE_BUDGET = 200 * 1024;
+
+__device__ unsigned int g_status;  // bit 0: a bounded wait expired
+
+template <int BN_>
+struct Geometry {
+  static_assert(BN_ == 256 || BN_ == 128, "BN is 256 or 128");
+  static constexpr int BN = BN_;
+  static constexpr int A_BYTES = BM * ROW_BYTES;
+  static constexpr int B_BYTES = BN * ROW_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES_FIT = SMEM_STAGE_BUDGET / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static_assert(STAGES >= 2, "at least two stages");
+  static constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulators
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment*/ + 256;
+};
+
+// Loads the `rows`-row tile of one operand for K tile k0 into `dst`.
+template <int ROWS, bool MN>
+__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, int r0,
+                                             int k0, uint32_t bar) {
+  if constexpr (!MN) {
+    tma_load_2d(dst, map, k0, r0, bar);  // box: 64 k x ROWS rows
+  } else {
+#pragma unroll
+    for (int c = 0; c < ROWS / MN_BOX; ++c)  // boxes: 64 m/n x 64 k
+      tma_load_2d(dst + c * MN_BOX_BYTES, map, r0 + c * MN_BOX, k0, bar);
+  }
+}
+
+// Descriptor of k-step j (16 values of K) of an operand tile at `base`.
+template <bool MN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int j) {
+  if constexpr (!MN)
+    return smem_desc(base + j * 32, 16, ATOM_BYTES, SWIZZLE_128B);  // 16 values = 32 bytes
+  else
+    return smem_desc(base + j * 16 * ROW_BYTES, MN_BOX_BYTES, ATOM_BYTES, SWIZZLE_128B);
+}
+
+template <int BN, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(THREADS, 1)
+    f16tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                      const __grid_constant__ CUtensorMap tmap_b, uint32_t idesc, Epilogue ep,
+                      int Kt, int tiles_m, int tiles_n, int group_m, Sched sched,
+                      int fault_inject) {
+  using G = Geometry<BN>;
+  constexpr int STAGES = G::STAGES;
+  constexpr int STAGE_BYTES = G::STAGE_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars: [0, S) full, [S, 2S) empty, 2S + b acc_full[b], 2S + 2 + b
+  // acc_empty[b], 2S + 4 drain.
+  constexpr int FULL = 0, EMPTY = STAGES, ACC_FULL = 2 * STAGES, ACC_EMPTY = 2 * STAGES + 2,
+                DRAIN = 2 * STAGES + 4, NBARS = 2 * STAGES + 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const WaitCtx wc{abort_flag, &g_status};
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int num_tiles = tiles_m * tiles_n;
+  const int num_units = sched.full_tiles + (num_tiles - sched.full_tiles) * sched.split;
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmap_a);
+    prefetch_tmap(&tmap_b);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(FULL + s), 1);   // producer arrival + tx bytes
+      mbar_init(bar(EMPTY + s), 1);  // MMA commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(ACC_FULL + b), 1);                  // MMA commit
+      mbar_init(bar(ACC_EMPTY + b), EPILOGUE_THREADS);  // every epilogue thread
+    }
+    mbar_init(bar(DRAIN), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), G::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  uint32_t issued = 0;  // producer: K tiles issued by this CTA, across its units
+  if (warp == 0) {
+    if (lane == 0) {
+      // Producer.  With fault_inject set it issues nothing, so every wait
+      // on its data runs out (the test of the timeout path).
+      uint32_t& g = issued;
+      bool stop = fault_inject != 0;
+      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
+        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+        for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
+          const uint32_t s = g % STAGES, round = g / STAGES;
+          if (g >= STAGES && !wait_phase(bar(EMPTY + s), (round + 1) & 1u, wc)) {
+            stop = true;
+            break;
+          }
+          const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
+          mbar_arrive_expect_tx(bar(FULL + s), STAGE_BYTES);
+          load_operand<BM, A_MN>(st, &tmap_a, w.tm * BM, kt * BK, bar(FULL + s));
+          load_operand<BN, B_MN>(st + G::A_BYTES, &tmap_b, w.tn * BN, kt * BK, bar(FULL + s));
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // MMA issuer.
+      uint32_t g = 0;
+      bool stop = false;
+      int it = 0;
+      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x, ++it) {
+        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+        const int b = it & 1;
+        // The epilogue must have drained this accumulator (used by unit it-2).
+        if (it >= 2 && !wait_phase(bar(ACC_EMPTY + b), ((it >> 1) + 1) & 1u, wc)) break;
+        tc_fence_after();
+        const uint32_t acc_tmem = tmem + static_cast<uint32_t>(b * BN);
+        uint32_t acc = 0;
+        for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
+          const uint32_t s = g % STAGES, round = g / STAGES;
+          if (!wait_phase(bar(FULL + s), round & 1u, wc)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + s * STAGE_BYTES);
+          const uint32_t b_base = a_base + G::A_BYTES;
+#pragma unroll
+          for (int j = 0; j < BK / 16; ++j) {
+            mma_f16(acc_tmem, operand_desc<A_MN>(a_base, j), operand_desc<B_MN>(b_base, j),
+                    idesc, acc);
+            acc = 1;
+          }
+          mma_commit(bar(EMPTY + s));
+        }
+        if (!stop) mma_commit(bar(ACC_FULL + b));
+      }
+      // Every MMA this thread issued has retired once DRAIN completes.
+      mma_commit(bar(DRAIN));
+      wait_phase(bar(DRAIN), 0, wc, false);
+    }
+  } else {
+    // Epilogue warps: warp w may access TMEM lanes 32*(w%4) .. +31.
+    const int q = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    int it = 0;
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++it) {
+      const int b = it & 1;
+      // A unit's accumulator is ready after its whole K loop.  The warp
+      // goes on only if every lane saw it (tcgen05.ld needs the whole warp).
+      const bool ready = wait_phase(bar(ACC_FULL + b), (it >> 1) & 1u, wc, true,
+                                    TIMEOUT_NS + 20000ull * static_cast<uint64_t>(Kt));
+      if (!__all_sync(0xffffffffu, ready)) break;
+      tc_fence_after();
+      __syncwarp();
+      const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      store_accumulator<BM, BN>(tmem + lane_base + static_cast<uint32_t>(b * BN), w, q, lane,
+                                ep, sched.partial);
+      tc_fence_before();
+      mbar_arrive(bar(ACC_EMPTY + b));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    // Let the copies the producer issued land before the CTA exits.
+    for (uint32_t q = issued > STAGES ? issued - STAGES : 0; q < issued; ++q)
+      wait_phase(bar(FULL + q % STAGES), (q / STAGES) & 1u, wc, false);
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, G::TMEM_COLS);
+  }
+}
+
+// dst[r * ldd + c] = src[r * lds + c] for c < cols, 0 for cols <= c < ldd
+// (16-bit values; ldd % 8 == 0 and dst 16-byte aligned, one 16-byte store
+// per thread and step).
+__global__ void __launch_bounds__(256) repack16_kernel(const uint16_t* __restrict__ src,
+                                                       int64_t lds, uint16_t* __restrict__ dst,
+                                                       int64_t ldd, int64_t rows, int64_t cols) {
+  const int64_t per_row = ldd / 8;
+  const int64_t total = rows * per_row;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = e / per_row, c0 = (e % per_row) * 8;
+    const uint16_t* s = src + r * lds;
+    uint16_t v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = c0 + i < cols ? s[c0 + i] : static_cast<uint16_t>(0);
+    uint4 o;
+    o.x = v[0] | (static_cast<uint32_t>(v[1]) << 16);
+    o.y = v[2] | (static_cast<uint32_t>(v[3]) << 16);
+    o.z = v[4] | (static_cast<uint32_t>(v[5]) << 16);
+    o.w = v[6] | (static_cast<uint32_t>(v[7]) << 16);
+    *reinterpret_cast<uint4*>(dst + r * ldd + c0) = o;
+  }
+}
+
+}  // namespace f16tc
+
+// ---------------------------------------------------------------------------
+// Host side.
+
+namespace {
+
+using f16tc::BK;
+using f16tc::BM;
+
+// cuTensorMapEncodeTiled, looked up once from the driver through the
+// runtime (the library does not link the driver library itself).
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      cudaGetLastError();
+  });
+  return g_encode;
+}
+
+// 2-D map of a stored rows x cols matrix of 16-bit values (row pitch ld
+// values), box of box_cols x box_rows, 128-byte swizzle, zero fill.
+bool encode_map(CUtensorMap* map, int dtype, const void* base, int64_t rows, int64_t cols,
+                int64_t ld, int box_cols, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols),
+                             static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType t =
+      dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return enc(map, t, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN>
+struct Cfg16 {
+  using G = f16tc::Geometry<BN>;
+
+  template <bool A_MN, bool B_MN>
+  static constexpr auto kernel() {
+    return f16tc::f16tc_gemm_kernel<BN, A_MN, B_MN>;
+  }
+
+  static cudaError_t prepare() {
+    cudaError_t e = cudaSuccess;
+    const void* ks[4] = {reinterpret_cast<const void*>(kernel<false, false>()),
+                         reinterpret_cast<const void*>(kernel<false, true>()),
+                         reinterpret_cast<const void*>(kernel<true, false>()),
+                         reinterpret_cast<const void*>(kernel<true, true>())};
+    for (const void* k : ks) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+    }
+    return e;
+  }
+
+  static cudaError_t launch(const GemmArgs& a, const F16Operands& f, void* workspace,
+                            bool vec_c, int max_ctas, int fault_inject, cudaStream_t stream) {
+    const int mt = (a.M + BM - 1) / BM, nt = (a.N + BN - 1) / BN, kt = (a.K + BK - 1) / BK;
+    const F16Layout L = f16tc_layout(a, f, BN);
+    char* ws = static_cast<char*>(workspace);
+    // Operands TMA cannot read in place go through padded copies.
+    const void* A = f.A;
+    int64_t lda = a.lda;
+    const void* B = f.B;
+    int64_t ldb = a.ldb;
+    if (L.repack_a_bytes) {
+      const int64_t rows = a.trans_a ? a.K : a.M, cols = a.trans_a ? a.M : a.K;
+      const int64_t ldd = (cols + 7) / 8 * 8;
+      f16tc::repack16_kernel<<<1216, 256, 0, stream>>>(static_cast<const uint16_t*>(f.A),
+                                                       a.lda, reinterpret_cast<uint16_t*>(ws),
+                                                       ldd, rows, cols);
+      A = ws;
+      lda = ldd;
+    }
+    if (L.repack_b_bytes) {
+      const int64_t rows = a.trans_b ? a.N : a.K, cols = a.trans_b ? a.K : a.N;
+      const int64_t ldd = (cols + 7) / 8 * 8;
+      uint16_t* dst = reinterpret_cast<uint16_t*>(ws + L.repack_a_bytes);
+      f16tc::repack16_kernel<<<1216, 256, 0, stream>>>(static_cast<const uint16_t*>(f.B),
+                                                       a.ldb, dst, ldd, rows, cols);
+      B = dst;
+      ldb = ldd;
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // A: K-major as stored (M x K), MN-major when stored transposed (K x M).
+    // B: MN-major as stored (K x N), K-major when stored transposed (N x K).
+    CUtensorMap map_a, map_b;
+    const bool a_mn = a.trans_a != 0, b_mn = a.trans_b == 0;
+    const bool ok_a = a_mn ? encode_map(&map_a, f.dtype, A, a.K, a.M, lda, f16tc::MN_BOX, BK)
+                           : encode_map(&map_a, f.dtype, A, a.M, a.K, lda, BK, BM);
+    const bool ok_b = b_mn ? encode_map(&map_b, f.dtype, B, a.K, a.N, ldb, f16tc::MN_BOX, BK)
+                           : encode_map(&map_b, f.dtype, B, a.N, a.K, ldb, BK, BN);
+    if (!ok_a || !ok_b) return cudaErrorInvalidValue;
+    const uint32_t fmt = f.dtype == 1 ? 0u : 1u;  // kind::f16 operand format: f16 0, bf16 1
+    const uint32_t idesc = tc::instr_desc(BM, BN, fmt, fmt, a_mn ? 1u : 0u, b_mn ? 1u : 0u);
+    const int tiles = mt * nt;
+    tc::Sched sched{a.full_tiles, a.split, a.kt_per_slice, nullptr};
+    if (a.split > 1) sched.partial = reinterpret_cast<float*>(ws + L.partial_offset);
+    const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
+    const int grid = units < max_ctas ? units : max_ctas;
+    const tc::Epilogue ep{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0};
+    auto go = [&](auto kern) {
+      kern<<<grid, f16tc::THREADS, G::SMEM_BYTES, stream>>>(map_a, map_b, idesc, ep, kt, mt, nt,
+                                                            a.group_m, sched, fault_inject);
+    };
+    if (!a_mn && !b_mn) go(kernel<false, false>());
+    else if (!a_mn && b_mn) go(kernel<false, true>());
+    else if (a_mn && !b_mn) go(kernel<true, false>());
+    else go(kernel<true, true>());
+    e = cudaGetLastError();
+    if (e != cudaSuccess || a.split <= 1) return e;
+    GemmArgs r = a;
+    r.partial = sched.partial;
+    return launch_splitk_reduce(r, BM, BN, vec_c, stream);
+  }
+};
+
+template <class F>
+bool dispatch16(int bn, F&& f) {
+  if (bn == 256) { f(Cfg16<256>{}); return true; }
+  if (bn == 128) { f(Cfg16<128>{}); return true; }
+  return false;
+}
+
+int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
+
+// Rows x cols of 16-bit values TMA can read in place: 16-byte aligned base,
+// row pitch a multiple of 16 bytes.
+bool tma_readable(const void* p, int64_t ld) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0 && ld % 8 == 0 && ld < (int64_t(1) << 38);
+}
+
+}  // namespace
+
+F16Layout f16tc_layout(const GemmArgs& a, const F16Operands& f, int bn) {
+  F16Layout L{};
+  if (!tma_readable(f.A, a.lda)) {
+    const int64_t rows = a.trans_a ? a.K : a.M, cols = a.trans_a ? a.M : a.K;
+    L.repack_a_bytes = round256(rows * ((cols + 7) / 8 * 8) * 2);
+  }
+  if (!tma_readable(f.B, a.ldb)) {
+    const int64_t rows = a.trans_b ? a.N : a.K, cols = a.trans_b ? a.K : a.N;
+    L.repack_b_bytes = round256(rows * ((cols + 7) / 8 * 8) * 2);
+  }
+  L.partial_offset = L.repack_a_bytes + L.repack_b_bytes;
+  const int64_t tiles = static_cast<int64_t>(a.tiles_m) * a.tiles_n;
+  const int64_t split_units = (tiles - a.full_tiles) * (a.split > 1 ? a.split : 0);
+  L.workspace_bytes = L.partial_offset + split_units * BM * bn * 4;
+  return L;
+}
+
+bool f16tc_valid(int bn) { return dispatch16(bn, [](auto) {}); }
+
+int f16tc_smem_bytes(int bn) {
+  int r = -1;
+  dispatch16(bn, [&](auto c) { r = decltype(c)::G::SMEM_BYTES; });
+  return r;
+}
+
+int f16tc_stages(int bn) {
+  int r = -1;
+  dispatch16(bn, [&](auto c) { r = decltype(c)::G::STAGES; });
+  return r;
+}
+
+int f16tc_threads() { return f16tc::THREADS; }
+int f16tc_bm() { return f16tc::BM; }
+int f16tc_bk() { return f16tc::BK; }
+
+cudaError_t f16tc_prepare(int bn) {
+  cudaError_t e = cudaErrorInvalidValue;
+  dispatch16(bn, [&](auto c) { e = decltype(c)::prepare(); });
+  return e;
+}
+
+bool f16tc_encoder_available() { return encoder() != nullptr; }
+
+cudaError_t launch_f16tc(const GemmArgs& a, const F16Operands& f, void* workspace, bool vec_c,
+                         int bn, int max_ctas, int fault_inject, cudaStream_t stream) {
+  cudaError_t e = cudaErrorInvalidValue;
+  dispatch16(bn, [&](auto c) {
+    e = decltype(c)::launch(a, f, workspace, vec_c, max_ctas, fault_inject, stream);
+  });
+  return e;
+}
+
+cudaError_t f16tc_read_and_clear_status(unsigned int* status) {
+  cudaError_t e = cudaMemcpyFromSymbol(status, f16tc::g_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(f16tc::g_status, &zero, sizeof(unsigned int));
+}
+
+}  // namespace mt

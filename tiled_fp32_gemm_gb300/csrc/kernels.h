@@ -96,4 +96,37 @@ cudaError_t tf32x3_noalloc_scratch(int device, void** ptr);
 // (bit 0: a bounded wait expired).  Synchronous.
 cudaError_t tf32x3_read_and_clear_status(unsigned int* status);
 
+// ---------------------------------------------------------------------------
+// tcgen05 kind::f16 kernel on 16-bit inputs (gemm_f16.cu).  GemmArgs carries
+// the sizes, leading dimensions, transposes, alpha/beta, C and the split
+// tail; its A and B are unused (the 16-bit operands come here).
+struct F16Operands {
+  const void* A;
+  const void* B;
+  int dtype;  // 1 = fp16, 2 = bf16
+};
+
+// Workspace of one call: padded copies of operands TMA cannot read in place
+// (row pitch not a multiple of 16 bytes or base not 16-byte aligned), then
+// the split tail's partial tiles.
+struct F16Layout {
+  int64_t repack_a_bytes, repack_b_bytes;
+  int64_t partial_offset;
+  int64_t workspace_bytes;
+};
+
+F16Layout f16tc_layout(const GemmArgs& a, const F16Operands& f, int bn);
+bool f16tc_valid(int bn);
+int f16tc_smem_bytes(int bn);
+int f16tc_stages(int bn);
+int f16tc_threads();
+int f16tc_bm();
+int f16tc_bk();
+cudaError_t f16tc_prepare(int bn);
+// Whether the driver's tensor-map encoder could be looked up.
+bool f16tc_encoder_available();
+cudaError_t launch_f16tc(const GemmArgs& a, const F16Operands& f, void* workspace, bool vec_c,
+                         int bn, int max_ctas, int fault_inject, cudaStream_t stream);
+cudaError_t f16tc_read_and_clear_status(unsigned int* status);
+
 }  // namespace mt

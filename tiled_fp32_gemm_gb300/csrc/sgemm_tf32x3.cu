@@ -46,6 +46,7 @@
 
 #include "device_util.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace mt {
 namespace tf32x3 {
@@ -53,7 +54,7 @@ namespace tf32x3 {
 constexpr int BM = 128;
 constexpr int THREADS = 192;
 constexpr int EPILOGUE_THREADS = 128;
-constexpr uint64_t TIMEOUT_NS = 1000000000ull;  // 1 s per wait
+using namespace tc;
 constexpr int SMEM_STAGE_BUDGET = 200 * 1024;   // shared memory for the operand ring
 
 __device__ unsigned int g_status;  // bit 0: a bounded wait expired
@@ -202,196 +203,10 @@ __global__ void __launch_bounds__(256) pack_rc_kernel(const float* __restrict__ 
   }
 }
 
-// ---------------------------------------------------------------------------
-// PTX wrappers.
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n"
-      " .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.b32 %0, 1, 0, p;\n"
-      "}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                              uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor of a K-major operand block: start address,
-// 8-row atoms `atom_bytes` apart (stride byte offset), swizzle `layout`
-// (2 = 128-byte, 4 = 64-byte), descriptor version 1.  The leading byte
-// offset is unused for swizzled K-major operands.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t atom_bytes,
-                                              uint64_t layout) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);  // start address, 16-byte units
-  d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused)
-  d |= static_cast<uint64_t>(atom_bytes >> 4) << 32;    // stride byte offset
-  d |= static_cast<uint64_t>(1) << 46;                  // descriptor version
-  d |= layout << 61;                                    // swizzle mode
-  return d;
-}
-
-// Instruction descriptor: D fp32, A and B tf32, both K-major, M x N.
-__host__ __device__ constexpr uint32_t instr_desc_tf32(int m, int n) {
-  return (1u << 4)                                 // D format: f32
-         | (2u << 7)                               // A format: tf32
-         | (2u << 10)                              // B format: tf32
-         | (static_cast<uint32_t>(n >> 3) << 17)   // N / 8
-         | (static_cast<uint32_t>(m >> 4) << 24);  // M / 16
-}
-
-__device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n"
-      " .reg .pred p;\n"
-      " setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n"
-      "}\n" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t slot_addr, uint32_t cols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   slot_addr),
-               "r"(cols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
-               : "memory");
-}
-
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-        "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Bounded wait on an mbarrier phase.  Returns false when the CTA is
-// aborting (another role gave up) or this wait itself ran out of time, in
-// which case it raises the abort flag and the device status word.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
-                                           volatile int* abort_flag, bool honour_abort = true,
-                                           uint64_t limit_ns = TIMEOUT_NS) {
-  const uint64_t t0 = globaltimer();
-  for (uint32_t i = 0;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 15u) == 15u) {
-      if (honour_abort && *abort_flag) return false;
-      if (globaltimer() - t0 > limit_ns) {
-        *abort_flag = 1;
-        atomicOr(&g_status, 1u);
-        return false;
-      }
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Work units of the persistent loop: below full_tiles a unit is a whole tile
-// (its index in the grouped raster); the tiles after those are split into
-// `split` K slices, one unit per slice, whose fp32 partial tiles (dense
-// 128 x BN, tail tile major, slice minor) are added by a second kernel.
-struct Sched {
-  int full_tiles;
-  int split;
-  int kt_per_slice;
-  float* partial;
-};
-
-struct Unit {
-  int tm, tn;    // tile coordinates
-  int kt0, kt1;  // K tiles [kt0, kt1)
-  int pidx;      // partial tile index, -1 for a whole tile
-};
-
-__device__ __forceinline__ Unit unit_of(int u, const Sched& sc, int tiles_m, int tiles_n,
-                                        int group_m, int Kt) {
-  Unit w;
-  int tile = u;
-  w.kt0 = 0;
-  w.kt1 = Kt;
-  w.pidx = -1;
-  if (u >= sc.full_tiles) {
-    const int v = u - sc.full_tiles;
-    tile = sc.full_tiles + v / sc.split;
-    w.kt0 = min(Kt, (v % sc.split) * sc.kt_per_slice);
-    w.kt1 = min(Kt, w.kt0 + sc.kt_per_slice);
-    w.pidx = v;
-  }
-  grouped_tile(tile, tiles_m, tiles_n, group_m, w.tm, w.tn);
-  return w;
-}
-
 template <class G>
 __global__ void __launch_bounds__(THREADS, 1)
     tf32x3_gemm_kernel(const float* __restrict__ Ap, const float* __restrict__ Bp,
-                       float* __restrict__ C, int64_t ldc, float alpha, float beta, int M,
-                       int N, int Kt, int tiles_m, int tiles_n, int group_m, int vec_c,
+                       Epilogue ep, int Kt, int tiles_m, int tiles_n, int group_m,
                        Sched sched, int fault_inject) {
   constexpr int BK = G::BK, BN = G::BN;
   constexpr int STAGES = G::STAGES;
@@ -406,6 +221,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 DRAIN = 2 * STAGES + 4, NBARS = 2 * STAGES + 5;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const WaitCtx wc{abort_flag, &g_status};
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -446,7 +262,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             static_cast<int64_t>(w.tn) * Kt * G::B_PAIR_BYTES;
         for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
           const uint32_t s = g % STAGES, round = g / STAGES;
-          if (g >= STAGES && !wait_phase(bar(EMPTY + s), (round + 1) & 1u, abort_flag)) {
+          if (g >= STAGES && !wait_phase(bar(EMPTY + s), (round + 1) & 1u, wc)) {
             stop = true;
             break;
           }
@@ -463,7 +279,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // MMA issuer.
-      constexpr uint32_t idesc = instr_desc_tf32(BM, BN);
+      constexpr uint32_t idesc = instr_desc(BM, BN, 2, 2);  // tf32 x tf32
       uint32_t g = 0;
       bool stop = false;
       int it = 0;
@@ -471,13 +287,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
         const int b = it & 1;
         // The epilogue must have drained this accumulator (used by unit it-2).
-        if (it >= 2 && !wait_phase(bar(ACC_EMPTY + b), ((it >> 1) + 1) & 1u, abort_flag)) break;
+        if (it >= 2 && !wait_phase(bar(ACC_EMPTY + b), ((it >> 1) + 1) & 1u, wc)) break;
         tc_fence_after();
         const uint32_t acc_tmem = tmem + static_cast<uint32_t>(b * BN);
         uint32_t acc = 0;
         for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
           const uint32_t s = g % STAGES, round = g / STAGES;
-          if (!wait_phase(bar(FULL + s), round & 1u, abort_flag)) {
+          if (!wait_phase(bar(FULL + s), round & 1u, wc)) {
             stop = true;
             break;
           }
@@ -489,10 +305,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int j = 0; j < BK / 8; ++j) {
             const uint32_t koff = j * 32;  // 8 tf32 = 32 bytes along K
-            const uint64_t ab = smem_desc(a_big + koff, G::ATOM_BYTES, G::LAYOUT);
-            const uint64_t as = smem_desc(a_small + koff, G::ATOM_BYTES, G::LAYOUT);
-            const uint64_t bb = smem_desc(b_big + koff, G::ATOM_BYTES, G::LAYOUT);
-            const uint64_t bs = smem_desc(b_small + koff, G::ATOM_BYTES, G::LAYOUT);
+            const uint64_t ab = smem_desc(a_big + koff, 16, G::ATOM_BYTES, G::LAYOUT);
+            const uint64_t as = smem_desc(a_small + koff, 16, G::ATOM_BYTES, G::LAYOUT);
+            const uint64_t bb = smem_desc(b_big + koff, 16, G::ATOM_BYTES, G::LAYOUT);
+            const uint64_t bs = smem_desc(b_small + koff, 16, G::ATOM_BYTES, G::LAYOUT);
             mma_tf32(acc_tmem, ab, bs, idesc, acc);
             acc = 1;
             mma_tf32(acc_tmem, as, bb, idesc, 1);
@@ -504,7 +320,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       // Every MMA this thread issued has retired once DRAIN completes.
       mma_commit(bar(DRAIN));
-      wait_phase(bar(DRAIN), 0, abort_flag, false);
+      wait_phase(bar(DRAIN), 0, wc, false);
     }
   } else {
     // Epilogue warps: warp w may access TMEM lanes 32*(w%4) .. +31.
@@ -515,53 +331,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int b = it & 1;
       // A tile's accumulator is ready after its whole K loop.  The warp
       // goes on only if every lane saw it (tcgen05.ld needs the whole warp).
-      const bool ready = wait_phase(bar(ACC_FULL + b), (it >> 1) & 1u, abort_flag, true,
+      const bool ready = wait_phase(bar(ACC_FULL + b), (it >> 1) & 1u, wc, true,
                                     TIMEOUT_NS + 20000ull * static_cast<uint64_t>(Kt));
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after();
       __syncwarp();
       const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
-      const int row = w.tm * BM + q * 32 + lane;
-      const uint32_t t_row = tmem + lane_base + static_cast<uint32_t>(b * BN);
-      float* c_row = C + static_cast<int64_t>(row) * ldc;
-#pragma unroll 1
-      for (int ch = 0; ch < BN / 32; ++ch) {
-        float v[32];
-        tmem_ld32(t_row + ch * 32, v);
-        const int col0 = w.tn * BN + ch * 32;
-        if (w.pidx >= 0) {
-          // A K slice: the raw partial tile, dense 128 x BN.
-          float* prow = sched.partial + static_cast<int64_t>(w.pidx) * (BM * BN) +
-                        (q * 32 + lane) * BN + ch * 32;
-#pragma unroll
-          for (int g4 = 0; g4 < 8; ++g4)
-            *reinterpret_cast<float4*>(prow + 4 * g4) =
-                make_float4(v[4 * g4], v[4 * g4 + 1], v[4 * g4 + 2], v[4 * g4 + 3]);
-        } else if (row < M) {
-          // C = alpha * acc + beta * C (C not read when beta == 0).
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= alpha;
-          if (vec_c) {
-#pragma unroll
-            for (int g4 = 0; g4 < 8; ++g4)
-              if (col0 + 4 * g4 < N) {
-                float4* cp = reinterpret_cast<float4*>(c_row + col0 + 4 * g4);
-                float4 o = make_float4(v[4 * g4], v[4 * g4 + 1], v[4 * g4 + 2], v[4 * g4 + 3]);
-                if (beta != 0.0f) {
-                  const float4 c0 = *cp;
-                  o = make_float4(fmaf(beta, c0.x, o.x), fmaf(beta, c0.y, o.y),
-                                  fmaf(beta, c0.z, o.z), fmaf(beta, c0.w, o.w));
-                }
-                *cp = o;
-              }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (col0 + i < N)
-                c_row[col0 + i] = beta != 0.0f ? fmaf(beta, c_row[col0 + i], v[i]) : v[i];
-          }
-        }
-      }
+      store_accumulator<BM, BN>(tmem + lane_base + static_cast<uint32_t>(b * BN), w, q, lane,
+                                ep, sched.partial);
       tc_fence_before();
       mbar_arrive(bar(ACC_EMPTY + b));
     }
@@ -572,7 +349,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0 && lane == 0 && *abort_flag) {
     // Let the copies the producer issued land before the CTA exits.
     for (uint32_t q = issued > STAGES ? issued - STAGES : 0; q < issued; ++q)
-      wait_phase(bar(FULL + q % STAGES), (q / STAGES) & 1u, abort_flag, false);
+      wait_phase(bar(FULL + q % STAGES), (q / STAGES) & 1u, wc, false);
   }
   if (warp == 1) {
     __syncwarp();
@@ -638,7 +415,8 @@ struct Cfg {
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int grid = units < max_ctas ? units : max_ctas;
     tf32x3_gemm_kernel<G><<<grid, THREADS, G::SMEM_BYTES, stream>>>(
-        Ap, Bp, a.C, a.ldc, a.alpha, a.beta, a.M, a.N, kt, mt, nt, a.group_m, vec_c ? 1 : 0,
+        Ap, Bp, Epilogue{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0}, kt, mt, nt,
+        a.group_m,
         sched, fault_inject);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.split <= 1) return e;

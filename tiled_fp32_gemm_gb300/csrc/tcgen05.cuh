@@ -1,0 +1,306 @@
+// Building blocks of the persistent tcgen05 GEMM kernels (3xTF32 on fp32
+// inputs, fp32-accumulating MMA on 16-bit inputs): inline PTX for mbarriers,
+// bulk and tensor (TMA) copies, tcgen05 MMA / TMEM, bounded waits, the
+// work-unit schedule with its split tail, and the TMEM -> C epilogue store.
+#pragma once
+
+#include <cstdint>
+
+#include "device_util.cuh"
+
+namespace mt {
+namespace tc {
+
+constexpr uint64_t TIMEOUT_NS = 1000000000ull;  // 1 s per wait
+
+// ---------------------------------------------------------------------------
+// mbarriers, copies, fences.
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.b32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Contiguous global -> shared copy (16-byte aligned, size % 16 == 0),
+// completing `bytes` transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Tiled tensor copy of one box at coordinates (x, y) of a 2-D tensor map
+// (x innermost) into shared memory; the whole box's bytes complete on `bar`,
+// elements outside the tensor arrive as zeros.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 MMA.
+
+// Shared-memory matrix descriptor: start address, leading byte offset,
+// stride byte offset (both in bytes, multiples of 16), swizzle `layout`
+// (2 = 128-byte, 4 = 64-byte), descriptor version 1.
+//   K-major swizzled operand: rows in 8-row atoms; stride = bytes between
+//     atoms; leading offset unused (the MMA's K extent lies inside one
+//     swizzle row).
+//   MN-major swizzled operand: 8 k-rows of one swizzle width of M/N values
+//     form an atom; leading = bytes between atoms along M/N, stride = bytes
+//     between atoms along K.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t leading_bytes,
+                                              uint32_t stride_bytes, uint64_t layout) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);           // start address, 16-byte units
+  d |= static_cast<uint64_t>((leading_bytes >> 4) & 0x3FFFu) << 16;  // leading byte offset
+  d |= static_cast<uint64_t>((stride_bytes >> 4) & 0x3FFFu) << 32;   // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                          // descriptor version
+  d |= layout << 61;                                            // swizzle mode
+  return d;
+}
+
+// Instruction descriptor: D fp32; A and B of format a_fmt / b_fmt (kind::tf32:
+// 2 = tf32; kind::f16: 0 = f16, 1 = bf16); a_mn / b_mn = 1 for an MN-major
+// operand; M x N.
+__host__ __device__ constexpr uint32_t instr_desc(int m, int n, uint32_t a_fmt,
+                                                  uint32_t b_fmt, uint32_t a_mn = 0,
+                                                  uint32_t b_mn = 0) {
+  return (1u << 4)                                 // D format: f32
+         | (a_fmt << 7) | (b_fmt << 10)            // operand formats
+         | (a_mn << 15) | (b_mn << 16)             // operand major-ness
+         | (static_cast<uint32_t>(n >> 3) << 17)   // N / 8
+         | (static_cast<uint32_t>(m >> 4) << 24);  // M / 16
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives on `bar` once every MMA this thread issued before it has retired.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_addr, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   slot_addr),
+               "r"(cols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------------------
+// Bounded waits.  A CTA's roles share an abort flag in shared memory; the
+// kernel's device status word (bit 0) records that a wait expired.
+struct WaitCtx {
+  volatile int* abort_flag;
+  unsigned int* status;
+};
+
+// Returns false when the CTA is aborting (another role gave up) or this wait
+// itself ran out of time, in which case it raises the abort flag and the
+// status word.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                           bool honour_abort = true,
+                                           uint64_t limit_ns = TIMEOUT_NS) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15u) == 15u) {
+      if (honour_abort && *w.abort_flag) return false;
+      if (globaltimer() - t0 > limit_ns) {
+        *w.abort_flag = 1;
+        atomicOr(w.status, 1u);
+        return false;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Work units of the persistent loop: below full_tiles a unit is a whole tile
+// (its index in the grouped raster); the tiles after those are split into
+// `split` K slices, one unit per slice, whose fp32 partial tiles (dense
+// BM x BN, tail tile major, slice minor) are added by a second kernel.
+struct Sched {
+  int full_tiles;
+  int split;
+  int kt_per_slice;
+  float* partial;
+};
+
+struct Unit {
+  int tm, tn;    // tile coordinates
+  int kt0, kt1;  // K tiles [kt0, kt1)
+  int pidx;      // partial tile index, -1 for a whole tile
+};
+
+__device__ __forceinline__ Unit unit_of(int u, const Sched& sc, int tiles_m, int tiles_n,
+                                        int group_m, int Kt) {
+  Unit w;
+  int tile = u;
+  w.kt0 = 0;
+  w.kt1 = Kt;
+  w.pidx = -1;
+  if (u >= sc.full_tiles) {
+    const int v = u - sc.full_tiles;
+    tile = sc.full_tiles + v / sc.split;
+    w.kt0 = min(Kt, (v % sc.split) * sc.kt_per_slice);
+    w.kt1 = min(Kt, w.kt0 + sc.kt_per_slice);
+    w.pidx = v;
+  }
+  grouped_tile(tile, tiles_m, tiles_n, group_m, w.tm, w.tn);
+  return w;
+}
+
+// The C update of a tile, shared by the epilogues.
+struct Epilogue {
+  float* C;
+  int64_t ldc;
+  float alpha, beta;
+  int M, N;
+  int vec_c;  // 16-byte stores of C allowed (N, ldc % 4 == 0, aligned base)
+};
+
+// Drains this warp's 32 TMEM lanes — rows q*32 .. q*32+31 of the BM x BN
+// accumulator whose first column of this warp's lanes is TMEM address
+// `t_row` — to C: C = alpha * acc + beta * C, masked to M x N, C not read
+// when beta == 0; or, for a K slice, to its dense partial tile.
+template <int BM, int BN>
+__device__ __forceinline__ void store_accumulator(uint32_t t_row, const Unit& w, int q,
+                                                  int lane, const Epilogue& ep,
+                                                  float* partial) {
+  const int row = w.tm * BM + q * 32 + lane;
+  float* c_row = ep.C + static_cast<int64_t>(row) * ep.ldc;
+#pragma unroll 1
+  for (int ch = 0; ch < BN / 32; ++ch) {
+    float v[32];
+    tmem_ld32(t_row + ch * 32, v);
+    const int col0 = w.tn * BN + ch * 32;
+    if (w.pidx >= 0) {
+      float* prow = partial + static_cast<int64_t>(w.pidx) * (BM * BN) + (q * 32 + lane) * BN +
+                    ch * 32;
+#pragma unroll
+      for (int g4 = 0; g4 < 8; ++g4)
+        *reinterpret_cast<float4*>(prow + 4 * g4) =
+            make_float4(v[4 * g4], v[4 * g4 + 1], v[4 * g4 + 2], v[4 * g4 + 3]);
+    } else if (row < ep.M) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] *= ep.alpha;
+      if (ep.vec_c) {
+#pragma unroll
+        for (int g4 = 0; g4 < 8; ++g4)
+          if (col0 + 4 * g4 < ep.N) {
+            float4* cp = reinterpret_cast<float4*>(c_row + col0 + 4 * g4);
+            float4 o = make_float4(v[4 * g4], v[4 * g4 + 1], v[4 * g4 + 2], v[4 * g4 + 3]);
+            if (ep.beta != 0.0f) {
+              const float4 c0 = *cp;
+              o = make_float4(fmaf(ep.beta, c0.x, o.x), fmaf(ep.beta, c0.y, o.y),
+                              fmaf(ep.beta, c0.z, o.z), fmaf(ep.beta, c0.w, o.w));
+            }
+            *cp = o;
+          }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (col0 + i < ep.N)
+            c_row[col0 + i] = ep.beta != 0.0f ? fmaf(ep.beta, c_row[col0 + i], v[i]) : v[i];
+      }
+    }
+  }
+}
+
+}  // namespace tc
+}  // namespace mt
