@@ -259,11 +259,16 @@ def launches_per_call(plan) -> int:
     """Kernels one library call launches: the GEMM (tf32x3: pack A, pack B,
     GEMM), plus the slice reduce when the plan splits K."""
     base = 3 if plan["variant"] == 1 else 1
+    if plan["variant"] == 3 and not plan["vec_ab"]:
+        base += 2  # the copy path pads both operands (the step's shapes never take it)
     return base + (1 if plan["split_k"] > 1 else 0)
 
 
 def variant_of(cfg_json):
-    return (cfg_json or {}).get("variant", "ffma")
+    cfg_json = cfg_json or {}
+    if cfg_json.get("dtype"):
+        return "tc16"  # 16-bit inputs: the tcgen05 kind::f16 kernel
+    return cfg_json.get("variant", "ffma")
 
 
 def run_gpu(args):
@@ -302,18 +307,41 @@ def run_gpu(args):
     sptr = stream.cuda_stream
     flops_step = sum(w.flops for (w, *_r) in bufs)
 
+    bufs16 = {}
+
+    def operands(dtype):
+        """The step's (w, a, b, c) with A and B in `dtype` ("bf16" / "f16",
+        rounded from the fp32 inputs before any timing) or fp32 (None)."""
+        if dtype is None:
+            return [(w, a, b, c) for (w, a, b, c, _, _) in bufs]
+        if dtype not in bufs16:
+            tdt = {"bf16": torch.bfloat16, "f16": torch.float16}[dtype]
+            bufs16[dtype] = [(w, a.to(tdt), b.to(tdt), c) for (w, a, b, c, _, _) in bufs]
+        return bufs16[dtype]
+
     def measure(cfg_json, steps, warmup, clocks=None):
-        """Per-launch CUDA-event times (ms) of every GEMM of `steps` steps."""
+        """Per-launch CUDA-event times (ms) of every GEMM of `steps` steps.
+        A "dtype" key ("bf16" / "f16") runs the 16-bit-input product
+        (mt_gemm_mixed_general) on the same shapes."""
+        cfg_json = dict(cfg_json or {})
+        dtype = cfg_json.pop("dtype", None)
         cfg = mt.make_config(**cfg_json) if cfg_json else None
+        ops = operands(dtype)
+        code = {"bf16": mt.MT_DTYPE_BF16, "f16": mt.MT_DTYPE_F16}.get(dtype)
 
         def launch(w, a, b, c):
-            st = mt.mt_sgemm_ex(a.data_ptr(), b.data_ptr(), c.data_ptr(), w.M, w.N, w.K, sptr,
-                                cfg)
+            if code is None:
+                st = mt.mt_sgemm_ex(a.data_ptr(), b.data_ptr(), c.data_ptr(), w.M, w.N, w.K,
+                                    sptr, cfg)
+            else:
+                st = mt.mt_gemm_mixed_general(code, 0, 0, w.M, w.N, w.K, 1.0, a.data_ptr(), w.K,
+                                              b.data_ptr(), w.N, 0.0, c.data_ptr(), w.N, sptr,
+                                              cfg)
             if st != mt.MT_OK:
-                raise mt.MtError(st, f"mt_sgemm_ex {w.name}")
+                raise mt.MtError(st, f"gemm {w.name}")
 
         for _ in range(warmup):
-            for (w, a, b, c, _, _) in bufs:
+            for (w, a, b, c) in ops:
                 launch(w, a, b, c)
         ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in bufs] for _ in range(steps)]
@@ -324,7 +352,7 @@ def run_gpu(args):
             clocks.mark("t0")
         t0.record(stream)
         for s_ in range(steps):
-            for i, (w, a, b, c, _, _) in enumerate(bufs):
+            for i, (w, a, b, c) in enumerate(ops):
                 ev[s_][i][0].record(stream)
                 launch(w, a, b, c)
                 ev[s_][i][1].record(stream)
@@ -340,8 +368,14 @@ def run_gpu(args):
         return total, per
 
     def plans_for(cfg_json):
-        return {w.name: mt.plan(w.M, w.N, w.K, a=a, b=b, c=c, **cfg_json)
-                for (w, a, b, c, _, _) in bufs}
+        cfg_json = dict(cfg_json or {})
+        dtype = cfg_json.pop("dtype", None)
+        if dtype is None:
+            return {w.name: mt.plan(w.M, w.N, w.K, a=a, b=b, c=c, **cfg_json)
+                    for (w, a, b, c) in operands(None)}
+        code = {"bf16": mt.MT_DTYPE_BF16, "f16": mt.MT_DTYPE_F16}[dtype]
+        return {w.name: mt.plan_mixed(code, w.M, w.N, w.K, a=a, b=b, c=c, **cfg_json)
+                for (w, a, b, c) in operands(dtype)}
 
     clocks = ClockSampler(dev).__enter__()
     total_ms, per_launch = measure(main_cfg, args.steps, args.warmup, clocks)
@@ -393,9 +427,21 @@ def run_gpu(args):
     def key_of(v, plan, name):
         return f"{v}_{plan['bm']}x{plan['bn']}x{plan['bk']}_s{plan['stages']}_{name}"
 
+    bf16_peak = bf16 if bf16 else 1900.0
+    bf16_basis = ("measured bf16 %.0f TFLOP/s burst (MEASURED_PEAKS.json)" % bf16_peak
+                  if bf16 else "fallback 1900 TFLOP/s bf16")
+
+    def tc16_roofline(achieved, key):
+        return {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
+                "frac": achieved / bf16_peak, "traffic": load_traffic(key), "kernel": key,
+                "peak_basis": bf16_basis,
+                "note": "achieved = 2MNK / time of the whole call (split-tail reduce included)"}
+
     kernel_key = key_of(variant, dp, dom.name)
     if variant == "tf32x3":
         roofline = tf32_roofline(3 * dom.flops / (dom_ms / 1e3) / 1e12, kernel_key)
+    elif variant == "tc16":
+        roofline = tc16_roofline(dom.flops / (dom_ms / 1e3) / 1e12, kernel_key)
     else:
         achieved = dom.flops / (dom_ms / 1e3) / 1e12
         roofline = {"bound": "alu", "achieved": achieved, "peak": ffma_peak, "unit": "TFLOP/s",
@@ -422,10 +468,26 @@ def run_gpu(args):
             o_ach = 3 * o_dom.flops / (statistics.mean(o_per[o_dom.name]) / 1e3) / 1e12
             variants["tf32x3"]["roofline"] = tf32_roofline(
                 o_ach, key_of("tf32x3", o_plans[o_dom.name], o_dom.name))
+        if variant != "tc16":
+            # bf16 inputs, fp32 accumulation and output (tcgen05 kind::f16).
+            h = {"dtype": "bf16"}
+            h_total, h_per = measure(h, o_steps, max(1, min(args.warmup, 3)))
+            h_plans = plans_for(h)
+            h_dom = max(bufs, key=lambda x: statistics.mean(h_per[x[0].name]))[0]
+            variants["tc16_bf16"] = {
+                "value": job_tflops(world, flops_step, o_steps, h_total / 1e3),
+                "unit": "TFLOP/s", "steps": o_steps, "inputs": "A, B rounded to bf16; C fp32",
+                "per_shape": shape_summary(h_per, h_plans),
+                "tolerance": "5e-5*|A||B| against the 16-bit oracle",
+                "roofline": tc16_roofline(
+                    h_dom.flops / (statistics.mean(h_per[h_dom.name]) / 1e3) / 1e12,
+                    key_of("tc16", h_plans[h_dom.name], h_dom.name))}
 
     # End to end through the host-buffer entry point (pinned host memory).
     e2e = None
-    if not args.no_e2e:
+    if main_cfg.get("dtype"):
+        e2e = {"unavailable": "the host-buffer entry point takes fp32 inputs only"}
+    elif not args.no_e2e:
         cfg = mt.make_config(**main_cfg) if main_cfg else None
         hbufs = []
         for (w, _a, _b, _c, A, B) in bufs:
@@ -463,7 +525,10 @@ def run_gpu(args):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if main_cfg.get("dtype") == "bf16" else
+                     "f16" if main_cfg.get("dtype") == "f16" else "f32",
+            "data": "synthetic",
             "config": {"workload": " + ".join(f"sgemm {w.M}x{w.N}x{w.K} ({w.dist}, seed {w.seed})"
                                               for (w, *_r) in bufs),
                        "variant": variant, "choices": main_cfg,

@@ -266,22 +266,30 @@ def plan16(M, N, K, dtype=mt.MT_DTYPE_BF16, ta=0, tb=0, lda=0, ldb=0, ldc=0, a=N
 
 
 def test_mixed_plan_tiles_and_tail():
+    # Without a GPU the plan assumes 152 SMs: 76 resident clusters of two.
     st, p = plan16(8192, 8192, 8192)
     assert st == mt.MT_OK
-    assert (p.variant, p.bm, p.bn, p.bk) == (mt.MT_VARIANT_TC16, 128, 256, 64)
+    # Automatic: CTA pairs on 256 x 256 tiles (32 x 32 = 1024 tiles >= 76).
+    assert (p.variant, p.bm, p.bn, p.bk) == (mt.MT_VARIANT_TC16, 256, 256, 64)
     assert p.threads == 192 and p.grid == 152 and p.vec_ab == 1 and p.vec_c == 1
-    # 64 x 32 = 2048 tiles on 152 SMs leave 72 (at most half the CTAs):
-    # those 72 run as 2 K slices each.
-    assert p.split_k == 2 and p.workspace_bytes == 72 * 2 * 128 * 256 * 4
-    assert p.smem_bytes <= GB300_SMEM and p.stages * (128 + 256) * 64 * 2 <= p.smem_bytes
-    # 4096^3: 512 tiles leave 56 on 152 CTAs: those 56 split in 2 K slices.
+    # 1024 tiles on 76 clusters leave 36 (at most half): split in 2 K slices.
+    assert p.split_k == 2 and p.workspace_bytes == 36 * 2 * 256 * 256 * 4
+    assert p.smem_bytes <= GB300_SMEM and p.stages * (128 + 128) * 64 * 2 <= p.smem_bytes
     st, p = plan16(4096, 4096, 4096)
-    assert p.split_k == 2 and p.workspace_bytes == 56 * 2 * 128 * 256 * 4
+    assert (p.bm, p.split_k) == (256, 2) and p.workspace_bytes == 28 * 2 * 256 * 256 * 4
     st, p = plan16(4096, 4096, 4096, split_k=1)
     assert p.split_k == 1 and p.workspace_bytes == 0
-    # Explicit 128-wide tiles.
+    # One CTA per 128 x 256 tile when asked: 512 tiles on 152 SMs leave 56.
+    st, p = plan16(4096, 4096, 4096, bm=128)
+    assert (p.bm, p.bn, p.grid, p.stages) == (128, 256, 152, 4)
+    assert p.split_k == 2 and p.workspace_bytes == 56 * 2 * 128 * 256 * 4
+    # Fewer pair tiles than clusters: single CTAs (1024^3: 16 pair tiles).
+    st, p = plan16(1024, 1024, 1024)
+    assert p.bm == 128
+    # Explicit 128-wide tiles; pairs take only 256-wide tiles.
     st, p = plan16(1024, 1024, 1024, bn=128)
-    assert st == mt.MT_OK and p.bn == 128 and p.stages >= 4
+    assert st == mt.MT_OK and (p.bm, p.bn) == (128, 128) and p.stages >= 4
+    assert plan16(1024, 1024, 1024, bm=256, bn=128)[0] == mt.MT_ERR_UNSUPPORTED
 
 
 def test_mixed_plan_repacks_what_tma_cannot_read():

@@ -23,6 +23,9 @@ import tiled_fp32_gemm_gb300 as mt
 pytestmark = pytest.mark.gpu
 
 TOL = 5e-5
+# Tile plans: automatic, one CTA per 128 x 256 or 128 x 128 tile, a CTA pair
+# per 256 x 256 tile (cta_group::2).
+TILES = {"auto": {}, "single": dict(bm=128), "bn128": dict(bn=128), "pair": dict(bm=256)}
 DTYPES = {"bf16": (mt.MT_DTYPE_BF16, torch.bfloat16), "f16": (mt.MT_DTYPE_F16, torch.float16)}
 assert (oracle.F16, oracle.BF16) == (mt.MT_DTYPE_F16, mt.MT_DTYPE_BF16)
 
@@ -76,8 +79,8 @@ def assert_within(got, want, W, what=""):
 @pytest.mark.parametrize("ta,tb", [(0, 0), (1, 0), (0, 1), (1, 1)])
 @pytest.mark.parametrize("path", ["direct", "repack"])
 @pytest.mark.parametrize("shape", [(133, 97, 71), (260, 300, 200), (31, 17, 300)])
-@pytest.mark.parametrize("bn", [0, 128])
-def test_mixed_matches_oracle(dt, ta, tb, path, shape, bn):
+@pytest.mark.parametrize("tile", sorted(TILES))
+def test_mixed_matches_oracle(dt, ta, tb, path, shape, tile):
     code, tdt = DTYPES[dt]
     M, N, K = shape
     g = np.random.default_rng(M + 7 * N + 13 * K + 2 * ta + tb + (path == "direct"))
@@ -89,7 +92,7 @@ def test_mixed_matches_oracle(dt, ta, tb, path, shape, bn):
     C0 = np.full((M, ldc), np.nan, np.float32)
     C0[:, :N] = draw(g, (M, N), "normal")
     alpha, beta = 1.75, -0.5
-    cfg = dict(bn=bn) if bn else {}
+    cfg = TILES[tile]
     p = mt.plan_mixed(code, M, N, K, ta, tb, lda, ldb, ldc, **cfg)
     assert p["vec_ab"] == (1 if path == "direct" else 0)
     got = run_mixed(code, ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, **cfg)
@@ -102,7 +105,8 @@ def test_mixed_matches_oracle(dt, ta, tb, path, shape, bn):
 
 @pytest.mark.parametrize("dt", sorted(DTYPES))
 @pytest.mark.parametrize("ta,tb", [(0, 0), (1, 1)])
-def test_mixed_integers_exact(dt, ta, tb):
+@pytest.mark.parametrize("tile", sorted(TILES))
+def test_mixed_integers_exact(dt, ta, tb, tile):
     code, tdt = DTYPES[dt]
     M, N, K = 300, 264, 1000
     g = np.random.default_rng(11 + ta)
@@ -111,7 +115,7 @@ def test_mixed_integers_exact(dt, ta, tb):
     A = stored16(g, a_rows, a_cols, a_cols, tdt, "int")
     B = stored16(g, b_rows, b_cols, b_cols, tdt, "int")
     C0 = draw(g, (M, N), "int")
-    got = run_mixed(code, ta, tb, M, N, K, 2.0, A, a_cols, B, b_cols, -3.0, C0, N)
+    got = run_mixed(code, ta, tb, M, N, K, 2.0, A, a_cols, B, b_cols, -3.0, C0, N, **TILES[tile])
     want = oracle.gemm_mixed_general(code, A, B, C0, M, N, K, a_cols, b_cols, N, 2.0, -3.0,
                                      ta, tb).reshape(M, N)
     assert np.array_equal(got, want)
@@ -144,20 +148,21 @@ def test_mixed_workloads(dt, name):
 
 
 @pytest.mark.parametrize("dt", sorted(DTYPES))
-def test_mixed_bench_size_sampled(dt):
+@pytest.mark.parametrize("tile", ["auto", "single"])
+def test_mixed_bench_size_sampled(dt, tile):
     """8192^3 in the launch configuration the benchmark times (packed rows,
     automatic plan with its split tail), checked on sampled rows."""
     code, tdt = DTYPES[dt]
     w = gemm_inputs.WORKLOADS["square_8192"]
     A, B = gemm_inputs.make_ab16(w.M, w.N, w.K, w.seed, w.dist, dt)
     a, b = A.cuda(), B.cuda()
-    c = mt.gemm_mixed(a, b)
+    c = mt.gemm_mixed(a, b, **TILES[tile])
     assert mt.mt_device_status(0) == mt.MT_OK
-    p = mt.plan_mixed(code, w.M, w.N, w.K, a=a, b=b, c=c)
+    p = mt.plan_mixed(code, w.M, w.N, w.K, a=a, b=b, c=c, **TILES[tile])
     assert p["vec_ab"] == 1 and p["split_k"] >= 1
     g = np.random.default_rng(3)
     # Rows of the first tile row, the split tail's last tile row and random ones.
-    rows = np.unique(np.concatenate([[0, 127, w.M - 1], g.integers(0, w.M, 13)]))
+    rows = np.unique(np.concatenate([[0, 127, 128, 255, w.M - 1], g.integers(0, w.M, 13)]))
     got = c.cpu().numpy()[rows]
     As = rows_of(A, torch.from_numpy(rows))
     want, W = oracle.gemm_mixed_general(code, As, B, np.zeros(len(rows) * w.N, np.float32),
@@ -166,7 +171,8 @@ def test_mixed_bench_size_sampled(dt):
 
 
 @pytest.mark.parametrize("dt", sorted(DTYPES))
-def test_mixed_split_tail_deterministic(dt):
+@pytest.mark.parametrize("tile", ["single", "pair"])
+def test_mixed_split_tail_deterministic(dt, tile):
     """512 tiles of 128 x 256 leave a partial round that is split along K;
     the slices are added in a fixed order, so repeated calls agree bit for
     bit, and both the split and the unsplit call match the oracle."""
@@ -174,16 +180,19 @@ def test_mixed_split_tail_deterministic(dt):
     M, N, K = 4096, 4096, 640
     A, B = gemm_inputs.make_ab16(M, N, K, 21, "normal", dt)
     a, b = A.cuda(), B.cuda()
-    p = mt.plan_mixed(code, M, N, K, a=a, b=b)
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    if 0 < 2 * (512 % sms) <= sms:
+    cfg = TILES[tile]
+    p = mt.plan_mixed(code, M, N, K, a=a, b=b, **cfg)
+    tiles = (M // p["bm"]) * (N // p["bn"])
+    units = p["grid"] // (2 if p["bm"] == 256 else 1)
+    if 0 < 2 * (tiles % units) <= units:
         assert p["split_k"] > 1
-    c1 = mt.gemm_mixed(a, b)
-    c2 = mt.gemm_mixed(a, b)
-    c3 = mt.gemm_mixed(a, b, split_k=1)
+    c1 = mt.gemm_mixed(a, b, **cfg)
+    c2 = mt.gemm_mixed(a, b, **cfg)
+    c3 = mt.gemm_mixed(a, b, split_k=1, **cfg)
     assert mt.mt_device_status(0) == mt.MT_OK
     assert torch.equal(c1, c2)
-    rows = np.array([0, 1, 2047, 3968, 4000, 4095])  # 3968.. lies in the last tile row
+    # 3840.. is the last row of 256-row tiles, 3968.. of 128-row tiles.
+    rows = np.array([0, 1, 130, 2047, 3900, 3968, 4000, 4095])
     As = rows_of(A, torch.from_numpy(rows))
     want, W = oracle.gemm_mixed_general(code, As, B, np.zeros(len(rows) * N, np.float32),
                                         len(rows), N, K, K, N, N, with_w=True)
@@ -229,18 +238,19 @@ def test_mixed_edge_cases(dt):
     assert mt.mt_device_status(0) == mt.MT_OK
 
 
-def test_mixed_timeout_path_reports_and_context_survives():
-    """The copy thread issues nothing: every bounded wait runs out (about a
+@pytest.mark.parametrize("tile", ["single", "pair"])
+def test_mixed_timeout_path_reports_and_context_survives(tile):
+    """The copy threads issue nothing: every bounded wait runs out (about a
     second), the kernel records the timeout and returns; the context stays
     usable for the next call."""
     A, B = gemm_inputs.make_ab16(100, 72, 80, 0, "uniform", "bf16")
     a, b = A.cuda(), B.cuda()
     c = torch.full((100, 72), 7.0, device="cuda")
-    mt.gemm_mixed(a, b, c, fault_inject=1)
+    mt.gemm_mixed(a, b, c, fault_inject=1, **TILES[tile])
     assert mt.mt_device_status(0) == mt.MT_ERR_TIMEOUT
     assert torch.all(c == 7.0)
     assert mt.mt_device_status(0) == mt.MT_OK
-    got = mt.gemm_mixed(a, b).cpu().numpy()
+    got = mt.gemm_mixed(a, b, **TILES[tile]).cpu().numpy()
     want, W = oracle.gemm_mixed_general(oracle.BF16, A, B, np.zeros(100 * 72, np.float32),
                                         100, 72, 80, 80, 72, 72, with_w=True)
     assert_within(got, want.reshape(100, 72), W, "after timeout")

@@ -264,23 +264,40 @@ void split_tail(int64_t tiles, int64_t ctas, int64_t ktiles, bool allowed, int64
 
 mt::GemmArgs make_args(const Problem& P, const Launch& L);
 
-// The 16-bit kernel (MT_VARIANT_TC16): 128 x BN tiles, BK = 64, persistent
-// with a split tail; operands TMA cannot read in place are copied first.
+// The automatic 16-bit plan takes CTA pairs (256 x 256 tiles) when 256-wide
+// tiles are chosen and there are at least as many pair tiles as resident
+// clusters: on GB300 pairs run 8192^3 bf16 at 1.19x and 4096^3 at 1.10x the
+// single-CTA 128 x 256 tiles, but are slower with fewer tiles than clusters
+// (1024^3: 0.79x).
+bool auto_pair(int64_t M, int64_t N, int bn, int sms, int pair_clusters) {
+  if (bn != 256) return false;
+  const int64_t clusters = pair_clusters > 0 ? pair_clusters : std::max(1, sms / 2);
+  return ceil_div(M, 256) * ceil_div(N, 256) >= clusters;
+}
+
+// The 16-bit kernels (MT_VARIANT_TC16): 128 x BN tiles on one CTA, or 256 x
+// 256 tiles on a CTA pair (bm = 256); BK = 64, persistent with a split
+// tail; operands TMA cannot read in place are copied first.  pair_clusters:
+// clusters of two resident at once (0: half the SMs).
 mt_status plan_f16(const Problem& P, const mt_config* cfg, int64_t smem_limit, int sms,
-                   Launch* L) {
+                   int pair_clusters, Launch* L) {
   if (P.dtype != MT_DTYPE_F16 && P.dtype != MT_DTYPE_BF16) return MT_ERR_INVALID_ARG;
   if (cfg && cfg->variant != MT_VARIANT_FFMA && cfg->variant != MT_VARIANT_TC16)
     return MT_ERR_UNSUPPORTED;
   if (cfg && (cfg->wm || cfg->wn || cfg->fma || cfg->no_pad || cfg->split_k > 1))
     return MT_ERR_UNSUPPORTED;
   const int64_t M = P.M, N = P.N, K = P.K;
-  const int bm = mt::f16tc_bm(), bk = mt::f16tc_bk();
-  const int bn = cfg && cfg->bn ? cfg->bn : pick_f16_bn(M, N, sms > 0 ? sms : 1);
-  if (!mt::f16tc_valid(bn)) return MT_ERR_UNSUPPORTED;
-  const int stages = mt::f16tc_stages(bn);
-  if (cfg && ((cfg->bm && cfg->bm != bm) || (cfg->bk && cfg->bk != bk) ||
-              (cfg->stages && cfg->stages != stages)))
+  const int bk = mt::f16tc_bk();
+  const int want_bm = cfg ? cfg->bm : 0;
+  const int bn = cfg && cfg->bn ? cfg->bn
+                 : want_bm == 256 ? 256 : pick_f16_bn(M, N, sms > 0 ? sms : 1);
+  const int bm = want_bm ? want_bm
+                         : auto_pair(M, N, bn, sms, pair_clusters) ? 256 : mt::f16tc_bm();
+  if (!mt::f16tc_valid(bm, bn)) return MT_ERR_UNSUPPORTED;
+  const int stages = mt::f16tc_stages(bm, bn);
+  if (cfg && ((cfg->bk && cfg->bk != bk) || (cfg->stages && cfg->stages != stages)))
     return MT_ERR_UNSUPPORTED;
+  const bool pair = bm == 256;
   L->fault_inject = cfg ? cfg->fault_inject : 0;
   mt_plan& p = L->plan;
   std::memset(&p, 0, sizeof(p));
@@ -288,13 +305,15 @@ mt_status plan_f16(const Problem& P, const mt_config* cfg, int64_t smem_limit, i
   p.bm = bm; p.bn = bn; p.bk = bk; p.stages = stages;
   p.threads = mt::f16tc_threads();
   p.vec_c = N % 4 == 0 && P.ldc % 4 == 0 && aligned16(P.C);
-  p.smem_bytes = mt::f16tc_smem_bytes(bn);
+  p.smem_bytes = mt::f16tc_smem_bytes(bm, bn);
   const int64_t tiles_m = ceil_div(M, bm), tiles_n = ceil_div(N, bn);
   if (tiles_m * tiles_n > INT32_MAX / 8) return MT_ERR_UNSUPPORTED;
   L->tiles_m = static_cast<int>(tiles_m);
   L->tiles_n = static_cast<int>(tiles_n);
   const int64_t tiles = tiles_m * tiles_n;
-  L->max_ctas = sms > 0 ? sms : 1;
+  // Persistent: one CTA per SM, or one cluster of two per two SMs.
+  if (pair) L->max_ctas = pair_clusters > 0 ? pair_clusters : std::max(1, sms / 2);
+  else L->max_ctas = sms > 0 ? sms : 1;
   int64_t full = tiles, split = 1;
   split_tail(tiles, std::min<int64_t>(tiles, L->max_ctas), ceil_div(K, bk),
              !(cfg && cfg->split_k == 1), &full, &split);
@@ -302,9 +321,9 @@ mt_status plan_f16(const Problem& P, const mt_config* cfg, int64_t smem_limit, i
   L->split = static_cast<int>(split);
   L->kt_per_slice = static_cast<int>(ceil_div(ceil_div(K, bk), split));
   p.split_k = L->split;
-  p.grid = std::min<int64_t>(full + (tiles - full) * split, L->max_ctas);
+  p.grid = std::min<int64_t>(full + (tiles - full) * split, L->max_ctas) * (pair ? 2 : 1);
   const mt::F16Layout lay =
-      mt::f16tc_layout(make_args(P, *L), mt::F16Operands{P.A, P.B, P.dtype}, bn);
+      mt::f16tc_layout(make_args(P, *L), mt::F16Operands{P.A, P.B, P.dtype}, bm, bn);
   p.vec_ab = lay.repack_a_bytes == 0 && lay.repack_b_bytes == 0;
   p.workspace_bytes = lay.workspace_bytes;
   if (p.smem_bytes > smem_limit) return MT_ERR_SMEM_BUDGET;
@@ -314,7 +333,7 @@ mt_status plan_f16(const Problem& P, const mt_config* cfg, int64_t smem_limit, i
 // Pointers are only inspected for alignment here (NULL counts as aligned);
 // check_problem checks them against the sizes.
 mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, int sms,
-                    Launch* L) {
+                    Launch* L, int pair_clusters = 0) {
   const int64_t M = P.M, N = P.N, K = P.K;
   mt_status st = check_dims(M, N, K);
   if (st != MT_OK) return st;
@@ -326,7 +345,7 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
               cfg->fma > 2 || cfg->fault_inject < 0 || cfg->fault_inject > 1 || cfg->wm < 0 ||
               cfg->wn < 0))
     return MT_ERR_INVALID_ARG;
-  if (P.dtype) return plan_f16(P, cfg, smem_limit, sms, L);
+  if (P.dtype) return plan_f16(P, cfg, smem_limit, sms, pair_clusters, L);
   if (variant == MT_VARIANT_TC16) return MT_ERR_UNSUPPORTED;  // 16-bit inputs only
   if (cfg && (cfg->wm || cfg->wn) && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
   if (cfg && cfg->fault_inject && variant != MT_VARIANT_TF32X3) return MT_ERR_UNSUPPORTED;
@@ -562,17 +581,19 @@ mt_status run_tf32x3(int dev, const mt::GemmArgs& args, const Launch& L, cudaStr
   return MT_OK;
 }
 
-// [device][bn == 128]: shared-memory attribute of the 16-bit kernels applied.
-std::atomic<uint8_t> g_f16_ready[kMaxDevices][2];
+// [device][128 x 256, 128 x 128, pair]: shared-memory attribute of the
+// 16-bit kernels applied.
+std::atomic<uint8_t> g_f16_ready[kMaxDevices][3];
 
 mt_status run_f16(int dev, const Problem& P, const mt::GemmArgs& args, const Launch& L,
                   cudaStream_t stream) {
   if (!mt::f16tc_encoder_available()) return MT_ERR_CUDA;
-  std::atomic<uint8_t>& ready = g_f16_ready[dev][L.plan.bn == 128 ? 1 : 0];
+  std::atomic<uint8_t>& ready =
+      g_f16_ready[dev][L.plan.bm == 256 ? 2 : L.plan.bn == 128 ? 1 : 0];
   if (!ready.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!ready.load(std::memory_order_relaxed)) {
-      if (mt::f16tc_prepare(L.plan.bn) != cudaSuccess) {
+      if (mt::f16tc_prepare(L.plan.bm, L.plan.bn) != cudaSuccess) {
         cudaGetLastError();
         return MT_ERR_LAUNCH;
       }
@@ -592,7 +613,7 @@ mt_status run_f16(int dev, const Problem& P, const mt::GemmArgs& args, const Lau
   }
   const cudaError_t e =
       mt::launch_f16tc(args, mt::F16Operands{P.A, P.B, P.dtype}, ws, L.plan.vec_c != 0,
-                       L.plan.bn, L.max_ctas, L.fault_inject, stream);
+                       L.plan.bm, L.plan.bn, L.max_ctas, L.fault_inject, stream);
   if (ws) cudaFreeAsync(ws, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -610,7 +631,8 @@ mt_status run(const Problem& P, cudaStream_t stream, const mt_config* cfg) {
   st = current_device(&dev, &info);
   if (st != MT_OK) return st;
   Launch L;
-  st = plan_call(P, cfg, info.smem_optin, info.sms, &L);
+  st = plan_call(P, cfg, info.smem_optin, info.sms, &L,
+                 P.dtype ? mt::f16tc_pair_max_clusters(dev) : 0);
   if (st != MT_OK) return st;
   if (!reads_ab(P)) {
     // No product to form (K == 0: the accumulator's zeros; alpha == 0):
@@ -822,7 +844,8 @@ mt_status mt_gemm_mixed_plan(int dtype, int trans_a, int trans_b, int64_t M, int
     sms = current_device(&dev, &info) == MT_OK ? info.sms : 152;
   }
   Launch L;
-  mt_status st = plan_call(P, cfg, smem_limit_bytes, sms, &L);
+  const int clusters = current_device(&dev, &info) == MT_OK ? mt::f16tc_pair_max_clusters(dev) : 0;
+  mt_status st = plan_call(P, cfg, smem_limit_bytes, sms, &L, clusters);
   *out = L.plan;
   return st;
 }

@@ -246,6 +246,202 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair kernel: a cluster of two CTAs on two SMs computes 256 x 256 tiles
+// with tcgen05.mma.cta_group::2.  CTA r (0 or 1) of the pair holds rows
+// m0 + 128 r .. +127 of A's tile and columns n0 + 128 r .. +127 of B's, so
+// each SM stages 32 KB per 64-deep K tile for a 128 x 256 share of the
+// product (a single-CTA 128 x 256 tile stages 48 KB for the same share).
+//   both CTAs, warp 0: TMA loads of the CTA's halves into its own ring; the
+//     bytes of both complete on the even CTA's full[s] (cta_group::2 copies),
+//     and only the even CTA arms it (expect_tx of both halves);
+//   even CTA, warp 1: per K tile 4 pair MMAs 256 x 256 x 16, then a commit
+//     multicast to empty[s] of both CTAs, and after a unit's last K tile to
+//     acc_full[b] of both;
+//   both CTAs, warps 2-5: drain their own TMEM half (128 rows x 256) to C,
+//     then one arrival per warp on the even CTA's acc_empty[b].
+// ACC_BUFS accumulators of 256 columns each (1 or 2) sit in TMEM.
+constexpr int PAIR_TILE = 256;
+constexpr int PAIR_HALF = 128;
+
+template <int ACC_BUFS_>
+struct PairGeometry {
+  static constexpr int ACC_BUFS = ACC_BUFS_;
+  static constexpr int A_BYTES = PAIR_HALF * ROW_BYTES;  // this CTA's half of A
+  static constexpr int B_BYTES = PAIR_HALF * ROW_BYTES;  // this CTA's half of B
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES_FIT = SMEM_STAGE_BUDGET / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr uint32_t TMEM_COLS = ACC_BUFS * PAIR_TILE;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment*/ + 256;
+};
+
+template <bool A_MN, bool B_MN, int ACC_BUFS>
+__global__ void __launch_bounds__(THREADS, 1)
+    f16tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                      const __grid_constant__ CUtensorMap tmap_b, uint32_t idesc, Epilogue ep,
+                      int Kt, int tiles_m, int tiles_n, int group_m, Sched sched,
+                      int fault_inject) {
+  using G = PairGeometry<ACC_BUFS>;
+  constexpr int STAGES = G::STAGES;
+  constexpr int STAGE_BYTES = G::STAGE_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars: [0, S) full (used on the even CTA), [S, 2S) empty, then
+  // acc_full[ACC_BUFS], acc_empty[ACC_BUFS] (used on the even CTA), drain.
+  constexpr int FULL = 0, EMPTY = STAGES, ACC_FULL = 2 * STAGES,
+                ACC_EMPTY = 2 * STAGES + ACC_BUFS, DRAIN = 2 * STAGES + 2 * ACC_BUFS,
+                NBARS = DRAIN + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const WaitCtx wc{abort_flag, &g_status};
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();  // 0: even (MMA issuer), 1: odd
+  const bool leader = rank == 0;
+  const int cluster = static_cast<int>(cluster_id_x());
+  const int clusters = static_cast<int>(cluster_count_x());
+  const int num_tiles = tiles_m * tiles_n;
+  const int num_units = sched.full_tiles + (num_tiles - sched.full_tiles) * sched.split;
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmap_a);
+    prefetch_tmap(&tmap_b);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(FULL + s), 1);   // the even CTA's arrival + both CTAs' bytes
+      mbar_init(bar(EMPTY + s), 1);  // pair MMA commit
+    }
+    for (int b = 0; b < ACC_BUFS; ++b) {
+      mbar_init(bar(ACC_FULL + b), 1);   // pair MMA commit
+      mbar_init(bar(ACC_EMPTY + b), 8);  // one arrival per epilogue warp of both CTAs
+    }
+    mbar_init(bar(DRAIN), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), G::TMEM_COLS);
+  tc_fence_before();
+  cluster_sync();  // barriers initialised and TMEM allocated in both CTAs
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // Producer (both CTAs): this CTA's halves into its own stages.
+      bool stop = fault_inject != 0;
+      uint32_t g = 0;
+      for (int u = cluster; u < num_units && !stop; u += clusters) {
+        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+        const int r0a = w.tm * PAIR_TILE + static_cast<int>(rank) * PAIR_HALF;
+        const int r0b = w.tn * PAIR_TILE + static_cast<int>(rank) * PAIR_HALF;
+        for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
+          const uint32_t s = g % STAGES, round = g / STAGES;
+          if (g >= STAGES && !wait_phase(bar(EMPTY + s), (round + 1) & 1u, wc)) {
+            stop = true;
+            break;
+          }
+          const uint32_t full_even = map_to_cta(bar(FULL + s), 0);
+          if (leader) mbar_arrive_expect_tx(bar(FULL + s), 2 * STAGE_BYTES);
+          const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
+          const int k0 = kt * BK;
+          if constexpr (!A_MN) {
+            tma_load_2d_pair(st, &tmap_a, k0, r0a, full_even);
+          } else {
+            tma_load_2d_pair(st, &tmap_a, r0a, k0, full_even);
+            tma_load_2d_pair(st + MN_BOX_BYTES, &tmap_a, r0a + MN_BOX, k0, full_even);
+          }
+          const uint32_t sb = st + G::A_BYTES;
+          if constexpr (!B_MN) {
+            tma_load_2d_pair(sb, &tmap_b, k0, r0b, full_even);
+          } else {
+            tma_load_2d_pair(sb, &tmap_b, r0b, k0, full_even);
+            tma_load_2d_pair(sb + MN_BOX_BYTES, &tmap_b, r0b + MN_BOX, k0, full_even);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // Pair MMA issuer (even CTA).
+      uint32_t g = 0;
+      bool stop = false;
+      int it = 0;
+      for (int u = cluster; u < num_units && !stop; u += clusters, ++it) {
+        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+        const int b = it % ACC_BUFS, use = it / ACC_BUFS;
+        // Both CTAs' epilogues must have drained this accumulator.
+        if (use >= 1 && !wait_phase(bar(ACC_EMPTY + b), (use + 1) & 1u, wc)) break;
+        tc_fence_after();
+        const uint32_t acc_tmem = tmem + static_cast<uint32_t>(b * PAIR_TILE);
+        uint32_t acc = 0;
+        for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
+          const uint32_t s = g % STAGES, round = g / STAGES;
+          if (!wait_phase(bar(FULL + s), round & 1u, wc)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + s * STAGE_BYTES);
+          const uint32_t b_base = a_base + G::A_BYTES;
+#pragma unroll
+          for (int j = 0; j < BK / 16; ++j) {
+            mma_f16_pair(acc_tmem, operand_desc<A_MN>(a_base, j), operand_desc<B_MN>(b_base, j),
+                         idesc, acc);
+            acc = 1;
+          }
+          mma_commit_pair(bar(EMPTY + s), 0x3);
+        }
+        if (!stop) mma_commit_pair(bar(ACC_FULL + b), 0x3);
+      }
+      // Every pair MMA issued has retired once DRAIN completes.
+      mma_commit_pair(bar(DRAIN), 0x1);
+      wait_phase(bar(DRAIN), 0, wc, false);
+    }
+  } else {
+    // Epilogue warps of both CTAs: warp w may access TMEM lanes 32*(w%4)..+31.
+    const int q = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t acc_empty_even = map_to_cta(bar(ACC_EMPTY), 0);
+    int it = 0;
+    for (int u = cluster; u < num_units; u += clusters, ++it) {
+      const int b = it % ACC_BUFS, use = it / ACC_BUFS;
+      const bool ready = wait_phase(bar(ACC_FULL + b), use & 1u, wc, true,
+                                    TIMEOUT_NS + 20000ull * static_cast<uint64_t>(Kt));
+      if (!__all_sync(0xffffffffu, ready)) break;
+      tc_fence_after();
+      __syncwarp();
+      const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      store_accumulator<PAIR_HALF, PAIR_TILE, PAIR_TILE>(
+          tmem + lane_base + static_cast<uint32_t>(b * PAIR_TILE), w, q, lane, ep,
+          sched.partial, static_cast<int>(rank) * PAIR_HALF);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty_even + 8u * static_cast<uint32_t>(b));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // Copies this CTA issued complete on the even CTA's barriers, which it
+    // cannot wait on: give any still in flight time to land (bounded).
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 200000ull) {
+    }
+  }
+  // The even CTA's MMAs (which read the odd CTA's shared memory) have
+  // retired and every cross-CTA arrival is done before either CTA leaves.
+  cluster_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, G::TMEM_COLS);
+  }
+}
+
 // dst[r * ldd + c] = src[r * lds + c] for c < cols, 0 for cols <= c < ldd
 // (16-bit values; ldd % 8 == 0 and dst 16-byte aligned, one 16-byte store
 // per thread and step).
@@ -318,6 +514,36 @@ bool encode_map(CUtensorMap* map, int dtype, const void* base, int64_t rows, int
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Operands TMA cannot read in place go through padded copies in the
+// workspace; returns the matrices and leading dimensions to read.
+cudaError_t repack_operands(const GemmArgs& a, const F16Operands& f, const F16Layout& L,
+                            char* ws, const void** A, int64_t* lda, const void** B,
+                            int64_t* ldb, cudaStream_t stream) {
+  *A = f.A;
+  *lda = a.lda;
+  *B = f.B;
+  *ldb = a.ldb;
+  if (L.repack_a_bytes) {
+    const int64_t rows = a.trans_a ? a.K : a.M, cols = a.trans_a ? a.M : a.K;
+    const int64_t ldd = (cols + 7) / 8 * 8;
+    f16tc::repack16_kernel<<<1216, 256, 0, stream>>>(static_cast<const uint16_t*>(f.A), a.lda,
+                                                     reinterpret_cast<uint16_t*>(ws), ldd, rows,
+                                                     cols);
+    *A = ws;
+    *lda = ldd;
+  }
+  if (L.repack_b_bytes) {
+    const int64_t rows = a.trans_b ? a.N : a.K, cols = a.trans_b ? a.K : a.N;
+    const int64_t ldd = (cols + 7) / 8 * 8;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(ws + L.repack_a_bytes);
+    f16tc::repack16_kernel<<<1216, 256, 0, stream>>>(static_cast<const uint16_t*>(f.B), a.ldb,
+                                                     dst, ldd, rows, cols);
+    *B = dst;
+    *ldb = ldd;
+  }
+  return cudaGetLastError();
+}
+
 template <int BN>
 struct Cfg16 {
   using G = f16tc::Geometry<BN>;
@@ -343,32 +569,12 @@ struct Cfg16 {
   static cudaError_t launch(const GemmArgs& a, const F16Operands& f, void* workspace,
                             bool vec_c, int max_ctas, int fault_inject, cudaStream_t stream) {
     const int mt = (a.M + BM - 1) / BM, nt = (a.N + BN - 1) / BN, kt = (a.K + BK - 1) / BK;
-    const F16Layout L = f16tc_layout(a, f, BN);
+    const F16Layout L = f16tc_layout(a, f, BM, BN);
     char* ws = static_cast<char*>(workspace);
-    // Operands TMA cannot read in place go through padded copies.
-    const void* A = f.A;
-    int64_t lda = a.lda;
-    const void* B = f.B;
-    int64_t ldb = a.ldb;
-    if (L.repack_a_bytes) {
-      const int64_t rows = a.trans_a ? a.K : a.M, cols = a.trans_a ? a.M : a.K;
-      const int64_t ldd = (cols + 7) / 8 * 8;
-      f16tc::repack16_kernel<<<1216, 256, 0, stream>>>(static_cast<const uint16_t*>(f.A),
-                                                       a.lda, reinterpret_cast<uint16_t*>(ws),
-                                                       ldd, rows, cols);
-      A = ws;
-      lda = ldd;
-    }
-    if (L.repack_b_bytes) {
-      const int64_t rows = a.trans_b ? a.N : a.K, cols = a.trans_b ? a.K : a.N;
-      const int64_t ldd = (cols + 7) / 8 * 8;
-      uint16_t* dst = reinterpret_cast<uint16_t*>(ws + L.repack_a_bytes);
-      f16tc::repack16_kernel<<<1216, 256, 0, stream>>>(static_cast<const uint16_t*>(f.B),
-                                                       a.ldb, dst, ldd, rows, cols);
-      B = dst;
-      ldb = ldd;
-    }
-    cudaError_t e = cudaGetLastError();
+    const void* A;
+    const void* B;
+    int64_t lda, ldb;
+    cudaError_t e = repack_operands(a, f, L, ws, &A, &lda, &B, &ldb, stream);
     if (e != cudaSuccess) return e;
     // A: K-major as stored (M x K), MN-major when stored transposed (K x M).
     // B: MN-major as stored (K x N), K-major when stored transposed (N x K).
@@ -403,6 +609,109 @@ struct Cfg16 {
   }
 };
 
+// Accumulators of the pair kernel in TMEM (256 columns each).
+constexpr int kPairAccBufs = 2;
+
+struct CfgPair {
+  using G = f16tc::PairGeometry<kPairAccBufs>;
+
+  template <bool A_MN, bool B_MN>
+  static constexpr auto kernel() {
+    return f16tc::f16tc_pair_kernel<A_MN, B_MN, kPairAccBufs>;
+  }
+
+  static const void* kernel_ptr(bool a_mn, bool b_mn) {
+    if (!a_mn && !b_mn) return reinterpret_cast<const void*>(kernel<false, false>());
+    if (!a_mn && b_mn) return reinterpret_cast<const void*>(kernel<false, true>());
+    if (a_mn && !b_mn) return reinterpret_cast<const void*>(kernel<true, false>());
+    return reinterpret_cast<const void*>(kernel<true, true>());
+  }
+
+  static cudaError_t prepare() {
+    for (int i = 0; i < 4; ++i) {
+      const cudaError_t e =
+          cudaFuncSetAttribute(kernel_ptr(i & 1, i >> 1),
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+
+  // Clusters of two that can be resident at once (the persistent grid).
+  static int max_clusters() {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(f16tc::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = G::SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel_ptr(false, true), &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return n;
+  }
+
+  static cudaError_t launch(const GemmArgs& a, const F16Operands& f, void* workspace,
+                            bool vec_c, int max_clusters, int fault_inject, cudaStream_t stream) {
+    using f16tc::PAIR_HALF;
+    using f16tc::PAIR_TILE;
+    const int mt = (a.M + PAIR_TILE - 1) / PAIR_TILE, nt = (a.N + PAIR_TILE - 1) / PAIR_TILE;
+    const int kt = (a.K + BK - 1) / BK;
+    const void* A;
+    const void* B;
+    int64_t lda, ldb;
+    char* ws = static_cast<char*>(workspace);
+    const F16Layout L = f16tc_layout(a, f, PAIR_TILE, PAIR_TILE);
+    cudaError_t e = repack_operands(a, f, L, ws, &A, &lda, &B, &ldb, stream);
+    if (e != cudaSuccess) return e;
+    CUtensorMap map_a, map_b;
+    const bool a_mn = a.trans_a != 0, b_mn = a.trans_b == 0;
+    // Each CTA loads 128 rows of A's tile and 128 columns of B's.
+    const bool ok_a = a_mn ? encode_map(&map_a, f.dtype, A, a.K, a.M, lda, f16tc::MN_BOX, BK)
+                           : encode_map(&map_a, f.dtype, A, a.M, a.K, lda, BK, PAIR_HALF);
+    const bool ok_b = b_mn ? encode_map(&map_b, f.dtype, B, a.K, a.N, ldb, f16tc::MN_BOX, BK)
+                           : encode_map(&map_b, f.dtype, B, a.N, a.K, ldb, BK, PAIR_HALF);
+    if (!ok_a || !ok_b) return cudaErrorInvalidValue;
+    const uint32_t fmt = f.dtype == 1 ? 0u : 1u;
+    const uint32_t idesc =
+        tc::instr_desc(PAIR_TILE, PAIR_TILE, fmt, fmt, a_mn ? 1u : 0u, b_mn ? 1u : 0u);
+    const int tiles = mt * nt;
+    tc::Sched sched{a.full_tiles, a.split, a.kt_per_slice, nullptr};
+    if (a.split > 1) sched.partial = reinterpret_cast<float*>(ws + L.partial_offset);
+    const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
+    const int clusters = units < max_clusters ? units : max_clusters;
+    const tc::Epilogue ep{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0};
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(f16tc::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = G::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int group_m = a.group_m;
+    void* args[] = {&map_a, &map_b, const_cast<uint32_t*>(&idesc), const_cast<tc::Epilogue*>(&ep),
+                    const_cast<int*>(&kt), const_cast<int*>(&mt), const_cast<int*>(&nt),
+                    &group_m, &sched, const_cast<int*>(&fault_inject)};
+    e = cudaLaunchKernelExC(&cfg, kernel_ptr(a_mn, b_mn), args);
+    if (e != cudaSuccess || a.split <= 1) return e;
+    GemmArgs r = a;
+    r.partial = sched.partial;
+    return launch_splitk_reduce(r, PAIR_TILE, PAIR_TILE, vec_c, stream);
+  }
+};
+
 template <class F>
 bool dispatch16(int bn, F&& f) {
   if (bn == 256) { f(Cfg16<256>{}); return true; }
@@ -420,7 +729,7 @@ bool tma_readable(const void* p, int64_t ld) {
 
 }  // namespace
 
-F16Layout f16tc_layout(const GemmArgs& a, const F16Operands& f, int bn) {
+F16Layout f16tc_layout(const GemmArgs& a, const F16Operands& f, int tile_m, int bn) {
   F16Layout L{};
   if (!tma_readable(f.A, a.lda)) {
     const int64_t rows = a.trans_a ? a.K : a.M, cols = a.trans_a ? a.M : a.K;
@@ -433,29 +742,53 @@ F16Layout f16tc_layout(const GemmArgs& a, const F16Operands& f, int bn) {
   L.partial_offset = L.repack_a_bytes + L.repack_b_bytes;
   const int64_t tiles = static_cast<int64_t>(a.tiles_m) * a.tiles_n;
   const int64_t split_units = (tiles - a.full_tiles) * (a.split > 1 ? a.split : 0);
-  L.workspace_bytes = L.partial_offset + split_units * BM * bn * 4;
+  L.workspace_bytes = L.partial_offset + split_units * tile_m * bn * 4;
   return L;
 }
 
-bool f16tc_valid(int bn) { return dispatch16(bn, [](auto) {}); }
+bool f16tc_valid(int bm, int bn) {
+  if (bm == f16tc::PAIR_TILE) return bn == f16tc::PAIR_TILE;
+  return bm == BM && dispatch16(bn, [](auto) {});
+}
 
-int f16tc_smem_bytes(int bn) {
+int f16tc_smem_bytes(int bm, int bn) {
+  if (bm == f16tc::PAIR_TILE) return CfgPair::G::SMEM_BYTES;
   int r = -1;
   dispatch16(bn, [&](auto c) { r = decltype(c)::G::SMEM_BYTES; });
   return r;
 }
 
-int f16tc_stages(int bn) {
+int f16tc_stages(int bm, int bn) {
+  if (bm == f16tc::PAIR_TILE) return CfgPair::G::STAGES;
   int r = -1;
   dispatch16(bn, [&](auto c) { r = decltype(c)::G::STAGES; });
   return r;
+}
+
+namespace {
+std::mutex g_pair_mutex;
+int g_pair_clusters[64];
+}  // namespace
+
+int f16tc_pair_max_clusters(int device) {
+  if (device < 0 || device >= 64) return 0;
+  std::lock_guard<std::mutex> lock(g_pair_mutex);
+  if (g_pair_clusters[device] == 0) {
+    if (CfgPair::prepare() != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    g_pair_clusters[device] = CfgPair::max_clusters();
+  }
+  return g_pair_clusters[device];
 }
 
 int f16tc_threads() { return f16tc::THREADS; }
 int f16tc_bm() { return f16tc::BM; }
 int f16tc_bk() { return f16tc::BK; }
 
-cudaError_t f16tc_prepare(int bn) {
+cudaError_t f16tc_prepare(int bm, int bn) {
+  if (bm == f16tc::PAIR_TILE) return CfgPair::prepare();
   cudaError_t e = cudaErrorInvalidValue;
   dispatch16(bn, [&](auto c) { e = decltype(c)::prepare(); });
   return e;
@@ -464,7 +797,9 @@ cudaError_t f16tc_prepare(int bn) {
 bool f16tc_encoder_available() { return encoder() != nullptr; }
 
 cudaError_t launch_f16tc(const GemmArgs& a, const F16Operands& f, void* workspace, bool vec_c,
-                         int bn, int max_ctas, int fault_inject, cudaStream_t stream) {
+                         int bm, int bn, int max_ctas, int fault_inject, cudaStream_t stream) {
+  if (bm == f16tc::PAIR_TILE)
+    return CfgPair::launch(a, f, workspace, vec_c, max_ctas, fault_inject, stream);
   cudaError_t e = cudaErrorInvalidValue;
   dispatch16(bn, [&](auto c) {
     e = decltype(c)::launch(a, f, workspace, vec_c, max_ctas, fault_inject, stream);

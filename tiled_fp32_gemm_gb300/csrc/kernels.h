@@ -115,18 +115,25 @@ struct F16Layout {
   int64_t workspace_bytes;
 };
 
-F16Layout f16tc_layout(const GemmArgs& a, const F16Operands& f, int bn);
-bool f16tc_valid(int bn);
-int f16tc_smem_bytes(int bn);
-int f16tc_stages(int bn);
+// Tiles: bm = 128 (one CTA per tile, bn = 256 or 128) or bm = 256 (a CTA
+// pair per 256 x 256 tile, bn = 256).
+F16Layout f16tc_layout(const GemmArgs& a, const F16Operands& f, int tile_m, int bn);
+bool f16tc_valid(int bm, int bn);
+int f16tc_smem_bytes(int bm, int bn);
+int f16tc_stages(int bm, int bn);
 int f16tc_threads();
 int f16tc_bm();
 int f16tc_bk();
-cudaError_t f16tc_prepare(int bn);
+cudaError_t f16tc_prepare(int bm, int bn);
+// Clusters of two CTAs of the pair kernel resident at once on `device` (the
+// current device); 0 if the query fails.  Sets the kernel's shared-memory
+// limit on first use.
+int f16tc_pair_max_clusters(int device);
 // Whether the driver's tensor-map encoder could be looked up.
 bool f16tc_encoder_available();
+// max_ctas: CTAs of the persistent grid at most (bm = 256: clusters of two).
 cudaError_t launch_f16tc(const GemmArgs& a, const F16Operands& f, void* workspace, bool vec_c,
-                         int bn, int max_ctas, int fault_inject, cudaStream_t stream);
+                         int bm, int bn, int max_ctas, int fault_inject, cudaStream_t stream);
 cudaError_t f16tc_read_and_clear_status(unsigned int* status);
 
 }  // namespace mt

@@ -71,8 +71,55 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
+// The same copy for a CTA pair (cta_group::2): the box lands in this CTA's
+// shared memory and its bytes complete on `bar`, which may be the peer's
+// barrier (a shared::cluster address from mapa).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, int x, int y,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Thread-block clusters.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Shared::cluster address of this CTA's shared address `addr` in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Every thread of every CTA of the cluster (release / acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                   cluster_addr)
+               : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -140,6 +187,47 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_
       "}\n" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// CTA-pair MMA (cta_group::2, issued by the even CTA of the pair): A's rows
+// are split between the pair (the first half from this CTA's shared memory,
+// the second half from the peer's at the same address), B's columns likewise,
+// and each CTA's TMEM receives its half of D's rows, all N columns.
+__device__ __forceinline__ void mma_f16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives on the barrier at `bar`'s offset in every CTA of `cta_mask` once
+// every pair MMA this thread issued before it has retired.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// Pair allocation: one warp of each CTA of the pair executes it together;
+// the same TMEM columns are allocated in both CTAs.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot_addr, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   slot_addr),
+               "r"(cols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+               : "memory");
 }
 
 // Arrives on `bar` once every MMA this thread issued before it has retired.
@@ -258,11 +346,15 @@ struct Epilogue {
 // accumulator whose first column of this warp's lanes is TMEM address
 // `t_row` — to C: C = alpha * acc + beta * C, masked to M x N, C not read
 // when beta == 0; or, for a K slice, to its dense partial tile.
-template <int BM, int BN>
+//
+// TILE_M is the tile's row count (BM for one CTA, 2 * BM for a CTA pair) and
+// sub_row0 the first tile row this CTA holds (0, or BM for the odd CTA of a
+// pair); partial tiles are dense TILE_M x BN.
+template <int BM, int BN, int TILE_M = BM>
 __device__ __forceinline__ void store_accumulator(uint32_t t_row, const Unit& w, int q,
                                                   int lane, const Epilogue& ep,
-                                                  float* partial) {
-  const int row = w.tm * BM + q * 32 + lane;
+                                                  float* partial, int sub_row0 = 0) {
+  const int row = w.tm * TILE_M + sub_row0 + q * 32 + lane;
   float* c_row = ep.C + static_cast<int64_t>(row) * ep.ldc;
 #pragma unroll 1
   for (int ch = 0; ch < BN / 32; ++ch) {
@@ -270,8 +362,8 @@ __device__ __forceinline__ void store_accumulator(uint32_t t_row, const Unit& w,
     tmem_ld32(t_row + ch * 32, v);
     const int col0 = w.tn * BN + ch * 32;
     if (w.pidx >= 0) {
-      float* prow = partial + static_cast<int64_t>(w.pidx) * (BM * BN) + (q * 32 + lane) * BN +
-                    ch * 32;
+      float* prow = partial + static_cast<int64_t>(w.pidx) * (TILE_M * BN) +
+                    (sub_row0 + q * 32 + lane) * BN + ch * 32;
 #pragma unroll
       for (int g4 = 0; g4 < 8; ++g4)
         *reinterpret_cast<float4*>(prow + 4 * g4) =
