@@ -24,12 +24,17 @@ Sources, by page and section:
   - "Cooperative copy mapping": thread t copies t, t+T, t+2T, ...
 * "Optimize Shared Memory Tiling" (skills page), "Required reasoning
   process" steps 1-3: map each access to a bank, k different addresses in
-  one bank cost k transactions, a broadcast costs one.
+  one bank cost k transactions, a broadcast costs one; "Correctness
+  requirements", the fp16 bank analysis: the bank of 16-bit element i is
+  (i * 2) / 4 % 32 = i / 2 % 32.
 
 Readings of points the pages leave open (each is listed in the design
 notes): 64-bit and 128-bit accesses are served in phases of 16 and 8 lanes
 (each phase moves at most 128 bytes through the 32 four-byte banks); a
 bank's cost inside a phase is the number of distinct 4-byte words it holds.
+16-bit accesses are served in one phase of 32 lanes, and two lanes reading
+the two halves of one 4-byte word share it (a broadcast), where the skills
+page counts consecutive fp16 elements as a possible 2-way conflict.
 """
 from __future__ import annotations
 
@@ -44,6 +49,12 @@ BANK_BYTES = 4
 def bank(word_offset: int) -> int:
     """Bank of a 4-byte word: word_offset % 32."""
     return word_offset % NUM_BANKS
+
+
+def element_bank(index: int, element_bytes: int) -> int:
+    """Bank of element `index` of an array of `element_bytes`-byte elements
+    (skills page, fp16 analysis: (i * 2) / 4 % 32 for 16-bit elements)."""
+    return (index * element_bytes) // BANK_BYTES % NUM_BANKS
 
 
 def column_banks(row_stride: int, rows: int, column: int = 0) -> tuple:
@@ -150,15 +161,16 @@ def wavefronts(byte_addresses, width_bytes: int = 4) -> int:
 
     `byte_addresses` holds one start address per active lane (None for an
     inactive lane), in lane order.  Lanes are served in phases of
-    128 / width_bytes lanes (32, 16 or 8).  Inside a phase each bank costs as
+    min(32, 128 / width_bytes) lanes (32 for 2- and 4-byte accesses,
+    16, 8).  Inside a phase each bank costs as
     many transactions as it holds distinct 4-byte words; identical words are
     broadcast.  Returns the sum over phases of the worst bank (at least one
     per phase with an active lane).
     """
-    if width_bytes not in (4, 8, 16):
-        raise ValueError("width must be 4, 8 or 16 bytes")
+    if width_bytes not in (2, 4, 8, 16):
+        raise ValueError("width must be 2, 4, 8 or 16 bytes")
     lanes = list(byte_addresses)
-    per_phase = 128 // width_bytes
+    per_phase = min(32, 128 // width_bytes)
     total = 0
     for p in range(0, len(lanes), per_phase):
         words_in_bank = {}
@@ -169,7 +181,7 @@ def wavefronts(byte_addresses, width_bytes: int = 4) -> int:
             if addr % width_bytes:
                 raise ValueError("misaligned shared-memory access")
             active = True
-            for w in range(width_bytes // BANK_BYTES):
+            for w in range(max(1, width_bytes // BANK_BYTES)):
                 word = addr // BANK_BYTES + w
                 words_in_bank.setdefault(bank(word), set()).add(word)
         if active:
@@ -180,7 +192,7 @@ def wavefronts(byte_addresses, width_bytes: int = 4) -> int:
 def ideal_wavefronts(byte_addresses, width_bytes: int = 4) -> int:
     """Transactions the same access would need with no bank conflict."""
     lanes = list(byte_addresses)
-    per_phase = 128 // width_bytes
+    per_phase = min(32, 128 // width_bytes)
     return sum(1 for p in range(0, len(lanes), per_phase)
                if any(a is not None for a in lanes[p:p + per_phase]))
 

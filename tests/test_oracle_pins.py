@@ -414,3 +414,23 @@ def test_mixed_rejects_unknown_dtype():
     with pytest.raises(RuntimeError):
         oracle.gemm_mixed_general(3, np.zeros(4, np.uint16), np.zeros(4, np.uint16),
                                   np.zeros(4, np.float32), 2, 2, 2, 2, 2, 2, lib=LIB)
+
+
+def test_fp16_bank_formula_and_simulator():
+    data = golden("fp16_banks.json")
+    got = [R.element_bank(i, data["element_bytes"]) for i in data["indices"]]
+    assert got == data["banks"]
+    assert all(R.element_bank(i, 2) == i // 2 % 32 for i in range(4096))
+    assert all(R.element_bank(i, 4) == R.bank(i) for i in range(4096))
+    # 32 lanes reading consecutive fp16 elements touch 16 words, two lanes
+    # per word: one transaction with the same-word broadcast (the page's
+    # "may cause 2-way conflicts" does not arise); reading them as half2
+    # (4 bytes per lane) is one transaction too.
+    assert R.wavefronts([2 * t for t in range(32)], 2) == 1
+    assert R.wavefronts([4 * t for t in range(32)], 4) == 1
+    # A column of a [rows][64] fp16 tile (128-byte rows): every lane in one
+    # bank, 32 distinct words, 32-way; a row pitch of 66 halves (33 words,
+    # the padding rule on the word count) makes it conflict-free.
+    assert R.conflict_degree([128 * t for t in range(32)], 2) == 32
+    assert R.conflict_degree([132 * t for t in range(32)], 2) == 1
+    assert R.row_padding(64 // 2, 32) == 1 and R.row_padding(66 // 2, 32) == 0
