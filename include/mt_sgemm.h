@@ -90,7 +90,9 @@ typedef struct {
                          returns MT_ERR_TIMEOUT. */
     int wm;        /* FFMA warp tile rows; 0 = automatic */
     int wn;        /* FFMA warp tile columns; 0 = automatic */
-    int reserved[1];
+    int tm;        /* FFMA outputs per thread along M; 0 = automatic */
+    int tn;        /* FFMA outputs per thread along N; 0 = automatic */
+    int reserved[2];
 } mt_config;
 
 /* What a call with the same arguments would launch. */

@@ -54,7 +54,7 @@ class mt_config(ctypes.Structure):
                 ("bk", ctypes.c_int), ("stages", ctypes.c_int), ("no_pad", ctypes.c_int),
                 ("split_k", ctypes.c_int), ("fma", ctypes.c_int),
                 ("fault_inject", ctypes.c_int), ("wm", ctypes.c_int), ("wn", ctypes.c_int),
-                ("reserved", ctypes.c_int * 1)]
+                ("tm", ctypes.c_int), ("tn", ctypes.c_int), ("reserved", ctypes.c_int * 2)]
 
 
 class mt_plan(ctypes.Structure):
@@ -134,7 +134,7 @@ def lib():
 
 
 def make_config(variant="ffma", bm=0, bn=0, bk=0, stages=0, no_pad=False, split_k=0,
-                fma=0, fault_inject=0, wm=0, wn=0) -> mt_config:
+                fma=0, fault_inject=0, wm=0, wn=0, tm=0, tn=0) -> mt_config:
     c = mt_config()
     c.variant = VARIANTS[variant] if isinstance(variant, str) else int(variant)
     c.bm, c.bn, c.bk, c.stages = bm, bn, bk, stages
@@ -143,6 +143,7 @@ def make_config(variant="ffma", bm=0, bn=0, bk=0, stages=0, no_pad=False, split_
     c.fma = fma
     c.fault_inject = fault_inject
     c.wm, c.wn = wm, wn
+    c.tm, c.tn = tm, tn
     return c
 
 

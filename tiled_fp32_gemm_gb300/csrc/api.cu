@@ -171,8 +171,8 @@ mt_status check_problem(const Problem& P) {
 int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms) {
   int count = 0;
   const mt::FfmaEntry* e = mt::ffma_entries(&count);
-  const bool explicit_tile =
-      cfg && (cfg->bm || cfg->bn || cfg->bk || cfg->stages || cfg->wm || cfg->wn);
+  const bool explicit_tile = cfg && (cfg->bm || cfg->bn || cfg->bk || cfg->stages || cfg->wm ||
+                                     cfg->wn || cfg->tm || cfg->tn);
   const int want_packed = cfg && cfg->fma ? (cfg->fma == 2 ? 1 : 0) : 1;
   if (explicit_tile || (cfg && cfg->fma)) {
     for (int i = 0; i < count; ++i) {
@@ -182,6 +182,8 @@ int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms) {
       if (cfg->stages && e[i].stages != cfg->stages) continue;
       if (cfg->wm && e[i].wm != cfg->wm) continue;
       if (cfg->wn && e[i].wn != cfg->wn) continue;
+      if (cfg->tm && e[i].tm != cfg->tm) continue;
+      if (cfg->tn && e[i].tn != cfg->tn) continue;
       if (e[i].packed != want_packed) continue;
       if (!explicit_tile && !(e[i].bm == 128 && e[i].bn == 128 && e[i].stages == 3)) continue;
       return i;
@@ -284,7 +286,8 @@ mt_status plan_f16(const Problem& P, const mt_config* cfg, int64_t smem_limit, i
   if (P.dtype != MT_DTYPE_F16 && P.dtype != MT_DTYPE_BF16) return MT_ERR_INVALID_ARG;
   if (cfg && cfg->variant != MT_VARIANT_FFMA && cfg->variant != MT_VARIANT_TC16)
     return MT_ERR_UNSUPPORTED;
-  if (cfg && (cfg->wm || cfg->wn || cfg->fma || cfg->no_pad || cfg->split_k > 1))
+  if (cfg && (cfg->wm || cfg->wn || cfg->tm || cfg->tn || cfg->fma || cfg->no_pad ||
+              cfg->split_k > 1))
     return MT_ERR_UNSUPPORTED;
   const int64_t M = P.M, N = P.N, K = P.K;
   const int bk = mt::f16tc_bk();
@@ -343,11 +346,12 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   if (cfg && (cfg->bm < 0 || cfg->bn < 0 || cfg->bk < 0 || cfg->stages < 0 ||
               cfg->no_pad < 0 || cfg->no_pad > 1 || cfg->split_k < 0 || cfg->fma < 0 ||
               cfg->fma > 2 || cfg->fault_inject < 0 || cfg->fault_inject > 1 || cfg->wm < 0 ||
-              cfg->wn < 0))
+              cfg->wn < 0 || cfg->tm < 0 || cfg->tn < 0))
     return MT_ERR_INVALID_ARG;
   if (P.dtype) return plan_f16(P, cfg, smem_limit, sms, pair_clusters, L);
   if (variant == MT_VARIANT_TC16) return MT_ERR_UNSUPPORTED;  // 16-bit inputs only
-  if (cfg && (cfg->wm || cfg->wn) && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
+  if (cfg && (cfg->wm || cfg->wn || cfg->tm || cfg->tn) && variant != MT_VARIANT_FFMA)
+    return MT_ERR_UNSUPPORTED;
   if (cfg && cfg->fault_inject && variant != MT_VARIANT_TF32X3) return MT_ERR_UNSUPPORTED;
   // 3xTF32 splits only its tail by itself (split_k = 1 turns that off).
   if (cfg && cfg->split_k > 1 && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
