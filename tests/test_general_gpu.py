@@ -17,8 +17,8 @@ pytestmark = pytest.mark.gpu
 
 VARIANTS = [(dict(), 1e-5), (dict(bm=128, bn=128), 1e-5), (dict(bm=64, bn=64), 1e-5),
             (dict(variant="p18"), 1e-5), (dict(variant="tf32x3"), 5e-5),
-            (dict(variant="tf32x3", bn=64), 5e-5)]
-VIDS = ["ffma", "ffma128", "ffma64", "p18", "tf32x3", "tf32x3-bn64"]
+            (dict(variant="tf32x3", bn=64), 5e-5), (dict(variant="tf32x3", bm=256), 5e-5)]
+VIDS = ["ffma", "ffma128", "ffma64", "p18", "tf32x3", "tf32x3-bn64", "tf32x3-pair"]
 
 
 @pytest.fixture(scope="module", autouse=True)

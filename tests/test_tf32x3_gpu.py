@@ -47,10 +47,16 @@ def assert_within(C, Cref, W, tol, what=""):
                     f"max err/W {(err / np.maximum(W, 1e-300)).max():.3g}")
 
 
-# Every configuration the kernel is built for: K depth 16 (64-byte swizzle)
-# or 32 (128-byte swizzle) x tile width 256, 128 or 64.
-DEPTHS = [dict(variant="tf32x3", bk=bk, bn=bn) for bk in (16, 32) for bn in (256, 128, 64)]
+# Every configuration the kernel is built for: one CTA per 128 x bn tile,
+# K depth 16 (64-byte swizzle) or 32 (128-byte swizzle) x tile width 256,
+# 128 or 64; and CTA pairs on 256 x 256 tiles with K depth 16 or 32.
+DEPTHS = [dict(variant="tf32x3", bm=128, bk=bk, bn=bn) for bk in (16, 32)
+          for bn in (256, 128, 64)]
 DEPTH_IDS = [f"bk{c['bk']}-bn{c['bn']}" for c in DEPTHS]
+PAIRS = [dict(variant="tf32x3", bm=256, bk=bk) for bk in (16, 32)]
+PAIR_IDS = [f"pair-bk{c['bk']}" for c in PAIRS]
+ALL = DEPTHS + PAIRS
+ALL_IDS = DEPTH_IDS + PAIR_IDS
 
 
 @pytest.mark.parametrize("cfg", DEPTHS, ids=DEPTH_IDS)
@@ -70,10 +76,24 @@ def test_plan_reports_tile_and_workspace(cfg):
     units = tiles + (p["split_k"] - 1) * rem if p["split_k"] > 1 else tiles
     assert p["grid"] == min(units, sms)  # persistent: one CTA per SM at most
     auto = mt.plan(4096, 4096, 4096, variant="tf32x3")
-    assert (auto["bn"], auto["bk"]) == (256, 16)  # the automatic choice for large squares
+    # The automatic choice for large squares: CTA pairs, K depth 16.
+    assert (auto["bm"], auto["bn"], auto["bk"]) == (256, 256, 16)
 
 
-@pytest.mark.parametrize("cfg", DEPTHS, ids=DEPTH_IDS)
+@pytest.mark.parametrize("cfg", PAIRS, ids=PAIR_IDS)
+def test_pair_plan_reports_tile_and_workspace(cfg):
+    p = mt.plan(4096, 4096, 4096, **cfg)
+    assert (p["bm"], p["bn"], p["bk"], p["threads"]) == (256, 256, cfg["bk"], 192)
+    # Both operands packed in 128-row blocks (big and small): 2 x 4 bytes
+    # per element of A and of B, plus the split tail's 256 x 256 partials.
+    tiles = 16 * 16
+    clusters = p["grid"] // 2
+    rem = tiles % clusters if tiles > clusters else 0
+    partial = rem * p["split_k"] * 256 * 256 * 4 if p["split_k"] > 1 else 0
+    assert p["workspace_bytes"] == 2 * 2 * 4096 * 4096 * 4 + partial
+
+
+@pytest.mark.parametrize("cfg", ALL, ids=ALL_IDS)
 @pytest.mark.parametrize("name", ["masked_100x72x80", "square_1024", "ragged_4097x3001x2053"])
 def test_workloads_full_oracle(name, cfg):
     A, B = gemm_inputs.make_workload(name)
@@ -82,11 +102,12 @@ def test_workloads_full_oracle(name, cfg):
 
 
 @pytest.mark.parametrize("split", [0, 1], ids=["auto-split-tail", "no-split"])
+@pytest.mark.parametrize("tile", [0, 128], ids=["auto", "single"])
 @pytest.mark.parametrize("name", ["square_4096", "square_8192", "skinny_65536x128x4096"])
-def test_full_size_sampled_rows(name, split):
+def test_full_size_sampled_rows(name, split, tile):
     w = gemm_inputs.WORKLOADS[name]
     A, B = gemm_inputs.make_workload(w)
-    c = mt.sgemm(A.cuda(), B.cuda(), split_k=split, **TF32)
+    c = mt.sgemm(A.cuda(), B.cuda(), split_k=split, bm=tile, **TF32)
     torch.cuda.synchronize()
     g = np.random.default_rng(1)
     rows = np.unique(np.concatenate([[0, w.M - 1, 127, 128, 255, 256],
@@ -95,7 +116,7 @@ def test_full_size_sampled_rows(name, split):
     assert_within(c[torch.from_numpy(rows).cuda()].cpu().numpy(), Cr, Wr, TOL, name)
 
 
-@pytest.mark.parametrize("cfg", DEPTHS, ids=DEPTH_IDS)
+@pytest.mark.parametrize("cfg", ALL, ids=ALL_IDS)
 @pytest.mark.parametrize("shape", [(100, 72, 80), (257, 130, 77), (128, 256, 96),
                                    (300, 520, 1000)])
 def test_integer_inputs_bit_exact(shape, cfg):
@@ -113,7 +134,7 @@ def test_tiny_ragged(shape):
     M, N, K = shape
     A, B = gemm_inputs.make_ab(M, N, K, seed=M * 7 + N * 3 + K, dist="normal")
     Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
-    for cfg in DEPTHS:
+    for cfg in ALL:
         assert_within(run(A, B, **cfg).numpy(), Cref, W, TOL, f"{shape} {cfg}")
 
 
@@ -163,14 +184,15 @@ def test_device_status_clean_after_runs():
     assert mt.mt_device_status(0) == mt.MT_OK
 
 
-def test_timeout_path_reports_and_context_survives():
-    """The copy thread issues nothing: every bounded wait runs out (about a
+@pytest.mark.parametrize("tile", [128, 256], ids=["single", "pair"])
+def test_timeout_path_reports_and_context_survives(tile):
+    """The copy threads issue nothing: every bounded wait runs out (about a
     second), the kernel records the timeout and returns; the context stays
     usable for the next call."""
     A, B = gemm_inputs.make_workload("masked_100x72x80")
     a, b = A.cuda(), B.cuda()
     c = torch.full((100, 72), 7.0, device="cuda")
-    mt.sgemm(a, b, out=c, variant="tf32x3", fault_inject=1)
+    mt.sgemm(a, b, out=c, variant="tf32x3", fault_inject=1, bm=tile)
     assert mt.mt_device_status(0) == mt.MT_ERR_TIMEOUT
     assert torch.all(c == 7.0)  # nothing written
     assert mt.mt_device_status(0) == mt.MT_OK  # the status word was cleared
@@ -183,18 +205,19 @@ def test_split_tail_plan_and_parity():
     # 512 tiles of 128 x 256 on one CTA per SM leave a partial last round;
     # its tiles are cut into K slices whose partials a second kernel adds.
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    p = mt.plan(4096, 4096, 4096, variant="tf32x3")
+    p = mt.plan(4096, 4096, 4096, variant="tf32x3", bm=128)
     rem = 512 % sms
     if 0 < 2 * rem <= sms:
         assert p["split_k"] == min(sms // rem, 4)
     # 32 x 5 = 160 tiles: 152 in the first round, 8 split into 4 K slices.
     M, N, K = 4096, 1280, 520
-    q = mt.plan(M, N, K, variant="tf32x3")
+    q = mt.plan(M, N, K, variant="tf32x3", bm=128)
     if sms == 152:
         assert (q["bn"], q["split_k"]) == (256, 4)
     A, B = gemm_inputs.make_ab(M, N, K, seed=24, dist="normal")
     rows = np.array([0, 1, 127, 128, 2047, 3968, 4095])
     Cr, Wr = oracle.sgemm_rows(A.numpy(), B.numpy(), rows, with_w=True)
-    got = run(A, B, **TF32).numpy()[rows]
-    assert_within(got, Cr, Wr, TOL, "split tail")
-    assert np.array_equal(run(A, B, **TF32).numpy()[rows], got)  # deterministic
+    for cfg in (dict(bm=128), dict(bm=256)):
+        got = run(A, B, **TF32, **cfg).numpy()[rows]
+        assert_within(got, Cr, Wr, TOL, f"split tail {cfg}")
+        assert np.array_equal(run(A, B, **TF32, **cfg).numpy()[rows], got)  # deterministic

@@ -335,8 +335,10 @@ mt_status plan_f16(const Problem& P, const mt_config* cfg, int64_t smem_limit, i
 
 // Pointers are only inspected for alignment here (NULL counts as aligned);
 // check_problem checks them against the sizes.
+// dev: the current device (-1 without one), asked for the resident-cluster
+// count of the CTA-pair kernels.
 mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, int sms,
-                    Launch* L, int pair_clusters = 0) {
+                    Launch* L, int dev = -1) {
   const int64_t M = P.M, N = P.N, K = P.K;
   mt_status st = check_dims(M, N, K);
   if (st != MT_OK) return st;
@@ -348,7 +350,9 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
               cfg->fma > 2 || cfg->fault_inject < 0 || cfg->fault_inject > 1 || cfg->wm < 0 ||
               cfg->wn < 0 || cfg->tm < 0 || cfg->tn < 0))
     return MT_ERR_INVALID_ARG;
-  if (P.dtype) return plan_f16(P, cfg, smem_limit, sms, pair_clusters, L);
+  if (P.dtype)
+    return plan_f16(P, cfg, smem_limit, sms, dev >= 0 ? mt::f16tc_pair_max_clusters(dev) : 0,
+                    L);
   if (variant == MT_VARIANT_TC16) return MT_ERR_UNSUPPORTED;  // 16-bit inputs only
   if (cfg && (cfg->wm || cfg->wn || cfg->tm || cfg->tn) && variant != MT_VARIANT_FFMA)
     return MT_ERR_UNSUPPORTED;
@@ -386,13 +390,19 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
     return MT_OK;
   }
   if (variant == MT_VARIANT_TF32X3) {
-    const int bm = mt::tf32x3_bm();
-    const int bn = cfg && cfg->bn ? cfg->bn : pick_tf32x3_bn(M, N, sms > 0 ? sms : 1);
-    const int bk = cfg && cfg->bk ? cfg->bk : tf32x3_default_bk(bn);
-    if (!mt::tf32x3_valid(bk, bn)) return MT_ERR_UNSUPPORTED;
-    const int stages = mt::tf32x3_stages(bk, bn);
-    if (cfg && ((cfg->bm && cfg->bm != bm) || (cfg->stages && cfg->stages != stages) ||
-                cfg->fma || cfg->no_pad))
+    const int want_bm = cfg ? cfg->bm : 0;
+    const int bn = cfg && cfg->bn ? cfg->bn
+                   : want_bm == 256 ? 256 : pick_tf32x3_bn(M, N, sms > 0 ? sms : 1);
+    // CTA pairs (256 x 256 tiles, K depth 16 unless asked) when the pair
+    // tiles fill the resident clusters, as for 16-bit inputs.
+    const int pair_clusters16 = dev >= 0 ? mt::tf32x3_pair_max_clusters(dev, 16) : 0;
+    const int bm = want_bm ? want_bm
+                           : auto_pair(M, N, bn, sms, pair_clusters16) ? 256 : mt::tf32x3_bm();
+    const bool pair = bm == 256;
+    const int bk = cfg && cfg->bk ? cfg->bk : pair ? 16 : tf32x3_default_bk(bn);
+    if (!mt::tf32x3_valid(bm, bk, bn)) return MT_ERR_UNSUPPORTED;
+    const int stages = mt::tf32x3_stages(bm, bk, bn);
+    if (cfg && ((cfg->stages && cfg->stages != stages) || cfg->fma || cfg->no_pad))
       return MT_ERR_UNSUPPORTED;
     p.bm = bm; p.bn = bn; p.bk = bk; p.stages = stages;
     p.threads = mt::tf32x3_threads();
@@ -403,15 +413,24 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
     L->vec_b = P.trans_b && K % 4 == 0 && P.ldb % 4 == 0 && aligned16(P.B);
     p.vec_ab = L->vec_a;
     p.vec_c = N % 4 == 0 && P.ldc % 4 == 0 && aligned16(P.C);
-    p.smem_bytes = mt::tf32x3_smem_bytes(bk, bn);
+    p.smem_bytes = mt::tf32x3_smem_bytes(bm, bk, bn);
     L->tiles_m = static_cast<int>(ceil_div(M, bm));
     L->tiles_n = static_cast<int>(ceil_div(N, bn));
-    if (L->tiles_m > 65535 || ceil_div(static_cast<int64_t>(L->tiles_n) * bn, 256) > 65535 ||
+    // Pack grids: up to 65535 blocks of rows per operand.
+    const int64_t blocks_m = pair ? 2 * L->tiles_m : L->tiles_m;
+    const int64_t blocks_n = pair ? 2 * L->tiles_n : L->tiles_n;
+    if (blocks_m > 65535 || blocks_n > 65535 ||
+        ceil_div(static_cast<int64_t>(L->tiles_n) * bn, 256) > 65535 ||
         ceil_div(static_cast<int64_t>(L->tiles_m) * bm, 256) > 65535)
       return MT_ERR_UNSUPPORTED;
-    // Persistent: one CTA per SM at most.
+    // Persistent: one CTA per SM, or one cluster of two per two SMs.
     const int64_t tiles = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
-    L->max_ctas = sms > 0 ? sms : 1;
+    if (pair) {
+      const int pc = dev >= 0 ? mt::tf32x3_pair_max_clusters(dev, bk) : 0;
+      L->max_ctas = pc > 0 ? pc : std::max(1, sms / 2);
+    } else {
+      L->max_ctas = sms > 0 ? sms : 1;
+    }
     // Split tail (split_k = 1 turns it off).
     const int64_t ctas = std::min<int64_t>(tiles, L->max_ctas);
     const int64_t ktiles = ceil_div(K, bk);
@@ -422,9 +441,9 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
     L->kt_per_slice = static_cast<int>(ceil_div(ktiles, split));
     p.split_k = L->split;
     const int64_t units = full + (tiles - full) * split;
-    p.grid = std::min<int64_t>(units, L->max_ctas);
+    p.grid = std::min<int64_t>(units, L->max_ctas) * (pair ? 2 : 1);
     p.workspace_bytes = mt::tf32x3_workspace_bytes(static_cast<int>(M), static_cast<int>(N),
-                                                   static_cast<int>(K), bk, bn) +
+                                                   static_cast<int>(K), bm, bk, bn) +
                         (tiles - full) * split * bm * bn * 4;
     if (p.smem_bytes > smem_limit) return MT_ERR_SMEM_BUDGET;
     return MT_OK;
@@ -518,16 +537,17 @@ mt_status pool_for(int dev, cudaMemPool_t* pool) {
 // [device][configuration]: shared-memory attribute of the 3xTF32 kernel applied.
 std::atomic<uint8_t> g_tf32x3_ready[kMaxDevices][8];
 
-int tf32x3_cfg_index(int bk, int bn) {
-  return (bk == 32 ? 4 : 0) + (bn == 256 ? 0 : bn == 128 ? 1 : 2);
+// [bk == 32][128 x 256, 128 x 128, 128 x 64, pair 256 x 256]
+int tf32x3_cfg_index(int bm, int bk, int bn) {
+  return (bk == 32 ? 4 : 0) + (bm == 256 ? 3 : bn == 256 ? 0 : bn == 128 ? 1 : 2);
 }
 
-mt_status prepare_tf32x3(int dev, int bk, int bn) {
-  std::atomic<uint8_t>& ready = g_tf32x3_ready[dev][tf32x3_cfg_index(bk, bn)];
+mt_status prepare_tf32x3(int dev, int bm, int bk, int bn) {
+  std::atomic<uint8_t>& ready = g_tf32x3_ready[dev][tf32x3_cfg_index(bm, bk, bn)];
   if (!ready.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!ready.load(std::memory_order_relaxed)) {
-      if (mt::tf32x3_prepare(dev, bk, bn) != cudaSuccess) {
+      if (mt::tf32x3_prepare(dev, bm, bk, bn) != cudaSuccess) {
         cudaGetLastError();
         return MT_ERR_LAUNCH;
       }
@@ -563,7 +583,7 @@ mt::GemmArgs make_args(const Problem& P, const Launch& L) {
 }
 
 mt_status run_tf32x3(int dev, const mt::GemmArgs& args, const Launch& L, cudaStream_t stream) {
-  mt_status st0 = prepare_tf32x3(dev, L.plan.bk, L.plan.bn);
+  mt_status st0 = prepare_tf32x3(dev, L.plan.bm, L.plan.bk, L.plan.bn);
   if (st0 != MT_OK) return st0;
   cudaMemPool_t pool = nullptr;
   mt_status st = pool_for(dev, &pool);
@@ -575,8 +595,8 @@ mt_status run_tf32x3(int dev, const mt::GemmArgs& args, const Launch& L, cudaStr
     return MT_ERR_CUDA;
   }
   const cudaError_t e =
-      mt::launch_tf32x3(args, ws, L.vec_a, L.vec_b, L.plan.vec_c != 0, L.plan.bk, L.plan.bn,
-                        L.max_ctas, L.fault_inject, stream);
+      mt::launch_tf32x3(args, ws, L.vec_a, L.vec_b, L.plan.vec_c != 0, L.plan.bm, L.plan.bk,
+                        L.plan.bn, L.max_ctas, L.fault_inject, stream);
   cudaFreeAsync(ws, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -635,8 +655,7 @@ mt_status run(const Problem& P, cudaStream_t stream, const mt_config* cfg) {
   st = current_device(&dev, &info);
   if (st != MT_OK) return st;
   Launch L;
-  st = plan_call(P, cfg, info.smem_optin, info.sms, &L,
-                 P.dtype ? mt::f16tc_pair_max_clusters(dev) : 0);
+  st = plan_call(P, cfg, info.smem_optin, info.sms, &L, dev);
   if (st != MT_OK) return st;
   if (!reads_ab(P)) {
     // No product to form (K == 0: the accumulator's zeros; alpha == 0):
@@ -759,7 +778,7 @@ mt_status mt_sgemm_tf32x3_noalloc(const float* A, const float* B, float* C, int6
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.variant = MT_VARIANT_TF32X3;
   Launch L;
-  st = plan_call(P, &cfg, info.smem_optin, info.sms, &L);
+  st = plan_call(P, &cfg, info.smem_optin, info.sms, &L, dev);
   if (st != MT_OK) return st;
   if (K == 0) {
     // Empty reduction: zeros, written without any scratch.
@@ -770,7 +789,7 @@ mt_status mt_sgemm_tf32x3_noalloc(const float* A, const float* B, float* C, int6
     return MT_OK;
   }
   if (L.plan.workspace_bytes > MT_NOALLOC_SCRATCH_BYTES) return MT_ERR_SCRATCH_LIMIT;
-  st = prepare_tf32x3(dev, L.plan.bk, L.plan.bn);
+  st = prepare_tf32x3(dev, L.plan.bm, L.plan.bk, L.plan.bn);
   if (st != MT_OK) return st;
   void* scratch = nullptr;
   if (mt::tf32x3_noalloc_scratch(dev, &scratch) != cudaSuccess || !scratch) {
@@ -778,8 +797,8 @@ mt_status mt_sgemm_tf32x3_noalloc(const float* A, const float* B, float* C, int6
     return MT_ERR_CUDA;
   }
   const mt::GemmArgs args = make_args(P, L);
-  if (mt::launch_tf32x3(args, scratch, L.vec_a, L.vec_b, L.plan.vec_c != 0, L.plan.bk,
-                        L.plan.bn, L.max_ctas, 0, stream) != cudaSuccess) {
+  if (mt::launch_tf32x3(args, scratch, L.vec_a, L.vec_b, L.plan.vec_c != 0, L.plan.bm,
+                        L.plan.bk, L.plan.bn, L.max_ctas, 0, stream) != cudaSuccess) {
     cudaGetLastError();
     return MT_ERR_LAUNCH;
   }
@@ -848,8 +867,8 @@ mt_status mt_gemm_mixed_plan(int dtype, int trans_a, int trans_b, int64_t M, int
     sms = current_device(&dev, &info) == MT_OK ? info.sms : 152;
   }
   Launch L;
-  const int clusters = current_device(&dev, &info) == MT_OK ? mt::f16tc_pair_max_clusters(dev) : 0;
-  mt_status st = plan_call(P, cfg, smem_limit_bytes, sms, &L, clusters);
+  mt_status st =
+      plan_call(P, cfg, smem_limit_bytes, sms, &L, current_device(&dev, &info) == MT_OK ? dev : -1);
   *out = L.plan;
   return st;
 }

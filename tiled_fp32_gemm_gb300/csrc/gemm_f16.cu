@@ -43,7 +43,6 @@
 #include <mutex>
 
 #include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "device_util.cuh"
@@ -476,42 +475,13 @@ namespace {
 using f16tc::BK;
 using f16tc::BM;
 
-// cuTensorMapEncodeTiled, looked up once from the driver through the
-// runtime (the library does not link the driver library itself).
-std::once_flag g_encode_once;
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-
-PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-  std::call_once(g_encode_once, [] {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    else
-      cudaGetLastError();
-  });
-  return g_encode;
-}
-
 // 2-D map of a stored rows x cols matrix of 16-bit values (row pitch ld
 // values), box of box_cols x box_rows, 128-byte swizzle, zero fill.
 bool encode_map(CUtensorMap* map, int dtype, const void* base, int64_t rows, int64_t cols,
                 int64_t ld, int box_cols, int box_rows) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols),
-                             static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapDataType t =
-      dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  return enc(map, t, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_tensor_map_2d(
+      map, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+      base, rows, cols, ld, box_cols, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // Operands TMA cannot read in place go through padded copies in the
@@ -794,7 +764,7 @@ cudaError_t f16tc_prepare(int bm, int bn) {
   return e;
 }
 
-bool f16tc_encoder_available() { return encoder() != nullptr; }
+bool f16tc_encoder_available() { return tensor_map_encoder_available(); }
 
 cudaError_t launch_f16tc(const GemmArgs& a, const F16Operands& f, void* workspace, bool vec_c,
                          int bm, int bn, int max_ctas, int fault_inject, cudaStream_t stream) {

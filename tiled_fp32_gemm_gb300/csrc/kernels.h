@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace mt {
@@ -69,23 +70,28 @@ int p18_pad_a(bool pad);
 int p18_smem_bytes(bool pad);
 
 // tcgen05 3xTF32 variant (sgemm_tf32x3.cu): persistent kernel over tiles of
-// 128 x bn (bn = 256, 128 or 64) with a K depth bk of 16 or 32 per stage.
-// A call needs a device workspace of tf32x3_workspace_bytes(M, N, K, bk, bn)
+// 128 x bn (bm = 128; bn = 256, 128 or 64) or, on CTA pairs, of 256 x 256
+// (bm = 256, bn = 256), with a K depth bk of 16 or 32 per stage.  A call
+// needs a device workspace of tf32x3_workspace_bytes(M, N, K, bm, bk, bn)
 // bytes (the packed, split, swizzled copies of A and B); launch_tf32x3 runs
-// the two pack kernels and the GEMM on at most max_ctas CTAs (one per SM).
-bool tf32x3_valid(int bk, int bn);
-int64_t tf32x3_workspace_bytes(int M, int N, int K, int bk, int bn);
-int tf32x3_smem_bytes(int bk, int bn);
-int tf32x3_stages(int bk, int bn);
+// the two pack kernels and the GEMM on at most max_ctas CTAs (one per SM;
+// bm = 256: clusters of two).
+bool tf32x3_valid(int bm, int bk, int bn);
+int64_t tf32x3_workspace_bytes(int M, int N, int K, int bm, int bk, int bn);
+int tf32x3_smem_bytes(int bm, int bk, int bn);
+int tf32x3_stages(int bm, int bk, int bn);
 int tf32x3_threads();
 int tf32x3_bm();
-cudaError_t tf32x3_prepare(int device, int bk, int bn);
+cudaError_t tf32x3_prepare(int device, int bm, int bk, int bn);
+// Clusters of two of the pair kernel resident at once on `device` (the
+// current device); 0 if the query fails.  Sets its shared-memory limit.
+int tf32x3_pair_max_clusters(int device, int bk);
 // vec_a / vec_b: that operand may be read with float4 by its packer (read
 // k-contiguous, leading dimension % 4 == 0, 16-byte aligned); vec_c: C may
-// be written with float4.  fault_inject = 1: the copy thread issues nothing
+// be written with float4.  fault_inject = 1: the copy threads issue nothing
 // (tests the bounded waits).
 cudaError_t launch_tf32x3(const GemmArgs& a, void* workspace, bool vec_a, bool vec_b,
-                          bool vec_c, int bk, int bn, int max_ctas, int fault_inject,
+                          bool vec_c, int bm, int bk, int bn, int max_ctas, int fault_inject,
                           cudaStream_t stream);
 // Size of the static scratch the allocation-free tf32x3 entry point uses,
 // and its device address on `device` (looked up once per device; the device
@@ -95,6 +101,16 @@ cudaError_t tf32x3_noalloc_scratch(int device, void** ptr);
 // Reads and zeroes the device status word of the tf32x3 kernels
 // (bit 0: a bounded wait expired).  Synchronous.
 cudaError_t tf32x3_read_and_clear_status(unsigned int* status);
+
+// ---------------------------------------------------------------------------
+// TMA tensor maps (tensor_map.cu).  A 2-D map of a rows x cols matrix of
+// elem_bytes-byte elements with row pitch ld elements, boxes of box_cols x
+// box_rows, zero fill outside the matrix.  false when the driver's encoder
+// is unavailable or rejects the arguments.
+bool tensor_map_encoder_available();
+bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, int elem_bytes,
+                          const void* base, int64_t rows, int64_t cols, int64_t ld,
+                          int box_cols, int box_rows, CUtensorMapSwizzle swizzle);
 
 // ---------------------------------------------------------------------------
 // tcgen05 kind::f16 kernel on 16-bit inputs (gemm_f16.cu).  GemmArgs carries

@@ -358,6 +358,191 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair kernel: a cluster of two CTAs on two SMs computes 256 x 256 tiles
+// with tcgen05.mma.cta_group::2 kind::tf32.  Both operands are packed in
+// 128-row blocks; CTA r of the pair stages block 2*t + r of A's tile row t
+// and of B's tile column, each K tile's (big, small) pair arriving by one
+// TMA copy that completes on the even CTA's full barrier.  The even CTA issues
+// 3 pair MMAs (256 x 256 x 8) per k8 step and commits to both CTAs' barriers;
+// each CTA's epilogue drains its 128 rows x 256 columns of TMEM.  Roles,
+// bounded waits and the exit protocol as the 16-bit pair kernel.
+constexpr int PAIR_TILE = 256;
+constexpr int PAIR_HALF = 128;
+
+template <int BK_>
+struct PairGeometry {
+  static constexpr int BK = BK_;
+  static constexpr int ROW_BYTES = BK * 4;
+  static constexpr int ATOM_BYTES = 8 * ROW_BYTES;
+  static constexpr uint64_t LAYOUT = BK == 32 ? 2 : 4;  // 128-B / 64-B swizzle
+  static constexpr int BLOCK_BYTES = PAIR_HALF * ROW_BYTES;
+  static constexpr int PAIR_BYTES = 2 * BLOCK_BYTES;  // big | small of one 128-row block
+  static constexpr int STAGE_BYTES = 2 * PAIR_BYTES;  // A pair | B pair
+  static constexpr int STAGES_FIT = SMEM_STAGE_BUDGET / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static_assert(STAGES >= 2, "at least two stages");
+  static constexpr uint32_t TMEM_COLS = 2 * PAIR_TILE;  // two accumulators
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  // The packed buffers seen as 2-D tensors of 1 KB rows: one TMA box of
+  // PAIR_ROWS rows is one block pair.
+  static constexpr int PAIR_ROWS = PAIR_BYTES / 1024;
+};
+
+template <int BK>
+__global__ void __launch_bounds__(THREADS, 1)
+    tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                       const __grid_constant__ CUtensorMap tmap_b, Epilogue ep, int Kt,
+                       int tiles_m, int tiles_n, int group_m, Sched sched, int fault_inject) {
+  using G = PairGeometry<BK>;
+  constexpr int STAGES = G::STAGES;
+  constexpr int STAGE_BYTES = G::STAGE_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  constexpr int FULL = 0, EMPTY = STAGES, ACC_FULL = 2 * STAGES, ACC_EMPTY = 2 * STAGES + 2,
+                DRAIN = 2 * STAGES + 4, NBARS = 2 * STAGES + 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const WaitCtx wc{abort_flag, &g_status};
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cluster = static_cast<int>(cluster_id_x());
+  const int clusters = static_cast<int>(cluster_count_x());
+  const int num_tiles = tiles_m * tiles_n;
+  const int num_units = sched.full_tiles + (num_tiles - sched.full_tiles) * sched.split;
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmap_a);
+    prefetch_tmap(&tmap_b);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(FULL + s), 1);
+      mbar_init(bar(EMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(ACC_FULL + b), 1);
+      mbar_init(bar(ACC_EMPTY + b), 8);  // one arrival per epilogue warp of both CTAs
+    }
+    mbar_init(bar(DRAIN), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), G::TMEM_COLS);
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool stop = fault_inject != 0;
+      uint32_t g = 0;
+      const uint32_t full_even0 = map_to_cta(bar(FULL), 0);
+      for (int u = cluster; u < num_units && !stop; u += clusters) {
+        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+        const int blk_a = 2 * w.tm + static_cast<int>(rank);
+        const int blk_b = 2 * w.tn + static_cast<int>(rank);
+        for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
+          const uint32_t s = g % STAGES, round = g / STAGES;
+          if (g >= STAGES && !wait_phase(bar(EMPTY + s), (round + 1) & 1u, wc)) {
+            stop = true;
+            break;
+          }
+          const uint32_t full_even = full_even0 + 8u * s;
+          if (leader) mbar_arrive_expect_tx(bar(FULL + s), 2 * STAGE_BYTES);
+          const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
+          tma_load_2d_pair(st, &tmap_a, 0, (blk_a * Kt + kt) * G::PAIR_ROWS, full_even);
+          tma_load_2d_pair(st + G::PAIR_BYTES, &tmap_b, 0, (blk_b * Kt + kt) * G::PAIR_ROWS,
+                           full_even);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = instr_desc(PAIR_TILE, PAIR_TILE, 2, 2);  // tf32 x tf32
+      uint32_t g = 0;
+      bool stop = false;
+      int it = 0;
+      for (int u = cluster; u < num_units && !stop; u += clusters, ++it) {
+        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+        const int b = it & 1;
+        if (it >= 2 && !wait_phase(bar(ACC_EMPTY + b), ((it >> 1) + 1) & 1u, wc)) break;
+        tc_fence_after();
+        const uint32_t acc_tmem = tmem + static_cast<uint32_t>(b * PAIR_TILE);
+        uint32_t acc = 0;
+        for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
+          const uint32_t s = g % STAGES, round = g / STAGES;
+          if (!wait_phase(bar(FULL + s), round & 1u, wc)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_big = smem_u32(smem + s * STAGE_BYTES);
+          const uint32_t a_small = a_big + G::BLOCK_BYTES;
+          const uint32_t b_big = a_big + G::PAIR_BYTES;
+          const uint32_t b_small = b_big + G::BLOCK_BYTES;
+#pragma unroll
+          for (int j = 0; j < BK / 8; ++j) {
+            const uint32_t koff = j * 32;  // 8 tf32 = 32 bytes along K
+            const uint64_t ab = smem_desc(a_big + koff, 16, G::ATOM_BYTES, G::LAYOUT);
+            const uint64_t as = smem_desc(a_small + koff, 16, G::ATOM_BYTES, G::LAYOUT);
+            const uint64_t bb = smem_desc(b_big + koff, 16, G::ATOM_BYTES, G::LAYOUT);
+            const uint64_t bs = smem_desc(b_small + koff, 16, G::ATOM_BYTES, G::LAYOUT);
+            mma_tf32_pair(acc_tmem, ab, bs, idesc, acc);
+            acc = 1;
+            mma_tf32_pair(acc_tmem, as, bb, idesc, 1);
+            mma_tf32_pair(acc_tmem, ab, bb, idesc, 1);
+          }
+          mma_commit_pair(bar(EMPTY + s), 0x3);
+        }
+        if (!stop) mma_commit_pair(bar(ACC_FULL + b), 0x3);
+      }
+      mma_commit_pair(bar(DRAIN), 0x1);
+      wait_phase(bar(DRAIN), 0, wc, false);
+    }
+  } else {
+    const int q = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t acc_empty_even = map_to_cta(bar(ACC_EMPTY), 0);
+    int it = 0;
+    for (int u = cluster; u < num_units; u += clusters, ++it) {
+      const int b = it & 1;
+      const bool ready = wait_phase(bar(ACC_FULL + b), (it >> 1) & 1u, wc, true,
+                                    TIMEOUT_NS + 20000ull * static_cast<uint64_t>(Kt));
+      if (!__all_sync(0xffffffffu, ready)) break;
+      tc_fence_after();
+      __syncwarp();
+      const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      store_accumulator<PAIR_HALF, PAIR_TILE, PAIR_TILE>(
+          tmem + lane_base + static_cast<uint32_t>(b * PAIR_TILE), w, q, lane, ep,
+          sched.partial, static_cast<int>(rank) * PAIR_HALF);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty_even + 8u * static_cast<uint32_t>(b));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // Copies this CTA issued complete on the even CTA's barriers, which it
+    // cannot wait on: give any still in flight time to land (bounded).
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 200000ull) {
+    }
+  }
+  cluster_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, G::TMEM_COLS);
+  }
+}
+
 }  // namespace tf32x3
 
 // ---------------------------------------------------------------------------
@@ -426,6 +611,113 @@ struct Cfg {
   }
 };
 
+// CTA-pair configuration (256 x 256 tiles), K depth BK.
+template <int BK>
+struct CfgPair {
+  using G = tf32x3::PairGeometry<BK>;
+  using GP = tf32x3::Geometry<BK, 128>;  // packing in 128-row blocks
+  static constexpr int ROWS = tf32x3::PAIR_HALF;
+
+  static int64_t workspace(int M, int N, int K) {
+    const int64_t mt = (M + 255) / 256, nt = (N + 255) / 256, kt = (K + BK - 1) / BK;
+    return (2 * mt + 2 * nt) * kt * G::PAIR_BYTES;
+  }
+  static cudaError_t prepare() {
+    return cudaFuncSetAttribute(tf32x3::tf32x3_pair_kernel<BK>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
+  }
+  static int max_clusters() {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(tf32x3::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = G::SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(
+                                               tf32x3::tf32x3_pair_kernel<BK>),
+                                       &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return n;
+  }
+  static cudaError_t launch(const GemmArgs& a, void* workspace, bool vec_a, bool vec_b,
+                            bool vec_c, int max_clusters, int fault_inject, cudaStream_t stream) {
+    using namespace tf32x3;
+    const int mt = (a.M + PAIR_TILE - 1) / PAIR_TILE, nt = (a.N + PAIR_TILE - 1) / PAIR_TILE;
+    const int kt = (a.K + BK - 1) / BK;
+    if (2 * mt > 65535 || 2 * nt > 65535) return cudaErrorInvalidValue;
+    float* Ap = static_cast<float*>(workspace);
+    float* Bp = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         static_cast<int64_t>(2 * mt) * kt * G::PAIR_BYTES);
+    if (a.trans_a)
+      pack_rc_kernel<GP, ROWS><<<dim3(kt, (2 * mt * ROWS + 255) / 256), 256, 0, stream>>>(
+          a.A, a.lda, Ap, a.M, a.K, kt, 2 * mt);
+    else
+      pack_kc_kernel<GP, ROWS><<<dim3(kt, 2 * mt), 256, 0, stream>>>(a.A, a.lda, Ap, a.M, a.K,
+                                                                     kt, vec_a ? 1 : 0);
+    if (a.trans_b)
+      pack_kc_kernel<GP, ROWS><<<dim3(kt, 2 * nt), 256, 0, stream>>>(a.B, a.ldb, Bp, a.N, a.K,
+                                                                     kt, vec_b ? 1 : 0);
+    else
+      pack_rc_kernel<GP, ROWS><<<dim3(kt, (2 * nt * ROWS + 255) / 256), 256, 0, stream>>>(
+          a.B, a.ldb, Bp, a.N, a.K, kt, 2 * nt);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // The packed buffers as 2-D tensors of 1 KB rows (256 floats, no
+    // swizzle: the blocks are already in the tensor core's order).
+    CUtensorMap map_a, map_b;
+    const int64_t rows_a = static_cast<int64_t>(2 * mt) * kt * G::PAIR_ROWS;
+    const int64_t rows_b = static_cast<int64_t>(2 * nt) * kt * G::PAIR_ROWS;
+    if (!encode_tensor_map_2d(&map_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Ap, rows_a, 256, 256,
+                              256, G::PAIR_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tensor_map_2d(&map_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Bp, rows_b, 256, 256,
+                              256, G::PAIR_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+    const int tiles = mt * nt;
+    Sched sched{a.full_tiles, a.split, a.kt_per_slice, nullptr};
+    if (a.split > 1)
+      sched.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                CfgPair::workspace(a.M, a.N, a.K));
+    const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
+    const int clusters = units < max_clusters ? units : max_clusters;
+    const Epilogue ep{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0};
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = G::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int kt_arg = kt, mt_arg = mt, nt_arg = nt, group_m = a.group_m, fi = fault_inject;
+    Epilogue ep_arg = ep;
+    void* args[] = {&map_a, &map_b, &ep_arg, &kt_arg, &mt_arg, &nt_arg, &group_m, &sched, &fi};
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(tf32x3_pair_kernel<BK>), args);
+    if (e != cudaSuccess || a.split <= 1) return e;
+    GemmArgs r = a;
+    r.partial = sched.partial;
+    return launch_splitk_reduce(r, PAIR_TILE, PAIR_TILE, vec_c, stream);
+  }
+};
+
+template <class F>
+bool dispatch_pair(int bk, F&& f) {
+  if (bk == 16) { f(CfgPair<16>{}); return true; }
+  if (bk == 32) { f(CfgPair<32>{}); return true; }
+  return false;
+}
+
 // Calls f.template operator()<BK, BN>() for the runtime choice; false when
 // the pair is not built.
 template <class F>
@@ -441,42 +733,82 @@ bool dispatch(int bk, int bn, F&& f) {
 
 }  // namespace
 
-bool tf32x3_valid(int bk, int bn) {
-  return dispatch(bk, bn, [](auto) {});
+bool tf32x3_valid(int bm, int bk, int bn) {
+  if (bm == tf32x3::PAIR_TILE) return bn == tf32x3::PAIR_TILE && dispatch_pair(bk, [](auto) {});
+  return bm == tf32x3::BM && dispatch(bk, bn, [](auto) {});
 }
 
-int64_t tf32x3_workspace_bytes(int M, int N, int K, int bk, int bn) {
+int64_t tf32x3_workspace_bytes(int M, int N, int K, int bm, int bk, int bn) {
   int64_t r = -1;
-  dispatch(bk, bn, [&](auto c) { r = decltype(c)::workspace(M, N, K); });
+  if (bm == tf32x3::PAIR_TILE)
+    dispatch_pair(bk, [&](auto c) { r = decltype(c)::workspace(M, N, K); });
+  else
+    dispatch(bk, bn, [&](auto c) { r = decltype(c)::workspace(M, N, K); });
   return r;
 }
 
-int tf32x3_smem_bytes(int bk, int bn) {
+int tf32x3_smem_bytes(int bm, int bk, int bn) {
   int r = -1;
-  dispatch(bk, bn, [&](auto c) { r = decltype(c)::G::SMEM_BYTES; });
+  if (bm == tf32x3::PAIR_TILE)
+    dispatch_pair(bk, [&](auto c) { r = decltype(c)::G::SMEM_BYTES; });
+  else
+    dispatch(bk, bn, [&](auto c) { r = decltype(c)::G::SMEM_BYTES; });
   return r;
 }
 
-int tf32x3_stages(int bk, int bn) {
+int tf32x3_stages(int bm, int bk, int bn) {
   int r = -1;
-  dispatch(bk, bn, [&](auto c) { r = decltype(c)::G::STAGES; });
+  if (bm == tf32x3::PAIR_TILE)
+    dispatch_pair(bk, [&](auto c) { r = decltype(c)::G::STAGES; });
+  else
+    dispatch(bk, bn, [&](auto c) { r = decltype(c)::G::STAGES; });
   return r;
+}
+
+namespace {
+std::mutex g_pair_mutex;
+int g_pair_clusters[64][2];  // [device][bk == 32]
+}  // namespace
+
+int tf32x3_pair_max_clusters(int device, int bk) {
+  if (device < 0 || device >= 64 || (bk != 16 && bk != 32)) return 0;
+  std::lock_guard<std::mutex> lock(g_pair_mutex);
+  int& n = g_pair_clusters[device][bk == 32 ? 1 : 0];
+  if (n == 0) {
+    cudaError_t e = cudaErrorInvalidValue;
+    dispatch_pair(bk, [&](auto c) {
+      e = decltype(c)::prepare();
+      if (e == cudaSuccess) n = decltype(c)::max_clusters();
+    });
+    if (e != cudaSuccess) cudaGetLastError();
+  }
+  return n;
 }
 
 int tf32x3_threads() { return tf32x3::THREADS; }
 int tf32x3_bm() { return tf32x3::BM; }
 
-cudaError_t tf32x3_prepare(int device, int bk, int bn) {
+cudaError_t tf32x3_prepare(int device, int bm, int bk, int bn) {
   (void)device;
   cudaError_t e = cudaErrorInvalidValue;
-  dispatch(bk, bn, [&](auto c) { e = decltype(c)::prepare(); });
+  if (bm == tf32x3::PAIR_TILE)
+    dispatch_pair(bk, [&](auto c) { e = decltype(c)::prepare(); });
+  else
+    dispatch(bk, bn, [&](auto c) { e = decltype(c)::prepare(); });
   return e;
 }
 
 cudaError_t launch_tf32x3(const GemmArgs& a, void* workspace, bool vec_a, bool vec_b,
-                          bool vec_c, int bk, int bn, int max_ctas, int fault_inject,
+                          bool vec_c, int bm, int bk, int bn, int max_ctas, int fault_inject,
                           cudaStream_t stream) {
   cudaError_t e = cudaErrorInvalidValue;
+  if (bm == tf32x3::PAIR_TILE) {
+    dispatch_pair(bk, [&](auto c) {
+      e = decltype(c)::launch(a, workspace, vec_a, vec_b, vec_c, max_ctas, fault_inject,
+                              stream);
+    });
+    return e;
+  }
   dispatch(bk, bn, [&](auto c) {
     e = decltype(c)::launch(a, workspace, vec_a, vec_b, vec_c, max_ctas, fault_inject, stream);
   });
