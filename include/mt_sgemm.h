@@ -92,7 +92,10 @@ typedef struct {
     int wn;        /* FFMA warp tile columns; 0 = automatic */
     int tm;        /* FFMA outputs per thread along M; 0 = automatic */
     int tn;        /* FFMA outputs per thread along N; 0 = automatic */
-    int reserved[2];
+    int pack_a;    /* MT_VARIANT_TF32X3: 0 = automatic, 1 = split A into a packed
+                      copy by a separate kernel, 2 = split A inside the GEMM kernel
+                      (A not transposed, 16-byte aligned, lda % 4 == 0) */
+    int reserved[1];
 } mt_config;
 
 /* What a call with the same arguments would launch. */
@@ -110,6 +113,9 @@ typedef struct {
     int64_t grid;             /* CTAs of the main kernel */
     int64_t smem_bytes;       /* dynamic shared memory per CTA */
     int64_t workspace_bytes;  /* device scratch the call needs (0 = none) */
+    int pack_a;               /* MT_VARIANT_TF32X3: 1 = A packed by its own kernel,
+                                 2 = A split inside the GEMM kernel; 0 otherwise */
+    int reserved;
 } mt_plan;
 
 /*
@@ -182,11 +188,12 @@ MT_API mt_status mt_sgemm_host(const float *A, const float *B, float *C,
  * cfg->variant = MT_VARIANT_TF32X3 (device pointers, stream-ordered).  The
  * packed copies of A and B that variant builds go to a static device array
  * of MT_NOALLOC_SCRATCH_BYTES (32 MiB) instead of memory allocated per call;
- * this call allocates nothing.  A problem needs
- * 8192*ceil(M/128)*ceil(K/16) + 16384*ceil(N/256)*ceil(K/16) bytes of it
- * (about 8*(M + N)*K; up to about 1448 x 1448 x 1448); a larger one returns
- * MT_ERR_SCRATCH_LIMIT and launches nothing (mt_sgemm_plan reports the
- * bytes as workspace_bytes).  Other errors as mt_sgemm_ex.
+ * this call allocates nothing.  A problem needs the workspace_bytes that
+ * mt_sgemm_plan reports for MT_VARIANT_TF32X3: the packed copies of A and B,
+ * about 8*(M + N)*K bytes (square problems up to about 1448^3), or of B
+ * alone, about 8*N*K, when A is split inside the GEMM kernel (N <= 512 and A
+ * 16-byte aligned); a larger problem returns MT_ERR_SCRATCH_LIMIT and
+ * launches nothing.  Other errors as mt_sgemm_ex.
  *
  * The array is shared by every call in the process: calls that overlap on
  * the GPU (different streams, or host threads) race on it and must be

@@ -50,13 +50,22 @@ def assert_within(C, Cref, W, tol, what=""):
 # Every configuration the kernel is built for: one CTA per 128 x bn tile,
 # K depth 16 (64-byte swizzle) or 32 (128-byte swizzle) x tile width 256,
 # 128 or 64; and CTA pairs on 256 x 256 tiles with K depth 16 or 32.
-DEPTHS = [dict(variant="tf32x3", bm=128, bk=bk, bn=bn) for bk in (16, 32)
+DEPTHS = [dict(variant="tf32x3", bm=128, bk=bk, bn=bn, pack_a=1) for bk in (16, 32)
           for bn in (256, 128, 64)]
 DEPTH_IDS = [f"bk{c['bk']}-bn{c['bn']}" for c in DEPTHS]
 PAIRS = [dict(variant="tf32x3", bm=256, bk=bk) for bk in (16, 32)]
 PAIR_IDS = [f"pair-bk{c['bk']}" for c in PAIRS]
-ALL = DEPTHS + PAIRS
-ALL_IDS = DEPTH_IDS + PAIR_IDS
+# A split inside the GEMM kernel (only B packed); A must be readable by TMA
+# in place (K % 4 == 0 for packed rows).
+ASPLIT = [dict(variant="tf32x3", bm=128, bk=bk, bn=bn, pack_a=2) for bk in (16, 32)
+          for bn in (256, 128, 64)]
+ASPLIT_IDS = [f"asplit-bk{c['bk']}-bn{c['bn']}" for c in ASPLIT]
+ALL = DEPTHS + PAIRS + ASPLIT
+ALL_IDS = DEPTH_IDS + PAIR_IDS + ASPLIT_IDS
+
+
+def eligible(cfg, K):
+    return cfg.get("pack_a") != 2 or K % 4 == 0
 
 
 @pytest.mark.parametrize("cfg", DEPTHS, ids=DEPTH_IDS)
@@ -96,6 +105,8 @@ def test_pair_plan_reports_tile_and_workspace(cfg):
 @pytest.mark.parametrize("cfg", ALL, ids=ALL_IDS)
 @pytest.mark.parametrize("name", ["masked_100x72x80", "square_1024", "ragged_4097x3001x2053"])
 def test_workloads_full_oracle(name, cfg):
+    if not eligible(cfg, gemm_inputs.WORKLOADS[name].K):
+        pytest.skip("A's rows are not 16-byte multiples: split-A needs TMA on A")
     A, B = gemm_inputs.make_workload(name)
     Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
     assert_within(run(A, B, **cfg).numpy(), Cref, W, TOL, name)
@@ -103,11 +114,16 @@ def test_workloads_full_oracle(name, cfg):
 
 @pytest.mark.parametrize("split", [0, 1], ids=["auto-split-tail", "no-split"])
 @pytest.mark.parametrize("tile", [0, 128], ids=["auto", "single"])
-@pytest.mark.parametrize("name", ["square_4096", "square_8192", "skinny_65536x128x4096"])
+@pytest.mark.parametrize("name", ["square_4096", "square_8192", "skinny_65536x128x4096",
+                                  "skinny_65536x128x4096/packed-A"])
 def test_full_size_sampled_rows(name, split, tile):
+    name, _, how = name.partition("/")
     w = gemm_inputs.WORKLOADS[name]
     A, B = gemm_inputs.make_workload(w)
-    c = mt.sgemm(A.cuda(), B.cuda(), split_k=split, bm=tile, **TF32)
+    pack = dict(pack_a=1) if how == "packed-A" else {}
+    c = mt.sgemm(A.cuda(), B.cuda(), split_k=split, bm=tile, **TF32, **pack)
+    if name.startswith("skinny"):
+        assert mt.plan(w.M, w.N, w.K, bm=tile, **TF32, **pack)["pack_a"] == (1 if pack else 2)
     torch.cuda.synchronize()
     g = np.random.default_rng(1)
     rows = np.unique(np.concatenate([[0, w.M - 1, 127, 128, 255, 256],
@@ -121,12 +137,14 @@ def test_full_size_sampled_rows(name, split, tile):
                                    (300, 520, 1000)])
 def test_integer_inputs_bit_exact(shape, cfg):
     M, N, K = shape
+    if not eligible(cfg, K):
+        pytest.skip("split-A needs K % 4 == 0 here")
     A, B = gemm_inputs.make_ab(M, N, K, seed=21, dist="int")
     assert np.array_equal(run(A, B, **cfg).numpy(), oracle.sgemm(A.numpy(), B.numpy()))
 
 
 TINY = [(1, 1, 1), (1, 7, 3), (5, 1, 9), (3, 5, 7), (17, 15, 33), (31, 33, 1),
-        (129, 257, 31), (130, 258, 65)]
+        (129, 257, 31), (130, 258, 65), (1, 1, 4), (5, 3, 8), (129, 257, 32), (130, 65, 36)]
 
 
 @pytest.mark.parametrize("shape", TINY)
@@ -135,7 +153,8 @@ def test_tiny_ragged(shape):
     A, B = gemm_inputs.make_ab(M, N, K, seed=M * 7 + N * 3 + K, dist="normal")
     Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
     for cfg in ALL:
-        assert_within(run(A, B, **cfg).numpy(), Cref, W, TOL, f"{shape} {cfg}")
+        if eligible(cfg, K):
+            assert_within(run(A, B, **cfg).numpy(), Cref, W, TOL, f"{shape} {cfg}")
 
 
 def test_identity_within_tolerance():
@@ -184,7 +203,8 @@ def test_device_status_clean_after_runs():
     assert mt.mt_device_status(0) == mt.MT_OK
 
 
-@pytest.mark.parametrize("tile", [128, 256], ids=["single", "pair"])
+@pytest.mark.parametrize("tile", [dict(bm=128, pack_a=1), dict(bm=256),
+                                  dict(bm=128, bk=16, pack_a=2)], ids=["single", "pair", "asplit"])
 def test_timeout_path_reports_and_context_survives(tile):
     """The copy threads issue nothing: every bounded wait runs out (about a
     second), the kernel records the timeout and returns; the context stays
@@ -192,7 +212,7 @@ def test_timeout_path_reports_and_context_survives(tile):
     A, B = gemm_inputs.make_workload("masked_100x72x80")
     a, b = A.cuda(), B.cuda()
     c = torch.full((100, 72), 7.0, device="cuda")
-    mt.sgemm(a, b, out=c, variant="tf32x3", fault_inject=1, bm=tile)
+    mt.sgemm(a, b, out=c, variant="tf32x3", fault_inject=1, **tile)
     assert mt.mt_device_status(0) == mt.MT_ERR_TIMEOUT
     assert torch.all(c == 7.0)  # nothing written
     assert mt.mt_device_status(0) == mt.MT_OK  # the status word was cleared

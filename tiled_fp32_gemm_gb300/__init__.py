@@ -54,7 +54,8 @@ class mt_config(ctypes.Structure):
                 ("bk", ctypes.c_int), ("stages", ctypes.c_int), ("no_pad", ctypes.c_int),
                 ("split_k", ctypes.c_int), ("fma", ctypes.c_int),
                 ("fault_inject", ctypes.c_int), ("wm", ctypes.c_int), ("wn", ctypes.c_int),
-                ("tm", ctypes.c_int), ("tn", ctypes.c_int), ("reserved", ctypes.c_int * 2)]
+                ("tm", ctypes.c_int), ("tn", ctypes.c_int), ("pack_a", ctypes.c_int),
+                ("reserved", ctypes.c_int * 1)]
 
 
 class mt_plan(ctypes.Structure):
@@ -65,7 +66,8 @@ class mt_plan(ctypes.Structure):
                 ("wm", ctypes.c_int), ("wn", ctypes.c_int), ("tm", ctypes.c_int),
                 ("tn", ctypes.c_int),
                 ("grid", ctypes.c_int64), ("smem_bytes", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64), ("pack_a", ctypes.c_int),
+                ("reserved", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -134,7 +136,7 @@ def lib():
 
 
 def make_config(variant="ffma", bm=0, bn=0, bk=0, stages=0, no_pad=False, split_k=0,
-                fma=0, fault_inject=0, wm=0, wn=0, tm=0, tn=0) -> mt_config:
+                fma=0, fault_inject=0, wm=0, wn=0, tm=0, tn=0, pack_a=0) -> mt_config:
     c = mt_config()
     c.variant = VARIANTS[variant] if isinstance(variant, str) else int(variant)
     c.bm, c.bn, c.bk, c.stages = bm, bn, bk, stages
@@ -144,6 +146,7 @@ def make_config(variant="ffma", bm=0, bn=0, bk=0, stages=0, no_pad=False, split_
     c.fault_inject = fault_inject
     c.wm, c.wn = wm, wn
     c.tm, c.tn = tm, tn
+    c.pack_a = pack_a
     return c
 
 

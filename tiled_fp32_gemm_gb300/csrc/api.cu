@@ -101,8 +101,10 @@ struct Launch {
   int max_ctas = 0;  // persistent kernels: CTAs to launch at most
   // FFMA split-K (see GemmArgs).
   int full_tiles = 0, split = 1, kt_per_slice = 0;
-  // 3xTF32: float4 reads of A / B by their packers.
+  // 3xTF32: float4 reads of A / B by their packers; A split inside the
+  // GEMM kernel instead of packed.
   bool vec_a = false, vec_b = false;
+  int split_a = 0;
 };
 
 mt_status check_dims(int64_t M, int64_t N, int64_t K) {
@@ -287,7 +289,7 @@ mt_status plan_f16(const Problem& P, const mt_config* cfg, int64_t smem_limit, i
   if (cfg && cfg->variant != MT_VARIANT_FFMA && cfg->variant != MT_VARIANT_TC16)
     return MT_ERR_UNSUPPORTED;
   if (cfg && (cfg->wm || cfg->wn || cfg->tm || cfg->tn || cfg->fma || cfg->no_pad ||
-              cfg->split_k > 1))
+              cfg->split_k > 1 || cfg->pack_a))
     return MT_ERR_UNSUPPORTED;
   const int64_t M = P.M, N = P.N, K = P.K;
   const int bk = mt::f16tc_bk();
@@ -348,7 +350,8 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   if (cfg && (cfg->bm < 0 || cfg->bn < 0 || cfg->bk < 0 || cfg->stages < 0 ||
               cfg->no_pad < 0 || cfg->no_pad > 1 || cfg->split_k < 0 || cfg->fma < 0 ||
               cfg->fma > 2 || cfg->fault_inject < 0 || cfg->fault_inject > 1 || cfg->wm < 0 ||
-              cfg->wn < 0 || cfg->tm < 0 || cfg->tn < 0))
+              cfg->wn < 0 || cfg->tm < 0 || cfg->tn < 0 || cfg->pack_a < 0 ||
+              cfg->pack_a > 2))
     return MT_ERR_INVALID_ARG;
   if (P.dtype)
     return plan_f16(P, cfg, smem_limit, sms, dev >= 0 ? mt::f16tc_pair_max_clusters(dev) : 0,
@@ -356,6 +359,7 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   if (variant == MT_VARIANT_TC16) return MT_ERR_UNSUPPORTED;  // 16-bit inputs only
   if (cfg && (cfg->wm || cfg->wn || cfg->tm || cfg->tn) && variant != MT_VARIANT_FFMA)
     return MT_ERR_UNSUPPORTED;
+  if (cfg && cfg->pack_a && variant != MT_VARIANT_TF32X3) return MT_ERR_UNSUPPORTED;
   if (cfg && cfg->fault_inject && variant != MT_VARIANT_TF32X3) return MT_ERR_UNSUPPORTED;
   // 3xTF32 splits only its tail by itself (split_k = 1 turns that off).
   if (cfg && cfg->split_k > 1 && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
@@ -391,21 +395,41 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   }
   if (variant == MT_VARIANT_TF32X3) {
     const int want_bm = cfg ? cfg->bm : 0;
+    // A split inside the GEMM kernel instead of packed (one CTA per tile):
+    // for up to 1024 columns or products up to 2048^3, where packing A costs
+    // more than it saves; A must be readable by TMA as stored.  Measured on
+    // GB300 against packing: 65536 x 128 x 4096 2.3x, 65536 x 256 x 4096
+    // 1.9x, 16384 x 512 x 4096 1.3x, 8192 x 1024 x 4096 1.1x, 2048^3 1.07x;
+    // 4096 x 2048 x 4096 0.97x and 4096^3 0.73x (packing stays there).
+    const bool a_tma_ok = !P.trans_a && P.lda % 4 == 0 && aligned16(P.A);
+    const int want_pack = cfg ? cfg->pack_a : 0;
+    const int split_a =
+        want_pack == 2 ? 1
+        : want_pack == 1 ? 0
+        : (a_tma_ok && want_bm != 256 && (N <= 1024 || M * N * K <= (int64_t(1) << 33))) ? 1
+                                                                                         : 0;
+    if (split_a && (want_bm == 256 || !a_tma_ok)) return MT_ERR_UNSUPPORTED;
     const int bn = cfg && cfg->bn ? cfg->bn
                    : want_bm == 256 ? 256 : pick_tf32x3_bn(M, N, sms > 0 ? sms : 1);
     // CTA pairs (256 x 256 tiles, K depth 16 unless asked) when the pair
     // tiles fill the resident clusters, as for 16-bit inputs.
     const int pair_clusters16 = dev >= 0 ? mt::tf32x3_pair_max_clusters(dev, 16) : 0;
     const int bm = want_bm ? want_bm
-                           : auto_pair(M, N, bn, sms, pair_clusters16) ? 256 : mt::tf32x3_bm();
+                   : !split_a && auto_pair(M, N, bn, sms, pair_clusters16) ? 256
+                                                                            : mt::tf32x3_bm();
     const bool pair = bm == 256;
-    const int bk = cfg && cfg->bk ? cfg->bk : pair ? 16 : tf32x3_default_bk(bn);
-    if (!mt::tf32x3_valid(bm, bk, bn)) return MT_ERR_UNSUPPORTED;
-    const int stages = mt::tf32x3_stages(bm, bk, bn);
+    // Split-A: K depth 16 for 256-wide tiles (4 stages instead of 2), 32
+    // for narrower ones (fewer, longer stages measured faster).
+    const int bk = cfg && cfg->bk ? cfg->bk
+                   : split_a ? (bn == 256 ? 16 : 32) : pair ? 16 : tf32x3_default_bk(bn);
+    if (!mt::tf32x3_valid(bm, bk, bn, split_a)) return MT_ERR_UNSUPPORTED;
+    const int stages = mt::tf32x3_stages(bm, bk, bn, split_a);
     if (cfg && ((cfg->stages && cfg->stages != stages) || cfg->fma || cfg->no_pad))
       return MT_ERR_UNSUPPORTED;
     p.bm = bm; p.bn = bn; p.bk = bk; p.stages = stages;
-    p.threads = mt::tf32x3_threads();
+    p.threads = mt::tf32x3_threads(split_a);
+    p.pack_a = split_a ? 2 : 1;
+    L->split_a = split_a;
     p.pad_a = 0; p.pad_b = 0;  // swizzled tiles: the tensor core's layout, no padding
     // A packer reads float4 when it walks k-contiguous rows (A as stored,
     // B stored transposed) that are whole float4s from an aligned base.
@@ -413,7 +437,7 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
     L->vec_b = P.trans_b && K % 4 == 0 && P.ldb % 4 == 0 && aligned16(P.B);
     p.vec_ab = L->vec_a;
     p.vec_c = N % 4 == 0 && P.ldc % 4 == 0 && aligned16(P.C);
-    p.smem_bytes = mt::tf32x3_smem_bytes(bm, bk, bn);
+    p.smem_bytes = mt::tf32x3_smem_bytes(bm, bk, bn, split_a);
     L->tiles_m = static_cast<int>(ceil_div(M, bm));
     L->tiles_n = static_cast<int>(ceil_div(N, bn));
     // Pack grids: up to 65535 blocks of rows per operand.
@@ -443,7 +467,7 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
     const int64_t units = full + (tiles - full) * split;
     p.grid = std::min<int64_t>(units, L->max_ctas) * (pair ? 2 : 1);
     p.workspace_bytes = mt::tf32x3_workspace_bytes(static_cast<int>(M), static_cast<int>(N),
-                                                   static_cast<int>(K), bm, bk, bn) +
+                                                   static_cast<int>(K), bm, bk, bn, split_a) +
                         (tiles - full) * split * bm * bn * 4;
     if (p.smem_bytes > smem_limit) return MT_ERR_SMEM_BUDGET;
     return MT_OK;
@@ -535,19 +559,20 @@ mt_status pool_for(int dev, cudaMemPool_t* pool) {
 }
 
 // [device][configuration]: shared-memory attribute of the 3xTF32 kernel applied.
-std::atomic<uint8_t> g_tf32x3_ready[kMaxDevices][8];
+std::atomic<uint8_t> g_tf32x3_ready[kMaxDevices][16];
 
-// [bk == 32][128 x 256, 128 x 128, 128 x 64, pair 256 x 256]
-int tf32x3_cfg_index(int bm, int bk, int bn) {
-  return (bk == 32 ? 4 : 0) + (bm == 256 ? 3 : bn == 256 ? 0 : bn == 128 ? 1 : 2);
+// [split_a][bk == 32][128 x 256, 128 x 128, 128 x 64, pair 256 x 256]
+int tf32x3_cfg_index(int bm, int bk, int bn, int split_a) {
+  return (split_a ? 8 : 0) + (bk == 32 ? 4 : 0) +
+         (bm == 256 ? 3 : bn == 256 ? 0 : bn == 128 ? 1 : 2);
 }
 
-mt_status prepare_tf32x3(int dev, int bm, int bk, int bn) {
-  std::atomic<uint8_t>& ready = g_tf32x3_ready[dev][tf32x3_cfg_index(bm, bk, bn)];
+mt_status prepare_tf32x3(int dev, int bm, int bk, int bn, int split_a) {
+  std::atomic<uint8_t>& ready = g_tf32x3_ready[dev][tf32x3_cfg_index(bm, bk, bn, split_a)];
   if (!ready.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!ready.load(std::memory_order_relaxed)) {
-      if (mt::tf32x3_prepare(dev, bm, bk, bn) != cudaSuccess) {
+      if (mt::tf32x3_prepare(dev, bm, bk, bn, split_a) != cudaSuccess) {
         cudaGetLastError();
         return MT_ERR_LAUNCH;
       }
@@ -583,7 +608,7 @@ mt::GemmArgs make_args(const Problem& P, const Launch& L) {
 }
 
 mt_status run_tf32x3(int dev, const mt::GemmArgs& args, const Launch& L, cudaStream_t stream) {
-  mt_status st0 = prepare_tf32x3(dev, L.plan.bm, L.plan.bk, L.plan.bn);
+  mt_status st0 = prepare_tf32x3(dev, L.plan.bm, L.plan.bk, L.plan.bn, L.split_a);
   if (st0 != MT_OK) return st0;
   cudaMemPool_t pool = nullptr;
   mt_status st = pool_for(dev, &pool);
@@ -596,7 +621,7 @@ mt_status run_tf32x3(int dev, const mt::GemmArgs& args, const Launch& L, cudaStr
   }
   const cudaError_t e =
       mt::launch_tf32x3(args, ws, L.vec_a, L.vec_b, L.plan.vec_c != 0, L.plan.bm, L.plan.bk,
-                        L.plan.bn, L.max_ctas, L.fault_inject, stream);
+                        L.plan.bn, L.split_a, L.max_ctas, L.fault_inject, stream);
   cudaFreeAsync(ws, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -789,7 +814,7 @@ mt_status mt_sgemm_tf32x3_noalloc(const float* A, const float* B, float* C, int6
     return MT_OK;
   }
   if (L.plan.workspace_bytes > MT_NOALLOC_SCRATCH_BYTES) return MT_ERR_SCRATCH_LIMIT;
-  st = prepare_tf32x3(dev, L.plan.bm, L.plan.bk, L.plan.bn);
+  st = prepare_tf32x3(dev, L.plan.bm, L.plan.bk, L.plan.bn, L.split_a);
   if (st != MT_OK) return st;
   void* scratch = nullptr;
   if (mt::tf32x3_noalloc_scratch(dev, &scratch) != cudaSuccess || !scratch) {
@@ -798,7 +823,7 @@ mt_status mt_sgemm_tf32x3_noalloc(const float* A, const float* B, float* C, int6
   }
   const mt::GemmArgs args = make_args(P, L);
   if (mt::launch_tf32x3(args, scratch, L.vec_a, L.vec_b, L.plan.vec_c != 0, L.plan.bm,
-                        L.plan.bk, L.plan.bn, L.max_ctas, 0, stream) != cudaSuccess) {
+                        L.plan.bk, L.plan.bn, L.split_a, L.max_ctas, 0, stream) != cudaSuccess) {
     cudaGetLastError();
     return MT_ERR_LAUNCH;
   }

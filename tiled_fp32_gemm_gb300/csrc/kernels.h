@@ -76,13 +76,16 @@ int p18_smem_bytes(bool pad);
 // bytes (the packed, split, swizzled copies of A and B); launch_tf32x3 runs
 // the two pack kernels and the GEMM on at most max_ctas CTAs (one per SM;
 // bm = 256: clusters of two).
-bool tf32x3_valid(int bm, int bk, int bn);
-int64_t tf32x3_workspace_bytes(int M, int N, int K, int bm, int bk, int bn);
-int tf32x3_smem_bytes(int bm, int bk, int bn);
-int tf32x3_stages(int bm, int bk, int bn);
-int tf32x3_threads();
+// split_a = 1: the split-A kernel (bm = 128, bk = 32, A not transposed with
+// a 16-byte aligned base and lda % 4 == 0): A is split inside the GEMM
+// kernel and only B is packed.
+bool tf32x3_valid(int bm, int bk, int bn, int split_a);
+int64_t tf32x3_workspace_bytes(int M, int N, int K, int bm, int bk, int bn, int split_a);
+int tf32x3_smem_bytes(int bm, int bk, int bn, int split_a);
+int tf32x3_stages(int bm, int bk, int bn, int split_a);
+int tf32x3_threads(int split_a);
 int tf32x3_bm();
-cudaError_t tf32x3_prepare(int device, int bm, int bk, int bn);
+cudaError_t tf32x3_prepare(int device, int bm, int bk, int bn, int split_a);
 // Clusters of two of the pair kernel resident at once on `device` (the
 // current device); 0 if the query fails.  Sets its shared-memory limit.
 int tf32x3_pair_max_clusters(int device, int bk);
@@ -91,8 +94,8 @@ int tf32x3_pair_max_clusters(int device, int bk);
 // be written with float4.  fault_inject = 1: the copy threads issue nothing
 // (tests the bounded waits).
 cudaError_t launch_tf32x3(const GemmArgs& a, void* workspace, bool vec_a, bool vec_b,
-                          bool vec_c, int bm, int bk, int bn, int max_ctas, int fault_inject,
-                          cudaStream_t stream);
+                          bool vec_c, int bm, int bk, int bn, int split_a, int max_ctas,
+                          int fault_inject, cudaStream_t stream);
 // Size of the static scratch the allocation-free tf32x3 entry point uses,
 // and its device address on `device` (looked up once per device; the device
 // must be current).

@@ -359,6 +359,215 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Split-A kernel: A is not packed.  TMA copies each 128 x BK fp32 tile of A
+// (row-major, k contiguous) into shared memory with the 128-byte (BK 32) or
+// 64-byte (BK 16) swizzle, which is byte for byte the K-major layout the MMA
+// reads; four converter
+// warps then split it there — big in place, small into a second buffer —
+// and publish it to the tensor core (fence.proxy.async, then conv[s]).  B
+// is packed as in the other kernels.  For problems with few columns, where
+// packing A (reading 4 and writing 8 bytes per element, then reading the 8
+// again) costs more than the product; the tensor pipe has time to spare
+// there, so the extra shared-memory traffic of the split is hidden.
+//   warp 0: TMA of A, bulk copy of the B pair -> full[s];
+//   warps 6-9: wait full[s], split, fence, arrive conv[s];
+//   warp 1: wait conv[s], 3 MMAs per k8 step, commit -> empty[s];
+//   warps 2-5: epilogue, as in the packed kernel.
+constexpr int ASPLIT_THREADS = 320;
+constexpr int CONVERT_THREADS = 128;
+
+template <int BK_, int BN_>
+struct ASplitGeometry {
+  using G = Geometry<BK_, BN_>;
+  static constexpr int BK = BK_;
+  static constexpr int BN = BN_;
+  // TMA swizzle of the fp32 A box: 128-byte rows (BK 32) or 64-byte rows
+  // (BK 16), matching the layout codes of G.
+  static constexpr CUtensorMapSwizzle TMA_SWIZZLE =
+      BK_ == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  static constexpr int A_BYTES = G::A_BLOCK_BYTES;  // fp32 tile, then its big part
+  static constexpr int STAGE_BYTES = 2 * A_BYTES + G::B_PAIR_BYTES;  // A | A small | B pair
+  static constexpr int STAGES_FIT = SMEM_STAGE_BUDGET / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static_assert(STAGES >= 2, "at least two stages");
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+};
+
+template <int BK, int BN>
+__global__ void __launch_bounds__(ASPLIT_THREADS, 1)
+    tf32x3_asplit_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                         const float* __restrict__ Bp, Epilogue ep, int Kt, int tiles_m,
+                         int tiles_n, int group_m, Sched sched, int fault_inject) {
+  using AG = ASplitGeometry<BK, BN>;
+  using G = typename AG::G;
+  constexpr int STAGES = AG::STAGES;
+  constexpr int STAGE_BYTES = AG::STAGE_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars: [0, S) full, [S, 2S) conv, [2S, 3S) empty, then acc_full[2],
+  // acc_empty[2], drain.
+  constexpr int FULL = 0, CONV = STAGES, EMPTY = 2 * STAGES, ACC_FULL = 3 * STAGES,
+                ACC_EMPTY = 3 * STAGES + 2, DRAIN = 3 * STAGES + 4, NBARS = 3 * STAGES + 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const WaitCtx wc{abort_flag, &g_status};
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int num_tiles = tiles_m * tiles_n;
+  const int num_units = sched.full_tiles + (num_tiles - sched.full_tiles) * sched.split;
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmap_a);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(FULL + s), 1);                // producer arrival + tx bytes
+      mbar_init(bar(CONV + s), CONVERT_THREADS);  // every converter thread
+      mbar_init(bar(EMPTY + s), 1);               // MMA commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(ACC_FULL + b), 1);
+      mbar_init(bar(ACC_EMPTY + b), EPILOGUE_THREADS);
+    }
+    mbar_init(bar(DRAIN), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), AG::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  uint32_t issued = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t& g = issued;
+      bool stop = fault_inject != 0;
+      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
+        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+        const char* b_src = reinterpret_cast<const char*>(Bp) +
+                            static_cast<int64_t>(w.tn) * Kt * G::B_PAIR_BYTES;
+        for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
+          const uint32_t s = g % STAGES, round = g / STAGES;
+          if (g >= STAGES && !wait_phase(bar(EMPTY + s), (round + 1) & 1u, wc)) {
+            stop = true;
+            break;
+          }
+          const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
+          mbar_arrive_expect_tx(bar(FULL + s), AG::A_BYTES + G::B_PAIR_BYTES);
+          tma_load_2d(st, &tmap_a, kt * BK, w.tm * BM, bar(FULL + s));
+          bulk_copy_g2s(st + 2 * AG::A_BYTES, b_src + static_cast<int64_t>(kt) * G::B_PAIR_BYTES,
+                        G::B_PAIR_BYTES, bar(FULL + s));
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = instr_desc(BM, BN, 2, 2);
+      uint32_t g = 0;
+      bool stop = false;
+      int it = 0;
+      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x, ++it) {
+        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+        const int b = it & 1;
+        if (it >= 2 && !wait_phase(bar(ACC_EMPTY + b), ((it >> 1) + 1) & 1u, wc)) break;
+        tc_fence_after();
+        const uint32_t acc_tmem = tmem + static_cast<uint32_t>(b * BN);
+        uint32_t acc = 0;
+        for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
+          const uint32_t s = g % STAGES, round = g / STAGES;
+          if (!wait_phase(bar(CONV + s), round & 1u, wc)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_big = smem_u32(smem + s * STAGE_BYTES);
+          const uint32_t a_small = a_big + AG::A_BYTES;
+          const uint32_t b_big = a_big + 2 * AG::A_BYTES;
+          const uint32_t b_small = b_big + G::B_BLOCK_BYTES;
+#pragma unroll
+          for (int j = 0; j < BK / 8; ++j) {
+            const uint32_t koff = j * 32;
+            const uint64_t ab = smem_desc(a_big + koff, 16, G::ATOM_BYTES, G::LAYOUT);
+            const uint64_t as = smem_desc(a_small + koff, 16, G::ATOM_BYTES, G::LAYOUT);
+            const uint64_t bb = smem_desc(b_big + koff, 16, G::ATOM_BYTES, G::LAYOUT);
+            const uint64_t bs = smem_desc(b_small + koff, 16, G::ATOM_BYTES, G::LAYOUT);
+            mma_tf32(acc_tmem, ab, bs, idesc, acc);
+            acc = 1;
+            mma_tf32(acc_tmem, as, bb, idesc, 1);
+            mma_tf32(acc_tmem, ab, bb, idesc, 1);
+          }
+          mma_commit(bar(EMPTY + s));
+        }
+        if (!stop) mma_commit(bar(ACC_FULL + b));
+      }
+      mma_commit(bar(DRAIN));
+      wait_phase(bar(DRAIN), 0, wc, false);
+    }
+  } else if (warp < 6) {
+    const int q = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    int it = 0;
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++it) {
+      const int b = it & 1;
+      const bool ready = wait_phase(bar(ACC_FULL + b), (it >> 1) & 1u, wc, true,
+                                    TIMEOUT_NS + 20000ull * static_cast<uint64_t>(Kt));
+      if (!__all_sync(0xffffffffu, ready)) break;
+      tc_fence_after();
+      __syncwarp();
+      const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      store_accumulator<BM, BN>(tmem + lane_base + static_cast<uint32_t>(b * BN), w, q, lane,
+                                ep, sched.partial);
+      tc_fence_before();
+      mbar_arrive(bar(ACC_EMPTY + b));
+    }
+  } else {
+    // Converters: thread t splits the 16-byte chunks t, t + 128, ... of the
+    // stage's A tile (consecutive threads, consecutive chunks).
+    const int t = threadIdx.x - (ASPLIT_THREADS - CONVERT_THREADS);
+    uint32_t g = 0;
+    bool stop = fault_inject != 0;
+    for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
+      const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
+        const uint32_t s = g % STAGES, round = g / STAGES;
+        if (!wait_phase(bar(FULL + s), round & 1u, wc)) {
+          stop = true;
+          break;
+        }
+        float4* a = reinterpret_cast<float4*>(smem + s * STAGE_BYTES);
+        float4* a_small = reinterpret_cast<float4*>(smem + s * STAGE_BYTES + AG::A_BYTES);
+#pragma unroll
+        for (int i = 0; i < AG::A_BYTES / 16 / CONVERT_THREADS; ++i) {
+          const int c = i * CONVERT_THREADS + t;
+          float4 big, small;
+          split4(a[c], big, small);
+          a[c] = big;
+          a_small[c] = small;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(CONV + s));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    for (uint32_t q = issued > STAGES ? issued - STAGES : 0; q < issued; ++q)
+      wait_phase(bar(FULL + q % STAGES), (q / STAGES) & 1u, wc, false);
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, AG::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // CTA-pair kernel: a cluster of two CTAs on two SMs computes 256 x 256 tiles
 // with tcgen05.mma.cta_group::2 kind::tf32.  Both operands are packed in
 // 128-row blocks; CTA r of the pair stages block 2*t + r of A's tile row t
@@ -711,6 +920,70 @@ struct CfgPair {
   }
 };
 
+// Split-A configuration (A split inside the GEMM kernel), K depth BK.
+template <int BK, int BN>
+struct CfgASplit {
+  using AG = tf32x3::ASplitGeometry<BK, BN>;
+  using G = typename AG::G;
+
+  static int64_t workspace(int M, int N, int K) {
+    (void)M;
+    const int64_t nt = (N + BN - 1) / BN, kt = (K + BK - 1) / BK;
+    return nt * kt * G::B_PAIR_BYTES;
+  }
+  static cudaError_t prepare() {
+    return cudaFuncSetAttribute(tf32x3::tf32x3_asplit_kernel<BK, BN>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, AG::SMEM_BYTES);
+  }
+  static cudaError_t launch(const GemmArgs& a, void* workspace, bool vec_b, bool vec_c,
+                            int max_ctas, int fault_inject, cudaStream_t stream) {
+    using namespace tf32x3;
+    const int mt = (a.M + BM - 1) / BM, nt = (a.N + BN - 1) / BN, kt = (a.K + BK - 1) / BK;
+    if (nt > 65535 || (nt * BN + 255) / 256 > 65535) return cudaErrorInvalidValue;
+    float* Bp = static_cast<float*>(workspace);
+    if (a.trans_b)
+      pack_kc_kernel<G, BN><<<dim3(kt, nt), 256, 0, stream>>>(a.B, a.ldb, Bp, a.N, a.K, kt,
+                                                              vec_b ? 1 : 0);
+    else
+      pack_rc_kernel<G, BN><<<dim3(kt, (nt * BN + 255) / 256), 256, 0, stream>>>(
+          a.B, a.ldb, Bp, a.N, a.K, kt, nt);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // A (M x K, row pitch lda) in 128 x BK boxes with the swizzle of the
+    // MMA's K-major layout; zero fill past M and K.
+    CUtensorMap map_a;
+    if (!encode_tensor_map_2d(&map_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.A, a.M, a.K, a.lda,
+                              BK, BM, AG::TMA_SWIZZLE))
+      return cudaErrorInvalidValue;
+    const int tiles = mt * nt;
+    Sched sched{a.full_tiles, a.split, a.kt_per_slice, nullptr};
+    if (a.split > 1)
+      sched.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                CfgASplit::workspace(a.M, a.N, a.K));
+    const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
+    const int grid = units < max_ctas ? units : max_ctas;
+    tf32x3_asplit_kernel<BK, BN><<<grid, ASPLIT_THREADS, AG::SMEM_BYTES, stream>>>(
+        map_a, Bp, Epilogue{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0}, kt, mt, nt,
+        a.group_m, sched, fault_inject);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || a.split <= 1) return e;
+    GemmArgs r = a;
+    r.partial = sched.partial;
+    return launch_splitk_reduce(r, BM, BN, vec_c, stream);
+  }
+};
+
+template <class F>
+bool dispatch_asplit(int bk, int bn, F&& f) {
+  if (bk == 16 && bn == 256) { f(CfgASplit<16, 256>{}); return true; }
+  if (bk == 16 && bn == 128) { f(CfgASplit<16, 128>{}); return true; }
+  if (bk == 16 && bn == 64) { f(CfgASplit<16, 64>{}); return true; }
+  if (bk == 32 && bn == 256) { f(CfgASplit<32, 256>{}); return true; }
+  if (bk == 32 && bn == 128) { f(CfgASplit<32, 128>{}); return true; }
+  if (bk == 32 && bn == 64) { f(CfgASplit<32, 64>{}); return true; }
+  return false;
+}
+
 template <class F>
 bool dispatch_pair(int bk, F&& f) {
   if (bk == 16) { f(CfgPair<16>{}); return true; }
@@ -733,32 +1006,39 @@ bool dispatch(int bk, int bn, F&& f) {
 
 }  // namespace
 
-bool tf32x3_valid(int bm, int bk, int bn) {
+bool tf32x3_valid(int bm, int bk, int bn, int split_a) {
+  if (split_a) return bm == tf32x3::BM && dispatch_asplit(bk, bn, [](auto) {});
   if (bm == tf32x3::PAIR_TILE) return bn == tf32x3::PAIR_TILE && dispatch_pair(bk, [](auto) {});
   return bm == tf32x3::BM && dispatch(bk, bn, [](auto) {});
 }
 
-int64_t tf32x3_workspace_bytes(int M, int N, int K, int bm, int bk, int bn) {
+int64_t tf32x3_workspace_bytes(int M, int N, int K, int bm, int bk, int bn, int split_a) {
   int64_t r = -1;
-  if (bm == tf32x3::PAIR_TILE)
+  if (split_a)
+    dispatch_asplit(bk, bn, [&](auto c) { r = decltype(c)::workspace(M, N, K); });
+  else if (bm == tf32x3::PAIR_TILE)
     dispatch_pair(bk, [&](auto c) { r = decltype(c)::workspace(M, N, K); });
   else
     dispatch(bk, bn, [&](auto c) { r = decltype(c)::workspace(M, N, K); });
   return r;
 }
 
-int tf32x3_smem_bytes(int bm, int bk, int bn) {
+int tf32x3_smem_bytes(int bm, int bk, int bn, int split_a) {
   int r = -1;
-  if (bm == tf32x3::PAIR_TILE)
+  if (split_a)
+    dispatch_asplit(bk, bn, [&](auto c) { r = decltype(c)::AG::SMEM_BYTES; });
+  else if (bm == tf32x3::PAIR_TILE)
     dispatch_pair(bk, [&](auto c) { r = decltype(c)::G::SMEM_BYTES; });
   else
     dispatch(bk, bn, [&](auto c) { r = decltype(c)::G::SMEM_BYTES; });
   return r;
 }
 
-int tf32x3_stages(int bm, int bk, int bn) {
+int tf32x3_stages(int bm, int bk, int bn, int split_a) {
   int r = -1;
-  if (bm == tf32x3::PAIR_TILE)
+  if (split_a)
+    dispatch_asplit(bk, bn, [&](auto c) { r = decltype(c)::AG::STAGES; });
+  else if (bm == tf32x3::PAIR_TILE)
     dispatch_pair(bk, [&](auto c) { r = decltype(c)::G::STAGES; });
   else
     dispatch(bk, bn, [&](auto c) { r = decltype(c)::G::STAGES; });
@@ -785,13 +1065,17 @@ int tf32x3_pair_max_clusters(int device, int bk) {
   return n;
 }
 
-int tf32x3_threads() { return tf32x3::THREADS; }
+int tf32x3_threads(int split_a) {
+  return split_a ? tf32x3::ASPLIT_THREADS : tf32x3::THREADS;
+}
 int tf32x3_bm() { return tf32x3::BM; }
 
-cudaError_t tf32x3_prepare(int device, int bm, int bk, int bn) {
+cudaError_t tf32x3_prepare(int device, int bm, int bk, int bn, int split_a) {
   (void)device;
   cudaError_t e = cudaErrorInvalidValue;
-  if (bm == tf32x3::PAIR_TILE)
+  if (split_a)
+    dispatch_asplit(bk, bn, [&](auto c) { e = decltype(c)::prepare(); });
+  else if (bm == tf32x3::PAIR_TILE)
     dispatch_pair(bk, [&](auto c) { e = decltype(c)::prepare(); });
   else
     dispatch(bk, bn, [&](auto c) { e = decltype(c)::prepare(); });
@@ -799,9 +1083,16 @@ cudaError_t tf32x3_prepare(int device, int bm, int bk, int bn) {
 }
 
 cudaError_t launch_tf32x3(const GemmArgs& a, void* workspace, bool vec_a, bool vec_b,
-                          bool vec_c, int bm, int bk, int bn, int max_ctas, int fault_inject,
-                          cudaStream_t stream) {
+                          bool vec_c, int bm, int bk, int bn, int split_a, int max_ctas,
+                          int fault_inject, cudaStream_t stream) {
   cudaError_t e = cudaErrorInvalidValue;
+  if (split_a) {
+    if (bm != tf32x3::BM || a.trans_a) return e;
+    dispatch_asplit(bk, bn, [&](auto c) {
+      e = decltype(c)::launch(a, workspace, vec_b, vec_c, max_ctas, fault_inject, stream);
+    });
+    return e;
+  }
   if (bm == tf32x3::PAIR_TILE) {
     dispatch_pair(bk, [&](auto c) {
       e = decltype(c)::launch(a, workspace, vec_a, vec_b, vec_c, max_ctas, fault_inject,
