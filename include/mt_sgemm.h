@@ -165,7 +165,11 @@ MT_API mt_status mt_sgemm_general(int trans_a, int trans_b, int64_t M, int64_t N
 /*
  * C = A*B with A, B, C in HOST memory (pageable or pinned).  Copies A and B
  * to the device, multiplies, copies C back and synchronises `stream` before
- * returning, so on MT_OK the host C holds the result.  Device buffers come
+ * returning, so on MT_OK the host C holds the result.  Large products are
+ * cut into row blocks of A and C: the copy in of one block and the copy out
+ * of another run on the library's own copy streams while the product of a
+ * third runs on `stream` (with pinned host memory the copies overlap the
+ * products; the result is the same as mt_sgemm_ex's).  Device buffers come
  * from the stream-ordered pool of the current device and are returned to it
  * before the call ends.  Errors as mt_sgemm_ex, plus MT_ERR_CUDA when a
  * copy, allocation or the final synchronisation fails.

@@ -273,3 +273,31 @@ def test_alias_rejected_without_launch():
     torch.cuda.synchronize()
     assert torch.all(a == 1.0)
     assert mt.mt_device_status(0) == mt.MT_OK
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_host_entry_point_pipelined_blocks(pinned):
+    """8192 x 8192 x 512 from host buffers: four row blocks, each copied in,
+    multiplied and copied out on its own stream while its neighbours move.
+    The FFMA result is bit-identical to the device entry point (the same FMA
+    chain per output); 3xTF32 through the same path stays within tolerance."""
+    M, N, K = 8192, 8192, 512
+    A, B = gemm_inputs.make_ab(M, N, K, seed=17, dist="normal")
+    if pinned:
+        A, B = A.pin_memory(), B.pin_memory()
+        c = torch.full((M, N), float("nan")).pin_memory()
+    else:
+        c = torch.full((M, N), float("nan"))
+    st = mt.mt_sgemm_host(A.data_ptr(), B.data_ptr(), c.data_ptr(), M, N, K, 0, None)
+    assert st == mt.MT_OK
+    dev = mt.sgemm(A.cuda(), B.cuda()).cpu()
+    assert torch.equal(c, dev)
+    rows = np.array([0, 2047, 2048, 4095, 4096, 6143, 6144, 8191])
+    Cr, Wr = oracle.sgemm_rows(A.numpy(), B.numpy(), rows, with_w=True)
+    assert_within(c.numpy()[rows], Cr, Wr, FFMA_TOL, "host pipelined")
+    c.fill_(float("nan"))
+    st = mt.mt_sgemm_host(A.data_ptr(), B.data_ptr(), c.data_ptr(), M, N, K, 0,
+                          mt.make_config(variant="tf32x3"))
+    assert st == mt.MT_OK
+    assert_within(c.numpy()[rows], Cr, Wr, 5e-5, "host pipelined tf32x3")
+    assert mt.mt_device_status(0) == mt.MT_OK

@@ -727,6 +727,48 @@ mt_status run(const Problem& P, cudaStream_t stream, const mt_config* cfg) {
   return MT_OK;
 }
 
+// Copy streams of the host-buffer entry point, per device (created once,
+// non-blocking).  Concurrent calls share them: their copies serialise, the
+// events keep each call's order.
+struct HostStreams {
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+};
+HostStreams g_host_streams[kMaxDevices];
+
+mt_status host_streams(int dev, HostStreams* out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  HostStreams& h = g_host_streams[dev];
+  if (!h.h2d) {
+    cudaStream_t a = nullptr, b = nullptr;
+    if (cudaStreamCreateWithFlags(&a, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&b, cudaStreamNonBlocking) != cudaSuccess) {
+      if (a) cudaStreamDestroy(a);
+      cudaGetLastError();
+      return MT_ERR_CUDA;
+    }
+    h.h2d = a;
+    h.d2h = b;
+  }
+  *out = h;
+  return MT_OK;
+}
+
+// Row blocks of the host entry point's copy/compute pipeline.  A block must
+// still fill the GPU several times over (at least 3 x 304 tiles of
+// 128 x 128: three waves of the default FFMA plan), and its rows start on a
+// multiple of 256, so its A and C rows stay 16-byte aligned; at most
+// kMaxHostBlocks blocks.  One block (no pipeline) when M is too small for
+// two such blocks.
+constexpr int kMaxHostBlocks = 4;
+
+int64_t host_block_rows(int64_t M, int64_t N, int64_t K) {
+  (void)K;
+  const int64_t tile_cols = std::max<int64_t>(1, ceil_div(N, 128));
+  const int64_t min_rows = ceil_div(ceil_div(3 * 304, tile_cols) * 128, 256) * 256;
+  const int64_t rows = std::max(min_rows, ceil_div(ceil_div(M, kMaxHostBlocks), 256) * 256);
+  return rows * 2 <= M ? rows : M;
+}
+
 }  // namespace
 
 extern "C" {
@@ -762,6 +804,9 @@ mt_status mt_sgemm_host(const float* A, const float* B, float* C, int64_t M, int
   cudaMemPool_t pool = nullptr;
   st = pool_for(dev, &pool);
   if (st != MT_OK) return st;
+  HostStreams hs;
+  st = host_streams(dev, &hs);
+  if (st != MT_OK) return st;
   const size_t a_bytes = static_cast<size_t>(M * K) * 4, b_bytes = static_cast<size_t>(K * N) * 4,
                c_bytes = static_cast<size_t>(M * N) * 4;
   float *dA = nullptr, *dB = nullptr, *dC = nullptr;
@@ -770,17 +815,61 @@ mt_status mt_sgemm_host(const float* A, const float* B, float* C, int64_t M, int
   if (a_bytes) ok = ok && cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dA), a_bytes, pool, stream) == cudaSuccess;
   if (b_bytes) ok = ok && cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dB), b_bytes, pool, stream) == cudaSuccess;
   ok = ok && cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dC), c_bytes, pool, stream) == cudaSuccess;
-  if (ok && a_bytes) ok = cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, stream) == cudaSuccess;
-  if (ok && b_bytes) ok = cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, stream) == cudaSuccess;
-  if (ok) {
-    st = run(packed_problem(dA, dB, dC, M, N, K), stream, cfg);
-    if (st == MT_OK)
-      ok = cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, stream) == cudaSuccess;
+
+  // Row blocks of A and C: block i's copy in, product and copy out run on
+  // the copy-in stream, the caller's stream and the copy-out stream, so the
+  // copies of neighbouring blocks overlap the product of this one.
+  const int64_t rows = host_block_rows(M, N, K);
+  const int64_t blocks = ceil_div(M, rows);
+  cudaEvent_t ev[2 * kMaxHostBlocks + 2] = {};
+  const int nev = static_cast<int>(2 * blocks + 2);
+  for (int i = 0; i < nev && ok; ++i)
+    ok = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
+  cudaEvent_t ev_alloc = ev[0], ev_done = ev[1];
+  // The buffers were allocated on the caller's stream.
+  if (ok) ok = cudaEventRecord(ev_alloc, stream) == cudaSuccess &&
+               cudaStreamWaitEvent(hs.h2d, ev_alloc, 0) == cudaSuccess &&
+               cudaStreamWaitEvent(hs.d2h, ev_alloc, 0) == cudaSuccess;
+  if (ok && b_bytes) ok = cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, hs.h2d) == cudaSuccess;
+  for (int64_t i = 0; i < blocks && ok && st == MT_OK; ++i) {
+    const int64_t r0 = i * rows, nr = std::min(rows, M - r0);
+    cudaEvent_t ev_in = ev[2 + 2 * i], ev_out = ev[3 + 2 * i];
+    // Block i of A (and, before block 0, all of B) is on the device ...
+    if (K > 0)
+      ok = cudaMemcpyAsync(dA + r0 * K, A + r0 * K, static_cast<size_t>(nr * K) * 4,
+                           cudaMemcpyHostToDevice, hs.h2d) == cudaSuccess;
+    ok = ok && cudaEventRecord(ev_in, hs.h2d) == cudaSuccess &&
+         cudaStreamWaitEvent(stream, ev_in, 0) == cudaSuccess;
+    if (!ok) break;
+    // ... its product runs on the caller's stream ...
+    st = run(packed_problem(K > 0 ? dA + r0 * K : nullptr, dB, dC + r0 * N, nr, N, K), stream,
+             cfg);
+    if (st != MT_OK) break;
+    // ... and its rows of C go back while the next block computes.
+    ok = cudaEventRecord(ev_out, stream) == cudaSuccess &&
+         cudaStreamWaitEvent(hs.d2h, ev_out, 0) == cudaSuccess &&
+         cudaMemcpyAsync(C + r0 * N, dC + r0 * N, static_cast<size_t>(nr * N) * 4,
+                         cudaMemcpyDeviceToHost, hs.d2h) == cudaSuccess;
+  }
+  // The caller's stream waits for both copy streams before the buffers go
+  // back to the pool, then the call synchronises it.
+  bool drained = ev_done && cudaEventRecord(ev_done, hs.d2h) == cudaSuccess &&
+                 cudaStreamWaitEvent(stream, ev_done, 0) == cudaSuccess;
+  if (ev_alloc) {
+    drained = drained && cudaEventRecord(ev_alloc, hs.h2d) == cudaSuccess &&
+              cudaStreamWaitEvent(stream, ev_alloc, 0) == cudaSuccess;
+  }
+  if (!drained) {
+    // Without the events, fall back to waiting for the copy streams here.
+    cudaStreamSynchronize(hs.h2d);
+    cudaStreamSynchronize(hs.d2h);
   }
   if (dA) cudaFreeAsync(dA, stream);
   if (dB) cudaFreeAsync(dB, stream);
   if (dC) cudaFreeAsync(dC, stream);
   const bool synced = cudaStreamSynchronize(stream) == cudaSuccess;
+  for (int i = 0; i < nev; ++i)
+    if (ev[i]) cudaEventDestroy(ev[i]);
   if (!ok || !synced) {
     cudaGetLastError();
     return st != MT_OK ? st : MT_ERR_CUDA;
