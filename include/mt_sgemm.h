@@ -95,7 +95,8 @@ typedef struct {
     int pack_a;    /* MT_VARIANT_TF32X3: 0 = automatic, 1 = split A into a packed
                       copy by a separate kernel, 2 = split A inside the GEMM kernel
                       (A not transposed, 16-byte aligned, lda % 4 == 0) */
-    int reserved[1];
+    int group_m;   /* tile rows per group of the tile raster (tiles are walked
+                      down a group's rows, then across); 0 = automatic */
 } mt_config;
 
 /* What a call with the same arguments would launch. */

@@ -55,7 +55,7 @@ class mt_config(ctypes.Structure):
                 ("split_k", ctypes.c_int), ("fma", ctypes.c_int),
                 ("fault_inject", ctypes.c_int), ("wm", ctypes.c_int), ("wn", ctypes.c_int),
                 ("tm", ctypes.c_int), ("tn", ctypes.c_int), ("pack_a", ctypes.c_int),
-                ("reserved", ctypes.c_int * 1)]
+                ("group_m", ctypes.c_int)]
 
 
 class mt_plan(ctypes.Structure):
@@ -136,7 +136,8 @@ def lib():
 
 
 def make_config(variant="ffma", bm=0, bn=0, bk=0, stages=0, no_pad=False, split_k=0,
-                fma=0, fault_inject=0, wm=0, wn=0, tm=0, tn=0, pack_a=0) -> mt_config:
+                fma=0, fault_inject=0, wm=0, wn=0, tm=0, tn=0, pack_a=0,
+                group_m=0) -> mt_config:
     c = mt_config()
     c.variant = VARIANTS[variant] if isinstance(variant, str) else int(variant)
     c.bm, c.bn, c.bk, c.stages = bm, bn, bk, stages
@@ -147,6 +148,7 @@ def make_config(variant="ffma", bm=0, bn=0, bk=0, stages=0, no_pad=False, split_
     c.wm, c.wn = wm, wn
     c.tm, c.tn = tm, tn
     c.pack_a = pack_a
+    c.group_m = group_m
     return c
 
 

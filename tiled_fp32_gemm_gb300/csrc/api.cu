@@ -304,6 +304,7 @@ mt_status plan_f16(const Problem& P, const mt_config* cfg, int64_t smem_limit, i
     return MT_ERR_UNSUPPORTED;
   const bool pair = bm == 256;
   L->fault_inject = cfg ? cfg->fault_inject : 0;
+  if (cfg && cfg->group_m) L->group_m = cfg->group_m;
   mt_plan& p = L->plan;
   std::memset(&p, 0, sizeof(p));
   p.variant = MT_VARIANT_TC16;
@@ -351,7 +352,7 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
               cfg->no_pad < 0 || cfg->no_pad > 1 || cfg->split_k < 0 || cfg->fma < 0 ||
               cfg->fma > 2 || cfg->fault_inject < 0 || cfg->fault_inject > 1 || cfg->wm < 0 ||
               cfg->wn < 0 || cfg->tm < 0 || cfg->tn < 0 || cfg->pack_a < 0 ||
-              cfg->pack_a > 2))
+              cfg->pack_a > 2 || cfg->group_m < 0))
     return MT_ERR_INVALID_ARG;
   if (P.dtype)
     return plan_f16(P, cfg, smem_limit, sms, dev >= 0 ? mt::f16tc_pair_max_clusters(dev) : 0,
@@ -366,6 +367,7 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   const bool pad = !(cfg && cfg->no_pad);
   const bool trans = P.trans_a || P.trans_b;
   L->fault_inject = cfg ? cfg->fault_inject : 0;
+  if (cfg && cfg->group_m) L->group_m = cfg->group_m;
   mt_plan& p = L->plan;
   std::memset(&p, 0, sizeof(p));
   p.variant = variant;
