@@ -27,6 +27,7 @@ counts the work of all ranks.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -305,6 +306,14 @@ def run_gpu(args):
         bufs.append((w, a, b, c, A, B))
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
+    # SHA-256 of each workload's A then B bytes (fp32, row-major), so a result
+    # can be matched to its exact inputs.
+    input_hashes = {}
+    for (w, _a, _b, _c, A, B) in bufs:
+        h = hashlib.sha256()
+        h.update(A.numpy().tobytes())
+        h.update(B.numpy().tobytes())
+        input_hashes[w.name] = h.hexdigest()
     flops_step = sum(w.flops for (w, *_r) in bufs)
 
     bufs16 = {}
@@ -534,7 +543,8 @@ def run_gpu(args):
                        "variant": variant, "choices": main_cfg,
                        "l2": "inputs larger than L2 (192 MB and 768 MB per GEMM vs 129 MB); "
                              "the 8192^3 GEMM between 4096^3 GEMMs evicts their operands",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "inputs_sha256": input_hashes},
             "per_shape": per_shape,
             "roofline": roofline,
             "clocks": clk,
