@@ -92,9 +92,14 @@ typedef struct {
     int wn;        /* FFMA warp tile columns; 0 = automatic */
     int tm;        /* FFMA outputs per thread along M; 0 = automatic */
     int tn;        /* FFMA outputs per thread along N; 0 = automatic */
-    int pack_a;    /* MT_VARIANT_TF32X3: 0 = automatic, 1 = split A into a packed
+    int pack_a;    /* 0 = automatic.  MT_VARIANT_TF32X3: 1 = split A into a packed
                       copy by a separate kernel, 2 = split A inside the GEMM kernel
-                      (A not transposed, 16-byte aligned, lda % 4 == 0) */
+                      (A not transposed, 16-byte aligned, lda % 4 == 0).
+                      MT_VARIANT_FFMA: 1 = copy operands the 16-byte staging cannot
+                      read as stored (transposed, rows not whole float4s, unaligned)
+                      into zero-padded row-major scratch first, 2 = stage them as
+                      stored (4-byte copies); automatic copies from 2^30
+                      multiply-adds up.  The results are the same either way. */
     int group_m;   /* tile rows per group of the tile raster (tiles are walked
                       down a group's rows, then across); 0 = automatic */
 } mt_config;
@@ -115,7 +120,9 @@ typedef struct {
     int64_t smem_bytes;       /* dynamic shared memory per CTA */
     int64_t workspace_bytes;  /* device scratch the call needs (0 = none) */
     int pack_a;               /* MT_VARIANT_TF32X3: 1 = A packed by its own kernel,
-                                 2 = A split inside the GEMM kernel; 0 otherwise */
+                                 2 = A split inside the GEMM kernel.  MT_VARIANT_FFMA:
+                                 1 = operands copied into padded scratch first.
+                                 0 otherwise */
     int reserved;
 } mt_plan;
 

@@ -185,8 +185,20 @@ def test_budget_is_checked_before_launch():
 
 
 def test_alignment_selects_staging_width():
-    assert plan(4096, 4096, 4096)[1].vec_ab == 1
-    assert plan(4097, 3001, 2053)[1].vec_ab == 0
+    p = plan(4096, 4096, 4096)[1]
+    assert (p.vec_ab, p.vec_c, p.pack_a, p.workspace_bytes) == (1, 1, 0, 0)
+    # Rows that are not whole float4s: 4-byte staging as stored ...
+    p = plan(4097, 3001, 2053, pack_a=2)[1]
+    assert (p.vec_ab, p.vec_c, p.pack_a, p.workspace_bytes) == (0, 0, 0, 0)
+    # ... or, automatically for a product this large, copies of A (4097 x
+    # 2056) and B (2053 x 3004) with padded rows, then 16-byte staging and
+    # scalar stores of C (N = 3001).
+    p = plan(4097, 3001, 2053)[1]
+    assert (p.vec_ab, p.vec_c, p.pack_a) == (1, 0, 1)
+    rnd = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    assert p.workspace_bytes == rnd(4097 * 2056 * 4) + rnd(2053 * 3004 * 4)
+    # Small products stay as stored.
+    assert plan(100, 72, 81)[1].pack_a == 0
     st, p = mt.mt_sgemm_plan(4, 16, 32, 64, 64, 64, None, GB300_SMEM)  # 4-byte aligned A
     assert st == mt.MT_OK and p.vec_ab == 0
 

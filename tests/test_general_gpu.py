@@ -17,8 +17,10 @@ pytestmark = pytest.mark.gpu
 
 VARIANTS = [(dict(), 1e-5), (dict(bm=128, bn=128), 1e-5), (dict(bm=64, bn=64), 1e-5),
             (dict(variant="p18"), 1e-5), (dict(variant="tf32x3"), 5e-5),
-            (dict(variant="tf32x3", bn=64), 5e-5), (dict(variant="tf32x3", bm=256), 5e-5)]
-VIDS = ["ffma", "ffma128", "ffma64", "p18", "tf32x3", "tf32x3-bn64", "tf32x3-pair"]
+            (dict(variant="tf32x3", bn=64), 5e-5), (dict(variant="tf32x3", bm=256), 5e-5),
+            (dict(pack_a=1), 1e-5)]
+VIDS = ["ffma", "ffma128", "ffma64", "p18", "tf32x3", "tf32x3-bn64", "tf32x3-pair",
+        "ffma-copied"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -140,3 +142,24 @@ def test_ffma_transposes_need_a_tile_built_for_them():
     st = mt.mt_sgemm_general(1, 0, 64, 64, 64, 1.0, a.data_ptr(), 64, a.data_ptr(), 64, 0.0,
                              c.data_ptr(), 64, 0, mt.make_config(bm=256, bn=128))
     assert st == mt.MT_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("ta,tb", [(0, 0), (1, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("shape", [(257, 130, 77), (300, 260, 200)])
+def test_ffma_operand_copy_is_bit_identical(ta, tb, shape):
+    """Copying operands into padded row-major scratch (pack_a = 1) changes
+    the staging, not the arithmetic: the same FMA chain per output."""
+    M, N, K = shape
+    g = np.random.default_rng(M + N + K + ta + 2 * tb)
+    lda, ldb, ldc = (M if ta else K) + 3, (K if tb else N) + 1, N + 2
+    A = stored(g, K if ta else M, M if ta else K, lda)
+    B = stored(g, N if tb else K, K if tb else N, ldb)
+    C0 = stored(g, M, N, ldc)
+    assert mt.plan(M, N, K, pack_a=1)["pack_a"] == (1 if (K % 4 or N % 4) else 0)
+    copied = run_general(ta, tb, M, N, K, 1.25, A, lda, B, ldb, 0.5, C0, ldc, pack_a=1)
+    stored_ = run_general(ta, tb, M, N, K, 1.25, A, lda, B, ldb, 0.5, C0, ldc, pack_a=2)
+    assert np.array_equal(copied, stored_, equal_nan=True)
+    want, W = oracle.sgemm_general(A, B, C0, M, N, K, lda, ldb, ldc, 1.25, 0.5, ta, tb,
+                                   with_w=True)
+    err = np.abs(copied.reshape(M, ldc)[:, :N].astype(np.float64) - want.reshape(M, ldc)[:, :N])
+    assert np.all(err <= 1e-5 * W)

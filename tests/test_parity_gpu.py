@@ -80,12 +80,20 @@ def test_small_workloads_all_variants(name, cfg):
 
 
 def test_ragged_workload_full():
-    # 4097 x 3001 x 2053: every tile edge on M, N and K is masked, and the
-    # odd leading dimensions force the 4-byte staging path.
+    # 4097 x 3001 x 2053: every tile edge on M, N and K is masked.  Staged as
+    # stored, the odd leading dimensions force 4-byte copies; automatically,
+    # A and B are first copied into rows padded to whole float4s and staged
+    # in 16-byte chunks.  Both give the same FMA chain per output.
     A, B = gemm_inputs.make_workload("ragged_4097x3001x2053")
-    assert mt.plan(4097, 3001, 2053, a=A.cuda(), b=B.cuda())["vec_ab"] == 0
+    a, b = A.cuda(), B.cuda()
+    assert mt.plan(4097, 3001, 2053, a=a, b=b, pack_a=2)["vec_ab"] == 0
+    p = mt.plan(4097, 3001, 2053, a=a, b=b)
+    assert (p["vec_ab"], p["vec_c"], p["pack_a"]) == (1, 0, 1)
     Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
-    assert_within(run(A, B).numpy(), Cref, W, FFMA_TOL, "ragged")
+    as_stored = run(A, B, pack_a=2).numpy()
+    copied = run(A, B).numpy()
+    assert_within(as_stored, Cref, W, FFMA_TOL, "ragged, as stored")
+    assert np.array_equal(copied, as_stored)
 
 
 def sampled_rows(M, bm=128, extra=24, seed=0):

@@ -105,6 +105,11 @@ struct Launch {
   // GEMM kernel instead of packed.
   bool vec_a = false, vec_b = false;
   int split_a = 0;
+  // FFMA: operands copied into zero-padded row-major scratch first (row
+  // pitches ldo_a = round_up(K, 4), ldo_b = round_up(N, 4)); workspace
+  // layout [copy of A][copy of B][split-K partials].
+  bool prep_a = false, prep_b = false;
+  int64_t ldo_a = 0, ldo_b = 0, prep_b_offset = 0, partial_offset = 0;
 };
 
 mt_status check_dims(int64_t M, int64_t N, int64_t K) {
@@ -360,7 +365,8 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   if (variant == MT_VARIANT_TC16) return MT_ERR_UNSUPPORTED;  // 16-bit inputs only
   if (cfg && (cfg->wm || cfg->wn || cfg->tm || cfg->tn) && variant != MT_VARIANT_FFMA)
     return MT_ERR_UNSUPPORTED;
-  if (cfg && cfg->pack_a && variant != MT_VARIANT_TF32X3) return MT_ERR_UNSUPPORTED;
+  if (cfg && cfg->pack_a && variant != MT_VARIANT_TF32X3 && variant != MT_VARIANT_FFMA)
+    return MT_ERR_UNSUPPORTED;
   if (cfg && cfg->fault_inject && variant != MT_VARIANT_TF32X3) return MT_ERR_UNSUPPORTED;
   // 3xTF32 splits only its tail by itself (split_k = 1 turns that off).
   if (cfg && cfg->split_k > 1 && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
@@ -481,15 +487,46 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   const int i = pick_ffma(cfg, M, N, sms > 0 ? sms : 1);
   if (i < 0) return MT_ERR_UNSUPPORTED;
   const mt::FfmaEntry& E = e[i];
-  const void* kern = trans ? (pad ? E.kern_t[P.trans_a][P.trans_b] : nullptr)
-                           : E.kern[p.vec_ab][pad ? 1 : 0];
+  // Operands the 16-byte staging cannot read as stored (transposed, rows
+  // not whole float4s, unaligned base) are copied once into zero-padded
+  // row-major scratch when the product repays the pass (2^30 multiply-adds
+  // or more), or when asked (pack_a = 1; pack_a = 2 stages them as stored).
+  // The copy is exact and the zero padding multiplies zero-filled rows of
+  // the other operand, so the result is the same FMA chain.
+  const bool a_vec = !P.trans_a && K % 4 == 0 && P.lda % 4 == 0 && aligned16(P.A);
+  const bool b_vec = !P.trans_b && N % 4 == 0 && P.ldb % 4 == 0 && aligned16(P.B);
+  const bool c_vec = N % 4 == 0 && P.ldc % 4 == 0 && aligned16(P.C);
+  const int want_pack = cfg ? cfg->pack_a : 0;
+  const bool prep = pad && E.kern_vsc && (!a_vec || !b_vec) &&
+                    (want_pack == 1 ||
+                     (want_pack == 0 && static_cast<double>(M) * N * K >= 1073741824.0));
+  L->prep_a = prep && !a_vec;
+  L->prep_b = prep && !b_vec;
+  const bool a_ok = a_vec || L->prep_a, b_ok = b_vec || L->prep_b;
+  const bool b_staged_trans = P.trans_b && !L->prep_b;
+  const void* kern = nullptr;
+  if (a_ok && b_ok) {
+    // 16-byte staging of both; float4 or scalar stores of C.
+    kern = c_vec ? E.kern[1][pad ? 1 : 0] : (pad ? E.kern_vsc : E.kern[0][0]);
+    p.vec_ab = c_vec || pad ? 1 : 0;
+    p.vec_c = c_vec ? 1 : 0;
+  } else if (trans) {
+    kern = pad ? E.kern_t[P.trans_a][P.trans_b] : nullptr;
+    p.vec_ab = 0;
+    p.vec_c = 0;
+  } else {
+    kern = E.kern[0][pad ? 1 : 0];
+    p.vec_ab = 0;
+    p.vec_c = 0;
+  }
   if (!kern) return MT_ERR_UNSUPPORTED;
+  p.pack_a = prep ? 1 : 0;
   p.bm = E.bm; p.bn = E.bn; p.bk = E.bk; p.stages = E.stages; p.threads = E.threads;
   p.fma = E.packed ? 2 : 1;
   p.wm = E.wm; p.wn = E.wn; p.tm = E.tm; p.tn = E.tn;
   p.pad_a = pad ? E.pad_a : 0;
-  p.pad_b = P.trans_b ? E.pad_b_t : (pad ? E.pad_b : 0);
-  p.smem_bytes = P.trans_b ? E.smem_bytes_t : E.smem_bytes[pad ? 1 : 0];
+  p.pad_b = b_staged_trans ? E.pad_b_t : (pad ? E.pad_b : 0);
+  p.smem_bytes = b_staged_trans ? E.smem_bytes_t : E.smem_bytes[pad ? 1 : 0];
   L->entry = i;
   L->kern = kern;
   L->tiles_m = static_cast<int>(ceil_div(M, E.bm));
@@ -516,7 +553,12 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   L->kt_per_slice = static_cast<int>(ceil_div(ktiles, split));
   p.split_k = L->split;
   p.grid = full + (tiles - full) * split;
-  p.workspace_bytes = (tiles - full) * split * E.bm * E.bn * 4;
+  const auto round256 = [](int64_t b) { return (b + 255) / 256 * 256; };
+  L->ldo_a = ceil_div(std::max<int64_t>(K, 1), 4) * 4;
+  L->ldo_b = ceil_div(std::max<int64_t>(N, 1), 4) * 4;
+  L->prep_b_offset = L->prep_a ? round256(M * L->ldo_a * 4) : 0;
+  L->partial_offset = L->prep_b_offset + (L->prep_b ? round256(K * L->ldo_b * 4) : 0);
+  p.workspace_bytes = L->partial_offset + (tiles - full) * split * E.bm * E.bn * 4;
   // The budget check comes before anything is launched ("Part 18", section
   // "Shared-memory budget checks include stages and padding").
   if (p.smem_bytes > smem_limit) return MT_ERR_SMEM_BUDGET;
@@ -705,6 +747,7 @@ mt_status run(const Problem& P, cudaStream_t stream, const mt_config* cfg) {
   if (st != MT_OK) return st;
   void* ws = nullptr;
   cudaMemPool_t pool = nullptr;
+  bool ok = true;
   if (L.plan.workspace_bytes > 0) {
     st = pool_for(dev, &pool);
     if (st != MT_OK) return st;
@@ -713,14 +756,35 @@ mt_status run(const Problem& P, cudaStream_t stream, const mt_config* cfg) {
       cudaGetLastError();
       return MT_ERR_CUDA;
     }
-    args.partial = static_cast<float*>(ws);
+    char* base = static_cast<char*>(ws);
+    if (L.split > 1) args.partial = reinterpret_cast<float*>(base + L.partial_offset);
+    // Operands copied into the layout the 16-byte staging reads.
+    if (L.prep_a) {
+      float* a = reinterpret_cast<float*>(base);
+      ok = mt::launch_prep_operand(static_cast<const float*>(P.A), P.lda, P.trans_a != 0, a,
+                                   L.ldo_a, static_cast<int>(P.M), static_cast<int>(P.K),
+                                   stream) == cudaSuccess;
+      args.A = a;
+      args.lda = L.ldo_a;
+      args.trans_a = 0;
+    }
+    if (ok && L.prep_b) {
+      float* b = reinterpret_cast<float*>(base + L.prep_b_offset);
+      ok = mt::launch_prep_operand(static_cast<const float*>(P.B), P.ldb, P.trans_b != 0, b,
+                                   L.ldo_b, static_cast<int>(P.K), static_cast<int>(P.N),
+                                   stream) == cudaSuccess;
+      args.B = b;
+      args.ldb = L.ldo_b;
+      args.trans_b = 0;
+    }
   }
   void* params[] = {&args};
-  bool ok = cudaLaunchKernel(L.kern, dim3(static_cast<unsigned>(L.plan.grid)),
-                             dim3(static_cast<unsigned>(L.plan.threads)), params,
-                             static_cast<size_t>(L.plan.smem_bytes), stream) == cudaSuccess;
-  if (ok && ws) ok = mt::launch_splitk_reduce(args, L.plan.bm, L.plan.bn, L.plan.vec_c != 0,
-                                              stream) == cudaSuccess;
+  ok = ok && cudaLaunchKernel(L.kern, dim3(static_cast<unsigned>(L.plan.grid)),
+                              dim3(static_cast<unsigned>(L.plan.threads)), params,
+                              static_cast<size_t>(L.plan.smem_bytes), stream) == cudaSuccess;
+  if (ok && L.split > 1)
+    ok = mt::launch_splitk_reduce(args, L.plan.bm, L.plan.bn, L.plan.vec_c != 0, stream) ==
+         cudaSuccess;
   if (ws) cudaFreeAsync(ws, stream);
   if (!ok) {
     cudaGetLastError();

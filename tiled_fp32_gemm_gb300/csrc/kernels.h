@@ -20,7 +20,16 @@ struct FfmaEntry {
   // [0][0] unused; nullptr when not built.
   const void* kern_t[2][2];
   int pad_b_t, smem_bytes_t;  // B padding and shared memory when B is transposed
+  // 16-byte staging of A and B with scalar stores of C (padded rows);
+  // nullptr when not built.
+  const void* kern_vsc;
 };
+
+// Copies op(src) (R x cols, op = transpose when trans) into row-major `out`
+// with row pitch ldo >= cols, zero-filling columns cols..ldo-1: the layout
+// the 16-byte staging reads, for operands it cannot read as stored.
+cudaError_t launch_prep_operand(const float* src, int64_t ld, bool trans, float* out,
+                                int64_t ldo, int R, int cols, cudaStream_t stream);
 
 // C = beta * C over an M x N view with row stride ldc (zeros when beta is
 // 0: C is not read).  The whole product when alpha == 0 or K == 0.

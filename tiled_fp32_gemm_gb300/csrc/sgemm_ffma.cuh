@@ -297,13 +297,14 @@ __device__ __forceinline__ float pick(const float4& v, int c) {
 }
 
 // ---------------------------------------------------------------------------
-// AMODE, BMODE: StageMode of each operand.  C is written with float4 stores
-// when A is staged in 16-byte chunks (the host picks that mode only when C is
-// 16-byte aligned with ldc % 4 == 0 too), else with scalar stores.
-template <class T, int AMODE, int BMODE, bool PAD, bool PACKED>
+// AMODE, BMODE: StageMode of each operand.  VEC_C: C is written with float4
+// stores (N % 4 == 0, ldc % 4 == 0, C 16-byte aligned), else with scalar
+// stores.
+template <class T, int AMODE, int BMODE, bool PAD, bool PACKED,
+          bool VEC_C = (AMODE == STAGE_VEC)>
 __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     sgemm_ffma_kernel(GemmArgs args) {
-  constexpr bool VEC = AMODE == STAGE_VEC;
+  constexpr bool VEC = VEC_C;
   constexpr SmemLayout LA = T::a_layout(PAD);
   constexpr SmemLayout LB = T::b_layout(PAD, BMODE == STAGE_TRANS);
   extern __shared__ float4 smem_f4[];
@@ -504,6 +505,8 @@ FfmaEntry make_entry() {
         &sgemm_ffma_kernel<T, STAGE_SCALAR, STAGE_TRANS, true, PACKED>);
     e.kern_t[1][1] = reinterpret_cast<const void*>(
         &sgemm_ffma_kernel<T, STAGE_TRANS, STAGE_TRANS, true, PACKED>);
+    e.kern_vsc = reinterpret_cast<const void*>(
+        &sgemm_ffma_kernel<T, STAGE_VEC, STAGE_VEC, true, PACKED, false>);
   }
   return e;
 }
