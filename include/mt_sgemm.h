@@ -152,8 +152,8 @@ MT_API mt_status mt_sgemm_ex(const float *A, const float *B, float *C,
  * K x M); op(B) is K x N: B[k*ldb + j], or B[j*ldb + k] when trans_b (B
  * stored N x K); C[i][j] is at C[i*ldc + j].  The pages' loads are the
  * row-major case with packed rows ("My Triton From Scratch, Part 14: Shared
- * Memory Tiles", section "Cooperative copy mapping": only row-major order
- * (1, 0)); this entry point adds any leading dimension, transposed storage
+ * Memory Tiles", section "Cooperative copy mapping" supports the order
+ * (1, 0) alone); this entry point adds any leading dimension, transposed storage
  * and the alpha/beta update.  trans_a, trans_b: 0 or 1.  Leading dimensions
  * in elements: lda >= (trans_a ? M : K), ldb >= (trans_b ? K : N),
  * ldc >= N, each at least 1.  beta == 0: C is only written (NaN or Inf in

@@ -423,8 +423,8 @@ def test_fp16_bank_formula_and_simulator():
     assert all(R.element_bank(i, 2) == i // 2 % 32 for i in range(4096))
     assert all(R.element_bank(i, 4) == R.bank(i) for i in range(4096))
     # 32 lanes reading consecutive fp16 elements touch 16 words, two lanes
-    # per word: one transaction with the same-word broadcast (the page's
-    # "may cause 2-way conflicts" does not arise); reading them as half2
+    # per word: one transaction with the same-word broadcast (the two-way
+    # conflict the page warns of does not arise); reading them as half2
     # (4 bytes per lane) is one transaction too.
     assert R.wavefronts([2 * t for t in range(32)], 2) == 1
     assert R.wavefronts([4 * t for t in range(32)], 4) == 1
