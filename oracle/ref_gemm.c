@@ -11,9 +11,9 @@
  * section "Shared buffers are physical storage": dot(block<BMxBK>,
  * block<BKxBN>) -> block<BMxBN>, accumulated over the runtime K loop of
  * section "Staging inside a runtime K loop").  Masked, zero-filled edge
- * tiles contribute nothing ("Matching the safety mask": an out-of-bounds
- * element must contribute nothing), so the tiled result is, up to rounding
- * order, the untiled textbook product:
+ * tiles contribute nothing (section "Matching the safety mask": the masked
+ * load gives elements outside the matrix no weight), so the tiled result
+ * is, up to rounding order, the untiled textbook product:
  *
  *     C[i][j] = fp32( sum_{k=0}^{K-1} (double)A[i][k] * (double)B[k][j] )
  *

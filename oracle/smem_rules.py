@@ -25,8 +25,9 @@ Sources, by page and section:
 * "Optimize Shared Memory Tiling" (skills page), "Required reasoning
   process" steps 1-3: map each access to a bank, k different addresses in
   one bank cost k transactions, a broadcast costs one; "Correctness
-  requirements", the fp16 bank analysis: the bank of 16-bit element i is
-  (i * 2) / 4 % 32 = i / 2 % 32.
+  requirements", the fp16 bank analysis: a 16-bit element at index i
+  starts at byte 2i, so its bank is floor(2i / 4) mod 32, which is
+  floor(i / 2) mod 32.
 
 Readings of points the pages leave open (each is listed in the design
 notes): 64-bit and 128-bit accesses are served in phases of 16 and 8 lanes
@@ -39,7 +40,7 @@ page counts consecutive fp16 elements as a possible 2-way conflict.
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass
+from dataclasses import dataclass, field
 
 NUM_BANKS = 32
 BANK_BYTES = 4
@@ -53,7 +54,7 @@ def bank(word_offset: int) -> int:
 
 def element_bank(index: int, element_bytes: int) -> int:
     """Bank of element `index` of an array of `element_bytes`-byte elements
-    (skills page, fp16 analysis: (i * 2) / 4 % 32 for 16-bit elements)."""
+    (skills page, fp16 analysis: byte offset over 4, modulo 32 banks)."""
     return (index * element_bytes) // BANK_BYTES % NUM_BANKS
 
 
@@ -95,12 +96,19 @@ def vector_row_padding(columns: int, simultaneous_rows: int,
 # --- Part 18, "A shared buffer needs a physical row stride" ----------------
 @dataclass(frozen=True)
 class SharedBuffer:
-    """Physical layout of a staged rank-2 shared tile."""
+    """Physical layout of a staged rank-2 shared tile.  The derived extents
+    are fixed when the layout is made: a padded row holds columns +
+    row_padding elements, a stage rows of them, the buffer stage_count
+    stages."""
     rows: int
     columns: int
     row_padding: int = 0
     stage_count: int = 1
     element_bytes: int = 4
+    row_stride: int = field(init=False)
+    stage_size: int = field(init=False)
+    size: int = field(init=False)
+    nbytes: int = field(init=False)
 
     def __post_init__(self):
         if self.rows <= 0 or self.columns <= 0:
@@ -109,22 +117,12 @@ class SharedBuffer:
             raise ValueError("row padding must be non-negative")
         if self.stage_count < 1:
             raise ValueError("stage count must be at least 1")
-
-    @property
-    def row_stride(self) -> int:
-        return self.columns + self.row_padding
-
-    @property
-    def stage_size(self) -> int:
-        return self.rows * self.row_stride
-
-    @property
-    def size(self) -> int:
-        return self.stage_count * self.stage_size
-
-    @property
-    def nbytes(self) -> int:
-        return self.size * self.element_bytes
+        stride = self.columns + self.row_padding
+        per_stage = stride * self.rows
+        elements = per_stage * self.stage_count
+        for name, value in (("row_stride", stride), ("stage_size", per_stage),
+                            ("size", elements), ("nbytes", elements * self.element_bytes)):
+            object.__setattr__(self, name, value)
 
     def element(self, stage: int, row: int, column: int) -> int:
         if not (0 <= stage < self.stage_count and 0 <= row < self.rows

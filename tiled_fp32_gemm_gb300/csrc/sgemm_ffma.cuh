@@ -1,9 +1,10 @@
 // CUDA-core fp32 GEMM: tiled, multi-stage, register-tile FFMA kernel.
 //
 // What it computes is the tiled matmul of "My Triton From Scratch, Part 14:
-// Shared Memory Tiles" (section "Staging inside a runtime K loop": acc =
-// zeros; for k_base in range(0, K, BK): acc += dot(A tile, B tile); masked
-// store), with the physical choices of "Part 18: Shared Memory Optimization"
+// Shared Memory Tiles" (section "Staging inside a runtime K loop": an
+// accumulator that starts at zero takes the product of each staged A and B
+// tile as K advances in steps of BK, then a masked store), with the
+// physical choices of "Part 18: Shared Memory Optimization"
 // and of the skills page "Optimize Shared Memory Tiling":
 //
 //  * tile scheduler — one CTA per BM x BN tile of C ("The canonical source

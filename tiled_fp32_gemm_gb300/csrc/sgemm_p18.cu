@@ -3,9 +3,10 @@
 // parity and for measuring the bank rule, not for speed.
 //
 // Tile BM=4, BN=8, BK=16 with one warp (the one-warp layout the page
-// describes, section "What Version 18 does not do"); each thread owns one
-// output (tile_i, tile_j).  Per K tile:
-//   * the stage is (k_base / BK) & 1 (section "One stage versus two stages");
+// describes, section "What Version 18 does not do"); each lane owns one
+// output of the 4 x 8 tile.  Per K tile:
+//   * K tiles alternate between two stages (section "One stage versus two
+//     stages");
 //   * both tiles are copied cooperatively, thread t taking elements t, t+32,
 //     ... ("Part 14: Shared Memory Tiles", section "Cooperative copy
 //     mapping"), with 0.0 where the element lies outside M, N or K
@@ -31,65 +32,72 @@ namespace {
 constexpr int P18_BM = 4, P18_BN = 8, P18_BK = 16, P18_THREADS = 32;
 
 constexpr SmemLayout p18_a_layout(bool pad) {
-  // Four output rows (tile_i = 0..3) read A at the same dot_k.
+  // The four output rows of a tile read A at the same k at once.
   return SmemLayout{P18_BM, P18_BK, pad ? row_padding_rule(P18_BK, P18_BM) : 0, 2};
 }
 constexpr SmemLayout p18_b_layout() { return SmemLayout{P18_BK, P18_BN, 0, 2}; }
 }  // namespace
 
+// op(A)[i][k] or op(B)[k][j] from its storage, 0.0 outside rows x cols.
+__device__ __forceinline__ float fetch_operand(const float* base, int64_t ld, int trans, int i,
+                                               int j, int rows, int cols) {
+  if (i >= rows || j >= cols) return 0.0f;
+  return base[trans ? static_cast<int64_t>(j) * ld + i : static_cast<int64_t>(i) * ld + j];
+}
+
 template <bool PAD>
 __global__ void __launch_bounds__(P18_THREADS) sgemm_p18_kernel(GemmArgs args) {
   constexpr SmemLayout LA = p18_a_layout(PAD);
   constexpr SmemLayout LB = p18_b_layout();
-  __shared__ float dot_lhs[LA.size()];
-  __shared__ float dot_rhs[LB.size()];
+  // Both staged operands, double-buffered: A's stages, then B's.
+  __shared__ float staged[LA.size() + LB.size()];
+  float* a_tiles = staged;
+  float* b_tiles = staged + LA.size();
 
-  const int M = args.M, N = args.N, K = args.K;
-  const int tile = blockIdx.x;
-  const int block_m = (tile / args.tiles_n) * P18_BM;
-  const int block_n = (tile % args.tiles_n) * P18_BN;
-  const int tid = threadIdx.x;
-  const int tile_i = tid / P18_BN, tile_j = tid % P18_BN;
+  const int lane = threadIdx.x;
+  const int m0 = (blockIdx.x / args.tiles_n) * P18_BM;
+  const int n0 = (blockIdx.x % args.tiles_n) * P18_BN;
+  // This lane's output: row r, column c of the 4 x 8 tile.
+  const int r = lane / P18_BN, c = lane % P18_BN;
+  // Elements of the A tile (64) and of the B tile (128) this lane copies:
+  // lane, lane + 32, ... in row-major order of the tile.
+  constexpr int A_PER_LANE = P18_BM * P18_BK / P18_THREADS;
+  constexpr int B_PER_LANE = P18_BK * P18_BN / P18_THREADS;
 
-  float accumulator = 0.0f;
-  for (int k_base = 0; k_base < K; k_base += P18_BK) {
-    const int dot_stage = (k_base / P18_BK) & 1;
-    for (int index = tid; index < P18_BM * P18_BK; index += P18_THREADS) {
-      const int row = index / P18_BK, column = index % P18_BK;
-      const int global_row = block_m + row, global_column = k_base + column;
-      // op(A)[global_row][global_column], stored row-major or transposed.
-      dot_lhs[LA.offset(dot_stage, row, column)] =
-          global_row < M && global_column < K
-              ? args.A[args.trans_a ? static_cast<int64_t>(global_column) * args.lda + global_row
-                                    : static_cast<int64_t>(global_row) * args.lda + global_column]
-              : 0.0f;
+  const int k_tiles = (args.K + P18_BK - 1) / P18_BK;
+  float acc = 0.0f;
+  for (int kt = 0; kt < k_tiles; ++kt) {
+    const int buf = kt & 1;  // stage of this K tile: tiles alternate
+    const int k0 = kt * P18_BK;
+#pragma unroll
+    for (int e = 0; e < A_PER_LANE; ++e) {
+      const int slot = e * P18_THREADS + lane;
+      const int ar = slot / P18_BK, ak = slot % P18_BK;
+      a_tiles[LA.offset(buf, ar, ak)] =
+          fetch_operand(args.A, args.lda, args.trans_a, m0 + ar, k0 + ak, args.M, args.K);
     }
-    for (int index = tid; index < P18_BK * P18_BN; index += P18_THREADS) {
-      const int row = index / P18_BN, column = index % P18_BN;
-      const int global_row = k_base + row, global_column = block_n + column;
-      dot_rhs[LB.offset(dot_stage, row, column)] =
-          global_row < K && global_column < N
-              ? args.B[args.trans_b ? static_cast<int64_t>(global_column) * args.ldb + global_row
-                                    : static_cast<int64_t>(global_row) * args.ldb + global_column]
-              : 0.0f;
+#pragma unroll
+    for (int e = 0; e < B_PER_LANE; ++e) {
+      const int slot = e * P18_THREADS + lane;
+      const int bk = slot / P18_BN, bn = slot % P18_BN;
+      b_tiles[LB.offset(buf, bk, bn)] =
+          fetch_operand(args.B, args.ldb, args.trans_b, k0 + bk, n0 + bn, args.K, args.N);
     }
     __syncthreads();
-    // One 4-byte shared load per operand and k, as the page's generated loop
-    // reads them (volatile keeps the compiler from merging the A reads of a
-    // row into wider loads, which would change the access pattern the
-    // padding rule is about).
-    const volatile float* lhs = dot_lhs;
-    const volatile float* rhs = dot_rhs;
+    // Scalar shared reads, one per operand and k (volatile keeps the
+    // compiler from merging a row's A reads into wider loads, which would
+    // change the access pattern the padding rule is about).
+    const volatile float* av = a_tiles;
+    const volatile float* bv = b_tiles;
 #pragma unroll
-    for (int dot_k = 0; dot_k < P18_BK; ++dot_k)
-      accumulator = fmaf(lhs[LA.offset(dot_stage, tile_i, dot_k)],
-                         rhs[LB.offset(dot_stage, dot_k, tile_j)], accumulator);
+    for (int kk = 0; kk < P18_BK; ++kk)
+      acc = fmaf(av[LA.offset(buf, r, kk)], bv[LB.offset(buf, kk, c)], acc);
   }
-  const int out_row = block_m + tile_i, out_col = block_n + tile_j;
-  if (out_row < M && out_col < N) {
-    float* c = args.C + static_cast<int64_t>(out_row) * args.ldc + out_col;
-    const float v = args.alpha * accumulator;
-    *c = args.beta != 0.0f ? fmaf(args.beta, *c, v) : v;
+  const int row = m0 + r, col = n0 + c;
+  if (row < args.M && col < args.N) {
+    float* out = args.C + static_cast<int64_t>(row) * args.ldc + col;
+    const float v = args.alpha * acc;
+    *out = args.beta != 0.0f ? fmaf(args.beta, *out, v) : v;
   }
 }
 

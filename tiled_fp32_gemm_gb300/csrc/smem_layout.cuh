@@ -8,7 +8,8 @@
 // (distinct_banks = 32 / gcd(columns, 32), pad when more rows are read at
 // once).  Producers (cp.async staging) and consumers (the FMA loops) address
 // shared memory only through SmemLayout::offset, so they cannot disagree on
-// the stride (section "Every producer and consumer must use the new stride").
+// the stride (the page's section on producers and consumers sharing the
+// padded stride).
 #pragma once
 
 namespace mt {
