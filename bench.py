@@ -258,8 +258,11 @@ def tf32_clock_peak(sms: int, mhz: float) -> float:
 
 def launches_per_call(plan) -> int:
     """Kernels one library call launches: the GEMM (tf32x3: pack A, pack B,
-    GEMM), plus the slice reduce when the plan splits K."""
+    GEMM; FFMA with A staged K-major from a copy: the transposing copy of A,
+    then the GEMM), plus the slice reduce when the plan splits K."""
     base = 3 if plan["variant"] == 1 else 1
+    if plan["variant"] == 0 and plan["pack_a"] == 5:
+        base += 1  # the step's operands need no copy of B
     if plan["variant"] == 3 and not plan["vec_ab"]:
         base += 2  # the copy path pads both operands (the step's shapes never take it)
     return base + (1 if plan["split_k"] > 1 else 0)
@@ -458,6 +461,10 @@ def run_gpu(args):
                     "kernel": kernel_key,
                     "peak_basis": f"{sms} SMs x 128 FP32 lanes x 2 flop x {sm_max:.0f} MHz "
                                   "(max SM clock)",
+                    "note": "achieved = 2MNK / time of the whole call; with A staged "
+                            "K-major from a copy the call includes the transposing copy "
+                            "kernel, so it understates the GEMM kernel's own rate by that "
+                            "kernel's share",
                     "frac_at_run_clock": achieved / ffma_live if ffma_live else None}
 
     # The other fp32 variant, measured in the same run for comparison.
@@ -477,6 +484,33 @@ def run_gpu(args):
             o_ach = 3 * o_dom.flops / (statistics.mean(o_per[o_dom.name]) / 1e3) / 1e12
             variants["tf32x3"]["roofline"] = tf32_roofline(
                 o_ach, key_of("tf32x3", o_plans[o_dom.name], o_dom.name))
+        # Context, not a target: cuBLAS's fp32 GEMM (torch.matmul with TF32
+        # off) on the same operands, timed the same way.
+        tf32_prev = torch.backends.cuda.matmul.allow_tf32
+        torch.backends.cuda.matmul.allow_tf32 = False
+        try:
+            for (w, a, b, c) in operands(None):
+                torch.matmul(a, b, out=c)
+            cb_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                      for _ in bufs] for _ in range(o_steps)]
+            torch.cuda.synchronize()
+            for s_ in range(o_steps):
+                for i, (w, a, b, c) in enumerate(operands(None)):
+                    cb_ev[s_][i][0].record(stream)
+                    torch.matmul(a, b, out=c)
+                    cb_ev[s_][i][1].record(stream)
+            torch.cuda.synchronize()
+        finally:
+            torch.backends.cuda.matmul.allow_tf32 = tf32_prev
+        cb_per = {w.name: [cb_ev[s_][i][0].elapsed_time(cb_ev[s_][i][1]) for s_ in range(o_steps)]
+                  for i, (w, *_r) in enumerate(bufs)}
+        variants["cublas_fp32"] = {
+            "value": job_tflops(world, flops_step, o_steps,
+                                sum(sum(v) for v in cb_per.values()) / 1e3),
+            "unit": "TFLOP/s", "steps": o_steps, "impl": "torch.matmul, TF32 off (cuBLAS)",
+            "per_shape": {w.name: {"ms_median": statistics.median(cb_per[w.name]),
+                                   "tflops": w.flops / (statistics.median(cb_per[w.name]) / 1e3)
+                                   / 1e12} for (w, *_r) in bufs}}
         if variant != "tc16":
             # bf16 inputs, fp32 accumulation and output (tcgen05 kind::f16).
             h = {"dtype": "bf16"}
@@ -509,7 +543,11 @@ def run_gpu(args):
                                       w.K, sptr, cfg)
                 if st != mt.MT_OK:
                     raise mt.MtError(st, "mt_sgemm_host")
-        host_step()  # warm the stream-ordered pool
+        # Untimed warm-up steps, as for the device timing: the first calls on
+        # freshly pinned host buffers and pool blocks run slower (measured on
+        # GB300: the first two of each shape, up to 2x).
+        for _ in range(max(2, args.warmup)):
+            host_step()
         e2e_steps = max(1, min(args.steps, 5))
         barrier()
         t0 = time.perf_counter()

@@ -95,11 +95,21 @@ typedef struct {
     int pack_a;    /* 0 = automatic.  MT_VARIANT_TF32X3: 1 = split A into a packed
                       copy by a separate kernel, 2 = split A inside the GEMM kernel
                       (A not transposed, 16-byte aligned, lda % 4 == 0).
-                      MT_VARIANT_FFMA: 1 = copy operands the 16-byte staging cannot
-                      read as stored (transposed, rows not whole float4s, unaligned)
-                      into zero-padded row-major scratch first, 2 = stage them as
-                      stored (4-byte copies); automatic copies from 2^30
-                      multiply-adds up.  The results are the same either way. */
+                      MT_VARIANT_FFMA, row-major A tiles: 1 = copy operands the
+                      16-byte staging cannot read as stored (transposed, rows not
+                      whole float4s, unaligned) into zero-padded row-major scratch
+                      first, 2 = stage them as stored (4-byte copies).
+                      MT_VARIANT_FFMA, A tiles K-major (each k row holds BM rows of
+                      A; the micro-kernel reads four rows with one float4): 3 =
+                      source chosen automatically, 4 = gathered from A stored M x K
+                      inside the kernel (A not transposed), 5 = from a K x M copy of
+                      A (transposing A stored M x K); A stored K x M with M % 4 ==
+                      0, lda % 4 == 0 and a 16-byte aligned base is read as stored.
+                      B is copied into padded rows when the 16-byte staging cannot
+                      read it.  Automatic (0): K-major A when padding is on and B
+                      is 16-byte readable or M >= 512, from a copy when A is stored
+                      K x M or N >= 2048 with 2^30 multiply-adds or more, else
+                      gathered.  Every choice gives the same bits. */
     int group_m;   /* tile rows per group of the tile raster (tiles are walked
                       down a group's rows, then across); 0 = automatic */
 } mt_config;
@@ -121,7 +131,9 @@ typedef struct {
     int64_t workspace_bytes;  /* device scratch the call needs (0 = none) */
     int pack_a;               /* MT_VARIANT_TF32X3: 1 = A packed by its own kernel,
                                  2 = A split inside the GEMM kernel.  MT_VARIANT_FFMA:
-                                 1 = operands copied into padded scratch first.
+                                 1 = operands copied into padded scratch first
+                                 (row-major A tiles); 3 = A tiles K-major read as
+                                 stored, 4 = gathered, 5 = from a K x M copy.
                                  0 otherwise */
     int reserved;
 } mt_plan;
@@ -268,6 +280,14 @@ MT_API mt_status mt_gemm_mixed_plan(int dtype, int trans_a, int trans_b, int64_t
                                     const void *B, int64_t ldb, const float *C, int64_t ldc,
                                     const mt_config *cfg, int64_t smem_limit_bytes,
                                     mt_plan *out);
+
+/* The launch mt_sgemm_general would make for these arguments, as
+ * mt_sgemm_plan (pointers inspected for alignment only, may be NULL). */
+MT_API mt_status mt_sgemm_general_plan(int trans_a, int trans_b, int64_t M, int64_t N,
+                                       int64_t K, const float *A, int64_t lda,
+                                       const float *B, int64_t ldb, const float *C,
+                                       int64_t ldc, const mt_config *cfg,
+                                       int64_t smem_limit_bytes, mt_plan *out);
 
 /*
  * Fills *out with the launch a call with these arguments would make,

@@ -100,34 +100,62 @@ def plan(M, N, K, limit=GB300_SMEM, **kw):
 
 
 def ffma_warp_accesses(p):
-    """Byte addresses of warp 0's shared reads and cp.async writes, per instruction.
+    """Byte addresses of warp 0's shared reads and cp.async writes, per
+    instruction, each with its access width in bytes.
 
     Lane layout restated from the kernel's description: a warp tile of
-    WM x WN, TM x TN outputs per thread, lanes numbered M-fastest; thread
-    (lm, ln) reads A rows i*LM + lm and B columns g*LN*4 + ln*4.
+    WM x WN, TM x TN outputs per thread, lanes numbered M-fastest.  Row-major
+    A (pack_a 0-2): thread (lm, ln) reads A rows i*LM + lm, a float4 of four
+    k at a time.  K-major A (pack_a 3-5, tile As[k][m]): it reads rows in
+    fours, q*LM*4 + lm*4 .. +3, one float4 per k.  Either way it reads B
+    columns g*LN*4 + ln*4.  A K-major tile is filled with 16-byte chunks
+    along M (pack_a 3, 5) or gathered with 4-byte copies in 8 x 4 blocks,
+    8 lanes along K (pack_a 4).
     """
     WM, WN, TM, TN = p.wm, p.wn, p.tm, p.tn
     LM = WM // TM
     LN = 32 // LM
-    la = R.SharedBuffer(p.bm, p.bk, p.pad_a, p.stages)
+    kmajor = p.pack_a >= 3
+    la = (R.SharedBuffer(p.bk, p.bm, p.pad_a, p.stages) if kmajor
+          else R.SharedBuffer(p.bm, p.bk, p.pad_a, p.stages))
     lb = R.SharedBuffer(p.bk, p.bn, p.pad_b, p.stages)
     b_base = la.nbytes
     reads = []
-    for k4 in range(p.bk // 4):
-        for i in range(TM):
-            reads.append([4 * la.element(0, i * LM + lane % LM, k4 * 4) for lane in range(32)])
+    if kmajor:
+        for k in range(p.bk):
+            for q in range(TM // 4):
+                reads.append(([4 * la.element(0, k, q * LM * 4 + (lane % LM) * 4)
+                               for lane in range(32)], 16))
+    else:
+        for k4 in range(p.bk // 4):
+            for i in range(TM):
+                reads.append(([4 * la.element(0, i * LM + lane % LM, k4 * 4)
+                               for lane in range(32)], 16))
     for k in range(p.bk):
         for g in range(TN // 4):
-            reads.append([b_base + 4 * lb.element(0, k, g * LN * 4 + (lane // LM) * 4)
-                          for lane in range(32)])
+            reads.append(([b_base + 4 * lb.element(0, k, g * LN * 4 + (lane // LM) * 4)
+                           for lane in range(32)], 16))
     writes = []
-    a_chunks, b_chunks = p.bk // 4, p.bn // 4
-    for t in range(p.bm * a_chunks // p.threads):
-        writes.append([4 * la.element(0, (tid + t * p.threads) // a_chunks,
-                                      (tid % a_chunks) * 4) for tid in range(32)])
+    if p.pack_a == 4:
+        kb, warps = p.bk // 8, p.threads // 32
+        m_step = warps // kb * 4
+        for t in range(kb * (p.bm // 4) // warps):
+            writes.append(([4 * la.element(0, lane % 8, lane // 8 + t * m_step)
+                            for lane in range(32)], 4))
+    elif kmajor:
+        chunks = p.bm // 4
+        for t in range(p.bk * chunks // p.threads):
+            writes.append(([4 * la.element(0, (tid + t * p.threads) // chunks,
+                                           (tid % chunks) * 4) for tid in range(32)], 16))
+    else:
+        a_chunks = p.bk // 4
+        for t in range(p.bm * a_chunks // p.threads):
+            writes.append(([4 * la.element(0, (tid + t * p.threads) // a_chunks,
+                                           (tid % a_chunks) * 4) for tid in range(32)], 16))
+    b_chunks = p.bn // 4
     for t in range(p.bk * b_chunks // p.threads):
-        writes.append([b_base + 4 * lb.element(0, (tid + t * p.threads) // b_chunks,
-                                               (tid % b_chunks) * 4) for tid in range(32)])
+        writes.append(([b_base + 4 * lb.element(0, (tid + t * p.threads) // b_chunks,
+                                                (tid % b_chunks) * 4) for tid in range(32)], 16))
     return reads, writes
 
 
@@ -139,9 +167,41 @@ def test_ffma_layout_is_conflict_free(shape, tile):
     st, p = plan(*shape, **tile)
     assert st == mt.MT_OK
     reads, writes = ffma_warp_accesses(p)
-    for addrs in reads + writes:
-        assert R.conflict_degree(addrs, 16) == 1
+    for addrs, width in reads + writes:
+        assert R.conflict_degree(addrs, width) == 1
     assert p.pad_b == 0  # B is read as a broadcast: the rule gives no padding
+    if p.pack_a == 4:
+        # Gathered K-major A: 8 k rows are written at the same column at
+        # once, so the scalar rule pads by one word, rounded up to a float4.
+        assert p.pad_a == -(-R.row_padding(p.bm, 8) // 4) * 4 == 4
+    elif p.pack_a in (3, 5):
+        # K-major A read one k row at a time: the rule gives no padding.
+        assert p.pad_a == R.vector_row_padding(p.bm, 1) == 0
+
+
+def test_ffma_kmajor_gather_unpadded_would_conflict():
+    """The gathered K-major tile without its padding: the 8 k rows a warp
+    writes at one column fall in one bank (stride 128 words)."""
+    st, p = plan(1024, 1024, 1024, pack_a=4)
+    assert st == mt.MT_OK and p.pack_a == 4 and p.pad_a == 4
+    la = R.SharedBuffer(p.bk, p.bm, 0, p.stages)
+    addrs = [4 * la.element(0, lane % 8, lane // 8) for lane in range(32)]
+    assert R.conflict_degree(addrs, 4) == 8
+
+
+@pytest.mark.parametrize("shape,trans_a,want", [
+    ((4096, 4096, 4096), False, 5),   # large N: transposing copy of A
+    ((65536, 128, 4096), False, 4),   # narrow N: gathered inside the kernel
+    ((4096, 4096, 4096), True, 3),    # A stored K x M: read as stored
+    ((4097, 3001, 2053), True, 5),    # A stored K x M, M % 4 != 0: copy
+    ((100, 72, 80), False, 4),
+])
+def test_ffma_kmajor_source_choice(shape, trans_a, want):
+    M, N, K = shape
+    st, p = mt.mt_sgemm_general_plan(int(trans_a), 0, M, N, K, None, M if trans_a else K,
+                                     None, N, None, N, None, GB300_SMEM)
+    assert st == mt.MT_OK and p.pack_a == want, p.pack_a
+    assert p.wm and p.tm % 4 == 0
 
 
 @pytest.mark.parametrize("warp", [dict(wm=64, wn=64), dict(wm=32, wn=64)])
@@ -149,8 +209,8 @@ def test_ffma_unpadded_layout_conflicts(warp):
     st, p = plan(4096, 4096, 4096, bm=128, bn=128, bk=32, stages=3, no_pad=True, fma=2, **warp)
     assert st == mt.MT_OK and p.pad_a == 0
     reads, _ = ffma_warp_accesses(p)
-    assert max(R.conflict_degree(a, 16) for a in reads) > 1
-    st, q = plan(4096, 4096, 4096, bm=128, bn=128, bk=32, stages=3, fma=2, **warp)
+    assert max(R.conflict_degree(a, w) for a, w in reads) > 1
+    st, q = plan(4096, 4096, 4096, bm=128, bn=128, bk=32, stages=3, fma=2, pack_a=1, **warp)
     rows_per_phase = min(q.wm // q.tm, 8)
     assert q.pad_a == R.vector_row_padding(32, rows_per_phase) == 4
 
@@ -185,20 +245,31 @@ def test_budget_is_checked_before_launch():
 
 
 def test_alignment_selects_staging_width():
+    rnd = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    # Default: A staged K-major from a transposed copy (K x M) for a product
+    # this wide, B and C with 16-byte accesses.
     p = plan(4096, 4096, 4096)[1]
-    assert (p.vec_ab, p.vec_c, p.pack_a, p.workspace_bytes) == (1, 1, 0, 0)
-    # Rows that are not whole float4s: 4-byte staging as stored ...
+    assert (p.vec_ab, p.vec_c, p.pack_a) == (1, 1, 5)
+    assert p.workspace_bytes == 4096 * 4096 * 4
+    # Row-major A tiles (pack_a = 2): rows that are not whole float4s are
+    # staged as stored with 4-byte copies ...
     p = plan(4097, 3001, 2053, pack_a=2)[1]
     assert (p.vec_ab, p.vec_c, p.pack_a, p.workspace_bytes) == (0, 0, 0, 0)
-    # ... or, automatically for a product this large, copies of A (4097 x
-    # 2056) and B (2053 x 3004) with padded rows, then 16-byte staging and
-    # scalar stores of C (N = 3001).
-    p = plan(4097, 3001, 2053)[1]
+    # ... or (pack_a = 1) copied into padded rows, A 4097 x 2056 and B
+    # 2053 x 3004, then staged in 16-byte chunks; C has scalar stores
+    # (N = 3001).
+    p = plan(4097, 3001, 2053, pack_a=1)[1]
     assert (p.vec_ab, p.vec_c, p.pack_a) == (1, 0, 1)
-    rnd = lambda b: (b + 255) // 256 * 256  # noqa: E731
     assert p.workspace_bytes == rnd(4097 * 2056 * 4) + rnd(2053 * 3004 * 4)
-    # Small products stay as stored.
-    assert plan(100, 72, 81)[1].pack_a == 0
+    # Automatic: K-major A from a copy (2053 x 4100) and B from a copy with
+    # padded rows, on 64 x 128 tiles (too few 128 x 128 tiles for three
+    # full waves).
+    p = plan(4097, 3001, 2053)[1]
+    assert (p.vec_ab, p.vec_c, p.pack_a, p.bm, p.bn) == (1, 0, 5, 64, 128)
+    assert p.workspace_bytes == rnd(2053 * 4100 * 4) + rnd(2053 * 3004 * 4)
+    # Small products gather K-major A inside the kernel: no copy.
+    p = plan(100, 72, 81)[1]
+    assert (p.pack_a, p.workspace_bytes, p.vec_ab) == (4, 0, 0)
     st, p = mt.mt_sgemm_plan(4, 16, 32, 64, 64, 64, None, GB300_SMEM)  # 4-byte aligned A
     assert st == mt.MT_OK and p.vec_ab == 0
 
@@ -231,16 +302,20 @@ def test_no_cpu_fallback_without_gpu():
 
 def test_split_k_plan():
     # No automatic split; an explicit split applies to every tile and needs
-    # one partial tile per slice; split_k = 1 is the same as none.
+    # one partial tile per slice (after the 64 MB transposed copy of A);
+    # split_k = 1 is the same as none.
+    a_copy = 4096 * 4096 * 4
     st, p = plan(4096, 4096, 4096)
     assert st == mt.MT_OK and (p.bm, p.bn) == (128, 128)
-    assert p.split_k == 1 and p.workspace_bytes == 0
+    assert p.split_k == 1 and p.workspace_bytes == a_copy
     st, p = plan(4096, 4096, 4096, split_k=2)
-    assert p.grid == 1024 * 2 and p.workspace_bytes == 1024 * 2 * 128 * 128 * 4
+    assert p.grid == 1024 * 2 and p.workspace_bytes == a_copy + 1024 * 2 * 128 * 128 * 4
     st, p = plan(4096, 4096, 4096, split_k=3)
     assert p.split_k == 3 and p.grid == 1024 * 3
     st, p = plan(4096, 4096, 4096, split_k=1)
-    assert p.split_k == 1 and p.grid == 1024 and p.workspace_bytes == 0
+    assert p.split_k == 1 and p.grid == 1024 and p.workspace_bytes == a_copy
+    st, p = plan(4096, 4096, 4096, split_k=2, pack_a=2)
+    assert p.workspace_bytes == 1024 * 2 * 128 * 128 * 4
     # A split larger than the K tiles is clamped to one K tile per slice.
     st, p = plan(64, 64, 64, split_k=4)
     assert p.split_k == 2

@@ -18,9 +18,18 @@ pytestmark = pytest.mark.gpu
 VARIANTS = [(dict(), 1e-5), (dict(bm=128, bn=128), 1e-5), (dict(bm=64, bn=64), 1e-5),
             (dict(variant="p18"), 1e-5), (dict(variant="tf32x3"), 5e-5),
             (dict(variant="tf32x3", bn=64), 5e-5), (dict(variant="tf32x3", bm=256), 5e-5),
-            (dict(pack_a=1), 1e-5)]
+            (dict(pack_a=1), 1e-5), (dict(pack_a=2), 1e-5),
+            (dict(pack_a=4), 1e-5), (dict(pack_a=5), 1e-5),
+            (dict(bm=64, bn=128, pack_a=4), 1e-5), (dict(bm=64, bn=128, pack_a=5), 1e-5),
+            (dict(bm=64, bn=64, pack_a=5), 1e-5), (dict(pack_a=4, split_k=3), 1e-5)]
 VIDS = ["ffma", "ffma128", "ffma64", "p18", "tf32x3", "tf32x3-bn64", "tf32x3-pair",
-        "ffma-copied"]
+        "ffma-copied", "ffma-rowmajor", "ffma-kgather", "ffma-kcopy", "ffma64x128-kgather",
+        "ffma64x128-kcopy", "ffma64-kcopy", "ffma-kgather-split3"]
+
+
+def supported(cfg, ta):
+    """A gathered K-major A tile reads A stored M x K only."""
+    return not (cfg.get("pack_a") == 4 and ta)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -55,6 +64,8 @@ def run_general(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, **cfg):
 @pytest.mark.parametrize("shape,pads", [((133, 97, 71), (3, 5, 7)), ((260, 300, 96), (4, 8, 4)),
                                         ((31, 17, 300), (0, 1, 2))])
 def test_general_matches_oracle(cfg, tol, ta, tb, shape, pads):
+    if not supported(cfg, ta):
+        pytest.skip("gathered K-major A needs A stored M x K")
     M, N, K = shape
     g = np.random.default_rng(M + 7 * N + 13 * K + 2 * ta + tb)
     lda = (M if ta else K) + pads[0]
@@ -78,6 +89,8 @@ def test_general_integers_exact(cfg, tol):
     M, N, K = 70, 90, 130
     g = np.random.default_rng(5)
     for ta, tb in [(0, 0), (1, 1)]:
+        if not supported(cfg, ta):
+            continue
         lda, ldb, ldc = (M if ta else K) + 2, (K if tb else N) + 3, N + 1
         A = stored(g, K if ta else M, M if ta else K, lda, "int")
         B = stored(g, N if tb else K, K if tb else N, ldb, "int")
@@ -162,4 +175,37 @@ def test_ffma_operand_copy_is_bit_identical(ta, tb, shape):
     want, W = oracle.sgemm_general(A, B, C0, M, N, K, lda, ldb, ldc, 1.25, 0.5, ta, tb,
                                    with_w=True)
     err = np.abs(copied.reshape(M, ldc)[:, :N].astype(np.float64) - want.reshape(M, ldc)[:, :N])
+    assert np.all(err <= 1e-5 * W)
+
+
+@pytest.mark.parametrize("ta,tb", [(0, 0), (1, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("shape,lda_pad", [((257, 130, 77), 3), ((300, 260, 200), 0),
+                                           ((1000, 2200, 96), 4)])
+@pytest.mark.parametrize("tile", [dict(), dict(bm=64, bn=128), dict(bm=64, bn=64)],
+                         ids=["128x128", "64x128", "64x64"])
+def test_ffma_kmajor_a_is_bit_identical(ta, tb, shape, lda_pad, tile):
+    """A staged K-major (read as stored K x M, gathered from M x K inside
+    the kernel, or from a K x M copy) changes which rows a float4 holds, not
+    the arithmetic: every source gives the row-major tiles' FMA chain bit for
+    bit.  Padding columns of A hold NaN: a 16-byte chunk that reaches past M
+    only feeds rows that are never stored."""
+    M, N, K = shape
+    g = np.random.default_rng(M + N + K + ta + 2 * tb)
+    lda, ldb, ldc = (M if ta else K) + lda_pad, (K if tb else N) + 1, N + 2
+    A = stored(g, K if ta else M, M if ta else K, lda)
+    B = stored(g, N if tb else K, K if tb else N, ldb)
+    C0 = stored(g, M, N, ldc)
+    # Reference: row-major A tiles of the default tile, staged as stored.
+    # Every FFMA tile sums each output over k in order with one fused
+    # multiply-add per k, so the tile does not change the bits either.
+    ref = run_general(ta, tb, M, N, K, 1.25, A, lda, B, ldb, 0.5, C0, ldc, pack_a=2)
+    for pack in (3, 4, 5):
+        if pack == 4 and ta:
+            continue
+        got = run_general(ta, tb, M, N, K, 1.25, A, lda, B, ldb, 0.5, C0, ldc, pack_a=pack,
+                          **tile)
+        assert np.array_equal(got, ref, equal_nan=True), pack
+    want, W = oracle.sgemm_general(A, B, C0, M, N, K, lda, ldb, ldc, 1.25, 0.5, ta, tb,
+                                   with_w=True)
+    err = np.abs(ref.reshape(M, ldc)[:, :N].astype(np.float64) - want.reshape(M, ldc)[:, :N])
     assert np.all(err <= 1e-5 * W)

@@ -23,6 +23,12 @@ FFMA_TOL = 1e-5
 FFMA_CONFIGS = [
     dict(),                                           # automatic
     dict(bm=128, bn=128, bk=32, stages=3, fma=2),     # 4 warps of 64 x 64
+    dict(pack_a=2),                                   # row-major A tiles
+    dict(pack_a=4),                                   # K-major A, gathered
+    dict(pack_a=5),                                   # K-major A, from a copy
+    dict(bm=64, bn=128, pack_a=4),
+    dict(bm=64, bn=128, pack_a=5),
+    dict(bm=64, bn=64, pack_a=5),
     dict(bm=128, bn=128, bk=32, stages=3, fma=2, wm=32, wn=64),
     dict(bm=128, bn=128, bk=32, stages=3, fma=2, wm=64, wn=32),
     dict(bm=128, bn=128, bk=16, stages=4, fma=2),
@@ -80,20 +86,24 @@ def test_small_workloads_all_variants(name, cfg):
 
 
 def test_ragged_workload_full():
-    # 4097 x 3001 x 2053: every tile edge on M, N and K is masked.  Staged as
-    # stored, the odd leading dimensions force 4-byte copies; automatically,
-    # A and B are first copied into rows padded to whole float4s and staged
-    # in 16-byte chunks.  Both give the same FMA chain per output.
+    # 4097 x 3001 x 2053: every tile edge on M, N and K is masked.  Row-major
+    # A tiles staged as stored: the odd leading dimensions force 4-byte
+    # copies.  Row-major A tiles from copies (pack_a = 1): A and B copied
+    # into rows padded to whole float4s, then 16-byte chunks.  Automatically:
+    # A staged K-major from a transposed copy, B from a padded copy, on
+    # 64 x 128 tiles; and A gathered K-major inside the kernel (pack_a = 4).
+    # All give the same FMA chain per output.
     A, B = gemm_inputs.make_workload("ragged_4097x3001x2053")
     a, b = A.cuda(), B.cuda()
     assert mt.plan(4097, 3001, 2053, a=a, b=b, pack_a=2)["vec_ab"] == 0
+    assert mt.plan(4097, 3001, 2053, a=a, b=b, pack_a=1)["pack_a"] == 1
     p = mt.plan(4097, 3001, 2053, a=a, b=b)
-    assert (p["vec_ab"], p["vec_c"], p["pack_a"]) == (1, 0, 1)
+    assert (p["vec_ab"], p["vec_c"], p["pack_a"], p["bm"], p["bn"]) == (1, 0, 5, 64, 128)
     Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
     as_stored = run(A, B, pack_a=2).numpy()
-    copied = run(A, B).numpy()
     assert_within(as_stored, Cref, W, FFMA_TOL, "ragged, as stored")
-    assert np.array_equal(copied, as_stored)
+    for choice in (dict(pack_a=1), dict(), dict(pack_a=4)):
+        assert np.array_equal(run(A, B, **choice).numpy(), as_stored), choice
 
 
 def sampled_rows(M, bm=128, extra=24, seed=0):

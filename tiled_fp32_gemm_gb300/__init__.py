@@ -5,7 +5,8 @@ by ``tiled_fp32_gemm_gb300.build``).  This module only marshals arguments:
 
 * ``mt_sgemm``, ``mt_sgemm_ex``, ``mt_sgemm_general``, ``mt_sgemm_host``,
   ``mt_sgemm_tf32x3_noalloc``,
-  ``mt_sgemm_plan``, ``mt_gemm_mixed``, ``mt_gemm_mixed_general``,
+  ``mt_sgemm_plan``, ``mt_sgemm_general_plan``, ``mt_gemm_mixed``,
+  ``mt_gemm_mixed_general``,
   ``mt_gemm_mixed_plan``,
   ``mt_smem_row_padding``, ``mt_smem_vector_row_padding``,
   ``mt_smem_layout_make``, ``mt_smem_layout_offset``, ``mt_device_status``,
@@ -103,6 +104,8 @@ SIGNATURES = {
                                    ctypes.POINTER(mt_config)]),
     "mt_gemm_mixed_plan": (_I, [_I, _I, _I, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64,
                                 ctypes.POINTER(mt_config), _I64, ctypes.POINTER(mt_plan)]),
+    "mt_sgemm_general_plan": (_I, [_I, _I, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64,
+                                   ctypes.POINTER(mt_config), _I64, ctypes.POINTER(mt_plan)]),
     "mt_smem_row_padding": (_I, [_I, _I]),
     "mt_smem_vector_row_padding": (_I, [_I, _I]),
     "mt_smem_layout_make": (_I, [_I, _I, _I, _I, ctypes.POINTER(mt_smem_layout)]),
@@ -213,6 +216,16 @@ def mt_gemm_mixed_plan(dtype: int, trans_a: int, trans_b: int, M: int, N: int, K
     st = lib().mt_gemm_mixed_plan(dtype, trans_a, trans_b, M, N, K, A, lda, B, ldb, C, ldc,
                                   ctypes.byref(cfg) if cfg is not None else None,
                                   smem_limit_bytes, ctypes.byref(out))
+    return st, out
+
+
+def mt_sgemm_general_plan(trans_a: int, trans_b: int, M: int, N: int, K: int,
+                          A: int | None, lda: int, B: int | None, ldb: int, C: int | None,
+                          ldc: int, cfg: mt_config | None = None, smem_limit_bytes: int = 0):
+    out = mt_plan()
+    st = lib().mt_sgemm_general_plan(trans_a, trans_b, M, N, K, A, lda, B, ldb, C, ldc,
+                                     ctypes.byref(cfg) if cfg is not None else None,
+                                     smem_limit_bytes, ctypes.byref(out))
     return st, out
 
 

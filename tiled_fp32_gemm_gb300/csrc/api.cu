@@ -110,6 +110,10 @@ struct Launch {
   // layout [copy of A][copy of B][split-K partials].
   bool prep_a = false, prep_b = false;
   int64_t ldo_a = 0, ldo_b = 0, prep_b_offset = 0, partial_offset = 0;
+  // FFMA with A staged K-major: A is read as a K x M matrix (stored so, or
+  // copied so into scratch with pitch ldo_a = round_up(M, 4) when
+  // prep_a_kmajor), or gathered from row-major storage (a_gather).
+  bool a_kmajor = false, prep_a_kmajor = false, a_gather = false;
 };
 
 mt_status check_dims(int64_t M, int64_t N, int64_t K) {
@@ -175,7 +179,7 @@ mt_status check_problem(const Problem& P) {
 // micro-kernel form) must all match one entry; the first match in table
 // order wins, so each tile's default warp layout comes first.  Otherwise
 // the choice is automatic.
-int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms) {
+int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms, bool kmajor) {
   int count = 0;
   const mt::FfmaEntry* e = mt::ffma_entries(&count);
   const bool explicit_tile = cfg && (cfg->bm || cfg->bn || cfg->bk || cfg->stages || cfg->wm ||
@@ -197,18 +201,28 @@ int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms) {
     }
     return -1;
   }
-  // Automatic: 128x128 tiles when they fill every SM twice over, else
-  // 64x64 tiles for more CTAs.
-  int big = -1, small = -1;
+  // Automatic.  Row-major A: 128x128 tiles when they fill every SM twice
+  // over, else 64x64 tiles for more CTAs.  K-major A: 128x128 tiles from
+  // three full waves (2 CTAs per SM) up, else 64x128 tiles (3 CTAs per SM)
+  // when they fill one wave, else 64x64.  Measured on GB300 (K-major A):
+  // 4097 x 3001 x 2053 54.7 TFLOP/s on 64x128 tiles against 49.3 on
+  // 128x128, 65536 x 128 x 4096 60.7 against 53.5.
+  int big = -1, mid = -1, small = -1;
   for (int i = 0; i < count; ++i) {
     if (!e[i].packed) continue;
     if (big < 0 && e[i].bm == 128 && e[i].bn == 128 && e[i].bk == 32 && e[i].stages == 3)
       big = i;
+    if (mid < 0 && e[i].bm == 64 && e[i].bn == 128 && e[i].kern_km[0]) mid = i;
     if (small < 0 && e[i].bm == 64 && e[i].bn == 64) small = i;
   }
   const int64_t tiles_big = ceil_div(M, 128) * ceil_div(N, 128);
-  if (tiles_big >= 2 * static_cast<int64_t>(sms) || small < 0) return big;
-  return small;
+  if (!kmajor) {
+    if (tiles_big >= 2 * static_cast<int64_t>(sms) || small < 0) return big;
+    return small;
+  }
+  if (tiles_big >= 6 * static_cast<int64_t>(sms) || (mid < 0 && small < 0)) return big;
+  if (mid >= 0 && ceil_div(M, 64) * ceil_div(N, 128) >= 3 * static_cast<int64_t>(sms)) return mid;
+  return small >= 0 ? small : big;
 }
 
 // Tile width of a persistent tensor-core kernel: the widest tile wins
@@ -357,7 +371,7 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
               cfg->no_pad < 0 || cfg->no_pad > 1 || cfg->split_k < 0 || cfg->fma < 0 ||
               cfg->fma > 2 || cfg->fault_inject < 0 || cfg->fault_inject > 1 || cfg->wm < 0 ||
               cfg->wn < 0 || cfg->tm < 0 || cfg->tn < 0 || cfg->pack_a < 0 ||
-              cfg->pack_a > 2 || cfg->group_m < 0))
+              cfg->pack_a > 5 || cfg->group_m < 0))
     return MT_ERR_INVALID_ARG;
   if (P.dtype)
     return plan_f16(P, cfg, smem_limit, sms, dev >= 0 ? mt::f16tc_pair_max_clusters(dev) : 0,
@@ -367,6 +381,7 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
     return MT_ERR_UNSUPPORTED;
   if (cfg && cfg->pack_a && variant != MT_VARIANT_TF32X3 && variant != MT_VARIANT_FFMA)
     return MT_ERR_UNSUPPORTED;
+  if (cfg && cfg->pack_a >= 3 && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
   if (cfg && cfg->fault_inject && variant != MT_VARIANT_TF32X3) return MT_ERR_UNSUPPORTED;
   // 3xTF32 splits only its tail by itself (split_k = 1 turns that off).
   if (cfg && cfg->split_k > 1 && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
@@ -484,7 +499,15 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
 
   int count = 0;
   const mt::FfmaEntry* e = mt::ffma_entries(&count);
-  const int i = pick_ffma(cfg, M, N, sms > 0 ? sms : 1);
+  // A staged K-major (pack_a 3-5, and automatically when padding is on
+  // and B can be staged in 16-byte chunks, as stored or, for products with
+  // 512 rows or more, from a copy): the micro-kernel then reads four rows of
+  // A with one float4 per k, which measured 9-12 % faster on GB300 than
+  // row-major A tiles (4096^3 67.4 against 59.9 TFLOP/s with A given K x M).
+  const int want_pack = cfg ? cfg->pack_a : 0;
+  const bool b_vec = !P.trans_b && N % 4 == 0 && P.ldb % 4 == 0 && aligned16(P.B);
+  const bool kmajor = want_pack >= 3 || (want_pack == 0 && pad && (b_vec || M >= 512));
+  const int i = pick_ffma(cfg, M, N, sms > 0 ? sms : 1, kmajor);
   if (i < 0) return MT_ERR_UNSUPPORTED;
   const mt::FfmaEntry& E = e[i];
   // Operands the 16-byte staging cannot read as stored (transposed, rows
@@ -494,18 +517,53 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   // The copy is exact and the zero padding multiplies zero-filled rows of
   // the other operand, so the result is the same FMA chain.
   const bool a_vec = !P.trans_a && K % 4 == 0 && P.lda % 4 == 0 && aligned16(P.A);
-  const bool b_vec = !P.trans_b && N % 4 == 0 && P.ldb % 4 == 0 && aligned16(P.B);
   const bool c_vec = N % 4 == 0 && P.ldc % 4 == 0 && aligned16(P.C);
-  const int want_pack = cfg ? cfg->pack_a : 0;
-  const bool prep = pad && E.kern_vsc && (!a_vec || !b_vec) &&
+  const auto round256 = [](int64_t b) { return (b + 255) / 256 * 256; };
+  if (kmajor && !(pad && E.kern_km[0] && E.kern_kg[0])) {
+    if (want_pack >= 3) return MT_ERR_UNSUPPORTED;
+  } else if (kmajor) {
+    // The K-major A tile comes straight from A stored K x M when its rows
+    // are whole float4s; otherwise from a K x M copy (pack_a = 5, or
+    // automatically for A stored K x M, and for A stored M x K when N >=
+    // 2048 and the product has 2^30 multiply-adds or more: the transposing
+    // pass costs about 70 / N of the product), else gathered element by
+    // element from A stored M x K inside the GEMM kernel (pack_a = 4, about
+    // 9 % slower than a K-major source on 4096^3).  B as the 16-byte staging
+    // reads it, copied first when it cannot be read as stored.
+    const bool direct = P.trans_a && M % 4 == 0 && P.lda % 4 == 0 && aligned16(P.A);
+    if (want_pack == 4 && P.trans_a) return MT_ERR_UNSUPPORTED;
+    const bool copy = want_pack == 5 ||
+                      (want_pack != 4 && !direct &&
+                       (P.trans_a ||
+                        (N >= 2048 && static_cast<double>(M) * N * K >= 1073741824.0)));
+    L->a_kmajor = true;
+    L->prep_a_kmajor = copy;
+    L->a_gather = !direct && !copy;
+    L->prep_b = !b_vec;
+    L->ldo_a = ceil_div(std::max<int64_t>(M, 1), 4) * 4;
+    L->ldo_b = ceil_div(std::max<int64_t>(N, 1), 4) * 4;
+    L->kern = L->a_gather ? E.kern_kg[c_vec ? 1 : 0] : E.kern_km[c_vec ? 1 : 0];
+    p.vec_ab = L->a_gather ? 0 : 1;
+    p.vec_c = c_vec ? 1 : 0;
+    p.pack_a = L->a_gather ? 4 : copy ? 5 : 3;
+    p.pad_a = L->a_gather ? E.pad_a_kg : 0;
+    p.pad_b = E.pad_b;
+    p.smem_bytes = L->a_gather ? E.smem_bytes_kg : E.smem_bytes_km;
+    L->prep_b_offset = L->prep_a_kmajor ? round256(K * L->ldo_a * 4) : 0;
+  }
+  const bool prep = !L->a_kmajor && pad && E.kern_vsc && (!a_vec || !b_vec) &&
                     (want_pack == 1 ||
                      (want_pack == 0 && static_cast<double>(M) * N * K >= 1073741824.0));
-  L->prep_a = prep && !a_vec;
-  L->prep_b = prep && !b_vec;
+  if (!L->a_kmajor) {
+    L->prep_a = prep && !a_vec;
+    L->prep_b = prep && !b_vec;
+  }
   const bool a_ok = a_vec || L->prep_a, b_ok = b_vec || L->prep_b;
   const bool b_staged_trans = P.trans_b && !L->prep_b;
   const void* kern = nullptr;
-  if (a_ok && b_ok) {
+  if (L->a_kmajor) {
+    kern = L->kern;
+  } else if (a_ok && b_ok) {
     // 16-byte staging of both; float4 or scalar stores of C.
     kern = c_vec ? E.kern[1][pad ? 1 : 0] : (pad ? E.kern_vsc : E.kern[0][0]);
     p.vec_ab = c_vec || pad ? 1 : 0;
@@ -520,13 +578,23 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
     p.vec_c = 0;
   }
   if (!kern) return MT_ERR_UNSUPPORTED;
-  p.pack_a = prep ? 1 : 0;
+  // A kernel that stages an operand in 16-byte chunks must get it 16-byte
+  // readable (as stored, or from its copy); anything else is a planning
+  // error, refused before a launch could read misaligned memory.
+  if (L->a_kmajor ? !(b_vec || L->prep_b) ||
+                        !(L->a_gather || L->prep_a_kmajor ||
+                          (P.trans_a && M % 4 == 0 && P.lda % 4 == 0 && aligned16(P.A)))
+                  : p.vec_ab && !(a_ok && b_ok))
+    return MT_ERR_UNSUPPORTED;
   p.bm = E.bm; p.bn = E.bn; p.bk = E.bk; p.stages = E.stages; p.threads = E.threads;
   p.fma = E.packed ? 2 : 1;
   p.wm = E.wm; p.wn = E.wn; p.tm = E.tm; p.tn = E.tn;
-  p.pad_a = pad ? E.pad_a : 0;
-  p.pad_b = b_staged_trans ? E.pad_b_t : (pad ? E.pad_b : 0);
-  p.smem_bytes = b_staged_trans ? E.smem_bytes_t : E.smem_bytes[pad ? 1 : 0];
+  if (!L->a_kmajor) {
+    p.pack_a = prep ? 1 : 0;
+    p.pad_a = pad ? E.pad_a : 0;
+    p.pad_b = b_staged_trans ? E.pad_b_t : (pad ? E.pad_b : 0);
+    p.smem_bytes = b_staged_trans ? E.smem_bytes_t : E.smem_bytes[pad ? 1 : 0];
+  }
   L->entry = i;
   L->kern = kern;
   L->tiles_m = static_cast<int>(ceil_div(M, E.bm));
@@ -553,10 +621,11 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   L->kt_per_slice = static_cast<int>(ceil_div(ktiles, split));
   p.split_k = L->split;
   p.grid = full + (tiles - full) * split;
-  const auto round256 = [](int64_t b) { return (b + 255) / 256 * 256; };
-  L->ldo_a = ceil_div(std::max<int64_t>(K, 1), 4) * 4;
-  L->ldo_b = ceil_div(std::max<int64_t>(N, 1), 4) * 4;
-  L->prep_b_offset = L->prep_a ? round256(M * L->ldo_a * 4) : 0;
+  if (!L->a_kmajor) {
+    L->ldo_a = ceil_div(std::max<int64_t>(K, 1), 4) * 4;
+    L->ldo_b = ceil_div(std::max<int64_t>(N, 1), 4) * 4;
+    L->prep_b_offset = L->prep_a ? round256(M * L->ldo_a * 4) : 0;
+  }
   L->partial_offset = L->prep_b_offset + (L->prep_b ? round256(K * L->ldo_b * 4) : 0);
   p.workspace_bytes = L->partial_offset + (tiles - full) * split * E.bm * E.bn * 4;
   // The budget check comes before anything is launched ("Part 18", section
@@ -767,6 +836,17 @@ mt_status run(const Problem& P, cudaStream_t stream, const mt_config* cfg) {
       args.A = a;
       args.lda = L.ldo_a;
       args.trans_a = 0;
+    }
+    if (L.prep_a_kmajor) {
+      // A^T (K x M) into scratch: a transposing copy of A stored M x K, a
+      // plain one of A stored K x M.
+      float* a = reinterpret_cast<float*>(base);
+      ok = mt::launch_prep_operand(static_cast<const float*>(P.A), P.lda, P.trans_a == 0, a,
+                                   L.ldo_a, static_cast<int>(P.K), static_cast<int>(P.M),
+                                   stream) == cudaSuccess;
+      args.A = a;
+      args.lda = L.ldo_a;
+      args.trans_a = 1;
     }
     if (ok && L.prep_b) {
       float* b = reinterpret_cast<float*>(base + L.prep_b_offset);
@@ -1026,12 +1106,12 @@ mt_status mt_gemm_mixed_general(int dtype, int trans_a, int trans_b, int64_t M, 
              stream, cfg);
 }
 
-mt_status mt_gemm_mixed_plan(int dtype, int trans_a, int trans_b, int64_t M, int64_t N,
-                             int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-                             const float* C, int64_t ldc, const mt_config* cfg,
-                             int64_t smem_limit_bytes, mt_plan* out) {
+// Plan of a general-form call of either element type (dtype 0: fp32).
+mt_status plan_general(int dtype, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
+                       const void* A, int64_t lda, const void* B, int64_t ldb, const float* C,
+                       int64_t ldc, const mt_config* cfg, int64_t smem_limit_bytes,
+                       mt_plan* out) {
   if (!out) return MT_ERR_INVALID_ARG;
-  if (dtype != MT_DTYPE_F16 && dtype != MT_DTYPE_BF16) return MT_ERR_INVALID_ARG;
   const Problem P{A, B, const_cast<float*>(C), M, N, K, lda, ldb, ldc, 1.0f, 0.0f,
                   trans_a, trans_b, dtype};
   if (trans_a < 0 || trans_a > 1 || trans_b < 0 || trans_b > 1) return MT_ERR_INVALID_ARG;
@@ -1051,6 +1131,23 @@ mt_status mt_gemm_mixed_plan(int dtype, int trans_a, int trans_b, int64_t M, int
       plan_call(P, cfg, smem_limit_bytes, sms, &L, current_device(&dev, &info) == MT_OK ? dev : -1);
   *out = L.plan;
   return st;
+}
+
+mt_status mt_gemm_mixed_plan(int dtype, int trans_a, int trans_b, int64_t M, int64_t N,
+                             int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                             const float* C, int64_t ldc, const mt_config* cfg,
+                             int64_t smem_limit_bytes, mt_plan* out) {
+  if (dtype != MT_DTYPE_F16 && dtype != MT_DTYPE_BF16) return MT_ERR_INVALID_ARG;
+  return plan_general(dtype, trans_a, trans_b, M, N, K, A, lda, B, ldb, C, ldc, cfg,
+                      smem_limit_bytes, out);
+}
+
+mt_status mt_sgemm_general_plan(int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
+                                const float* A, int64_t lda, const float* B, int64_t ldb,
+                                const float* C, int64_t ldc, const mt_config* cfg,
+                                int64_t smem_limit_bytes, mt_plan* out) {
+  return plan_general(0, trans_a, trans_b, M, N, K, A, lda, B, ldb, C, ldc, cfg,
+                      smem_limit_bytes, out);
 }
 
 int mt_smem_row_padding(int columns, int simultaneous_rows) {

@@ -23,6 +23,14 @@ struct FfmaEntry {
   // 16-byte staging of A and B with scalar stores of C (padded rows);
   // nullptr when not built.
   const void* kern_vsc;
+  // A staged K-major from A stored K x M (16-byte chunks), B as kern[1][1];
+  // [vec_c].  smem_bytes_km: its dynamic shared memory.
+  const void* kern_km[2];
+  int smem_bytes_km;
+  // A gathered K-major from row-major storage (4-byte copies), B as
+  // kern[1][1]; [vec_c].  pad_a_kg: padding words of its K-major A rows.
+  const void* kern_kg[2];
+  int smem_bytes_kg, pad_a_kg;
 };
 
 // Copies op(src) (R x cols, op = transpose when trans) into row-major `out`

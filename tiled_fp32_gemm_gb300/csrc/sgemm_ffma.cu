@@ -86,52 +86,72 @@ cudaError_t launch_scale_c(float* C, int M, int N, int64_t ldc, float beta,
 }
 
 // out[r * ldo + c] = op(src)[r][c] for r < R, c < cols, and 0.0 for
-// cols <= c < ldo, with op(src)[r][c] = trans ? src[c * ld + r] : src[r * ld + c].
-// 32 x 32 tiles through shared memory (a 33-word row stride: the transposed
-// read of a column touches 32 distinct banks), so global reads and writes are
-// both row-contiguous.  grid (ceil(ldo / 32), ceil(R / 32)), 256 threads.
+// cols <= c < ldo, with op(src)[r][c] = TRANS ? src[c * ld + r] : src[r * ld + c].
+// 64 x 64 tiles of out through shared memory (a 65-word row stride: the
+// transposed read of a column touches 32 distinct banks), so global reads
+// and writes are both row-contiguous; each thread has 16 loads in flight.
+// 1-D grid of tiles_r * tiles_c CTAs, 256 threads.
+template <bool TRANS>
 __global__ void __launch_bounds__(256) prep_operand_kernel(const float* __restrict__ src,
-                                                           int64_t ld, int trans,
-                                                           float* __restrict__ out, int64_t ldo,
-                                                           int R, int cols) {
-  __shared__ float t[32][33];
-  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
-  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
-  for (int i = ty; i < 32; i += 8) {
-    if (trans) {
-      // Source row c0 + i holds column c0 + i of op(src); t[c][r].
-      const int c = c0 + i, r = r0 + tx;
-      t[i][tx] = c < cols && r < R ? src[static_cast<int64_t>(c) * ld + r] : 0.0f;
-    } else {
-      const int r = r0 + i, c = c0 + tx;
-      t[i][tx] = r < R && c < cols ? src[static_cast<int64_t>(r) * ld + c] : 0.0f;
+                                                           int64_t ld, float* __restrict__ out,
+                                                           int64_t ldo, int R, int cols,
+                                                           int tiles_c) {
+  __shared__ float t[64][65];
+  const int r0 = static_cast<int>(blockIdx.x / tiles_c) * 64;
+  const int c0 = static_cast<int>(blockIdx.x % tiles_c) * 64;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+#pragma unroll
+  for (int i = ty; i < 64; i += 8) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int x = tx + 32 * h;
+      if constexpr (TRANS) {
+        // Source row c0 + i holds column c0 + i of op(src): t[c][r].
+        const int c = c0 + i, r = r0 + x;
+        t[i][x] = c < cols && r < R ? src[static_cast<int64_t>(c) * ld + r] : 0.0f;
+      } else {
+        const int r = r0 + i, c = c0 + x;
+        t[i][x] = r < R && c < cols ? src[static_cast<int64_t>(r) * ld + c] : 0.0f;
+      }
     }
   }
   __syncthreads();
-  for (int i = ty; i < 32; i += 8) {
-    const int r = r0 + i, c = c0 + tx;
-    if (r < R && c < ldo) out[static_cast<int64_t>(r) * ldo + c] = trans ? t[tx][i] : t[i][tx];
+#pragma unroll
+  for (int i = ty; i < 64; i += 8) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int x = tx + 32 * h;
+      const int r = r0 + i, c = c0 + x;
+      if (r < R && c < ldo) out[static_cast<int64_t>(r) * ldo + c] = TRANS ? t[x][i] : t[i][x];
+    }
   }
 }
 
 cudaError_t launch_prep_operand(const float* src, int64_t ld, bool trans, float* out,
                                 int64_t ldo, int R, int cols, cudaStream_t stream) {
   if (R <= 0 || ldo <= 0) return cudaSuccess;
-  const int64_t gy = (R + 31) / 32, gx = (ldo + 31) / 32;
-  if (gy > 65535 || gx > INT32_MAX) return cudaErrorInvalidValue;
-  prep_operand_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0,
-                        stream>>>(src, ld, trans ? 1 : 0, out, ldo, R, cols);
+  const int64_t tiles_r = (R + 63) / 64, tiles_c = (ldo + 63) / 64;
+  if (tiles_c > INT32_MAX || tiles_r * tiles_c > INT32_MAX) return cudaErrorInvalidValue;
+  const unsigned grid = static_cast<unsigned>(tiles_r * tiles_c);
+  if (trans)
+    prep_operand_kernel<true><<<grid, 256, 0, stream>>>(src, ld, out, ldo, R, cols,
+                                                        static_cast<int>(tiles_c));
+  else
+    prep_operand_kernel<false><<<grid, 256, 0, stream>>>(src, ld, out, ldo, R, cols,
+                                                         static_cast<int>(tiles_c));
   return cudaGetLastError();
 }
 
 int ffma_entries_128(FfmaEntry* out);
-int ffma_entries_other(FfmaEntry* out);
+int ffma_entries_alt(FfmaEntry* out);
+int ffma_entries_64(FfmaEntry* out);
 
 const FfmaEntry* ffma_entries(int* count) {
   static FfmaEntry entries[32];
   static const int n = [] {
     int k = ffma_entries_128(entries);
-    k += ffma_entries_other(entries + k);
+    k += ffma_entries_alt(entries + k);
+    k += ffma_entries_64(entries + k);
     return k;
   }();
   *count = n;

@@ -18,15 +18,23 @@
 //    in 16-byte slots (section "Choosing padding instead of hard-coding it");
 //    B rows are read as a broadcast and get no padding, as the rule says
 //    (section "Why shared-memory banks matter", last paragraphs);
+//  * A tiles row-major (As[m][k], a thread reads a float4 of four k of one
+//    row) or K-major (As[k][m], a thread reads a float4 of four rows at one
+//    k).  The K-major tile is read one k row at a time, so the rule gives
+//    it no padding; filled from A stored K x M in 16-byte chunks, or
+//    gathered from A stored M x K with 4-byte copies that write 8 k rows at
+//    one column at once, for which the rule pads each row by one word
+//    (rounded up to a float4).  Only the rows a thread owns change: 4 x 4
+//    blocks instead of a stride of LM rows;
 //  * K pipeline — STAGES shared stages filled by cp.async with zero fill,
 //    one barrier per K tile (Part 18 "What ping-pong changes about
 //    synchronization"; skills page step 7: commit, wait_group, then
 //    __syncthreads), with STAGES-1 tiles in flight while one is computed;
 //  * unrolled register-tile micro-kernel — each thread keeps a TM x TN block
 //    of C in registers and, for every k of the fixed-size BK loop (fully
-//    unrolled, Part 18 "Unrolling the inner reduction loop"), reads a float4
-//    of A per row and float4s of B and issues TM*TN FMAs; the packed form
-//    issues them as fma.rn.f32x2 pairs;
+//    unrolled, Part 18 "Unrolling the inner reduction loop"), reads its A
+//    values (float4s) and float4s of B and issues TM*TN FMAs; the packed
+//    form issues them as fma.rn.f32x2 pairs;
 //  * masked epilogue — float4 or scalar stores where row < M and col < N.
 //
 // Every output is a sequence of fp32 FMAs in increasing k, one per k, so
@@ -76,6 +84,24 @@ struct FfmaTile {
   static constexpr int smem_bytes(bool pad, bool trans_b = false) {
     return a_layout(pad).nbytes() + b_layout(pad, trans_b).nbytes();
   }
+  // A staged K-major (As[k][m]): a warp reads one k row at a time, float4s
+  // of four consecutive rows of A, so the rule gives no padding.
+  static constexpr SmemLayout a_layout_kmajor() {
+    return SmemLayout{BK, BM, vector_row_padding_rule(BM, 1), STAGES};
+  }
+  static constexpr int smem_bytes_kmajor() {
+    return a_layout_kmajor().nbytes() + b_layout(true).nbytes();
+  }
+  // A gathered K-major from row-major storage: the copies write 8 k rows at
+  // the same column at once, so the scalar rule asks for one padding word,
+  // rounded up to a float4 to keep rows 16-byte aligned for the reads.
+  static constexpr int A_GATHER_PAD = (row_padding_rule(BM, 8) + 3) / 4 * 4;
+  static constexpr SmemLayout a_layout_gather() {
+    return SmemLayout{BK, BM, A_GATHER_PAD, STAGES};
+  }
+  static constexpr int smem_bytes_gather() {
+    return a_layout_gather().nbytes() + b_layout(true).nbytes();
+  }
 };
 
 // ---------------------------------------------------------------------------
@@ -89,7 +115,20 @@ struct FfmaTile {
 //                the contiguous dimension, so global reads stay within
 //                32-byte sectors and the shared writes land in 32 distinct
 //                banks.
-enum StageMode { STAGE_VEC = 0, STAGE_SCALAR = 1, STAGE_TRANS = 2 };
+//   STAGE_KMAJOR A only: A stored K x M (M % 4 == 0, lda % 4 == 0, 16-byte
+//                aligned) copied in 16-byte chunks along M into a K-major
+//                tile As[k][m]; the micro-kernel then reads four rows of A
+//                with one float4.
+//   STAGE_GATHER A only: A stored M x K (any lda and alignment) copied
+//                element by element into the same K-major tile; a warp
+//                copies 8 x 4 blocks, 8 lanes along K.
+enum StageMode {
+  STAGE_VEC = 0,
+  STAGE_SCALAR = 1,
+  STAGE_TRANS = 2,
+  STAGE_KMAJOR = 3,
+  STAGE_GATHER = 4
+};
 
 template <class T, int MODE>
 struct AStage;
@@ -195,6 +234,82 @@ struct AStage<T, STAGE_TRANS> {
       const bool ok = m0 + r < M && k0 + c < K;
       cp_async_4(smem_u32(As + la.offset(stage, r, c)),
                  ok ? At + static_cast<int64_t>(k0 + c) * lda + m0 + r : At, ok ? 4u : 0u);
+    }
+  }
+};
+
+template <class T>
+struct AStage<T, STAGE_KMAJOR> {
+  static constexpr int CHUNKS_ROW = T::BM / 4;
+  static_assert(T::THREADS % CHUNKS_ROW == 0, "");
+  static constexpr int ROWS_STEP = T::THREADS / CHUNKS_ROW;
+  static constexpr int ITERS = T::BK / ROWS_STEP;
+  static_assert(ITERS * ROWS_STEP == T::BK, "");
+  const float* base;
+  const float* src;  // At[k * lda + m0 + col], k = this thread's first row
+  int64_t lda, row_step;
+  int row, col, K;
+  bool col_ok;
+
+  __device__ AStage(const GemmArgs& a, int m0, int tid) : base(a.A), lda(a.lda), K(a.K) {
+    row = tid / CHUNKS_ROW;
+    col = (tid % CHUNKS_ROW) * 4;
+    row_step = static_cast<int64_t>(ROWS_STEP) * a.lda;
+    src = a.A + static_cast<int64_t>(row) * a.lda + m0 + col;
+    col_ok = m0 + col < a.M;
+  }
+  template <class L>
+  __device__ __forceinline__ void load(float* As, const L& la, int stage, int kt) const {
+    const int k0 = kt * T::BK;
+#pragma unroll
+    for (int t = 0; t < ITERS; ++t) {
+      const bool ok = col_ok && k0 + row + t * ROWS_STEP < K;
+      cp_async_16(smem_u32(As + la.offset(stage, row + t * ROWS_STEP, col)),
+                  ok ? src + static_cast<int64_t>(k0) * lda + t * row_step : base, ok ? 16u : 0u);
+    }
+  }
+};
+
+template <class T>
+struct AStage<T, STAGE_GATHER> {
+  // Lane l copies k = 8*kb + l%8 and m = 4*mb + l/8 of block b = warp +
+  // t*NW (kb = b % KB, mb = b / KB) from A[(m0 + m) * lda + k0 + k].  With
+  // NW a multiple of KB a thread's k is fixed and its m advances by M_STEP.
+  // Eight lanes read 32 consecutive bytes of one row of A; the row stride
+  // BM + 4 is 4 (mod 32) words, so a warp's 32 shared writes (8 k x 4 m)
+  // land in 32 distinct banks.
+  static constexpr int KB = T::BK / 8, MB = T::BM / 4;
+  static constexpr int NW = T::THREADS / 32;
+  static_assert(T::BK % 8 == 0 && NW % KB == 0, "gather blocks");
+  static constexpr int ITERS = KB * MB / NW;
+  static constexpr int M_STEP = NW / KB * 4;
+  static_assert(ITERS * NW == KB * MB && ITERS <= 32, "");
+  const float* base;
+  const float* src;  // A[(m0 + m_first) * lda + k_off]
+  int64_t row_step;  // M_STEP * lda
+  int k_off, m_first, K;
+  uint32_t rows_ok;  // bit t: row m0 + m_first + t*M_STEP is inside M
+
+  __device__ AStage(const GemmArgs& a, int m0, int tid) : base(a.A), K(a.K) {
+    const int warp = tid >> 5, lane = tid & 31;
+    k_off = (warp % KB) * 8 + (lane & 7);
+    m_first = (warp / KB) * 4 + (lane >> 3);
+    row_step = static_cast<int64_t>(M_STEP) * a.lda;
+    src = a.A + static_cast<int64_t>(m0 + m_first) * a.lda + k_off;
+    rows_ok = 0;
+#pragma unroll
+    for (int t = 0; t < ITERS; ++t)
+      if (m0 + m_first + t * M_STEP < a.M) rows_ok |= 1u << t;
+  }
+  template <class L>
+  __device__ __forceinline__ void load(float* As, const L& la, int stage, int kt) const {
+    const int k0 = kt * T::BK;
+    const bool k_ok = k0 + k_off < K;
+#pragma unroll
+    for (int t = 0; t < ITERS; ++t) {
+      const bool ok = k_ok && (rows_ok >> t & 1u);
+      cp_async_4(smem_u32(As + la.offset(stage, k_off, m_first + t * M_STEP)),
+                 ok ? src + t * row_step + k0 : base, ok ? 4u : 0u);
     }
   }
 };
@@ -306,7 +421,11 @@ template <class T, int AMODE, int BMODE, bool PAD, bool PACKED,
 __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     sgemm_ffma_kernel(GemmArgs args) {
   constexpr bool VEC = VEC_C;
-  constexpr SmemLayout LA = T::a_layout(PAD);
+  constexpr bool KMAJOR = AMODE == STAGE_KMAJOR || AMODE == STAGE_GATHER;
+  static_assert(!KMAJOR || T::TM % 4 == 0, "K-major A reads rows in fours");
+  constexpr SmemLayout LA = AMODE == STAGE_GATHER ? T::a_layout_gather()
+                            : KMAJOR              ? T::a_layout_kmajor()
+                                                  : T::a_layout(PAD);
   constexpr SmemLayout LB = T::b_layout(PAD, BMODE == STAGE_TRANS);
   extern __shared__ float4 smem_f4[];
   float* As = reinterpret_cast<float*>(smem_f4);
@@ -350,8 +469,12 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
   const int wm = warp / T::WARPS_N, wn = warp % T::WARPS_N;
   const int lm = lane % T::LM, ln = lane / T::LM;
   // Thread (lm, ln) of warp (wm, wn) owns rows wm*WM + i*LM + lm (i < TM)
-  // and columns wn*WN + g*LN*4 + ln*4 + c (g < TN/4, c < 4).
-  const int a_off = LA.offset(0, wm * T::WM + lm, 0);
+  // and columns wn*WN + g*LN*4 + ln*4 + c (g < TN/4, c < 4).  With A
+  // K-major the rows come in fours: wm*WM + (i/4)*LM*4 + lm*4 + i%4.
+  const auto row_of = [&](int i) {
+    return KMAJOR ? wm * T::WM + (i / 4) * T::LM * 4 + lm * 4 + i % 4 : wm * T::WM + i * T::LM + lm;
+  };
+  const int a_off = KMAJOR ? LA.offset(0, 0, wm * T::WM + lm * 4) : LA.offset(0, wm * T::WM + lm, 0);
   const int b_off = LB.offset(0, 0, wn * T::WN + ln * 4);
 
   float2 acc[T::TM][T::TN / 2];
@@ -378,22 +501,33 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     const float* b_ptr = Bs + stage * LB.stage_size() + b_off;
 #pragma unroll
     for (int k4 = 0; k4 < T::BK / 4; ++k4) {
-      float4 a[T::TM];
+      // Row-major A: one float4 of four k per row, used over the next four
+      // k.  K-major A: one float4 of four rows per k.
+      float4 a[KMAJOR ? 1 : T::TM];
+      if constexpr (!KMAJOR) {
 #pragma unroll
-      for (int i = 0; i < T::TM; ++i)
-        a[i] = *reinterpret_cast<const float4*>(a_ptr + i * T::LM * LA.row_stride() + k4 * 4);
+        for (int i = 0; i < T::TM; ++i)
+          a[i] = *reinterpret_cast<const float4*>(a_ptr + i * T::LM * LA.row_stride() + k4 * 4);
+      }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
+        float4 ak[KMAJOR ? T::TM / 4 : 1];
+        if constexpr (KMAJOR) {
+#pragma unroll
+          for (int q = 0; q < T::TM / 4; ++q)
+            ak[q] = *reinterpret_cast<const float4*>(a_ptr + (k4 * 4 + kk) * LA.row_stride() +
+                                                     q * T::LM * 4);
+        }
         float4 b[T::TN / 4];
 #pragma unroll
         for (int g = 0; g < T::TN / 4; ++g)
           b[g] = *reinterpret_cast<const float4*>(b_ptr + (k4 * 4 + kk) * LB.row_stride() +
                                                   g * T::LN * 4);
 #pragma unroll
-        for (int i = 0; i < T::TM; ++i) {
-          const float av = pick(a[i], kk);
+        for (int g = 0; g < T::TN / 4; ++g) {
 #pragma unroll
-          for (int g = 0; g < T::TN / 4; ++g) {
+          for (int i = 0; i < T::TM; ++i) {
+            const float av = KMAJOR ? pick(ak[i / 4], i % 4) : pick(a[i], kk);
             if constexpr (PACKED) {
               const float2 a2 = make_float2(av, av);
               acc[i][2 * g] = __ffma2_rn(a2, make_float2(b[g].x, b[g].y), acc[i][2 * g]);
@@ -420,7 +554,7 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
                    (T::BM * T::BN);
 #pragma unroll
     for (int i = 0; i < T::TM; ++i) {
-      const int r = wm * T::WM + i * T::LM + lm;
+      const int r = row_of(i);
 #pragma unroll
       for (int g = 0; g < T::TN / 4; ++g) {
         const int c = wn * T::WN + g * T::LN * 4 + ln * 4;
@@ -439,7 +573,7 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
   const float alpha = args.alpha, beta = args.beta;
 #pragma unroll
   for (int i = 0; i < T::TM; ++i) {
-    const int row = m0 + wm * T::WM + i * T::LM + lm;
+    const int row = m0 + row_of(i);
     if (row >= M) continue;
     float* c_row = C + static_cast<int64_t>(row) * args.ldc;
 #pragma unroll
@@ -469,7 +603,10 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
   }
 }
 
-template <class T, bool PACKED, bool WITH_UNPADDED, bool WITH_TRANS = false>
+// Only the kernels a flag asks for are instantiated (the others stay
+// nullptr in the entry).
+template <class T, bool PACKED, bool WITH_UNPADDED, bool WITH_TRANS = false,
+          bool WITH_KMAJOR = false>
 FfmaEntry make_entry() {
   FfmaEntry e{};
   e.bm = T::BM;
@@ -491,15 +628,28 @@ FfmaEntry make_entry() {
       &sgemm_ffma_kernel<T, STAGE_VEC, STAGE_VEC, true, PACKED>);
   e.kern[0][1] = reinterpret_cast<const void*>(
       &sgemm_ffma_kernel<T, STAGE_SCALAR, STAGE_SCALAR, true, PACKED>);
-  if (WITH_UNPADDED) {
+  if constexpr (WITH_UNPADDED) {
     e.kern[1][0] = reinterpret_cast<const void*>(
         &sgemm_ffma_kernel<T, STAGE_VEC, STAGE_VEC, false, PACKED>);
     e.kern[0][0] = reinterpret_cast<const void*>(
         &sgemm_ffma_kernel<T, STAGE_SCALAR, STAGE_SCALAR, false, PACKED>);
   }
+  if constexpr (WITH_KMAJOR) {
+    e.smem_bytes_km = T::smem_bytes_kmajor();
+    e.smem_bytes_kg = T::smem_bytes_gather();
+    e.pad_a_kg = T::A_GATHER_PAD;
+    e.kern_kg[1] = reinterpret_cast<const void*>(
+        &sgemm_ffma_kernel<T, STAGE_GATHER, STAGE_VEC, true, PACKED, true>);
+    e.kern_kg[0] = reinterpret_cast<const void*>(
+        &sgemm_ffma_kernel<T, STAGE_GATHER, STAGE_VEC, true, PACKED, false>);
+    e.kern_km[1] = reinterpret_cast<const void*>(
+        &sgemm_ffma_kernel<T, STAGE_KMAJOR, STAGE_VEC, true, PACKED, true>);
+    e.kern_km[0] = reinterpret_cast<const void*>(
+        &sgemm_ffma_kernel<T, STAGE_KMAJOR, STAGE_VEC, true, PACKED, false>);
+  }
   e.pad_b_t = T::b_layout(true, true).row_padding;
   e.smem_bytes_t = T::smem_bytes(true, true);
-  if (WITH_TRANS) {
+  if constexpr (WITH_TRANS) {
     e.kern_t[1][0] = reinterpret_cast<const void*>(
         &sgemm_ffma_kernel<T, STAGE_TRANS, STAGE_SCALAR, true, PACKED>);
     e.kern_t[0][1] = reinterpret_cast<const void*>(
