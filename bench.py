@@ -548,6 +548,22 @@ def run_gpu(args):
         # GB300: the first two of each shape, up to 2x).
         for _ in range(max(2, args.warmup)):
             host_step()
+        # The link this run got: pinned copies of the largest A, each way (the
+        # host side of the link is shared with other jobs on the machine, so
+        # e2e, which is bound by it, moves with it).
+        big = max(hbufs, key=lambda x: x[0].M * x[0].K)
+        dev_buf = torch.empty_like(big[1], device="cuda")
+        link = {}
+        for name, (dst, src) in (("h2d_gbs", (dev_buf, big[1])), ("d2h_gbs", (big[1], dev_buf))):
+            dst.copy_(src, non_blocking=True)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            link[name] = big[1].numel() * 4 / (e0.elapsed_time(e1) / 1e3) / 1e9
+        del dev_buf
         e2e_steps = max(1, min(args.steps, 5))
         barrier()
         t0 = time.perf_counter()
@@ -558,7 +574,7 @@ def run_gpu(args):
                "steps": e2e_steps,
                "h2d_bytes_per_step": sum(4 * (w.M * w.K + w.K * w.N) for (w, *_r) in hbufs),
                "d2h_bytes_per_step": sum(4 * w.M * w.N for (w, *_r) in hbufs),
-               "api": "mt_sgemm_host"}
+               "api": "mt_sgemm_host", "link": link}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -91,19 +91,23 @@ def test_ragged_workload_full():
     # copies.  Row-major A tiles from copies (pack_a = 1): A and B copied
     # into rows padded to whole float4s, then 16-byte chunks.  Automatically:
     # A staged K-major from a transposed copy, B from a padded copy, on
-    # 64 x 128 tiles; and A gathered K-major inside the kernel (pack_a = 4).
-    # All give the same FMA chain per output.
+    # 64 x 128 tiles, the last partial wave split in two K slices; and A
+    # gathered K-major inside the kernel (pack_a = 4).  Without K slices all
+    # give the same FMA chain per output; the split tail adds two partial
+    # sums, within the tolerance.
     A, B = gemm_inputs.make_workload("ragged_4097x3001x2053")
     a, b = A.cuda(), B.cuda()
     assert mt.plan(4097, 3001, 2053, a=a, b=b, pack_a=2)["vec_ab"] == 0
     assert mt.plan(4097, 3001, 2053, a=a, b=b, pack_a=1)["pack_a"] == 1
     p = mt.plan(4097, 3001, 2053, a=a, b=b)
     assert (p["vec_ab"], p["vec_c"], p["pack_a"], p["bm"], p["bn"]) == (1, 0, 5, 64, 128)
+    assert p["split_k"] == 2
     Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
     as_stored = run(A, B, pack_a=2).numpy()
     assert_within(as_stored, Cref, W, FFMA_TOL, "ragged, as stored")
-    for choice in (dict(pack_a=1), dict(), dict(pack_a=4)):
+    for choice in (dict(pack_a=1), dict(split_k=1), dict(pack_a=4, split_k=1)):
         assert np.array_equal(run(A, B, **choice).numpy(), as_stored), choice
+    assert_within(run(A, B).numpy(), Cref, W, FFMA_TOL, "ragged, automatic (split tail)")
 
 
 def sampled_rows(M, bm=128, extra=24, seed=0):
@@ -173,6 +177,32 @@ def test_split_k_matches_oracle_and_is_deterministic(shape, split):
     first = run(A, B, split_k=split)
     assert_within(first.numpy(), Cref, W, FFMA_TOL, f"split {split}")
     assert torch.equal(run(A, B, split_k=split), first)  # slices add in a fixed order
+
+
+@pytest.mark.parametrize("shape,rows_only", [((512, 512, 4096), False),
+                                             ((2048, 2048, 8192), True),
+                                             ((65536, 128, 4096), True)])
+def test_automatic_k_slices_match_oracle(shape, rows_only):
+    """The automatic plans cut K: 512 x 512 x 4096 has fewer tiles than SMs
+    (every tile in slices), 2048 x 2048 x 8192 and 65536 x 128 x 4096 leave
+    a last partial wave (only those tiles in slices).  Within the tolerance
+    and deterministic."""
+    M, N, K = shape
+    A, B = gemm_inputs.make_ab(M, N, K, seed=18, dist="uniform")
+    a, b = A.cuda(), B.cuda()
+    assert mt.plan(M, N, K, a=a, b=b)["split_k"] > 1
+    first = mt.sgemm(a, b)
+    again = mt.sgemm(a, b)
+    torch.cuda.synchronize()
+    assert torch.equal(first, again)
+    if rows_only:
+        rows = sampled_rows(M, bm=64, extra=24)
+        Cr, Wr = oracle.sgemm_rows(A.numpy(), B.numpy(), rows, with_w=True)
+        got = first[torch.from_numpy(rows).cuda()].cpu().numpy()
+    else:
+        Cr, Wr = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
+        got = first.cpu().numpy()
+    assert_within(got, Cr, Wr, FFMA_TOL, f"{shape} automatic split")
 
 
 def test_split_k_integer_inputs_bit_exact():
@@ -297,8 +327,10 @@ def test_alias_rejected_without_launch():
 def test_host_entry_point_pipelined_blocks(pinned):
     """8192 x 8192 x 512 from host buffers: four row blocks, each copied in,
     multiplied and copied out on its own stream while its neighbours move.
-    The FFMA result is bit-identical to the device entry point (the same FMA
-    chain per output); 3xTF32 through the same path stays within tolerance."""
+    Without K slices the FFMA result is bit-identical to the device entry
+    point (the same FMA chain per output); the automatic plans split the
+    last partial wave of each call (different tiles for a block than for the
+    whole product) and stay within tolerance, as does 3xTF32."""
     M, N, K = 8192, 8192, 512
     A, B = gemm_inputs.make_ab(M, N, K, seed=17, dist="normal")
     if pinned:
@@ -306,13 +338,19 @@ def test_host_entry_point_pipelined_blocks(pinned):
         c = torch.full((M, N), float("nan")).pin_memory()
     else:
         c = torch.full((M, N), float("nan"))
-    st = mt.mt_sgemm_host(A.data_ptr(), B.data_ptr(), c.data_ptr(), M, N, K, 0, None)
+    unsplit = mt.make_config(split_k=1)
+    st = mt.mt_sgemm_host(A.data_ptr(), B.data_ptr(), c.data_ptr(), M, N, K, 0, unsplit)
     assert st == mt.MT_OK
-    dev = mt.sgemm(A.cuda(), B.cuda()).cpu()
+    dev = mt.sgemm(A.cuda(), B.cuda(), split_k=1).cpu()
     assert torch.equal(c, dev)
     rows = np.array([0, 2047, 2048, 4095, 4096, 6143, 6144, 8191])
     Cr, Wr = oracle.sgemm_rows(A.numpy(), B.numpy(), rows, with_w=True)
     assert_within(c.numpy()[rows], Cr, Wr, FFMA_TOL, "host pipelined")
+    c.fill_(float("nan"))
+    st = mt.mt_sgemm_host(A.data_ptr(), B.data_ptr(), c.data_ptr(), M, N, K, 0, None)
+    assert st == mt.MT_OK
+    assert not torch.isnan(c).any()
+    assert_within(c.numpy()[rows], Cr, Wr, FFMA_TOL, "host pipelined, automatic")
     c.fill_(float("nan"))
     st = mt.mt_sgemm_host(A.data_ptr(), B.data_ptr(), c.data_ptr(), M, N, K, 0,
                           mt.make_config(variant="tf32x3"))

@@ -204,9 +204,10 @@ int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms, bool kmajor) 
   // Automatic.  Row-major A: 128x128 tiles when they fill every SM twice
   // over, else 64x64 tiles for more CTAs.  K-major A: 128x128 tiles from
   // three full waves (2 CTAs per SM) up, else 64x128 tiles (3 CTAs per SM)
-  // when they fill one wave, else 64x64.  Measured on GB300 (K-major A):
-  // 4097 x 3001 x 2053 54.7 TFLOP/s on 64x128 tiles against 49.3 on
-  // 128x128, 65536 x 128 x 4096 60.7 against 53.5.
+  // when there are at least half as many as SMs, else 64x64.  Measured on
+  // GB300 (K-major A): 4097 x 3001 x 2053 54.7 TFLOP/s on 64x128 tiles
+  // against 49.3 on 128x128, 65536 x 128 x 4096 60.7 against 53.5, 1024^3
+  // 38.4 against 33.5 on 64x64.
   int big = -1, mid = -1, small = -1;
   for (int i = 0; i < count; ++i) {
     if (!e[i].packed) continue;
@@ -221,7 +222,7 @@ int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms, bool kmajor) 
     return small;
   }
   if (tiles_big >= 6 * static_cast<int64_t>(sms) || (mid < 0 && small < 0)) return big;
-  if (mid >= 0 && ceil_div(M, 64) * ceil_div(N, 128) >= 3 * static_cast<int64_t>(sms)) return mid;
+  if (mid >= 0 && 2 * ceil_div(M, 64) * ceil_div(N, 128) >= static_cast<int64_t>(sms)) return mid;
   return small >= 0 ? small : big;
 }
 
@@ -611,6 +612,23 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   if (cfg && cfg->split_k > 1) {
     full = 0;
     split = std::min<int64_t>(cfg->split_k, ktiles > 0 ? ktiles : 1);
+  } else if (L->a_kmajor && !(cfg && cfg->split_k == 1)) {
+    // K-major A (split_k = 1 turns both off): fewer tiles than SMs are cut
+    // into up to 4 K slices of at least 512 (512 x 512 x 4096: 2.7x); a
+    // last wave under half full is cut into K slices (the CTAs of whole
+    // tiles come first, so the slices make up the last wave; 4097 x 3001 x
+    // 2053 and 65536 x 128 x 4096 1.04x, 2048 x 2048 x 8192 1.15x).
+    const int64_t n_sm = std::max(sms, 1);
+    if (tiles < n_sm) {
+      int64_t sk = std::min<int64_t>(4, n_sm / std::max<int64_t>(tiles, 1));
+      while (sk > 1 && (K / sk < 512 || (sk - 1) * ceil_div(ktiles, sk) >= ktiles)) --sk;
+      if (sk > 1) {
+        full = 0;
+        split = sk;
+      }
+    } else {
+      split_tail(tiles, n_sm * E.min_blocks, ktiles, true, &full, &split);
+    }
   }
   if (split <= 1) {
     split = 1;
