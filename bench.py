@@ -564,17 +564,21 @@ def run_gpu(args):
             torch.cuda.synchronize()
             link[name] = big[1].numel() * 4 / (e0.elapsed_time(e1) / 1e3) / 1e9
         del dev_buf
-        e2e_steps = max(1, min(args.steps, 5))
+        e2e_steps = max(1, min(args.steps, 10))
         barrier()
+        step_s = []
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
+            t_step = time.perf_counter()
             host_step()
+            step_s.append(time.perf_counter() - t_step)
         e2e_s = max_over_ranks(time.perf_counter() - t0)
         e2e = {"value": job_tflops(world, flops_step, e2e_steps, e2e_s), "unit": "TFLOP/s",
                "steps": e2e_steps,
                "h2d_bytes_per_step": sum(4 * (w.M * w.K + w.K * w.N) for (w, *_r) in hbufs),
                "d2h_bytes_per_step": sum(4 * w.M * w.N for (w, *_r) in hbufs),
-               "api": "mt_sgemm_host", "link": link}
+               "api": "mt_sgemm_host", "link": link,
+               "step_ms": [round(t * 1e3, 3) for t in step_s]}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

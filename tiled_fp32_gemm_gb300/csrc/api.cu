@@ -208,11 +208,15 @@ int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms, bool kmajor) 
   // GB300 (K-major A): 4097 x 3001 x 2053 54.7 TFLOP/s on 64x128 tiles
   // against 49.3 on 128x128, 65536 x 128 x 4096 60.7 against 53.5, 1024^3
   // 38.4 against 33.5 on 64x64.
-  int big = -1, mid = -1, small = -1;
+  int big = -1, big_km = -1, mid = -1, small = -1;
   for (int i = 0; i < count; ++i) {
     if (!e[i].packed) continue;
     if (big < 0 && e[i].bm == 128 && e[i].bn == 128 && e[i].bk == 32 && e[i].stages == 3)
       big = i;
+    // K-major A: the K depth 16 tile (0.5 % faster at 4096^3 and 8192^3).
+    if (big_km < 0 && e[i].bm == 128 && e[i].bn == 128 && e[i].bk == 16 && e[i].wm == 64 &&
+        e[i].kern_km[0])
+      big_km = i;
     if (mid < 0 && e[i].bm == 64 && e[i].bn == 128 && e[i].kern_km[0]) mid = i;
     if (small < 0 && e[i].bm == 64 && e[i].bn == 64) small = i;
   }
@@ -221,6 +225,7 @@ int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms, bool kmajor) 
     if (tiles_big >= 2 * static_cast<int64_t>(sms) || small < 0) return big;
     return small;
   }
+  if (big_km >= 0) big = big_km;
   if (tiles_big >= 6 * static_cast<int64_t>(sms) || (mid < 0 && small < 0)) return big;
   if (mid >= 0 && 2 * ceil_div(M, 64) * ceil_div(N, 128) >= static_cast<int64_t>(sms)) return mid;
   return small >= 0 ? small : big;

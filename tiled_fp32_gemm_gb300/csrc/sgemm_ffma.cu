@@ -144,6 +144,7 @@ cudaError_t launch_prep_operand(const float* src, int64_t ld, bool trans, float*
 
 int ffma_entries_128(FfmaEntry* out);
 int ffma_entries_alt(FfmaEntry* out);
+int ffma_entries_k16(FfmaEntry* out);
 int ffma_entries_64(FfmaEntry* out);
 
 const FfmaEntry* ffma_entries(int* count) {
@@ -152,6 +153,7 @@ const FfmaEntry* ffma_entries(int* count) {
     int k = ffma_entries_128(entries);
     k += ffma_entries_alt(entries + k);
     k += ffma_entries_64(entries + k);
+    k += ffma_entries_k16(entries + k);
     return k;
   }();
   *count = n;
