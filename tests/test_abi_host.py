@@ -322,10 +322,13 @@ def test_split_k_plan():
     st, p = plan(4096, 4096, 4096, split_k=2, pack_a=2)
     assert p.workspace_bytes == 1024 * 2 * 128 * 128 * 4
     # Fewer tiles than SMs: K is cut so the units fill the SMs, slices of at
-    # least 512 (512 x 512 x 4096: 64 tiles of 64 x 64, two slices).
+    # least 512.  512 x 512 x 4096 (long K, few tiles): 32 tiles of 64 x 128,
+    # each CTA with two K groups of 4 warps (256 threads), and 4 slices.
     st, p = plan(512, 512, 4096)
-    assert (p.bm, p.bn, p.split_k, p.grid) == (64, 64, 2, 128)
-    assert plan(512, 512, 512)[1].split_k == 1
+    assert (p.bm, p.bn, p.split_k, p.grid, p.threads) == (64, 128, 4, 128, 256)
+    # Short K: 64 x 64 tiles, one K group, no slices of 512.
+    st, p = plan(512, 512, 512)
+    assert (p.bm, p.bn, p.split_k, p.threads) == (64, 64, 1, 128)
     # A split larger than the K tiles is clamped to one K tile per slice.
     st, p = plan(64, 64, 64, split_k=4)
     assert p.split_k == 2

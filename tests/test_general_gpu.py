@@ -21,10 +21,13 @@ VARIANTS = [(dict(), 1e-5), (dict(bm=128, bn=128), 1e-5), (dict(bm=64, bn=64), 1
             (dict(pack_a=1), 1e-5), (dict(pack_a=2), 1e-5),
             (dict(pack_a=4), 1e-5), (dict(pack_a=5), 1e-5),
             (dict(bm=64, bn=128, pack_a=4), 1e-5), (dict(bm=64, bn=128, pack_a=5), 1e-5),
-            (dict(bm=64, bn=64, pack_a=5), 1e-5), (dict(pack_a=4, split_k=3), 1e-5)]
+            (dict(bm=64, bn=64, pack_a=5), 1e-5), (dict(pack_a=4, split_k=3), 1e-5),
+            (dict(bm=64, bn=128, stages=3, pack_a=4), 1e-5),
+            (dict(bm=64, bn=128, stages=3, pack_a=5), 1e-5)]
 VIDS = ["ffma", "ffma128", "ffma64", "p18", "tf32x3", "tf32x3-bn64", "tf32x3-pair",
         "ffma-copied", "ffma-rowmajor", "ffma-kgather", "ffma-kcopy", "ffma64x128-kgather",
-        "ffma64x128-kcopy", "ffma64-kcopy", "ffma-kgather-split3"]
+        "ffma64x128-kcopy", "ffma64-kcopy", "ffma-kgather-split3", "ffma-kslices2-gather",
+        "ffma-kslices2-copy"]
 
 
 def supported(cfg, ta):

@@ -40,7 +40,13 @@ FFMA_CONFIGS = [
     dict(bm=128, bn=128, bk=32, stages=3, fma=2, no_pad=True),
     dict(bm=128, bn=128, bk=32, stages=3, fma=2, wm=32, wn=64, no_pad=True),
 ]
-ALL_VARIANTS = FFMA_CONFIGS + [dict(variant="p18"), dict(variant="p18", no_pad=True)]
+# Tiles whose warps form two K groups (64 x 128, 3 stages): each output is
+# the sum of two partial chains, so they agree with the others within the
+# tolerance, not bit for bit.
+SLICED_CONFIGS = [dict(bm=64, bn=128, stages=3, pack_a=4), dict(bm=64, bn=128, stages=3, pack_a=5),
+                  dict(bm=64, bn=128, stages=3, pack_a=2)]
+ALL_VARIANTS = FFMA_CONFIGS + SLICED_CONFIGS + [dict(variant="p18"),
+                                                dict(variant="p18", no_pad=True)]
 
 
 def ids(cfgs):

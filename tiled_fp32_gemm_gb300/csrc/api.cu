@@ -179,7 +179,7 @@ mt_status check_problem(const Problem& P) {
 // micro-kernel form) must all match one entry; the first match in table
 // order wins, so each tile's default warp layout comes first.  Otherwise
 // the choice is automatic.
-int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms, bool kmajor) {
+int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int64_t K, int sms, bool kmajor) {
   int count = 0;
   const mt::FfmaEntry* e = mt::ffma_entries(&count);
   const bool explicit_tile = cfg && (cfg->bm || cfg->bn || cfg->bk || cfg->stages || cfg->wm ||
@@ -207,8 +207,10 @@ int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms, bool kmajor) 
   // when there are at least half as many as SMs, else 64x64.  Measured on
   // GB300 (K-major A): 4097 x 3001 x 2053 54.7 TFLOP/s on 64x128 tiles
   // against 49.3 on 128x128, 65536 x 128 x 4096 60.7 against 53.5, 1024^3
-  // 38.4 against 33.5 on 64x64.
-  int big = -1, big_km = -1, mid = -1, small = -1;
+  // 38.4 against 33.5 on 64x64.  Fewer 64x128 tiles than that with K >=
+  // 2048: 64x128 tiles with two K groups of warps per CTA (512 x 512 x 4096
+  // 62 us against 82 on 64x64; with K = 768 it lost, 44 us against 31).
+  int big = -1, big_km = -1, mid = -1, small = -1, sliced = -1;
   for (int i = 0; i < count; ++i) {
     if (!e[i].packed) continue;
     if (big < 0 && e[i].bm == 128 && e[i].bn == 128 && e[i].bk == 32 && e[i].stages == 3)
@@ -217,7 +219,9 @@ int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms, bool kmajor) 
     if (big_km < 0 && e[i].bm == 128 && e[i].bn == 128 && e[i].bk == 16 && e[i].wm == 64 &&
         e[i].kern_km[0])
       big_km = i;
-    if (mid < 0 && e[i].bm == 64 && e[i].bn == 128 && e[i].kern_km[0]) mid = i;
+    if (mid < 0 && e[i].bm == 64 && e[i].bn == 128 && e[i].kslices == 1 && e[i].kern_km[0])
+      mid = i;
+    if (sliced < 0 && e[i].kslices > 1 && e[i].kern_km[0]) sliced = i;
     if (small < 0 && e[i].bm == 64 && e[i].bn == 64) small = i;
   }
   const int64_t tiles_big = ceil_div(M, 128) * ceil_div(N, 128);
@@ -228,6 +232,7 @@ int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int sms, bool kmajor) 
   if (big_km >= 0) big = big_km;
   if (tiles_big >= 6 * static_cast<int64_t>(sms) || (mid < 0 && small < 0)) return big;
   if (mid >= 0 && 2 * ceil_div(M, 64) * ceil_div(N, 128) >= static_cast<int64_t>(sms)) return mid;
+  if (sliced >= 0 && K >= 2048) return sliced;
   return small >= 0 ? small : big;
 }
 
@@ -513,7 +518,7 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   const int want_pack = cfg ? cfg->pack_a : 0;
   const bool b_vec = !P.trans_b && N % 4 == 0 && P.ldb % 4 == 0 && aligned16(P.B);
   const bool kmajor = want_pack >= 3 || (want_pack == 0 && pad && (b_vec || M >= 512));
-  const int i = pick_ffma(cfg, M, N, sms > 0 ? sms : 1, kmajor);
+  const int i = pick_ffma(cfg, M, N, K, sms > 0 ? sms : 1, kmajor);
   if (i < 0) return MT_ERR_UNSUPPORTED;
   const mt::FfmaEntry& E = e[i];
   // Operands the 16-byte staging cannot read as stored (transposed, rows

@@ -11,6 +11,7 @@ namespace mt {
 // One compiled FFMA tile configuration and its kernel instantiations.
 struct FfmaEntry {
   int bm, bn, bk, stages, threads, min_blocks;
+  int kslices;         // K groups of warps inside a CTA (1 = none)
   int wm, wn, tm, tn;  // warp tile and per-thread tile
   int packed;          // 1: fma.rn.f32x2 micro-kernel, 0: scalar fma
   int pad_a, pad_b;    // padding words per shared row under the rule

@@ -49,14 +49,27 @@
 
 namespace mt {
 
+// KSLICES_ > 1: the CTA's warps form KSLICES_ groups that each cover the
+// whole tile for 1/KSLICES_ of every staged K tile's k steps (group g takes
+// k steps g*BK/KSLICES_ ...); the groups' sums are added through shared
+// memory at the end, group 0's first.  More warps per tile for grids with
+// fewer tiles than SMs.
 template <int BM_, int BN_, int BK_, int WM_, int WN_, int TM_, int TN_,
-          int STAGES_, int MINB_>
+          int STAGES_, int MINB_, int KSLICES_ = 1>
 struct FfmaTile {
   static constexpr int BM = BM_, BN = BN_, BK = BK_;
   static constexpr int WM = WM_, WN = WN_, TM = TM_, TN = TN_;
   static constexpr int STAGES = STAGES_, MIN_BLOCKS = MINB_;
+  static constexpr int KSLICES = KSLICES_;
   static constexpr int WARPS_M = BM / WM, WARPS_N = BN / WN;
-  static constexpr int THREADS = WARPS_M * WARPS_N * 32;
+  static constexpr int TILE_WARPS = WARPS_M * WARPS_N;  // warps covering the tile once
+  static constexpr int THREADS = TILE_WARPS * 32 * KSLICES;
+  static_assert(BK % (4 * KSLICES) == 0, "each K slice takes whole float4 steps");
+  // Shared memory the slice sums go through (groups 1.. of a sliced tile).
+  static constexpr int REDUCE_BYTES = (KSLICES - 1) * BM * BN * 4;
+  static constexpr int at_least_reduce(int bytes) {
+    return bytes > REDUCE_BYTES ? bytes : REDUCE_BYTES;
+  }
   static constexpr int LM = WM / TM;  // lanes of a warp along M
   static constexpr int LN = 32 / LM;  // lanes of a warp along N
   static_assert(BM % WM == 0 && BN % WN == 0, "warp tiles must cover the CTA tile");
@@ -82,7 +95,7 @@ struct FfmaTile {
                       trans ? B_TRANS_PAD : (pad ? vector_row_padding_rule(BN, 1) : 0), STAGES};
   }
   static constexpr int smem_bytes(bool pad, bool trans_b = false) {
-    return a_layout(pad).nbytes() + b_layout(pad, trans_b).nbytes();
+    return at_least_reduce(a_layout(pad).nbytes() + b_layout(pad, trans_b).nbytes());
   }
   // A staged K-major (As[k][m]): a warp reads one k row at a time, float4s
   // of four consecutive rows of A, so the rule gives no padding.
@@ -90,7 +103,7 @@ struct FfmaTile {
     return SmemLayout{BK, BM, vector_row_padding_rule(BM, 1), STAGES};
   }
   static constexpr int smem_bytes_kmajor() {
-    return a_layout_kmajor().nbytes() + b_layout(true).nbytes();
+    return at_least_reduce(a_layout_kmajor().nbytes() + b_layout(true).nbytes());
   }
   // A gathered K-major from row-major storage: the copies write 8 k rows at
   // the same column at once, so the scalar rule asks for one padding word,
@@ -100,7 +113,7 @@ struct FfmaTile {
     return SmemLayout{BK, BM, A_GATHER_PAD, STAGES};
   }
   static constexpr int smem_bytes_gather() {
-    return a_layout_gather().nbytes() + b_layout(true).nbytes();
+    return at_least_reduce(a_layout_gather().nbytes() + b_layout(true).nbytes());
   }
 };
 
@@ -465,7 +478,9 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     cp_async_commit();
   }
 
-  const int warp = tid / 32, lane = tid % 32;
+  // Warp `warp` of K group kg (kg = 0 without K slices).
+  const int kg = tid / 32 / T::TILE_WARPS;
+  const int warp = tid / 32 % T::TILE_WARPS, lane = tid % 32;
   const int wm = warp / T::WARPS_N, wn = warp % T::WARPS_N;
   const int lm = lane % T::LM, ln = lane / T::LM;
   // Thread (lm, ln) of warp (wm, wn) owns rows wm*WM + i*LM + lm (i < TM)
@@ -474,8 +489,12 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
   const auto row_of = [&](int i) {
     return KMAJOR ? wm * T::WM + (i / 4) * T::LM * 4 + lm * 4 + i % 4 : wm * T::WM + i * T::LM + lm;
   };
-  const int a_off = KMAJOR ? LA.offset(0, 0, wm * T::WM + lm * 4) : LA.offset(0, wm * T::WM + lm, 0);
-  const int b_off = LB.offset(0, 0, wn * T::WN + ln * 4);
+  // This group's first k step within a staged K tile.
+  constexpr int KS_STEPS = T::BK / T::KSLICES;
+  const int k_first = kg * KS_STEPS;
+  const int a_off = KMAJOR ? LA.offset(0, k_first, wm * T::WM + lm * 4)
+                           : LA.offset(0, wm * T::WM + lm, k_first);
+  const int b_off = LB.offset(0, k_first, wn * T::WN + ln * 4);
 
   float2 acc[T::TM][T::TN / 2];
 #pragma unroll
@@ -500,7 +519,7 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     const float* a_ptr = As + stage * LA.stage_size() + a_off;
     const float* b_ptr = Bs + stage * LB.stage_size() + b_off;
 #pragma unroll
-    for (int k4 = 0; k4 < T::BK / 4; ++k4) {
+    for (int k4 = 0; k4 < KS_STEPS / 4; ++k4) {
       // Row-major A: one float4 of four k per row, used over the next four
       // k.  K-major A: one float4 of four rows per k.
       float4 a[KMAJOR ? 1 : T::TM];
@@ -544,6 +563,48 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     }
     stage = stage + 1 == T::STAGES ? 0 : stage + 1;
     load_stage = load_stage + 1 == T::STAGES ? 0 : load_stage + 1;
+  }
+
+  if constexpr (T::KSLICES > 1) {
+    // Add the K groups' sums through shared memory (the stages are free once
+    // every copy has landed and every thread is past its last read): groups
+    // 1.. store theirs, group 0 adds them in group order and goes on alone.
+    cp_async_wait<0>();
+    __syncthreads();
+    float* red = reinterpret_cast<float*>(smem_f4);
+    if (kg > 0) {
+      float* mine = red + (kg - 1) * (T::BM * T::BN);
+#pragma unroll
+      for (int i = 0; i < T::TM; ++i) {
+        const int r = row_of(i);
+#pragma unroll
+        for (int g = 0; g < T::TN / 4; ++g) {
+          const int c = wn * T::WN + g * T::LN * 4 + ln * 4;
+          *reinterpret_cast<float4*>(mine + r * T::BN + c) =
+              make_float4(acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
+                          acc[i][2 * g + 1].y);
+        }
+      }
+    }
+    __syncthreads();
+    if (kg > 0) return;
+#pragma unroll
+    for (int s_ = 1; s_ < T::KSLICES; ++s_) {
+      const float* other = red + (s_ - 1) * (T::BM * T::BN);
+#pragma unroll
+      for (int i = 0; i < T::TM; ++i) {
+        const int r = row_of(i);
+#pragma unroll
+        for (int g = 0; g < T::TN / 4; ++g) {
+          const int c = wn * T::WN + g * T::LN * 4 + ln * 4;
+          const float4 o = *reinterpret_cast<const float4*>(other + r * T::BN + c);
+          acc[i][2 * g].x += o.x;
+          acc[i][2 * g].y += o.y;
+          acc[i][2 * g + 1].x += o.z;
+          acc[i][2 * g + 1].y += o.w;
+        }
+      }
+    }
   }
 
   if (partial) {
@@ -614,6 +675,7 @@ FfmaEntry make_entry() {
   e.bk = T::BK;
   e.stages = T::STAGES;
   e.threads = T::THREADS;
+  e.kslices = T::KSLICES;
   e.min_blocks = T::MIN_BLOCKS;
   e.wm = T::WM;
   e.wn = T::WN;
