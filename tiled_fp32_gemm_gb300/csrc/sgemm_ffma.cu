@@ -148,12 +148,19 @@ int ffma_entries_k16(FfmaEntry* out);
 int ffma_entries_64(FfmaEntry* out);
 
 const FfmaEntry* ffma_entries(int* count) {
-  static FfmaEntry entries[32];
+  // Each tile unit fills at most kUnitMax entries into a scratch block;
+  // only whole units that fit are kept, so the table never overruns.
+  constexpr int kCapacity = 32, kUnitMax = 8;
+  static FfmaEntry entries[kCapacity];
   static const int n = [] {
-    int k = ffma_entries_128(entries);
-    k += ffma_entries_alt(entries + k);
-    k += ffma_entries_64(entries + k);
-    k += ffma_entries_k16(entries + k);
+    int (*const units[])(FfmaEntry*) = {ffma_entries_128, ffma_entries_alt, ffma_entries_64,
+                                        ffma_entries_k16};
+    int k = 0;
+    for (auto unit : units) {
+      FfmaEntry scratch[kUnitMax] = {};
+      const int got = unit(scratch);
+      for (int i = 0; i < got && i < kUnitMax && k < kCapacity; ++i) entries[k++] = scratch[i];
+    }
     return k;
   }();
   *count = n;
