@@ -183,6 +183,26 @@ MT_API mt_status mt_sgemm_general(int trans_a, int trans_b, int64_t M, int64_t N
                                   cudaStream_t stream, const mt_config *cfg);
 
 /*
+ * The general form with a bias row, fused into the epilogue:
+ *
+ *     C[i][j] = alpha * (op(A) * op(B))[i][j] + beta * C[i][j] + bias[j]
+ *
+ * bias: N floats in device memory (4-byte aligned), added to every row of C
+ * after the alpha/beta update, in fp32; NULL is the same as
+ * mt_sgemm_general.  The pages stop at the plain product; the bias epilogue
+ * is the usual one of a linear layer (a per-output-column vector) and is
+ * the plainest reading of "bias" for this product.  With alpha == 0 or
+ * K == 0, C = beta * C + bias.  bias overlapping C is MT_ERR_ALIAS; a bias
+ * not 4-byte aligned is MT_ERR_INVALID_ARG.  Every variant applies it,
+ * including its K-slice reduce.  Other errors as mt_sgemm_general.
+ */
+MT_API mt_status mt_sgemm_general_bias(int trans_a, int trans_b, int64_t M, int64_t N,
+                                       int64_t K, float alpha, const float *A, int64_t lda,
+                                       const float *B, int64_t ldb, float beta,
+                                       const float *bias, float *C, int64_t ldc,
+                                       cudaStream_t stream, const mt_config *cfg);
+
+/*
  * C = A*B with A, B, C in HOST memory (pageable or pinned).  Copies A and B
  * to the device, multiplies, copies C back and synchronises `stream` before
  * returning, so on MT_OK the host C holds the result.  Large products are

@@ -71,6 +71,10 @@ def load(path: str | None = None):
                                              ctypes.c_double, ctypes.c_double, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_int]
         lib.oracle_sgemm_general.restype = ctypes.c_int
+        lib.oracle_sgemm_general_bias.argtypes = [p, i64, p, i64, p, p, i64, p, i64, i64,
+                                                  i64, ctypes.c_double, ctypes.c_double,
+                                                  ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.oracle_sgemm_general_bias.restype = ctypes.c_int
         lib.oracle_gemm_mixed_general.argtypes = [ctypes.c_int, p, i64, p, i64, p, i64, p, i64,
                                                   i64, i64, ctypes.c_double, ctypes.c_double,
                                                   ctypes.c_int, ctypes.c_int, ctypes.c_int]
@@ -156,20 +160,26 @@ def sgemm_elements(A, B, ii, jj, lib=None):
 
 
 def sgemm_general(A, B, C0, M, N, K, lda, ldb, ldc, alpha=1.0, beta=0.0,
-                  trans_a=False, trans_b=False, with_w=False, threads: int = 0, lib=None):
-    """alpha*op(A)*op(B) + beta*C on flat float32 buffers with leading
-    dimensions (see oracle_sgemm_general); returns the new C buffer (and W,
-    M x N, if asked).  C0 is copied, never modified."""
+                  trans_a=False, trans_b=False, with_w=False, threads: int = 0, lib=None,
+                  bias=None):
+    """alpha*op(A)*op(B) + beta*C (+ bias[j] on every row) on flat float32
+    buffers with leading dimensions (see oracle_sgemm_general_bias); returns
+    the new C buffer (and W, M x N, if asked).  C0 is copied, never
+    modified."""
     A = np.ascontiguousarray(np.asarray(A, np.float32).reshape(-1))
     B = np.ascontiguousarray(np.asarray(B, np.float32).reshape(-1))
     C = np.array(np.asarray(C0, np.float32).reshape(-1), copy=True)
     W = np.empty((M, N), np.float64) if with_w else None
-    rc = (lib or load()).oracle_sgemm_general(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc,
-                                              _ptr(W) if with_w else None, M, N, K,
-                                              float(alpha), float(beta), int(trans_a),
-                                              int(trans_b), threads)
+    if bias is not None:
+        bias = np.ascontiguousarray(np.asarray(bias, np.float32).reshape(-1))
+        if bias.size < N:
+            raise ValueError("bias needs N values")
+    rc = (lib or load()).oracle_sgemm_general_bias(
+        _ptr(A), lda, _ptr(B), ldb, _ptr(bias) if bias is not None else None, _ptr(C), ldc,
+        _ptr(W) if with_w else None, M, N, K, float(alpha), float(beta), int(trans_a),
+        int(trans_b), threads)
     if rc:
-        raise RuntimeError("oracle_sgemm_general failed")
+        raise RuntimeError("oracle_sgemm_general_bias failed")
     return (C, W) if with_w else C
 
 

@@ -134,9 +134,9 @@ int oracle_sgemm_elements(const float *A, const float *B, float *out,
     return 0;
 }
 
-/* The general form (BLAS-style):
+/* The general form (BLAS-style), with an optional bias row:
  *
- *     C[i][j] = fp32( alpha * sum_k a(i,k) * b(k,j)  +  beta * C[i][j] )
+ *     C[i][j] = fp32( alpha * sum_k a(i,k) * b(k,j)  +  beta * C[i][j]  +  bias[j] )
  *
  * summed in increasing k in double, rounded once, with
  *   a(i,k) = trans_a ? A[k*lda + i] : A[i*lda + k]
@@ -146,12 +146,15 @@ int oracle_sgemm_elements(const float *A, const float *B, float *out,
  * beta = 0, no transposes and packed leading dimensions this is exactly
  * oracle_sgemm (same sum, same rounding).  W (optional, M x N packed)
  * receives |alpha| * sum_k |a(i,k)| |b(k,j)| + |beta| * |C[i][j]|, the
- * scale of the general form's tolerance.  Returns 0, or -1 on a bad
- * argument or allocation failure. */
-int oracle_sgemm_general(const float *A, int64_t lda, const float *B, int64_t ldb,
-                         float *C, int64_t ldc, double *W, int64_t M, int64_t N,
-                         int64_t K, double alpha, double beta, int trans_a, int trans_b,
-                         int nthreads)
+ * scale of the general form's tolerance, plus |bias[j]|.  bias (N floats)
+ * may be NULL: no bias.  The pages stop at the plain product; the bias is
+ * read as a linear layer's, one value per output column added to every
+ * row, inside the same fp64 sum before the single rounding.  Returns 0, or
+ * -1 on a bad argument or allocation failure. */
+int oracle_sgemm_general_bias(const float *A, int64_t lda, const float *B, int64_t ldb,
+                              const float *bias, float *C, int64_t ldc, double *W,
+                              int64_t M, int64_t N, int64_t K, double alpha, double beta,
+                              int trans_a, int trans_b, int nthreads)
 {
     if (M < 0 || N < 0 || K < 0 || ldc < N) return -1;
     if (!trans_a && lda < K) return -1;
@@ -182,11 +185,25 @@ int oracle_sgemm_general(const float *A, int64_t lda, const float *B, int64_t ld
                 c += beta * c0;
                 wc += fabs(beta) * fabs(c0);
             }
+            if (bias) {
+                c += (double)bias[j];
+                wc += fabs((double)bias[j]);
+            }
             C[i * ldc + j] = (float)c;
             if (W) W[i * N + j] = wc;
         }
     }
     return failed ? -1 : 0;
+}
+
+/* The general form without a bias. */
+int oracle_sgemm_general(const float *A, int64_t lda, const float *B, int64_t ldb,
+                         float *C, int64_t ldc, double *W, int64_t M, int64_t N,
+                         int64_t K, double alpha, double beta, int trans_a, int trans_b,
+                         int nthreads)
+{
+    return oracle_sgemm_general_bias(A, lda, B, ldb, NULL, C, ldc, W, M, N, K, alpha, beta,
+                                     trans_a, trans_b, nthreads);
 }
 
 /* ------------------------------------------------------------------------

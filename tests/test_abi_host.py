@@ -290,6 +290,12 @@ def test_invalid_arguments_rejected_on_host():
     assert mt.mt_sgemm(1 << 20, 1 << 30, (1 << 20) + 64, 16, 16, 16, 0) == mt.MT_ERR_ALIAS
     # M == 0 or N == 0 is a no-op.
     assert mt.mt_sgemm(0, 0, 0, 0, 16, 16, 0) == mt.MT_OK
+    # A bias row overlapping C is aliasing; one not 4-byte aligned is invalid.
+    gb = mt.mt_sgemm_general_bias
+    assert gb(0, 0, 16, 16, 16, 1.0, 1 << 20, 16, 1 << 30, 16, 0.0, (1 << 34) + 64, 1 << 34, 16,
+              0, None) == mt.MT_ERR_ALIAS
+    assert gb(0, 0, 16, 16, 16, 1.0, 1 << 20, 16, 1 << 30, 16, 0.0, (1 << 36) + 2, 1 << 34, 16,
+              0, None) == mt.MT_ERR_INVALID_ARG
 
 
 @pytest.mark.skipif(HAS_GPU, reason="checks the no-device path")

@@ -212,3 +212,76 @@ def test_ffma_kmajor_a_is_bit_identical(ta, tb, shape, lda_pad, tile):
                                    with_w=True)
     err = np.abs(ref.reshape(M, ldc)[:, :N].astype(np.float64) - want.reshape(M, ldc)[:, :N])
     assert np.all(err <= 1e-5 * W)
+
+
+@pytest.mark.parametrize("cfg,tol", VARIANTS, ids=VIDS)
+@pytest.mark.parametrize("ta,tb", [(0, 0), (1, 1)])
+def test_bias_epilogue_matches_oracle(cfg, tol, ta, tb):
+    """C = alpha*op(A)*op(B) + beta*C + bias[j], bias fused into every
+    variant's epilogue (and its K-slice reduce).  Tolerance scale W grows by
+    |bias[j]|; integer inputs are exact."""
+    if not supported(cfg, ta):
+        pytest.skip("gathered K-major A needs A stored M x K")
+    M, N, K = 133, 97, 71
+    g = np.random.default_rng(40 + 2 * ta + tb)
+    lda, ldb, ldc = (M if ta else K) + 3, (K if tb else N) + 5, N + 7
+    A = stored(g, K if ta else M, M if ta else K, lda)
+    B = stored(g, N if tb else K, K if tb else N, ldb)
+    C0 = stored(g, M, N, ldc)
+    bias = g.standard_normal(N).astype(np.float32)
+    a, b, c = (torch.from_numpy(x).cuda() for x in (A, B, C0))
+    bias_d = torch.from_numpy(bias).cuda()
+    st = mt.mt_sgemm_general_bias(ta, tb, M, N, K, 1.75, a.data_ptr(), lda, b.data_ptr(), ldb,
+                                  -0.5, bias_d.data_ptr(), c.data_ptr(), ldc,
+                                  torch.cuda.current_stream().cuda_stream,
+                                  mt.make_config(**cfg))
+    assert st == mt.MT_OK, mt.mt_status_string(st)
+    got = c.cpu().numpy()
+    want, W = oracle.sgemm_general(A, B, C0, M, N, K, lda, ldb, ldc, 1.75, -0.5, ta, tb,
+                                   with_w=True, bias=bias)
+    err = np.abs(got[:, :N].astype(np.float64) - want.reshape(M, ldc)[:, :N])
+    assert np.all(err <= tol * W), f"max err/W {(err / np.maximum(W, 1e-30)).max():.3g}"
+    assert np.isnan(got[:, N:]).all()
+    # Integer inputs: exact.
+    Ai = stored(g, K if ta else M, M if ta else K, lda, "int")
+    Bi = stored(g, N if tb else K, K if tb else N, ldb, "int")
+    Ci = stored(g, M, N, ldc, "int")
+    bi = g.integers(-9, 10, N).astype(np.float32)
+    # Device copies held in names for the whole call (a temporary's memory
+    # could be handed to the next allocation before the kernel reads it).
+    ai, bi_, biasi, c = (torch.from_numpy(x).cuda() for x in (Ai, Bi, bi, Ci))
+    st = mt.mt_sgemm_general_bias(ta, tb, M, N, K, 2.0, ai.data_ptr(), lda, bi_.data_ptr(), ldb,
+                                  -3.0, biasi.data_ptr(), c.data_ptr(), ldc,
+                                  torch.cuda.current_stream().cuda_stream,
+                                  mt.make_config(**cfg))
+    torch.cuda.synchronize()
+    assert st == mt.MT_OK
+    want = oracle.sgemm_general(Ai, Bi, Ci, M, N, K, lda, ldb, ldc, 2.0, -3.0, ta, tb, bias=bi)
+    assert np.array_equal(c.cpu().numpy()[:, :N], want.reshape(M, ldc)[:, :N])
+
+
+@pytest.mark.parametrize("shape", [(4096, 4096, 4096), (65536, 128, 4096)])
+def test_bias_on_split_plans_and_empty_product(shape):
+    """The automatic plans of the benchmark shapes (K-major A, K slices in
+    the last partial wave, the transposing copy) with a bias, on sampled
+    rows; alpha = 0 and K = 0 give beta*C + bias."""
+    M, N, K = shape
+    g = torch.Generator().manual_seed(41)
+    A = torch.rand(M, K, generator=g) * 2 - 1
+    B = torch.rand(K, N, generator=g) * 2 - 1
+    bias = torch.randn(N, generator=g)
+    a, b, bd = A.cuda(), B.cuda(), bias.cuda()
+    c = mt.gemm(a, b, bias=bd)
+    torch.cuda.synchronize()
+    rows = np.array(sorted({0, 1, 127, 128, M // 2, M - 1}))
+    Cr, Wr = oracle.sgemm_rows(A.numpy(), B.numpy(), rows, with_w=True)
+    got = c[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
+    want = Cr.astype(np.float64) + bias.numpy()[None, :]
+    assert np.all(np.abs(got - want) <= 1e-5 * (Wr + np.abs(bias.numpy())[None, :]) + 1e-7)
+    c0 = torch.randn(64, 48, generator=g).cuda()
+    bd2 = torch.randn(48, generator=g).cuda()
+    x = torch.zeros(64, 0, device="cuda")
+    y = torch.zeros(0, 48, device="cuda")
+    out = mt.gemm(x, y, c0.clone(), beta=0.5, bias=bd2)
+    torch.cuda.synchronize()
+    assert torch.equal(out, 0.5 * c0 + bd2)

@@ -53,6 +53,8 @@ MUTANTS = {
                               "value(A[i * lda + k])"),
     "general_lda_ignored": ("(trans_a ? A[k * lda + i] : A[i * lda + k])",
                             "(trans_a ? A[k * lda + i] : A[i * K + k])", 0),
+    "bias_reversed": ("c += (double)bias[j];", "c += (double)bias[N - 1 - j];"),
+    "bias_scaled_by_alpha": ("c += (double)bias[j];", "c += alpha * (double)bias[j];"),
 }
 
 

@@ -320,6 +320,33 @@ def test_general_alpha_beta_exact_on_integers():
     assert np.array_equal(C.reshape(M, N), (0.5 * Ci).astype(np.float32))
 
 
+def test_general_bias_closed_forms():
+    """The bias row (one value per output column, added to every row): with
+    alpha = beta = 0 the result is the bias repeated on every row; with
+    integer inputs the whole update is exact against integer arithmetic; W
+    grows by |bias[j]|; no bias is the plain general form."""
+    g = rng(33)
+    M, N, K = 7, 11, 5            # M != N, so a row/column slip shows
+    bias = g.integers(-9, 10, N)
+    C = general(np.full(M * K, np.nan, np.float32), np.full(K * N, np.nan, np.float32),
+                np.full(M * N, np.nan, np.float32), M, N, K, K, N, N, alpha=0.0, beta=0.0,
+                bias=bias.astype(np.float32))
+    assert np.array_equal(C.reshape(M, N), np.tile(bias, (M, 1)).astype(np.float32))
+    Ai = g.integers(-8, 9, (M, K))
+    Bi = g.integers(-8, 9, (K, N))
+    Ci = g.integers(-50, 51, (M, N))
+    C, W = general(Ai.astype(np.float32), Bi.astype(np.float32), Ci.astype(np.float32),
+                   M, N, K, K, N, N, alpha=3.0, beta=-2.0, with_w=True,
+                   bias=bias.astype(np.float32))
+    assert np.array_equal(C.reshape(M, N).astype(np.int64), 3 * (Ai @ Bi) - 2 * Ci + bias)
+    assert np.array_equal(W, 3 * (np.abs(Ai) @ np.abs(Bi)) + 2 * np.abs(Ci) + np.abs(bias))
+    plain = general(Ai.astype(np.float32), Bi.astype(np.float32), Ci.astype(np.float32),
+                    M, N, K, K, N, N, alpha=3.0, beta=-2.0)
+    zero_bias = general(Ai.astype(np.float32), Bi.astype(np.float32), Ci.astype(np.float32),
+                        M, N, K, K, N, N, alpha=3.0, beta=-2.0, bias=np.zeros(N, np.float32))
+    assert np.array_equal(plain, zero_bias)
+
+
 # --- 16-bit inputs (fp16 / bf16 patterns, fp32 result) ------------------------
 ALL16 = np.arange(1 << 16, dtype=np.uint16)
 

@@ -3,7 +3,8 @@
 The compute lives in ``libmtsgemm.so`` (hand-written CUDA for sm_103a, built
 by ``tiled_fp32_gemm_gb300.build``).  This module only marshals arguments:
 
-* ``mt_sgemm``, ``mt_sgemm_ex``, ``mt_sgemm_general``, ``mt_sgemm_host``,
+* ``mt_sgemm``, ``mt_sgemm_ex``, ``mt_sgemm_general``, ``mt_sgemm_general_bias``,
+  ``mt_sgemm_host``,
   ``mt_sgemm_tf32x3_noalloc``,
   ``mt_sgemm_plan``, ``mt_sgemm_general_plan``, ``mt_gemm_mixed``,
   ``mt_gemm_mixed_general``,
@@ -96,6 +97,9 @@ SIGNATURES = {
     "mt_sgemm_tf32x3_noalloc": (_I, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "mt_sgemm_general": (_I, [_I, _I, _I64, _I64, _I64, ctypes.c_float, _P, _I64, _P, _I64,
                               ctypes.c_float, _P, _I64, _P, ctypes.POINTER(mt_config)]),
+    "mt_sgemm_general_bias": (_I, [_I, _I, _I64, _I64, _I64, ctypes.c_float, _P, _I64, _P,
+                                   _I64, ctypes.c_float, _P, _P, _I64, _P,
+                                   ctypes.POINTER(mt_config)]),
     "mt_sgemm_plan": (_I, [_P, _P, _P, _I64, _I64, _I64, ctypes.POINTER(mt_config), _I64,
                            ctypes.POINTER(mt_plan)]),
     "mt_gemm_mixed": (_I, [_I, _P, _P, _P, _I64, _I64, _I64, _P]),
@@ -177,6 +181,15 @@ def mt_sgemm_general(trans_a: int, trans_b: int, M: int, N: int, K: int, alpha: 
                      stream: int = 0, cfg: mt_config | None = None) -> int:
     return lib().mt_sgemm_general(trans_a, trans_b, M, N, K, alpha, A, lda, B, ldb, beta, C,
                                   ldc, stream, ctypes.byref(cfg) if cfg is not None else None)
+
+
+def mt_sgemm_general_bias(trans_a: int, trans_b: int, M: int, N: int, K: int, alpha: float,
+                          A: int, lda: int, B: int, ldb: int, beta: float, bias: int | None,
+                          C: int, ldc: int, stream: int = 0,
+                          cfg: mt_config | None = None) -> int:
+    return lib().mt_sgemm_general_bias(trans_a, trans_b, M, N, K, alpha, A, lda, B, ldb, beta,
+                                       bias, C, ldc, stream,
+                                       ctypes.byref(cfg) if cfg is not None else None)
 
 
 def mt_sgemm_tf32x3_noalloc(A: int, B: int, C: int, M: int, N: int, K: int,
@@ -304,8 +317,9 @@ def plan(M: int, N: int, K: int, smem_limit_bytes: int = 0, a=None, b=None, c=No
 
 
 def gemm(a, b, c=None, alpha=1.0, beta=0.0, trans_a=False, trans_b=False, stream=None,
-         **choices):
-    """c = alpha * op(a) @ op(b) + beta * c on 2-D float32 CUDA tensors whose
+         bias=None, **choices):
+    """c = alpha * op(a) @ op(b) + beta * c (+ bias, a contiguous float32
+    CUDA vector of N added to every row) on 2-D float32 CUDA tensors whose
     rows may be strided (unit column stride); op transposes the stored
     matrix when asked.  Returns c (allocated when not given; then beta must
     be 0)."""
@@ -328,11 +342,21 @@ def gemm(a, b, c=None, alpha=1.0, beta=0.0, trans_a=False, trans_b=False, stream
     def ld(t):  # row stride; any value >= the row length works for one row
         return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
 
+    if bias is not None:
+        if (not isinstance(bias, torch.Tensor) or bias.dtype != torch.float32 or
+                not bias.is_cuda or bias.dim() != 1 or bias.shape[0] != N or
+                not bias.is_contiguous()):
+            raise ValueError("bias must be a contiguous float32 CUDA vector of N")
     s = stream if stream is not None else torch.cuda.current_stream(a.device).cuda_stream
+    cfg = make_config(**choices) if choices else None
     with torch.cuda.device(a.device):
-        st = mt_sgemm_general(int(trans_a), int(trans_b), M, N, K, alpha, a.data_ptr(), ld(a),
-                              b.data_ptr(), ld(b), beta, c.data_ptr(), ld(c), s,
-                              make_config(**choices) if choices else None)
+        if bias is None:
+            st = mt_sgemm_general(int(trans_a), int(trans_b), M, N, K, alpha, a.data_ptr(),
+                                  ld(a), b.data_ptr(), ld(b), beta, c.data_ptr(), ld(c), s, cfg)
+        else:
+            st = mt_sgemm_general_bias(int(trans_a), int(trans_b), M, N, K, alpha, a.data_ptr(),
+                                       ld(a), b.data_ptr(), ld(b), beta, bias.data_ptr(),
+                                       c.data_ptr(), ld(c), s, cfg)
     if st != MT_OK:
         raise MtError(st, "mt_sgemm_general")
     return c

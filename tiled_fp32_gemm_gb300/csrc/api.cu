@@ -78,6 +78,7 @@ struct Problem {
   float alpha, beta;
   int trans_a, trans_b;
   int dtype;
+  const float* bias;  // N floats added to every row of C (nullptr: none)
 };
 
 int ab_bytes(const Problem& P) { return P.dtype ? 2 : 4; }
@@ -170,6 +171,11 @@ mt_status check_problem(const Problem& P) {
                                       : extent_bytes(P.K, P.N, P.ldb, e);
     if (overlaps(P.C, c_bytes, P.A, a_bytes) || overlaps(P.C, c_bytes, P.B, b_bytes))
       return MT_ERR_ALIAS;
+  }
+  if (P.bias) {
+    // Read by every row's epilogue while C is written.
+    if (!aligned4(P.bias)) return MT_ERR_INVALID_ARG;
+    if (overlaps(P.C, c_bytes, P.bias, P.N * 4)) return MT_ERR_ALIAS;
   }
   return MT_OK;
 }
@@ -739,6 +745,7 @@ mt::GemmArgs make_args(const Problem& P, const Launch& L) {
   a.ldc = P.ldc;
   a.alpha = P.alpha;
   a.beta = P.beta;
+  a.bias = P.bias;
   a.trans_a = P.trans_a;
   a.trans_b = P.trans_b;
   a.full_tiles = L.full_tiles;
@@ -825,9 +832,9 @@ mt_status run(const Problem& P, cudaStream_t stream, const mt_config* cfg) {
   if (st != MT_OK) return st;
   if (!reads_ab(P)) {
     // No product to form (K == 0: the accumulator's zeros; alpha == 0):
-    // C = beta * C, A and B untouched.
+    // C = beta * C (+ bias), A and B untouched.
     if (mt::launch_scale_c(P.C, static_cast<int>(P.M), static_cast<int>(P.N), P.ldc, P.beta,
-                           stream) != cudaSuccess) {
+                           P.bias, stream) != cudaSuccess) {
       cudaGetLastError();
       return MT_ERR_LAUNCH;
     }
@@ -963,6 +970,15 @@ mt_status mt_sgemm_general(int trans_a, int trans_b, int64_t M, int64_t N, int64
                            const mt_config* cfg) {
   return run(Problem{A, B, C, M, N, K, lda, ldb, ldc, alpha, beta, trans_a, trans_b}, stream,
              cfg);
+}
+
+mt_status mt_sgemm_general_bias(int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
+                                float alpha, const float* A, int64_t lda, const float* B,
+                                int64_t ldb, float beta, const float* bias, float* C,
+                                int64_t ldc, cudaStream_t stream, const mt_config* cfg) {
+  Problem P{A, B, C, M, N, K, lda, ldb, ldc, alpha, beta, trans_a, trans_b};
+  P.bias = bias;
+  return run(P, stream, cfg);
 }
 
 mt_status mt_sgemm_host(const float* A, const float* B, float* C, int64_t M, int64_t N,

@@ -562,7 +562,7 @@ struct Cfg16 {
     if (a.split > 1) sched.partial = reinterpret_cast<float*>(ws + L.partial_offset);
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int grid = units < max_ctas ? units : max_ctas;
-    const tc::Epilogue ep{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0};
+    const tc::Epilogue ep{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0, a.bias};
     auto go = [&](auto kern) {
       kern<<<grid, f16tc::THREADS, G::SMEM_BYTES, stream>>>(map_a, map_b, idesc, ep, kt, mt, nt,
                                                             a.group_m, sched, fault_inject);
@@ -657,7 +657,7 @@ struct CfgPair {
     if (a.split > 1) sched.partial = reinterpret_cast<float*>(ws + L.partial_offset);
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int clusters = units < max_clusters ? units : max_clusters;
-    const tc::Epilogue ep{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0};
+    const tc::Epilogue ep{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0, a.bias};
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

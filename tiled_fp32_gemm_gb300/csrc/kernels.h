@@ -40,10 +40,11 @@ struct FfmaEntry {
 cudaError_t launch_prep_operand(const float* src, int64_t ld, bool trans, float* out,
                                 int64_t ldo, int R, int cols, cudaStream_t stream);
 
-// C = beta * C over an M x N view with row stride ldc (zeros when beta is
-// 0: C is not read).  The whole product when alpha == 0 or K == 0.
+// C = beta * C (+ bias[col] when bias is not null) over an M x N view with
+// row stride ldc (C is not read when beta is 0).  The whole product when
+// alpha == 0 or K == 0.
 cudaError_t launch_scale_c(float* C, int M, int N, int64_t ldc, float beta,
-                           cudaStream_t stream);
+                           const float* bias, cudaStream_t stream);
 
 // All FFMA configurations built into the library (null-terminated count).
 const FfmaEntry* ffma_entries(int* count);
@@ -62,6 +63,9 @@ struct GemmArgs {
   int64_t lda, ldb, ldc;
   float alpha, beta;
   int trans_a, trans_b;
+  // N floats added to every row of C after alpha * op(A) * op(B) + beta * C
+  // (nullptr: none).
+  const float* bias;
   // Split-K tail (FFMA kernel): work units below full_tiles are whole tiles
   // (tile = unit, in grouped raster order); the remaining tiles are cut
   // into `split` K slices of kt_per_slice K tiles each, one unit per slice,

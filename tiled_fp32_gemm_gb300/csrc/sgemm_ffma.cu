@@ -9,7 +9,7 @@
 namespace mt {
 
 // C[tile] = alpha * (sum over slices s = 0, 1, ... of the slice partials,
-// added in that order) + beta * C[tile], masked to M x N.  Each split tile
+// added in that order) + beta * C[tile] (+ bias[col]), masked to M x N.  Each split tile
 // is cut into `pieces` CTAs of up to 1024 float4 (4 per thread), so a
 // small tail still spreads over the GPU.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(GemmArgs a, int bm, int bn,
@@ -45,11 +45,20 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(GemmArgs a, int bm, 
         o = make_float4(fmaf(a.beta, c0.x, v[0]), fmaf(a.beta, c0.y, v[1]),
                         fmaf(a.beta, c0.z, v[2]), fmaf(a.beta, c0.w, v[3]));
       }
+      if (a.bias) {
+        o.x += a.bias[col];
+        o.y += a.bias[col + 1];
+        o.z += a.bias[col + 2];
+        o.w += a.bias[col + 3];
+      }
       *cp = o;
     } else {
       for (int e = 0; e < 4; ++e)
-        if (col + e < a.N)
-          c_row[col + e] = a.beta != 0.0f ? fmaf(a.beta, c_row[col + e], v[e]) : v[e];
+        if (col + e < a.N) {
+          float o = a.beta != 0.0f ? fmaf(a.beta, c_row[col + e], v[e]) : v[e];
+          if (a.bias) o += a.bias[col + e];
+          c_row[col + e] = o;
+        }
     }
   }
 }
@@ -63,25 +72,27 @@ cudaError_t launch_splitk_reduce(const GemmArgs& a, int bm, int bn, bool vec_c,
   return cudaGetLastError();
 }
 
-// C = beta * C on an M x N view (zeros when beta is 0, C not read).
+// C = beta * C (+ bias[col]) on an M x N view (C not read when beta is 0).
 __global__ void __launch_bounds__(256) scale_c_kernel(float* C, int M, int N, int64_t ldc,
-                                                     float beta) {
+                                                     float beta, const float* bias) {
   const int64_t total = static_cast<int64_t>(M) * N;
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t i = e / N, j = e % N;
     float* c = C + i * ldc + j;
-    *c = beta != 0.0f ? beta * *c : 0.0f;
+    float v = beta != 0.0f ? beta * *c : 0.0f;
+    if (bias) v += bias[j];
+    *c = v;
   }
 }
 
 cudaError_t launch_scale_c(float* C, int M, int N, int64_t ldc, float beta,
-                           cudaStream_t stream) {
+                           const float* bias, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(M) * N;
   if (total <= 0) return cudaSuccess;
   const int64_t blocks = (total + 255) / 256;
   scale_c_kernel<<<static_cast<unsigned>(blocks < 65536 ? blocks : 65536), 256, 0, stream>>>(
-      C, M, N, ldc, beta);
+      C, M, N, ldc, beta, bias);
   return cudaGetLastError();
 }
 

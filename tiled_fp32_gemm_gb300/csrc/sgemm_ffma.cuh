@@ -627,11 +627,12 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     return;
   }
 
-  // Masked epilogue: C[row, col] = alpha * acc + beta * C[row, col] for
-  // row < M, col < N (C is not read when beta == 0; alpha == 1 and
-  // beta == 0 store acc unchanged).
+  // Masked epilogue: C[row, col] = alpha * acc + beta * C[row, col]
+  // (+ bias[col]) for row < M, col < N (C is not read when beta == 0;
+  // alpha == 1, beta == 0 and no bias store acc unchanged).
   float* C = args.C;
   const float alpha = args.alpha, beta = args.beta;
+  const float* bias = args.bias;
 #pragma unroll
   for (int i = 0; i < T::TM; ++i) {
     const int row = m0 + row_of(i);
@@ -651,14 +652,23 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
             v = make_float4(fmaf(beta, o.x, v.x), fmaf(beta, o.y, v.y), fmaf(beta, o.z, v.z),
                             fmaf(beta, o.w, v.w));
           }
+          if (bias) {
+            v.x += bias[col];
+            v.y += bias[col + 1];
+            v.z += bias[col + 2];
+            v.w += bias[col + 3];
+          }
           *cp = v;
         }
       } else {
         const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (col + e < N)
-            c_row[col + e] = beta != 0.0f ? fmaf(beta, c_row[col + e], vv[e]) : vv[e];
+          if (col + e < N) {
+            float o = beta != 0.0f ? fmaf(beta, c_row[col + e], vv[e]) : vv[e];
+            if (bias) o += bias[col + e];
+            c_row[col + e] = o;
+          }
       }
     }
   }

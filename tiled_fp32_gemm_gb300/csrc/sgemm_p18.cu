@@ -97,7 +97,9 @@ __global__ void __launch_bounds__(P18_THREADS) sgemm_p18_kernel(GemmArgs args) {
   if (row < args.M && col < args.N) {
     float* out = args.C + static_cast<int64_t>(row) * args.ldc + col;
     const float v = args.alpha * acc;
-    *out = args.beta != 0.0f ? fmaf(args.beta, *out, v) : v;
+    float o = args.beta != 0.0f ? fmaf(args.beta, *out, v) : v;
+    if (args.bias) o += args.bias[col];
+    *out = o;
   }
 }
 

@@ -809,7 +809,7 @@ struct Cfg {
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int grid = units < max_ctas ? units : max_ctas;
     tf32x3_gemm_kernel<G><<<grid, THREADS, G::SMEM_BYTES, stream>>>(
-        Ap, Bp, Epilogue{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0}, kt, mt, nt,
+        Ap, Bp, Epilogue{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0, a.bias}, kt, mt, nt,
         a.group_m,
         sched, fault_inject);
     cudaError_t e = cudaGetLastError();
@@ -896,7 +896,7 @@ struct CfgPair {
                                                 CfgPair::workspace(a.M, a.N, a.K));
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int clusters = units < max_clusters ? units : max_clusters;
-    const Epilogue ep{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0};
+    const Epilogue ep{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0, a.bias};
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -963,7 +963,7 @@ struct CfgASplit {
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int grid = units < max_ctas ? units : max_ctas;
     tf32x3_asplit_kernel<BK, BN><<<grid, ASPLIT_THREADS, AG::SMEM_BYTES, stream>>>(
-        map_a, Bp, Epilogue{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0}, kt, mt, nt,
+        map_a, Bp, Epilogue{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0, a.bias}, kt, mt, nt,
         a.group_m, sched, fault_inject);
     e = cudaGetLastError();
     if (e != cudaSuccess || a.split <= 1) return e;

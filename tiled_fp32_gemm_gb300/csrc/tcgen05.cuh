@@ -358,12 +358,14 @@ struct Epilogue {
   float alpha, beta;
   int M, N;
   int vec_c;  // 16-byte stores of C allowed (N, ldc % 4 == 0, aligned base)
+  const float* bias;  // N floats added to every row (nullptr: none)
 };
 
 // Drains this warp's 32 TMEM lanes — rows q*32 .. q*32+31 of the BM x BN
 // accumulator whose first column of this warp's lanes is TMEM address
-// `t_row` — to C: C = alpha * acc + beta * C, masked to M x N, C not read
-// when beta == 0; or, for a K slice, to its dense partial tile.
+// `t_row` — to C: C = alpha * acc + beta * C (+ bias[col]), masked to
+// M x N, C not read when beta == 0; or, for a K slice, to its dense partial
+// tile.
 //
 // TILE_M is the tile's row count (BM for one CTA, 2 * BM for a CTA pair) and
 // sub_row0 the first tile row this CTA holds (0, or BM for the odd CTA of a
@@ -400,13 +402,23 @@ __device__ __forceinline__ void store_accumulator(uint32_t t_row, const Unit& w,
               o = make_float4(fmaf(ep.beta, c0.x, o.x), fmaf(ep.beta, c0.y, o.y),
                               fmaf(ep.beta, c0.z, o.z), fmaf(ep.beta, c0.w, o.w));
             }
+            if (ep.bias) {
+              const int c = col0 + 4 * g4;
+              o.x += ep.bias[c];
+              o.y += ep.bias[c + 1];
+              o.z += ep.bias[c + 2];
+              o.w += ep.bias[c + 3];
+            }
             *cp = o;
           }
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          if (col0 + i < ep.N)
-            c_row[col0 + i] = ep.beta != 0.0f ? fmaf(ep.beta, c_row[col0 + i], v[i]) : v[i];
+          if (col0 + i < ep.N) {
+            float o = ep.beta != 0.0f ? fmaf(ep.beta, c_row[col0 + i], v[i]) : v[i];
+            if (ep.bias) o += ep.bias[col0 + i];
+            c_row[col0 + i] = o;
+          }
       }
     }
   }
