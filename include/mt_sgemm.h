@@ -287,6 +287,15 @@ MT_API mt_status mt_gemm_mixed_general(int dtype, int trans_a, int trans_b, int6
                                        float *C, int64_t ldc, cudaStream_t stream,
                                        const mt_config *cfg);
 
+/* mt_gemm_mixed_general with the bias row of mt_sgemm_general_bias (N fp32
+ * values added to every row of C after the alpha/beta update; NULL = none). */
+MT_API mt_status mt_gemm_mixed_general_bias(int dtype, int trans_a, int trans_b, int64_t M,
+                                            int64_t N, int64_t K, float alpha, const void *A,
+                                            int64_t lda, const void *B, int64_t ldb,
+                                            float beta, const float *bias, float *C,
+                                            int64_t ldc, cudaStream_t stream,
+                                            const mt_config *cfg);
+
 /* C = A*B with 16-bit A (M x K, row stride K) and B (K x N, row stride N),
  * fp32 C (M x N): mt_gemm_mixed_general(dtype, 0, 0, M, N, K, 1, A, K, B, N,
  * 0, C, N, stream, NULL). */

@@ -79,6 +79,11 @@ def load(path: str | None = None):
                                                   i64, i64, ctypes.c_double, ctypes.c_double,
                                                   ctypes.c_int, ctypes.c_int, ctypes.c_int]
         lib.oracle_gemm_mixed_general.restype = ctypes.c_int
+        lib.oracle_gemm_mixed_general_bias.argtypes = [ctypes.c_int, p, i64, p, i64, p, p, i64,
+                                                       p, i64, i64, i64, ctypes.c_double,
+                                                       ctypes.c_double, ctypes.c_int,
+                                                       ctypes.c_int, ctypes.c_int]
+        lib.oracle_gemm_mixed_general_bias.restype = ctypes.c_int
         lib.oracle_f16_value.argtypes = [ctypes.c_uint16]
         lib.oracle_f16_value.restype = ctypes.c_double
         lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
@@ -215,17 +220,21 @@ def value16(dtype: int, patterns) -> np.ndarray:
 
 def gemm_mixed_general(dtype, A, B, C0, M, N, K, lda, ldb, ldc, alpha=1.0, beta=0.0,
                        trans_a=False, trans_b=False, with_w=False, threads: int = 0,
-                       lib=None):
-    """alpha*op(A)*op(B) + beta*C on flat 16-bit A and B (dtype F16 or BF16)
-    and a flat float32 C; returns the new C buffer (and W, M x N, if asked).
-    C0 is copied, never modified."""
+                       lib=None, bias=None):
+    """alpha*op(A)*op(B) + beta*C (+ bias[j] on every row) on flat 16-bit A
+    and B (dtype F16 or BF16) and a flat float32 C; returns the new C buffer
+    (and W, M x N, if asked).  C0 is copied, never modified."""
     A, B = _u16(A), _u16(B)
     C = np.array(np.asarray(C0, np.float32).reshape(-1), copy=True)
     W = np.empty((M, N), np.float64) if with_w else None
-    rc = (lib or load()).oracle_gemm_mixed_general(int(dtype), _ptr(A), lda, _ptr(B), ldb,
-                                                   _ptr(C), ldc, _ptr(W) if with_w else None,
-                                                   M, N, K, float(alpha), float(beta),
-                                                   int(trans_a), int(trans_b), threads)
+    if bias is not None:
+        bias = np.ascontiguousarray(np.asarray(bias, np.float32).reshape(-1))
+        if bias.size < N:
+            raise ValueError("bias needs N values")
+    rc = (lib or load()).oracle_gemm_mixed_general_bias(
+        int(dtype), _ptr(A), lda, _ptr(B), ldb, _ptr(bias) if bias is not None else None,
+        _ptr(C), ldc, _ptr(W) if with_w else None, M, N, K, float(alpha), float(beta),
+        int(trans_a), int(trans_b), threads)
     if rc:
-        raise RuntimeError("oracle_gemm_mixed_general failed")
+        raise RuntimeError("oracle_gemm_mixed_general_bias failed")
     return (C, W) if with_w else C

@@ -249,12 +249,14 @@ double oracle_bf16_value(uint16_t h)
 }
 
 /* The general form on 16-bit A and B (both of type `dtype`, ORACLE_F16 or
- * ORACLE_BF16), fp32 C; layouts, W and the alpha/beta rules as in
- * oracle_sgemm_general.  Returns 0, or -1 on a bad argument. */
-int oracle_gemm_mixed_general(int dtype, const uint16_t *A, int64_t lda, const uint16_t *B,
-                              int64_t ldb, float *C, int64_t ldc, double *W, int64_t M,
-                              int64_t N, int64_t K, double alpha, double beta, int trans_a,
-                              int trans_b, int nthreads)
+ * ORACLE_BF16), fp32 C; layouts, W, the alpha/beta rules and the optional
+ * bias row (NULL: none) as in oracle_sgemm_general_bias.  Returns 0, or -1
+ * on a bad argument. */
+int oracle_gemm_mixed_general_bias(int dtype, const uint16_t *A, int64_t lda,
+                                   const uint16_t *B, int64_t ldb, const float *bias, float *C,
+                                   int64_t ldc, double *W, int64_t M, int64_t N, int64_t K,
+                                   double alpha, double beta, int trans_a, int trans_b,
+                                   int nthreads)
 {
     if (dtype != ORACLE_F16 && dtype != ORACLE_BF16) return -1;
     if (M < 0 || N < 0 || K < 0 || ldc < N) return -1;
@@ -286,11 +288,25 @@ int oracle_gemm_mixed_general(int dtype, const uint16_t *A, int64_t lda, const u
                 c += beta * c0;
                 wc += fabs(beta) * fabs(c0);
             }
+            if (bias) {
+                c += (double)bias[j];
+                wc += fabs((double)bias[j]);
+            }
             C[i * ldc + j] = (float)c;
             if (W) W[i * N + j] = wc;
         }
     }
     return 0;
+}
+
+/* The 16-bit general form without a bias. */
+int oracle_gemm_mixed_general(int dtype, const uint16_t *A, int64_t lda, const uint16_t *B,
+                              int64_t ldb, float *C, int64_t ldc, double *W, int64_t M,
+                              int64_t N, int64_t K, double alpha, double beta, int trans_a,
+                              int trans_b, int nthreads)
+{
+    return oracle_gemm_mixed_general_bias(dtype, A, lda, B, ldb, NULL, C, ldc, W, M, N, K,
+                                          alpha, beta, trans_a, trans_b, nthreads);
 }
 
 int oracle_max_threads(void)

@@ -255,3 +255,42 @@ def test_mixed_timeout_path_reports_and_context_survives(tile):
                                         100, 72, 80, 80, 72, 72, with_w=True)
     assert_within(got, want.reshape(100, 72), W, "after timeout")
     assert mt.mt_device_status(0) == mt.MT_OK
+
+
+@pytest.mark.parametrize("dt", sorted(DTYPES))
+@pytest.mark.parametrize("ta,tb", [(0, 0), (1, 1)])
+@pytest.mark.parametrize("tile", sorted(TILES))
+def test_mixed_bias_epilogue(dt, ta, tb, tile):
+    """The bias row on 16-bit inputs (mt_gemm_mixed_general_bias): integer
+    inputs exact; normal inputs within 5e-5 * (W + |bias|), on every tile
+    and its split tail."""
+    code, tdt = DTYPES[dt]
+    M, N, K = 300, 264, 1000
+    g = np.random.default_rng(21 + ta)
+    a_rows, a_cols = (K, M) if ta else (M, K)
+    b_rows, b_cols = (N, K) if tb else (K, N)
+    for dist in ("int", "normal"):
+        A = stored16(g, a_rows, a_cols, a_cols, tdt, dist)
+        B = stored16(g, b_rows, b_cols, b_cols, tdt, dist)
+        C0 = draw(g, (M, N), dist)
+        bias = draw(g, (N,), dist)
+        a, b, c, bd = A.cuda(), B.cuda(), torch.from_numpy(C0).cuda(), torch.from_numpy(bias).cuda()
+        st = mt.mt_gemm_mixed_general_bias(code, ta, tb, M, N, K, 2.0, a.data_ptr(), a_cols,
+                                           b.data_ptr(), b_cols, -3.0, bd.data_ptr(),
+                                           c.data_ptr(), N, torch.cuda.current_stream().cuda_stream,
+                                           mt.make_config(**TILES[tile]) if TILES[tile] else None)
+        assert st == mt.MT_OK, mt.mt_status_string(st)
+        got = c.cpu().numpy()
+        want, W = oracle.gemm_mixed_general(code, A, B, C0, M, N, K, a_cols, b_cols, N, 2.0,
+                                            -3.0, ta, tb, with_w=True, bias=bias)
+        want = want.reshape(M, N)
+        if dist == "int":
+            assert np.array_equal(got, want)
+        else:
+            assert_within(got, want, W, f"bias {dt} {tile}")
+    # The same through the torch-level call.
+    out = mt.gemm_mixed(a, b, trans_a=bool(ta), trans_b=bool(tb), bias=bd, **TILES[tile])
+    want0, W0 = oracle.gemm_mixed_general(code, A, B, np.zeros(M * N, np.float32), M, N, K,
+                                          a_cols, b_cols, N, 1.0, 0.0, ta, tb, with_w=True,
+                                          bias=bias)
+    assert_within(out.cpu().numpy(), want0.reshape(M, N), W0, "gemm_mixed bias")

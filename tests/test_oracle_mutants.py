@@ -53,8 +53,9 @@ MUTANTS = {
                               "value(A[i * lda + k])"),
     "general_lda_ignored": ("(trans_a ? A[k * lda + i] : A[i * lda + k])",
                             "(trans_a ? A[k * lda + i] : A[i * K + k])", 0),
-    "bias_reversed": ("c += (double)bias[j];", "c += (double)bias[N - 1 - j];"),
-    "bias_scaled_by_alpha": ("c += (double)bias[j];", "c += alpha * (double)bias[j];"),
+    "bias_reversed": ("c += (double)bias[j];", "c += (double)bias[N - 1 - j];", 0),
+    "bias_scaled_by_alpha": ("c += (double)bias[j];", "c += alpha * (double)bias[j];", 0),
+    "mixed_bias_reversed": ("c += (double)bias[j];", "c += (double)bias[N - 1 - j];", 1),
 }
 
 

@@ -437,6 +437,29 @@ def test_mixed_reduces_to_fp32_oracle_on_widened_inputs(dtype):
     assert np.array_equal(C.reshape(M, N), ref)
 
 
+@pytest.mark.parametrize("dtype", [1, 2])
+def test_mixed_bias_closed_forms(dtype):
+    """16-bit inputs with a bias row: integer inputs give the exact integer
+    update plus the bias on every column j (M != N, so a row/column slip
+    shows); the bias alone with alpha = beta = 0."""
+    g = rng(60 + dtype)
+    M, N, K = 9, 14, 7
+    Ai = g.integers(-8, 9, (M, K))
+    Bi = g.integers(-8, 9, (K, N))
+    Ci = g.integers(-50, 51, (M, N))
+    bias = g.integers(-9, 10, N)
+    A16, B16 = _int16_operands(dtype, Ai, Bi)
+    C, W = oracle.gemm_mixed_general(dtype, A16, B16, Ci.astype(np.float32), M, N, K, K, N, N,
+                                     alpha=2.0, beta=-3.0, with_w=True, lib=LIB,
+                                     bias=bias.astype(np.float32))
+    assert np.array_equal(C.reshape(M, N).astype(np.int64), 2 * (Ai @ Bi) - 3 * Ci + bias)
+    assert np.array_equal(W, 2 * (np.abs(Ai) @ np.abs(Bi)) + 3 * np.abs(Ci) + np.abs(bias))
+    C = oracle.gemm_mixed_general(dtype, A16, B16, np.full(M * N, np.nan, np.float32), M, N, K,
+                                  K, N, N, alpha=0.0, beta=0.0, lib=LIB,
+                                  bias=bias.astype(np.float32))
+    assert np.array_equal(C.reshape(M, N), np.tile(bias, (M, 1)).astype(np.float32))
+
+
 def test_mixed_rejects_unknown_dtype():
     with pytest.raises(RuntimeError):
         oracle.gemm_mixed_general(3, np.zeros(4, np.uint16), np.zeros(4, np.uint16),

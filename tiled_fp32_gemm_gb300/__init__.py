@@ -7,7 +7,7 @@ by ``tiled_fp32_gemm_gb300.build``).  This module only marshals arguments:
   ``mt_sgemm_host``,
   ``mt_sgemm_tf32x3_noalloc``,
   ``mt_sgemm_plan``, ``mt_sgemm_general_plan``, ``mt_gemm_mixed``,
-  ``mt_gemm_mixed_general``,
+  ``mt_gemm_mixed_general``, ``mt_gemm_mixed_general_bias``,
   ``mt_gemm_mixed_plan``,
   ``mt_smem_row_padding``, ``mt_smem_vector_row_padding``,
   ``mt_smem_layout_make``, ``mt_smem_layout_offset``, ``mt_device_status``,
@@ -106,6 +106,9 @@ SIGNATURES = {
     "mt_gemm_mixed_general": (_I, [_I, _I, _I, _I64, _I64, _I64, ctypes.c_float, _P, _I64,
                                    _P, _I64, ctypes.c_float, _P, _I64, _P,
                                    ctypes.POINTER(mt_config)]),
+    "mt_gemm_mixed_general_bias": (_I, [_I, _I, _I, _I64, _I64, _I64, ctypes.c_float, _P,
+                                        _I64, _P, _I64, ctypes.c_float, _P, _P, _I64, _P,
+                                        ctypes.POINTER(mt_config)]),
     "mt_gemm_mixed_plan": (_I, [_I, _I, _I, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64,
                                 ctypes.POINTER(mt_config), _I64, ctypes.POINTER(mt_plan)]),
     "mt_sgemm_general_plan": (_I, [_I, _I, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64,
@@ -220,6 +223,15 @@ def mt_gemm_mixed_general(dtype: int, trans_a: int, trans_b: int, M: int, N: int
     return lib().mt_gemm_mixed_general(dtype, trans_a, trans_b, M, N, K, alpha, A, lda, B,
                                        ldb, beta, C, ldc, stream,
                                        ctypes.byref(cfg) if cfg is not None else None)
+
+
+def mt_gemm_mixed_general_bias(dtype: int, trans_a: int, trans_b: int, M: int, N: int, K: int,
+                               alpha: float, A: int, lda: int, B: int, ldb: int, beta: float,
+                               bias: int | None, C: int, ldc: int, stream: int = 0,
+                               cfg: mt_config | None = None) -> int:
+    return lib().mt_gemm_mixed_general_bias(dtype, trans_a, trans_b, M, N, K, alpha, A, lda,
+                                            B, ldb, beta, bias, C, ldc, stream,
+                                            ctypes.byref(cfg) if cfg is not None else None)
 
 
 def mt_gemm_mixed_plan(dtype: int, trans_a: int, trans_b: int, M: int, N: int, K: int,
@@ -372,11 +384,12 @@ def _dtype_code(t) -> int:
 
 
 def gemm_mixed(a, b, c=None, alpha=1.0, beta=0.0, trans_a=False, trans_b=False, stream=None,
-               **choices):
-    """c (float32) = alpha * op(a) @ op(b) + beta * c with a and b 2-D CUDA
-    tensors of the same 16-bit dtype (float16 or bfloat16) whose rows may be
-    strided (unit column stride), through mt_gemm_mixed_general.  Returns c
-    (allocated when not given; then beta must be 0)."""
+               bias=None, **choices):
+    """c (float32) = alpha * op(a) @ op(b) + beta * c (+ bias, N float32
+    values on every row) with a and b 2-D CUDA tensors of the same 16-bit
+    dtype (float16 or bfloat16) whose rows may be strided (unit column
+    stride), through mt_gemm_mixed_general(_bias).  Returns c (allocated
+    when not given; then beta must be 0)."""
     import torch
     for t, name in ((a, "a"), (b, "b")):
         if not isinstance(t, torch.Tensor) or not t.is_cuda:
@@ -400,12 +413,22 @@ def gemm_mixed(a, b, c=None, alpha=1.0, beta=0.0, trans_a=False, trans_b=False, 
     def ld(t):  # row stride; any value >= the row length works for one row
         return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
 
+    if bias is not None:
+        if (not isinstance(bias, torch.Tensor) or bias.dtype != torch.float32 or
+                not bias.is_cuda or bias.dim() != 1 or bias.shape[0] != N or
+                not bias.is_contiguous()):
+            raise ValueError("bias must be a contiguous float32 CUDA vector of N")
     s = stream if stream is not None else torch.cuda.current_stream(a.device).cuda_stream
+    cfg = make_config(**choices) if choices else None
     with torch.cuda.device(a.device):
-        st = mt_gemm_mixed_general(code, int(trans_a), int(trans_b), M, N, K, alpha,
-                                   a.data_ptr(), ld(a), b.data_ptr(), ld(b), beta,
-                                   c.data_ptr(), ld(c), s,
-                                   make_config(**choices) if choices else None)
+        if bias is None:
+            st = mt_gemm_mixed_general(code, int(trans_a), int(trans_b), M, N, K, alpha,
+                                       a.data_ptr(), ld(a), b.data_ptr(), ld(b), beta,
+                                       c.data_ptr(), ld(c), s, cfg)
+        else:
+            st = mt_gemm_mixed_general_bias(code, int(trans_a), int(trans_b), M, N, K, alpha,
+                                            a.data_ptr(), ld(a), b.data_ptr(), ld(b), beta,
+                                            bias.data_ptr(), c.data_ptr(), ld(c), s, cfg)
     if st != MT_OK:
         raise MtError(st, "mt_gemm_mixed_general")
     return c

@@ -1150,6 +1150,17 @@ mt_status mt_gemm_mixed_general(int dtype, int trans_a, int trans_b, int64_t M, 
              stream, cfg);
 }
 
+mt_status mt_gemm_mixed_general_bias(int dtype, int trans_a, int trans_b, int64_t M, int64_t N,
+                                     int64_t K, float alpha, const void* A, int64_t lda,
+                                     const void* B, int64_t ldb, float beta, const float* bias,
+                                     float* C, int64_t ldc, cudaStream_t stream,
+                                     const mt_config* cfg) {
+  if (dtype != MT_DTYPE_F16 && dtype != MT_DTYPE_BF16) return MT_ERR_INVALID_ARG;
+  Problem P{A, B, C, M, N, K, lda, ldb, ldc, alpha, beta, trans_a, trans_b, dtype};
+  P.bias = bias;
+  return run(P, stream, cfg);
+}
+
 // Plan of a general-form call of either element type (dtype 0: fp32).
 mt_status plan_general(int dtype, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
                        const void* A, int64_t lda, const void* B, int64_t ldb, const float* C,
