@@ -578,7 +578,11 @@ def run_gpu(args):
                "h2d_bytes_per_step": sum(4 * (w.M * w.K + w.K * w.N) for (w, *_r) in hbufs),
                "d2h_bytes_per_step": sum(4 * w.M * w.N for (w, *_r) in hbufs),
                "api": "mt_sgemm_host", "link": link,
-               "step_ms": [round(t * 1e3, 3) for t in step_s]}
+               "step_ms": [round(t * 1e3, 3) for t in step_s],
+               # Context for a step that stalled on the shared host: the same
+               # metric over the median step (value stays total work / total time).
+               "value_at_median_step": job_tflops(world, flops_step, 1,
+                                                  statistics.median(step_s))}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
