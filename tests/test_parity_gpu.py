@@ -186,13 +186,16 @@ def test_split_k_matches_oracle_and_is_deterministic(shape, split):
 
 
 @pytest.mark.parametrize("shape,rows_only", [((512, 512, 4096), False),
+                                             ((300, 200, 5000), False),
+                                             ((33, 17, 9000), False),
                                              ((2048, 2048, 8192), True),
                                              ((65536, 128, 4096), True)])
 def test_automatic_k_slices_match_oracle(shape, rows_only):
-    """The automatic plans cut K: 512 x 512 x 4096 has fewer tiles than SMs
-    (every tile in slices), 2048 x 2048 x 8192 and 65536 x 128 x 4096 leave
-    a last partial wave (only those tiles in slices).  Within the tolerance
-    and deterministic."""
+    """The automatic plans cut K: 512 x 512 x 4096 and the ragged 300 x 200
+    x 5000 and 33 x 17 x 9000 have fewer tiles than SMs (every tile in
+    slices, each CTA with two K groups of warps), 2048 x 2048 x 8192 and
+    65536 x 128 x 4096 leave a last partial wave (only those tiles in
+    slices).  Within the tolerance and deterministic."""
     M, N, K = shape
     A, B = gemm_inputs.make_ab(M, N, K, seed=18, dist="uniform")
     a, b = A.cuda(), B.cuda()

@@ -628,10 +628,10 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   if (cfg && cfg->split_k > 1) {
     full = 0;
     split = std::min<int64_t>(cfg->split_k, ktiles > 0 ? ktiles : 1);
-  } else if (L->a_kmajor && !(cfg && cfg->split_k == 1)) {
-    // K-major A (split_k = 1 turns both off): fewer tiles than SMs are cut
-    // into up to 4 K slices of at least 512 (512 x 512 x 4096: 2.7x); a
-    // last wave under half full is cut into K slices (the CTAs of whole
+  } else if (!(cfg && cfg->split_k == 1)) {
+    // split_k = 1 turns both off.  Fewer tiles than SMs are cut into up to
+    // 4 K slices of at least 512 (512 x 512 x 4096: 2.7x).  With K-major A,
+    // a last wave under half full is cut into K slices (the CTAs of whole
     // tiles come first, so the slices make up the last wave; 4097 x 3001 x
     // 2053 and 65536 x 128 x 4096 1.04x, 2048 x 2048 x 8192 1.15x).
     const int64_t n_sm = std::max(sms, 1);
@@ -642,7 +642,7 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
         full = 0;
         split = sk;
       }
-    } else {
+    } else if (L->a_kmajor) {
       split_tail(tiles, n_sm * E.min_blocks, ktiles, true, &full, &split);
     }
   }
