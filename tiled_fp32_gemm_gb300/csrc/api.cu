@@ -549,10 +549,16 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
     // reads it, copied first when it cannot be read as stored.
     const bool direct = P.trans_a && M % 4 == 0 && P.lda % 4 == 0 && aligned16(P.A);
     if (want_pack == 4 && P.trans_a) return MT_ERR_UNSUPPORTED;
+    // For A stored M x K the automatic copy is capped at 2 GiB of workspace
+    // (A^T is as large as A): a larger A is gathered, which needs none.  A
+    // stored K x M that cannot be read as stored is always copied (the
+    // gather reads A stored M x K only).
+    const int64_t copy_bytes = K * (ceil_div(std::max<int64_t>(M, 1), 4) * 4) * 4;
     const bool copy = want_pack == 5 ||
                       (want_pack != 4 && !direct &&
                        (P.trans_a ||
-                        (N >= 2048 && static_cast<double>(M) * N * K >= 1073741824.0)));
+                        (copy_bytes <= (int64_t(2) << 30) && N >= 2048 &&
+                         static_cast<double>(M) * N * K >= 1073741824.0)));
     L->a_kmajor = true;
     L->prep_a_kmajor = copy;
     L->a_gather = !direct && !copy;
