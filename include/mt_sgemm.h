@@ -219,6 +219,22 @@ MT_API mt_status mt_sgemm_host(const float *A, const float *B, float *C,
                         const mt_config *cfg);
 
 /*
+ * mt_sgemm_host without the final synchronisation: the copies in, products
+ * and copies out are enqueued and the call returns; the result is in the
+ * host C once `stream` has completed the work enqueued before the return
+ * (for example after cudaStreamSynchronize(stream)).  A, B and C must stay
+ * valid and A, B unchanged until then.  With pinned host memory successive
+ * calls overlap: a call's copies in start while the products of the calls
+ * before it still run.  With pageable C the copies out are synchronous, so
+ * the call returns only when it is done.  Errors found before anything is
+ * enqueued are returned; a failure of enqueued work shows at the
+ * synchronisation, as for any stream work.
+ */
+MT_API mt_status mt_sgemm_host_async(const float *A, const float *B, float *C,
+                                     int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+                                     const mt_config *cfg);
+
+/*
  * Allocation-free form of the MT_VARIANT_TF32X3 call, for callers that must
  * not allocate device memory while they run: code whose device memory is
  * owned by someone else (a host application or framework that hands it a

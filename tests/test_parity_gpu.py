@@ -366,3 +366,29 @@ def test_host_entry_point_pipelined_blocks(pinned):
     assert st == mt.MT_OK
     assert_within(c.numpy()[rows], Cr, Wr, 5e-5, "host pipelined tf32x3")
     assert mt.mt_device_status(0) == mt.MT_OK
+
+
+def test_host_entry_point_async_calls_overlap_and_match():
+    """Two mt_sgemm_host_async calls back to back on one stream (pinned
+    buffers), then one synchronisation: each result equals the synchronous
+    entry point's bit for bit."""
+    shapes = [(4096, 2048, 1024), (2048, 4096, 2048)]
+    bufs = []
+    for i, (M, N, K) in enumerate(shapes):
+        A, B = gemm_inputs.make_ab(M, N, K, seed=60 + i, dist="normal")
+        bufs.append((M, N, K, A.pin_memory(), B.pin_memory(),
+                     torch.full((M, N), float("nan")).pin_memory(),
+                     torch.full((M, N), float("nan")).pin_memory()))
+    s = torch.cuda.Stream()
+    for (M, N, K, A, B, c_async, _c) in bufs:
+        assert mt.mt_sgemm_host_async(A.data_ptr(), B.data_ptr(), c_async.data_ptr(), M, N, K,
+                                      s.cuda_stream, None) == mt.MT_OK
+    s.synchronize()
+    for (M, N, K, A, B, c_async, c_sync) in bufs:
+        assert mt.mt_sgemm_host(A.data_ptr(), B.data_ptr(), c_sync.data_ptr(), M, N, K, 0,
+                                None) == mt.MT_OK
+        assert torch.equal(c_async, c_sync)
+        rows = np.array([0, M // 2, M - 1])
+        Cr, Wr = oracle.sgemm_rows(A.numpy(), B.numpy(), rows, with_w=True)
+        assert_within(c_async.numpy()[rows], Cr, Wr, FFMA_TOL, "host async")
+    assert mt.mt_device_status(0) == mt.MT_OK

@@ -4,7 +4,7 @@ The compute lives in ``libmtsgemm.so`` (hand-written CUDA for sm_103a, built
 by ``tiled_fp32_gemm_gb300.build``).  This module only marshals arguments:
 
 * ``mt_sgemm``, ``mt_sgemm_ex``, ``mt_sgemm_general``, ``mt_sgemm_general_bias``,
-  ``mt_sgemm_host``,
+  ``mt_sgemm_host``, ``mt_sgemm_host_async``,
   ``mt_sgemm_tf32x3_noalloc``,
   ``mt_sgemm_plan``, ``mt_sgemm_general_plan``, ``mt_gemm_mixed``,
   ``mt_gemm_mixed_general``, ``mt_gemm_mixed_general_bias``,
@@ -94,6 +94,7 @@ SIGNATURES = {
     "mt_sgemm": (_I, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "mt_sgemm_ex": (_I, [_P, _P, _P, _I64, _I64, _I64, _P, ctypes.POINTER(mt_config)]),
     "mt_sgemm_host": (_I, [_P, _P, _P, _I64, _I64, _I64, _P, ctypes.POINTER(mt_config)]),
+    "mt_sgemm_host_async": (_I, [_P, _P, _P, _I64, _I64, _I64, _P, ctypes.POINTER(mt_config)]),
     "mt_sgemm_tf32x3_noalloc": (_I, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "mt_sgemm_general": (_I, [_I, _I, _I64, _I64, _I64, ctypes.c_float, _P, _I64, _P, _I64,
                               ctypes.c_float, _P, _I64, _P, ctypes.POINTER(mt_config)]),
@@ -177,6 +178,12 @@ def mt_sgemm_host(A: int, B: int, C: int, M: int, N: int, K: int, stream: int = 
                   cfg: mt_config | None = None) -> int:
     return lib().mt_sgemm_host(A, B, C, M, N, K, stream,
                                ctypes.byref(cfg) if cfg is not None else None)
+
+
+def mt_sgemm_host_async(A: int, B: int, C: int, M: int, N: int, K: int, stream: int = 0,
+                        cfg: mt_config | None = None) -> int:
+    return lib().mt_sgemm_host_async(A, B, C, M, N, K, stream,
+                                     ctypes.byref(cfg) if cfg is not None else None)
 
 
 def mt_sgemm_general(trans_a: int, trans_b: int, M: int, N: int, K: int, alpha: float,

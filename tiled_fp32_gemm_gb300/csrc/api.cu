@@ -956,6 +956,113 @@ int64_t host_block_rows(int64_t M, int64_t N, int64_t K) {
   return rows * 2 <= M ? rows : M;
 }
 
+// The host-buffer pipeline behind mt_sgemm_host (sync) and
+// mt_sgemm_host_async.  A and B's device copies are allocated on the
+// copy-in stream, so a call's copies in do not queue behind the products of
+// an earlier call on `stream`; C's copy comes from `stream` and goes back to
+// the pool from the copy-out stream after its last copy out.  `stream` waits
+// for the last copy out, so the call is complete once `stream` is.
+mt_status host_pipeline(const float* A, const float* B, float* C, int64_t M, int64_t N,
+                        int64_t K, cudaStream_t stream, const mt_config* cfg, bool sync) {
+  mt_status st0 = check_dims(M, N, K);
+  if (st0 != MT_OK) return st0;
+  if (M == 0 || N == 0) return MT_OK;
+  if (!C || (K > 0 && (!A || !B))) return MT_ERR_INVALID_ARG;
+  int dev = 0;
+  DeviceInfo info;
+  mt_status st = current_device(&dev, &info);
+  if (st != MT_OK) return st;
+  cudaMemPool_t pool = nullptr;
+  st = pool_for(dev, &pool);
+  if (st != MT_OK) return st;
+  HostStreams hs;
+  st = host_streams(dev, &hs);
+  if (st != MT_OK) return st;
+  const size_t a_bytes = static_cast<size_t>(M * K) * 4, b_bytes = static_cast<size_t>(K * N) * 4,
+               c_bytes = static_cast<size_t>(M * N) * 4;
+  float *dA = nullptr, *dB = nullptr, *dC = nullptr;
+  bool ok = true;
+  const int64_t rows = host_block_rows(M, N, K);
+  const int64_t blocks = ceil_div(M, rows);
+  cudaEvent_t ev[2 * kMaxHostBlocks + 3] = {};
+  const int nev = static_cast<int>(2 * blocks + 3);
+  for (int i = 0; i < nev && ok; ++i)
+    ok = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
+  cudaEvent_t ev_calloc = ev[0], ev_done = ev[1], ev_in_done = ev[2];
+  // 256-byte aligned pool blocks keep the 16-byte staging path available.
+  if (ok && a_bytes)
+    ok = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dA), a_bytes, pool, hs.h2d) ==
+         cudaSuccess;
+  if (ok && b_bytes)
+    ok = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dB), b_bytes, pool, hs.h2d) ==
+         cudaSuccess;
+  if (ok)
+    ok = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dC), c_bytes, pool, stream) ==
+         cudaSuccess;
+  // C's buffer was allocated on the caller's stream; the copy-out stream
+  // writes from it.
+  if (ok) ok = cudaEventRecord(ev_calloc, stream) == cudaSuccess &&
+               cudaStreamWaitEvent(hs.d2h, ev_calloc, 0) == cudaSuccess;
+  if (ok && b_bytes) ok = cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, hs.h2d) == cudaSuccess;
+  // Row blocks of A and C: block i's copy in, product and copy out run on
+  // the copy-in stream, the caller's stream and the copy-out stream, so the
+  // copies of neighbouring blocks overlap the product of this one.
+  for (int64_t i = 0; i < blocks && ok && st == MT_OK; ++i) {
+    const int64_t r0 = i * rows, nr = std::min(rows, M - r0);
+    cudaEvent_t ev_in = ev[3 + 2 * i], ev_out = ev[4 + 2 * i];
+    // Block i of A (and, before block 0, all of B) is on the device ...
+    if (K > 0)
+      ok = cudaMemcpyAsync(dA + r0 * K, A + r0 * K, static_cast<size_t>(nr * K) * 4,
+                           cudaMemcpyHostToDevice, hs.h2d) == cudaSuccess;
+    ok = ok && cudaEventRecord(ev_in, hs.h2d) == cudaSuccess &&
+         cudaStreamWaitEvent(stream, ev_in, 0) == cudaSuccess;
+    if (!ok) break;
+    // ... its product runs on the caller's stream ...
+    st = run(packed_problem(K > 0 ? dA + r0 * K : nullptr, dB, dC + r0 * N, nr, N, K), stream,
+             cfg);
+    if (st != MT_OK) break;
+    // ... and its rows of C go back while the next block computes.
+    ok = cudaEventRecord(ev_out, stream) == cudaSuccess &&
+         cudaStreamWaitEvent(hs.d2h, ev_out, 0) == cudaSuccess &&
+         cudaMemcpyAsync(C + r0 * N, dC + r0 * N, static_cast<size_t>(nr * N) * 4,
+                         cudaMemcpyDeviceToHost, hs.d2h) == cudaSuccess;
+  }
+  // A and B go back to the pool after the last product (the copies in all
+  // precede it, and a failed loop may have left some in flight: the caller's
+  // stream waits for the copy-in stream first); C after the last copy out.
+  // The caller's stream then waits for the copy-out stream, so the whole
+  // call is complete once it is.
+  bool drained = ev_in_done && cudaEventRecord(ev_in_done, hs.h2d) == cudaSuccess &&
+                 cudaStreamWaitEvent(stream, ev_in_done, 0) == cudaSuccess;
+  if (!drained) cudaStreamSynchronize(hs.h2d);
+  if (dA) cudaFreeAsync(dA, stream);
+  if (dB) cudaFreeAsync(dB, stream);
+  if (dC) {
+    // The copy-out stream frees C once its copies (and, through ev_calloc,
+    // the allocation) are ordered before.
+    if (ev_calloc && cudaEventRecord(ev_calloc, stream) == cudaSuccess &&
+        cudaStreamWaitEvent(hs.d2h, ev_calloc, 0) == cudaSuccess) {
+      cudaFreeAsync(dC, hs.d2h);
+    } else {
+      cudaStreamSynchronize(hs.d2h);
+      cudaFreeAsync(dC, stream);
+    }
+  }
+  drained = ev_done && cudaEventRecord(ev_done, hs.d2h) == cudaSuccess &&
+            cudaStreamWaitEvent(stream, ev_done, 0) == cudaSuccess;
+  if (!drained) cudaStreamSynchronize(hs.d2h);
+  // Events may be destroyed while work still waits on them (their release
+  // is deferred until they complete).
+  for (int i = 0; i < nev; ++i)
+    if (ev[i]) cudaEventDestroy(ev[i]);
+  const bool synced = !sync || cudaStreamSynchronize(stream) == cudaSuccess;
+  if (!ok || !synced) {
+    cudaGetLastError();
+    return st != MT_OK ? st : MT_ERR_CUDA;
+  }
+  return st;
+}
+
 }  // namespace
 
 extern "C" {
@@ -989,88 +1096,12 @@ mt_status mt_sgemm_general_bias(int trans_a, int trans_b, int64_t M, int64_t N, 
 
 mt_status mt_sgemm_host(const float* A, const float* B, float* C, int64_t M, int64_t N,
                         int64_t K, cudaStream_t stream, const mt_config* cfg) {
-  mt_status st0 = check_dims(M, N, K);
-  if (st0 != MT_OK) return st0;
-  if (M == 0 || N == 0) return MT_OK;
-  if (!C || (K > 0 && (!A || !B))) return MT_ERR_INVALID_ARG;
-  int dev = 0;
-  DeviceInfo info;
-  mt_status st = current_device(&dev, &info);
-  if (st != MT_OK) return st;
-  cudaMemPool_t pool = nullptr;
-  st = pool_for(dev, &pool);
-  if (st != MT_OK) return st;
-  HostStreams hs;
-  st = host_streams(dev, &hs);
-  if (st != MT_OK) return st;
-  const size_t a_bytes = static_cast<size_t>(M * K) * 4, b_bytes = static_cast<size_t>(K * N) * 4,
-               c_bytes = static_cast<size_t>(M * N) * 4;
-  float *dA = nullptr, *dB = nullptr, *dC = nullptr;
-  bool ok = true;
-  // 256-byte aligned pool blocks keep the 16-byte staging path available.
-  if (a_bytes) ok = ok && cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dA), a_bytes, pool, stream) == cudaSuccess;
-  if (b_bytes) ok = ok && cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dB), b_bytes, pool, stream) == cudaSuccess;
-  ok = ok && cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dC), c_bytes, pool, stream) == cudaSuccess;
+  return host_pipeline(A, B, C, M, N, K, stream, cfg, true);
+}
 
-  // Row blocks of A and C: block i's copy in, product and copy out run on
-  // the copy-in stream, the caller's stream and the copy-out stream, so the
-  // copies of neighbouring blocks overlap the product of this one.
-  const int64_t rows = host_block_rows(M, N, K);
-  const int64_t blocks = ceil_div(M, rows);
-  cudaEvent_t ev[2 * kMaxHostBlocks + 2] = {};
-  const int nev = static_cast<int>(2 * blocks + 2);
-  for (int i = 0; i < nev && ok; ++i)
-    ok = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
-  cudaEvent_t ev_alloc = ev[0], ev_done = ev[1];
-  // The buffers were allocated on the caller's stream.
-  if (ok) ok = cudaEventRecord(ev_alloc, stream) == cudaSuccess &&
-               cudaStreamWaitEvent(hs.h2d, ev_alloc, 0) == cudaSuccess &&
-               cudaStreamWaitEvent(hs.d2h, ev_alloc, 0) == cudaSuccess;
-  if (ok && b_bytes) ok = cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, hs.h2d) == cudaSuccess;
-  for (int64_t i = 0; i < blocks && ok && st == MT_OK; ++i) {
-    const int64_t r0 = i * rows, nr = std::min(rows, M - r0);
-    cudaEvent_t ev_in = ev[2 + 2 * i], ev_out = ev[3 + 2 * i];
-    // Block i of A (and, before block 0, all of B) is on the device ...
-    if (K > 0)
-      ok = cudaMemcpyAsync(dA + r0 * K, A + r0 * K, static_cast<size_t>(nr * K) * 4,
-                           cudaMemcpyHostToDevice, hs.h2d) == cudaSuccess;
-    ok = ok && cudaEventRecord(ev_in, hs.h2d) == cudaSuccess &&
-         cudaStreamWaitEvent(stream, ev_in, 0) == cudaSuccess;
-    if (!ok) break;
-    // ... its product runs on the caller's stream ...
-    st = run(packed_problem(K > 0 ? dA + r0 * K : nullptr, dB, dC + r0 * N, nr, N, K), stream,
-             cfg);
-    if (st != MT_OK) break;
-    // ... and its rows of C go back while the next block computes.
-    ok = cudaEventRecord(ev_out, stream) == cudaSuccess &&
-         cudaStreamWaitEvent(hs.d2h, ev_out, 0) == cudaSuccess &&
-         cudaMemcpyAsync(C + r0 * N, dC + r0 * N, static_cast<size_t>(nr * N) * 4,
-                         cudaMemcpyDeviceToHost, hs.d2h) == cudaSuccess;
-  }
-  // The caller's stream waits for both copy streams before the buffers go
-  // back to the pool, then the call synchronises it.
-  bool drained = ev_done && cudaEventRecord(ev_done, hs.d2h) == cudaSuccess &&
-                 cudaStreamWaitEvent(stream, ev_done, 0) == cudaSuccess;
-  if (ev_alloc) {
-    drained = drained && cudaEventRecord(ev_alloc, hs.h2d) == cudaSuccess &&
-              cudaStreamWaitEvent(stream, ev_alloc, 0) == cudaSuccess;
-  }
-  if (!drained) {
-    // Without the events, fall back to waiting for the copy streams here.
-    cudaStreamSynchronize(hs.h2d);
-    cudaStreamSynchronize(hs.d2h);
-  }
-  if (dA) cudaFreeAsync(dA, stream);
-  if (dB) cudaFreeAsync(dB, stream);
-  if (dC) cudaFreeAsync(dC, stream);
-  const bool synced = cudaStreamSynchronize(stream) == cudaSuccess;
-  for (int i = 0; i < nev; ++i)
-    if (ev[i]) cudaEventDestroy(ev[i]);
-  if (!ok || !synced) {
-    cudaGetLastError();
-    return st != MT_OK ? st : MT_ERR_CUDA;
-  }
-  return st;
+mt_status mt_sgemm_host_async(const float* A, const float* B, float* C, int64_t M, int64_t N,
+                              int64_t K, cudaStream_t stream, const mt_config* cfg) {
+  return host_pipeline(A, B, C, M, N, K, stream, cfg, false);
 }
 
 mt_status mt_sgemm_tf32x3_noalloc(const float* A, const float* B, float* C, int64_t M,
