@@ -376,143 +376,98 @@ mt_status plan_f16(const Problem& P, const mt_config* cfg, int64_t smem_limit, i
 // check_problem checks them against the sizes.
 // dev: the current device (-1 without one), asked for the resident-cluster
 // count of the CTA-pair kernels.
-mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, int sms,
-                    Launch* L, int dev = -1) {
+// The 3xTF32 plan (called by plan_call after the common checks): A packed or
+// split in the kernel, tile, K depth, CTA pairs, split tail and workspace.
+mt_status plan_tf32x3(const Problem& P, const mt_config* cfg, int64_t smem_limit, int sms,
+                      int dev, Launch* L) {
   const int64_t M = P.M, N = P.N, K = P.K;
-  mt_status st = check_dims(M, N, K);
-  if (st != MT_OK) return st;
-  st = check_lds(P);
-  if (st != MT_OK) return st;
-  const int variant = cfg ? cfg->variant : MT_VARIANT_FFMA;
-  if (cfg && (cfg->bm < 0 || cfg->bn < 0 || cfg->bk < 0 || cfg->stages < 0 ||
-              cfg->no_pad < 0 || cfg->no_pad > 1 || cfg->split_k < 0 || cfg->fma < 0 ||
-              cfg->fma > 2 || cfg->fault_inject < 0 || cfg->fault_inject > 1 || cfg->wm < 0 ||
-              cfg->wn < 0 || cfg->tm < 0 || cfg->tn < 0 || cfg->pack_a < 0 ||
-              cfg->pack_a > 5 || cfg->group_m < 0))
-    return MT_ERR_INVALID_ARG;
-  if (P.dtype)
-    return plan_f16(P, cfg, smem_limit, sms, dev >= 0 ? mt::f16tc_pair_max_clusters(dev) : 0,
-                    L);
-  if (variant == MT_VARIANT_TC16) return MT_ERR_UNSUPPORTED;  // 16-bit inputs only
-  if (cfg && (cfg->wm || cfg->wn || cfg->tm || cfg->tn) && variant != MT_VARIANT_FFMA)
-    return MT_ERR_UNSUPPORTED;
-  if (cfg && cfg->pack_a && variant != MT_VARIANT_TF32X3 && variant != MT_VARIANT_FFMA)
-    return MT_ERR_UNSUPPORTED;
-  if (cfg && cfg->pack_a >= 3 && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
-  if (cfg && cfg->fault_inject && variant != MT_VARIANT_TF32X3) return MT_ERR_UNSUPPORTED;
-  // 3xTF32 splits only its tail by itself (split_k = 1 turns that off).
-  if (cfg && cfg->split_k > 1 && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
-  const bool pad = !(cfg && cfg->no_pad);
-  const bool trans = P.trans_a || P.trans_b;
-  L->fault_inject = cfg ? cfg->fault_inject : 0;
-  if (cfg && cfg->group_m) L->group_m = cfg->group_m;
   mt_plan& p = L->plan;
-  std::memset(&p, 0, sizeof(p));
-  p.variant = variant;
-  p.split_k = 1;
-  // 16-byte staging of both operands and 16-byte stores of C: untransposed
-  // operands whose rows are whole float4s (K, N and every leading dimension
-  // multiples of 4) from 16-byte aligned bases.
-  p.vec_ab = !trans && K % 4 == 0 && N % 4 == 0 && P.lda % 4 == 0 && P.ldb % 4 == 0 &&
-             P.ldc % 4 == 0 && aligned16(P.A) && aligned16(P.B) && aligned16(P.C);
-  p.vec_c = p.vec_ab;
-  L->pad = pad;
+  const int want_bm = cfg ? cfg->bm : 0;
+  // A split inside the GEMM kernel instead of packed (one CTA per tile):
+  // for up to 1024 columns or products up to 2048^3, where packing A costs
+  // more than it saves; A must be readable by TMA as stored.  Measured on
+  // GB300 against packing: 65536 x 128 x 4096 2.3x, 65536 x 256 x 4096
+  // 1.9x, 16384 x 512 x 4096 1.3x, 8192 x 1024 x 4096 1.1x, 2048^3 1.07x;
+  // 4096 x 2048 x 4096 0.97x and 4096^3 0.73x (packing stays there).
+  const bool a_tma_ok = !P.trans_a && P.lda % 4 == 0 && aligned16(P.A);
+  const int want_pack = cfg ? cfg->pack_a : 0;
+  const int split_a =
+      want_pack == 2 ? 1
+      : want_pack == 1 ? 0
+      : (a_tma_ok && want_bm != 256 && (N <= 1024 || M * N * K <= (int64_t(1) << 33))) ? 1
+                                                                                       : 0;
+  if (split_a && (want_bm == 256 || !a_tma_ok)) return MT_ERR_UNSUPPORTED;
+  const int bn = cfg && cfg->bn ? cfg->bn
+                 : want_bm == 256 ? 256 : pick_tf32x3_bn(M, N, sms > 0 ? sms : 1);
+  // CTA pairs (256 x 256 tiles, K depth 16 unless asked) when the pair
+  // tiles fill the resident clusters, as for 16-bit inputs.
+  const int pair_clusters16 = dev >= 0 ? mt::tf32x3_pair_max_clusters(dev, 16) : 0;
+  const int bm = want_bm ? want_bm
+                 : !split_a && auto_pair(M, N, bn, sms, pair_clusters16) ? 256
+                                                                          : mt::tf32x3_bm();
+  const bool pair = bm == 256;
+  // Split-A: K depth 16 for 256-wide tiles (4 stages instead of 2), 32
+  // for narrower ones (fewer, longer stages measured faster).
+  const int bk = cfg && cfg->bk ? cfg->bk
+                 : split_a ? (bn == 256 ? 16 : 32) : pair ? 16 : tf32x3_default_bk(bn);
+  if (!mt::tf32x3_valid(bm, bk, bn, split_a)) return MT_ERR_UNSUPPORTED;
+  const int stages = mt::tf32x3_stages(bm, bk, bn, split_a);
+  if (cfg && ((cfg->stages && cfg->stages != stages) || cfg->fma || cfg->no_pad))
+    return MT_ERR_UNSUPPORTED;
+  p.bm = bm; p.bn = bn; p.bk = bk; p.stages = stages;
+  p.threads = mt::tf32x3_threads(split_a);
+  p.pack_a = split_a ? 2 : 1;
+  L->split_a = split_a;
+  p.pad_a = 0; p.pad_b = 0;  // swizzled tiles: the tensor core's layout, no padding
+  // A packer reads float4 when it walks k-contiguous rows (A as stored,
+  // B stored transposed) that are whole float4s from an aligned base.
+  L->vec_a = !P.trans_a && K % 4 == 0 && P.lda % 4 == 0 && aligned16(P.A);
+  L->vec_b = P.trans_b && K % 4 == 0 && P.ldb % 4 == 0 && aligned16(P.B);
+  p.vec_ab = L->vec_a;
+  p.vec_c = N % 4 == 0 && P.ldc % 4 == 0 && aligned16(P.C);
+  p.smem_bytes = mt::tf32x3_smem_bytes(bm, bk, bn, split_a);
+  L->tiles_m = static_cast<int>(ceil_div(M, bm));
+  L->tiles_n = static_cast<int>(ceil_div(N, bn));
+  // Pack grids: up to 65535 blocks of rows per operand.
+  const int64_t blocks_m = pair ? 2 * L->tiles_m : L->tiles_m;
+  const int64_t blocks_n = pair ? 2 * L->tiles_n : L->tiles_n;
+  if (blocks_m > 65535 || blocks_n > 65535 ||
+      ceil_div(static_cast<int64_t>(L->tiles_n) * bn, 256) > 65535 ||
+      ceil_div(static_cast<int64_t>(L->tiles_m) * bm, 256) > 65535)
+    return MT_ERR_UNSUPPORTED;
+  // Persistent: one CTA per SM, or one cluster of two per two SMs.
+  const int64_t tiles = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
+  if (pair) {
+    const int pc = dev >= 0 ? mt::tf32x3_pair_max_clusters(dev, bk) : 0;
+    L->max_ctas = pc > 0 ? pc : std::max(1, sms / 2);
+  } else {
+    L->max_ctas = sms > 0 ? sms : 1;
+  }
+  // Split tail (split_k = 1 turns it off).
+  const int64_t ctas = std::min<int64_t>(tiles, L->max_ctas);
+  const int64_t ktiles = ceil_div(K, bk);
+  int64_t full = tiles, split = 1;
+  split_tail(tiles, ctas, ktiles, !(cfg && cfg->split_k == 1), &full, &split);
+  L->full_tiles = static_cast<int>(full);
+  L->split = static_cast<int>(split);
+  L->kt_per_slice = static_cast<int>(ceil_div(ktiles, split));
+  p.split_k = L->split;
+  const int64_t units = full + (tiles - full) * split;
+  p.grid = std::min<int64_t>(units, L->max_ctas) * (pair ? 2 : 1);
+  p.workspace_bytes = mt::tf32x3_workspace_bytes(static_cast<int>(M), static_cast<int>(N),
+                                                 static_cast<int>(K), bm, bk, bn, split_a) +
+                      (tiles - full) * split * bm * bn * 4;
+  if (p.smem_bytes > smem_limit) return MT_ERR_SMEM_BUDGET;
+  return MT_OK;
+}
 
-  if (variant == MT_VARIANT_P18) {
-    if (cfg && ((cfg->bm && cfg->bm != 4) || (cfg->bn && cfg->bn != 8) ||
-                (cfg->bk && cfg->bk != 16) || (cfg->stages && cfg->stages != 2) || cfg->fma))
-      return MT_ERR_UNSUPPORTED;
-    p.bm = 4; p.bn = 8; p.bk = 16; p.stages = 2; p.threads = 32;
-    p.pad_a = mt::p18_pad_a(pad);
-    p.pad_b = 0;
-    p.vec_ab = 0; p.vec_c = 0;
-    p.smem_bytes = 0;  // static shared memory only
-    L->tiles_m = static_cast<int>(ceil_div(M, 4));
-    L->tiles_n = static_cast<int>(ceil_div(N, 8));
-    p.grid = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
-    if (p.grid > INT32_MAX) return MT_ERR_UNSUPPORTED;
-    return MT_OK;
-  }
-  if (variant == MT_VARIANT_TF32X3) {
-    const int want_bm = cfg ? cfg->bm : 0;
-    // A split inside the GEMM kernel instead of packed (one CTA per tile):
-    // for up to 1024 columns or products up to 2048^3, where packing A costs
-    // more than it saves; A must be readable by TMA as stored.  Measured on
-    // GB300 against packing: 65536 x 128 x 4096 2.3x, 65536 x 256 x 4096
-    // 1.9x, 16384 x 512 x 4096 1.3x, 8192 x 1024 x 4096 1.1x, 2048^3 1.07x;
-    // 4096 x 2048 x 4096 0.97x and 4096^3 0.73x (packing stays there).
-    const bool a_tma_ok = !P.trans_a && P.lda % 4 == 0 && aligned16(P.A);
-    const int want_pack = cfg ? cfg->pack_a : 0;
-    const int split_a =
-        want_pack == 2 ? 1
-        : want_pack == 1 ? 0
-        : (a_tma_ok && want_bm != 256 && (N <= 1024 || M * N * K <= (int64_t(1) << 33))) ? 1
-                                                                                         : 0;
-    if (split_a && (want_bm == 256 || !a_tma_ok)) return MT_ERR_UNSUPPORTED;
-    const int bn = cfg && cfg->bn ? cfg->bn
-                   : want_bm == 256 ? 256 : pick_tf32x3_bn(M, N, sms > 0 ? sms : 1);
-    // CTA pairs (256 x 256 tiles, K depth 16 unless asked) when the pair
-    // tiles fill the resident clusters, as for 16-bit inputs.
-    const int pair_clusters16 = dev >= 0 ? mt::tf32x3_pair_max_clusters(dev, 16) : 0;
-    const int bm = want_bm ? want_bm
-                   : !split_a && auto_pair(M, N, bn, sms, pair_clusters16) ? 256
-                                                                            : mt::tf32x3_bm();
-    const bool pair = bm == 256;
-    // Split-A: K depth 16 for 256-wide tiles (4 stages instead of 2), 32
-    // for narrower ones (fewer, longer stages measured faster).
-    const int bk = cfg && cfg->bk ? cfg->bk
-                   : split_a ? (bn == 256 ? 16 : 32) : pair ? 16 : tf32x3_default_bk(bn);
-    if (!mt::tf32x3_valid(bm, bk, bn, split_a)) return MT_ERR_UNSUPPORTED;
-    const int stages = mt::tf32x3_stages(bm, bk, bn, split_a);
-    if (cfg && ((cfg->stages && cfg->stages != stages) || cfg->fma || cfg->no_pad))
-      return MT_ERR_UNSUPPORTED;
-    p.bm = bm; p.bn = bn; p.bk = bk; p.stages = stages;
-    p.threads = mt::tf32x3_threads(split_a);
-    p.pack_a = split_a ? 2 : 1;
-    L->split_a = split_a;
-    p.pad_a = 0; p.pad_b = 0;  // swizzled tiles: the tensor core's layout, no padding
-    // A packer reads float4 when it walks k-contiguous rows (A as stored,
-    // B stored transposed) that are whole float4s from an aligned base.
-    L->vec_a = !P.trans_a && K % 4 == 0 && P.lda % 4 == 0 && aligned16(P.A);
-    L->vec_b = P.trans_b && K % 4 == 0 && P.ldb % 4 == 0 && aligned16(P.B);
-    p.vec_ab = L->vec_a;
-    p.vec_c = N % 4 == 0 && P.ldc % 4 == 0 && aligned16(P.C);
-    p.smem_bytes = mt::tf32x3_smem_bytes(bm, bk, bn, split_a);
-    L->tiles_m = static_cast<int>(ceil_div(M, bm));
-    L->tiles_n = static_cast<int>(ceil_div(N, bn));
-    // Pack grids: up to 65535 blocks of rows per operand.
-    const int64_t blocks_m = pair ? 2 * L->tiles_m : L->tiles_m;
-    const int64_t blocks_n = pair ? 2 * L->tiles_n : L->tiles_n;
-    if (blocks_m > 65535 || blocks_n > 65535 ||
-        ceil_div(static_cast<int64_t>(L->tiles_n) * bn, 256) > 65535 ||
-        ceil_div(static_cast<int64_t>(L->tiles_m) * bm, 256) > 65535)
-      return MT_ERR_UNSUPPORTED;
-    // Persistent: one CTA per SM, or one cluster of two per two SMs.
-    const int64_t tiles = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
-    if (pair) {
-      const int pc = dev >= 0 ? mt::tf32x3_pair_max_clusters(dev, bk) : 0;
-      L->max_ctas = pc > 0 ? pc : std::max(1, sms / 2);
-    } else {
-      L->max_ctas = sms > 0 ? sms : 1;
-    }
-    // Split tail (split_k = 1 turns it off).
-    const int64_t ctas = std::min<int64_t>(tiles, L->max_ctas);
-    const int64_t ktiles = ceil_div(K, bk);
-    int64_t full = tiles, split = 1;
-    split_tail(tiles, ctas, ktiles, !(cfg && cfg->split_k == 1), &full, &split);
-    L->full_tiles = static_cast<int>(full);
-    L->split = static_cast<int>(split);
-    L->kt_per_slice = static_cast<int>(ceil_div(ktiles, split));
-    p.split_k = L->split;
-    const int64_t units = full + (tiles - full) * split;
-    p.grid = std::min<int64_t>(units, L->max_ctas) * (pair ? 2 : 1);
-    p.workspace_bytes = mt::tf32x3_workspace_bytes(static_cast<int>(M), static_cast<int>(N),
-                                                   static_cast<int>(K), bm, bk, bn, split_a) +
-                        (tiles - full) * split * bm * bn * 4;
-    if (p.smem_bytes > smem_limit) return MT_ERR_SMEM_BUDGET;
-    return MT_OK;
-  }
-  if (variant != MT_VARIANT_FFMA) return MT_ERR_INVALID_ARG;
+// The FFMA plan (called by plan_call after the common checks): the tile,
+// A's layout and source, operand copies, K slices, workspace and shared
+// memory.
+mt_status plan_ffma(const Problem& P, const mt_config* cfg, int64_t smem_limit, int sms,
+                    bool pad, bool trans, Launch* L) {
+  const int64_t M = P.M, N = P.N, K = P.K;
+  mt_plan& p = L->plan;
 
   int count = 0;
   const mt::FfmaEntry* e = mt::ffma_entries(&count);
@@ -672,6 +627,68 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   // "Shared-memory budget checks include stages and padding").
   if (p.smem_bytes > smem_limit) return MT_ERR_SMEM_BUDGET;
   return MT_OK;
+}
+
+mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, int sms,
+                    Launch* L, int dev = -1) {
+  const int64_t M = P.M, N = P.N, K = P.K;
+  mt_status st = check_dims(M, N, K);
+  if (st != MT_OK) return st;
+  st = check_lds(P);
+  if (st != MT_OK) return st;
+  const int variant = cfg ? cfg->variant : MT_VARIANT_FFMA;
+  if (cfg && (cfg->bm < 0 || cfg->bn < 0 || cfg->bk < 0 || cfg->stages < 0 ||
+              cfg->no_pad < 0 || cfg->no_pad > 1 || cfg->split_k < 0 || cfg->fma < 0 ||
+              cfg->fma > 2 || cfg->fault_inject < 0 || cfg->fault_inject > 1 || cfg->wm < 0 ||
+              cfg->wn < 0 || cfg->tm < 0 || cfg->tn < 0 || cfg->pack_a < 0 ||
+              cfg->pack_a > 5 || cfg->group_m < 0))
+    return MT_ERR_INVALID_ARG;
+  if (P.dtype)
+    return plan_f16(P, cfg, smem_limit, sms, dev >= 0 ? mt::f16tc_pair_max_clusters(dev) : 0,
+                    L);
+  if (variant == MT_VARIANT_TC16) return MT_ERR_UNSUPPORTED;  // 16-bit inputs only
+  if (cfg && (cfg->wm || cfg->wn || cfg->tm || cfg->tn) && variant != MT_VARIANT_FFMA)
+    return MT_ERR_UNSUPPORTED;
+  if (cfg && cfg->pack_a && variant != MT_VARIANT_TF32X3 && variant != MT_VARIANT_FFMA)
+    return MT_ERR_UNSUPPORTED;
+  if (cfg && cfg->pack_a >= 3 && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
+  if (cfg && cfg->fault_inject && variant != MT_VARIANT_TF32X3) return MT_ERR_UNSUPPORTED;
+  // 3xTF32 splits only its tail by itself (split_k = 1 turns that off).
+  if (cfg && cfg->split_k > 1 && variant != MT_VARIANT_FFMA) return MT_ERR_UNSUPPORTED;
+  const bool pad = !(cfg && cfg->no_pad);
+  const bool trans = P.trans_a || P.trans_b;
+  L->fault_inject = cfg ? cfg->fault_inject : 0;
+  if (cfg && cfg->group_m) L->group_m = cfg->group_m;
+  mt_plan& p = L->plan;
+  std::memset(&p, 0, sizeof(p));
+  p.variant = variant;
+  p.split_k = 1;
+  // 16-byte staging of both operands and 16-byte stores of C: untransposed
+  // operands whose rows are whole float4s (K, N and every leading dimension
+  // multiples of 4) from 16-byte aligned bases.
+  p.vec_ab = !trans && K % 4 == 0 && N % 4 == 0 && P.lda % 4 == 0 && P.ldb % 4 == 0 &&
+             P.ldc % 4 == 0 && aligned16(P.A) && aligned16(P.B) && aligned16(P.C);
+  p.vec_c = p.vec_ab;
+  L->pad = pad;
+
+  if (variant == MT_VARIANT_P18) {
+    if (cfg && ((cfg->bm && cfg->bm != 4) || (cfg->bn && cfg->bn != 8) ||
+                (cfg->bk && cfg->bk != 16) || (cfg->stages && cfg->stages != 2) || cfg->fma))
+      return MT_ERR_UNSUPPORTED;
+    p.bm = 4; p.bn = 8; p.bk = 16; p.stages = 2; p.threads = 32;
+    p.pad_a = mt::p18_pad_a(pad);
+    p.pad_b = 0;
+    p.vec_ab = 0; p.vec_c = 0;
+    p.smem_bytes = 0;  // static shared memory only
+    L->tiles_m = static_cast<int>(ceil_div(M, 4));
+    L->tiles_n = static_cast<int>(ceil_div(N, 8));
+    p.grid = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
+    if (p.grid > INT32_MAX) return MT_ERR_UNSUPPORTED;
+    return MT_OK;
+  }
+  if (variant == MT_VARIANT_TF32X3) return plan_tf32x3(P, cfg, smem_limit, sms, dev, L);
+  if (variant != MT_VARIANT_FFMA) return MT_ERR_INVALID_ARG;
+  return plan_ffma(P, cfg, smem_limit, sms, pad, trans, L);
 }
 
 mt_status set_smem_attr(int dev, const Launch& L) {
