@@ -27,6 +27,7 @@ counts the work of all ranks.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -360,16 +361,21 @@ def run_gpu(args):
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
         torch.cuda.synchronize()
-        if clocks:
-            clocks.mark("t0")
-        t0.record(stream)
-        for s_ in range(steps):
-            for i, (w, a, b, c) in enumerate(ops):
-                ev[s_][i][0].record(stream)
-                launch(w, a, b, c)
-                ev[s_][i][1].record(stream)
-        t1.record(stream)
-        torch.cuda.synchronize()
+        gc.collect()
+        gc.disable()  # no collection pass while the launches are enqueued
+        try:
+            if clocks:
+                clocks.mark("t0")
+            t0.record(stream)
+            for s_ in range(steps):
+                for i, (w, a, b, c) in enumerate(ops):
+                    ev[s_][i][0].record(stream)
+                    launch(w, a, b, c)
+                    ev[s_][i][1].record(stream)
+            t1.record(stream)
+            torch.cuda.synchronize()
+        finally:
+            gc.enable()
         if clocks:
             clocks.mark("t1")
         total = max_over_ranks(t0.elapsed_time(t1))
@@ -467,6 +473,86 @@ def run_gpu(args):
                             "kernel's share",
                     "frac_at_run_clock": achieved / ffma_live if ffma_live else None}
 
+    # End to end through the host-buffer entry point (pinned host memory),
+    # right after the device timing and before the variants: after the bf16
+    # variant's power draw, steps of this loop were seen to stall (one step
+    # +27 ms) while the link itself measured normal.
+    e2e = None
+    if main_cfg.get("dtype"):
+        e2e = {"unavailable": "the host-buffer entry point takes fp32 inputs only"}
+    elif not args.no_e2e:
+        cfg = mt.make_config(**main_cfg) if main_cfg else None
+        hbufs = []
+        for (w, _a, _b, _c, A, B) in bufs:
+            hbufs.append((w, A.pin_memory(), B.pin_memory(),
+                          torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()))
+
+        def host_step():
+            # Each GEMM through the asynchronous host-buffer entry point (its
+            # copies in overlap the previous GEMM's products), then one wait
+            # for the step: the results are in the host buffers after it.
+            for (w, hA, hB, hC) in hbufs:
+                st = mt.mt_sgemm_host_async(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), w.M,
+                                            w.N, w.K, sptr, cfg)
+                if st != mt.MT_OK:
+                    raise mt.MtError(st, "mt_sgemm_host_async")
+            stream.synchronize()
+        # Untimed warm-up steps, as for the device timing: the first calls on
+        # freshly pinned host buffers and pool blocks run slower (measured on
+        # GB300: the first two of each shape, up to 2x).
+        for _ in range(max(2, args.warmup)):
+            host_step()
+        # The link this run got: pinned copies of the largest A, each way (the
+        # host side of the link is shared with other jobs on the machine, so
+        # e2e, which is bound by it, moves with it).
+        big = max(hbufs, key=lambda x: x[0].M * x[0].K)
+        dev_buf = torch.empty_like(big[1], device="cuda")
+        link = {}
+        for name, (dst, src) in (("h2d_gbs", (dev_buf, big[1])), ("d2h_gbs", (big[1], dev_buf))):
+            dst.copy_(src, non_blocking=True)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            link[name] = big[1].numel() * 4 / (e0.elapsed_time(e1) / 1e3) / 1e9
+        del dev_buf
+        e2e_steps = max(1, min(args.steps, 10))
+        barrier()
+        step_s = []
+        e2e_clocks = ClockSampler(dev).__enter__()
+        # No garbage collection inside the timed loop (as timeit does): a
+        # collection pass between two asynchronous calls leaves the GPU idle
+        # until the next one is enqueued (seen as single steps ~30 ms long).
+        gc.collect()
+        gc.disable()
+        try:
+            e2e_clocks.mark("t0")
+            t0 = time.perf_counter()
+            for _ in range(e2e_steps):
+                t_step = time.perf_counter()
+                host_step()
+                step_s.append(time.perf_counter() - t_step)
+            e2e_s = max_over_ranks(time.perf_counter() - t0)
+            e2e_clocks.mark("t1")
+        finally:
+            gc.enable()
+        e2e_clocks.__exit__(None, None, None)
+        e2e = {"value": job_tflops(world, flops_step, e2e_steps, e2e_s), "unit": "TFLOP/s",
+               "steps": e2e_steps,
+               "h2d_bytes_per_step": sum(4 * (w.M * w.K + w.K * w.N) for (w, *_r) in hbufs),
+               "d2h_bytes_per_step": sum(4 * w.M * w.N for (w, *_r) in hbufs),
+               "api": "mt_sgemm_host_async per GEMM, one stream synchronisation per step",
+               "link": link,
+               "step_ms": [round(t * 1e3, 3) for t in step_s],
+               # Context for a step that stalled on the shared host: the same
+               # metric over the median step (value stays total work / total time).
+               "value_at_median_step": job_tflops(world, flops_step, 1,
+                                                  statistics.median(step_s)),
+               "clocks": e2e_clocks.summary()}
+
+
     # The other fp32 variant, measured in the same run for comparison.
     variants = {}
     if not args.no_variants:
@@ -525,69 +611,6 @@ def run_gpu(args):
                 "roofline": tc16_roofline(
                     h_dom.flops / (statistics.mean(h_per[h_dom.name]) / 1e3) / 1e12,
                     key_of("tc16", h_plans[h_dom.name], h_dom.name))}
-
-    # End to end through the host-buffer entry point (pinned host memory).
-    e2e = None
-    if main_cfg.get("dtype"):
-        e2e = {"unavailable": "the host-buffer entry point takes fp32 inputs only"}
-    elif not args.no_e2e:
-        cfg = mt.make_config(**main_cfg) if main_cfg else None
-        hbufs = []
-        for (w, _a, _b, _c, A, B) in bufs:
-            hbufs.append((w, A.pin_memory(), B.pin_memory(),
-                          torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()))
-
-        def host_step():
-            # Each GEMM through the asynchronous host-buffer entry point (its
-            # copies in overlap the previous GEMM's products), then one wait
-            # for the step: the results are in the host buffers after it.
-            for (w, hA, hB, hC) in hbufs:
-                st = mt.mt_sgemm_host_async(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), w.M,
-                                            w.N, w.K, sptr, cfg)
-                if st != mt.MT_OK:
-                    raise mt.MtError(st, "mt_sgemm_host_async")
-            stream.synchronize()
-        # Untimed warm-up steps, as for the device timing: the first calls on
-        # freshly pinned host buffers and pool blocks run slower (measured on
-        # GB300: the first two of each shape, up to 2x).
-        for _ in range(max(2, args.warmup)):
-            host_step()
-        # The link this run got: pinned copies of the largest A, each way (the
-        # host side of the link is shared with other jobs on the machine, so
-        # e2e, which is bound by it, moves with it).
-        big = max(hbufs, key=lambda x: x[0].M * x[0].K)
-        dev_buf = torch.empty_like(big[1], device="cuda")
-        link = {}
-        for name, (dst, src) in (("h2d_gbs", (dev_buf, big[1])), ("d2h_gbs", (big[1], dev_buf))):
-            dst.copy_(src, non_blocking=True)
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            dst.copy_(src, non_blocking=True)
-            e1.record(stream)
-            torch.cuda.synchronize()
-            link[name] = big[1].numel() * 4 / (e0.elapsed_time(e1) / 1e3) / 1e9
-        del dev_buf
-        e2e_steps = max(1, min(args.steps, 10))
-        barrier()
-        step_s = []
-        t0 = time.perf_counter()
-        for _ in range(e2e_steps):
-            t_step = time.perf_counter()
-            host_step()
-            step_s.append(time.perf_counter() - t_step)
-        e2e_s = max_over_ranks(time.perf_counter() - t0)
-        e2e = {"value": job_tflops(world, flops_step, e2e_steps, e2e_s), "unit": "TFLOP/s",
-               "steps": e2e_steps,
-               "h2d_bytes_per_step": sum(4 * (w.M * w.K + w.K * w.N) for (w, *_r) in hbufs),
-               "d2h_bytes_per_step": sum(4 * w.M * w.N for (w, *_r) in hbufs),
-               "api": "mt_sgemm_host_async per GEMM, one stream synchronisation per step",
-               "link": link,
-               "step_ms": [round(t * 1e3, 3) for t in step_s],
-               # Context for a step that stalled on the shared host: the same
-               # metric over the median step (value stays total work / total time).
-               "value_at_median_step": job_tflops(world, flops_step, 1,
-                                                  statistics.median(step_s))}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
