@@ -1020,7 +1020,8 @@ mt_status host_pipeline(const float* A, const float* B, float* C, int64_t M, int
   // writes from it.
   if (ok) ok = cudaEventRecord(ev_calloc, stream) == cudaSuccess &&
                cudaStreamWaitEvent(hs.d2h, ev_calloc, 0) == cudaSuccess;
-  if (ok && b_bytes) ok = cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, hs.h2d) == cudaSuccess;
+  if (ok && b_bytes)
+    ok = cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, hs.h2d) == cudaSuccess;
   // Row blocks of A and C: block i's copy in, product and copy out run on
   // the copy-in stream, the caller's stream and the copy-out stream, so the
   // copies of neighbouring blocks overlap the product of this one.

@@ -963,8 +963,8 @@ struct CfgASplit {
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int grid = units < max_ctas ? units : max_ctas;
     tf32x3_asplit_kernel<BK, BN><<<grid, ASPLIT_THREADS, AG::SMEM_BYTES, stream>>>(
-        map_a, Bp, Epilogue{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0, a.bias}, kt, mt, nt,
-        a.group_m, sched, fault_inject);
+        map_a, Bp, Epilogue{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0, a.bias}, kt,
+        mt, nt, a.group_m, sched, fault_inject);
     e = cudaGetLastError();
     if (e != cudaSuccess || a.split <= 1) return e;
     GemmArgs r = a;
