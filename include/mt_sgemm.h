@@ -78,7 +78,10 @@ typedef struct {
     int bm;        /* CTA tile rows (M); 0 = automatic */
     int bn;        /* CTA tile columns (N); 0 = automatic */
     int bk;        /* K depth of one staged tile; 0 = automatic */
-    int stages;    /* shared-memory stages in the K pipeline; 0 = automatic */
+    int stages;    /* shared-memory stages in the K pipeline; 0 = automatic.  1 = one
+                      stage, no double buffering (copy, barrier, compute, barrier):
+                      MT_VARIANT_P18 and the FFMA 128 x 128 x 16 tile, to measure
+                      what the pipeline buys */
     int no_pad;    /* 1 = store rows unpadded (bank-conflict measurements); 0 = padding rule */
     int split_k;   /* K slices reduced in a second pass; 0 = automatic, 1 = none */
     int fma;       /* FFMA micro-kernel: 0 = automatic, 1 = scalar fma.rn.f32,

@@ -231,6 +231,27 @@ def test_p18_plan_follows_the_pages():
         assert R.conflict_degree(addrs, 4) == expect
     st, p = plan(100, 72, 80, variant="p18", no_pad=True)
     assert p.pad_a == 0
+    # The single-stage form the page falls back to (two barriers per tile).
+    st, p = plan(100, 72, 80, variant="p18", stages=1)
+    assert st == mt.MT_OK and p.stages == 1 and p.pad_a == 1
+    assert plan(100, 72, 80, variant="p18", stages=3)[0] == mt.MT_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("stages", [1, 2, 3, 4])
+def test_ffma_pipeline_depth_plans(stages):
+    """The 128 x 128 x 16 tile at every K-pipeline depth: the same tile and
+    padding, shared memory growing with the stage count by the pages'
+    formula (stages * rows * (cols + pad) * 4 for A and for B)."""
+    st, p = plan(4096, 4096, 4096, bm=128, bn=128, bk=16, wm=64, stages=stages)
+    assert st == mt.MT_OK
+    assert (p.bm, p.bn, p.bk, p.stages, p.wm, p.tm, p.tn) == (128, 128, 16, stages, 64, 8, 16)
+    assert p.pack_a == 5 and p.pad_a == 0 and p.pad_b == 0
+    assert p.smem_bytes == (R.SharedBuffer(p.bk, p.bm, p.pad_a, stages).nbytes +
+                            R.SharedBuffer(p.bk, p.bn, p.pad_b, stages).nbytes) == \
+        stages * 16 * 256 * 4
+    reads, writes = ffma_warp_accesses(p)
+    for addrs, width in reads + writes:
+        assert R.conflict_degree(addrs, width) == 1
 
 
 def test_budget_is_checked_before_launch():

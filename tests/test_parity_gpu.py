@@ -32,6 +32,12 @@ FFMA_CONFIGS = [
     dict(bm=128, bn=128, bk=32, stages=3, fma=2, wm=32, wn=64),
     dict(bm=128, bn=128, bk=32, stages=3, fma=2, wm=64, wn=32),
     dict(bm=128, bn=128, bk=16, stages=4, fma=2),
+    # The same tile with shallower K pipelines: one stage (no double
+    # buffering, two barriers per K tile), two and three.
+    dict(bm=128, bn=128, bk=16, stages=1),
+    dict(bm=128, bn=128, bk=16, stages=1, pack_a=4),
+    dict(bm=128, bn=128, bk=16, stages=2),
+    dict(bm=128, bn=128, bk=16, stages=3, pack_a=4),
     dict(bm=256, bn=128, fma=2),
     dict(bm=128, bn=128, bk=32, stages=3, fma=1),
     dict(bm=128, bn=128, bk=32, stages=4, fma=2),
@@ -46,7 +52,8 @@ FFMA_CONFIGS = [
 SLICED_CONFIGS = [dict(bm=64, bn=128, stages=3, pack_a=4), dict(bm=64, bn=128, stages=3, pack_a=5),
                   dict(bm=64, bn=128, stages=3, pack_a=2)]
 ALL_VARIANTS = FFMA_CONFIGS + SLICED_CONFIGS + [dict(variant="p18"),
-                                                dict(variant="p18", no_pad=True)]
+                                                dict(variant="p18", no_pad=True),
+                                                dict(variant="p18", stages=1)]
 
 
 def ids(cfgs):
@@ -170,8 +177,29 @@ def test_all_variants_agree_bitwise():
     # FMAs in increasing k, so every variant must produce the same bits.
     A, B = gemm_inputs.make_ab(200, 136, 300, seed=12, dist="normal")
     ref = run(A, B, variant="p18")
+    assert torch.equal(run(A, B, variant="p18", stages=1), ref)
     for cfg in FFMA_CONFIGS:
         assert torch.equal(run(A, B, split_k=1, **cfg), ref), cfg
+
+
+@pytest.mark.parametrize("stages", [1, 2, 3])
+def test_pipeline_depths_bit_identical_at_4096(stages):
+    """The K pipeline's depth changes when tiles are copied, not what is
+    summed: on the 4096^3 workload (the depth measurements' shape, A from
+    its transposed copy) every depth gives the 4-stage kernel's bits."""
+    A, B = gemm_inputs.make_workload("square_4096")
+    a, b = A.cuda(), B.cuda()
+    tile = dict(bm=128, bn=128, bk=16, wm=64, split_k=1, pack_a=5)
+    p = mt.plan(4096, 4096, 4096, a=a, b=b, stages=stages, **tile)
+    assert (p["stages"], p["pack_a"], p["split_k"]) == (stages, 5, 1)
+    ref = mt.sgemm(a, b, stages=4, **tile)
+    got = mt.sgemm(a, b, stages=stages, **tile)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref)
+    rows = sampled_rows(4096, extra=8)
+    Cr, Wr = oracle.sgemm_rows(A.numpy(), B.numpy(), rows, with_w=True)
+    assert_within(got[torch.from_numpy(rows).cuda()].cpu().numpy(), Cr, Wr, FFMA_TOL,
+                  f"4096^3, {stages} stages")
 
 
 @pytest.mark.parametrize("split", [2, 3, 4])

@@ -673,9 +673,10 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
 
   if (variant == MT_VARIANT_P18) {
     if (cfg && ((cfg->bm && cfg->bm != 4) || (cfg->bn && cfg->bn != 8) ||
-                (cfg->bk && cfg->bk != 16) || (cfg->stages && cfg->stages != 2) || cfg->fma))
+                (cfg->bk && cfg->bk != 16) || (cfg->stages && cfg->stages > 2) || cfg->fma))
       return MT_ERR_UNSUPPORTED;
-    p.bm = 4; p.bn = 8; p.bk = 16; p.stages = 2; p.threads = 32;
+    // Two stages (Version 18's ping-pong) unless one is asked for.
+    p.bm = 4; p.bn = 8; p.bk = 16; p.stages = cfg && cfg->stages == 1 ? 1 : 2; p.threads = 32;
     p.pad_a = mt::p18_pad_a(pad);
     p.pad_b = 0;
     p.vec_ab = 0; p.vec_c = 0;
@@ -867,7 +868,7 @@ mt_status run(const Problem& P, cudaStream_t stream, const mt_config* cfg) {
   if (P.dtype) return run_f16(dev, P, args, L, stream);
   if (L.plan.variant == MT_VARIANT_TF32X3) return run_tf32x3(dev, args, L, stream);
   if (L.plan.variant == MT_VARIANT_P18) {
-    if (mt::launch_p18(args, L.pad, stream) != cudaSuccess) return MT_ERR_LAUNCH;
+    if (mt::launch_p18(args, L.pad, L.plan.stages, stream) != cudaSuccess) return MT_ERR_LAUNCH;
     return MT_OK;
   }
   st = set_smem_attr(dev, L);

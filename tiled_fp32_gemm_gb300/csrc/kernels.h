@@ -86,10 +86,11 @@ cudaError_t launch_splitk_reduce(const GemmArgs& a, int bm, int bn, bool vec_c,
 
 // The one-warp kernel restating the pages' Version 18 (BM=4, BN=8, BK=16,
 // two stages, synchronous staging, padded A).  pad selects the rule's
-// padding (true) or an unpadded A tile (false).
-cudaError_t launch_p18(const GemmArgs& a, bool pad, cudaStream_t stream);
+// padding (true) or an unpadded A tile (false); stages = 1 selects the
+// single-stage form with two barriers per K tile, else 2.
+cudaError_t launch_p18(const GemmArgs& a, bool pad, int stages, cudaStream_t stream);
 int p18_pad_a(bool pad);
-int p18_smem_bytes(bool pad);
+int p18_smem_bytes(bool pad, int stages);
 
 // tcgen05 3xTF32 variant (sgemm_tf32x3.cu): persistent kernel over tiles of
 // 128 x bn (bm = 128; bn = 256, 128 or 64) or, on CTA pairs, of 256 x 256

@@ -157,6 +157,7 @@ int ffma_entries_128(FfmaEntry* out);
 int ffma_entries_alt(FfmaEntry* out);
 int ffma_entries_k16(FfmaEntry* out);
 int ffma_entries_64(FfmaEntry* out);
+int ffma_entries_depth(FfmaEntry* out);
 
 const FfmaEntry* ffma_entries(int* count) {
   // Each tile unit fills at most kUnitMax entries into a scratch block;
@@ -165,7 +166,7 @@ const FfmaEntry* ffma_entries(int* count) {
   static FfmaEntry entries[kCapacity];
   static const int n = [] {
     int (*const units[])(FfmaEntry*) = {ffma_entries_128, ffma_entries_alt, ffma_entries_64,
-                                        ffma_entries_k16};
+                                        ffma_entries_k16, ffma_entries_depth};
     int k = 0;
     for (auto unit : units) {
       FfmaEntry scratch[kUnitMax] = {};

@@ -29,7 +29,10 @@
 //  * K pipeline — STAGES shared stages filled by cp.async with zero fill,
 //    one barrier per K tile (Part 18 "What ping-pong changes about
 //    synchronization"; skills page step 7: commit, wait_group, then
-//    __syncthreads), with STAGES-1 tiles in flight while one is computed;
+//    __syncthreads), with STAGES-1 tiles in flight while one is computed.
+//    STAGES = 1 is the single-buffer form the pages fall back to (Part 18
+//    "One stage versus two stages": copy, barrier, compute, barrier), kept
+//    to measure what the pipeline buys;
 //  * unrolled register-tile micro-kernel — each thread keeps a TM x TN block
 //    of C in registers and, for every k of the fixed-size BK loop (fully
 //    unrolled, Part 18 "Unrolling the inner reduction loop"), reads its A
@@ -505,16 +508,28 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
   int stage = 0;
   int load_stage = T::STAGES - 1;
   for (int kt = 0; kt < ktiles; ++kt) {
-    // Tile kt has landed for this thread; the barrier makes every thread's
-    // copies visible and guarantees that the stage refilled below (read in
-    // iteration kt-1) is no longer being read.
-    cp_async_wait<T::STAGES - 2>();
-    __syncthreads();
-    if (kt + T::STAGES - 1 < ktiles) {
-      stage_a.load(As, LA, load_stage, kt_begin + kt + T::STAGES - 1);
-      stage_b.load(Bs, LB, load_stage, kt_begin + kt + T::STAGES - 1);
+    if constexpr (T::STAGES == 1) {
+      // One stage, no double buffering (the pages' fallback form): copy
+      // tile kt, wait for it, barrier, compute, and a second barrier below
+      // before the next copy overwrites the stage.  Nothing overlaps the
+      // copies.
+      stage_a.load(As, LA, 0, kt_begin + kt);
+      stage_b.load(Bs, LB, 0, kt_begin + kt);
+      cp_async_commit();
+      cp_async_wait<0>();
+      __syncthreads();
+    } else {
+      // Tile kt has landed for this thread; the barrier makes every
+      // thread's copies visible and guarantees that the stage refilled
+      // below (read in iteration kt-1) is no longer being read.
+      cp_async_wait<T::STAGES - 2>();
+      __syncthreads();
+      if (kt + T::STAGES - 1 < ktiles) {
+        stage_a.load(As, LA, load_stage, kt_begin + kt + T::STAGES - 1);
+        stage_b.load(Bs, LB, load_stage, kt_begin + kt + T::STAGES - 1);
+      }
+      cp_async_commit();
     }
-    cp_async_commit();
 
     const float* a_ptr = As + stage * LA.stage_size() + a_off;
     const float* b_ptr = Bs + stage * LB.stage_size() + b_off;
@@ -561,6 +576,7 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
         }
       }
     }
+    if constexpr (T::STAGES == 1) __syncthreads();  // every read of the stage is done
     stage = stage + 1 == T::STAGES ? 0 : stage + 1;
     load_stage = load_stage + 1 == T::STAGES ? 0 : load_stage + 1;
   }

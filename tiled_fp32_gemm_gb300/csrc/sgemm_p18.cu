@@ -15,6 +15,11 @@
 //     "Unrolling the inner reduction loop"); the trailing barrier is not
 //     needed because the next tile goes to the other stage (section "What
 //     ping-pong changes about synchronization").
+// STAGES = 1 is the form the page falls back to when its double-buffer
+// matcher declines (section "Why a conservative matcher matters"): every K
+// tile overwrites the same storage, so a second barrier after the dot loop
+// protects it from the next tile's copies.  Both forms run the same FMA
+// chain, so their results are bit-identical.
 // A rows are read by four output rows at once at the same k, so the A tile
 // gets the rule's padding (16 columns, 4 rows -> one word, stride 17); B is
 // read as a broadcast and is not padded (section "Why shared-memory banks
@@ -31,11 +36,11 @@ namespace mt {
 namespace {
 constexpr int P18_BM = 4, P18_BN = 8, P18_BK = 16, P18_THREADS = 32;
 
-constexpr SmemLayout p18_a_layout(bool pad) {
+constexpr SmemLayout p18_a_layout(bool pad, int stages) {
   // The four output rows of a tile read A at the same k at once.
-  return SmemLayout{P18_BM, P18_BK, pad ? row_padding_rule(P18_BK, P18_BM) : 0, 2};
+  return SmemLayout{P18_BM, P18_BK, pad ? row_padding_rule(P18_BK, P18_BM) : 0, stages};
 }
-constexpr SmemLayout p18_b_layout() { return SmemLayout{P18_BK, P18_BN, 0, 2}; }
+constexpr SmemLayout p18_b_layout(int stages) { return SmemLayout{P18_BK, P18_BN, 0, stages}; }
 }  // namespace
 
 // op(A)[i][k] or op(B)[k][j] from its storage, 0.0 outside rows x cols.
@@ -45,11 +50,12 @@ __device__ __forceinline__ float fetch_operand(const float* base, int64_t ld, in
   return base[trans ? static_cast<int64_t>(j) * ld + i : static_cast<int64_t>(i) * ld + j];
 }
 
-template <bool PAD>
+template <bool PAD, int STAGES>
 __global__ void __launch_bounds__(P18_THREADS) sgemm_p18_kernel(GemmArgs args) {
-  constexpr SmemLayout LA = p18_a_layout(PAD);
-  constexpr SmemLayout LB = p18_b_layout();
-  // Both staged operands, double-buffered: A's stages, then B's.
+  static_assert(STAGES == 1 || STAGES == 2, "one stage or a ping-pong pair");
+  constexpr SmemLayout LA = p18_a_layout(PAD, STAGES);
+  constexpr SmemLayout LB = p18_b_layout(STAGES);
+  // Both staged operands: A's stages, then B's.
   __shared__ float staged[LA.size() + LB.size()];
   float* a_tiles = staged;
   float* b_tiles = staged + LA.size();
@@ -67,7 +73,7 @@ __global__ void __launch_bounds__(P18_THREADS) sgemm_p18_kernel(GemmArgs args) {
   const int k_tiles = (args.K + P18_BK - 1) / P18_BK;
   float acc = 0.0f;
   for (int kt = 0; kt < k_tiles; ++kt) {
-    const int buf = kt & 1;  // stage of this K tile: tiles alternate
+    const int buf = STAGES == 2 ? kt & 1 : 0;  // stage of this K tile: tiles alternate
     const int k0 = kt * P18_BK;
 #pragma unroll
     for (int e = 0; e < A_PER_LANE; ++e) {
@@ -92,6 +98,7 @@ __global__ void __launch_bounds__(P18_THREADS) sgemm_p18_kernel(GemmArgs args) {
 #pragma unroll
     for (int kk = 0; kk < P18_BK; ++kk)
       acc = fmaf(av[LA.offset(buf, r, kk)], bv[LB.offset(buf, kk, c)], acc);
+    if (STAGES == 1) __syncthreads();  // the next tile's copies overwrite this stage
   }
   const int row = m0 + r, col = n0 + c;
   if (row < args.M && col < args.N) {
@@ -103,16 +110,25 @@ __global__ void __launch_bounds__(P18_THREADS) sgemm_p18_kernel(GemmArgs args) {
   }
 }
 
-cudaError_t launch_p18(const GemmArgs& a, bool pad, cudaStream_t stream) {
-  const int64_t grid = static_cast<int64_t>(a.tiles_m) * a.tiles_n;
-  if (pad)
-    sgemm_p18_kernel<true><<<static_cast<unsigned>(grid), P18_THREADS, 0, stream>>>(a);
-  else
-    sgemm_p18_kernel<false><<<static_cast<unsigned>(grid), P18_THREADS, 0, stream>>>(a);
+cudaError_t launch_p18(const GemmArgs& a, bool pad, int stages, cudaStream_t stream) {
+  const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(a.tiles_m) * a.tiles_n);
+  if (stages == 1) {
+    if (pad)
+      sgemm_p18_kernel<true, 1><<<grid, P18_THREADS, 0, stream>>>(a);
+    else
+      sgemm_p18_kernel<false, 1><<<grid, P18_THREADS, 0, stream>>>(a);
+  } else {
+    if (pad)
+      sgemm_p18_kernel<true, 2><<<grid, P18_THREADS, 0, stream>>>(a);
+    else
+      sgemm_p18_kernel<false, 2><<<grid, P18_THREADS, 0, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 
-int p18_pad_a(bool pad) { return p18_a_layout(pad).row_padding; }
-int p18_smem_bytes(bool pad) { return p18_a_layout(pad).nbytes() + p18_b_layout().nbytes(); }
+int p18_pad_a(bool pad) { return p18_a_layout(pad, 2).row_padding; }
+int p18_smem_bytes(bool pad, int stages) {
+  return p18_a_layout(pad, stages).nbytes() + p18_b_layout(stages).nbytes();
+}
 
 }  // namespace mt
