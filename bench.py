@@ -518,7 +518,10 @@ def run_gpu(args):
             torch.cuda.synchronize()
             link[name] = big[1].numel() * 4 / (e0.elapsed_time(e1) / 1e3) / 1e9
         del dev_buf
-        e2e_steps = max(1, min(args.steps, 10))
+        # The same K steps as the device timing (at most 100, about 2 s): the
+        # box's host-copy path pauses for 30-55 ms about every 0.5 s, so a loop
+        # much shorter than that meets a pause or not by chance.
+        e2e_steps = max(1, min(args.steps, 100))
         barrier()
         step_s = []
         e2e_clocks = ClockSampler(dev).__enter__()

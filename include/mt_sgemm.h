@@ -111,7 +111,7 @@ typedef struct {
                       B is copied into padded rows when the 16-byte staging cannot
                       read it.  Automatic (0): K-major A when padding is on and B
                       is 16-byte readable or M >= 512, from a copy when A is stored
-                      K x M or N >= 2048 with 2^30 multiply-adds or more, else
+                      K x M or N >= 1024 with 2^30 multiply-adds or more, else
                       gathered.  Every choice gives the same bits. */
     int group_m;   /* tile rows per group of the tile raster (tiles are walked
                       down a group's rows, then across); 0 = automatic */

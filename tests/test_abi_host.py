@@ -195,6 +195,8 @@ def test_ffma_kmajor_gather_unpadded_would_conflict():
     ((4096, 4096, 4096), True, 3),    # A stored K x M: read as stored
     ((4097, 3001, 2053), True, 5),    # A stored K x M, M % 4 != 0: copy
     ((100, 72, 80), False, 4),
+    ((1024, 1024, 1024), False, 5),   # N = 1024, 2^30 multiply-adds: copy
+    ((1024, 1023, 1024), False, 4),   # just under: gathered
     ((32768, 4096, 32768), False, 4),  # A^T would need 4 GiB: gathered instead
     ((32768, 4096, 32768), True, 3),   # A stored K x M, readable: as stored
 ])

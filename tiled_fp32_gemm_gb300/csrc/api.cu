@@ -497,11 +497,14 @@ mt_status plan_ffma(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
     // The K-major A tile comes straight from A stored K x M when its rows
     // are whole float4s; otherwise from a K x M copy (pack_a = 5, or
     // automatically for A stored K x M, and for A stored M x K when N >=
-    // 2048 and the product has 2^30 multiply-adds or more: the transposing
+    // 1024 and the product has 2^30 multiply-adds or more: the transposing
     // pass costs about 70 / N of the product), else gathered element by
     // element from A stored M x K inside the GEMM kernel (pack_a = 4, about
-    // 9 % slower than a K-major source on 4096^3).  B as the 16-byte staging
-    // reads it, copied first when it cannot be read as stored.
+    // 9 % slower than a K-major source on 4096^3).  Measured on GB300 at
+    // 1024^3 (64 x 128 tiles): 52.7 us from the copy against 55.2 gathered;
+    // at N = 128 (65536 x 128 x 4096) the copy loses, 40 against 61 TFLOP/s.
+    // B as the 16-byte staging reads it, copied first when it cannot be read
+    // as stored.
     const bool direct = P.trans_a && M % 4 == 0 && P.lda % 4 == 0 && aligned16(P.A);
     if (want_pack == 4 && P.trans_a) return MT_ERR_UNSUPPORTED;
     // For A stored M x K the automatic copy is capped at 2 GiB of workspace
@@ -512,7 +515,7 @@ mt_status plan_ffma(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
     const bool copy = want_pack == 5 ||
                       (want_pack != 4 && !direct &&
                        (P.trans_a ||
-                        (copy_bytes <= (int64_t(2) << 30) && N >= 2048 &&
+                        (copy_bytes <= (int64_t(2) << 30) && N >= 1024 &&
                          static_cast<double>(M) * N * K >= 1073741824.0)));
     L->a_kmajor = true;
     L->prep_a_kmajor = copy;
