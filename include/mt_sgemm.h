@@ -396,6 +396,42 @@ MT_API int64_t mt_smem_layout_offset(const mt_smem_layout *layout, int stage, in
  */
 MT_API mt_status mt_device_status(cudaStream_t stream);
 
+/*
+ * The bounds-checked build.  libmtsgemm_checked.so is these sources built
+ * with MT_BOUNDS_CHECK=1: the kernels of the FFMA path (the FFMA GEMM, its
+ * operand copies, the K-slice reduce and C scaling, the one-warp kernel)
+ * test every global and shared access against the extent of its buffer
+ * before making it.  An access outside is skipped (a copy zero-fills, a
+ * read gives 0, a store is dropped), so a checked kernel never touches
+ * memory outside its buffers, and it is counted.  This stands in for a
+ * memory checker where none can run; it is for tests and is slower than the
+ * normal build.  Sites of the first access found outside:
+ */
+typedef enum {
+    MT_SITE_A_LOAD = 1,     /* global read of A by the staging copies */
+    MT_SITE_B_LOAD = 2,     /* global read of B by the staging copies */
+    MT_SITE_A_SMEM = 3,     /* shared write of a staged A tile */
+    MT_SITE_B_SMEM = 4,     /* shared write of a staged B tile */
+    MT_SITE_FRAG = 5,       /* shared read of an A or B fragment */
+    MT_SITE_C_STORE = 6,    /* global read or write of C */
+    MT_SITE_PARTIAL = 7,    /* global read or write of a K-slice partial tile */
+    MT_SITE_BIAS = 8,       /* global read of the bias row */
+    MT_SITE_SLICE_SUM = 9,  /* shared read or write of a K group's sum */
+    MT_SITE_PREP_SRC = 10,  /* global read of an operand by the copy kernel */
+    MT_SITE_PREP_DST = 11,  /* global write of an operand copy */
+    MT_SITE_P18 = 12        /* any access of the one-warp kernel */
+} mt_bounds_site;
+
+/*
+ * Checked build: synchronises the current device, then reads and clears its
+ * record of accesses found outside their buffers: *count of them, and the
+ * first one's *site (mt_bounds_site), element *offset within its buffer and
+ * the buffer's *extent in elements (any pointer may be NULL).  Errors:
+ * MT_ERR_NO_DEVICE, MT_ERR_CUDA.  The normal build checks nothing and
+ * returns MT_ERR_UNSUPPORTED without touching the outputs.
+ */
+MT_API mt_status mt_bounds_status(int64_t *count, int *site, int64_t *offset, int64_t *extent);
+
 /* Static English name of a status code. */
 MT_API const char *mt_status_string(mt_status status);
 

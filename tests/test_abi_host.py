@@ -57,6 +57,22 @@ def test_every_declared_function_is_exported_and_bound():
     assert mt.mt_status_string(mt.MT_ERR_SMEM_BUDGET) == "shared-memory budget exceeded"
 
 
+def test_checked_build_exports_the_same_entry_points_and_says_so():
+    """The bounds-checked variant has the whole C ABI; its mt_bounds_status
+    answers (no device here: MT_ERR_NO_DEVICE), while the normal build
+    reports that it checks nothing."""
+    assert mt_build.build(checked=True) == mt.CHECKED_LIB_PATH
+    handle = mt.checked_lib()
+    for n in sorted(declared_functions()):
+        assert hasattr(handle, n), f"{n} not exported by the checked build"
+    out = ctypes.c_int64(-7)
+    site = ctypes.c_int(-7)
+    st = mt.lib().mt_bounds_status(ctypes.byref(out), ctypes.byref(site), None, None)
+    assert st == mt.MT_ERR_UNSUPPORTED and out.value == -7 and site.value == -7
+    st = handle.mt_bounds_status(ctypes.byref(out), ctypes.byref(site), None, None)
+    assert st == (mt.MT_OK if HAS_GPU else mt.MT_ERR_NO_DEVICE)
+
+
 def test_padding_rule_matches_pages_and_oracle():
     for c in (1, 2, 3, 4, 5, 7, 8, 12, 16, 17, 24, 31, 32, 33, 48, 64, 96, 128):
         for r in range(1, 33):

@@ -11,6 +11,7 @@ by ``tiled_fp32_gemm_gb300.build``).  This module only marshals arguments:
   ``mt_gemm_mixed_plan``,
   ``mt_smem_row_padding``, ``mt_smem_vector_row_padding``,
   ``mt_smem_layout_make``, ``mt_smem_layout_offset``, ``mt_device_status``,
+  ``mt_bounds_status``,
   ``mt_status_string``, ``mt_version`` — the C entry points under the same
   names, taking plain integers for pointers and streams;
 * ``sgemm(a, b, out=None, **choices)`` — the same call on torch CUDA tensors
@@ -48,7 +49,14 @@ VARIANTS = {"ffma": MT_VARIANT_FFMA, "tf32x3": MT_VARIANT_TF32X3, "p18": MT_VARI
 MT_DTYPE_F16 = 1
 MT_DTYPE_BF16 = 2
 
+# mt_bounds_site: where the checked build found an access outside its buffer.
+MT_SITE_A_LOAD, MT_SITE_B_LOAD, MT_SITE_A_SMEM, MT_SITE_B_SMEM = 1, 2, 3, 4
+MT_SITE_FRAG, MT_SITE_C_STORE, MT_SITE_PARTIAL, MT_SITE_BIAS = 5, 6, 7, 8
+MT_SITE_SLICE_SUM, MT_SITE_PREP_SRC, MT_SITE_PREP_DST, MT_SITE_P18 = 9, 10, 11, 12
+
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libmtsgemm.so")
+CHECKED_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "checked",
+                                "libmtsgemm_checked.so")
 
 
 class mt_config(ctypes.Structure):
@@ -119,12 +127,28 @@ SIGNATURES = {
     "mt_smem_layout_make": (_I, [_I, _I, _I, _I, ctypes.POINTER(mt_smem_layout)]),
     "mt_smem_layout_offset": (_I64, [ctypes.POINTER(mt_smem_layout), _I, _I, _I]),
     "mt_device_status": (_I, [_P]),
+    "mt_bounds_status": (_I, [ctypes.POINTER(_I64), ctypes.POINTER(_I), ctypes.POINTER(_I64),
+                              ctypes.POINTER(_I64)]),
     "mt_status_string": (ctypes.c_char_p, [_I]),
     "mt_version": (_I, []),
 }
 
 _lock = threading.Lock()
 _lib = None
+_checked = None
+
+
+def _load(path: str, how: str):
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           f"`python -m tiled_fp32_gemm_gb300.build{how}` (there is no CPU "
+                           "fallback)")
+    handle = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
 
 
 def lib():
@@ -133,17 +157,34 @@ def lib():
     if _lib is None:
         with _lock:
             if _lib is None:
-                if not os.path.exists(LIB_PATH):
-                    raise RuntimeError(
-                        f"{LIB_PATH} is missing: build it with "
-                        "`python -m tiled_fp32_gemm_gb300.build` (there is no CPU fallback)")
-                handle = ctypes.CDLL(LIB_PATH)
-                for name, (res, args) in SIGNATURES.items():
-                    fn = getattr(handle, name)
-                    fn.restype = res
-                    fn.argtypes = args
-                _lib = handle
+                _lib = _load(LIB_PATH, "")
     return _lib
+
+
+def checked_lib():
+    """The bounds-checked build (libmtsgemm_checked.so, same entry points):
+    its FFMA-path kernels skip and count any access outside their buffers;
+    read the count with ``bounds_status(checked_lib())``."""
+    global _checked
+    if _checked is None:
+        with _lock:
+            if _checked is None:
+                _checked = _load(CHECKED_LIB_PATH, " --checked")
+    return _checked
+
+
+def bounds_status(handle=None) -> dict:
+    """mt_bounds_status of `handle` (default: the checked build) as a dict;
+    raises MtError if the call fails (MT_ERR_UNSUPPORTED: a normal build)."""
+    h = handle if handle is not None else checked_lib()
+    count, site, offset, extent = ctypes.c_int64(), ctypes.c_int(), ctypes.c_int64(), \
+        ctypes.c_int64()
+    st = h.mt_bounds_status(ctypes.byref(count), ctypes.byref(site), ctypes.byref(offset),
+                            ctypes.byref(extent))
+    if st != MT_OK:
+        raise MtError(st, "mt_bounds_status")
+    return {"count": count.value, "site": site.value, "offset": offset.value,
+            "extent": extent.value}
 
 
 def make_config(variant="ffma", bm=0, bn=0, bk=0, stages=0, no_pad=False, split_k=0,

@@ -5,7 +5,13 @@ one nvcc call links the shared library.  Objects and the library go to
 ``tiled_fp32_gemm_gb300/_build/``; a source newer than its object (or any
 header newer than it) triggers a rebuild.
 
-    python -m tiled_fp32_gemm_gb300.build [--force] [--verbose]
+``checked=True`` builds the same sources with ``-DMT_BOUNDS_CHECK=1`` into
+``_build/checked/libmtsgemm_checked.so``: the FFMA path's kernels (the FFMA
+GEMM, its operand copies and K-slice reduce, the one-warp kernel) test every
+global and shared access against its buffer, skip any that falls outside and
+count it (``mt_bounds_status``).  For tests; slower than the normal build.
+
+    python -m tiled_fp32_gemm_gb300.build [--force] [--verbose] [--checked]
 """
 from __future__ import annotations
 
@@ -23,6 +29,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmtsgemm.so")
+CHECKED_BUILD = os.path.join(BUILD, "checked")
+CHECKED_LIB = os.path.join(CHECKED_BUILD, "libmtsgemm_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
@@ -49,8 +57,8 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src: str, obj: str, verbose: bool) -> str:
-    cmd = [nvcc(), *NVCC_FLAGS, "-c", src, "-o", obj]
+def _compile(src: str, obj: str, verbose: bool, defines=()) -> str:
+    cmd = [nvcc(), *NVCC_FLAGS, *defines, "-c", src, "-o", obj]
     if verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -59,37 +67,41 @@ def _compile(src: str, obj: str, verbose: bool) -> str:
     return r.stderr if verbose else ""
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link the library if anything changed; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Compile and link the library if anything changed; returns its path.
+    checked=True: the bounds-checked build instead (see the module doc)."""
+    out_dir, lib = (CHECKED_BUILD, CHECKED_LIB) if checked else (BUILD, LIB)
+    defines = ["-DMT_BOUNDS_CHECK=1"] if checked else []
+    os.makedirs(out_dir, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = _headers()
     jobs = []
     objects = []
     for src in sources:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         objects.append(obj)
         if force or _stale(obj, [src, *headers]):
             jobs.append((src, obj))
     if jobs:
         with ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
-            logs = list(ex.map(lambda j: _compile(j[0], j[1], verbose), jobs))
+            logs = list(ex.map(lambda j: _compile(j[0], j[1], verbose, defines), jobs))
         if verbose:
             for (src, _), log in zip(jobs, logs):
                 print(f"== {os.path.basename(src)}\n{log}", file=sys.stderr)
-    if force or jobs or _stale(LIB, objects):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib, objects):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objects, "-cudart", "static"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true", help="print -Xptxas -v")
+    ap.add_argument("--checked", action="store_true", help="the bounds-checked build")
     a = ap.parse_args()
-    print(build(force=a.force, verbose=a.verbose))
+    print(build(force=a.force, verbose=a.verbose, checked=a.checked))

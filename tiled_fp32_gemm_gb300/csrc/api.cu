@@ -4,12 +4,14 @@
 #include <atomic>
 #include <climits>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <unordered_set>
 
 #include <cuda_runtime.h>
 
+#include "device_util.cuh"
 #include "kernels.h"
 #include "mt_sgemm.h"
 #include "smem_layout.cuh"
@@ -303,6 +305,37 @@ void split_tail(int64_t tiles, int64_t ctas, int64_t ktiles, bool allowed, int64
 }
 
 mt::GemmArgs make_args(const Problem& P, const Launch& L);
+
+#if MT_BOUNDS_CHECK
+// The checked build's record of out-of-range accesses; kernels get its
+// device address through GemmArgs::bounds (looked up once per device).
+__device__ mt::BoundsRecord g_bounds;
+mt::BoundsRecord* g_bounds_ptr[kMaxDevices];
+#endif
+
+// The record the current device's kernels write to: nullptr in normal
+// builds (and if the lookup fails).
+mt::BoundsRecord* bounds_record() {
+#if MT_BOUNDS_CHECK
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_bounds_ptr[d]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bounds) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_bounds_ptr[d] = static_cast<mt::BoundsRecord*>(p);
+  }
+  return g_bounds_ptr[d];
+#else
+  return nullptr;
+#endif
+}
 
 // The automatic 16-bit plan takes CTA pairs (256 x 256 tiles) when 256-wide
 // tiles are chosen and there are at least as many pair tiles as resident
@@ -779,6 +812,17 @@ mt::GemmArgs make_args(const Problem& P, const Launch& L) {
   a.split = L.split;
   a.kt_per_slice = L.kt_per_slice;
   a.partial = nullptr;
+  a.a_extent = P.trans_a ? mt::view_extent(P.K, P.M, P.lda) : mt::view_extent(P.M, P.K, P.lda);
+  a.b_extent = P.trans_b ? mt::view_extent(P.N, P.K, P.ldb) : mt::view_extent(P.K, P.N, P.ldb);
+  a.c_extent = mt::view_extent(P.M, P.N, P.ldc);
+  a.partial_extent = 0;
+  a.bounds = bounds_record();
+#if MT_BOUNDS_CHECK
+  // Test hook of the checked build only: C is declared one element shorter
+  // than it is, so the store of its last element counts as outside and is
+  // skipped (no access leaves the real buffer).
+  if (std::getenv("MT_CHECKED_SHRINK_C_EXTENT")) a.c_extent -= 1;
+#endif
   return a;
 }
 
@@ -861,7 +905,7 @@ mt_status run(const Problem& P, cudaStream_t stream, const mt_config* cfg) {
     // No product to form (K == 0: the accumulator's zeros; alpha == 0):
     // C = beta * C (+ bias), A and B untouched.
     if (mt::launch_scale_c(P.C, static_cast<int>(P.M), static_cast<int>(P.N), P.ldc, P.beta,
-                           P.bias, stream) != cudaSuccess) {
+                           P.bias, stream, bounds_record()) != cudaSuccess) {
       cudaGetLastError();
       return MT_ERR_LAUNCH;
     }
@@ -888,16 +932,20 @@ mt_status run(const Problem& P, cudaStream_t stream, const mt_config* cfg) {
       return MT_ERR_CUDA;
     }
     char* base = static_cast<char*>(ws);
-    if (L.split > 1) args.partial = reinterpret_cast<float*>(base + L.partial_offset);
+    if (L.split > 1) {
+      args.partial = reinterpret_cast<float*>(base + L.partial_offset);
+      args.partial_extent = (L.plan.workspace_bytes - L.partial_offset) / 4;
+    }
     // Operands copied into the layout the 16-byte staging reads.
     if (L.prep_a) {
       float* a = reinterpret_cast<float*>(base);
       ok = mt::launch_prep_operand(static_cast<const float*>(P.A), P.lda, P.trans_a != 0, a,
                                    L.ldo_a, static_cast<int>(P.M), static_cast<int>(P.K),
-                                   stream) == cudaSuccess;
+                                   stream, args.bounds) == cudaSuccess;
       args.A = a;
       args.lda = L.ldo_a;
       args.trans_a = 0;
+      args.a_extent = P.M * L.ldo_a;
     }
     if (L.prep_a_kmajor) {
       // A^T (K x M) into scratch: a transposing copy of A stored M x K, a
@@ -905,19 +953,21 @@ mt_status run(const Problem& P, cudaStream_t stream, const mt_config* cfg) {
       float* a = reinterpret_cast<float*>(base);
       ok = mt::launch_prep_operand(static_cast<const float*>(P.A), P.lda, P.trans_a == 0, a,
                                    L.ldo_a, static_cast<int>(P.K), static_cast<int>(P.M),
-                                   stream) == cudaSuccess;
+                                   stream, args.bounds) == cudaSuccess;
       args.A = a;
       args.lda = L.ldo_a;
       args.trans_a = 1;
+      args.a_extent = P.K * L.ldo_a;
     }
     if (ok && L.prep_b) {
       float* b = reinterpret_cast<float*>(base + L.prep_b_offset);
       ok = mt::launch_prep_operand(static_cast<const float*>(P.B), P.ldb, P.trans_b != 0, b,
                                    L.ldo_b, static_cast<int>(P.K), static_cast<int>(P.N),
-                                   stream) == cudaSuccess;
+                                   stream, args.bounds) == cudaSuccess;
       args.B = b;
       args.ldb = L.ldo_b;
       args.trans_b = 0;
+      args.b_extent = P.K * L.ldo_b;
     }
   }
   void* params[] = {&args};
@@ -1299,6 +1349,44 @@ int64_t mt_smem_layout_offset(const mt_smem_layout* layout, int stage, int row, 
   const mt::SmemLayout L{layout->rows, layout->columns, layout->row_padding,
                          layout->stage_count};
   return L.offset(stage, row, column);
+}
+
+static_assert(MT_SITE_A_LOAD == mt::SITE_A_LOAD && MT_SITE_B_LOAD == mt::SITE_B_LOAD &&
+                  MT_SITE_A_SMEM == mt::SITE_A_SMEM && MT_SITE_B_SMEM == mt::SITE_B_SMEM &&
+                  MT_SITE_FRAG == mt::SITE_FRAG && MT_SITE_C_STORE == mt::SITE_C_STORE &&
+                  MT_SITE_PARTIAL == mt::SITE_PARTIAL && MT_SITE_BIAS == mt::SITE_BIAS &&
+                  MT_SITE_SLICE_SUM == mt::SITE_SLICE_SUM &&
+                  MT_SITE_PREP_SRC == mt::SITE_PREP_SRC &&
+                  MT_SITE_PREP_DST == mt::SITE_PREP_DST && MT_SITE_P18 == mt::SITE_P18,
+              "site numbers of the header and the kernels");
+
+mt_status mt_bounds_status(int64_t* count, int* site, int64_t* offset, int64_t* extent) {
+#if MT_BOUNDS_CHECK
+  int dev = 0;
+  DeviceInfo info;
+  mt_status st = current_device(&dev, &info);
+  if (st != MT_OK) return st;
+  if (!bounds_record()) return MT_ERR_CUDA;
+  mt::BoundsRecord r{};
+  const mt::BoundsRecord zero{};
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpyFromSymbol(&r, g_bounds, sizeof(r)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_bounds, &zero, sizeof(zero)) != cudaSuccess) {
+    cudaGetLastError();
+    return MT_ERR_CUDA;
+  }
+  if (count) *count = r.count;
+  if (site) *site = r.site;
+  if (offset) *offset = r.offset;
+  if (extent) *extent = r.extent;
+  return MT_OK;
+#else
+  (void)count;
+  (void)site;
+  (void)offset;
+  (void)extent;
+  return MT_ERR_UNSUPPORTED;  // the normal build checks nothing
+#endif
 }
 
 mt_status mt_device_status(cudaStream_t stream) {

@@ -4,7 +4,39 @@
 
 #include <cstdint>
 
+#include "kernels.h"
+
+// Checked builds: -DMT_BOUNDS_CHECK=1 (the library built as
+// libmtsgemm_checked.so).  Normal builds compile every check away.
+#ifndef MT_BOUNDS_CHECK
+#define MT_BOUNDS_CHECK 0
+#endif
+
 namespace mt {
+
+// True when elements [offset, offset + width) lie inside [0, extent).  In a
+// checked build an access outside is counted in `rec` (the first one's site,
+// offset and extent kept) and the caller skips it; normal builds always
+// return true without looking.
+__device__ __forceinline__ bool bounds_ok(BoundsRecord* rec, int site, int64_t offset,
+                                          int width, int64_t extent) {
+#if MT_BOUNDS_CHECK
+  if (offset >= 0 && offset + width <= extent) return true;
+  if (rec && atomicAdd(&rec->count, 1u) == 0u) {
+    rec->site = site;
+    rec->offset = offset;
+    rec->extent = extent;
+  }
+  return false;
+#else
+  (void)rec;
+  (void)site;
+  (void)offset;
+  (void)width;
+  (void)extent;
+  return true;
+#endif
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -8,6 +8,34 @@
 
 namespace mt {
 
+// Record of the accesses a checked build (compiled with MT_BOUNDS_CHECK=1)
+// found outside their buffers: how many, and the first one's site, element
+// offset and the buffer's extent in elements.  Those accesses are skipped
+// (a copy becomes a zero fill, a load reads 0, a store is dropped), so a
+// checked kernel never touches memory outside its buffers.
+struct BoundsRecord {
+  unsigned int count;
+  int site;
+  long long offset;
+  long long extent;
+};
+
+// Access sites a checked build names in BoundsRecord::site.
+enum BoundsSite {
+  SITE_A_LOAD = 1,      // global read of A by the staging copies
+  SITE_B_LOAD = 2,      // global read of B by the staging copies
+  SITE_A_SMEM = 3,      // shared write of a staged A tile
+  SITE_B_SMEM = 4,      // shared write of a staged B tile
+  SITE_FRAG = 5,        // shared read of an A or B fragment by the micro-kernel
+  SITE_C_STORE = 6,     // global read or write of C
+  SITE_PARTIAL = 7,     // global read or write of a K-slice partial tile
+  SITE_BIAS = 8,        // global read of the bias row
+  SITE_SLICE_SUM = 9,   // shared read or write of a K group's sum
+  SITE_PREP_SRC = 10,   // global read of an operand by the copy kernel
+  SITE_PREP_DST = 11,   // global write of an operand copy
+  SITE_P18 = 12         // any access of the one-warp kernel
+};
+
 // One compiled FFMA tile configuration and its kernel instantiations.
 struct FfmaEntry {
   int bm, bn, bk, stages, threads, min_blocks;
@@ -38,13 +66,15 @@ struct FfmaEntry {
 // with row pitch ldo >= cols, zero-filling columns cols..ldo-1: the layout
 // the 16-byte staging reads, for operands it cannot read as stored.
 cudaError_t launch_prep_operand(const float* src, int64_t ld, bool trans, float* out,
-                                int64_t ldo, int R, int cols, cudaStream_t stream);
+                                int64_t ldo, int R, int cols, cudaStream_t stream,
+                                BoundsRecord* bounds = nullptr);
 
 // C = beta * C (+ bias[col] when bias is not null) over an M x N view with
 // row stride ldc (C is not read when beta is 0).  The whole product when
 // alpha == 0 or K == 0.
 cudaError_t launch_scale_c(float* C, int M, int N, int64_t ldc, float beta,
-                           const float* bias, cudaStream_t stream);
+                           const float* bias, cudaStream_t stream,
+                           BoundsRecord* bounds = nullptr);
 
 // All FFMA configurations built into the library (null-terminated count).
 const FfmaEntry* ffma_entries(int* count);
@@ -76,7 +106,17 @@ struct GemmArgs {
   int split;
   int kt_per_slice;
   float* partial;
+  // Elements from A, B, C, partial up to the last element the product
+  // addresses (checked builds test every access against them), and the
+  // checked build's record (nullptr otherwise).
+  int64_t a_extent, b_extent, c_extent, partial_extent;
+  BoundsRecord* bounds;
 };
+
+// Elements a rows x cols view with row pitch ld spans (0 if empty).
+__host__ __device__ inline int64_t view_extent(int64_t rows, int64_t cols, int64_t ld) {
+  return rows > 0 && cols > 0 ? (rows - 1) * ld + cols : 0;
+}
 
 // Sums the K-slice partials of the split tiles (in slice order, so the
 // result does not depend on scheduling) and writes them to C with the

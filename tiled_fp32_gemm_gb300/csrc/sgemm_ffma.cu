@@ -21,23 +21,32 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(GemmArgs a, int bm, 
   const int per_piece = (block4 + pieces - 1) / pieces;
   const int e_begin = piece * per_piece;
   const int e_end = min(block4, e_begin + per_piece);
-  const float4* P = reinterpret_cast<const float4*>(a.partial) +
-                    static_cast<int64_t>(t) * a.split * block4;
+  const int64_t tile_off = static_cast<int64_t>(t) * a.split * block4;  // in float4s
+  const float4* P = reinterpret_cast<const float4*>(a.partial) + tile_off;
   for (int e4 = e_begin + threadIdx.x; e4 < e_end; e4 += blockDim.x) {
     const int r = (e4 * 4) / bn, c = (e4 * 4) % bn;
     const int row = tm * bm + r, col = tn * bn + c;
     if (row >= a.M || col >= a.N) continue;
-    float4 s = P[e4];
-    for (int sl = 1; sl < a.split; ++sl) {
-      const float4 v = P[static_cast<int64_t>(sl) * block4 + e4];
-      s.x += v.x;
-      s.y += v.y;
-      s.z += v.z;
-      s.w += v.w;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sl = 0; sl < a.split; ++sl) {
+      const int64_t e = static_cast<int64_t>(sl) * block4 + e4;
+      if (!bounds_ok(a.bounds, SITE_PARTIAL, (tile_off + e) * 4, 4, a.partial_extent)) continue;
+      const float4 v = P[e];
+      if (sl == 0) {
+        s = v;
+      } else {
+        s.x += v.x;
+        s.y += v.y;
+        s.z += v.z;
+        s.w += v.w;
+      }
     }
     float* c_row = a.C + static_cast<int64_t>(row) * a.ldc;
     const float v[4] = {a.alpha * s.x, a.alpha * s.y, a.alpha * s.z, a.alpha * s.w};
     if (vec_c) {
+      if (!bounds_ok(a.bounds, SITE_C_STORE, (c_row - a.C) + col, 4, a.c_extent) ||
+          (a.bias && !bounds_ok(a.bounds, SITE_BIAS, col, 4, a.N)))
+        continue;
       float4* cp = reinterpret_cast<float4*>(c_row + col);
       float4 o = make_float4(v[0], v[1], v[2], v[3]);
       if (a.beta != 0.0f) {
@@ -54,7 +63,9 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(GemmArgs a, int bm, 
       *cp = o;
     } else {
       for (int e = 0; e < 4; ++e)
-        if (col + e < a.N) {
+        if (col + e < a.N &&
+            bounds_ok(a.bounds, SITE_C_STORE, (c_row - a.C) + col + e, 1, a.c_extent) &&
+            (!a.bias || bounds_ok(a.bounds, SITE_BIAS, col + e, 1, a.N))) {
           float o = a.beta != 0.0f ? fmaf(a.beta, c_row[col + e], v[e]) : v[e];
           if (a.bias) o += a.bias[col + e];
           c_row[col + e] = o;
@@ -68,17 +79,27 @@ cudaError_t launch_splitk_reduce(const GemmArgs& a, int bm, int bn, bool vec_c,
   const int tail = a.tiles_m * a.tiles_n - a.full_tiles;
   if (tail <= 0) return cudaSuccess;
   const int pieces = std::max(1, bm * bn / 4096);
-  splitk_reduce_kernel<<<tail * pieces, 256, 0, stream>>>(a, bm, bn, pieces, vec_c ? 1 : 0);
+  GemmArgs r = a;
+  // Callers that did not state the partial buffer's extent (the tensor-core
+  // paths) have exactly one dense bm x bn tile per slice of each split tile.
+  if (r.partial_extent == 0)
+    r.partial_extent = static_cast<int64_t>(tail) * a.split * bm * bn;
+  splitk_reduce_kernel<<<tail * pieces, 256, 0, stream>>>(r, bm, bn, pieces, vec_c ? 1 : 0);
   return cudaGetLastError();
 }
 
 // C = beta * C (+ bias[col]) on an M x N view (C not read when beta is 0).
 __global__ void __launch_bounds__(256) scale_c_kernel(float* C, int M, int N, int64_t ldc,
-                                                     float beta, const float* bias) {
+                                                     float beta, const float* bias,
+                                                     BoundsRecord* rec) {
   const int64_t total = static_cast<int64_t>(M) * N;
+  const int64_t extent = view_extent(M, N, ldc);
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t i = e / N, j = e % N;
+    if (!bounds_ok(rec, SITE_C_STORE, i * ldc + j, 1, extent) ||
+        (bias && !bounds_ok(rec, SITE_BIAS, j, 1, N)))
+      continue;
     float* c = C + i * ldc + j;
     float v = beta != 0.0f ? beta * *c : 0.0f;
     if (bias) v += bias[j];
@@ -87,12 +108,12 @@ __global__ void __launch_bounds__(256) scale_c_kernel(float* C, int M, int N, in
 }
 
 cudaError_t launch_scale_c(float* C, int M, int N, int64_t ldc, float beta,
-                           const float* bias, cudaStream_t stream) {
+                           const float* bias, cudaStream_t stream, BoundsRecord* bounds) {
   const int64_t total = static_cast<int64_t>(M) * N;
   if (total <= 0) return cudaSuccess;
   const int64_t blocks = (total + 255) / 256;
   scale_c_kernel<<<static_cast<unsigned>(blocks < 65536 ? blocks : 65536), 256, 0, stream>>>(
-      C, M, N, ldc, beta, bias);
+      C, M, N, ldc, beta, bias, bounds);
   return cudaGetLastError();
 }
 
@@ -106,7 +127,9 @@ template <bool TRANS>
 __global__ void __launch_bounds__(256) prep_operand_kernel(const float* __restrict__ src,
                                                            int64_t ld, float* __restrict__ out,
                                                            int64_t ldo, int R, int cols,
-                                                           int tiles_c) {
+                                                           int tiles_c, BoundsRecord* rec) {
+  const int64_t src_extent = TRANS ? view_extent(cols, R, ld) : view_extent(R, cols, ld);
+  const int64_t out_extent = static_cast<int64_t>(R) * ldo;
   __shared__ float t[64][65];
   const int r0 = static_cast<int>(blockIdx.x / tiles_c) * 64;
   const int c0 = static_cast<int>(blockIdx.x % tiles_c) * 64;
@@ -119,10 +142,14 @@ __global__ void __launch_bounds__(256) prep_operand_kernel(const float* __restri
       if constexpr (TRANS) {
         // Source row c0 + i holds column c0 + i of op(src): t[c][r].
         const int c = c0 + i, r = r0 + x;
-        t[i][x] = c < cols && r < R ? src[static_cast<int64_t>(c) * ld + r] : 0.0f;
+        const int64_t o = static_cast<int64_t>(c) * ld + r;
+        t[i][x] = c < cols && r < R && bounds_ok(rec, SITE_PREP_SRC, o, 1, src_extent) ? src[o]
+                                                                                       : 0.0f;
       } else {
         const int r = r0 + i, c = c0 + x;
-        t[i][x] = r < R && c < cols ? src[static_cast<int64_t>(r) * ld + c] : 0.0f;
+        const int64_t o = static_cast<int64_t>(r) * ld + c;
+        t[i][x] = r < R && c < cols && bounds_ok(rec, SITE_PREP_SRC, o, 1, src_extent) ? src[o]
+                                                                                       : 0.0f;
       }
     }
   }
@@ -133,23 +160,26 @@ __global__ void __launch_bounds__(256) prep_operand_kernel(const float* __restri
     for (int h = 0; h < 2; ++h) {
       const int x = tx + 32 * h;
       const int r = r0 + i, c = c0 + x;
-      if (r < R && c < ldo) out[static_cast<int64_t>(r) * ldo + c] = TRANS ? t[x][i] : t[i][x];
+      if (r < R && c < ldo &&
+          bounds_ok(rec, SITE_PREP_DST, static_cast<int64_t>(r) * ldo + c, 1, out_extent))
+        out[static_cast<int64_t>(r) * ldo + c] = TRANS ? t[x][i] : t[i][x];
     }
   }
 }
 
 cudaError_t launch_prep_operand(const float* src, int64_t ld, bool trans, float* out,
-                                int64_t ldo, int R, int cols, cudaStream_t stream) {
+                                int64_t ldo, int R, int cols, cudaStream_t stream,
+                                BoundsRecord* bounds) {
   if (R <= 0 || ldo <= 0) return cudaSuccess;
   const int64_t tiles_r = (R + 63) / 64, tiles_c = (ldo + 63) / 64;
   if (tiles_c > INT32_MAX || tiles_r * tiles_c > INT32_MAX) return cudaErrorInvalidValue;
   const unsigned grid = static_cast<unsigned>(tiles_r * tiles_c);
   if (trans)
     prep_operand_kernel<true><<<grid, 256, 0, stream>>>(src, ld, out, ldo, R, cols,
-                                                        static_cast<int>(tiles_c));
+                                                        static_cast<int>(tiles_c), bounds);
   else
     prep_operand_kernel<false><<<grid, 256, 0, stream>>>(src, ld, out, ldo, R, cols,
-                                                         static_cast<int>(tiles_c));
+                                                         static_cast<int>(tiles_c), bounds);
   return cudaGetLastError();
 }
 

@@ -163,8 +163,11 @@ struct AStage<T, STAGE_VEC> {
   int64_t row_step;   // ROWS_STEP * lda
   int row, col, K;
   uint32_t rows_ok;   // bit t: row t of this thread's chunks is inside M
+  int64_t extent;     // checked builds: elements of A
+  BoundsRecord* rec;
 
-  __device__ AStage(const GemmArgs& a, int m0, int tid) : base(a.A), K(a.K) {
+  __device__ AStage(const GemmArgs& a, int m0, int tid)
+      : base(a.A), K(a.K), extent(a.a_extent), rec(a.bounds) {
     row = tid / CHUNKS_ROW;
     col = (tid % CHUNKS_ROW) * 4;
     row_step = static_cast<int64_t>(ROWS_STEP) * a.lda;
@@ -180,9 +183,11 @@ struct AStage<T, STAGE_VEC> {
     const bool k_ok = k0 + col < K;
 #pragma unroll
     for (int t = 0; t < ITERS; ++t) {
-      const bool ok = k_ok && (rows_ok >> t & 1u);
-      cp_async_16(smem_u32(As + la.offset(stage, row + t * ROWS_STEP, col)),
-                  ok ? src + t * row_step + k0 : base, ok ? 16u : 0u);
+      const float* g = src + t * row_step + k0;
+      const int so = la.offset(stage, row + t * ROWS_STEP, col);
+      const bool ok = k_ok && (rows_ok >> t & 1u) && bounds_ok(rec, SITE_A_LOAD, g - base, 4, extent);
+      if (bounds_ok(rec, SITE_A_SMEM, so, 4, la.size()))
+        cp_async_16(smem_u32(As + so), ok ? g : base, ok ? 16u : 0u);
     }
   }
 };
@@ -198,8 +203,11 @@ struct AStage<T, STAGE_SCALAR> {
   int64_t row_step;
   int row, col, K;
   uint32_t rows_ok;
+  int64_t extent;
+  BoundsRecord* rec;
 
-  __device__ AStage(const GemmArgs& a, int m0, int tid) : base(a.A), K(a.K) {
+  __device__ AStage(const GemmArgs& a, int m0, int tid)
+      : base(a.A), K(a.K), extent(a.a_extent), rec(a.bounds) {
     row = tid / T::BK;
     col = tid % T::BK;
     row_step = static_cast<int64_t>(ROWS_STEP) * a.lda;
@@ -215,9 +223,11 @@ struct AStage<T, STAGE_SCALAR> {
     const bool k_ok = k0 + col < K;
 #pragma unroll
     for (int t = 0; t < ITERS; ++t) {
-      const bool ok = k_ok && (rows_ok >> t & 1u);
-      cp_async_4(smem_u32(As + la.offset(stage, row + t * ROWS_STEP, col)),
-                 ok ? src + t * row_step + k0 : base, ok ? 4u : 0u);
+      const float* g = src + t * row_step + k0;
+      const int so = la.offset(stage, row + t * ROWS_STEP, col);
+      const bool ok = k_ok && (rows_ok >> t & 1u) && bounds_ok(rec, SITE_A_LOAD, g - base, 1, extent);
+      if (bounds_ok(rec, SITE_A_SMEM, so, 1, la.size()))
+        cp_async_4(smem_u32(As + so), ok ? g : base, ok ? 4u : 0u);
     }
   }
 };
@@ -233,9 +243,11 @@ struct AStage<T, STAGE_TRANS> {
   const float* At;
   int64_t lda;
   int M, K, m0, lr, lc, warp;
+  int64_t extent;
+  BoundsRecord* rec;
 
   __device__ AStage(const GemmArgs& a, int m0_, int tid)
-      : At(a.A), lda(a.lda), M(a.M), K(a.K), m0(m0_) {
+      : At(a.A), lda(a.lda), M(a.M), K(a.K), m0(m0_), extent(a.a_extent), rec(a.bounds) {
     lr = tid & 7;
     lc = (tid & 31) >> 3;
     warp = tid >> 5;
@@ -247,9 +259,11 @@ struct AStage<T, STAGE_TRANS> {
     for (int t = 0; t < ITERS; ++t) {
       const int b = warp + t * NW;
       const int r = (b % RB) * 8 + lr, c = (b / RB) * 4 + lc;
-      const bool ok = m0 + r < M && k0 + c < K;
-      cp_async_4(smem_u32(As + la.offset(stage, r, c)),
-                 ok ? At + static_cast<int64_t>(k0 + c) * lda + m0 + r : At, ok ? 4u : 0u);
+      const int64_t go = static_cast<int64_t>(k0 + c) * lda + m0 + r;
+      const int so = la.offset(stage, r, c);
+      const bool ok = m0 + r < M && k0 + c < K && bounds_ok(rec, SITE_A_LOAD, go, 1, extent);
+      if (bounds_ok(rec, SITE_A_SMEM, so, 1, la.size()))
+        cp_async_4(smem_u32(As + so), ok ? At + go : At, ok ? 4u : 0u);
     }
   }
 };
@@ -266,8 +280,11 @@ struct AStage<T, STAGE_KMAJOR> {
   int64_t lda, row_step;
   int row, col, K;
   bool col_ok;
+  int64_t extent;
+  BoundsRecord* rec;
 
-  __device__ AStage(const GemmArgs& a, int m0, int tid) : base(a.A), lda(a.lda), K(a.K) {
+  __device__ AStage(const GemmArgs& a, int m0, int tid)
+      : base(a.A), lda(a.lda), K(a.K), extent(a.a_extent), rec(a.bounds) {
     row = tid / CHUNKS_ROW;
     col = (tid % CHUNKS_ROW) * 4;
     row_step = static_cast<int64_t>(ROWS_STEP) * a.lda;
@@ -279,9 +296,12 @@ struct AStage<T, STAGE_KMAJOR> {
     const int k0 = kt * T::BK;
 #pragma unroll
     for (int t = 0; t < ITERS; ++t) {
-      const bool ok = col_ok && k0 + row + t * ROWS_STEP < K;
-      cp_async_16(smem_u32(As + la.offset(stage, row + t * ROWS_STEP, col)),
-                  ok ? src + static_cast<int64_t>(k0) * lda + t * row_step : base, ok ? 16u : 0u);
+      const float* g = src + static_cast<int64_t>(k0) * lda + t * row_step;
+      const int so = la.offset(stage, row + t * ROWS_STEP, col);
+      const bool ok = col_ok && k0 + row + t * ROWS_STEP < K &&
+                      bounds_ok(rec, SITE_A_LOAD, g - base, 4, extent);
+      if (bounds_ok(rec, SITE_A_SMEM, so, 4, la.size()))
+        cp_async_16(smem_u32(As + so), ok ? g : base, ok ? 16u : 0u);
     }
   }
 };
@@ -305,8 +325,11 @@ struct AStage<T, STAGE_GATHER> {
   int64_t row_step;  // M_STEP * lda
   int k_off, m_first, K;
   uint32_t rows_ok;  // bit t: row m0 + m_first + t*M_STEP is inside M
+  int64_t extent;
+  BoundsRecord* rec;
 
-  __device__ AStage(const GemmArgs& a, int m0, int tid) : base(a.A), K(a.K) {
+  __device__ AStage(const GemmArgs& a, int m0, int tid)
+      : base(a.A), K(a.K), extent(a.a_extent), rec(a.bounds) {
     const int warp = tid >> 5, lane = tid & 31;
     k_off = (warp % KB) * 8 + (lane & 7);
     m_first = (warp / KB) * 4 + (lane >> 3);
@@ -323,9 +346,11 @@ struct AStage<T, STAGE_GATHER> {
     const bool k_ok = k0 + k_off < K;
 #pragma unroll
     for (int t = 0; t < ITERS; ++t) {
-      const bool ok = k_ok && (rows_ok >> t & 1u);
-      cp_async_4(smem_u32(As + la.offset(stage, k_off, m_first + t * M_STEP)),
-                 ok ? src + t * row_step + k0 : base, ok ? 4u : 0u);
+      const float* g = src + t * row_step + k0;
+      const int so = la.offset(stage, k_off, m_first + t * M_STEP);
+      const bool ok = k_ok && (rows_ok >> t & 1u) && bounds_ok(rec, SITE_A_LOAD, g - base, 1, extent);
+      if (bounds_ok(rec, SITE_A_SMEM, so, 1, la.size()))
+        cp_async_4(smem_u32(As + so), ok ? g : base, ok ? 4u : 0u);
     }
   }
 };
@@ -342,8 +367,11 @@ struct BStage<T, STAGE_VEC> {
   int64_t ldb, row_step;
   int row, col, K;
   bool col_ok;
+  int64_t extent;
+  BoundsRecord* rec;
 
-  __device__ BStage(const GemmArgs& a, int n0, int tid) : base(a.B), ldb(a.ldb), K(a.K) {
+  __device__ BStage(const GemmArgs& a, int n0, int tid)
+      : base(a.B), ldb(a.ldb), K(a.K), extent(a.b_extent), rec(a.bounds) {
     row = tid / CHUNKS_ROW;
     col = (tid % CHUNKS_ROW) * 4;
     row_step = static_cast<int64_t>(ROWS_STEP) * a.ldb;
@@ -355,9 +383,12 @@ struct BStage<T, STAGE_VEC> {
     const int k0 = kt * T::BK;
 #pragma unroll
     for (int t = 0; t < ITERS; ++t) {
-      const bool ok = col_ok && k0 + row + t * ROWS_STEP < K;
-      cp_async_16(smem_u32(Bs + lb.offset(stage, row + t * ROWS_STEP, col)),
-                  ok ? src + static_cast<int64_t>(k0) * ldb + t * row_step : base, ok ? 16u : 0u);
+      const float* g = src + static_cast<int64_t>(k0) * ldb + t * row_step;
+      const int so = lb.offset(stage, row + t * ROWS_STEP, col);
+      const bool ok = col_ok && k0 + row + t * ROWS_STEP < K &&
+                      bounds_ok(rec, SITE_B_LOAD, g - base, 4, extent);
+      if (bounds_ok(rec, SITE_B_SMEM, so, 4, lb.size()))
+        cp_async_16(smem_u32(Bs + so), ok ? g : base, ok ? 16u : 0u);
     }
   }
 };
@@ -372,8 +403,11 @@ struct BStage<T, STAGE_SCALAR> {
   int64_t ldb, row_step;
   int row, col, K;
   bool col_ok;
+  int64_t extent;
+  BoundsRecord* rec;
 
-  __device__ BStage(const GemmArgs& a, int n0, int tid) : base(a.B), ldb(a.ldb), K(a.K) {
+  __device__ BStage(const GemmArgs& a, int n0, int tid)
+      : base(a.B), ldb(a.ldb), K(a.K), extent(a.b_extent), rec(a.bounds) {
     row = tid / T::BN;
     col = tid % T::BN;
     row_step = static_cast<int64_t>(ROWS_STEP) * a.ldb;
@@ -385,9 +419,12 @@ struct BStage<T, STAGE_SCALAR> {
     const int k0 = kt * T::BK;
 #pragma unroll
     for (int t = 0; t < ITERS; ++t) {
-      const bool ok = col_ok && k0 + row + t * ROWS_STEP < K;
-      cp_async_4(smem_u32(Bs + lb.offset(stage, row + t * ROWS_STEP, col)),
-                 ok ? src + static_cast<int64_t>(k0) * ldb + t * row_step : base, ok ? 4u : 0u);
+      const float* g = src + static_cast<int64_t>(k0) * ldb + t * row_step;
+      const int so = lb.offset(stage, row + t * ROWS_STEP, col);
+      const bool ok = col_ok && k0 + row + t * ROWS_STEP < K &&
+                      bounds_ok(rec, SITE_B_LOAD, g - base, 1, extent);
+      if (bounds_ok(rec, SITE_B_SMEM, so, 1, lb.size()))
+        cp_async_4(smem_u32(Bs + so), ok ? g : base, ok ? 4u : 0u);
     }
   }
 };
@@ -403,9 +440,11 @@ struct BStage<T, STAGE_TRANS> {
   const float* Bt;
   int64_t ldb;
   int N, K, n0, lk, ln, warp;
+  int64_t extent;
+  BoundsRecord* rec;
 
   __device__ BStage(const GemmArgs& a, int n0_, int tid)
-      : Bt(a.B), ldb(a.ldb), N(a.N), K(a.K), n0(n0_) {
+      : Bt(a.B), ldb(a.ldb), N(a.N), K(a.K), n0(n0_), extent(a.b_extent), rec(a.bounds) {
     lk = tid & 7;
     ln = (tid & 31) >> 3;
     warp = tid >> 5;
@@ -417,15 +456,25 @@ struct BStage<T, STAGE_TRANS> {
     for (int t = 0; t < ITERS; ++t) {
       const int b = warp + t * NW;
       const int kk = (b % KB) * 8 + lk, n = (b / KB) * 4 + ln;
-      const bool ok = n0 + n < N && k0 + kk < K;
-      cp_async_4(smem_u32(Bs + lb.offset(stage, kk, n)),
-                 ok ? Bt + static_cast<int64_t>(n0 + n) * ldb + k0 + kk : Bt, ok ? 4u : 0u);
+      const int64_t go = static_cast<int64_t>(n0 + n) * ldb + k0 + kk;
+      const int so = lb.offset(stage, kk, n);
+      const bool ok = n0 + n < N && k0 + kk < K && bounds_ok(rec, SITE_B_LOAD, go, 1, extent);
+      if (bounds_ok(rec, SITE_B_SMEM, so, 1, lb.size()))
+        cp_async_4(smem_u32(Bs + so), ok ? Bt + go : Bt, ok ? 4u : 0u);
     }
   }
 };
 
 __device__ __forceinline__ float pick(const float4& v, int c) {
   return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
+}
+
+// A float4 fragment read from a staged region of `size` floats (a checked
+// build reads zeros for one outside it and records it).
+__device__ __forceinline__ float4 frag4(const float* region, const float* p, int size,
+                                        BoundsRecord* rec) {
+  if (!bounds_ok(rec, SITE_FRAG, p - region, 4, size)) return make_float4(0.f, 0.f, 0.f, 0.f);
+  return *reinterpret_cast<const float4*>(p);
 }
 
 // ---------------------------------------------------------------------------
@@ -541,7 +590,7 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
       if constexpr (!KMAJOR) {
 #pragma unroll
         for (int i = 0; i < T::TM; ++i)
-          a[i] = *reinterpret_cast<const float4*>(a_ptr + i * T::LM * LA.row_stride() + k4 * 4);
+          a[i] = frag4(As, a_ptr + i * T::LM * LA.row_stride() + k4 * 4, LA.size(), args.bounds);
       }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
@@ -549,14 +598,14 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
         if constexpr (KMAJOR) {
 #pragma unroll
           for (int q = 0; q < T::TM / 4; ++q)
-            ak[q] = *reinterpret_cast<const float4*>(a_ptr + (k4 * 4 + kk) * LA.row_stride() +
-                                                     q * T::LM * 4);
+            ak[q] = frag4(As, a_ptr + (k4 * 4 + kk) * LA.row_stride() + q * T::LM * 4, LA.size(),
+                          args.bounds);
         }
         float4 b[T::TN / 4];
 #pragma unroll
         for (int g = 0; g < T::TN / 4; ++g)
-          b[g] = *reinterpret_cast<const float4*>(b_ptr + (k4 * 4 + kk) * LB.row_stride() +
-                                                  g * T::LN * 4);
+          b[g] = frag4(Bs, b_ptr + (k4 * 4 + kk) * LB.row_stride() + g * T::LN * 4, LB.size(),
+                       args.bounds);
 #pragma unroll
         for (int g = 0; g < T::TN / 4; ++g) {
 #pragma unroll
@@ -596,9 +645,11 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
 #pragma unroll
         for (int g = 0; g < T::TN / 4; ++g) {
           const int c = wn * T::WN + g * T::LN * 4 + ln * 4;
-          *reinterpret_cast<float4*>(mine + r * T::BN + c) =
-              make_float4(acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
-                          acc[i][2 * g + 1].y);
+          if (bounds_ok(args.bounds, SITE_SLICE_SUM, (mine - red) + r * T::BN + c, 4,
+                        T::REDUCE_BYTES / 4))
+            *reinterpret_cast<float4*>(mine + r * T::BN + c) =
+                make_float4(acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
+                            acc[i][2 * g + 1].y);
         }
       }
     }
@@ -613,7 +664,7 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
 #pragma unroll
         for (int g = 0; g < T::TN / 4; ++g) {
           const int c = wn * T::WN + g * T::LN * 4 + ln * 4;
-          const float4 o = *reinterpret_cast<const float4*>(other + r * T::BN + c);
+          const float4 o = frag4(red, other + r * T::BN + c, T::REDUCE_BYTES / 4, args.bounds);
           acc[i][2 * g].x += o.x;
           acc[i][2 * g].y += o.y;
           acc[i][2 * g + 1].x += o.z;
@@ -635,9 +686,11 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
 #pragma unroll
       for (int g = 0; g < T::TN / 4; ++g) {
         const int c = wn * T::WN + g * T::LN * 4 + ln * 4;
-        *reinterpret_cast<float4*>(P + r * T::BN + c) =
-            make_float4(acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
-                        acc[i][2 * g + 1].y);
+        if (bounds_ok(args.bounds, SITE_PARTIAL, (P - args.partial) + r * T::BN + c, 4,
+                      args.partial_extent))
+          *reinterpret_cast<float4*>(P + r * T::BN + c) =
+              make_float4(acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
+                          acc[i][2 * g + 1].y);
       }
     }
     return;
@@ -661,7 +714,8 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
                              alpha * acc[i][2 * g + 1].x, alpha * acc[i][2 * g + 1].y);
       if constexpr (VEC) {
         // N % 4 == 0, so a float4 group is either wholly inside or outside.
-        if (col < N) {
+        if (col < N && bounds_ok(args.bounds, SITE_C_STORE, (c_row - C) + col, 4, args.c_extent) &&
+            (!bias || bounds_ok(args.bounds, SITE_BIAS, col, 4, N))) {
           float4* cp = reinterpret_cast<float4*>(c_row + col);
           if (beta != 0.0f) {
             const float4 o = *cp;
@@ -680,7 +734,9 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
         const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (col + e < N) {
+          if (col + e < N &&
+              bounds_ok(args.bounds, SITE_C_STORE, (c_row - C) + col + e, 1, args.c_extent) &&
+              (!bias || bounds_ok(args.bounds, SITE_BIAS, col + e, 1, N))) {
             float o = beta != 0.0f ? fmaf(beta, c_row[col + e], vv[e]) : vv[e];
             if (bias) o += bias[col + e];
             c_row[col + e] = o;

@@ -28,6 +28,7 @@
 // copies index A and B and how the result is written.
 #include <cuda_runtime.h>
 
+#include "device_util.cuh"
 #include "kernels.h"
 #include "smem_layout.cuh"
 
@@ -43,11 +44,14 @@ constexpr SmemLayout p18_a_layout(bool pad, int stages) {
 constexpr SmemLayout p18_b_layout(int stages) { return SmemLayout{P18_BK, P18_BN, 0, stages}; }
 }  // namespace
 
-// op(A)[i][k] or op(B)[k][j] from its storage, 0.0 outside rows x cols.
+// op(A)[i][k] or op(B)[k][j] from its storage, 0.0 outside rows x cols
+// (and, in a checked build, outside the `extent` elements of the storage).
 __device__ __forceinline__ float fetch_operand(const float* base, int64_t ld, int trans, int i,
-                                               int j, int rows, int cols) {
+                                               int j, int rows, int cols, int64_t extent,
+                                               BoundsRecord* rec) {
   if (i >= rows || j >= cols) return 0.0f;
-  return base[trans ? static_cast<int64_t>(j) * ld + i : static_cast<int64_t>(i) * ld + j];
+  const int64_t o = trans ? static_cast<int64_t>(j) * ld + i : static_cast<int64_t>(i) * ld + j;
+  return bounds_ok(rec, SITE_P18, o, 1, extent) ? base[o] : 0.0f;
 }
 
 template <bool PAD, int STAGES>
@@ -79,15 +83,19 @@ __global__ void __launch_bounds__(P18_THREADS) sgemm_p18_kernel(GemmArgs args) {
     for (int e = 0; e < A_PER_LANE; ++e) {
       const int slot = e * P18_THREADS + lane;
       const int ar = slot / P18_BK, ak = slot % P18_BK;
-      a_tiles[LA.offset(buf, ar, ak)] =
-          fetch_operand(args.A, args.lda, args.trans_a, m0 + ar, k0 + ak, args.M, args.K);
+      const float v = fetch_operand(args.A, args.lda, args.trans_a, m0 + ar, k0 + ak, args.M,
+                                    args.K, args.a_extent, args.bounds);
+      if (bounds_ok(args.bounds, SITE_P18, LA.offset(buf, ar, ak), 1, LA.size()))
+        a_tiles[LA.offset(buf, ar, ak)] = v;
     }
 #pragma unroll
     for (int e = 0; e < B_PER_LANE; ++e) {
       const int slot = e * P18_THREADS + lane;
       const int bk = slot / P18_BN, bn = slot % P18_BN;
-      b_tiles[LB.offset(buf, bk, bn)] =
-          fetch_operand(args.B, args.ldb, args.trans_b, k0 + bk, n0 + bn, args.K, args.N);
+      const float v = fetch_operand(args.B, args.ldb, args.trans_b, k0 + bk, n0 + bn, args.K,
+                                    args.N, args.b_extent, args.bounds);
+      if (bounds_ok(args.bounds, SITE_P18, LB.offset(buf, bk, bn), 1, LB.size()))
+        b_tiles[LB.offset(buf, bk, bn)] = v;
     }
     __syncthreads();
     // Scalar shared reads, one per operand and k (volatile keeps the
@@ -96,12 +104,21 @@ __global__ void __launch_bounds__(P18_THREADS) sgemm_p18_kernel(GemmArgs args) {
     const volatile float* av = a_tiles;
     const volatile float* bv = b_tiles;
 #pragma unroll
-    for (int kk = 0; kk < P18_BK; ++kk)
+    for (int kk = 0; kk < P18_BK; ++kk) {
+      if (MT_BOUNDS_CHECK && (!bounds_ok(args.bounds, SITE_P18, LA.offset(buf, r, kk), 1,
+                                         LA.size()) ||
+                              !bounds_ok(args.bounds, SITE_P18, LB.offset(buf, kk, c), 1,
+                                         LB.size())))
+        continue;
       acc = fmaf(av[LA.offset(buf, r, kk)], bv[LB.offset(buf, kk, c)], acc);
+    }
     if (STAGES == 1) __syncthreads();  // the next tile's copies overwrite this stage
   }
   const int row = m0 + r, col = n0 + c;
-  if (row < args.M && col < args.N) {
+  if (row < args.M && col < args.N &&
+      bounds_ok(args.bounds, SITE_P18, static_cast<int64_t>(row) * args.ldc + col, 1,
+                args.c_extent) &&
+      (!args.bias || bounds_ok(args.bounds, SITE_BIAS, col, 1, args.N))) {
     float* out = args.C + static_cast<int64_t>(row) * args.ldc + col;
     const float v = args.alpha * acc;
     float o = args.beta != 0.0f ? fmaf(args.beta, *out, v) : v;
