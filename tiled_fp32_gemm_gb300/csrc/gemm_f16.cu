@@ -446,22 +446,28 @@ __global__ void __launch_bounds__(THREADS, 1)
 // per thread and step).
 __global__ void __launch_bounds__(256) repack16_kernel(const uint16_t* __restrict__ src,
                                                        int64_t lds, uint16_t* __restrict__ dst,
-                                                       int64_t ldd, int64_t rows, int64_t cols) {
+                                                       int64_t ldd, int64_t rows, int64_t cols,
+                                                       BoundsRecord* rec) {
   const int64_t per_row = ldd / 8;
   const int64_t total = rows * per_row;
+  const int64_t src_extent = view_extent(rows, cols, lds), dst_extent = rows * ldd;
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t r = e / per_row, c0 = (e % per_row) * 8;
     const uint16_t* s = src + r * lds;
     uint16_t v[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = c0 + i < cols ? s[c0 + i] : static_cast<uint16_t>(0);
+    for (int i = 0; i < 8; ++i)
+      v[i] = c0 + i < cols && bounds_ok(rec, SITE_PREP_SRC, r * lds + c0 + i, 1, src_extent)
+                 ? s[c0 + i]
+                 : static_cast<uint16_t>(0);
     uint4 o;
     o.x = v[0] | (static_cast<uint32_t>(v[1]) << 16);
     o.y = v[2] | (static_cast<uint32_t>(v[3]) << 16);
     o.z = v[4] | (static_cast<uint32_t>(v[5]) << 16);
     o.w = v[6] | (static_cast<uint32_t>(v[7]) << 16);
-    *reinterpret_cast<uint4*>(dst + r * ldd + c0) = o;
+    if (bounds_ok(rec, SITE_PREP_DST, r * ldd + c0, 8, dst_extent))
+      *reinterpret_cast<uint4*>(dst + r * ldd + c0) = o;
   }
 }
 
@@ -498,7 +504,7 @@ cudaError_t repack_operands(const GemmArgs& a, const F16Operands& f, const F16La
     const int64_t ldd = (cols + 7) / 8 * 8;
     f16tc::repack16_kernel<<<1216, 256, 0, stream>>>(static_cast<const uint16_t*>(f.A), a.lda,
                                                      reinterpret_cast<uint16_t*>(ws), ldd, rows,
-                                                     cols);
+                                                     cols, a.bounds);
     *A = ws;
     *lda = ldd;
   }
@@ -507,7 +513,7 @@ cudaError_t repack_operands(const GemmArgs& a, const F16Operands& f, const F16La
     const int64_t ldd = (cols + 7) / 8 * 8;
     uint16_t* dst = reinterpret_cast<uint16_t*>(ws + L.repack_a_bytes);
     f16tc::repack16_kernel<<<1216, 256, 0, stream>>>(static_cast<const uint16_t*>(f.B), a.ldb,
-                                                     dst, ldd, rows, cols);
+                                                     dst, ldd, rows, cols, a.bounds);
     *B = dst;
     *ldb = ldd;
   }
@@ -562,7 +568,7 @@ struct Cfg16 {
     if (a.split > 1) sched.partial = reinterpret_cast<float*>(ws + L.partial_offset);
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int grid = units < max_ctas ? units : max_ctas;
-    const tc::Epilogue ep{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0, a.bias};
+    const tc::Epilogue ep = tc::make_epilogue(a, vec_c, tiles, BM, BN);
     auto go = [&](auto kern) {
       kern<<<grid, f16tc::THREADS, G::SMEM_BYTES, stream>>>(map_a, map_b, idesc, ep, kt, mt, nt,
                                                             a.group_m, sched, fault_inject);
@@ -657,7 +663,7 @@ struct CfgPair {
     if (a.split > 1) sched.partial = reinterpret_cast<float*>(ws + L.partial_offset);
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int clusters = units < max_clusters ? units : max_clusters;
-    const tc::Epilogue ep{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0, a.bias};
+    const tc::Epilogue ep = tc::make_epilogue(a, vec_c, tiles, PAIR_TILE, PAIR_TILE);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

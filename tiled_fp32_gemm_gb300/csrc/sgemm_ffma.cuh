@@ -185,7 +185,8 @@ struct AStage<T, STAGE_VEC> {
     for (int t = 0; t < ITERS; ++t) {
       const float* g = src + t * row_step + k0;
       const int so = la.offset(stage, row + t * ROWS_STEP, col);
-      const bool ok = k_ok && (rows_ok >> t & 1u) && bounds_ok(rec, SITE_A_LOAD, g - base, 4, extent);
+      const bool ok = k_ok && (rows_ok >> t & 1u) &&
+                      bounds_ok(rec, SITE_A_LOAD, g - base, 4, extent);
       if (bounds_ok(rec, SITE_A_SMEM, so, 4, la.size()))
         cp_async_16(smem_u32(As + so), ok ? g : base, ok ? 16u : 0u);
     }
@@ -225,7 +226,8 @@ struct AStage<T, STAGE_SCALAR> {
     for (int t = 0; t < ITERS; ++t) {
       const float* g = src + t * row_step + k0;
       const int so = la.offset(stage, row + t * ROWS_STEP, col);
-      const bool ok = k_ok && (rows_ok >> t & 1u) && bounds_ok(rec, SITE_A_LOAD, g - base, 1, extent);
+      const bool ok = k_ok && (rows_ok >> t & 1u) &&
+                      bounds_ok(rec, SITE_A_LOAD, g - base, 1, extent);
       if (bounds_ok(rec, SITE_A_SMEM, so, 1, la.size()))
         cp_async_4(smem_u32(As + so), ok ? g : base, ok ? 4u : 0u);
     }
@@ -348,7 +350,8 @@ struct AStage<T, STAGE_GATHER> {
     for (int t = 0; t < ITERS; ++t) {
       const float* g = src + t * row_step + k0;
       const int so = la.offset(stage, k_off, m_first + t * M_STEP);
-      const bool ok = k_ok && (rows_ok >> t & 1u) && bounds_ok(rec, SITE_A_LOAD, g - base, 1, extent);
+      const bool ok = k_ok && (rows_ok >> t & 1u) &&
+                      bounds_ok(rec, SITE_A_LOAD, g - base, 1, extent);
       if (bounds_ok(rec, SITE_A_SMEM, so, 1, la.size()))
         cp_async_4(smem_u32(As + so), ok ? g : base, ok ? 4u : 0u);
     }

@@ -133,10 +133,13 @@ __device__ __forceinline__ void split4(float4 x, float4& big, float4& small) {
 template <class G, int ROWS>
 __global__ void __launch_bounds__(256) pack_kc_kernel(const float* __restrict__ src, int64_t ld,
                                                       float* __restrict__ dst_base, int R, int K,
-                                                      int Kt, int vec) {
+                                                      int Kt, int vec, BoundsRecord* rec) {
   constexpr int BK = G::BK;
   constexpr int BLOCK = ROWS * G::ROW_BYTES;
   const int kt = blockIdx.x, rt = blockIdx.y;
+  // Checked builds: the source view and the gridDim.y x Kt packed blocks.
+  const int64_t src_extent = view_extent(R, K, ld);
+  const int64_t dst_words = static_cast<int64_t>(gridDim.y) * Kt * (2 * BLOCK / 4);
   char* dst = reinterpret_cast<char*>(dst_base) +
               (static_cast<int64_t>(rt) * Kt + kt) * static_cast<int64_t>(2 * BLOCK);
   for (int c = threadIdx.x; c < ROWS * (BK / 4); c += 256) {
@@ -144,21 +147,27 @@ __global__ void __launch_bounds__(256) pack_kc_kernel(const float* __restrict__ 
     const int row = rt * ROWS + r, k = kt * BK + ch * 4;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (row < R) {
-      const float* p = src + static_cast<int64_t>(row) * ld + k;
+      const int64_t o = static_cast<int64_t>(row) * ld + k;
+      const float* p = src + o;
       if (vec) {
-        if (k < K) v = *reinterpret_cast<const float4*>(p);
+        if (k < K && bounds_ok(rec, SITE_PREP_SRC, o, 4, src_extent))
+          v = *reinterpret_cast<const float4*>(p);
       } else {
-        if (k + 0 < K) v.x = p[0];
-        if (k + 1 < K) v.y = p[1];
-        if (k + 2 < K) v.z = p[2];
-        if (k + 3 < K) v.w = p[3];
+        if (k + 0 < K && bounds_ok(rec, SITE_PREP_SRC, o + 0, 1, src_extent)) v.x = p[0];
+        if (k + 1 < K && bounds_ok(rec, SITE_PREP_SRC, o + 1, 1, src_extent)) v.y = p[1];
+        if (k + 2 < K && bounds_ok(rec, SITE_PREP_SRC, o + 2, 1, src_extent)) v.z = p[2];
+        if (k + 3 < K && bounds_ok(rec, SITE_PREP_SRC, o + 3, 1, src_extent)) v.w = p[3];
       }
     }
     float4 big, small;
     split4(v, big, small);
     const uint32_t off = G::offset(r, ch * 4);
-    *reinterpret_cast<float4*>(dst + off) = big;
-    *reinterpret_cast<float4*>(dst + BLOCK + off) = small;
+    const int64_t w = (dst - reinterpret_cast<char*>(dst_base) + off) / 4;
+    if (bounds_ok(rec, SITE_PREP_DST, w, 4, dst_words) &&
+        bounds_ok(rec, SITE_PREP_DST, w + BLOCK / 4, 4, dst_words)) {
+      *reinterpret_cast<float4*>(dst + off) = big;
+      *reinterpret_cast<float4*>(dst + BLOCK + off) = small;
+    }
   }
 }
 
@@ -170,7 +179,7 @@ __global__ void __launch_bounds__(256) pack_kc_kernel(const float* __restrict__ 
 template <class G, int ROWS>
 __global__ void __launch_bounds__(256) pack_rc_kernel(const float* __restrict__ src, int64_t ld,
                                                       float* __restrict__ dst_base, int R, int K,
-                                                      int Kt, int Rt) {
+                                                      int Kt, int Rt, BoundsRecord* rec) {
   static_assert(256 % ROWS == 0, "a CTA covers whole blocks");
   constexpr int BK = G::BK;
   constexpr int BLOCK = ROWS * G::ROW_BYTES;
@@ -179,10 +188,15 @@ __global__ void __launch_bounds__(256) pack_rc_kernel(const float* __restrict__ 
   __shared__ float tile[BK * TS];
   const int kt = blockIdx.x;
   const int n0 = blockIdx.y * 256;
+  // Checked builds: the source view (K rows of R) and the Rt x Kt blocks.
+  const int64_t src_extent = view_extent(K, R, ld);
+  const int64_t dst_words = static_cast<int64_t>(Rt) * Kt * (2 * BLOCK / 4);
 #pragma unroll 4
   for (int j = 0; j < BK; ++j) {
     const int k = kt * BK + j, n = n0 + threadIdx.x;
-    tile[j * TS + threadIdx.x] = (n < R && k < K) ? src[static_cast<int64_t>(k) * ld + n] : 0.f;
+    const int64_t o = static_cast<int64_t>(k) * ld + n;
+    tile[j * TS + threadIdx.x] =
+        (n < R && k < K && bounds_ok(rec, SITE_PREP_SRC, o, 1, src_extent)) ? src[o] : 0.f;
   }
   __syncthreads();
   for (int p = threadIdx.x; p < 256 * CPR; p += 256) {
@@ -198,8 +212,12 @@ __global__ void __launch_bounds__(256) pack_rc_kernel(const float* __restrict__ 
     char* dst = reinterpret_cast<char*>(dst_base) +
                 (static_cast<int64_t>(rt) * Kt + kt) * static_cast<int64_t>(2 * BLOCK);
     const uint32_t off = (r >> 3) * G::ATOM_BYTES + r8 * G::ROW_BYTES + pc * 16;
-    *reinterpret_cast<float4*>(dst + off) = big;
-    *reinterpret_cast<float4*>(dst + BLOCK + off) = small;
+    const int64_t w = (dst - reinterpret_cast<char*>(dst_base) + off) / 4;
+    if (bounds_ok(rec, SITE_PREP_DST, w, 4, dst_words) &&
+        bounds_ok(rec, SITE_PREP_DST, w + BLOCK / 4, 4, dst_words)) {
+      *reinterpret_cast<float4*>(dst + off) = big;
+      *reinterpret_cast<float4*>(dst + BLOCK + off) = small;
+    }
   }
 }
 
@@ -789,17 +807,17 @@ struct Cfg {
     // A: rows m, k contiguous unless stored transposed.
     if (a.trans_a)
       pack_rc_kernel<G, BM><<<dim3(kt, (mt * BM + 255) / 256), 256, 0, stream>>>(
-          a.A, a.lda, Ap, a.M, a.K, kt, mt);
+          a.A, a.lda, Ap, a.M, a.K, kt, mt, a.bounds);
     else
       pack_kc_kernel<G, BM><<<dim3(kt, mt), 256, 0, stream>>>(a.A, a.lda, Ap, a.M, a.K, kt,
-                                                              vec_a ? 1 : 0);
+                                                              vec_a ? 1 : 0, a.bounds);
     // B: rows n, n contiguous (row-major K x N) unless stored transposed.
     if (a.trans_b)
       pack_kc_kernel<G, BN><<<dim3(kt, nt), 256, 0, stream>>>(a.B, a.ldb, Bp, a.N, a.K, kt,
-                                                              vec_b ? 1 : 0);
+                                                              vec_b ? 1 : 0, a.bounds);
     else
       pack_rc_kernel<G, BN><<<dim3(kt, (nt * BN + 255) / 256), 256, 0, stream>>>(
-          a.B, a.ldb, Bp, a.N, a.K, kt, nt);
+          a.B, a.ldb, Bp, a.N, a.K, kt, nt, a.bounds);
     const int tiles = mt * nt;
     // Split tail: the partial tiles follow the packed operands.
     Sched sched{a.full_tiles, a.split, a.kt_per_slice, nullptr};
@@ -809,7 +827,7 @@ struct Cfg {
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int grid = units < max_ctas ? units : max_ctas;
     tf32x3_gemm_kernel<G><<<grid, THREADS, G::SMEM_BYTES, stream>>>(
-        Ap, Bp, Epilogue{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0, a.bias}, kt, mt, nt,
+        Ap, Bp, make_epilogue(a, vec_c, tiles, BM, BN), kt, mt, nt,
         a.group_m,
         sched, fault_inject);
     cudaError_t e = cudaGetLastError();
@@ -867,16 +885,16 @@ struct CfgPair {
                                          static_cast<int64_t>(2 * mt) * kt * G::PAIR_BYTES);
     if (a.trans_a)
       pack_rc_kernel<GP, ROWS><<<dim3(kt, (2 * mt * ROWS + 255) / 256), 256, 0, stream>>>(
-          a.A, a.lda, Ap, a.M, a.K, kt, 2 * mt);
+          a.A, a.lda, Ap, a.M, a.K, kt, 2 * mt, a.bounds);
     else
       pack_kc_kernel<GP, ROWS><<<dim3(kt, 2 * mt), 256, 0, stream>>>(a.A, a.lda, Ap, a.M, a.K,
-                                                                     kt, vec_a ? 1 : 0);
+                                                                     kt, vec_a ? 1 : 0, a.bounds);
     if (a.trans_b)
       pack_kc_kernel<GP, ROWS><<<dim3(kt, 2 * nt), 256, 0, stream>>>(a.B, a.ldb, Bp, a.N, a.K,
-                                                                     kt, vec_b ? 1 : 0);
+                                                                     kt, vec_b ? 1 : 0, a.bounds);
     else
       pack_rc_kernel<GP, ROWS><<<dim3(kt, (2 * nt * ROWS + 255) / 256), 256, 0, stream>>>(
-          a.B, a.ldb, Bp, a.N, a.K, kt, 2 * nt);
+          a.B, a.ldb, Bp, a.N, a.K, kt, 2 * nt, a.bounds);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // The packed buffers as 2-D tensors of 1 KB rows (256 floats, no
@@ -896,7 +914,7 @@ struct CfgPair {
                                                 CfgPair::workspace(a.M, a.N, a.K));
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int clusters = units < max_clusters ? units : max_clusters;
-    const Epilogue ep{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0, a.bias};
+    const Epilogue ep = make_epilogue(a, vec_c, tiles, PAIR_TILE, PAIR_TILE);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -943,10 +961,10 @@ struct CfgASplit {
     float* Bp = static_cast<float*>(workspace);
     if (a.trans_b)
       pack_kc_kernel<G, BN><<<dim3(kt, nt), 256, 0, stream>>>(a.B, a.ldb, Bp, a.N, a.K, kt,
-                                                              vec_b ? 1 : 0);
+                                                              vec_b ? 1 : 0, a.bounds);
     else
       pack_rc_kernel<G, BN><<<dim3(kt, (nt * BN + 255) / 256), 256, 0, stream>>>(
-          a.B, a.ldb, Bp, a.N, a.K, kt, nt);
+          a.B, a.ldb, Bp, a.N, a.K, kt, nt, a.bounds);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // A (M x K, row pitch lda) in 128 x BK boxes with the swizzle of the
@@ -963,7 +981,7 @@ struct CfgASplit {
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int grid = units < max_ctas ? units : max_ctas;
     tf32x3_asplit_kernel<BK, BN><<<grid, ASPLIT_THREADS, AG::SMEM_BYTES, stream>>>(
-        map_a, Bp, Epilogue{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0, a.bias}, kt,
+        map_a, Bp, make_epilogue(a, vec_c, tiles, BM, BN), kt,
         mt, nt, a.group_m, sched, fault_inject);
     e = cudaGetLastError();
     if (e != cudaSuccess || a.split <= 1) return e;

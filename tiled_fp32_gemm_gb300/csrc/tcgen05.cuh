@@ -359,7 +359,21 @@ struct Epilogue {
   int M, N;
   int vec_c;  // 16-byte stores of C allowed (N, ldc % 4 == 0, aligned base)
   const float* bias;  // N floats added to every row (nullptr: none)
+  // Elements of C's view and of the split tail's partial tiles, and the
+  // checked build's record (see bounds_ok).
+  int64_t c_extent = 0, partial_extent = 0;
+  BoundsRecord* bounds = nullptr;
 };
+
+// The epilogue of a call: C's view, and the split tail's partial tiles
+// (one dense tile_m x bn tile per slice of each split tile).
+inline Epilogue make_epilogue(const GemmArgs& a, bool vec_c, int tiles, int tile_m, int bn) {
+  Epilogue ep{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0, a.bias};
+  ep.c_extent = a.c_extent;
+  ep.partial_extent = static_cast<int64_t>(tiles - a.full_tiles) * a.split * tile_m * bn;
+  ep.bounds = a.bounds;
+  return ep;
+}
 
 // Drains this warp's 32 TMEM lanes — rows q*32 .. q*32+31 of the BM x BN
 // accumulator whose first column of this warp's lanes is TMEM address
@@ -386,15 +400,19 @@ __device__ __forceinline__ void store_accumulator(uint32_t t_row, const Unit& w,
                     (sub_row0 + q * 32 + lane) * BN + ch * 32;
 #pragma unroll
       for (int g4 = 0; g4 < 8; ++g4)
-        *reinterpret_cast<float4*>(prow + 4 * g4) =
-            make_float4(v[4 * g4], v[4 * g4 + 1], v[4 * g4 + 2], v[4 * g4 + 3]);
+        if (bounds_ok(ep.bounds, SITE_PARTIAL, (prow - partial) + 4 * g4, 4, ep.partial_extent))
+          *reinterpret_cast<float4*>(prow + 4 * g4) =
+              make_float4(v[4 * g4], v[4 * g4 + 1], v[4 * g4 + 2], v[4 * g4 + 3]);
     } else if (row < ep.M) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] *= ep.alpha;
       if (ep.vec_c) {
 #pragma unroll
         for (int g4 = 0; g4 < 8; ++g4)
-          if (col0 + 4 * g4 < ep.N) {
+          if (col0 + 4 * g4 < ep.N &&
+              bounds_ok(ep.bounds, SITE_C_STORE, (c_row - ep.C) + col0 + 4 * g4, 4,
+                        ep.c_extent) &&
+              (!ep.bias || bounds_ok(ep.bounds, SITE_BIAS, col0 + 4 * g4, 4, ep.N))) {
             float4* cp = reinterpret_cast<float4*>(c_row + col0 + 4 * g4);
             float4 o = make_float4(v[4 * g4], v[4 * g4 + 1], v[4 * g4 + 2], v[4 * g4 + 3]);
             if (ep.beta != 0.0f) {
@@ -414,7 +432,9 @@ __device__ __forceinline__ void store_accumulator(uint32_t t_row, const Unit& w,
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          if (col0 + i < ep.N) {
+          if (col0 + i < ep.N &&
+              bounds_ok(ep.bounds, SITE_C_STORE, (c_row - ep.C) + col0 + i, 1, ep.c_extent) &&
+              (!ep.bias || bounds_ok(ep.bounds, SITE_BIAS, col0 + i, 1, ep.N))) {
             float o = ep.beta != 0.0f ? fmaf(ep.beta, c_row[col0 + i], v[i]) : v[i];
             if (ep.bias) o += ep.bias[col0 + i];
             c_row[col0 + i] = o;
