@@ -616,10 +616,8 @@ mt_status plan_ffma(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   const int64_t tiles = static_cast<int64_t>(L->tiles_m) * L->tiles_n;
   if (tiles > INT32_MAX / 4) return MT_ERR_UNSUPPORTED;
   // Split-K: the tiles of the split part are cut along K into slices whose
-  // partial tiles add up in a second kernel (see GemmArgs).  Automatic
-  // splitting is off: on GB300 a partial last wave runs one CTA per SM at
-  // most of the two-CTA rate, and splitting it (or a small grid) measured
-  // no faster; an explicit split_k splits every tile.
+  // partial tiles add up in a second kernel (see GemmArgs).  An explicit
+  // split_k splits every tile; the automatic splits are below.
   const int64_t ktiles = ceil_div(K, E.bk);
   int64_t full = tiles, split = 1;
   if (cfg && cfg->split_k > 1) {
