@@ -289,10 +289,10 @@ def test_alignment_selects_staging_width():
     rnd = lambda b: (b + 255) // 256 * 256  # noqa: E731
     # Default: A staged K-major from a transposed copy (K x M) for a product
     # this wide, B and C with 16-byte accesses; the last partial wave (1024
-    # tiles on 2 x 152 CTA slots leave 112) is split in two K slices.
+    # tiles on 2 x 152 CTA slots leave 112) is split in four K slices.
     p = plan(4096, 4096, 4096)[1]
-    assert (p.vec_ab, p.vec_c, p.pack_a, p.split_k) == (1, 1, 5, 2)
-    assert p.workspace_bytes == 4096 * 4096 * 4 + 112 * 2 * 128 * 128 * 4
+    assert (p.vec_ab, p.vec_c, p.pack_a, p.split_k) == (1, 1, 5, 4)
+    assert p.workspace_bytes == 4096 * 4096 * 4 + 112 * 4 * 128 * 128 * 4
     # Row-major A tiles (pack_a = 2): rows that are not whole float4s are
     # staged as stored with 4-byte copies ...
     p = plan(4097, 3001, 2053, pack_a=2)[1]
@@ -306,11 +306,11 @@ def test_alignment_selects_staging_width():
     # Automatic: K-major A from a copy (2053 x 4100) and B from a copy with
     # padded rows, on 64 x 128 tiles (too few 128 x 128 tiles for three
     # full waves); 1560 tiles on 3 x 152 CTA slots leave 192 for a last
-    # wave, split in two K slices.
+    # wave, split in four K slices.
     p = plan(4097, 3001, 2053)[1]
-    assert (p.vec_ab, p.vec_c, p.pack_a, p.bm, p.bn, p.split_k) == (1, 0, 5, 64, 128, 2)
+    assert (p.vec_ab, p.vec_c, p.pack_a, p.bm, p.bn, p.split_k) == (1, 0, 5, 64, 128, 4)
     assert p.workspace_bytes == (rnd(2053 * 4100 * 4) + rnd(2053 * 3004 * 4) +
-                                 192 * 2 * 64 * 128 * 4)
+                                 192 * 4 * 64 * 128 * 4)
     # Small products gather K-major A inside the kernel: no copy.
     p = plan(100, 72, 81)[1]
     assert (p.pack_a, p.workspace_bytes, p.vec_ab) == (4, 0, 0)
@@ -352,14 +352,14 @@ def test_no_cpu_fallback_without_gpu():
 
 def test_split_k_plan():
     # Automatically only the last partial wave is split (112 of 1024 tiles
-    # on 304 CTA slots, two slices each); an explicit split applies to every
+    # on 304 CTA slots, four slices each); an explicit split applies to every
     # tile; each split tile needs one partial tile per slice (after the 64 MB
     # transposed copy of A); split_k = 1 turns splitting off.
     a_copy = 4096 * 4096 * 4
     st, p = plan(4096, 4096, 4096)
     assert st == mt.MT_OK and (p.bm, p.bn) == (128, 128)
-    assert p.split_k == 2 and p.grid == 912 + 112 * 2
-    assert p.workspace_bytes == a_copy + 112 * 2 * 128 * 128 * 4
+    assert p.split_k == 4 and p.grid == 912 + 112 * 4
+    assert p.workspace_bytes == a_copy + 112 * 4 * 128 * 128 * 4
     st, p = plan(4096, 4096, 4096, split_k=2)
     assert p.grid == 1024 * 2 and p.workspace_bytes == a_copy + 1024 * 2 * 128 * 128 * 4
     st, p = plan(4096, 4096, 4096, split_k=3)

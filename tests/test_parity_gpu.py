@@ -104,9 +104,9 @@ def test_ragged_workload_full():
     # copies.  Row-major A tiles from copies (pack_a = 1): A and B copied
     # into rows padded to whole float4s, then 16-byte chunks.  Automatically:
     # A staged K-major from a transposed copy, B from a padded copy, on
-    # 64 x 128 tiles, the last partial wave split in two K slices; and A
+    # 64 x 128 tiles, the last partial wave split in four K slices; and A
     # gathered K-major inside the kernel (pack_a = 4).  Without K slices all
-    # give the same FMA chain per output; the split tail adds two partial
+    # give the same FMA chain per output; the split tail adds four partial
     # sums, within the tolerance.
     A, B = gemm_inputs.make_workload("ragged_4097x3001x2053")
     a, b = A.cuda(), B.cuda()
@@ -114,7 +114,7 @@ def test_ragged_workload_full():
     assert mt.plan(4097, 3001, 2053, a=a, b=b, pack_a=1)["pack_a"] == 1
     p = mt.plan(4097, 3001, 2053, a=a, b=b)
     assert (p["vec_ab"], p["vec_c"], p["pack_a"], p["bm"], p["bn"]) == (1, 0, 5, 64, 128)
-    assert p["split_k"] == 2
+    assert p["split_k"] == 4
     Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
     as_stored = run(A, B, pack_a=2).numpy()
     assert_within(as_stored, Cref, W, FFMA_TOL, "ragged, as stored")

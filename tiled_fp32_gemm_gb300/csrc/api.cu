@@ -288,15 +288,16 @@ int pick_f16_bn(int64_t M, int64_t N, int sms) {
 // most half of the `ctas` CTAs, those tiles are cut into K slices that run
 // on the idle ones (at most 4, every slice non-empty and at least 2 K tiles
 // long) and are added by a second kernel.  Outputs the whole tiles and the
-// slice count (1: no split).
+// slice count (1: no split).  slices = 0: as many slices as fit the idle
+// CTAs (at most 4); else that many (fewer if K is short).
 void split_tail(int64_t tiles, int64_t ctas, int64_t ktiles, bool allowed, int64_t* full,
-                int64_t* split) {
+                int64_t* split, int slices = 0) {
   *full = tiles;
   *split = 1;
   if (!allowed || tiles <= ctas) return;
   const int64_t rem = tiles % ctas;
   if (rem == 0 || 2 * rem > ctas) return;
-  int64_t s = std::min<int64_t>(ctas / rem, 4);
+  int64_t s = slices > 0 ? slices : std::min<int64_t>(ctas / rem, 4);
   while (s > 1 && ((s - 1) * ceil_div(ktiles, s) >= ktiles || ktiles / s < 2)) --s;
   if (s > 1) {
     *full = tiles - rem;
@@ -638,7 +639,13 @@ mt_status plan_ffma(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
         split = sk;
       }
     } else if (L->a_kmajor) {
-      split_tail(tiles, n_sm * E.min_blocks, ktiles, true, &full, &split);
+      // Four slices, even when the idle CTAs would only take two at once:
+      // the slices then run as two short rounds that even out where the
+      // whole tiles ended.  Measured on GB300 (against as many slices as fit
+      // the idle CTAs): 4096^3 2052 -> 1984 us, 4097 x 3001 x 2053 854 ->
+      // 848 us; 8192^3, 2048 x 2048 x 8192 and 65536 x 128 x 4096 unchanged
+      // (three slices gained nothing at 4096^3, six less than four).
+      split_tail(tiles, n_sm * E.min_blocks, ktiles, true, &full, &split, 4);
     }
   }
   if (split <= 1) {
