@@ -253,6 +253,24 @@ NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25
 TF32_FLOP_PER_CLK_SM = 4096
 
 
+def device_record(dev: int) -> dict:
+    """The GPU, driver and software the run used."""
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    rec = {"name": props.name, "sms": props.multi_processor_count,
+           "compute_capability": f"{props.major}.{props.minor}",
+           "memory_gib": round(props.total_memory / 2 ** 30, 1),
+           "torch": torch.__version__, "torch_cuda": torch.version.cuda}
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(dev), "--query-gpu=driver_version",
+                              "--format=csv,noheader"], capture_output=True, text=True,
+                             timeout=20)
+        rec["driver"] = out.stdout.strip() or None
+    except (OSError, subprocess.SubprocessError):
+        rec["driver"] = None
+    return rec
+
+
 def tf32_clock_peak(sms: int, mhz: float) -> float:
     return sms * TF32_FLOP_PER_CLK_SM * mhz * 1e6 / 1e12
 
@@ -645,6 +663,7 @@ def run_gpu(args):
             "gpu_launches": sum(launches_per_call(p) for p in plans.values()) * args.steps,
             "variants": variants,
             "cpu_baseline": cpu,
+            "device": device_record(dev),
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -142,7 +142,13 @@ typedef struct {
 } mt_plan;
 
 /*
- * C = A*B on `stream` with the default variant and automatic tiling.
+ * C = A*B on `stream` with the default variant and automatic tiling.  The
+ * default variant of every fp32 call made without a configuration (cfg ==
+ * NULL here and in the _ex, general and host entry points) is FFMA, or the
+ * one the environment variable MT_SGEMM_VARIANT names when the call is
+ * made: "ffma", "tf32x3" or "p18" (unset or empty: "ffma"; any other value:
+ * MT_ERR_INVALID_ARG, nothing launched).  A configuration's variant field
+ * always wins.
  * A, B, C: device pointers, layouts above.  A and B may be NULL only when
  * the product has no element that reads them (M*K == 0 or K*N == 0).
  * Errors: MT_ERR_INVALID_ARG (size < 0 or > INT32_MAX per dimension,

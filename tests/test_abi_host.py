@@ -235,6 +235,22 @@ def test_ffma_unpadded_layout_conflicts(warp):
     assert q.pad_a == R.vector_row_padding(32, rows_per_phase) == 4
 
 
+def test_default_variant_from_the_environment(monkeypatch):
+    """Calls without a configuration take MT_SGEMM_VARIANT's variant; a
+    configuration wins; an unknown name is refused before any launch."""
+    for name, want in (("", mt.MT_VARIANT_FFMA), ("ffma", mt.MT_VARIANT_FFMA),
+                       ("tf32x3", mt.MT_VARIANT_TF32X3), ("p18", mt.MT_VARIANT_P18)):
+        monkeypatch.setenv("MT_SGEMM_VARIANT", name)
+        st, p = plan(300, 200, 100)
+        assert st == mt.MT_OK and p.variant == want, name
+        st, p = plan(300, 200, 100, variant="ffma", bm=128, bn=128)
+        assert st == mt.MT_OK and p.variant == mt.MT_VARIANT_FFMA
+    monkeypatch.setenv("MT_SGEMM_VARIANT", "cublas")
+    assert plan(300, 200, 100)[0] == mt.MT_ERR_INVALID_ARG
+    monkeypatch.delenv("MT_SGEMM_VARIANT")
+    assert plan(300, 200, 100)[1].variant == mt.MT_VARIANT_FFMA
+
+
 def test_p18_plan_follows_the_pages():
     st, p = plan(100, 72, 80, variant="p18")
     assert st == mt.MT_OK

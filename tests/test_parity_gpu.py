@@ -160,6 +160,23 @@ def test_integer_inputs_bit_exact(shape, cfg):
     assert np.array_equal(got, Cref)
 
 
+@pytest.mark.parametrize("name", ["tf32x3", "p18"])
+def test_environment_selects_the_default_variant(name, monkeypatch):
+    """mt_sgemm (no configuration) under MT_SGEMM_VARIANT gives the bits of
+    the explicitly chosen variant."""
+    A, B = gemm_inputs.make_workload("masked_100x72x80")
+    a, b = A.cuda(), B.cuda()
+    want = mt.sgemm(a, b, variant=name)
+    c = torch.full((100, 72), float("nan"), device="cuda")
+    monkeypatch.setenv("MT_SGEMM_VARIANT", name)
+    st = mt.mt_sgemm(a.data_ptr(), b.data_ptr(), c.data_ptr(), 100, 72, 80,
+                     torch.cuda.current_stream().cuda_stream)
+    monkeypatch.delenv("MT_SGEMM_VARIANT")
+    assert st == mt.MT_OK
+    torch.cuda.synchronize()
+    assert torch.equal(c, want)
+
+
 @pytest.mark.parametrize("cfg", [dict(), dict(variant="p18")], ids=["ffma", "p18"])
 def test_identity_and_permutation_exact(cfg):
     g = torch.Generator().manual_seed(5)

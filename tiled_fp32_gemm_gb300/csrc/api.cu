@@ -670,6 +670,16 @@ mt_status plan_ffma(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   return MT_OK;
 }
 
+// The fp32 variant of a call made without a configuration: MT_SGEMM_VARIANT
+// = "ffma" (or unset or empty), "tf32x3" or "p18"; -1 for any other value.
+int default_variant() {
+  const char* v = std::getenv("MT_SGEMM_VARIANT");
+  if (!v || !*v || std::strcmp(v, "ffma") == 0) return MT_VARIANT_FFMA;
+  if (std::strcmp(v, "tf32x3") == 0) return MT_VARIANT_TF32X3;
+  if (std::strcmp(v, "p18") == 0) return MT_VARIANT_P18;
+  return -1;
+}
+
 mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, int sms,
                     Launch* L, int dev = -1) {
   const int64_t M = P.M, N = P.N, K = P.K;
@@ -677,7 +687,8 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   if (st != MT_OK) return st;
   st = check_lds(P);
   if (st != MT_OK) return st;
-  const int variant = cfg ? cfg->variant : MT_VARIANT_FFMA;
+  const int variant = cfg ? cfg->variant : P.dtype ? MT_VARIANT_TC16 : default_variant();
+  if (variant < 0) return MT_ERR_INVALID_ARG;  // MT_SGEMM_VARIANT names no variant
   if (cfg && (cfg->bm < 0 || cfg->bn < 0 || cfg->bk < 0 || cfg->stages < 0 ||
               cfg->no_pad < 0 || cfg->no_pad > 1 || cfg->split_k < 0 || cfg->fma < 0 ||
               cfg->fma > 2 || cfg->fault_inject < 0 || cfg->fault_inject > 1 || cfg->wm < 0 ||
