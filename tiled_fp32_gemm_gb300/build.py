@@ -67,35 +67,53 @@ def _compile(src: str, obj: str, verbose: bool, defines=()) -> str:
     return r.stderr if verbose else ""
 
 
+def _variant(checked: bool):
+    """(object dir, library, extra nvcc flags) of the normal or checked build."""
+    if checked:
+        return CHECKED_BUILD, CHECKED_LIB, ["-DMT_BOUNDS_CHECK=1"]
+    return BUILD, LIB, []
+
+
+def build_many(variants, force: bool = False, verbose: bool = False):
+    """Compile the stale objects of every requested variant (False: normal,
+    True: checked) in one pool of nvcc processes, then link each library.
+    Returns the library paths in the order asked."""
+    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    headers = _headers()
+    jobs, plans = [], []
+    for checked in variants:
+        out_dir, lib, defines = _variant(checked)
+        os.makedirs(out_dir, exist_ok=True)
+        objects = []
+        for src in sources:
+            obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
+            objects.append(obj)
+            if force or _stale(obj, [src, *headers]):
+                jobs.append((src, obj, defines))
+        plans.append((lib, objects))
+    if jobs:
+        # The longest translation units first, so they overlap the rest.
+        jobs.sort(key=lambda j: -os.path.getsize(j[0]))
+        with ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
+            logs = list(ex.map(lambda j: _compile(j[0], j[1], verbose, j[2]), jobs))
+        if verbose:
+            for (src, obj, _), log in zip(jobs, logs):
+                print(f"== {os.path.relpath(obj, BUILD)}\n{log}", file=sys.stderr)
+    for lib, objects in plans:
+        if force or jobs or _stale(lib, objects):
+            tmp = lib + f".tmp{os.getpid()}"
+            cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objects, "-cudart", "static"]
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError(f"link failed:\n{r.stderr}")
+            os.replace(tmp, lib)
+    return [lib for lib, _ in plans]
+
+
 def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
     """Compile and link the library if anything changed; returns its path.
     checked=True: the bounds-checked build instead (see the module doc)."""
-    out_dir, lib = (CHECKED_BUILD, CHECKED_LIB) if checked else (BUILD, LIB)
-    defines = ["-DMT_BOUNDS_CHECK=1"] if checked else []
-    os.makedirs(out_dir, exist_ok=True)
-    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    headers = _headers()
-    jobs = []
-    objects = []
-    for src in sources:
-        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
-        objects.append(obj)
-        if force or _stale(obj, [src, *headers]):
-            jobs.append((src, obj))
-    if jobs:
-        with ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
-            logs = list(ex.map(lambda j: _compile(j[0], j[1], verbose, defines), jobs))
-        if verbose:
-            for (src, _), log in zip(jobs, logs):
-                print(f"== {os.path.basename(src)}\n{log}", file=sys.stderr)
-    if force or jobs or _stale(lib, objects):
-        tmp = lib + f".tmp{os.getpid()}"
-        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objects, "-cudart", "static"]
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            raise RuntimeError(f"link failed:\n{r.stderr}")
-        os.replace(tmp, lib)
-    return lib
+    return build_many([checked], force=force, verbose=verbose)[0]
 
 
 if __name__ == "__main__":
@@ -103,5 +121,9 @@ if __name__ == "__main__":
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true", help="print -Xptxas -v")
     ap.add_argument("--checked", action="store_true", help="the bounds-checked build")
+    ap.add_argument("--all", action="store_true", help="the normal and the checked build")
     a = ap.parse_args()
-    print(build(force=a.force, verbose=a.verbose, checked=a.checked))
+    if a.all:
+        print("\n".join(build_many([False, True], force=a.force, verbose=a.verbose)))
+    else:
+        print(build(force=a.force, verbose=a.verbose, checked=a.checked))
