@@ -112,6 +112,23 @@ SHAPES = [(1, 1, 1), (3, 5, 7), (9, 2, 16), (15, 17, 16), (16, 16, 17),
           (17, 15, 33), (31, 33, 9), (33, 31, 32), (2, 65, 5), (63, 3, 8)]
 
 
+def _grid_sample(count=24, seed=2024, max_macs=40000):
+    """A seeded sample of (M, N, K) from {1..9, 15, 16, 17, 31, 32, 33, 63,
+    65}^3 (each axis on both sides of the tile edges the kernels use), kept
+    small enough for exact rational sums."""
+    axis = [1, 2, 3, 4, 5, 6, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 65]
+    g = np.random.default_rng(seed)
+    out = []
+    while len(out) < count:
+        t = tuple(int(x) for x in g.choice(axis, 3))
+        if t not in out and t not in SHAPES and t[0] * t[1] * t[2] <= max_macs:
+            out.append(t)
+    return out
+
+
+SHAPES = SHAPES + _grid_sample()
+
+
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_brute_force_tiny(M, N, K):
     """Exact rational sum, rounded once, versus the oracle.

@@ -272,6 +272,14 @@ def test_split_k_integer_inputs_bit_exact():
 # --- edge cases ---------------------------------------------------------------------
 TINY = [(1, 1, 1), (1, 7, 3), (5, 1, 9), (3, 5, 7), (16, 16, 16), (17, 15, 33),
         (31, 33, 1), (33, 31, 32), (63, 65, 31), (129, 127, 64), (130, 258, 33)]
+# Plus a seeded sample of {1..9, 15, 16, 17, 31, 32, 33, 63, 65}^3: every axis
+# just under, on and just over the staging widths and tile edges.
+_AXIS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 65]
+_g = np.random.default_rng(77)
+while len(TINY) < 35:
+    _t = tuple(int(x) for x in _g.choice(_AXIS, 3))
+    if _t not in TINY:
+        TINY.append(_t)
 
 
 @pytest.mark.parametrize("shape", TINY)
