@@ -120,7 +120,10 @@ __host__ __device__ inline int64_t view_extent(int64_t rows, int64_t cols, int64
 
 // Sums the K-slice partials of the split tiles (in slice order, so the
 // result does not depend on scheduling) and writes them to C with the
-// edge masks.  One CTA per split tile.
+// edge masks (alpha, beta, bias applied).  bm*bn/4096 CTAs (at least one)
+// per split tile, launched as a programmatic dependent of the GEMM kernel
+// before it on `stream`.  A zero a.partial_extent is taken as one dense
+// bm x bn tile per slice of each split tile.
 cudaError_t launch_splitk_reduce(const GemmArgs& a, int bm, int bn, bool vec_c,
                                  cudaStream_t stream);
 

@@ -1,6 +1,8 @@
-// Registry of the FFMA tile configurations built into the library.  The
+// Registry of the FFMA tile configurations built into the library (the
 // kernels themselves are in sgemm_ffma.cuh; each ffma_tiles_*.cu instantiates
-// a few configurations (separate translation units build in parallel).
+// a few configurations, so the translation units build in parallel), and the
+// helper kernels of the path: the K-slice reduce (shared by every variant's
+// split tail), the C scaling of empty products, and the operand copy.
 #include <algorithm>
 
 #include "device_util.cuh"
