@@ -72,8 +72,8 @@ def _mutate(name, tmp_path):
         assert text.count(old) == 1, f"mutation site for {name} not unique"
         text = text.replace(old, new)
     if "M_" in new:  # the transposed index needs M inside oracle_row
-        text = text.replace("static void oracle_row(const float *A, const float *B, int64_t N, int64_t K,",
-                            "static int64_t M_ = 1;\nstatic void oracle_row(const float *A, const float *B, int64_t N, int64_t K,")
+        head = "static void oracle_row(const float *A, const float *B, int64_t N, int64_t K,"
+        text = text.replace(head, "static int64_t M_ = 1;\n" + head)
         text = text.replace("if (nrows == 0 || N == 0) return 0;",
                             "if (nrows == 0 || N == 0) return 0;\n    M_ = M;")
     src = tmp_path / f"{name}.c"

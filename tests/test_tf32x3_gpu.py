@@ -175,8 +175,8 @@ def test_guard_bands_and_canaries(offset):
     sentinel = -12345.0
     cbuf = torch.full((M * N + 2 * guard,), sentinel, device="cuda")
     a_d, b_d = abuf.cuda(), bbuf.cuda()
-    st = mt.mt_sgemm_ex(a_d.data_ptr() + 4 * (guard + offset), b_d.data_ptr() + 4 * (guard + offset),
-                        cbuf.data_ptr() + 4 * (guard + offset), M, N, K,
+    off = 4 * (guard + offset)
+    st = mt.mt_sgemm_ex(a_d.data_ptr() + off, b_d.data_ptr() + off, cbuf.data_ptr() + off, M, N, K,
                         torch.cuda.current_stream().cuda_stream, mt.make_config(**TF32))
     assert st == mt.MT_OK
     torch.cuda.synchronize()
