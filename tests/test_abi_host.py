@@ -73,6 +73,18 @@ def test_checked_build_exports_the_same_entry_points_and_says_so():
     assert st == (mt.MT_OK if HAS_GPU else mt.MT_ERR_NO_DEVICE)
 
 
+def test_binding_refuses_host_tensors():
+    """The torch wrappers hand only CUDA tensors to the library: a host
+    tensor is refused before any call (there is no CPU path)."""
+    import torch
+    a = torch.zeros(4, 3)
+    b = torch.zeros(3, 5)
+    for call in (lambda: mt.sgemm(a, b), lambda: mt.gemm(a, b),
+                 lambda: mt.gemm_mixed(a.to(torch.bfloat16), b.to(torch.bfloat16))):
+        with pytest.raises(TypeError):
+            call()
+
+
 def test_padding_rule_matches_pages_and_oracle():
     for c in (1, 2, 3, 4, 5, 7, 8, 12, 16, 17, 24, 31, 32, 33, 48, 64, 96, 128):
         for r in range(1, 33):

@@ -285,3 +285,19 @@ def test_bias_on_split_plans_and_empty_product(shape):
     out = mt.gemm(x, y, c0.clone(), beta=0.5, bias=bd2)
     torch.cuda.synchronize()
     assert torch.equal(out, 0.5 * c0 + bd2)
+
+
+def test_binding_refuses_operands_off_the_device():
+    """A host c (or bias) beside device operands is refused before any call:
+    its pointer would otherwise reach a kernel."""
+    a = torch.zeros((8, 4), device="cuda")
+    b = torch.zeros((4, 6), device="cuda")
+    with pytest.raises(TypeError):
+        mt.gemm(a, b, c=torch.zeros((8, 6)))
+    with pytest.raises((TypeError, ValueError)):
+        mt.gemm(a, b, bias=torch.zeros(6))
+    with pytest.raises(TypeError):
+        mt.sgemm(a, b, out=torch.zeros((8, 6)))
+    a16, b16 = a.to(torch.bfloat16), b.to(torch.bfloat16)
+    with pytest.raises(TypeError):
+        mt.gemm_mixed(a16, b16, c=torch.zeros((8, 6)))

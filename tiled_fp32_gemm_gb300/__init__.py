@@ -333,10 +333,21 @@ def mt_version() -> int:
 
 
 # --- torch convenience (marshalling only) ------------------------------------
-def _check_tensor(t, name):
+def _check_device(t, name, device):
+    """t must live on `device` (every operand of a call on one GPU): a host
+    or other-GPU pointer handed to a kernel would read the wrong memory."""
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the other operands on {device}")
+
+
+def _check_tensor(t, name, device=None):
     import torch
     if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda:
         raise TypeError(f"{name} must be a float32 CUDA tensor")
+    _check_device(t, name, device)
     if t.dim() != 2 or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous 2-D (row-major) tensor")
 
@@ -345,7 +356,7 @@ def sgemm(a, b, out=None, stream=None, **choices):
     """out = a @ b through mt_sgemm_ex on torch tensors (float32, CUDA, row-major)."""
     import torch
     _check_tensor(a, "a")
-    _check_tensor(b, "b")
+    _check_tensor(b, "b", a.device)
     M, K = a.shape
     K2, N = b.shape
     if K != K2:
@@ -353,7 +364,7 @@ def sgemm(a, b, out=None, stream=None, **choices):
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=a.device)
     else:
-        _check_tensor(out, "out")
+        _check_tensor(out, "out", a.device)
         if tuple(out.shape) != (M, N):
             raise ValueError("out has the wrong shape")
     s = stream if stream is not None else torch.cuda.current_stream(a.device).cuda_stream
@@ -387,6 +398,7 @@ def gemm(a, b, c=None, alpha=1.0, beta=0.0, trans_a=False, trans_b=False, stream
     for t, name in ((a, "a"), (b, "b")):
         if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda:
             raise TypeError(f"{name} must be a float32 CUDA tensor")
+        _check_device(t, name, a.device)
         if t.dim() != 2 or t.stride(1) != 1:
             raise ValueError(f"{name} must be 2-D with unit column stride")
     M, K = (a.shape[1], a.shape[0]) if trans_a else (a.shape[0], a.shape[1])
@@ -397,6 +409,9 @@ def gemm(a, b, c=None, alpha=1.0, beta=0.0, trans_a=False, trans_b=False, stream
         if beta != 0.0:
             raise ValueError("beta != 0 needs c")
         c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    if not isinstance(c, torch.Tensor) or c.dtype != torch.float32:
+        raise TypeError("c must be a float32 CUDA tensor")
+    _check_device(c, "c", a.device)
     if c.dim() != 2 or c.stride(1) != 1 or tuple(c.shape) != (M, N):
         raise ValueError("c must be M x N with unit column stride")
     def ld(t):  # row stride; any value >= the row length works for one row
@@ -407,6 +422,7 @@ def gemm(a, b, c=None, alpha=1.0, beta=0.0, trans_a=False, trans_b=False, stream
                 not bias.is_cuda or bias.dim() != 1 or bias.shape[0] != N or
                 not bias.is_contiguous()):
             raise ValueError("bias must be a contiguous float32 CUDA vector of N")
+        _check_device(bias, "bias", a.device)
     s = stream if stream is not None else torch.cuda.current_stream(a.device).cuda_stream
     cfg = make_config(**choices) if choices else None
     with torch.cuda.device(a.device):
@@ -440,8 +456,7 @@ def gemm_mixed(a, b, c=None, alpha=1.0, beta=0.0, trans_a=False, trans_b=False, 
     when not given; then beta must be 0)."""
     import torch
     for t, name in ((a, "a"), (b, "b")):
-        if not isinstance(t, torch.Tensor) or not t.is_cuda:
-            raise TypeError(f"{name} must be a CUDA tensor")
+        _check_device(t, name, a.device if isinstance(a, torch.Tensor) else None)
         if t.dim() != 2 or t.stride(1) != 1:
             raise ValueError(f"{name} must be 2-D with unit column stride")
     code = _dtype_code(a)
@@ -455,7 +470,10 @@ def gemm_mixed(a, b, c=None, alpha=1.0, beta=0.0, trans_a=False, trans_b=False, 
         if beta != 0.0:
             raise ValueError("beta != 0 needs c")
         c = torch.empty((M, N), dtype=torch.float32, device=a.device)
-    if c.dtype != torch.float32 or c.dim() != 2 or c.stride(1) != 1 or tuple(c.shape) != (M, N):
+    if not isinstance(c, torch.Tensor) or c.dtype != torch.float32:
+        raise TypeError("c must be a float32 CUDA tensor")
+    _check_device(c, "c", a.device)
+    if c.dim() != 2 or c.stride(1) != 1 or tuple(c.shape) != (M, N):
         raise ValueError("c must be float32, M x N, with unit column stride")
 
     def ld(t):  # row stride; any value >= the row length works for one row
@@ -466,6 +484,7 @@ def gemm_mixed(a, b, c=None, alpha=1.0, beta=0.0, trans_a=False, trans_b=False, 
                 not bias.is_cuda or bias.dim() != 1 or bias.shape[0] != N or
                 not bias.is_contiguous()):
             raise ValueError("bias must be a contiguous float32 CUDA vector of N")
+        _check_device(bias, "bias", a.device)
     s = stream if stream is not None else torch.cuda.current_stream(a.device).cuda_stream
     cfg = make_config(**choices) if choices else None
     with torch.cuda.device(a.device):
