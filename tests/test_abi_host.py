@@ -73,6 +73,52 @@ def test_checked_build_exports_the_same_entry_points_and_says_so():
     assert st == (mt.MT_OK if HAS_GPU else mt.MT_ERR_NO_DEVICE)
 
 
+C_PROGRAM = r"""
+#include <stdio.h>
+#include "mt_sgemm.h"
+
+int main(void) {
+    mt_smem_layout l;
+    mt_plan p;
+    mt_config c = {0};
+    if (mt_smem_row_padding(16, 4) != 1 || mt_smem_row_padding(16, 2) != 0) return 1;
+    if (mt_smem_layout_make(4, 16, 1, 2, &l) != MT_OK || l.row_stride != 17) return 2;
+    if (mt_smem_layout_offset(&l, 1, 2, 3) != 1 * 68 + 2 * 17 + 3) return 3;
+    c.variant = MT_VARIANT_P18;
+    if (mt_sgemm_plan(NULL, NULL, NULL, 100, 72, 80, &c, 48 * 1024, &p) != MT_OK) return 4;
+    if (p.bm != 4 || p.bn != 8 || p.bk != 16 || p.pad_a != 1) return 5;
+    if (mt_sgemm_plan(NULL, NULL, NULL, -1, 4, 4, NULL, 48 * 1024, &p) != MT_ERR_INVALID_ARG)
+        return 6;
+    printf("%s|%d\n", mt_status_string(MT_ERR_SMEM_BUDGET), mt_version());
+    return 0;
+}
+"""
+
+
+def test_header_is_c_and_the_library_links_from_c(tmp_path):
+    """A C99 program includes include/mt_sgemm.h, links libmtsgemm.so and
+    calls its host-only entry points (padding rule, layout, plan, status
+    names): the boundary works from plain C, no C++ or torch involved."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if not cc:
+        pytest.skip("no C compiler")
+    cuda_inc = os.path.join(os.path.dirname(os.path.dirname(mt_build.nvcc())), "include")
+    src = tmp_path / "use_abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "use_abi"
+    lib_dir = os.path.dirname(mt.LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        "-I", cuda_inc, str(src), "-o", str(exe), "-L", lib_dir, "-lmtsgemm",
+                        f"-Wl,-rpath,{lib_dir}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, (r.returncode, r.stderr)
+    name, version = r.stdout.strip().split("|")
+    assert name == "shared-memory budget exceeded" and int(version) == mt.mt_version()
+
+
 def test_binding_refuses_host_tensors():
     """The torch wrappers hand only CUDA tensors to the library: a host
     tensor is refused before any call (there is no CPU path)."""
