@@ -95,22 +95,26 @@ int main(void) {
 """
 
 
-def test_header_is_c_and_the_library_links_from_c(tmp_path):
-    """A C99 program includes include/mt_sgemm.h, links libmtsgemm.so and
-    calls its host-only entry points (padding rule, layout, plan, status
-    names): the boundary works from plain C, no C++ or torch involved."""
+@pytest.mark.parametrize("checked", [False, True], ids=["normal", "checked"])
+def test_header_is_c_and_the_library_links_from_c(tmp_path, checked):
+    """A C99 program includes include/mt_sgemm.h, links the library (or its
+    bounds-checked build) and calls its host-only entry points (padding
+    rule, layout, plan, status names): the boundary works from plain C, no
+    C++ or torch involved."""
     import shutil
     import subprocess
     cc = shutil.which("gcc") or shutil.which("cc")
     if not cc:
         pytest.skip("no C compiler")
+    lib_path = mt_build.build(checked=checked)
     cuda_inc = os.path.join(os.path.dirname(os.path.dirname(mt_build.nvcc())), "include")
     src = tmp_path / "use_abi.c"
     src.write_text(C_PROGRAM)
     exe = tmp_path / "use_abi"
-    lib_dir = os.path.dirname(mt.LIB_PATH)
+    lib_dir = os.path.dirname(lib_path)
+    lib_name = os.path.basename(lib_path)[3:-3]  # libX.so -> X
     r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
-                        "-I", cuda_inc, str(src), "-o", str(exe), "-L", lib_dir, "-lmtsgemm",
+                        "-I", cuda_inc, str(src), "-o", str(exe), "-L", lib_dir, f"-l{lib_name}",
                         f"-Wl,-rpath,{lib_dir}"], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
