@@ -1,10 +1,10 @@
 """Plants plausible mistakes in a copy of the oracle and checks the pins catch them.
 
 Each mutant is a one-line edit of a private copy of ``oracle/ref_gemm.c``
-(the committed oracle is untouched), built with the oracle's own flags and
-run against ``test_oracle_pins.py`` in a child process, so a mutant that
-reads out of bounds cannot take the test run down with it.  Every mutant
-must make the pins fail.
+(built with the oracle's own flags) or of ``oracle/smem_rules.py`` (the
+committed oracle is untouched), run against ``test_oracle_pins.py`` in a
+child process, so a mutant that reads out of bounds cannot take the test run
+down with it.  Every mutant must make the pins fail.
 """
 import os
 import subprocess
@@ -16,6 +16,7 @@ import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "ref_gemm.c")
+RULES = os.path.join(ROOT, "oracle", "smem_rules.py")
 
 MUTANTS = {
     "dropped_last_k_term": (
@@ -59,6 +60,33 @@ MUTANTS = {
 }
 
 
+# One-line slips in the shared-memory rules and the bank simulator.
+RULE_MUTANTS = {
+    "vector_rule_counts_words_not_slots": (
+        "distinct = slots // math.gcd(columns // vector_words, slots)",
+        "distinct = slots // math.gcd(columns, slots)"),
+    "eight_byte_access_in_32_lane_phases": (
+        "per_phase = min(32, 128 // width_bytes)\n    total = 0",
+        "per_phase = 32 if width_bytes <= 8 else 128 // width_bytes\n    total = 0"),
+    "broadcast_not_honoured": (
+        "words_in_bank.setdefault(bank(word), set()).add(word)",
+        "words_in_bank.setdefault(bank(word), []).append(word)"),
+    "padding_rule_not_strict": (
+        "return int(simultaneous_rows > distinct_banks(columns))",
+        "return int(simultaneous_rows >= distinct_banks(columns))"),
+    "bank_of_word_modulo_16": ("return word_offset % NUM_BANKS",
+                               "return word_offset % 16"),
+}
+
+
+def _run_pins(env):
+    return subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p",
+                           "no:cacheprovider",
+                           os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                          cwd=ROOT, env=env, capture_output=True, text=True,
+                          timeout=600)
+
+
 def _mutate(name, tmp_path):
     old, new, *which = MUTANTS[name]
     text = open(SRC).read()
@@ -93,12 +121,27 @@ def test_pins_catch_mutant(name, tmp_path):
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
 
 
+@pytest.mark.parametrize("name", sorted(RULE_MUTANTS))
+def test_pins_catch_rule_mutant(name, tmp_path):
+    old, new = RULE_MUTANTS[name]
+    text = open(RULES).read()
+    assert text.count(old) == 1, f"mutation site for {name} not unique"
+    src = tmp_path / f"rules_{name}.py"
+    src.write_text(text.replace(old, new))
+    r = _run_pins(dict(os.environ, MT_ORACLE_RULES=str(src)))
+    # A failed pin, not a copy that does not even load.
+    assert r.returncode == 1 and " failed" in r.stdout, r.stdout[-2000:]
+
+
 def test_unmutated_copy_passes(tmp_path):
     # Control: the same procedure without an edit must pass.
     src = tmp_path / "same.c"
     src.write_text(open(SRC).read())
     lib = oracle.build(force=True, src=str(src), out=str(tmp_path / "libsame.so"))
-    env = dict(os.environ, MT_ORACLE_LIB=lib, OMP_NUM_THREADS="2")
+    rules = tmp_path / "rules_same.py"
+    rules.write_text(open(RULES).read())
+    env = dict(os.environ, MT_ORACLE_LIB=lib, MT_ORACLE_RULES=str(rules),
+               OMP_NUM_THREADS="2")
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p",
                         "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],

@@ -5,12 +5,15 @@ a wrong sign, a wrong index or leading dimension, a transposed operand,
 fp32 instead of fp64 accumulation) fails at least one of them;
 ``test_oracle_mutants.py`` plants such slips and confirms it.
 
-Setting MT_ORACLE_LIB runs these pins against another build of the oracle
-(the mutant test uses that).
+Setting MT_ORACLE_LIB runs these pins against another build of the oracle,
+and MT_ORACLE_RULES against another copy of ``oracle/smem_rules.py`` (the
+mutant test uses both).
 """
+import importlib.util
 import json
 import math
 import os
+import sys
 from fractions import Fraction
 
 import numpy as np
@@ -18,6 +21,13 @@ import pytest
 
 import oracle
 from oracle import smem_rules as R
+
+if os.environ.get("MT_ORACLE_RULES"):
+    _spec = importlib.util.spec_from_file_location("mt_rules_under_test",
+                                                   os.environ["MT_ORACLE_RULES"])
+    R = importlib.util.module_from_spec(_spec)
+    sys.modules[_spec.name] = R  # dataclasses resolve the module by name
+    _spec.loader.exec_module(R)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 LIB = oracle.load(os.environ.get("MT_ORACLE_LIB") or None)
@@ -274,13 +284,82 @@ def test_budget_formula():
     assert R.fits_budget(limit, limit) and not R.fits_budget(limit + 1, limit)
 
 
-def test_vector_rule_reduces_to_scalar_rule_on_slots():
-    # Our float4 reading counts 16-byte slots: a row of 4*c words is c slots,
-    # 8 slots in all; it must agree with the scalar rule on a 8-bank machine.
-    for cols in (4, 8, 12, 16, 20, 32, 36, 64):
-        for rows in (1, 2, 4, 8):
-            slots = 8 // math.gcd(cols // 4, 8)
-            assert R.vector_row_padding(cols, rows) == 4 * int(rows > slots)
+def _column_read(row_stride_words, rows, lanes_per_phase, column=0):
+    """Byte addresses of one warp reading word `column` of `rows` distinct rows.
+
+    Lane l of each phase reads row l % rows; lanes that share a row read the
+    same address (a broadcast).  Every phase repeats the pattern."""
+    return [4 * ((lane % lanes_per_phase % rows) * row_stride_words + column)
+            for lane in range(32)]
+
+
+def test_scalar_rule_agrees_with_the_simulator():
+    # The Part 18 rule against first principles: for every row width and
+    # count of rows read at once, the padded layout serves a column read in
+    # one transaction per phase, and whenever the rule asks for padding the
+    # unpadded layout does not.
+    for cols in range(1, 129):
+        for rows in range(1, 33):
+            pad = R.row_padding(cols, rows)
+            assert R.conflict_degree(_column_read(cols + pad, rows, 32), 4) == 1, \
+                (cols, rows)
+            if pad:
+                assert R.conflict_degree(_column_read(cols, rows, 32), 4) > 1
+            else:
+                # No padding where none is needed: the rule is not just "always pad".
+                assert R.conflict_degree(_column_read(cols, rows, 32), 4) == 1
+
+
+def test_vector_rule_agrees_with_the_simulator():
+    # Our float4 reading of the rule, checked the same way: float4 reads are
+    # served 8 lanes at a time, so up to 8 distinct rows share a phase.  The
+    # column is any 16-byte aligned one; padding keeps every row 16-byte aligned.
+    for cols in range(4, 257, 4):
+        for rows in range(1, 9):
+            pad = R.vector_row_padding(cols, rows)
+            assert pad in (0, 4) and (cols + pad) % 4 == 0
+            for column in (0, 4, cols - 4):
+                padded = _column_read(cols + pad, rows, 8, column)
+                assert R.conflict_degree(padded, 16) == 1, (cols, rows, column)
+                plain = _column_read(cols, rows, 8, column)
+                if pad:
+                    assert R.conflict_degree(plain, 16) > 1, (cols, rows)
+                else:
+                    assert R.conflict_degree(plain, 16) == 1, (cols, rows)
+    with pytest.raises(ValueError):
+        R.vector_row_padding(6, 2)
+
+
+def test_simulator_wide_access_phases():
+    # Skills page, bank-analysis steps, with the phase sizes this oracle
+    # reads for wide accesses: 8-byte accesses in two phases of 16 lanes,
+    # 16-byte accesses in four phases of 8 lanes (each phase moves at most
+    # 128 bytes through the 32 four-byte banks).
+    # Consecutive 8-byte words: each half-warp covers the 32 banks once.
+    consecutive8 = [8 * t for t in range(32)]
+    assert R.wavefronts(consecutive8, 8) == R.ideal_wavefronts(consecutive8, 8) == 2
+    assert R.conflict_degree(consecutive8, 8) == 1
+    # A stride of 32 words: the 16 lanes of a phase all land in banks 0 and 1.
+    stride32 = [128 * t for t in range(32)]
+    assert R.conflict_degree(stride32, 8) == 16
+    assert R.wavefronts(stride32, 8) == 32
+    # A stride of 32 words read as float4: 8 lanes per phase in banks 0..3.
+    assert R.conflict_degree(stride32, 16) == 8
+    assert R.wavefronts(stride32, 16) == 32
+    # Both half-warps on the same 128 bytes: each phase is served on its own,
+    # so the repeat is a second transaction, not a broadcast.
+    repeat8 = [8 * (t % 16) for t in range(32)]
+    assert R.wavefronts(repeat8, 8) == 2
+    # First half-warp strided (16 words in bank 0), second consecutive: the
+    # phases cost 16 and 1; served as one they would cost 16.
+    mixed8 = [128 * t for t in range(16)] + [8 * t for t in range(16)]
+    assert R.wavefronts(mixed8, 8) == 17
+    # Inactive lanes cost nothing; a phase with no active lane costs nothing.
+    assert R.wavefronts([None] * 16 + [8 * t for t in range(16)], 8) == 1
+    assert R.wavefronts([None] * 32, 16) == 0
+    # Misaligned wide addresses are refused.
+    with pytest.raises(ValueError):
+        R.wavefronts([4] + [0] * 31, 8)
 
 
 # --- the general form: leading dimensions, transposes, alpha and beta --------
