@@ -89,8 +89,8 @@ typedef struct {
     int fault_inject; /* test hook, 0 = off.  1 (MT_VARIANT_TF32X3 and the
                          mt_gemm_mixed* kernel only): the copy thread issues
                          nothing, so every wait on its data runs out; the call
-                         then leaves C unwritten and the next mt_device_status
-                         returns MT_ERR_TIMEOUT. */
+                         then leaves C unwritten and the next
+                         mt_check_device_status returns MT_ERR_TIMEOUT. */
     int wm;        /* FFMA warp tile rows; 0 = automatic */
     int wn;        /* FFMA warp tile columns; 0 = automatic */
     int tm;        /* FFMA outputs per thread along M; 0 = automatic */
@@ -159,7 +159,12 @@ MT_API mt_status mt_sgemm(const float *A, const float *B, float *C,
                    int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
 /* As mt_sgemm, with explicit choices (cfg == NULL: same as mt_sgemm).
- * A choice the library was not built for returns MT_ERR_UNSUPPORTED. */
+ * A choice the library was not built for returns MT_ERR_UNSUPPORTED.
+ * The product is the one cited for mt_sgemm; the choices themselves have no
+ * counterpart on the pages, whose compiler picks one tile (BM = 4, BN = 8,
+ * BK = 16 in "My Triton From Scratch, Part 14: Shared Memory Tiles",
+ * section "Shared buffers are physical storage") and two stages ("Part 18",
+ * section "One stage versus two stages"). */
 MT_API mt_status mt_sgemm_ex(const float *A, const float *B, float *C,
                       int64_t M, int64_t N, int64_t K, cudaStream_t stream,
                       const mt_config *cfg);
@@ -328,7 +333,9 @@ MT_API mt_status mt_gemm_mixed(int dtype, const void *A, const void *B, float *C
                                int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
 /* The launch mt_gemm_mixed_general would make for these arguments, as
- * mt_sgemm_plan (pointers inspected for alignment only, may be NULL). */
+ * mt_sgemm_plan (pointers inspected for alignment only, may be NULL).  No
+ * counterpart on the pages beyond the budget check cited for
+ * mt_sgemm_plan. */
 MT_API mt_status mt_gemm_mixed_plan(int dtype, int trans_a, int trans_b, int64_t M,
                                     int64_t N, int64_t K, const void *A, int64_t lda,
                                     const void *B, int64_t ldb, const float *C, int64_t ldc,
@@ -336,7 +343,9 @@ MT_API mt_status mt_gemm_mixed_plan(int dtype, int trans_a, int trans_b, int64_t
                                     mt_plan *out);
 
 /* The launch mt_sgemm_general would make for these arguments, as
- * mt_sgemm_plan (pointers inspected for alignment only, may be NULL). */
+ * mt_sgemm_plan (pointers inspected for alignment only, may be NULL).  No
+ * counterpart on the pages beyond the budget check cited for
+ * mt_sgemm_plan. */
 MT_API mt_status mt_sgemm_general_plan(int trans_a, int trans_b, int64_t M, int64_t N,
                                        int64_t K, const float *A, int64_t lda,
                                        const float *B, int64_t ldb, const float *C,
@@ -349,7 +358,11 @@ MT_API mt_status mt_sgemm_general_plan(int trans_a, int trans_b, int64_t M, int6
  * alignment (they may be NULL, which counts as aligned).  smem_limit_bytes
  * is the per-CTA dynamic shared-memory limit to check against; <= 0 asks
  * the current device (MT_ERR_NO_DEVICE without one).  Returns the status the
- * call itself would return for these sizes and choices.
+ * call itself would return for these sizes and choices.  The pages check the
+ * staged tiles' bytes against the device limit before a kernel is emitted
+ * ("My Triton From Scratch, Part 18", section "Shared-memory budget checks
+ * include stages and padding"; Part 14, section "Tracking the shared-memory
+ * budget"); this is that check, plus the rest of the launch, made visible.
  */
 MT_API mt_status mt_sgemm_plan(const float *A, const float *B, const float *C,
                         int64_t M, int64_t N, int64_t K, const mt_config *cfg,
@@ -398,8 +411,18 @@ MT_API int64_t mt_smem_layout_offset(const mt_smem_layout *layout, int stage, in
 /*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device: MT_ERR_TIMEOUT if a kernel gave up a bounded wait since
- * the last check, MT_ERR_CUDA if the synchronisation failed, else MT_OK.
+ * the last check, MT_ERR_CUDA if the synchronisation failed,
+ * MT_ERR_NO_DEVICE without a usable device, else MT_OK.
+ * No counterpart on the pages: their kernels never wait on a flag, and an
+ * error of theirs surfaces at the caller's next synchronisation.  The
+ * tensor-core kernels here wait on mbarriers with an iteration limit, and
+ * this call is how a caller learns that a limit ran out.  Thread-safe; the
+ * status word is per device and shared by every stream on it, so a check
+ * clears what work on any stream of the device recorded.
  */
+MT_API mt_status mt_check_device_status(cudaStream_t stream);
+
+/* The same call under its earlier name (kept for existing callers). */
 MT_API mt_status mt_device_status(cudaStream_t stream);
 
 /*
@@ -411,7 +434,10 @@ MT_API mt_status mt_device_status(cudaStream_t stream);
  * read gives 0, a store is dropped), so a checked kernel never touches
  * memory outside its buffers, and it is counted.  This stands in for a
  * memory checker where none can run; it is for tests and is slower than the
- * normal build.  Sites of the first access found outside:
+ * normal build.  No counterpart on the pages: they validate shared-memory
+ * budgets before emitting a kernel ("My Triton From Scratch, Part 18",
+ * section "Shared-memory budget checks include stages and padding") but
+ * check no access at run time.  Sites of the first access found outside:
  */
 typedef enum {
     MT_SITE_A_LOAD = 1,     /* global read of A by the staging copies */
@@ -438,10 +464,11 @@ typedef enum {
  */
 MT_API mt_status mt_bounds_status(int64_t *count, int *site, int64_t *offset, int64_t *extent);
 
-/* Static English name of a status code. */
+/* Static English name of a status code.  No counterpart on the pages. */
 MT_API const char *mt_status_string(mt_status status);
 
-/* Library version: major*10000 + minor*100 + patch. */
+/* Library version: major*10000 + minor*100 + patch.  No counterpart on the
+ * pages. */
 MT_API int mt_version(void);
 
 #ifdef __cplusplus

@@ -213,9 +213,13 @@ def test_timeout_path_reports_and_context_survives(tile):
     a, b = A.cuda(), B.cuda()
     c = torch.full((100, 72), 7.0, device="cuda")
     mt.sgemm(a, b, out=c, variant="tf32x3", fault_inject=1, **tile)
-    assert mt.mt_device_status(0) == mt.MT_ERR_TIMEOUT
+    assert mt.mt_check_device_status(0) == mt.MT_ERR_TIMEOUT
     assert torch.all(c == 7.0)  # nothing written
-    assert mt.mt_device_status(0) == mt.MT_OK  # the status word was cleared
+    assert mt.mt_check_device_status(0) == mt.MT_OK  # the status word was cleared
+    # The earlier name is the same call: a second timeout shows through it.
+    mt.sgemm(a, b, out=c, variant="tf32x3", fault_inject=1, **tile)
+    assert mt.mt_device_status(0) == mt.MT_ERR_TIMEOUT
+    assert mt.mt_check_device_status(0) == mt.MT_OK
     Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
     assert_within(run(A, B, **TF32).numpy(), Cref, W, TOL, "after timeout")
     assert mt.mt_device_status(0) == mt.MT_OK

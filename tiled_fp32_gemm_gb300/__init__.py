@@ -10,7 +10,8 @@ by ``tiled_fp32_gemm_gb300.build``).  This module only marshals arguments:
   ``mt_gemm_mixed_general``, ``mt_gemm_mixed_general_bias``,
   ``mt_gemm_mixed_plan``,
   ``mt_smem_row_padding``, ``mt_smem_vector_row_padding``,
-  ``mt_smem_layout_make``, ``mt_smem_layout_offset``, ``mt_device_status``,
+  ``mt_smem_layout_make``, ``mt_smem_layout_offset``, ``mt_check_device_status``
+  (also under its earlier name ``mt_device_status``),
   ``mt_bounds_status``,
   ``mt_status_string``, ``mt_version`` — the C entry points under the same
   names, taking plain integers for pointers and streams;
@@ -126,6 +127,7 @@ SIGNATURES = {
     "mt_smem_vector_row_padding": (_I, [_I, _I]),
     "mt_smem_layout_make": (_I, [_I, _I, _I, _I, ctypes.POINTER(mt_smem_layout)]),
     "mt_smem_layout_offset": (_I64, [ctypes.POINTER(mt_smem_layout), _I, _I, _I]),
+    "mt_check_device_status": (_I, [_P]),
     "mt_device_status": (_I, [_P]),
     "mt_bounds_status": (_I, [ctypes.POINTER(_I64), ctypes.POINTER(_I), ctypes.POINTER(_I64),
                               ctypes.POINTER(_I64)]),
@@ -318,6 +320,10 @@ def mt_smem_layout_make(rows: int, columns: int, row_padding: int, stage_count: 
 
 def mt_smem_layout_offset(layout: mt_smem_layout, stage: int, row: int, column: int) -> int:
     return lib().mt_smem_layout_offset(ctypes.byref(layout), stage, row, column)
+
+
+def mt_check_device_status(stream: int = 0) -> int:
+    return lib().mt_check_device_status(stream)
 
 
 def mt_device_status(stream: int = 0) -> int:

@@ -1405,7 +1405,10 @@ mt_status mt_bounds_status(int64_t* count, int* site, int64_t* offset, int64_t* 
 #endif
 }
 
-mt_status mt_device_status(cudaStream_t stream) {
+mt_status mt_check_device_status(cudaStream_t stream) {
+  int dev = -1;
+  DeviceInfo info;
+  if (current_device(&dev, &info) != MT_OK) return MT_ERR_NO_DEVICE;
   if (cudaStreamSynchronize(stream) != cudaSuccess) {
     cudaGetLastError();
     return MT_ERR_CUDA;
@@ -1419,6 +1422,8 @@ mt_status mt_device_status(cudaStream_t stream) {
   flags |= flags16;
   return flags ? MT_ERR_TIMEOUT : MT_OK;
 }
+
+mt_status mt_device_status(cudaStream_t stream) { return mt_check_device_status(stream); }
 
 const char* mt_status_string(mt_status status) {
   switch (status) {
