@@ -263,11 +263,15 @@ MT_API mt_status mt_sgemm_host_async(const float *A, const float *B, float *C,
  * packed copies of A and B that variant builds go to a static device array
  * of MT_NOALLOC_SCRATCH_BYTES (32 MiB) instead of memory allocated per call;
  * this call allocates nothing.  A problem needs the workspace_bytes that
- * mt_sgemm_plan reports for MT_VARIANT_TF32X3: the packed copies of A and B,
- * about 8*(M + N)*K bytes (square problems up to about 1448^3), or of B
- * alone, about 8*N*K, when A is split inside the GEMM kernel (N <= 512 and A
- * 16-byte aligned); a larger problem returns MT_ERR_SCRATCH_LIMIT and
- * launches nothing.  Other errors as mt_sgemm_ex.
+ * mt_sgemm_plan reports for MT_VARIANT_TF32X3 (with the same A, B and C, as
+ * the plan depends on their alignment); that figure is the exact test.  It
+ * holds the packed big and small copies of B, about 8*N*K bytes, and of A,
+ * about 8*M*K more, unless A is split inside the GEMM kernel (A row-major,
+ * lda % 4 == 0, 16-byte aligned, and N <= 1024 or M*N*K <= 2^33: square
+ * problems up to 2048^3 pack only B), plus the fp32 partial tiles of a
+ * last round split over K (this call cannot turn that split off).  A
+ * problem over the limit returns MT_ERR_SCRATCH_LIMIT and launches nothing.
+ * Other errors as mt_sgemm_ex.
  *
  * The array is shared by every call in the process: calls that overlap on
  * the GPU (different streams, or host threads) race on it and must be
@@ -276,7 +280,9 @@ MT_API mt_status mt_sgemm_host_async(const float *A, const float *B, float *C,
  * library holds the array until the process exits.  The first call on a
  * device looks up the array's device address and sets the kernel's
  * shared-memory limit (no allocation); make that first call before any
- * stream capture.
+ * stream capture.  The address is kept for the life of the process, like
+ * the library's other per-device set-up: calls on a device after
+ * cudaDeviceReset on it are not supported.
  */
 #define MT_NOALLOC_SCRATCH_BYTES (32ll << 20)
 MT_API mt_status mt_sgemm_tf32x3_noalloc(const float *A, const float *B, float *C,

@@ -137,16 +137,14 @@ def sampled_rows(M, bm=128, extra=24, seed=0):
 
 
 @pytest.mark.parametrize("name", ["square_4096", "square_8192", "skinny_65536x128x4096"])
-def test_full_size_sampled_rows(name):
-    """The benchmark's workloads in the benchmark's launch configuration."""
-    w = gemm_inputs.WORKLOADS[name]
-    A, B = gemm_inputs.make_workload(w)
-    a, b = A.cuda(), B.cuda()
-    c = mt.sgemm(a, b)  # automatic choice, as the benchmark calls it
+def test_full_size_every_element(name, full_oracle):
+    """The benchmark's workloads in the benchmark's launch configuration,
+    every output against the full oracle."""
+    A, B = gemm_inputs.make_workload(name)
+    c = mt.sgemm(A.cuda(), B.cuda())  # automatic choice, as the benchmark calls it
     torch.cuda.synchronize()
-    rows = sampled_rows(w.M, extra=16 if w.N > 4096 else 40)
-    Cr, Wr = oracle.sgemm_rows(A.numpy(), B.numpy(), rows, with_w=True)
-    assert_within(c[torch.from_numpy(rows).cuda()].cpu().numpy(), Cr, Wr, FFMA_TOL, name)
+    Cref, W = full_oracle(name)
+    assert_within(c.cpu().numpy(), Cref, W, FFMA_TOL, name)
 
 
 # --- exact cases ----------------------------------------------------------------

@@ -116,7 +116,7 @@ def test_workloads_full_oracle(name, cfg):
 @pytest.mark.parametrize("tile", [0, 128], ids=["auto", "single"])
 @pytest.mark.parametrize("name", ["square_4096", "square_8192", "skinny_65536x128x4096",
                                   "skinny_65536x128x4096/packed-A"])
-def test_full_size_sampled_rows(name, split, tile):
+def test_full_size_every_element(name, split, tile, full_oracle):
     name, _, how = name.partition("/")
     w = gemm_inputs.WORKLOADS[name]
     A, B = gemm_inputs.make_workload(w)
@@ -125,11 +125,8 @@ def test_full_size_sampled_rows(name, split, tile):
     if name.startswith("skinny"):
         assert mt.plan(w.M, w.N, w.K, bm=tile, **TF32, **pack)["pack_a"] == (1 if pack else 2)
     torch.cuda.synchronize()
-    g = np.random.default_rng(1)
-    rows = np.unique(np.concatenate([[0, w.M - 1, 127, 128, 255, 256],
-                                     g.integers(0, w.M, 24)]))
-    Cr, Wr = oracle.sgemm_rows(A.numpy(), B.numpy(), rows, with_w=True)
-    assert_within(c[torch.from_numpy(rows).cuda()].cpu().numpy(), Cr, Wr, TOL, name)
+    Cref, W = full_oracle(name)
+    assert_within(c.cpu().numpy(), Cref, W, TOL, name)
 
 
 @pytest.mark.parametrize("cfg", ALL, ids=ALL_IDS)

@@ -1135,6 +1135,9 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 namespace {
 std::mutex g_noalloc_mutex;
+// Device address of the array per device ordinal, kept for the life of the
+// process (a cudaDeviceReset that reloads the module is not supported, as
+// for the library's other per-device set-up).
 void* g_noalloc_ptr[64];
 }  // namespace
 
