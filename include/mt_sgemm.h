@@ -115,6 +115,16 @@ typedef struct {
                       gathered.  Every choice gives the same bits. */
     int group_m;   /* tile rows per group of the tile raster (tiles are walked
                       down a group's rows, then across); 0 = automatic */
+    int schedule;  /* MT_VARIANT_FFMA: how tiles that do not fill a whole wave of
+                      resident CTAs are run.  0 = automatic; 1 = whole tiles, with
+                      a grid smaller than the SMs or a last wave under half full
+                      cut into equal K slices (split tail); 2 = stream-K: those
+                      tiles' K tiles spread evenly over one wave of CTAs, each
+                      taking a contiguous run across tile boundaries, and the
+                      pieces of a tile added in k order by a second kernel
+                      (deterministic).  split_k = 1 turns both off; split_k > 1
+                      with 2 is MT_ERR_UNSUPPORTED, as are tiles whose warps form
+                      K groups.  Other variants: 0 only. */
 } mt_config;
 
 /* What a call with the same arguments would launch. */
@@ -138,7 +148,8 @@ typedef struct {
                                  (row-major A tiles); 3 = A tiles K-major read as
                                  stored, 4 = gathered, 5 = from a K x M copy.
                                  0 otherwise */
-    int reserved;
+    int stream_k;             /* CTAs running stream-K runs (the last ones of the
+                                 grid; 0 = none) */
 } mt_plan;
 
 /*

@@ -33,13 +33,16 @@ TOL = 1e-5
 
 # FFMA-path plans: every staging form of A (row-major as stored / from a
 # copy, K-major gathered / from a copy / as stored), tile, pipeline depth,
-# K groups of warps, explicit and automatic K splits, and the one-warp kernel.
+# K groups of warps, explicit and automatic K splits, stream-K runs and their
+# fix-up, and the one-warp kernel.
 CONFIGS = [dict(), dict(pack_a=1), dict(pack_a=2), dict(pack_a=4), dict(pack_a=5),
            dict(bm=64, bn=128, pack_a=4), dict(bm=64, bn=64, pack_a=5),
            dict(bm=64, bn=128, stages=3, pack_a=5),
            dict(bm=128, bn=128, bk=32, stages=3, fma=2),
            dict(bm=128, bn=128, bk=16, stages=1), dict(bm=128, bn=128, bk=16, stages=2),
            dict(pack_a=4, split_k=3), dict(bm=128, bn=128, bk=32, stages=3, no_pad=True),
+           dict(schedule=2), dict(bm=128, bn=128, bk=16, stages=4, wm=64, pack_a=5, schedule=2),
+           dict(bm=64, bn=64, pack_a=4, schedule=2),
            dict(variant="p18"), dict(variant="p18", stages=1)]
 
 

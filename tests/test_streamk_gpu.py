@@ -1,0 +1,146 @@
+"""GPU parity of the FFMA kernel's stream-K schedule against the CPU oracle.
+
+Stream-K (mt_config.schedule = 2) spreads the K tiles of the tiles past the
+last whole wave over one wave of CTAs, each taking a contiguous run across
+tile boundaries; a second kernel adds the pieces of every tile that no run
+covered whole, in k order.  Each output is then a sum of a few fp32 FMA
+chains over consecutive k ranges: within the FFMA tolerance 1e-5 * |A|*|B|
+of the oracle, bit-exact on integer inputs (every partial sum is an integer
+below 2^24), and the same bits on every run (the order of the additions is
+fixed by the plan, not by scheduling).
+"""
+import numpy as np
+import pytest
+import torch
+
+import gemm_inputs
+import oracle
+import tiled_fp32_gemm_gb300 as mt
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5
+SK = dict(schedule="stream_k")
+# Tiles with every K-major A source and the row-major A tile.
+TILES = [
+    dict(),                                                   # automatic tile
+    dict(bm=128, bn=128, bk=16, stages=4, wm=64, pack_a=5),   # A from a K x M copy
+    dict(bm=128, bn=128, bk=16, stages=4, wm=64, pack_a=4),   # A gathered
+    dict(bm=64, bn=128, bk=32, stages=2, pack_a=4),
+    dict(bm=128, bn=128, bk=32, stages=3, fma=2, pack_a=2),   # row-major A tiles
+    dict(bm=64, bn=64, pack_a=5),
+]
+TILE_IDS = ["-".join(f"{k}{v}" for k, v in c.items()) or "auto" for c in TILES]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    from tiled_fp32_gemm_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+    return mt.lib()
+
+
+def run(a, b, **cfg):
+    c = mt.sgemm(a, b, **cfg)
+    torch.cuda.synchronize()
+    return c.cpu().numpy()
+
+
+def assert_within(C, Cref, W, what):
+    err = np.abs(np.asarray(C, np.float64) - Cref)
+    bad = err > TOL * W
+    if bad.any():
+        i, j = np.argwhere(bad)[0]
+        pytest.fail(f"{what}: {bad.sum()} outputs outside {TOL}*W, first at ({i},{j}): "
+                    f"got {C[i, j]!r} want {Cref[i, j]!r} W={W[i, j]!r}")
+
+
+@pytest.mark.parametrize("cfg", TILES, ids=TILE_IDS)
+@pytest.mark.parametrize("name", ["masked_100x72x80", "square_1024", "ragged_4097x3001x2053"])
+def test_stream_k_workloads_full_oracle(name, cfg, full_oracle):
+    A, B = gemm_inputs.make_workload(name)
+    a, b = A.cuda(), B.cuda()
+    w = gemm_inputs.WORKLOADS[name]
+    p = mt.plan(w.M, w.N, w.K, a=a, b=b, **SK, **cfg)
+    assert p["stream_k"] > 0 and p["split_k"] == 1
+    got = run(a, b, **SK, **cfg)
+    Cref, W = full_oracle(name)
+    assert_within(got, Cref, W, f"{name} {cfg}")
+    # Deterministic: the same bits again.
+    assert np.array_equal(run(a, b, **SK, **cfg), got)
+
+
+@pytest.mark.parametrize("name", ["square_4096", "skinny_65536x128x4096"])
+def test_stream_k_large_workloads_every_element(name, full_oracle):
+    A, B = gemm_inputs.make_workload(name)
+    got = run(A.cuda(), B.cuda(), **SK)
+    Cref, W = full_oracle(name)
+    assert_within(got, Cref, W, name)
+
+
+@pytest.mark.parametrize("cfg", TILES, ids=TILE_IDS)
+@pytest.mark.parametrize("shape", [(100, 72, 80), (257, 130, 77), (1024, 1024, 1024),
+                                   (1000, 1000, 1200)])
+def test_stream_k_integer_inputs_bit_exact(shape, cfg):
+    M, N, K = shape
+    A, B = gemm_inputs.make_ab(M, N, K, seed=11, dist="int")
+    Cref = oracle.sgemm(A.numpy(), B.numpy())
+    assert np.array_equal(run(A.cuda(), B.cuda(), **SK, **cfg), Cref)
+
+
+def test_stream_k_runs_across_tile_boundaries():
+    # 1024^3 on 128 x 128 tiles: 64 tiles of 64 K tiles over one wave of
+    # CTAs, so every tile is cut into pieces taken by several CTAs and
+    # most CTAs start or end inside a tile.
+    cfg = dict(bm=128, bn=128, bk=16, stages=4, wm=64, pack_a=5, **SK)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = mt.plan(1024, 1024, 1024, **cfg)
+    assert p["stream_k"] == min(2 * sms, 64 * 64 // 2) and p["grid"] == p["stream_k"]
+    # Two partial slots per stream-K CTA, after the copy of A.
+    assert p["workspace_bytes"] >= 2 * p["stream_k"] * 128 * 128 * 4
+    A, B = gemm_inputs.make_ab(1024, 1024, 1024, seed=21, dist="uniform")
+    Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
+    assert_within(run(A.cuda(), B.cuda(), **cfg), Cref, W, "1024^3 128x128 stream-K")
+
+
+def test_stream_k_runs_shorter_than_a_tile_and_empty_runs():
+    # Few K tiles: fewer iterations than resident CTAs, so the plan uses
+    # fewer CTAs (each at least two K tiles); one tile of three K tiles on
+    # one CTA that covers it whole (no fix-up work at all).
+    for (M, N, K) in [(64, 64, 96), (300, 200, 64), (128, 128, 4)]:
+        A, B = gemm_inputs.make_ab(M, N, K, seed=5, dist="uniform")
+        Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
+        for cfg in TILES:
+            assert_within(run(A.cuda(), B.cuda(), **SK, **cfg), Cref, W, f"{(M, N, K)} {cfg}")
+
+
+def test_stream_k_general_form_alpha_beta_bias():
+    # The fix-up applies alpha, beta and the bias row like every epilogue.
+    M, N, K = 1000, 520, 700
+    A, B = gemm_inputs.make_ab(M, N, K, seed=8, dist="uniform")
+    g = torch.Generator().manual_seed(9)
+    C0 = torch.rand(M, N, generator=g) * 2 - 1
+    bias = torch.rand(N, generator=g) * 2 - 1
+    alpha, beta = 0.75, -1.5
+    ref, W = oracle.sgemm_general(A.numpy(), B.numpy(), C0.numpy().ravel().copy(), M, N, K,
+                                  K, N, N, alpha=alpha, beta=beta, bias=bias.numpy(),
+                                  with_w=True)
+    c = C0.cuda()
+    mt.gemm(A.cuda(), B.cuda(), c, alpha=alpha, beta=beta, bias=bias.cuda(), **SK)
+    torch.cuda.synchronize()
+    assert_within(c.cpu().numpy(), ref.reshape(M, N), W.reshape(M, N), "general stream-K")
+
+
+def test_stream_k_choices_refused():
+    # Explicit split_k with stream-K, tiles whose warps form K groups, and
+    # the other variants refuse the schedule before any launch.
+    with pytest.raises(mt.MtError):
+        mt.plan(1024, 1024, 1024, split_k=2, **SK)
+    with pytest.raises(mt.MtError):
+        mt.plan(1024, 1024, 1024, bm=64, bn=128, stages=3, pack_a=4, **SK)
+    with pytest.raises(mt.MtError):
+        mt.plan(1024, 1024, 1024, variant="tf32x3", **SK)
+    # split_k = 1 turns stream-K off like the split tail.
+    p = mt.plan(1024, 1024, 1024, split_k=1, **SK)
+    assert p["stream_k"] == 0 and p["split_k"] == 1

@@ -46,6 +46,8 @@ MT_VARIANT_P18 = 2
 MT_VARIANT_TC16 = 3
 VARIANTS = {"ffma": MT_VARIANT_FFMA, "tf32x3": MT_VARIANT_TF32X3, "p18": MT_VARIANT_P18,
             "tc16": MT_VARIANT_TC16}
+# mt_config.schedule: automatic, split tail, stream-K.
+SCHEDULES = {"auto": 0, "split_tail": 1, "stream_k": 2}
 
 MT_DTYPE_F16 = 1
 MT_DTYPE_BF16 = 2
@@ -66,7 +68,7 @@ class mt_config(ctypes.Structure):
                 ("split_k", ctypes.c_int), ("fma", ctypes.c_int),
                 ("fault_inject", ctypes.c_int), ("wm", ctypes.c_int), ("wn", ctypes.c_int),
                 ("tm", ctypes.c_int), ("tn", ctypes.c_int), ("pack_a", ctypes.c_int),
-                ("group_m", ctypes.c_int)]
+                ("group_m", ctypes.c_int), ("schedule", ctypes.c_int)]
 
 
 class mt_plan(ctypes.Structure):
@@ -78,7 +80,7 @@ class mt_plan(ctypes.Structure):
                 ("tn", ctypes.c_int),
                 ("grid", ctypes.c_int64), ("smem_bytes", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_int64), ("pack_a", ctypes.c_int),
-                ("reserved", ctypes.c_int)]
+                ("stream_k", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -191,7 +193,7 @@ def bounds_status(handle=None) -> dict:
 
 def make_config(variant="ffma", bm=0, bn=0, bk=0, stages=0, no_pad=False, split_k=0,
                 fma=0, fault_inject=0, wm=0, wn=0, tm=0, tn=0, pack_a=0,
-                group_m=0) -> mt_config:
+                group_m=0, schedule=0) -> mt_config:
     c = mt_config()
     c.variant = VARIANTS[variant] if isinstance(variant, str) else int(variant)
     c.bm, c.bn, c.bk, c.stages = bm, bn, bk, stages
@@ -203,6 +205,7 @@ def make_config(variant="ffma", bm=0, bn=0, bk=0, stages=0, no_pad=False, split_
     c.tm, c.tn = tm, tn
     c.pack_a = pack_a
     c.group_m = group_m
+    c.schedule = SCHEDULES[schedule] if isinstance(schedule, str) else int(schedule)
     return c
 
 

@@ -102,8 +102,10 @@ struct Launch {
   bool pad = true;
   int fault_inject = 0;
   int max_ctas = 0;  // persistent kernels: CTAs to launch at most
-  // FFMA split-K (see GemmArgs).
+  // FFMA split-K and stream-K (see GemmArgs).
   int full_tiles = 0, split = 1, kt_per_slice = 0;
+  int sk_ctas = 0;
+  int64_t sk_iters = 0;
   // 3xTF32: float4 reads of A / B by their packers; A split inside the
   // GEMM kernel instead of packed.
   bool vec_a = false, vec_b = false;
@@ -652,18 +654,43 @@ mt_status plan_ffma(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
     split = 1;
     full = tiles;
   }
+  // Stream-K (schedule 2): the tiles past the last whole wave of resident
+  // CTAs (all of them when there is less than one wave) are not cut into
+  // equal K slices but spread evenly, K tile by K tile, over one wave of
+  // units, each taking a contiguous run across tile boundaries; a second
+  // kernel adds the pieces of the tiles no run covered whole.
+  const int schedule = cfg ? cfg->schedule : 0;
+  if (schedule == 2) {
+    if (E.kslices != 1 || (cfg && cfg->split_k > 1)) return MT_ERR_UNSUPPORTED;
+    split = 1;
+    full = tiles;
+    if (!(cfg && cfg->split_k == 1) && ktiles > 0) {
+      const int64_t slots = static_cast<int64_t>(std::max(sms, 1)) * E.min_blocks;
+      const int64_t rem = tiles % slots;
+      if (rem != 0) {
+        full = tiles - rem;
+        L->sk_iters = rem * ktiles;
+        // Every unit takes at least two K tiles.
+        L->sk_ctas = static_cast<int>(std::max<int64_t>(
+            1, std::min<int64_t>(slots, L->sk_iters / 2)));
+      }
+    }
+  }
   L->full_tiles = static_cast<int>(full);
   L->split = static_cast<int>(split);
   L->kt_per_slice = static_cast<int>(ceil_div(ktiles, split));
   p.split_k = L->split;
-  p.grid = full + (tiles - full) * split;
+  p.stream_k = L->sk_ctas;
+  p.grid = L->sk_ctas > 0 ? full + L->sk_ctas : full + (tiles - full) * split;
   if (!L->a_kmajor) {
     L->ldo_a = ceil_div(std::max<int64_t>(K, 1), 4) * 4;
     L->ldo_b = ceil_div(std::max<int64_t>(N, 1), 4) * 4;
     L->prep_b_offset = L->prep_a ? round256(M * L->ldo_a * 4) : 0;
   }
   L->partial_offset = L->prep_b_offset + (L->prep_b ? round256(K * L->ldo_b * 4) : 0);
-  p.workspace_bytes = L->partial_offset + (tiles - full) * split * E.bm * E.bn * 4;
+  p.workspace_bytes = L->partial_offset + (L->sk_ctas > 0 ? 2 * int64_t(L->sk_ctas)
+                                                          : (tiles - full) * split) *
+                                             E.bm * E.bn * 4;
   // The budget check comes before anything is launched ("Part 18", section
   // "Shared-memory budget checks include stages and padding").
   if (p.smem_bytes > smem_limit) return MT_ERR_SMEM_BUDGET;
@@ -693,8 +720,13 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
               cfg->no_pad < 0 || cfg->no_pad > 1 || cfg->split_k < 0 || cfg->fma < 0 ||
               cfg->fma > 2 || cfg->fault_inject < 0 || cfg->fault_inject > 1 || cfg->wm < 0 ||
               cfg->wn < 0 || cfg->tm < 0 || cfg->tn < 0 || cfg->pack_a < 0 ||
-              cfg->pack_a > 5 || cfg->group_m < 0))
+              cfg->pack_a > 5 || cfg->group_m < 0 || cfg->schedule < 0 ||
+              cfg->schedule > 2))
     return MT_ERR_INVALID_ARG;
+  // The schedule choice is the FFMA kernel's (the tensor-core kernels are
+  // persistent with a split tail of their own).
+  if (cfg && cfg->schedule && (P.dtype || variant != MT_VARIANT_FFMA))
+    return MT_ERR_UNSUPPORTED;
   if (P.dtype)
     return plan_f16(P, cfg, smem_limit, sms, dev >= 0 ? mt::f16tc_pair_max_clusters(dev) : 0,
                     L);
@@ -827,6 +859,8 @@ mt::GemmArgs make_args(const Problem& P, const Launch& L) {
   a.full_tiles = L.full_tiles;
   a.split = L.split;
   a.kt_per_slice = L.kt_per_slice;
+  a.sk_ctas = L.sk_ctas;
+  a.sk_iters = L.sk_iters;
   a.partial = nullptr;
   a.a_extent = P.trans_a ? mt::view_extent(P.K, P.M, P.lda) : mt::view_extent(P.M, P.K, P.lda);
   a.b_extent = P.trans_b ? mt::view_extent(P.N, P.K, P.ldb) : mt::view_extent(P.K, P.N, P.ldb);
@@ -948,7 +982,7 @@ mt_status run(const Problem& P, cudaStream_t stream, const mt_config* cfg) {
       return MT_ERR_CUDA;
     }
     char* base = static_cast<char*>(ws);
-    if (L.split > 1) {
+    if (L.split > 1 || L.sk_ctas > 0) {
       args.partial = reinterpret_cast<float*>(base + L.partial_offset);
       args.partial_extent = (L.plan.workspace_bytes - L.partial_offset) / 4;
     }
@@ -987,12 +1021,28 @@ mt_status run(const Problem& P, cudaStream_t stream, const mt_config* cfg) {
     }
   }
   void* params[] = {&args};
-  ok = ok && cudaLaunchKernel(L.kern, dim3(static_cast<unsigned>(L.plan.grid)),
-                              dim3(static_cast<unsigned>(L.plan.threads)), params,
-                              static_cast<size_t>(L.plan.smem_bytes), stream) == cudaSuccess;
+  // After an operand copy the GEMM is launched as its programmatic
+  // dependent: its CTAs are scheduled as the copy's CTAs retire and wait
+  // inside (griddepcontrol.wait) for the copy to complete, so the launch
+  // latency overlaps the copy.
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.gridDim = dim3(static_cast<unsigned>(L.plan.grid));
+  lc.blockDim = dim3(static_cast<unsigned>(L.plan.threads));
+  lc.dynamicSmemBytes = static_cast<size_t>(L.plan.smem_bytes);
+  lc.stream = stream;
+  lc.attrs = attr;
+  lc.numAttrs = (L.prep_a || L.prep_a_kmajor || L.prep_b) ? 1 : 0;
+  ok = ok && cudaLaunchKernelExC(&lc, L.kern, params) == cudaSuccess;
   if (ok && L.split > 1)
     ok = mt::launch_splitk_reduce(args, L.plan.bm, L.plan.bn, L.plan.vec_c != 0, stream) ==
          cudaSuccess;
+  if (ok && L.sk_ctas > 0)
+    ok = mt::launch_streamk_fixup(args, L.plan.bm, L.plan.bn,
+                                  static_cast<int>(ceil_div(P.K, L.plan.bk)),
+                                  L.plan.vec_c != 0, stream) == cudaSuccess;
   if (ws) cudaFreeAsync(ws, stream);
   if (!ok) {
     cudaGetLastError();

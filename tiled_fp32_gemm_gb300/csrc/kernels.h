@@ -106,6 +106,16 @@ struct GemmArgs {
   int split;
   int kt_per_slice;
   float* partial;
+  // Stream-K (FFMA kernel; sk_ctas > 0, split = 1): the tiles from
+  // full_tiles on hold sk_iters K tiles in all (tile-major, k ascending);
+  // unit full_tiles + c (c < sk_ctas) takes the contiguous run
+  // [c*sk_iters/sk_ctas, (c+1)*sk_iters/sk_ctas) across tile boundaries.
+  // A tile the run covers whole goes to C; a piece of a tile goes to
+  // `partial` as a dense BM x BN block: slot 2c for the run's first tile,
+  // 2c+1 for its last.  launch_streamk_fixup adds the pieces of each tile in
+  // k order.
+  int sk_ctas;
+  int64_t sk_iters;
   // Elements from A, B, C, partial up to the last element the product
   // addresses (checked builds test every access against them), and the
   // checked build's record (nullptr otherwise).
@@ -126,6 +136,25 @@ __host__ __device__ inline int64_t view_extent(int64_t rows, int64_t cols, int64
 // bm x bn tile per slice of each split tile.
 cudaError_t launch_splitk_reduce(const GemmArgs& a, int bm, int bn, bool vec_c,
                                  cudaStream_t stream);
+
+// Stream-K fix-up: for every stream-K tile that no single unit covered,
+// adds its pieces (the partial slots of the units whose runs overlap it, in
+// unit order, which is k order) and writes the sum to C with the edge masks
+// (alpha, beta, bias applied); tiles a unit covered whole were written by
+// the GEMM kernel and are skipped.  ktiles: K tiles per tile.  Launched as
+// a programmatic dependent of the GEMM kernel before it on `stream`.
+cudaError_t launch_streamk_fixup(const GemmArgs& a, int bm, int bn, int ktiles, bool vec_c,
+                                 cudaStream_t stream);
+
+// First unit of the stream-K split whose run holds stream-K iteration x:
+// the largest c with c * iters / ctas <= x (runs may be empty when there
+// are fewer iterations than units; the one returned is not).
+__host__ __device__ inline int streamk_unit_of(int64_t x, int64_t iters, int ctas) {
+  int64_t c = x * ctas / iters;  // c * iters / ctas <= x by construction, or one past
+  while (c + 1 < ctas && (c + 1) * iters / ctas <= x) ++c;
+  while (c > 0 && c * iters / ctas > x) --c;
+  return static_cast<int>(c);
+}
 
 // The one-warp kernel restating the pages' Version 18 (BM=4, BN=8, BK=16,
 // two stages, synchronous staging, padded A).  pad selects the rule's

@@ -10,10 +10,46 @@
 
 namespace mt {
 
+// C[row][col..col+3] = alpha * s + beta * C (+ bias), masked to M x N: the
+// epilogue of the second-pass kernels that add partial tiles.
+__device__ __forceinline__ void store_sum4(const GemmArgs& a, int row, int col, float4 s,
+                                           int vec_c) {
+  float* c_row = a.C + static_cast<int64_t>(row) * a.ldc;
+  const float v[4] = {a.alpha * s.x, a.alpha * s.y, a.alpha * s.z, a.alpha * s.w};
+  if (vec_c) {
+    if (!bounds_ok(a.bounds, SITE_C_STORE, (c_row - a.C) + col, 4, a.c_extent) ||
+        (a.bias && !bounds_ok(a.bounds, SITE_BIAS, col, 4, a.N)))
+      return;
+    float4* cp = reinterpret_cast<float4*>(c_row + col);
+    float4 o = make_float4(v[0], v[1], v[2], v[3]);
+    if (a.beta != 0.0f) {
+      const float4 c0 = *cp;
+      o = make_float4(fmaf(a.beta, c0.x, v[0]), fmaf(a.beta, c0.y, v[1]),
+                      fmaf(a.beta, c0.z, v[2]), fmaf(a.beta, c0.w, v[3]));
+    }
+    if (a.bias) {
+      o.x += a.bias[col];
+      o.y += a.bias[col + 1];
+      o.z += a.bias[col + 2];
+      o.w += a.bias[col + 3];
+    }
+    *cp = o;
+  } else {
+    for (int e = 0; e < 4; ++e)
+      if (col + e < a.N &&
+          bounds_ok(a.bounds, SITE_C_STORE, (c_row - a.C) + col + e, 1, a.c_extent) &&
+          (!a.bias || bounds_ok(a.bounds, SITE_BIAS, col + e, 1, a.N))) {
+        float o = a.beta != 0.0f ? fmaf(a.beta, c_row[col + e], v[e]) : v[e];
+        if (a.bias) o += a.bias[col + e];
+        c_row[col + e] = o;
+      }
+  }
+}
+
 // C[tile] = alpha * (sum over slices s = 0, 1, ... of the slice partials,
-// added in that order) + beta * C[tile] (+ bias[col]), masked to M x N.  Each split tile
-// is cut into `pieces` CTAs of up to 1024 float4 (4 per thread), so a
-// small tail still spreads over the GPU.
+// added in that order) + beta * C[tile] (+ bias[col]), masked to M x N.
+// Each split tile is cut into `pieces` CTAs of up to 1024 float4 (4 per
+// thread), so a small tail still spreads over the GPU.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(GemmArgs a, int bm, int bn,
                                                            int pieces, int vec_c) {
   // Launched as a programmatic dependent of the GEMM kernel before it on the
@@ -29,54 +65,104 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(GemmArgs a, int bm, 
   const int e_end = min(block4, e_begin + per_piece);
   const int64_t tile_off = static_cast<int64_t>(t) * a.split * block4;  // in float4s
   const float4* P = reinterpret_cast<const float4*>(a.partial) + tile_off;
-  for (int e4 = e_begin + threadIdx.x; e4 < e_end; e4 += blockDim.x) {
+  // A thread's (at most) four float4 of the piece are read slice by slice,
+  // four independent loads at a time.
+  float4 s[4];
+  for (int sl = 0; sl < a.split; ++sl) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int e4 = e_begin + threadIdx.x + q * 256;
+      if (e4 >= e_end) continue;
+      const int64_t e = static_cast<int64_t>(sl) * block4 + e4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (bounds_ok(a.bounds, SITE_PARTIAL, (tile_off + e) * 4, 4, a.partial_extent)) v = P[e];
+      if (sl == 0) {
+        s[q] = v;
+      } else {
+        s[q].x += v.x;
+        s[q].y += v.y;
+        s[q].z += v.z;
+        s[q].w += v.w;
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int e4 = e_begin + threadIdx.x + q * 256;
+    if (e4 >= e_end) continue;
     const int r = (e4 * 4) / bn, c = (e4 * 4) % bn;
     const int row = tm * bm + r, col = tn * bn + c;
-    if (row >= a.M || col >= a.N) continue;
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int sl = 0; sl < a.split; ++sl) {
-      const int64_t e = static_cast<int64_t>(sl) * block4 + e4;
-      if (!bounds_ok(a.bounds, SITE_PARTIAL, (tile_off + e) * 4, 4, a.partial_extent)) continue;
-      const float4 v = P[e];
-      if (sl == 0) {
-        s = v;
-      } else {
-        s.x += v.x;
-        s.y += v.y;
-        s.z += v.z;
-        s.w += v.w;
+    if (row < a.M && col < a.N) store_sum4(a, row, col, s[q], vec_c);
+  }
+}
+
+// The stream-K fix-up (see launch_streamk_fixup): tile t of the stream-K
+// tiles is cut into `pieces` CTAs like the split-K reduce.  The units whose
+// runs overlap the tile's K tiles [t*ktiles, (t+1)*ktiles) are consecutive;
+// their pieces are added in unit order, which is k order, so the result
+// does not depend on scheduling.  The slots of those units are worked out
+// once per CTA, up to 256 at a time, into shared memory.
+__global__ void __launch_bounds__(256) streamk_fixup_kernel(GemmArgs a, int bm, int bn,
+                                                           int pieces, int ktiles, int vec_c) {
+  __shared__ long long slot_of[256];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int t = blockIdx.x / pieces, piece = blockIdx.x % pieces;
+  const int64_t first = static_cast<int64_t>(t) * ktiles, last = first + ktiles;
+  const int c0 = streamk_unit_of(first, a.sk_iters, a.sk_ctas);
+  const int c1 = streamk_unit_of(last - 1, a.sk_iters, a.sk_ctas);
+  if (c0 == c1) return;  // one run covered the tile whole: already in C
+  int tm, tn;
+  grouped_tile(a.full_tiles + t, a.tiles_m, a.tiles_n, a.group_m, tm, tn);
+  const int block4 = bm * bn / 4;
+  const int per_piece = (block4 + pieces - 1) / pieces;
+  const int e_begin = piece * per_piece;
+  const int e_end = min(block4, e_begin + per_piece);
+  const float4* P = reinterpret_cast<const float4*>(a.partial);
+  // Each thread sums at most this many float4 of the piece.
+  constexpr int kMaxPerThread = 4;
+  float4 s[kMaxPerThread];
+#pragma unroll
+  for (int q = 0; q < kMaxPerThread; ++q) s[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int base = c0; base <= c1; base += 256) {
+    const int n = min(256, c1 - base + 1);
+    __syncthreads();  // the previous chunk's slots are no longer read
+    if (static_cast<int>(threadIdx.x) < n) {
+      const int u = base + threadIdx.x;
+      const int64_t b = static_cast<int64_t>(u) * a.sk_iters / a.sk_ctas;
+      const int64_t e = static_cast<int64_t>(u + 1) * a.sk_iters / a.sk_ctas;
+      // An empty run has no piece; the tile is the first of u's run unless
+      // the run began before it.
+      slot_of[threadIdx.x] = e <= b ? -1 : 2 * static_cast<int64_t>(u) + (b < first ? 1 : 0);
+    }
+    __syncthreads();
+    // Piece by piece in k order, the thread's float4 four independent loads
+    // at a time.  The sum starts from zero: adding the first piece to +0.0
+    // leaves it unchanged, except that -0.0 becomes +0.0, as it does in any
+    // fp32 sum.
+    for (int j = 0; j < n; ++j) {
+      const long long slot = slot_of[j];
+      if (slot < 0) continue;
+#pragma unroll
+      for (int q = 0; q < kMaxPerThread; ++q) {
+        const int e4 = e_begin + threadIdx.x + q * 256;
+        if (e4 >= e_end) continue;
+        const int64_t at = slot * block4 + e4;
+        if (!bounds_ok(a.bounds, SITE_PARTIAL, at * 4, 4, a.partial_extent)) continue;
+        const float4 v = P[at];
+        s[q].x += v.x;
+        s[q].y += v.y;
+        s[q].z += v.z;
+        s[q].w += v.w;
       }
     }
-    float* c_row = a.C + static_cast<int64_t>(row) * a.ldc;
-    const float v[4] = {a.alpha * s.x, a.alpha * s.y, a.alpha * s.z, a.alpha * s.w};
-    if (vec_c) {
-      if (!bounds_ok(a.bounds, SITE_C_STORE, (c_row - a.C) + col, 4, a.c_extent) ||
-          (a.bias && !bounds_ok(a.bounds, SITE_BIAS, col, 4, a.N)))
-        continue;
-      float4* cp = reinterpret_cast<float4*>(c_row + col);
-      float4 o = make_float4(v[0], v[1], v[2], v[3]);
-      if (a.beta != 0.0f) {
-        const float4 c0 = *cp;
-        o = make_float4(fmaf(a.beta, c0.x, v[0]), fmaf(a.beta, c0.y, v[1]),
-                        fmaf(a.beta, c0.z, v[2]), fmaf(a.beta, c0.w, v[3]));
-      }
-      if (a.bias) {
-        o.x += a.bias[col];
-        o.y += a.bias[col + 1];
-        o.z += a.bias[col + 2];
-        o.w += a.bias[col + 3];
-      }
-      *cp = o;
-    } else {
-      for (int e = 0; e < 4; ++e)
-        if (col + e < a.N &&
-            bounds_ok(a.bounds, SITE_C_STORE, (c_row - a.C) + col + e, 1, a.c_extent) &&
-            (!a.bias || bounds_ok(a.bounds, SITE_BIAS, col + e, 1, a.N))) {
-          float o = a.beta != 0.0f ? fmaf(a.beta, c_row[col + e], v[e]) : v[e];
-          if (a.bias) o += a.bias[col + e];
-          c_row[col + e] = o;
-        }
-    }
+  }
+#pragma unroll
+  for (int q = 0; q < kMaxPerThread; ++q) {
+    const int e4 = e_begin + threadIdx.x + q * 256;
+    if (e4 >= e_end) continue;
+    const int r = (e4 * 4) / bn, c = (e4 * 4) % bn;
+    const int row = tm * bm + r, col = tn * bn + c;
+    if (row < a.M && col < a.N) store_sum4(a, row, col, s[q], vec_c);
   }
 }
 
@@ -84,7 +170,8 @@ cudaError_t launch_splitk_reduce(const GemmArgs& a, int bm, int bn, bool vec_c,
                                  cudaStream_t stream) {
   const int tail = a.tiles_m * a.tiles_n - a.full_tiles;
   if (tail <= 0) return cudaSuccess;
-  const int pieces = std::max(1, bm * bn / 4096);
+  // Pieces of at most 1024 float4: four per thread of 256.
+  const int pieces = std::max(1, (bm * bn / 4 + 1023) / 1024);
   GemmArgs r = a;
   // Callers that did not state the partial buffer's extent (the tensor-core
   // paths) have exactly one dense bm x bn tile per slice of each split tile.
@@ -106,6 +193,26 @@ cudaError_t launch_splitk_reduce(const GemmArgs& a, int bm, int bn, bool vec_c,
   cfg.numAttrs = 1;
   const int vc = vec_c ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, r, bm, bn, pieces, vc);
+}
+
+cudaError_t launch_streamk_fixup(const GemmArgs& a, int bm, int bn, int ktiles, bool vec_c,
+                                 cudaStream_t stream) {
+  if (a.sk_ctas <= 0 || a.sk_iters <= 0 || ktiles <= 0) return cudaSuccess;
+  const int64_t tiles = a.sk_iters / ktiles;
+  // Pieces of at most 1024 float4: four per thread of 256.
+  const int pieces = std::max(1, (bm * bn / 4 + 1023) / 1024);
+  if (tiles <= 0 || tiles * pieces > INT32_MAX) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles * pieces));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int vc = vec_c ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, streamk_fixup_kernel, a, bm, bn, pieces, ktiles, vc);
 }
 
 // C = beta * C (+ bias[col]) on an M x N view (C not read when beta is 0).

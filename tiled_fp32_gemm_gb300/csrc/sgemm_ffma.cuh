@@ -501,252 +501,289 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
 
   const int M = args.M, N = args.N, K = args.K;
   const int tid = threadIdx.x;
+  // Launched as a programmatic dependent of the operand copy before it on
+  // the stream: wait until the copies are complete and visible (a no-op
+  // when launched without the attribute).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // Work unit: a whole tile, or one K slice of a tile of the split tail,
-  // whose fp32 partial goes to the workspace instead of C.
+  // Work unit: a whole tile; one K slice of a tile of the split tail; or a
+  // stream-K run of K tiles across tile boundaries, taken as one segment
+  // per tile it touches.  A segment's fp32 partial goes to the workspace
+  // instead of C unless it covers its tile whole.
   const int ktiles_all = (K + T::BK - 1) / T::BK;
-  int tile = blockIdx.x, slice = 0, kt_begin = 0, kt_end = ktiles_all;
-  const bool partial = static_cast<int>(blockIdx.x) >= args.full_tiles;
-  if (partial) {
-    const int v = blockIdx.x - args.full_tiles;
-    tile = args.full_tiles + v / args.split;
-    slice = v % args.split;
-    kt_begin = min(ktiles_all, slice * args.kt_per_slice);
-    kt_end = min(ktiles_all, kt_begin + args.kt_per_slice);
+  const int unit = blockIdx.x;
+  const bool streamk = args.sk_ctas > 0 && unit >= args.full_tiles;
+  const int sk_unit = unit - args.full_tiles;
+  int64_t run_begin = 0, run_end = 0, run_at = 0;
+  if (streamk) {
+    run_begin = static_cast<int64_t>(sk_unit) * args.sk_iters / args.sk_ctas;
+    run_end = static_cast<int64_t>(sk_unit + 1) * args.sk_iters / args.sk_ctas;
+    run_at = run_begin;
   }
-  const int ktiles = kt_end - kt_begin;
-  int tm, tn;
-  grouped_tile(tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
-  const int m0 = tm * T::BM, n0 = tn * T::BN;
-
-  const AStage<T, AMODE> stage_a(args, m0, tid);
-  const BStage<T, BMODE> stage_b(args, n0, tid);
-
-  // Prologue: STAGES-1 tiles in flight.  One commit group per tile (empty
-  // groups keep the count uniform when K has fewer tiles).
-#pragma unroll
-  for (int s = 0; s < T::STAGES - 1; ++s) {
-    if (s < ktiles) {
-      stage_a.load(As, LA, s, kt_begin + s);
-      stage_b.load(Bs, LB, s, kt_begin + s);
-    }
-    cp_async_commit();
-  }
-
-  // Warp `warp` of K group kg (kg = 0 without K slices).
-  const int kg = tid / 32 / T::TILE_WARPS;
-  const int warp = tid / 32 % T::TILE_WARPS, lane = tid % 32;
-  const int wm = warp / T::WARPS_N, wn = warp % T::WARPS_N;
-  const int lm = lane % T::LM, ln = lane / T::LM;
-  // Thread (lm, ln) of warp (wm, wn) owns rows wm*WM + i*LM + lm (i < TM)
-  // and columns wn*WN + g*LN*4 + ln*4 + c (g < TN/4, c < 4).  With A
-  // K-major the rows come in fours: wm*WM + (i/4)*LM*4 + lm*4 + i%4.
-  const auto row_of = [&](int i) {
-    return KMAJOR ? wm * T::WM + (i / 4) * T::LM * 4 + lm * 4 + i % 4 : wm * T::WM + i * T::LM + lm;
-  };
-  // This group's first k step within a staged K tile.
-  constexpr int KS_STEPS = T::BK / T::KSLICES;
-  const int k_first = kg * KS_STEPS;
-  const int a_off = KMAJOR ? LA.offset(0, k_first, wm * T::WM + lm * 4)
-                           : LA.offset(0, wm * T::WM + lm, k_first);
-  const int b_off = LB.offset(0, k_first, wn * T::WN + ln * 4);
-
-  float2 acc[T::TM][T::TN / 2];
-#pragma unroll
-  for (int i = 0; i < T::TM; ++i)
-#pragma unroll
-    for (int j = 0; j < T::TN / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
-
-  int stage = 0;
-  int load_stage = T::STAGES - 1;
-  for (int kt = 0; kt < ktiles; ++kt) {
-    if constexpr (T::STAGES == 1) {
-      // One stage, no double buffering (the pages' fallback form): copy
-      // tile kt, wait for it, barrier, compute, and a second barrier below
-      // before the next copy overwrites the stage.  Nothing overlaps the
-      // copies.
-      stage_a.load(As, LA, 0, kt_begin + kt);
-      stage_b.load(Bs, LB, 0, kt_begin + kt);
-      cp_async_commit();
-      cp_async_wait<0>();
-      __syncthreads();
+  for (int segment = 0;; ++segment) {
+    int tile = unit, kt_begin = 0, kt_end = ktiles_all;
+    int64_t partial_slot = -1;  // < 0: the segment's tile goes to C
+    if (streamk) {
+      if (run_at >= run_end) break;
+      const int64_t t_rel = run_at / ktiles_all;
+      tile = args.full_tiles + static_cast<int>(t_rel);
+      kt_begin = static_cast<int>(run_at - t_rel * ktiles_all);
+      kt_end = static_cast<int>(
+          min(static_cast<int64_t>(ktiles_all), kt_begin + (run_end - run_at)));
+      if (kt_begin > 0 || kt_end < ktiles_all)
+        partial_slot = 2 * static_cast<int64_t>(sk_unit) + (run_at == run_begin ? 0 : 1);
+      run_at += kt_end - kt_begin;
+      if (segment > 0) {
+        // The stages and the K-group sums of the previous segment are reused:
+        // every copy must have landed and every thread be past its reads.
+        cp_async_wait<0>();
+        __syncthreads();
+      }
     } else {
-      // Tile kt has landed for this thread; the barrier makes every
-      // thread's copies visible and guarantees that the stage refilled
-      // below (read in iteration kt-1) is no longer being read.
-      cp_async_wait<T::STAGES - 2>();
-      __syncthreads();
-      if (kt + T::STAGES - 1 < ktiles) {
-        stage_a.load(As, LA, load_stage, kt_begin + kt + T::STAGES - 1);
-        stage_b.load(Bs, LB, load_stage, kt_begin + kt + T::STAGES - 1);
+      if (segment > 0) break;
+      if (unit >= args.full_tiles) {
+        const int v = unit - args.full_tiles;
+        tile = args.full_tiles + v / args.split;
+        const int slice = v % args.split;
+        kt_begin = min(ktiles_all, slice * args.kt_per_slice);
+        kt_end = min(ktiles_all, kt_begin + args.kt_per_slice);
+        partial_slot = v;  // slice-major per tile
+      }
+    }
+    const int ktiles = kt_end - kt_begin;
+    int tm, tn;
+    grouped_tile(tile, args.tiles_m, args.tiles_n, args.group_m, tm, tn);
+    const int m0 = tm * T::BM, n0 = tn * T::BN;
+
+    const AStage<T, AMODE> stage_a(args, m0, tid);
+    const BStage<T, BMODE> stage_b(args, n0, tid);
+
+    // Prologue: STAGES-1 tiles in flight.  One commit group per tile (empty
+    // groups keep the count uniform when K has fewer tiles).
+#pragma unroll
+    for (int s = 0; s < T::STAGES - 1; ++s) {
+      if (s < ktiles) {
+        stage_a.load(As, LA, s, kt_begin + s);
+        stage_b.load(Bs, LB, s, kt_begin + s);
       }
       cp_async_commit();
     }
 
-    const float* a_ptr = As + stage * LA.stage_size() + a_off;
-    const float* b_ptr = Bs + stage * LB.stage_size() + b_off;
+    // Warp `warp` of K group kg (kg = 0 without K slices).
+    const int kg = tid / 32 / T::TILE_WARPS;
+    const int warp = tid / 32 % T::TILE_WARPS, lane = tid % 32;
+    const int wm = warp / T::WARPS_N, wn = warp % T::WARPS_N;
+    const int lm = lane % T::LM, ln = lane / T::LM;
+    // Thread (lm, ln) of warp (wm, wn) owns rows wm*WM + i*LM + lm (i < TM)
+    // and columns wn*WN + g*LN*4 + ln*4 + c (g < TN/4, c < 4).  With A
+    // K-major the rows come in fours: wm*WM + (i/4)*LM*4 + lm*4 + i%4.
+    const auto row_of = [&](int i) {
+      return KMAJOR ? wm * T::WM + (i / 4) * T::LM * 4 + lm * 4 + i % 4
+                    : wm * T::WM + i * T::LM + lm;
+    };
+    // This group's first k step within a staged K tile.
+    constexpr int KS_STEPS = T::BK / T::KSLICES;
+    const int k_first = kg * KS_STEPS;
+    const int a_off = KMAJOR ? LA.offset(0, k_first, wm * T::WM + lm * 4)
+                             : LA.offset(0, wm * T::WM + lm, k_first);
+    const int b_off = LB.offset(0, k_first, wn * T::WN + ln * 4);
+
+    float2 acc[T::TM][T::TN / 2];
 #pragma unroll
-    for (int k4 = 0; k4 < KS_STEPS / 4; ++k4) {
-      // Row-major A: one float4 of four k per row, used over the next four
-      // k.  K-major A: one float4 of four rows per k.
-      float4 a[KMAJOR ? 1 : T::TM];
-      if constexpr (!KMAJOR) {
+    for (int i = 0; i < T::TM; ++i)
 #pragma unroll
-        for (int i = 0; i < T::TM; ++i)
-          a[i] = frag4(As, a_ptr + i * T::LM * LA.row_stride() + k4 * 4, LA.size(), args.bounds);
-      }
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        float4 ak[KMAJOR ? T::TM / 4 : 1];
-        if constexpr (KMAJOR) {
-#pragma unroll
-          for (int q = 0; q < T::TM / 4; ++q)
-            ak[q] = frag4(As, a_ptr + (k4 * 4 + kk) * LA.row_stride() + q * T::LM * 4, LA.size(),
-                          args.bounds);
+      for (int j = 0; j < T::TN / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
+
+    int stage = 0;
+    int load_stage = T::STAGES - 1;
+    for (int kt = 0; kt < ktiles; ++kt) {
+      if constexpr (T::STAGES == 1) {
+        // One stage, no double buffering (the pages' fallback form): copy
+        // tile kt, wait for it, barrier, compute, and a second barrier below
+        // before the next copy overwrites the stage.  Nothing overlaps the
+        // copies.
+        stage_a.load(As, LA, 0, kt_begin + kt);
+        stage_b.load(Bs, LB, 0, kt_begin + kt);
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+      } else {
+        // Tile kt has landed for this thread; the barrier makes every
+        // thread's copies visible and guarantees that the stage refilled
+        // below (read in iteration kt-1) is no longer being read.
+        cp_async_wait<T::STAGES - 2>();
+        __syncthreads();
+        if (kt + T::STAGES - 1 < ktiles) {
+          stage_a.load(As, LA, load_stage, kt_begin + kt + T::STAGES - 1);
+          stage_b.load(Bs, LB, load_stage, kt_begin + kt + T::STAGES - 1);
         }
-        float4 b[T::TN / 4];
+        cp_async_commit();
+      }
+
+      const float* a_ptr = As + stage * LA.stage_size() + a_off;
+      const float* b_ptr = Bs + stage * LB.stage_size() + b_off;
 #pragma unroll
-        for (int g = 0; g < T::TN / 4; ++g)
-          b[g] = frag4(Bs, b_ptr + (k4 * 4 + kk) * LB.row_stride() + g * T::LN * 4, LB.size(),
-                       args.bounds);
+      for (int k4 = 0; k4 < KS_STEPS / 4; ++k4) {
+        // Row-major A: one float4 of four k per row, used over the next four
+        // k.  K-major A: one float4 of four rows per k.
+        float4 a[KMAJOR ? 1 : T::TM];
+        if constexpr (!KMAJOR) {
 #pragma unroll
-        for (int g = 0; g < T::TN / 4; ++g) {
+          for (int i = 0; i < T::TM; ++i)
+            a[i] = frag4(As, a_ptr + i * T::LM * LA.row_stride() + k4 * 4, LA.size(), args.bounds);
+        }
 #pragma unroll
-          for (int i = 0; i < T::TM; ++i) {
-            const float av = KMAJOR ? pick(ak[i / 4], i % 4) : pick(a[i], kk);
-            if constexpr (PACKED) {
-              const float2 a2 = make_float2(av, av);
-              acc[i][2 * g] = __ffma2_rn(a2, make_float2(b[g].x, b[g].y), acc[i][2 * g]);
-              acc[i][2 * g + 1] = __ffma2_rn(a2, make_float2(b[g].z, b[g].w), acc[i][2 * g + 1]);
-            } else {
-              acc[i][2 * g].x = fmaf(av, b[g].x, acc[i][2 * g].x);
-              acc[i][2 * g].y = fmaf(av, b[g].y, acc[i][2 * g].y);
-              acc[i][2 * g + 1].x = fmaf(av, b[g].z, acc[i][2 * g + 1].x);
-              acc[i][2 * g + 1].y = fmaf(av, b[g].w, acc[i][2 * g + 1].y);
+        for (int kk = 0; kk < 4; ++kk) {
+          float4 ak[KMAJOR ? T::TM / 4 : 1];
+          if constexpr (KMAJOR) {
+#pragma unroll
+            for (int q = 0; q < T::TM / 4; ++q)
+              ak[q] = frag4(As, a_ptr + (k4 * 4 + kk) * LA.row_stride() + q * T::LM * 4, LA.size(),
+                            args.bounds);
+          }
+          float4 b[T::TN / 4];
+#pragma unroll
+          for (int g = 0; g < T::TN / 4; ++g)
+            b[g] = frag4(Bs, b_ptr + (k4 * 4 + kk) * LB.row_stride() + g * T::LN * 4, LB.size(),
+                         args.bounds);
+#pragma unroll
+          for (int g = 0; g < T::TN / 4; ++g) {
+#pragma unroll
+            for (int i = 0; i < T::TM; ++i) {
+              const float av = KMAJOR ? pick(ak[i / 4], i % 4) : pick(a[i], kk);
+              if constexpr (PACKED) {
+                const float2 a2 = make_float2(av, av);
+                acc[i][2 * g] = __ffma2_rn(a2, make_float2(b[g].x, b[g].y), acc[i][2 * g]);
+                acc[i][2 * g + 1] = __ffma2_rn(a2, make_float2(b[g].z, b[g].w), acc[i][2 * g + 1]);
+              } else {
+                acc[i][2 * g].x = fmaf(av, b[g].x, acc[i][2 * g].x);
+                acc[i][2 * g].y = fmaf(av, b[g].y, acc[i][2 * g].y);
+                acc[i][2 * g + 1].x = fmaf(av, b[g].z, acc[i][2 * g + 1].x);
+                acc[i][2 * g + 1].y = fmaf(av, b[g].w, acc[i][2 * g + 1].y);
+              }
             }
           }
         }
       }
+      if constexpr (T::STAGES == 1) __syncthreads();  // every read of the stage is done
+      stage = stage + 1 == T::STAGES ? 0 : stage + 1;
+      load_stage = load_stage + 1 == T::STAGES ? 0 : load_stage + 1;
     }
-    if constexpr (T::STAGES == 1) __syncthreads();  // every read of the stage is done
-    stage = stage + 1 == T::STAGES ? 0 : stage + 1;
-    load_stage = load_stage + 1 == T::STAGES ? 0 : load_stage + 1;
-  }
 
-  if constexpr (T::KSLICES > 1) {
-    // Add the K groups' sums through shared memory (the stages are free once
-    // every copy has landed and every thread is past its last read): groups
-    // 1.. store theirs, group 0 adds them in group order and goes on alone.
-    cp_async_wait<0>();
-    __syncthreads();
-    float* red = reinterpret_cast<float*>(smem_f4);
-    if (kg > 0) {
-      float* mine = red + (kg - 1) * (T::BM * T::BN);
+    if constexpr (T::KSLICES > 1) {
+      // Add the K groups' sums through shared memory (the stages are free once
+      // every copy has landed and every thread is past its last read): groups
+      // 1.. store theirs, group 0 adds them in group order and goes on alone.
+      cp_async_wait<0>();
+      __syncthreads();
+      float* red = reinterpret_cast<float*>(smem_f4);
+      if (kg > 0) {
+        float* mine = red + (kg - 1) * (T::BM * T::BN);
+#pragma unroll
+        for (int i = 0; i < T::TM; ++i) {
+          const int r = row_of(i);
+#pragma unroll
+          for (int g = 0; g < T::TN / 4; ++g) {
+            const int c = wn * T::WN + g * T::LN * 4 + ln * 4;
+            if (bounds_ok(args.bounds, SITE_SLICE_SUM, (mine - red) + r * T::BN + c, 4,
+                          T::REDUCE_BYTES / 4))
+              *reinterpret_cast<float4*>(mine + r * T::BN + c) =
+                  make_float4(acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
+                              acc[i][2 * g + 1].y);
+          }
+        }
+      }
+      __syncthreads();
+      if (kg > 0) continue;  // group 0 finishes the segment
+#pragma unroll
+      for (int s_ = 1; s_ < T::KSLICES; ++s_) {
+        const float* other = red + (s_ - 1) * (T::BM * T::BN);
+#pragma unroll
+        for (int i = 0; i < T::TM; ++i) {
+          const int r = row_of(i);
+#pragma unroll
+          for (int g = 0; g < T::TN / 4; ++g) {
+            const int c = wn * T::WN + g * T::LN * 4 + ln * 4;
+            const float4 o = frag4(red, other + r * T::BN + c, T::REDUCE_BYTES / 4, args.bounds);
+            acc[i][2 * g].x += o.x;
+            acc[i][2 * g].y += o.y;
+            acc[i][2 * g + 1].x += o.z;
+            acc[i][2 * g + 1].y += o.w;
+          }
+        }
+      }
+    }
+
+    if (partial_slot >= 0) {
+      // The segment's partial tile, dense BM x BN (rows and columns past M or
+      // N hold zeros from the zero-filled staging and are never read back).
+      float* P = args.partial + partial_slot * (T::BM * T::BN);
 #pragma unroll
       for (int i = 0; i < T::TM; ++i) {
         const int r = row_of(i);
 #pragma unroll
         for (int g = 0; g < T::TN / 4; ++g) {
           const int c = wn * T::WN + g * T::LN * 4 + ln * 4;
-          if (bounds_ok(args.bounds, SITE_SLICE_SUM, (mine - red) + r * T::BN + c, 4,
-                        T::REDUCE_BYTES / 4))
-            *reinterpret_cast<float4*>(mine + r * T::BN + c) =
+          if (bounds_ok(args.bounds, SITE_PARTIAL, (P - args.partial) + r * T::BN + c, 4,
+                        args.partial_extent))
+            *reinterpret_cast<float4*>(P + r * T::BN + c) =
                 make_float4(acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
                             acc[i][2 * g + 1].y);
         }
       }
+      continue;
     }
-    __syncthreads();
-    if (kg > 0) return;
-#pragma unroll
-    for (int s_ = 1; s_ < T::KSLICES; ++s_) {
-      const float* other = red + (s_ - 1) * (T::BM * T::BN);
-#pragma unroll
-      for (int i = 0; i < T::TM; ++i) {
-        const int r = row_of(i);
-#pragma unroll
-        for (int g = 0; g < T::TN / 4; ++g) {
-          const int c = wn * T::WN + g * T::LN * 4 + ln * 4;
-          const float4 o = frag4(red, other + r * T::BN + c, T::REDUCE_BYTES / 4, args.bounds);
-          acc[i][2 * g].x += o.x;
-          acc[i][2 * g].y += o.y;
-          acc[i][2 * g + 1].x += o.z;
-          acc[i][2 * g + 1].y += o.w;
-        }
-      }
-    }
-  }
 
-  if (partial) {
-    // The slice's partial tile, dense BM x BN (rows and columns past M or N
-    // hold zeros from the zero-filled staging and are never read back).
-    float* P = args.partial +
-               (static_cast<int64_t>(tile - args.full_tiles) * args.split + slice) *
-                   (T::BM * T::BN);
+    // Masked epilogue: C[row, col] = alpha * acc + beta * C[row, col]
+    // (+ bias[col]) for row < M, col < N (C is not read when beta == 0;
+    // alpha == 1, beta == 0 and no bias store acc unchanged).
+    float* C = args.C;
+    const float alpha = args.alpha, beta = args.beta;
+    const float* bias = args.bias;
 #pragma unroll
     for (int i = 0; i < T::TM; ++i) {
-      const int r = row_of(i);
+      const int row = m0 + row_of(i);
+      if (row >= M) continue;
+      float* c_row = C + static_cast<int64_t>(row) * args.ldc;
 #pragma unroll
       for (int g = 0; g < T::TN / 4; ++g) {
-        const int c = wn * T::WN + g * T::LN * 4 + ln * 4;
-        if (bounds_ok(args.bounds, SITE_PARTIAL, (P - args.partial) + r * T::BN + c, 4,
-                      args.partial_extent))
-          *reinterpret_cast<float4*>(P + r * T::BN + c) =
-              make_float4(acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
-                          acc[i][2 * g + 1].y);
-      }
-    }
-    return;
-  }
-
-  // Masked epilogue: C[row, col] = alpha * acc + beta * C[row, col]
-  // (+ bias[col]) for row < M, col < N (C is not read when beta == 0;
-  // alpha == 1, beta == 0 and no bias store acc unchanged).
-  float* C = args.C;
-  const float alpha = args.alpha, beta = args.beta;
-  const float* bias = args.bias;
-#pragma unroll
-  for (int i = 0; i < T::TM; ++i) {
-    const int row = m0 + row_of(i);
-    if (row >= M) continue;
-    float* c_row = C + static_cast<int64_t>(row) * args.ldc;
-#pragma unroll
-    for (int g = 0; g < T::TN / 4; ++g) {
-      const int col = n0 + wn * T::WN + g * T::LN * 4 + ln * 4;
-      float4 v = make_float4(alpha * acc[i][2 * g].x, alpha * acc[i][2 * g].y,
-                             alpha * acc[i][2 * g + 1].x, alpha * acc[i][2 * g + 1].y);
-      if constexpr (VEC) {
-        // N % 4 == 0, so a float4 group is either wholly inside or outside.
-        if (col < N && bounds_ok(args.bounds, SITE_C_STORE, (c_row - C) + col, 4, args.c_extent) &&
-            (!bias || bounds_ok(args.bounds, SITE_BIAS, col, 4, N))) {
-          float4* cp = reinterpret_cast<float4*>(c_row + col);
-          if (beta != 0.0f) {
-            const float4 o = *cp;
-            v = make_float4(fmaf(beta, o.x, v.x), fmaf(beta, o.y, v.y), fmaf(beta, o.z, v.z),
-                            fmaf(beta, o.w, v.w));
+        const int col = n0 + wn * T::WN + g * T::LN * 4 + ln * 4;
+        float4 v = make_float4(alpha * acc[i][2 * g].x, alpha * acc[i][2 * g].y,
+                               alpha * acc[i][2 * g + 1].x, alpha * acc[i][2 * g + 1].y);
+        if constexpr (VEC) {
+          // N % 4 == 0, so a float4 group is either wholly inside or outside.
+          if (col < N &&
+              bounds_ok(args.bounds, SITE_C_STORE, (c_row - C) + col, 4, args.c_extent) &&
+              (!bias || bounds_ok(args.bounds, SITE_BIAS, col, 4, N))) {
+            float4* cp = reinterpret_cast<float4*>(c_row + col);
+            if (beta != 0.0f) {
+              const float4 o = *cp;
+              v = make_float4(fmaf(beta, o.x, v.x), fmaf(beta, o.y, v.y), fmaf(beta, o.z, v.z),
+                              fmaf(beta, o.w, v.w));
+            }
+            if (bias) {
+              v.x += bias[col];
+              v.y += bias[col + 1];
+              v.z += bias[col + 2];
+              v.w += bias[col + 3];
+            }
+            *cp = v;
           }
-          if (bias) {
-            v.x += bias[col];
-            v.y += bias[col + 1];
-            v.z += bias[col + 2];
-            v.w += bias[col + 3];
-          }
-          *cp = v;
+        } else {
+          const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (col + e < N &&
+                bounds_ok(args.bounds, SITE_C_STORE, (c_row - C) + col + e, 1, args.c_extent) &&
+                (!bias || bounds_ok(args.bounds, SITE_BIAS, col + e, 1, N))) {
+              float o = beta != 0.0f ? fmaf(beta, c_row[col + e], vv[e]) : vv[e];
+              if (bias) o += bias[col + e];
+              c_row[col + e] = o;
+            }
         }
-      } else {
-        const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (col + e < N &&
-              bounds_ok(args.bounds, SITE_C_STORE, (c_row - C) + col + e, 1, args.c_extent) &&
-              (!bias || bounds_ok(args.bounds, SITE_BIAS, col + e, 1, N))) {
-            float o = beta != 0.0f ? fmaf(beta, c_row[col + e], vv[e]) : vv[e];
-            if (bias) o += bias[col + e];
-            c_row[col + e] = o;
-          }
       }
     }
-  }
+  }  // segment
 }
 
 // Only the kernels a flag asks for are instantiated (the others stay
