@@ -446,19 +446,54 @@ def run_gpu(args):
     dom = max(bufs, key=lambda x: statistics.mean(per_launch[x[0].name]))[0]
     dom_ms = statistics.mean(per_launch[dom.name])
     dp = plans[dom.name]
+    tf32_measured = {}
+
+    def cublas_tf32_peak():
+        """cuBLAS's TF32 GEMM (torch.matmul with TF32 on) on the step's
+        largest operands, best of 5 by CUDA events after 3 warm-ups: the
+        measured TF32 tensor rate of this GPU in this run."""
+        if not tf32_measured:
+            w, a, b, c = max(operands(None), key=lambda x: x[0].flops)
+            prev = torch.backends.cuda.matmul.allow_tf32
+            torch.backends.cuda.matmul.allow_tf32 = True
+            try:
+                for _ in range(3):
+                    torch.matmul(a, b, out=c)
+                best = float("inf")
+                for _ in range(5):
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    torch.matmul(a, b, out=c)
+                    e1.record(stream)
+                    e1.synchronize()
+                    best = min(best, e0.elapsed_time(e1))
+            finally:
+                torch.backends.cuda.matmul.allow_tf32 = prev
+            tf32_measured.update(value=w.flops / (best / 1e3) / 1e12, workload=w.name,
+                                 ms=best)
+        return tf32_measured
+
     def tf32_roofline(achieved, key):
         clock_peak = tf32_clock_peak(sms, sm_max)
-        return {"bound": "tensor", "achieved": achieved, "peak": tf32_peak,
-                "unit": "TFLOP/s", "frac": achieved / tf32_peak,
-                "traffic": load_traffic(key), "kernel": key, "peak_basis": tf32_basis,
+        m = cublas_tf32_peak()
+        return {"bound": "tensor", "achieved": achieved, "peak": m["value"],
+                "unit": "TFLOP/s", "frac": achieved / m["value"],
+                "traffic": load_traffic(key), "kernel": key,
+                "peak_basis": "measured: cuBLAS TF32 GEMM (torch.matmul, TF32 on) on the "
+                              f"{m['workload']} operands in this run, best of 5 "
+                              f"({m['ms']:.3f} ms)",
+                "nominal_peak": tf32_peak, "frac_of_nominal_peak": achieved / tf32_peak,
+                "nominal_peak_basis": tf32_basis,
                 "clock_peak": clock_peak, "frac_of_clock_peak": achieved / clock_peak,
                 "clock_peak_basis": f"{sms} SMs x {TF32_FLOP_PER_CLK_SM} tf32 flop/clk "
                                     f"x {sm_max:.0f} MHz",
                 "note": "achieved = 3 x 2MNK tf32 flops / time of the whole call (pack "
                         "kernels included, so it understates the GEMM kernel's own rate); "
-                        "traffic is the GEMM kernel's.  Half-rate tf32 MMAs are not held "
-                        "down by the power cap the way the bf16 reference GEMM is, so frac "
-                        "can read above 1"}
+                        "traffic is the GEMM kernel's.  cuBLAS's TF32 GEMM is a library "
+                        "kernel, not the hardware's limit, so frac can read above 1; "
+                        "frac_of_clock_peak is against the tensor pipe's rate at the "
+                        "maximum clock"}
 
     def key_of(v, plan, name):
         return f"{v}_{plan['bm']}x{plan['bn']}x{plan['bk']}_s{plan['stages']}_{name}"

@@ -614,6 +614,12 @@ mt_status plan_ffma(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
   }
   L->entry = i;
   L->kern = kern;
+  // Raster groups of 16 tile rows: a wave of 304 CTAs then spans about 16 x
+  // 19 tiles, close to square, so it touches fewer A and B panels than with
+  // groups of 8 (38 columns).  Measured on GB300 with 128 x 128 tiles, the
+  // time unchanged: DRAM read 333 -> 284 MB at 4096^3, 3.30 -> 3.23 GB at
+  // 8192^3 (32 rows: 499 MB and 4.72 GB).
+  if (!(cfg && cfg->group_m)) L->group_m = 16;
   L->tiles_m = static_cast<int>(ceil_div(M, E.bm));
   L->tiles_n = static_cast<int>(ceil_div(N, E.bn));
   const int64_t tiles = static_cast<int64_t>(L->tiles_m) * L->tiles_n;

@@ -264,6 +264,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched as a programmatic dependent of the pack kernel before it on the
+  // stream: the set-up above overlaps that kernel's end; nothing below reads
+  // or writes global memory before it has completed and its stores are
+  // visible (a no-op when launched without the attribute).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   uint32_t issued = 0;  // producer: K tiles issued by this CTA, across its tiles
   if (warp == 0) {
@@ -458,6 +463,11 @@ __global__ void __launch_bounds__(ASPLIT_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched as a programmatic dependent of the pack kernel before it on the
+  // stream: the set-up above overlaps that kernel's end; nothing below reads
+  // or writes global memory before it has completed and its stores are
+  // visible (a no-op when launched without the attribute).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   uint32_t issued = 0;
   if (warp == 0) {
@@ -663,6 +673,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched as a programmatic dependent of the pack kernel before it on the
+  // stream: the set-up above overlaps that kernel's end; nothing below reads
+  // or writes global memory before it has completed and its stores are
+  // visible (a no-op when launched without the attribute).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
     if (lane == 0) {
@@ -777,6 +792,37 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 namespace {
 
+// Launches a GEMM kernel as a programmatic dependent of the pack kernel
+// before it on `stream` (clusters of `cluster` CTAs when > 1): its CTAs are
+// scheduled as the packer's retire and set up their barriers and tensor
+// memory, then wait for the packed operands (griddepcontrol.wait).  The
+// arguments are passed by address in declaration order.
+template <class... Args>
+cudaError_t launch_after_pack(const void* kernel, dim3 grid, int threads, int smem_bytes,
+                              int cluster, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  void* ptrs[] = {static_cast<void*>(&args)...};
+  return cudaLaunchKernelExC(&cfg, kernel, ptrs);
+}
+
 template <int BK, int BN>
 struct Cfg {
   using G = tf32x3::Geometry<BK, BN>;
@@ -826,11 +872,12 @@ struct Cfg {
                                                 workspace_bytes_packed(a.M, a.N, a.K));
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int grid = units < max_ctas ? units : max_ctas;
-    tf32x3_gemm_kernel<G><<<grid, THREADS, G::SMEM_BYTES, stream>>>(
-        Ap, Bp, make_epilogue(a, vec_c, tiles, BM, BN), kt, mt, nt,
-        a.group_m,
-        sched, fault_inject);
     cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const Epilogue ep = make_epilogue(a, vec_c, tiles, BM, BN);
+    e = launch_after_pack(reinterpret_cast<const void*>(tf32x3_gemm_kernel<G>), dim3(grid),
+                          THREADS, G::SMEM_BYTES, 1, stream, Ap, Bp, ep, kt, mt, nt,
+                          a.group_m, sched, fault_inject);
     if (e != cudaSuccess || a.split <= 1) return e;
     GemmArgs r = a;
     r.partial = sched.partial;
@@ -915,22 +962,9 @@ struct CfgPair {
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int clusters = units < max_clusters ? units : max_clusters;
     const Epilogue ep = make_epilogue(a, vec_c, tiles, PAIR_TILE, PAIR_TILE);
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = G::SMEM_BYTES;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int kt_arg = kt, mt_arg = mt, nt_arg = nt, group_m = a.group_m, fi = fault_inject;
-    Epilogue ep_arg = ep;
-    void* args[] = {&map_a, &map_b, &ep_arg, &kt_arg, &mt_arg, &nt_arg, &group_m, &sched, &fi};
-    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(tf32x3_pair_kernel<BK>), args);
+    e = launch_after_pack(reinterpret_cast<const void*>(tf32x3_pair_kernel<BK>),
+                          dim3(2 * clusters), THREADS, G::SMEM_BYTES, 2, stream, map_a, map_b,
+                          ep, kt, mt, nt, a.group_m, sched, fault_inject);
     if (e != cudaSuccess || a.split <= 1) return e;
     GemmArgs r = a;
     r.partial = sched.partial;
@@ -980,10 +1014,11 @@ struct CfgASplit {
                                                 CfgASplit::workspace(a.M, a.N, a.K));
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int grid = units < max_ctas ? units : max_ctas;
-    tf32x3_asplit_kernel<BK, BN><<<grid, ASPLIT_THREADS, AG::SMEM_BYTES, stream>>>(
-        map_a, Bp, make_epilogue(a, vec_c, tiles, BM, BN), kt,
-        mt, nt, a.group_m, sched, fault_inject);
-    e = cudaGetLastError();
+    const Epilogue ep = make_epilogue(a, vec_c, tiles, BM, BN);
+    e = launch_after_pack(reinterpret_cast<const void*>(tf32x3_asplit_kernel<BK, BN>),
+                          dim3(grid), ASPLIT_THREADS, AG::SMEM_BYTES, 1, stream, map_a,
+                          static_cast<const float*>(Bp), ep, kt, mt, nt, a.group_m, sched,
+                          fault_inject);
     if (e != cudaSuccess || a.split <= 1) return e;
     GemmArgs r = a;
     r.partial = sched.partial;
