@@ -115,16 +115,18 @@ typedef struct {
                       gathered.  Every choice gives the same bits. */
     int group_m;   /* tile rows per group of the tile raster (tiles are walked
                       down a group's rows, then across); 0 = automatic */
-    int schedule;  /* MT_VARIANT_FFMA: how tiles that do not fill a whole wave of
-                      resident CTAs are run.  0 = automatic; 1 = whole tiles, with
-                      a grid smaller than the SMs or a last wave under half full
-                      cut into equal K slices (split tail); 2 = stream-K: those
-                      tiles' K tiles spread evenly over one wave of CTAs, each
-                      taking a contiguous run across tile boundaries, and the
-                      pieces of a tile added in k order by a second kernel
-                      (deterministic).  split_k = 1 turns both off; split_k > 1
-                      with 2 is MT_ERR_UNSUPPORTED, as are tiles whose warps form
-                      K groups.  Other variants: 0 only. */
+    int schedule;  /* How tiles that do not fill a whole wave of resident CTAs
+                      are run.  0 = automatic; 1 = whole tiles, with a grid
+                      smaller than the SMs or a last wave under half full cut
+                      into equal K slices (split tail); 2 = stream-K: those
+                      tiles' K tiles spread evenly over one wave of CTAs (for
+                      the persistent tensor-core kernels, over the grid after
+                      each CTA's whole tiles), each taking a contiguous run
+                      across tile boundaries, and the pieces of a tile added in
+                      k order by a second kernel (deterministic).  split_k = 1
+                      turns both off; split_k > 1 with 2, FFMA tiles whose
+                      warps form K groups and MT_VARIANT_P18 are
+                      MT_ERR_UNSUPPORTED. */
 } mt_config;
 
 /* What a call with the same arguments would launch. */

@@ -1,4 +1,4 @@
-"""GPU parity of the FFMA kernel's stream-K schedule against the CPU oracle.
+"""GPU parity of the stream-K schedule (FFMA and tensor-core kernels) against the CPU oracle.
 
 Stream-K (mt_config.schedule = 2) spreads the K tiles of the tiles past the
 last whole wave over one wave of CTAs, each taking a contiguous run across
@@ -134,13 +134,108 @@ def test_stream_k_general_form_alpha_beta_bias():
 
 def test_stream_k_choices_refused():
     # Explicit split_k with stream-K, tiles whose warps form K groups, and
-    # the other variants refuse the schedule before any launch.
+    # the one-warp kernel refuse the schedule before any launch.
     with pytest.raises(mt.MtError):
         mt.plan(1024, 1024, 1024, split_k=2, **SK)
     with pytest.raises(mt.MtError):
         mt.plan(1024, 1024, 1024, bm=64, bn=128, stages=3, pack_a=4, **SK)
     with pytest.raises(mt.MtError):
-        mt.plan(1024, 1024, 1024, variant="tf32x3", **SK)
+        mt.plan(1024, 1024, 1024, variant="p18", **SK)
     # split_k = 1 turns stream-K off like the split tail.
     p = mt.plan(1024, 1024, 1024, split_k=1, **SK)
     assert p["stream_k"] == 0 and p["split_k"] == 1
+
+
+# --- the persistent tensor-core kernels ----------------------------------------
+# The same schedule on the tcgen05 kernels: after its whole tiles, each CTA
+# (CTA pair) of the persistent grid takes a run of the remaining tiles' K
+# tiles; the same fix-up adds the pieces.  Tolerance 5e-5 * W, as for every
+# tensor-core path.
+TC_TOL = 5e-5
+TF32_TILES = [dict(variant="tf32x3"),                                  # automatic
+              dict(variant="tf32x3", bm=128, bn=256, bk=16, pack_a=1),  # one CTA per tile
+              dict(variant="tf32x3", bm=128, bn=64, bk=32, pack_a=1),
+              dict(variant="tf32x3", bm=256, bk=16),                    # CTA pairs
+              dict(variant="tf32x3", bm=128, bn=128, bk=32, pack_a=2)]  # A split in the kernel
+TF32_IDS = ["-".join(f"{k}{v}" for k, v in c.items()) for c in TF32_TILES]
+
+
+def assert_tc(C, Cref, W, what):
+    err = np.abs(np.asarray(C, np.float64) - Cref)
+    bad = err > TC_TOL * W
+    if bad.any():
+        i, j = np.argwhere(bad)[0]
+        pytest.fail(f"{what}: {bad.sum()} outputs outside {TC_TOL}*W, first at ({i},{j})")
+
+
+@pytest.mark.parametrize("cfg", TF32_TILES, ids=TF32_IDS)
+@pytest.mark.parametrize("name", ["masked_100x72x80", "square_1024", "ragged_4097x3001x2053"])
+def test_stream_k_tf32x3_workloads(name, cfg, full_oracle):
+    w = gemm_inputs.WORKLOADS[name]
+    if cfg.get("pack_a") == 2 and w.K % 4:
+        pytest.skip("A split in the kernel needs rows of whole float4s")
+    A, B = gemm_inputs.make_workload(name)
+    a, b = A.cuda(), B.cuda()
+    p = mt.plan(w.M, w.N, w.K, a=a, b=b, **SK, **cfg)
+    assert p["stream_k"] > 0 and p["split_k"] == 1
+    got = run(a, b, **SK, **cfg)
+    Cref, W = full_oracle(name)
+    assert_tc(got, Cref, W, f"{name} {cfg}")
+    assert np.array_equal(run(a, b, **SK, **cfg), got)
+
+
+@pytest.mark.parametrize("cfg", TF32_TILES, ids=TF32_IDS)
+@pytest.mark.parametrize("shape", [(100, 72, 80), (1000, 1000, 1200), (2304, 2304, 256)])
+def test_stream_k_tf32x3_integer_inputs_bit_exact(shape, cfg):
+    M, N, K = shape
+    A, B = gemm_inputs.make_ab(M, N, K, seed=12, dist="int")
+    Cref = oracle.sgemm(A.numpy(), B.numpy())
+    assert np.array_equal(run(A.cuda(), B.cuda(), **SK, **cfg), Cref)
+
+
+def test_stream_k_tf32x3_square_4096_every_element(full_oracle):
+    A, B = gemm_inputs.make_workload("square_4096")
+    p = mt.plan(4096, 4096, 4096, variant="tf32x3", **SK)
+    assert p["stream_k"] > 0 and p["bm"] == 256
+    got = run(A.cuda(), B.cuda(), variant="tf32x3", **SK)
+    Cref, W = full_oracle("square_4096")
+    assert_tc(got, Cref, W, "square_4096 tf32x3 stream-K")
+
+
+_MIXED_REF = {}
+
+
+@pytest.mark.parametrize("tile", [dict(), dict(bm=128), dict(bm=128, bn=128), dict(bm=256)],
+                         ids=["auto", "single", "bn128", "pair"])
+@pytest.mark.parametrize("shape", [(100, 72, 80), (1024, 1024, 1024), (4097, 3001, 2053),
+                                   (4096, 4096, 4096)])
+def test_stream_k_16bit_inputs(shape, tile):
+    M, N, K = shape
+    A16, B16 = gemm_inputs.make_ab16(M, N, K, 3, "normal", "bf16")
+    p = mt.plan_mixed(mt.MT_DTYPE_BF16, M, N, K, **SK, **tile)
+    assert p["stream_k"] > 0 and p["split_k"] == 1
+    if shape not in _MIXED_REF:  # one oracle run per shape for all tiles
+        _MIXED_REF.clear()
+        _MIXED_REF[shape] = oracle.gemm_mixed_general(
+            oracle.BF16, A16, B16, np.zeros(M * N, np.float32), M, N, K, K, N, N, with_w=True)
+    Cref, W = _MIXED_REF[shape]
+    a, b = A16.cuda(), B16.cuda()
+    got = mt.gemm_mixed(a, b, **SK, **tile)
+    torch.cuda.synchronize()
+    got = got.cpu().numpy()
+    assert_tc(got, Cref.reshape(M, N), W.reshape(M, N), f"bf16 {shape} {tile}")
+    again = mt.gemm_mixed(a, b, **SK, **tile)
+    torch.cuda.synchronize()
+    assert np.array_equal(again.cpu().numpy(), got)
+    assert mt.mt_check_device_status(0) == mt.MT_OK
+
+
+def test_stream_k_16bit_integer_inputs_bit_exact():
+    M, N, K = 1000, 1000, 1200
+    A16, B16 = gemm_inputs.make_ab16(M, N, K, 4, "int", "bf16")
+    Cref = oracle.gemm_mixed_general(oracle.BF16, A16, B16, np.zeros(M * N, np.float32),
+                                     M, N, K, K, N, N)
+    for tile in (dict(), dict(bm=128), dict(bm=256)):
+        got = mt.gemm_mixed(A16.cuda(), B16.cuda(), **SK, **tile)
+        torch.cuda.synchronize()
+        assert np.array_equal(got.cpu().numpy(), Cref.reshape(M, N)), tile

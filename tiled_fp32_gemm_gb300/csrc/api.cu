@@ -351,6 +351,22 @@ bool auto_pair(int64_t M, int64_t N, int bn, int sms, int pair_clusters) {
   return ceil_div(M, 256) * ceil_div(N, 256) >= clusters;
 }
 
+// Stream-K plan of a persistent tensor-core kernel (schedule 2) over
+// `tiles` tiles of `ktiles` K tiles on `max_ctas` resident CTAs (clusters):
+// the full waves stay whole tiles; the tiles past them are dealt out as
+// contiguous runs of K tiles, at least two per run.  Sets the launch's
+// stream-K fields; false when there is nothing to deal out.
+bool plan_persistent_streamk(int64_t tiles, int64_t ktiles, int max_ctas, Launch* L) {
+  const int64_t G = std::max(1, max_ctas);
+  const int64_t rem = tiles % G;
+  if (rem == 0 || ktiles <= 0) return false;
+  L->full_tiles = static_cast<int>(tiles - rem);
+  L->split = 1;
+  L->sk_iters = rem * ktiles;
+  L->sk_ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(G, L->sk_iters / 2)));
+  return true;
+}
+
 // The 16-bit kernels (MT_VARIANT_TC16): 128 x BN tiles on one CTA, or 256 x
 // 256 tiles on a CTA pair (bm = 256); BK = 64, persistent with a split
 // tail; operands TMA cannot read in place are copied first.  pair_clusters:
@@ -393,13 +409,19 @@ mt_status plan_f16(const Problem& P, const mt_config* cfg, int64_t smem_limit, i
   if (pair) L->max_ctas = pair_clusters > 0 ? pair_clusters : std::max(1, sms / 2);
   else L->max_ctas = sms > 0 ? sms : 1;
   int64_t full = tiles, split = 1;
-  split_tail(tiles, std::min<int64_t>(tiles, L->max_ctas), ceil_div(K, bk),
-             !(cfg && cfg->split_k == 1), &full, &split);
+  const bool streamk = cfg && cfg->schedule == 2 && cfg->split_k != 1;
+  if (!streamk)
+    split_tail(tiles, std::min<int64_t>(tiles, L->max_ctas), ceil_div(K, bk),
+               !(cfg && cfg->split_k == 1), &full, &split);
   L->full_tiles = static_cast<int>(full);
   L->split = static_cast<int>(split);
   L->kt_per_slice = static_cast<int>(ceil_div(ceil_div(K, bk), split));
+  if (streamk) plan_persistent_streamk(tiles, ceil_div(K, bk), L->max_ctas, L);
   p.split_k = L->split;
-  p.grid = std::min<int64_t>(full + (tiles - full) * split, L->max_ctas) * (pair ? 2 : 1);
+  p.stream_k = L->sk_ctas;
+  p.grid = (L->sk_ctas > 0 ? (L->full_tiles > 0 ? L->max_ctas : L->sk_ctas)
+                           : std::min<int64_t>(full + (tiles - full) * split, L->max_ctas)) *
+           (pair ? 2 : 1);
   const mt::F16Layout lay =
       mt::f16tc_layout(make_args(P, *L), mt::F16Operands{P.A, P.B, P.dtype}, bm, bn);
   p.vec_ab = lay.repack_a_bytes == 0 && lay.repack_b_bytes == 0;
@@ -483,16 +505,23 @@ mt_status plan_tf32x3(const Problem& P, const mt_config* cfg, int64_t smem_limit
   const int64_t ctas = std::min<int64_t>(tiles, L->max_ctas);
   const int64_t ktiles = ceil_div(K, bk);
   int64_t full = tiles, split = 1;
-  split_tail(tiles, ctas, ktiles, !(cfg && cfg->split_k == 1), &full, &split);
+  const bool streamk = cfg && cfg->schedule == 2 && cfg->split_k != 1;
+  if (!streamk) split_tail(tiles, ctas, ktiles, !(cfg && cfg->split_k == 1), &full, &split);
   L->full_tiles = static_cast<int>(full);
   L->split = static_cast<int>(split);
   L->kt_per_slice = static_cast<int>(ceil_div(ktiles, split));
+  if (streamk) plan_persistent_streamk(tiles, ktiles, L->max_ctas, L);
   p.split_k = L->split;
+  p.stream_k = L->sk_ctas;
   const int64_t units = full + (tiles - full) * split;
-  p.grid = std::min<int64_t>(units, L->max_ctas) * (pair ? 2 : 1);
+  p.grid = (L->sk_ctas > 0 ? (L->full_tiles > 0 ? L->max_ctas : L->sk_ctas)
+                           : std::min<int64_t>(units, L->max_ctas)) *
+           (pair ? 2 : 1);
   p.workspace_bytes = mt::tf32x3_workspace_bytes(static_cast<int>(M), static_cast<int>(N),
                                                  static_cast<int>(K), bm, bk, bn, split_a) +
-                      (tiles - full) * split * bm * bn * 4;
+                      (L->sk_ctas > 0 ? 2 * static_cast<int64_t>(L->sk_ctas)
+                                      : (tiles - full) * split) *
+                          bm * bn * 4;
   if (p.smem_bytes > smem_limit) return MT_ERR_SMEM_BUDGET;
   return MT_OK;
 }
@@ -729,10 +758,8 @@ mt_status plan_call(const Problem& P, const mt_config* cfg, int64_t smem_limit, 
               cfg->pack_a > 5 || cfg->group_m < 0 || cfg->schedule < 0 ||
               cfg->schedule > 2))
     return MT_ERR_INVALID_ARG;
-  // The schedule choice is the FFMA kernel's (the tensor-core kernels are
-  // persistent with a split tail of their own).
-  if (cfg && cfg->schedule && (P.dtype || variant != MT_VARIANT_FFMA))
-    return MT_ERR_UNSUPPORTED;
+  // The one-warp kernel has one schedule: a CTA per tile.
+  if (cfg && cfg->schedule && !P.dtype && variant == MT_VARIANT_P18) return MT_ERR_UNSUPPORTED;
   if (P.dtype)
     return plan_f16(P, cfg, smem_limit, sms, dev >= 0 ? mt::f16tc_pair_max_clusters(dev) : 0,
                     L);

@@ -127,7 +127,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int num_tiles = tiles_m * tiles_n;
-  const int num_units = sched.full_tiles + (num_tiles - sched.full_tiles) * sched.split;
+  const int cta = static_cast<int>(blockIdx.x), ctas = static_cast<int>(gridDim.x);
+  const int num_units = units_of(cta, ctas, sched, num_tiles, Kt);  // this CTA's units
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmap_a);
@@ -157,8 +158,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       // on its data runs out (the test of the timeout path).
       uint32_t& g = issued;
       bool stop = fault_inject != 0;
-      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
-        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      for (int u = 0; u < num_units && !stop; ++u) {
+        const Unit w = unit_at(u, cta, ctas, sched, tiles_m, tiles_n, group_m, Kt);
         for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
           const uint32_t s = g % STAGES, round = g / STAGES;
           if (g >= STAGES && !wait_phase(bar(EMPTY + s), (round + 1) & 1u, wc)) {
@@ -178,8 +179,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t g = 0;
       bool stop = false;
       int it = 0;
-      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x, ++it) {
-        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      for (int u = 0; u < num_units && !stop; ++u, ++it) {
+        const Unit w = unit_at(u, cta, ctas, sched, tiles_m, tiles_n, group_m, Kt);
         const int b = it & 1;
         // The epilogue must have drained this accumulator (used by unit it-2).
         if (it >= 2 && !wait_phase(bar(ACC_EMPTY + b), ((it >> 1) + 1) & 1u, wc)) break;
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int it = 0;
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++it) {
+    for (int u = 0; u < num_units; ++u, ++it) {
       const int b = it & 1;
       // A unit's accumulator is ready after its whole K loop.  The warp
       // goes on only if every lane saw it (tcgen05.ld needs the whole warp).
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after();
       __syncwarp();
-      const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      const Unit w = unit_at(u, cta, ctas, sched, tiles_m, tiles_n, group_m, Kt);
       store_accumulator<BM, BN>(tmem + lane_base + static_cast<uint32_t>(b * BN), w, q, lane,
                                 ep, sched.partial);
       tc_fence_before();
@@ -304,7 +305,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int cluster = static_cast<int>(cluster_id_x());
   const int clusters = static_cast<int>(cluster_count_x());
   const int num_tiles = tiles_m * tiles_n;
-  const int num_units = sched.full_tiles + (num_tiles - sched.full_tiles) * sched.split;
+  const int num_units = units_of(cluster, clusters, sched, num_tiles, Kt);  // this cluster's units
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmap_a);
@@ -332,8 +333,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       // Producer (both CTAs): this CTA's halves into its own stages.
       bool stop = fault_inject != 0;
       uint32_t g = 0;
-      for (int u = cluster; u < num_units && !stop; u += clusters) {
-        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      for (int u = 0; u < num_units && !stop; ++u) {
+        const Unit w = unit_at(u, cluster, clusters, sched, tiles_m, tiles_n, group_m, Kt);
         const int r0a = w.tm * PAIR_TILE + static_cast<int>(rank) * PAIR_HALF;
         const int r0b = w.tn * PAIR_TILE + static_cast<int>(rank) * PAIR_HALF;
         for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
@@ -368,8 +369,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t g = 0;
       bool stop = false;
       int it = 0;
-      for (int u = cluster; u < num_units && !stop; u += clusters, ++it) {
-        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      for (int u = 0; u < num_units && !stop; ++u, ++it) {
+        const Unit w = unit_at(u, cluster, clusters, sched, tiles_m, tiles_n, group_m, Kt);
         const int b = it % ACC_BUFS, use = it / ACC_BUFS;
         // Both CTAs' epilogues must have drained this accumulator.
         if (use >= 1 && !wait_phase(bar(ACC_EMPTY + b), (use + 1) & 1u, wc)) break;
@@ -405,14 +406,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t acc_empty_even = map_to_cta(bar(ACC_EMPTY), 0);
     int it = 0;
-    for (int u = cluster; u < num_units; u += clusters, ++it) {
+    for (int u = 0; u < num_units; ++u, ++it) {
       const int b = it % ACC_BUFS, use = it / ACC_BUFS;
       const bool ready = wait_phase(bar(ACC_FULL + b), use & 1u, wc, true,
                                     TIMEOUT_NS + 20000ull * static_cast<uint64_t>(Kt));
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after();
       __syncwarp();
-      const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      const Unit w = unit_at(u, cluster, clusters, sched, tiles_m, tiles_n, group_m, Kt);
       store_accumulator<PAIR_HALF, PAIR_TILE, PAIR_TILE>(
           tmem + lane_base + static_cast<uint32_t>(b * PAIR_TILE), w, q, lane, ep,
           sched.partial, static_cast<int>(rank) * PAIR_HALF);
@@ -564,10 +565,11 @@ struct Cfg16 {
     const uint32_t fmt = f.dtype == 1 ? 0u : 1u;  // kind::f16 operand format: f16 0, bf16 1
     const uint32_t idesc = tc::instr_desc(BM, BN, fmt, fmt, a_mn ? 1u : 0u, b_mn ? 1u : 0u);
     const int tiles = mt * nt;
-    tc::Sched sched{a.full_tiles, a.split, a.kt_per_slice, nullptr};
-    if (a.split > 1) sched.partial = reinterpret_cast<float*>(ws + L.partial_offset);
+    tc::Sched sched{a.full_tiles, a.split, a.kt_per_slice, nullptr, a.sk_ctas, a.sk_iters};
+    if (a.split > 1 || a.sk_ctas > 0)
+      sched.partial = reinterpret_cast<float*>(ws + L.partial_offset);
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
-    const int grid = units < max_ctas ? units : max_ctas;
+    const int grid = persistent_grid(a, units, max_ctas);
     const tc::Epilogue ep = tc::make_epilogue(a, vec_c, tiles, BM, BN);
     auto go = [&](auto kern) {
       kern<<<grid, f16tc::THREADS, G::SMEM_BYTES, stream>>>(map_a, map_b, idesc, ep, kt, mt, nt,
@@ -578,10 +580,8 @@ struct Cfg16 {
     else if (a_mn && !b_mn) go(kernel<true, false>());
     else go(kernel<true, true>());
     e = cudaGetLastError();
-    if (e != cudaSuccess || a.split <= 1) return e;
-    GemmArgs r = a;
-    r.partial = sched.partial;
-    return launch_splitk_reduce(r, BM, BN, vec_c, stream);
+    if (e != cudaSuccess) return e;
+    return launch_second_pass(a, sched.partial, BM, BN, kt, vec_c, stream);
   }
 };
 
@@ -659,10 +659,11 @@ struct CfgPair {
     const uint32_t idesc =
         tc::instr_desc(PAIR_TILE, PAIR_TILE, fmt, fmt, a_mn ? 1u : 0u, b_mn ? 1u : 0u);
     const int tiles = mt * nt;
-    tc::Sched sched{a.full_tiles, a.split, a.kt_per_slice, nullptr};
-    if (a.split > 1) sched.partial = reinterpret_cast<float*>(ws + L.partial_offset);
+    tc::Sched sched{a.full_tiles, a.split, a.kt_per_slice, nullptr, a.sk_ctas, a.sk_iters};
+    if (a.split > 1 || a.sk_ctas > 0)
+      sched.partial = reinterpret_cast<float*>(ws + L.partial_offset);
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
-    const int clusters = units < max_clusters ? units : max_clusters;
+    const int clusters = persistent_grid(a, units, max_clusters);
     const tc::Epilogue ep = tc::make_epilogue(a, vec_c, tiles, PAIR_TILE, PAIR_TILE);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -681,10 +682,8 @@ struct CfgPair {
                     const_cast<int*>(&kt), const_cast<int*>(&mt), const_cast<int*>(&nt),
                     &group_m, &sched, const_cast<int*>(&fault_inject)};
     e = cudaLaunchKernelExC(&cfg, kernel_ptr(a_mn, b_mn), args);
-    if (e != cudaSuccess || a.split <= 1) return e;
-    GemmArgs r = a;
-    r.partial = sched.partial;
-    return launch_splitk_reduce(r, PAIR_TILE, PAIR_TILE, vec_c, stream);
+    if (e != cudaSuccess) return e;
+    return launch_second_pass(a, sched.partial, PAIR_TILE, PAIR_TILE, kt, vec_c, stream);
   }
 };
 
@@ -717,8 +716,11 @@ F16Layout f16tc_layout(const GemmArgs& a, const F16Operands& f, int tile_m, int 
   }
   L.partial_offset = L.repack_a_bytes + L.repack_b_bytes;
   const int64_t tiles = static_cast<int64_t>(a.tiles_m) * a.tiles_n;
-  const int64_t split_units = (tiles - a.full_tiles) * (a.split > 1 ? a.split : 0);
-  L.workspace_bytes = L.partial_offset + split_units * tile_m * bn * 4;
+  // Partial tiles: two slots per stream-K CTA, or one per slice of a split tile.
+  const int64_t partial_tiles =
+      a.sk_ctas > 0 ? 2 * static_cast<int64_t>(a.sk_ctas)
+                    : (tiles - a.full_tiles) * (a.split > 1 ? a.split : 0);
+  L.workspace_bytes = L.partial_offset + partial_tiles * tile_m * bn * 4;
   return L;
 }
 

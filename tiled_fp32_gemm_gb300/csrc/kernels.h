@@ -146,6 +146,20 @@ cudaError_t launch_splitk_reduce(const GemmArgs& a, int bm, int bn, bool vec_c,
 cudaError_t launch_streamk_fixup(const GemmArgs& a, int bm, int bn, int ktiles, bool vec_c,
                                  cudaStream_t stream);
 
+// The second pass of a call whose GEMM kernel wrote partial tiles to
+// `partial` (bm x bn each, ktiles K tiles per tile): the stream-K fix-up when
+// a.sk_ctas > 0, the split-K reduce when a.split > 1, else nothing.
+cudaError_t launch_second_pass(const GemmArgs& a, float* partial, int bm, int bn, int ktiles,
+                               bool vec_c, cudaStream_t stream);
+
+// CTAs (clusters, for CTA pairs) of a persistent grid with at most max_ctas
+// resident: every unit gets one when they fit; with stream-K, the whole
+// tiles' full waves or, without any, the stream-K units.
+inline int persistent_grid(const GemmArgs& a, int units, int max_ctas) {
+  if (a.sk_ctas > 0) return a.full_tiles > 0 ? max_ctas : a.sk_ctas;
+  return units < max_ctas ? units : max_ctas;
+}
+
 // First unit of the stream-K split whose run holds stream-K iteration x:
 // the largest c with c * iters / ctas <= x (runs may be empty when there
 // are fewer iterations than units; the one returned is not).

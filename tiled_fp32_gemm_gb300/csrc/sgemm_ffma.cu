@@ -215,6 +215,18 @@ cudaError_t launch_streamk_fixup(const GemmArgs& a, int bm, int bn, int ktiles, 
   return cudaLaunchKernelEx(&cfg, streamk_fixup_kernel, a, bm, bn, pieces, ktiles, vc);
 }
 
+cudaError_t launch_second_pass(const GemmArgs& a, float* partial, int bm, int bn, int ktiles,
+                               bool vec_c, cudaStream_t stream) {
+  GemmArgs r = a;
+  r.partial = partial;
+  if (a.sk_ctas > 0) {
+    r.partial_extent = 2 * static_cast<int64_t>(a.sk_ctas) * bm * bn;
+    return launch_streamk_fixup(r, bm, bn, ktiles, vec_c, stream);
+  }
+  if (a.split > 1) return launch_splitk_reduce(r, bm, bn, vec_c, stream);
+  return cudaSuccess;
+}
+
 // C = beta * C (+ bias[col]) on an M x N view (C not read when beta is 0).
 __global__ void __launch_bounds__(256) scale_c_kernel(float* C, int M, int N, int64_t ldc,
                                                      float beta, const float* bias,

@@ -244,7 +244,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int num_tiles = tiles_m * tiles_n;
-  const int num_units = sched.full_tiles + (num_tiles - sched.full_tiles) * sched.split;
+  const int cta = static_cast<int>(blockIdx.x), ctas = static_cast<int>(gridDim.x);
+  const int num_units = units_of(cta, ctas, sched, num_tiles, Kt);  // this CTA's units
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -277,8 +278,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       // on its data runs out (the test of the timeout path).
       uint32_t& g = issued;
       bool stop = fault_inject != 0;
-      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
-        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      for (int u = 0; u < num_units && !stop; ++u) {
+        const Unit w = unit_at(u, cta, ctas, sched, tiles_m, tiles_n, group_m, Kt);
         const char* a_src = reinterpret_cast<const char*>(Ap) +
                             static_cast<int64_t>(w.tm) * Kt * G::A_PAIR_BYTES;
         const char* b_src = reinterpret_cast<const char*>(Bp) +
@@ -306,8 +307,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t g = 0;
       bool stop = false;
       int it = 0;
-      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x, ++it) {
-        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      for (int u = 0; u < num_units && !stop; ++u, ++it) {
+        const Unit w = unit_at(u, cta, ctas, sched, tiles_m, tiles_n, group_m, Kt);
         const int b = it & 1;
         // The epilogue must have drained this accumulator (used by unit it-2).
         if (it >= 2 && !wait_phase(bar(ACC_EMPTY + b), ((it >> 1) + 1) & 1u, wc)) break;
@@ -350,7 +351,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int it = 0;
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++it) {
+    for (int u = 0; u < num_units; ++u, ++it) {
       const int b = it & 1;
       // A tile's accumulator is ready after its whole K loop.  The warp
       // goes on only if every lane saw it (tcgen05.ld needs the whole warp).
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after();
       __syncwarp();
-      const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      const Unit w = unit_at(u, cta, ctas, sched, tiles_m, tiles_n, group_m, Kt);
       store_accumulator<BM, BN>(tmem + lane_base + static_cast<uint32_t>(b * BN), w, q, lane,
                                 ep, sched.partial);
       tc_fence_before();
@@ -441,7 +442,8 @@ __global__ void __launch_bounds__(ASPLIT_THREADS, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int num_tiles = tiles_m * tiles_n;
-  const int num_units = sched.full_tiles + (num_tiles - sched.full_tiles) * sched.split;
+  const int cta = static_cast<int>(blockIdx.x), ctas = static_cast<int>(gridDim.x);
+  const int num_units = units_of(cta, ctas, sched, num_tiles, Kt);  // this CTA's units
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmap_a);
@@ -474,8 +476,8 @@ __global__ void __launch_bounds__(ASPLIT_THREADS, 1)
     if (lane == 0) {
       uint32_t& g = issued;
       bool stop = fault_inject != 0;
-      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
-        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      for (int u = 0; u < num_units && !stop; ++u) {
+        const Unit w = unit_at(u, cta, ctas, sched, tiles_m, tiles_n, group_m, Kt);
         const char* b_src = reinterpret_cast<const char*>(Bp) +
                             static_cast<int64_t>(w.tn) * Kt * G::B_PAIR_BYTES;
         for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
@@ -498,8 +500,8 @@ __global__ void __launch_bounds__(ASPLIT_THREADS, 1)
       uint32_t g = 0;
       bool stop = false;
       int it = 0;
-      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x, ++it) {
-        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      for (int u = 0; u < num_units && !stop; ++u, ++it) {
+        const Unit w = unit_at(u, cta, ctas, sched, tiles_m, tiles_n, group_m, Kt);
         const int b = it & 1;
         if (it >= 2 && !wait_phase(bar(ACC_EMPTY + b), ((it >> 1) + 1) & 1u, wc)) break;
         tc_fence_after();
@@ -539,14 +541,14 @@ __global__ void __launch_bounds__(ASPLIT_THREADS, 1)
     const int q = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int it = 0;
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++it) {
+    for (int u = 0; u < num_units; ++u, ++it) {
       const int b = it & 1;
       const bool ready = wait_phase(bar(ACC_FULL + b), (it >> 1) & 1u, wc, true,
                                     TIMEOUT_NS + 20000ull * static_cast<uint64_t>(Kt));
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after();
       __syncwarp();
-      const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      const Unit w = unit_at(u, cta, ctas, sched, tiles_m, tiles_n, group_m, Kt);
       store_accumulator<BM, BN>(tmem + lane_base + static_cast<uint32_t>(b * BN), w, q, lane,
                                 ep, sched.partial);
       tc_fence_before();
@@ -558,8 +560,8 @@ __global__ void __launch_bounds__(ASPLIT_THREADS, 1)
     const int t = threadIdx.x - (ASPLIT_THREADS - CONVERT_THREADS);
     uint32_t g = 0;
     bool stop = fault_inject != 0;
-    for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
-      const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+    for (int u = 0; u < num_units && !stop; ++u) {
+      const Unit w = unit_at(u, cta, ctas, sched, tiles_m, tiles_n, group_m, Kt);
       for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
         const uint32_t s = g % STAGES, round = g / STAGES;
         if (!wait_phase(bar(FULL + s), round & 1u, wc)) {
@@ -651,7 +653,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int cluster = static_cast<int>(cluster_id_x());
   const int clusters = static_cast<int>(cluster_count_x());
   const int num_tiles = tiles_m * tiles_n;
-  const int num_units = sched.full_tiles + (num_tiles - sched.full_tiles) * sched.split;
+  const int num_units = units_of(cluster, clusters, sched, num_tiles, Kt);  // this cluster's units
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmap_a);
@@ -684,8 +686,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool stop = fault_inject != 0;
       uint32_t g = 0;
       const uint32_t full_even0 = map_to_cta(bar(FULL), 0);
-      for (int u = cluster; u < num_units && !stop; u += clusters) {
-        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      for (int u = 0; u < num_units && !stop; ++u) {
+        const Unit w = unit_at(u, cluster, clusters, sched, tiles_m, tiles_n, group_m, Kt);
         const int blk_a = 2 * w.tm + static_cast<int>(rank);
         const int blk_b = 2 * w.tn + static_cast<int>(rank);
         for (int kt = w.kt0; kt < w.kt1; ++kt, ++g) {
@@ -709,8 +711,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t g = 0;
       bool stop = false;
       int it = 0;
-      for (int u = cluster; u < num_units && !stop; u += clusters, ++it) {
-        const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      for (int u = 0; u < num_units && !stop; ++u, ++it) {
+        const Unit w = unit_at(u, cluster, clusters, sched, tiles_m, tiles_n, group_m, Kt);
         const int b = it & 1;
         if (it >= 2 && !wait_phase(bar(ACC_EMPTY + b), ((it >> 1) + 1) & 1u, wc)) break;
         tc_fence_after();
@@ -751,14 +753,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t acc_empty_even = map_to_cta(bar(ACC_EMPTY), 0);
     int it = 0;
-    for (int u = cluster; u < num_units; u += clusters, ++it) {
+    for (int u = 0; u < num_units; ++u, ++it) {
       const int b = it & 1;
       const bool ready = wait_phase(bar(ACC_FULL + b), (it >> 1) & 1u, wc, true,
                                     TIMEOUT_NS + 20000ull * static_cast<uint64_t>(Kt));
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after();
       __syncwarp();
-      const Unit w = unit_of(u, sched, tiles_m, tiles_n, group_m, Kt);
+      const Unit w = unit_at(u, cluster, clusters, sched, tiles_m, tiles_n, group_m, Kt);
       store_accumulator<PAIR_HALF, PAIR_TILE, PAIR_TILE>(
           tmem + lane_base + static_cast<uint32_t>(b * PAIR_TILE), w, q, lane, ep,
           sched.partial, static_cast<int>(rank) * PAIR_HALF);
@@ -866,22 +868,20 @@ struct Cfg {
           a.B, a.ldb, Bp, a.N, a.K, kt, nt, a.bounds);
     const int tiles = mt * nt;
     // Split tail: the partial tiles follow the packed operands.
-    Sched sched{a.full_tiles, a.split, a.kt_per_slice, nullptr};
-    if (a.split > 1)
+    Sched sched{a.full_tiles, a.split, a.kt_per_slice, nullptr, a.sk_ctas, a.sk_iters};
+    if (a.split > 1 || a.sk_ctas > 0)
       sched.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                                 workspace_bytes_packed(a.M, a.N, a.K));
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
-    const int grid = units < max_ctas ? units : max_ctas;
+    const int grid = persistent_grid(a, units, max_ctas);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const Epilogue ep = make_epilogue(a, vec_c, tiles, BM, BN);
     e = launch_after_pack(reinterpret_cast<const void*>(tf32x3_gemm_kernel<G>), dim3(grid),
                           THREADS, G::SMEM_BYTES, 1, stream, Ap, Bp, ep, kt, mt, nt,
                           a.group_m, sched, fault_inject);
-    if (e != cudaSuccess || a.split <= 1) return e;
-    GemmArgs r = a;
-    r.partial = sched.partial;
-    return launch_splitk_reduce(r, BM, BN, vec_c, stream);
+    if (e != cudaSuccess) return e;
+    return launch_second_pass(a, sched.partial, BM, BN, kt, vec_c, stream);
   }
 };
 
@@ -955,20 +955,18 @@ struct CfgPair {
                               256, G::PAIR_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
     const int tiles = mt * nt;
-    Sched sched{a.full_tiles, a.split, a.kt_per_slice, nullptr};
-    if (a.split > 1)
+    Sched sched{a.full_tiles, a.split, a.kt_per_slice, nullptr, a.sk_ctas, a.sk_iters};
+    if (a.split > 1 || a.sk_ctas > 0)
       sched.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                                 CfgPair::workspace(a.M, a.N, a.K));
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
-    const int clusters = units < max_clusters ? units : max_clusters;
+    const int clusters = persistent_grid(a, units, max_clusters);
     const Epilogue ep = make_epilogue(a, vec_c, tiles, PAIR_TILE, PAIR_TILE);
     e = launch_after_pack(reinterpret_cast<const void*>(tf32x3_pair_kernel<BK>),
                           dim3(2 * clusters), THREADS, G::SMEM_BYTES, 2, stream, map_a, map_b,
                           ep, kt, mt, nt, a.group_m, sched, fault_inject);
-    if (e != cudaSuccess || a.split <= 1) return e;
-    GemmArgs r = a;
-    r.partial = sched.partial;
-    return launch_splitk_reduce(r, PAIR_TILE, PAIR_TILE, vec_c, stream);
+    if (e != cudaSuccess) return e;
+    return launch_second_pass(a, sched.partial, PAIR_TILE, PAIR_TILE, kt, vec_c, stream);
   }
 };
 
@@ -1008,21 +1006,19 @@ struct CfgASplit {
                               BK, BM, AG::TMA_SWIZZLE))
       return cudaErrorInvalidValue;
     const int tiles = mt * nt;
-    Sched sched{a.full_tiles, a.split, a.kt_per_slice, nullptr};
-    if (a.split > 1)
+    Sched sched{a.full_tiles, a.split, a.kt_per_slice, nullptr, a.sk_ctas, a.sk_iters};
+    if (a.split > 1 || a.sk_ctas > 0)
       sched.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                                 CfgASplit::workspace(a.M, a.N, a.K));
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
-    const int grid = units < max_ctas ? units : max_ctas;
+    const int grid = persistent_grid(a, units, max_ctas);
     const Epilogue ep = make_epilogue(a, vec_c, tiles, BM, BN);
     e = launch_after_pack(reinterpret_cast<const void*>(tf32x3_asplit_kernel<BK, BN>),
                           dim3(grid), ASPLIT_THREADS, AG::SMEM_BYTES, 1, stream, map_a,
                           static_cast<const float*>(Bp), ep, kt, mt, nt, a.group_m, sched,
                           fault_inject);
-    if (e != cudaSuccess || a.split <= 1) return e;
-    GemmArgs r = a;
-    r.partial = sched.partial;
-    return launch_splitk_reduce(r, BM, BN, vec_c, stream);
+    if (e != cudaSuccess) return e;
+    return launch_second_pass(a, sched.partial, BM, BN, kt, vec_c, stream);
   }
 };
 

@@ -320,11 +320,21 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 // (its index in the grouped raster); the tiles after those are split into
 // `split` K slices, one unit per slice, whose fp32 partial tiles (dense
 // BM x BN, tail tile major, slice minor) are added by a second kernel.
+//
+// Stream-K (sk_ctas > 0, split = 1): CTA (or cluster) c of the persistent
+// grid takes its whole tiles below full_tiles (c, c + grid, ...), then, if c
+// < sk_ctas, the run [c*sk_iters/sk_ctas, (c+1)*sk_iters/sk_ctas) of the K
+// tiles of the tiles from full_tiles on (tile-major, k ascending), one unit
+// per tile the run touches.  A unit that covers its tile whole goes to C;
+// a piece goes to partial slot 2c (the run's first tile) or 2c+1 (its
+// last), added in k order by the stream-K fix-up kernel.
 struct Sched {
   int full_tiles;
   int split;
   int kt_per_slice;
   float* partial;
+  int sk_ctas;
+  long long sk_iters;
 };
 
 struct Unit {
@@ -351,6 +361,46 @@ __device__ __forceinline__ Unit unit_of(int u, const Sched& sc, int tiles_m, int
   return w;
 }
 
+// Units of CTA (or cluster) c of a persistent grid of `ctas`, in the order
+// it runs them: with the split tail, units c, c + ctas, ...; with stream-K,
+// its whole tiles, then the tiles its run touches.
+__device__ __forceinline__ int units_of(int c, int ctas, const Sched& sc, int num_tiles,
+                                        int Kt) {
+  if (sc.sk_ctas > 0) {
+    const int dp = sc.full_tiles > c ? (sc.full_tiles - 1 - c) / ctas + 1 : 0;
+    if (c >= sc.sk_ctas) return dp;
+    const long long b = static_cast<long long>(c) * sc.sk_iters / sc.sk_ctas;
+    const long long e = static_cast<long long>(c + 1) * sc.sk_iters / sc.sk_ctas;
+    return dp + (e > b ? static_cast<int>((e - 1) / Kt - b / Kt + 1) : 0);
+  }
+  const int num_units = sc.full_tiles + (num_tiles - sc.full_tiles) * sc.split;
+  return num_units > c ? (num_units - 1 - c) / ctas + 1 : 0;
+}
+
+// Unit j (0 <= j < units_of(c, ...)) of CTA (or cluster) c.
+__device__ __forceinline__ Unit unit_at(int j, int c, int ctas, const Sched& sc, int tiles_m,
+                                        int tiles_n, int group_m, int Kt) {
+  if (sc.sk_ctas > 0) {
+    const int dp = sc.full_tiles > c ? (sc.full_tiles - 1 - c) / ctas + 1 : 0;
+    if (j >= dp) {
+      const int s = j - dp;
+      const long long b = static_cast<long long>(c) * sc.sk_iters / sc.sk_ctas;
+      const long long e = static_cast<long long>(c + 1) * sc.sk_iters / sc.sk_ctas;
+      const long long start = s == 0 ? b : (b / Kt + s) * Kt;
+      const long long t_rel = start / Kt;
+      const long long end = min(e, (t_rel + 1) * Kt);
+      Unit w;
+      w.kt0 = static_cast<int>(start - t_rel * Kt);
+      w.kt1 = static_cast<int>(end - t_rel * Kt);
+      w.pidx = w.kt0 == 0 && w.kt1 == Kt ? -1 : 2 * c + (s == 0 ? 0 : 1);
+      grouped_tile(sc.full_tiles + static_cast<int>(t_rel), tiles_m, tiles_n, group_m, w.tm,
+                   w.tn);
+      return w;
+    }
+  }
+  return unit_of(c + j * ctas, sc, tiles_m, tiles_n, group_m, Kt);
+}
+
 // The C update of a tile, shared by the epilogues.
 struct Epilogue {
   float* C;
@@ -370,7 +420,9 @@ struct Epilogue {
 inline Epilogue make_epilogue(const GemmArgs& a, bool vec_c, int tiles, int tile_m, int bn) {
   Epilogue ep{a.C, a.ldc, a.alpha, a.beta, a.M, a.N, vec_c ? 1 : 0, a.bias};
   ep.c_extent = a.c_extent;
-  ep.partial_extent = static_cast<int64_t>(tiles - a.full_tiles) * a.split * tile_m * bn;
+  ep.partial_extent = a.sk_ctas > 0
+                          ? 2 * static_cast<int64_t>(a.sk_ctas) * tile_m * bn
+                          : static_cast<int64_t>(tiles - a.full_tiles) * a.split * tile_m * bn;
   ep.bounds = a.bounds;
   return ep;
 }
