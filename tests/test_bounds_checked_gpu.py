@@ -198,7 +198,9 @@ def test_checked_record_catches_a_planted_short_extent(checked, cfg, site, monke
 TC_TOL = 5e-5
 TF32_CONFIGS = [dict(variant="tf32x3"), dict(variant="tf32x3", bn=64),
                 dict(variant="tf32x3", bm=256), dict(variant="tf32x3", pack_a=1),
-                dict(variant="tf32x3", pack_a=2)]
+                dict(variant="tf32x3", pack_a=2),
+                # stream-K runs: pieces in partial slots, added by the fix-up
+                dict(variant="tf32x3", schedule=2), dict(variant="tf32x3", bm=256, schedule=2)]
 
 
 @pytest.mark.parametrize("cfg", TF32_CONFIGS, ids=ids(TF32_CONFIGS))
@@ -249,8 +251,10 @@ def test_checked_tf32x3_workloads(checked, name):
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f16"])
-@pytest.mark.parametrize("tile", [dict(), dict(bm=128), dict(bn=128), dict(bm=256)],
-                         ids=["auto", "single", "bn128", "pair"])
+@pytest.mark.parametrize("tile", [dict(), dict(bm=128), dict(bn=128), dict(bm=256),
+                                  dict(bm=128, schedule=2), dict(bm=256, schedule=2)],
+                         ids=["auto", "single", "bn128", "pair", "single-streamk",
+                              "pair-streamk"])
 @pytest.mark.parametrize("ta,tb", [(0, 0), (1, 1)])
 @pytest.mark.parametrize("lds", ["direct", "repack"])
 def test_checked_16bit_inputs_stay_inside_their_buffers(checked, dt, tile, ta, tb, lds):
