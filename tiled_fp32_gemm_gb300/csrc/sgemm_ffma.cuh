@@ -9,7 +9,10 @@
 //
 //  * tile scheduler — one CTA per BM x BN tile of C ("The canonical source
 //    pattern": program_id -> tile origin), walked in a grouped raster so a
-//    wave shares A and B panels in L2;
+//    wave shares A and B panels in L2; the tiles past the last full wave are
+//    either cut into K slices (split tail) or dealt out as stream-K runs of
+//    K tiles across tile boundaries, one segment per tile a run touches,
+//    whose pieces a second kernel adds in k order;
 //  * masked staging — A[m0+r, k0+c] and B[k0+r, n0+c] are copied into a
 //    shared stage, 0.0 where the element lies outside M, N or K ("Zero-filled
 //    boundary tiles"); every shared slot is written, so all threads reach the
