@@ -1069,13 +1069,10 @@ mt_status run(const Problem& P, cudaStream_t stream, const mt_config* cfg) {
   lc.attrs = attr;
   lc.numAttrs = (L.prep_a || L.prep_a_kmajor || L.prep_b) ? 1 : 0;
   ok = ok && cudaLaunchKernelExC(&lc, L.kern, params) == cudaSuccess;
-  if (ok && L.split > 1)
-    ok = mt::launch_splitk_reduce(args, L.plan.bm, L.plan.bn, L.plan.vec_c != 0, stream) ==
-         cudaSuccess;
-  if (ok && L.sk_ctas > 0)
-    ok = mt::launch_streamk_fixup(args, L.plan.bm, L.plan.bn,
-                                  static_cast<int>(ceil_div(P.K, L.plan.bk)),
-                                  L.plan.vec_c != 0, stream) == cudaSuccess;
+  // The split tail's reduce or the stream-K fix-up, when the plan has one.
+  ok = ok && mt::launch_second_pass(args, args.partial, L.plan.bm, L.plan.bn,
+                                    static_cast<int>(ceil_div(P.K, L.plan.bk)),
+                                    L.plan.vec_c != 0, stream) == cudaSuccess;
   if (ws) cudaFreeAsync(ws, stream);
   if (!ok) {
     cudaGetLastError();

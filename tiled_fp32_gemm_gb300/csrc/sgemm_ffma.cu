@@ -220,7 +220,10 @@ cudaError_t launch_second_pass(const GemmArgs& a, float* partial, int bm, int bn
   GemmArgs r = a;
   r.partial = partial;
   if (a.sk_ctas > 0) {
-    r.partial_extent = 2 * static_cast<int64_t>(a.sk_ctas) * bm * bn;
+    // Two dense bm x bn slots per stream-K unit (callers that stated a larger
+    // extent keep theirs).
+    const int64_t slots = 2 * static_cast<int64_t>(a.sk_ctas) * bm * bn;
+    if (r.partial_extent < slots) r.partial_extent = slots;
     return launch_streamk_fixup(r, bm, bn, ktiles, vec_c, stream);
   }
   if (a.split > 1) return launch_splitk_reduce(r, bm, bn, vec_c, stream);
