@@ -104,23 +104,27 @@ def test_ragged_workload_full():
     # copies.  Row-major A tiles from copies (pack_a = 1): A and B copied
     # into rows padded to whole float4s, then 16-byte chunks.  Automatically:
     # A staged K-major from a transposed copy, B from a padded copy, on
-    # 64 x 128 tiles, the last partial wave split in four K slices; and A
-    # gathered K-major inside the kernel (pack_a = 4).  Without K slices all
-    # give the same FMA chain per output; the split tail adds four partial
-    # sums, within the tolerance.
+    # 64 x 128 tiles, the tiles past the last full wave run as stream-K (the
+    # split tail of four K slices on request); and A gathered K-major inside
+    # the kernel (pack_a = 4).  Without K splits all give the same FMA chain
+    # per output; stream-K and the split tail add a few partial sums, within
+    # the tolerance.
     A, B = gemm_inputs.make_workload("ragged_4097x3001x2053")
     a, b = A.cuda(), B.cuda()
     assert mt.plan(4097, 3001, 2053, a=a, b=b, pack_a=2)["vec_ab"] == 0
     assert mt.plan(4097, 3001, 2053, a=a, b=b, pack_a=1)["pack_a"] == 1
     p = mt.plan(4097, 3001, 2053, a=a, b=b)
     assert (p["vec_ab"], p["vec_c"], p["pack_a"], p["bm"], p["bn"]) == (1, 0, 5, 64, 128)
-    assert p["split_k"] == 4
+    assert p["stream_k"] > 0 and p["split_k"] == 1
+    assert mt.plan(4097, 3001, 2053, a=a, b=b, schedule="split_tail")["split_k"] == 4
     Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
     as_stored = run(A, B, pack_a=2).numpy()
     assert_within(as_stored, Cref, W, FFMA_TOL, "ragged, as stored")
     for choice in (dict(pack_a=1), dict(split_k=1), dict(pack_a=4, split_k=1)):
         assert np.array_equal(run(A, B, **choice).numpy(), as_stored), choice
-    assert_within(run(A, B).numpy(), Cref, W, FFMA_TOL, "ragged, automatic (split tail)")
+    assert_within(run(A, B).numpy(), Cref, W, FFMA_TOL, "ragged, automatic (stream-K)")
+    assert_within(run(A, B, schedule="split_tail").numpy(), Cref, W, FFMA_TOL,
+                  "ragged, split tail")
 
 
 def sampled_rows(M, bm=128, extra=24, seed=0):
@@ -237,12 +241,14 @@ def test_automatic_k_slices_match_oracle(shape, rows_only):
     """The automatic plans cut K: 512 x 512 x 4096 and the ragged 300 x 200
     x 5000 and 33 x 17 x 9000 have fewer tiles than SMs (every tile in
     slices, each CTA with two K groups of warps), 2048 x 2048 x 8192 and
-    65536 x 128 x 4096 leave a last partial wave (only those tiles in
-    slices).  Within the tolerance and deterministic."""
+    65536 x 128 x 4096 leave a last partial wave (those tiles' K tiles dealt
+    out as stream-K runs on 64 x 128 tiles).  Within the tolerance and
+    deterministic."""
     M, N, K = shape
     A, B = gemm_inputs.make_ab(M, N, K, seed=18, dist="uniform")
     a, b = A.cuda(), B.cuda()
-    assert mt.plan(M, N, K, a=a, b=b)["split_k"] > 1
+    p = mt.plan(M, N, K, a=a, b=b)
+    assert p["split_k"] > 1 or p["stream_k"] > 0
     first = mt.sgemm(a, b)
     again = mt.sgemm(a, b)
     torch.cuda.synchronize()
