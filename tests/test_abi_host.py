@@ -526,11 +526,12 @@ def test_mixed_plan_tiles_and_tail():
 
 def test_mixed_plan_repacks_what_tma_cannot_read():
     # Row pitches that are not multiples of 8 elements (16 bytes): both
-    # operands get padded copies, sized rows x round_up(cols, 8) x 2 bytes.
+    # operands get padded copies whose rows are whole 128-byte lines, sized
+    # rows x round_up(cols, 64) x 2 bytes.
     st, p = plan16(4097, 3001, 2053)
     assert st == mt.MT_OK and p.vec_ab == 0
     rnd = lambda x: (x + 255) // 256 * 256  # noqa: E731
-    assert p.workspace_bytes == rnd(4097 * 2056 * 2) + rnd(2053 * 3008 * 2)
+    assert p.workspace_bytes == rnd(4097 * 2112 * 2) + rnd(2053 * 3008 * 2)
     # A 2-byte (not 16-byte) aligned base alone also needs the copy.
     st, p = plan16(256, 256, 256, a=(1 << 20) + 2)
     assert p.vec_ab == 0 and p.workspace_bytes == rnd(256 * 256 * 2)

@@ -491,6 +491,10 @@ bool encode_map(CUtensorMap* map, int dtype, const void* base, int64_t rows, int
       base, rows, cols, ld, box_cols, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// Row pitch (elements) of a repacked 16-bit operand: whole 128-byte lines,
+// so every row TMA reads starts on a line.
+int64_t repack_pitch(int64_t cols) { return (cols + 63) / 64 * 64; }
+
 // Operands TMA cannot read in place go through padded copies in the
 // workspace; returns the matrices and leading dimensions to read.
 cudaError_t repack_operands(const GemmArgs& a, const F16Operands& f, const F16Layout& L,
@@ -502,7 +506,7 @@ cudaError_t repack_operands(const GemmArgs& a, const F16Operands& f, const F16La
   *ldb = a.ldb;
   if (L.repack_a_bytes) {
     const int64_t rows = a.trans_a ? a.K : a.M, cols = a.trans_a ? a.M : a.K;
-    const int64_t ldd = (cols + 7) / 8 * 8;
+    const int64_t ldd = repack_pitch(cols);
     f16tc::repack16_kernel<<<1216, 256, 0, stream>>>(static_cast<const uint16_t*>(f.A), a.lda,
                                                      reinterpret_cast<uint16_t*>(ws), ldd, rows,
                                                      cols, a.bounds);
@@ -511,7 +515,7 @@ cudaError_t repack_operands(const GemmArgs& a, const F16Operands& f, const F16La
   }
   if (L.repack_b_bytes) {
     const int64_t rows = a.trans_b ? a.N : a.K, cols = a.trans_b ? a.K : a.N;
-    const int64_t ldd = (cols + 7) / 8 * 8;
+    const int64_t ldd = repack_pitch(cols);
     uint16_t* dst = reinterpret_cast<uint16_t*>(ws + L.repack_a_bytes);
     f16tc::repack16_kernel<<<1216, 256, 0, stream>>>(static_cast<const uint16_t*>(f.B), a.ldb,
                                                      dst, ldd, rows, cols, a.bounds);
@@ -708,11 +712,11 @@ F16Layout f16tc_layout(const GemmArgs& a, const F16Operands& f, int tile_m, int 
   F16Layout L{};
   if (!tma_readable(f.A, a.lda)) {
     const int64_t rows = a.trans_a ? a.K : a.M, cols = a.trans_a ? a.M : a.K;
-    L.repack_a_bytes = round256(rows * ((cols + 7) / 8 * 8) * 2);
+    L.repack_a_bytes = round256(rows * repack_pitch(cols) * 2);
   }
   if (!tma_readable(f.B, a.ldb)) {
     const int64_t rows = a.trans_b ? a.N : a.K, cols = a.trans_b ? a.K : a.N;
-    L.repack_b_bytes = round256(rows * ((cols + 7) / 8 * 8) * 2);
+    L.repack_b_bytes = round256(rows * repack_pitch(cols) * 2);
   }
   L.partial_offset = L.repack_a_bytes + L.repack_b_bytes;
   const int64_t tiles = static_cast<int64_t>(a.tiles_m) * a.tiles_n;
