@@ -563,3 +563,48 @@ def test_mixed_argument_checks():
     assert st in (mt.MT_OK, mt.MT_ERR_NO_DEVICE)
     assert mt.mt_gemm_mixed(5, 0, 0, 0, 4, 4, 4, 0) == mt.MT_ERR_INVALID_ARG
     assert mt.mt_gemm_mixed(mt.MT_DTYPE_F16, 0, 0, 0, 0, 4, 4, 0) == mt.MT_OK  # M == 0
+
+
+def test_stream_k_plans():
+    """The stream-K schedule on the host (no GPU: 152 SMs assumed).  The
+    tiles past the last whole wave of resident CTAs are dealt out as runs
+    of K tiles, two partial slots per stream-K CTA."""
+    rnd = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    # FFMA at 4096^3, asked for: 1024 tiles of 128 x 128 on 152 x 2 slots,
+    # 912 whole tiles, the other 112 tiles' K tiles over 304 CTAs, after
+    # the transposed copy of A.
+    st, p = plan(4096, 4096, 4096, schedule=2)
+    assert st == mt.MT_OK and (p.bm, p.bn, p.split_k, p.stream_k) == (128, 128, 1, 304)
+    assert p.grid == 912 + 304
+    assert p.workspace_bytes == 4096 * 4096 * 4 + 2 * 304 * 128 * 128 * 4
+    # Automatic on the ragged case's 64 x 128 tiles: 1560 tiles on 152 x 3
+    # slots, 1368 whole; the copies of A^T and B have rows of whole 128-byte
+    # lines (4128 and 3008 floats).
+    st, p = plan(4097, 3001, 2053)
+    assert (p.bm, p.bn, p.split_k, p.stream_k, p.grid) == (64, 128, 1, 456, 1368 + 456)
+    assert p.workspace_bytes == (rnd(2053 * 4128 * 4) + rnd(2053 * 3008 * 4)
+                                 + 2 * 456 * 64 * 128 * 4)
+    # The split tail on request, and where the split tail leaves a plan
+    # whole, stream-K does too (the same bits as before).
+    st, p = plan(4097, 3001, 2053, schedule=1)
+    assert (p.split_k, p.stream_k, p.grid) == (4, 0, 1368 + 192 * 4)
+    st, p = plan(1024, 1024, 1024)
+    assert (p.split_k, p.stream_k, p.grid) == (1, 0, 128)
+    # Few K tiles: every CTA takes at least two (4 tiles x 3 K tiles: 6 CTAs).
+    st, p = plan(100, 72, 80, schedule=2)
+    assert st == mt.MT_OK and (p.bm, p.bn, p.stream_k, p.grid) == (64, 64, 6, 6)
+    # split_k = 1 turns it off; an explicit split or the one-warp kernel
+    # refuses it; an unknown schedule is an argument error.
+    assert plan(4096, 4096, 4096, schedule=2, split_k=1)[1].stream_k == 0
+    assert plan(4096, 4096, 4096, schedule=2, split_k=2)[0] == mt.MT_ERR_UNSUPPORTED
+    assert plan(1024, 1024, 1024, variant="p18", schedule=2)[0] == mt.MT_ERR_UNSUPPORTED
+    assert plan(1024, 1024, 1024, schedule=3)[0] == mt.MT_ERR_INVALID_ARG
+    # 3xTF32 on CTA pairs at 4096^3: 256 tiles of 256 x 256 on 76 clusters,
+    # 228 whole, the other 28 tiles' K tiles over the 76 clusters.
+    st, p = plan(4096, 4096, 4096, variant="tf32x3", schedule=2)
+    assert st == mt.MT_OK and (p.bm, p.split_k, p.stream_k, p.grid) == (256, 1, 76, 152)
+    assert p.workspace_bytes == 2 * 2 * 4096 * 4096 * 4 + 2 * 76 * 256 * 256 * 4
+    # 16-bit inputs read in place: the partial slots are the whole workspace.
+    st, p = plan16(4096, 4096, 4096, schedule=2)
+    assert st == mt.MT_OK and (p.bm, p.stream_k, p.grid) == (256, 76, 152)
+    assert p.workspace_bytes == 2 * 76 * 256 * 256 * 4
