@@ -239,3 +239,35 @@ def test_stream_k_16bit_integer_inputs_bit_exact():
         got = mt.gemm_mixed(A16.cuda(), B16.cuda(), **SK, **tile)
         torch.cuda.synchronize()
         assert np.array_equal(got.cpu().numpy(), Cref.reshape(M, N)), tile
+
+
+@pytest.mark.parametrize("variant", ["tf32x3", "bf16"])
+def test_stream_k_tensor_cores_general_form(variant):
+    # alpha, beta and the bias row through the fix-up on the tensor-core
+    # paths, with transposed A (the pieces' sums are the same; only the
+    # operand order differs).
+    M, N, K = 700, 1300, 900
+    g = torch.Generator().manual_seed(19)
+    C0 = torch.rand(M, N, generator=g) * 2 - 1
+    bias = torch.rand(N, generator=g) * 2 - 1
+    alpha, beta = -0.5, 1.25
+    c = C0.cuda()
+    if variant == "tf32x3":
+        A, B = gemm_inputs.make_ab(M, N, K, seed=20, dist="uniform")
+        At = A.t().contiguous()  # stored K x M
+        ref, W = oracle.sgemm_general(At.numpy(), B.numpy(), C0.numpy().ravel().copy(), M, N,
+                                      K, M, N, N, alpha=alpha, beta=beta, trans_a=True,
+                                      bias=bias.numpy(), with_w=True)
+        mt.gemm(At.cuda(), B.cuda(), c, alpha=alpha, beta=beta, trans_a=True, bias=bias.cuda(),
+                variant="tf32x3", **SK)
+    else:
+        A16, B16 = gemm_inputs.make_ab16(M, N, K, 20, "uniform", "bf16")
+        At16 = A16.t().contiguous()
+        ref, W = oracle.gemm_mixed_general(oracle.BF16, At16, B16, C0.numpy().ravel().copy(),
+                                           M, N, K, M, N, N, alpha, beta, 1, 0, with_w=True,
+                                           bias=bias.numpy())
+        mt.gemm_mixed(At16.cuda(), B16.cuda(), c, alpha=alpha, beta=beta, trans_a=True,
+                      bias=bias.cuda(), **SK)
+    torch.cuda.synchronize()
+    assert_tc(c.cpu().numpy(), ref.reshape(M, N), W.reshape(M, N), f"{variant} general stream-K")
+    assert mt.mt_check_device_status(0) == mt.MT_OK
