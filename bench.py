@@ -278,13 +278,15 @@ def tf32_clock_peak(sms: int, mhz: float) -> float:
 def launches_per_call(plan) -> int:
     """Kernels one library call launches: the GEMM (tf32x3: pack A, pack B,
     GEMM; FFMA with A staged K-major from a copy: the transposing copy of A,
-    then the GEMM), plus the slice reduce when the plan splits K."""
+    then the GEMM), plus the slice reduce when the plan splits K or the
+    stream-K fix-up when it deals out stream-K runs."""
     base = 3 if plan["variant"] == 1 else 1
     if plan["variant"] == 0 and plan["pack_a"] == 5:
         base += 1  # the step's operands need no copy of B
     if plan["variant"] == 3 and not plan["vec_ab"]:
         base += 2  # the copy path pads both operands (the step's shapes never take it)
-    return base + (1 if plan["split_k"] > 1 else 0)
+    second_pass = plan["split_k"] > 1 or plan.get("stream_k", 0) > 0
+    return base + (1 if second_pass else 0)
 
 
 def variant_of(cfg_json):

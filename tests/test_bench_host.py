@@ -78,6 +78,8 @@ def test_peaks_from_unit_counts_and_clock():
     (dict(variant=0, pack_a=5, split_k=4, workspace_bytes=1), 3),   # copy, GEMM, reduce
     (dict(variant=0, pack_a=4, split_k=1, workspace_bytes=0), 1),   # gathered, no split
     (dict(variant=2, pack_a=0, split_k=1, workspace_bytes=0), 1),   # the one-warp kernel
+    (dict(variant=0, pack_a=5, split_k=1, stream_k=456, workspace_bytes=1), 3),  # copy, GEMM, fix-up
+    (dict(variant=1, pack_a=1, split_k=1, stream_k=76, workspace_bytes=1), 4),   # packs, GEMM, fix-up
 ])
 def test_launch_count_follows_the_plan(plan, want):
     assert bench.launches_per_call(plan) == want
