@@ -382,19 +382,25 @@ def test_alignment_selects_staging_width():
     # staged as stored with 4-byte copies ...
     p = plan(4097, 3001, 2053, pack_a=2)[1]
     assert (p.vec_ab, p.vec_c, p.pack_a, p.workspace_bytes) == (0, 0, 0, 0)
-    # ... or (pack_a = 1) copied into padded rows, A 4097 x 2056 and B
-    # 2053 x 3004, then staged in 16-byte chunks; C has scalar stores
-    # (N = 3001).
+    # ... or (pack_a = 1) copied into padded rows of whole 128-byte lines,
+    # A 4097 x 2080 and B 2053 x 3008, then staged in 16-byte chunks; C has
+    # scalar stores (N = 3001).
     p = plan(4097, 3001, 2053, pack_a=1)[1]
     assert (p.vec_ab, p.vec_c, p.pack_a) == (1, 0, 1)
-    assert p.workspace_bytes == rnd(4097 * 2056 * 4) + rnd(2053 * 3004 * 4)
-    # Automatic: K-major A from a copy (2053 x 4100) and B from a copy with
+    assert p.workspace_bytes == rnd(4097 * 2080 * 4) + rnd(2053 * 3008 * 4)
+    # Automatic: K-major A from a copy (2053 x 4128) and B from a copy with
     # padded rows, on 64 x 128 tiles (too few 128 x 128 tiles for three
     # full waves); 1560 tiles on 3 x 152 CTA slots leave 192 for a last
-    # wave, split in four K slices.
+    # wave, whose K tiles go as stream-K runs to 456 CTAs (two partial
+    # slots each); on request the split tail cuts them in four K slices.
     p = plan(4097, 3001, 2053)[1]
-    assert (p.vec_ab, p.vec_c, p.pack_a, p.bm, p.bn, p.split_k) == (1, 0, 5, 64, 128, 4)
-    assert p.workspace_bytes == (rnd(2053 * 4100 * 4) + rnd(2053 * 3004 * 4) +
+    assert (p.vec_ab, p.vec_c, p.pack_a, p.bm, p.bn, p.split_k, p.stream_k) == \
+        (1, 0, 5, 64, 128, 1, 456)
+    assert p.workspace_bytes == (rnd(2053 * 4128 * 4) + rnd(2053 * 3008 * 4) +
+                                 2 * 456 * 64 * 128 * 4)
+    p = plan(4097, 3001, 2053, schedule=1)[1]
+    assert (p.split_k, p.stream_k) == (4, 0)
+    assert p.workspace_bytes == (rnd(2053 * 4128 * 4) + rnd(2053 * 3008 * 4) +
                                  192 * 4 * 64 * 128 * 4)
     # Small products gather K-major A inside the kernel: no copy.
     p = plan(100, 72, 81)[1]
