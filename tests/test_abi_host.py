@@ -614,3 +614,17 @@ def test_stream_k_plans():
     st, p = plan16(4096, 4096, 4096, schedule=2)
     assert st == mt.MT_OK and (p.bm, p.stream_k, p.grid) == (256, 76, 152)
     assert p.workspace_bytes == 2 * 76 * 256 * 256 * 4
+
+
+def test_tensor_core_small_grid_split_plans():
+    """Tensor-core grids of fewer tiles than half the resident CTAs cut K
+    into slices at least 1024 deep (no GPU: 152 SMs assumed)."""
+    st, p = plan16(512, 512, 4096)
+    assert st == mt.MT_OK and (p.bm, p.bn, p.split_k, p.grid) == (128, 128, 4, 64)
+    assert p.workspace_bytes == 16 * 4 * 128 * 128 * 4  # a partial tile per slice
+    st, p = plan16(1024, 1024, 1024)  # slices of 512 would not repay the reduce
+    assert (p.split_k, p.grid) == (1, 64)
+    st, p = plan(512, 512, 4096, variant="tf32x3")
+    assert st == mt.MT_OK and (p.bm, p.bn, p.split_k, p.grid) == (128, 64, 4, 128)
+    st, p = plan(512, 512, 4096, variant="tf32x3", split_k=1)
+    assert (p.split_k, p.grid) == (1, 32)

@@ -294,3 +294,20 @@ def test_mixed_bias_epilogue(dt, ta, tb, tile):
                                           a_cols, b_cols, N, 1.0, 0.0, ta, tb, with_w=True,
                                           bias=bias)
     assert_within(out.cpu().numpy(), want0.reshape(M, N), W0, "gemm_mixed bias")
+
+
+@pytest.mark.parametrize("shape", [(512, 512, 4096), (300, 200, 5000)])
+def test_mixed_small_grid_k_slices(shape):
+    # Fewer tiles than half the SMs: K cut into slices of at least 1024.
+    M, N, K = shape
+    p = mt.plan_mixed(mt.MT_DTYPE_BF16, M, N, K)
+    assert p["split_k"] > 1
+    A16, B16 = gemm_inputs.make_ab16(M, N, K, 25, "uniform", "bf16")
+    Cref, W = oracle.gemm_mixed_general(oracle.BF16, A16, B16, np.zeros(M * N, np.float32),
+                                        M, N, K, K, N, N, with_w=True)
+    a, b = A16.cuda(), B16.cuda()
+    got = mt.gemm_mixed(a, b)
+    again = mt.gemm_mixed(a, b)
+    torch.cuda.synchronize()
+    assert_within(got.cpu().numpy(), Cref.reshape(M, N), W.reshape(M, N), f"{shape}")
+    assert torch.equal(got, again)

@@ -242,3 +242,20 @@ def test_split_tail_plan_and_parity():
         got = run(A, B, **TF32, **cfg).numpy()[rows]
         assert_within(got, Cr, Wr, TOL, f"split tail {cfg}")
         assert np.array_equal(run(A, B, **TF32, **cfg).numpy()[rows], got)  # deterministic
+
+
+@pytest.mark.parametrize("shape", [(512, 512, 4096), (300, 200, 5000)])
+def test_small_grid_k_slices(shape):
+    # Fewer tiles than half the SMs: K cut into slices of at least 1024,
+    # added in slice order by the reduce; within the tolerance,
+    # deterministic, and integer inputs exact.
+    M, N, K = shape
+    p = mt.plan(M, N, K, **TF32)
+    assert p["split_k"] > 1
+    A, B = gemm_inputs.make_ab(M, N, K, seed=23, dist="uniform")
+    Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
+    got = run(A, B, **TF32).numpy()
+    assert_within(got, Cref, W, TOL, f"{shape} small-grid split")
+    assert np.array_equal(run(A, B, **TF32).numpy(), got)
+    Ai, Bi = gemm_inputs.make_ab(M, N, K, seed=24, dist="int")
+    assert np.array_equal(run(Ai, Bi, **TF32).numpy(), oracle.sgemm(Ai.numpy(), Bi.numpy()))

@@ -357,6 +357,25 @@ bool auto_pair(int64_t M, int64_t N, int bn, int sms, int pair_clusters) {
   return ceil_div(M, 256) * ceil_div(N, 256) >= clusters;
 }
 
+// Small grid of a persistent tensor-core kernel: fewer tiles than half the
+// resident CTAs (clusters) are cut into K slices, so more of them work (at
+// most 4 slices, as many as fit, each at least 1024 deep; the slices are
+// added by the second kernel).  Measured on GB300: 512 x 512 x 4096 with
+// bf16 inputs 27.3 -> 22.2 us and 3xTF32 98.0 -> 45.8 us in four slices;
+// 1024^3 bf16 lost in two slices of 512 (15.0 -> 18.1 us).  Leaves *full
+// and *split alone otherwise.
+void split_small_grid(int64_t tiles, int64_t max_ctas, int64_t K, int bk, int64_t* full,
+                      int64_t* split) {
+  if (tiles <= 0 || 2 * tiles > max_ctas) return;
+  const int64_t ktiles = ceil_div(K, bk);
+  int64_t s = std::min<int64_t>(4, max_ctas / tiles);
+  while (s > 1 && ((s - 1) * ceil_div(ktiles, s) >= ktiles || K / s < 1024)) --s;
+  if (s > 1) {
+    *full = 0;
+    *split = s;
+  }
+}
+
 // Stream-K plan of a persistent tensor-core kernel (schedule 2) over
 // `tiles` tiles of `ktiles` K tiles on `max_ctas` resident CTAs (clusters):
 // the full waves stay whole tiles; the tiles past them are dealt out as
@@ -416,9 +435,11 @@ mt_status plan_f16(const Problem& P, const mt_config* cfg, int64_t smem_limit, i
   else L->max_ctas = sms > 0 ? sms : 1;
   int64_t full = tiles, split = 1;
   const bool streamk = cfg && cfg->schedule == 2 && cfg->split_k != 1;
-  if (!streamk)
-    split_tail(tiles, std::min<int64_t>(tiles, L->max_ctas), ceil_div(K, bk),
-               !(cfg && cfg->split_k == 1), &full, &split);
+  if (!streamk && !(cfg && cfg->split_k == 1)) {
+    split_tail(tiles, std::min<int64_t>(tiles, L->max_ctas), ceil_div(K, bk), true, &full,
+               &split);
+    split_small_grid(tiles, L->max_ctas, K, bk, &full, &split);
+  }
   L->full_tiles = static_cast<int>(full);
   L->split = static_cast<int>(split);
   L->kt_per_slice = static_cast<int>(ceil_div(ceil_div(K, bk), split));
@@ -512,7 +533,10 @@ mt_status plan_tf32x3(const Problem& P, const mt_config* cfg, int64_t smem_limit
   const int64_t ktiles = ceil_div(K, bk);
   int64_t full = tiles, split = 1;
   const bool streamk = cfg && cfg->schedule == 2 && cfg->split_k != 1;
-  if (!streamk) split_tail(tiles, ctas, ktiles, !(cfg && cfg->split_k == 1), &full, &split);
+  if (!streamk && !(cfg && cfg->split_k == 1)) {
+    split_tail(tiles, ctas, ktiles, true, &full, &split);
+    split_small_grid(tiles, L->max_ctas, K, bk, &full, &split);
+  }
   L->full_tiles = static_cast<int>(full);
   L->split = static_cast<int>(split);
   L->kt_per_slice = static_cast<int>(ceil_div(ktiles, split));
