@@ -124,9 +124,9 @@ typedef struct {
                       each CTA's whole tiles), each taking a contiguous run
                       across tile boundaries, and the pieces of a tile added in
                       k order by a second kernel (deterministic).  split_k = 1
-                      turns both off; split_k > 1 with 2, FFMA tiles whose
-                      warps form K groups and MT_VARIANT_P18 are
-                      MT_ERR_UNSUPPORTED. */
+                      turns both off; split_k > 1 with 2, an explicit FFMA
+                      tile whose warps form K groups (automatic tiles avoid
+                      them) and MT_VARIANT_P18 are MT_ERR_UNSUPPORTED. */
 } mt_config;
 
 /* What a call with the same arguments would launch. */

@@ -604,6 +604,12 @@ def test_stream_k_plans():
     assert plan(4096, 4096, 4096, schedule=2, split_k=1)[1].stream_k == 0
     assert plan(4096, 4096, 4096, schedule=2, split_k=2)[0] == mt.MT_ERR_UNSUPPORTED
     assert plan(1024, 1024, 1024, variant="p18", schedule=2)[0] == mt.MT_ERR_UNSUPPORTED
+    # A small grid with long K would take the K-grouped tile; asked for
+    # stream-K, the automatic choice keeps one group of warps per tile.
+    st, p = plan(512, 512, 4096, schedule=2)
+    assert st == mt.MT_OK and p.threads == 128 and p.stream_k > 0
+    assert plan(512, 512, 4096, bm=64, bn=128, stages=3, schedule=2)[0] == \
+        mt.MT_ERR_UNSUPPORTED
     assert plan(1024, 1024, 1024, schedule=3)[0] == mt.MT_ERR_INVALID_ARG
     # 3xTF32 on CTA pairs at 4096^3: 256 tiles of 256 x 256 on 76 clusters,
     # 228 whole, the other 28 tiles' K tiles over the 76 clusters.

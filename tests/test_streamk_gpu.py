@@ -139,6 +139,8 @@ def test_stream_k_choices_refused():
         mt.plan(1024, 1024, 1024, split_k=2, **SK)
     with pytest.raises(mt.MtError):
         mt.plan(1024, 1024, 1024, bm=64, bn=128, stages=3, pack_a=4, **SK)
+    # ... but the automatic tile of such a grid is one without K groups.
+    assert mt.plan(512, 512, 4096, **SK)["threads"] == 128
     with pytest.raises(mt.MtError):
         mt.plan(1024, 1024, 1024, variant="p18", **SK)
     # split_k = 1 turns stream-K off like the split tail.
@@ -271,3 +273,24 @@ def test_stream_k_tensor_cores_general_form(variant):
     torch.cuda.synchronize()
     assert_tc(c.cpu().numpy(), ref.reshape(M, N), W.reshape(M, N), f"{variant} general stream-K")
     assert mt.mt_check_device_status(0) == mt.MT_OK
+
+
+@pytest.mark.parametrize("shape", [(64, 64, 100000), (1, 4096, 8192), (4096, 1, 8192),
+                                   (3, 5, 70000)])
+def test_stream_k_one_tile_many_runs(shape):
+    """A tile whose K is dealt out to hundreds of CTAs: its pieces exceed
+    the fix-up's 256 slots per pass, so the sum runs over several passes,
+    still in k order.  Single rows and columns of C."""
+    M, N, K = shape
+    for cfg in (dict(), dict(bm=128, bn=128, bk=16, stages=4, wm=64, pack_a=5)):
+        p = mt.plan(M, N, K, **SK, **cfg)
+        assert p["stream_k"] > 0
+        A, B = gemm_inputs.make_ab(M, N, K, seed=26, dist="uniform")
+        Cref, W = oracle.sgemm(A.numpy(), B.numpy(), with_w=True)
+        a, b = A.cuda(), B.cuda()
+        got = run(a, b, **SK, **cfg)
+        assert_within(got, Cref, W, f"{shape} {cfg}")
+        assert np.array_equal(run(a, b, **SK, **cfg), got)
+    # The persistent tensor-core kernels on the same shapes.
+    got = run(a, b, variant="tf32x3", **SK)
+    assert_tc(got, Cref, W, f"{shape} tf32x3")

@@ -196,6 +196,8 @@ mt_status check_problem(const Problem& P) {
 // order wins, so each tile's default warp layout comes first.  Otherwise
 // the choice is automatic.
 int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int64_t K, int sms, bool kmajor) {
+  // Stream-K runs need one group of warps per tile: no K-grouped tile then.
+  const bool kgroups_ok = !(cfg && cfg->schedule == 2);
   int count = 0;
   const mt::FfmaEntry* e = mt::ffma_entries(&count);
   const bool explicit_tile = cfg && (cfg->bm || cfg->bn || cfg->bk || cfg->stages || cfg->wm ||
@@ -248,7 +250,7 @@ int pick_ffma(const mt_config* cfg, int64_t M, int64_t N, int64_t K, int sms, bo
   if (big_km >= 0) big = big_km;
   if (tiles_big >= 6 * static_cast<int64_t>(sms) || (mid < 0 && small < 0)) return big;
   if (mid >= 0 && 2 * ceil_div(M, 64) * ceil_div(N, 128) >= static_cast<int64_t>(sms)) return mid;
-  if (sliced >= 0 && K >= 2048) return sliced;
+  if (sliced >= 0 && K >= 2048 && kgroups_ok) return sliced;
   return small >= 0 ? small : big;
 }
 
