@@ -137,6 +137,10 @@ __global__ void __launch_bounds__(256) pack_kc_kernel(const float* __restrict__ 
   constexpr int BK = G::BK;
   constexpr int BLOCK = ROWS * G::ROW_BYTES;
   const int kt = blockIdx.x, rt = blockIdx.y;
+  // The GEMM kernel launched after the packers as their programmatic
+  // dependent may be scheduled from now on; it waits inside
+  // (griddepcontrol.wait) until this grid has completed.
+  asm volatile("griddepcontrol.launch_dependents;");
   // Checked builds: the source view and the gridDim.y x Kt packed blocks.
   const int64_t src_extent = view_extent(R, K, ld);
   const int64_t dst_words = static_cast<int64_t>(gridDim.y) * Kt * (2 * BLOCK / 4);
@@ -186,6 +190,7 @@ __global__ void __launch_bounds__(256) pack_rc_kernel(const float* __restrict__ 
   constexpr int CPR = G::ROW_BYTES / 16;  // 16-byte chunks per packed row
   constexpr int TS = 256 + 1;             // tile row stride (words): k rows, banks spread
   __shared__ float tile[BK * TS];
+  asm volatile("griddepcontrol.launch_dependents;");  // as in pack_kc_kernel
   const int kt = blockIdx.x;
   const int n0 = blockIdx.y * 256;
   // Checked builds: the source view (K rows of R) and the Rt x Kt blocks.
