@@ -9,11 +9,14 @@
   show the conflict the rule removes;
 * argument errors, aliasing and the shared-memory budget are rejected on the
   host before anything is launched; without a GPU the computing entry points
-  report MT_ERR_NO_DEVICE (there is no CPU fallback).
+  report MT_ERR_NO_DEVICE, and without the library the binding raises
+  (there is no CPU fallback); no source of the package names the oracle.
 """
 import ctypes
 import os
 import re
+import subprocess
+import sys
 
 import pytest
 
@@ -439,6 +442,43 @@ def test_no_cpu_fallback_without_gpu():
     st = mt.mt_sgemm_host(a.ctypes.data, a.ctypes.data, c.ctypes.data, 4, 4, 4, 0, None)
     assert st == mt.MT_ERR_NO_DEVICE
     assert np.all(c == 0)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    # No CPU fallback: in a fresh interpreter whose library path names
+    # nothing, the first call raises instead of computing, and nothing has
+    # imported the oracle.
+    code = (
+        "import sys\n"
+        "import tiled_fp32_gemm_gb300 as mt\n"
+        f"mt.LIB_PATH = {str(tmp_path / 'absent.so')!r}\n"
+        "try:\n"
+        "    mt.mt_sgemm(0, 0, 0, 4, 4, 4, 0)\n"
+        "except RuntimeError as e:\n"
+        "    assert 'no CPU fallback' in str(e), e\n"
+        "    print('raised')\n"
+        "assert not [m for m in sys.modules if m == 'oracle' or m.startswith('oracle.')]\n"
+    )
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0 and r.stdout.split() == ["raised"], r.stdout + r.stderr
+
+
+def test_product_sources_never_name_the_oracle():
+    # The oracle is test infrastructure: no source of the package or of the
+    # exported headers imports, includes or names it.
+    dirs = [os.path.join(ROOT, "tiled_fp32_gemm_gb300"), os.path.join(ROOT, "include")]
+    seen = 0
+    for top in dirs:
+        for dirpath, dirnames, files in os.walk(top):
+            dirnames[:] = [d for d in dirnames if d not in ("_build", "_build_checked",
+                                                            "__pycache__")]
+            for fn in files:
+                if fn.endswith((".py", ".cu", ".cuh", ".h", ".c", ".cpp")):
+                    text = open(os.path.join(dirpath, fn)).read()
+                    assert not re.search(r"\boracle\b|ref_gemm|smem_rules", text), fn
+                    seen += 1
+    assert seen >= 10
 
 
 def test_split_k_plan():
