@@ -78,7 +78,8 @@ struct Geometry {
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static_assert(STAGES >= 2, "at least two stages");
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulators
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment*/ + 256;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment*/ + 256 +
+                                   EPI_STAGE_BYTES;
 };
 
 // Loads the `rows`-row tile of one operand for K tile k0 into `dst`.
@@ -120,6 +121,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // acc_empty[b], 2S + 4 drain.
   constexpr int FULL = 0, EMPTY = STAGES, ACC_FULL = 2 * STAGES, ACC_EMPTY = 2 * STAGES + 2,
                 DRAIN = 2 * STAGES + 4, NBARS = 2 * STAGES + 5;
+  static_assert(NBARS * 8 + 8 <= 256, "barriers, TMEM slot and abort flag fit 256 bytes");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const WaitCtx wc{abort_flag, &g_status};
@@ -213,6 +215,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // Epilogue warps: warp w may access TMEM lanes 32*(w%4) .. +31.
     const int q = warp & 3;
+    // This warp's staging square, past the barriers.
+    float* const epi_square =
+        reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 256) + q * EPI_WARP_FLOATS;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int it = 0;
     for (int u = 0; u < num_units; ++u, ++it) {
@@ -226,7 +231,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       const Unit w = unit_at(u, cta, ctas, sched, tiles_m, tiles_n, group_m, Kt);
       store_accumulator<BM, BN>(tmem + lane_base + static_cast<uint32_t>(b * BN), w, q, lane,
-                                ep, sched.partial);
+                                ep, sched.partial, epi_square);
       tc_fence_before();
       mbar_arrive(bar(ACC_EMPTY + b));
     }
@@ -273,7 +278,8 @@ struct PairGeometry {
   static constexpr int STAGES_FIT = SMEM_STAGE_BUDGET / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr uint32_t TMEM_COLS = ACC_BUFS * PAIR_TILE;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment*/ + 256;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment*/ + 256 +
+                                   EPI_STAGE_BYTES;
 };
 
 template <bool A_MN, bool B_MN, int ACC_BUFS>
@@ -294,6 +300,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int FULL = 0, EMPTY = STAGES, ACC_FULL = 2 * STAGES,
                 ACC_EMPTY = 2 * STAGES + ACC_BUFS, DRAIN = 2 * STAGES + 2 * ACC_BUFS,
                 NBARS = DRAIN + 1;
+  static_assert(NBARS * 8 + 8 <= 256, "barriers, TMEM slot and abort flag fit 256 bytes");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const WaitCtx wc{abort_flag, &g_status};
@@ -403,6 +410,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // Epilogue warps of both CTAs: warp w may access TMEM lanes 32*(w%4)..+31.
     const int q = warp & 3;
+    // This warp's staging square, past the barriers.
+    float* const epi_square =
+        reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 256) + q * EPI_WARP_FLOATS;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t acc_empty_even = map_to_cta(bar(ACC_EMPTY), 0);
     int it = 0;
@@ -416,7 +426,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const Unit w = unit_at(u, cluster, clusters, sched, tiles_m, tiles_n, group_m, Kt);
       store_accumulator<PAIR_HALF, PAIR_TILE, PAIR_TILE>(
           tmem + lane_base + static_cast<uint32_t>(b * PAIR_TILE), w, q, lane, ep,
-          sched.partial, static_cast<int>(rank) * PAIR_HALF);
+          sched.partial, epi_square, static_cast<int>(rank) * PAIR_HALF);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty_even + 8u * static_cast<uint32_t>(b));
@@ -574,7 +584,7 @@ struct Cfg16 {
       sched.partial = reinterpret_cast<float*>(ws + L.partial_offset);
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int grid = persistent_grid(a, units, max_ctas);
-    const tc::Epilogue ep = tc::make_epilogue(a, vec_c, tiles, BM, BN);
+    const tc::Epilogue ep = tc::make_epilogue(a, vec_c, tiles, BM, BN, true);
     auto go = [&](auto kern) {
       kern<<<grid, f16tc::THREADS, G::SMEM_BYTES, stream>>>(map_a, map_b, idesc, ep, kt, mt, nt,
                                                             a.group_m, sched, fault_inject);
@@ -668,7 +678,7 @@ struct CfgPair {
       sched.partial = reinterpret_cast<float*>(ws + L.partial_offset);
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int clusters = persistent_grid(a, units, max_clusters);
-    const tc::Epilogue ep = tc::make_epilogue(a, vec_c, tiles, PAIR_TILE, PAIR_TILE);
+    const tc::Epilogue ep = tc::make_epilogue(a, vec_c, tiles, PAIR_TILE, PAIR_TILE, true);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -88,7 +88,8 @@ struct Geometry {
   static_assert(STAGES >= 2, "at least two stages");
   // Two fp32 accumulators of 128 lanes x BN columns.
   static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment*/ + 256 /*barriers*/;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment*/ + 256 /*barriers*/ +
+                                   EPI_STAGE_BYTES /*epilogue squares*/;
 
   // Byte offset of element (r, k), k < BK, inside a block.
   __host__ __device__ static __forceinline__ uint32_t offset(uint32_t r, uint32_t k) {
@@ -242,6 +243,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // acc_empty[b], 2S + 4 drain.
   constexpr int FULL = 0, EMPTY = STAGES, ACC_FULL = 2 * STAGES, ACC_EMPTY = 2 * STAGES + 2,
                 DRAIN = 2 * STAGES + 4, NBARS = 2 * STAGES + 5;
+  static_assert(NBARS * 8 + 8 <= 256, "barriers, TMEM slot and abort flag fit 256 bytes");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const WaitCtx wc{abort_flag, &g_status};
@@ -354,6 +356,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // Epilogue warps: warp w may access TMEM lanes 32*(w%4) .. +31.
     const int q = warp & 3;
+    // This warp's staging square, past the barriers.
+    float* const epi_square =
+        reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 256) + q * EPI_WARP_FLOATS;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int it = 0;
     for (int u = 0; u < num_units; ++u, ++it) {
@@ -367,7 +372,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       const Unit w = unit_at(u, cta, ctas, sched, tiles_m, tiles_n, group_m, Kt);
       store_accumulator<BM, BN>(tmem + lane_base + static_cast<uint32_t>(b * BN), w, q, lane,
-                                ep, sched.partial);
+                                ep, sched.partial, epi_square);
       tc_fence_before();
       mbar_arrive(bar(ACC_EMPTY + b));
     }
@@ -420,7 +425,7 @@ struct ASplitGeometry {
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static_assert(STAGES >= 2, "at least two stages");
   static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + EPI_STAGE_BYTES;
 };
 
 template <int BK, int BN>
@@ -440,6 +445,7 @@ __global__ void __launch_bounds__(ASPLIT_THREADS, 1)
   // acc_empty[2], drain.
   constexpr int FULL = 0, CONV = STAGES, EMPTY = 2 * STAGES, ACC_FULL = 3 * STAGES,
                 ACC_EMPTY = 3 * STAGES + 2, DRAIN = 3 * STAGES + 4, NBARS = 3 * STAGES + 5;
+  static_assert(NBARS * 8 + 8 <= 256, "barriers, TMEM slot and abort flag fit 256 bytes");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const WaitCtx wc{abort_flag, &g_status};
@@ -544,6 +550,9 @@ __global__ void __launch_bounds__(ASPLIT_THREADS, 1)
     }
   } else if (warp < 6) {
     const int q = warp & 3;
+    // This warp's staging square, past the barriers.
+    float* const epi_square =
+        reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 256) + q * EPI_WARP_FLOATS;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int it = 0;
     for (int u = 0; u < num_units; ++u, ++it) {
@@ -555,7 +564,7 @@ __global__ void __launch_bounds__(ASPLIT_THREADS, 1)
       __syncwarp();
       const Unit w = unit_at(u, cta, ctas, sched, tiles_m, tiles_n, group_m, Kt);
       store_accumulator<BM, BN>(tmem + lane_base + static_cast<uint32_t>(b * BN), w, q, lane,
-                                ep, sched.partial);
+                                ep, sched.partial, epi_square);
       tc_fence_before();
       mbar_arrive(bar(ACC_EMPTY + b));
     }
@@ -627,7 +636,7 @@ struct PairGeometry {
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static_assert(STAGES >= 2, "at least two stages");
   static constexpr uint32_t TMEM_COLS = 2 * PAIR_TILE;  // two accumulators
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + EPI_STAGE_BYTES;
   // The packed buffers seen as 2-D tensors of 1 KB rows: one TMA box of
   // PAIR_ROWS rows is one block pair.
   static constexpr int PAIR_ROWS = PAIR_BYTES / 1024;
@@ -647,6 +656,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   constexpr int FULL = 0, EMPTY = STAGES, ACC_FULL = 2 * STAGES, ACC_EMPTY = 2 * STAGES + 2,
                 DRAIN = 2 * STAGES + 4, NBARS = 2 * STAGES + 5;
+  static_assert(NBARS * 8 + 8 <= 256, "barriers, TMEM slot and abort flag fit 256 bytes");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const WaitCtx wc{abort_flag, &g_status};
@@ -755,6 +765,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     const int q = warp & 3;
+    // This warp's staging square, past the barriers.
+    float* const epi_square =
+        reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 256) + q * EPI_WARP_FLOATS;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t acc_empty_even = map_to_cta(bar(ACC_EMPTY), 0);
     int it = 0;
@@ -768,7 +781,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const Unit w = unit_at(u, cluster, clusters, sched, tiles_m, tiles_n, group_m, Kt);
       store_accumulator<PAIR_HALF, PAIR_TILE, PAIR_TILE>(
           tmem + lane_base + static_cast<uint32_t>(b * PAIR_TILE), w, q, lane, ep,
-          sched.partial, static_cast<int>(rank) * PAIR_HALF);
+          sched.partial, epi_square, static_cast<int>(rank) * PAIR_HALF);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty_even + 8u * static_cast<uint32_t>(b));
@@ -804,6 +817,15 @@ namespace {
 // scheduled as the packer's retire and set up their barriers and tensor
 // memory, then wait for the packed operands (griddepcontrol.wait).  The
 // arguments are passed by address in declaration order.
+// Shared memory to launch a kernel with: its staging squares only when the
+// epilogue uses them.  The 3xTF32 epilogue stages only rows of C that are
+// not float4-aligned: otherwise the kernel stays small enough (193 KB) to
+// share an SM with a packer CTA (33 KB), so its CTAs are placed while the
+// packers run (1024^3 32.7 us, against 34.6 us staged).
+inline int epilogue_smem(int smem_bytes, const tc::Epilogue& ep) {
+  return ep.staged ? smem_bytes : smem_bytes - tc::EPI_STAGE_BYTES;
+}
+
 template <class... Args>
 cudaError_t launch_after_pack(const void* kernel, dim3 grid, int threads, int smem_bytes,
                               int cluster, cudaStream_t stream, Args... args) {
@@ -881,10 +903,10 @@ struct Cfg {
     const int grid = persistent_grid(a, units, max_ctas);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const Epilogue ep = make_epilogue(a, vec_c, tiles, BM, BN);
+    const Epilogue ep = make_epilogue(a, vec_c, tiles, BM, BN, !vec_c);
     e = launch_after_pack(reinterpret_cast<const void*>(tf32x3_gemm_kernel<G>), dim3(grid),
-                          THREADS, G::SMEM_BYTES, 1, stream, Ap, Bp, ep, kt, mt, nt,
-                          a.group_m, sched, fault_inject);
+                          THREADS, epilogue_smem(G::SMEM_BYTES, ep), 1, stream, Ap, Bp, ep,
+                          kt, mt, nt, a.group_m, sched, fault_inject);
     if (e != cudaSuccess) return e;
     return launch_second_pass(a, sched.partial, BM, BN, kt, vec_c, stream);
   }
@@ -966,10 +988,11 @@ struct CfgPair {
                                                 CfgPair::workspace(a.M, a.N, a.K));
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int clusters = persistent_grid(a, units, max_clusters);
-    const Epilogue ep = make_epilogue(a, vec_c, tiles, PAIR_TILE, PAIR_TILE);
+    const Epilogue ep = make_epilogue(a, vec_c, tiles, PAIR_TILE, PAIR_TILE, !vec_c);
     e = launch_after_pack(reinterpret_cast<const void*>(tf32x3_pair_kernel<BK>),
-                          dim3(2 * clusters), THREADS, G::SMEM_BYTES, 2, stream, map_a, map_b,
-                          ep, kt, mt, nt, a.group_m, sched, fault_inject);
+                          dim3(2 * clusters), THREADS, epilogue_smem(G::SMEM_BYTES, ep), 2,
+                          stream, map_a, map_b, ep, kt, mt, nt, a.group_m, sched,
+                          fault_inject);
     if (e != cudaSuccess) return e;
     return launch_second_pass(a, sched.partial, PAIR_TILE, PAIR_TILE, kt, vec_c, stream);
   }
@@ -1017,9 +1040,10 @@ struct CfgASplit {
                                                 CfgASplit::workspace(a.M, a.N, a.K));
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int grid = persistent_grid(a, units, max_ctas);
-    const Epilogue ep = make_epilogue(a, vec_c, tiles, BM, BN);
+    const Epilogue ep = make_epilogue(a, vec_c, tiles, BM, BN, !vec_c);
     e = launch_after_pack(reinterpret_cast<const void*>(tf32x3_asplit_kernel<BK, BN>),
-                          dim3(grid), ASPLIT_THREADS, AG::SMEM_BYTES, 1, stream, map_a,
+                          dim3(grid), ASPLIT_THREADS, epilogue_smem(AG::SMEM_BYTES, ep), 1,
+                          stream, map_a,
                           static_cast<const float*>(Bp), ep, kt, mt, nt, a.group_m, sched,
                           fault_inject);
     if (e != cudaSuccess) return e;
