@@ -817,15 +817,6 @@ namespace {
 // scheduled as the packer's retire and set up their barriers and tensor
 // memory, then wait for the packed operands (griddepcontrol.wait).  The
 // arguments are passed by address in declaration order.
-// Shared memory to launch a kernel with: its staging squares only when the
-// epilogue uses them.  The 3xTF32 epilogue stages only rows of C that are
-// not float4-aligned: otherwise the kernel stays small enough (193 KB) to
-// share an SM with a packer CTA (33 KB), so its CTAs are placed while the
-// packers run (1024^3 32.7 us, against 34.6 us staged).
-inline int epilogue_smem(int smem_bytes, const tc::Epilogue& ep) {
-  return ep.staged ? smem_bytes : smem_bytes - tc::EPI_STAGE_BYTES;
-}
-
 template <class... Args>
 cudaError_t launch_after_pack(const void* kernel, dim3 grid, int threads, int smem_bytes,
                               int cluster, cudaStream_t stream, Args... args) {
@@ -903,6 +894,10 @@ struct Cfg {
     const int grid = persistent_grid(a, units, max_ctas);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    // The staged epilogue only for rows of C that are not float4-aligned:
+    // otherwise the kernel stays small enough (193 KB) to share an SM with a
+    // packer CTA (33 KB), so its CTAs are placed while the packers run
+    // (1024^3 back to back 32.7 us, against 34.6 us staged).
     const Epilogue ep = make_epilogue(a, vec_c, tiles, BM, BN, !vec_c);
     e = launch_after_pack(reinterpret_cast<const void*>(tf32x3_gemm_kernel<G>), dim3(grid),
                           THREADS, epilogue_smem(G::SMEM_BYTES, ep), 1, stream, Ap, Bp, ep,
@@ -988,7 +983,7 @@ struct CfgPair {
                                                 CfgPair::workspace(a.M, a.N, a.K));
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int clusters = persistent_grid(a, units, max_clusters);
-    const Epilogue ep = make_epilogue(a, vec_c, tiles, PAIR_TILE, PAIR_TILE, !vec_c);
+    const Epilogue ep = make_epilogue(a, vec_c, tiles, PAIR_TILE, PAIR_TILE, !vec_c);  // as above
     e = launch_after_pack(reinterpret_cast<const void*>(tf32x3_pair_kernel<BK>),
                           dim3(2 * clusters), THREADS, epilogue_smem(G::SMEM_BYTES, ep), 2,
                           stream, map_a, map_b, ep, kt, mt, nt, a.group_m, sched,
@@ -1040,7 +1035,7 @@ struct CfgASplit {
                                                 CfgASplit::workspace(a.M, a.N, a.K));
     const int units = a.full_tiles + (tiles - a.full_tiles) * a.split;
     const int grid = persistent_grid(a, units, max_ctas);
-    const Epilogue ep = make_epilogue(a, vec_c, tiles, BM, BN, !vec_c);
+    const Epilogue ep = make_epilogue(a, vec_c, tiles, BM, BN, !vec_c);  // as above
     e = launch_after_pack(reinterpret_cast<const void*>(tf32x3_asplit_kernel<BK, BN>),
                           dim3(grid), ASPLIT_THREADS, epilogue_smem(AG::SMEM_BYTES, ep), 1,
                           stream, map_a,

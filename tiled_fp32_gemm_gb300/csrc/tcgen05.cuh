@@ -401,6 +401,14 @@ __device__ __forceinline__ Unit unit_at(int j, int c, int ctas, const Sched& sc,
   return unit_of(c + j * ctas, sc, tiles_m, tiles_n, group_m, Kt);
 }
 
+// Each epilogue warp's 32 x 32 staging square in shared memory: with a row
+// stride of 33 words a warp's row-wise writes (lane l writes row l) and its
+// column-wise reads (lane l reads column l) each fall on 32 distinct banks.
+constexpr int EPI_STRIDE = 33;
+constexpr int EPI_WARP_FLOATS = 32 * EPI_STRIDE;
+// The squares of a CTA's four epilogue warps.
+constexpr int EPI_STAGE_BYTES = 4 * EPI_WARP_FLOATS * 4;
+
 // The C update of a tile, shared by the epilogues.
 struct Epilogue {
   float* C;
@@ -419,6 +427,12 @@ struct Epilogue {
   BoundsRecord* bounds = nullptr;
 };
 
+// Shared memory to launch a kernel of `smem_bytes` (its staging squares
+// included) with: the squares only when the epilogue uses them.
+inline int epilogue_smem(int smem_bytes, const Epilogue& ep) {
+  return ep.staged ? smem_bytes : smem_bytes - EPI_STAGE_BYTES;
+}
+
 // The epilogue of a call: C's view, and the split tail's partial tiles
 // (one dense tile_m x bn tile per slice of each split tile).
 inline Epilogue make_epilogue(const GemmArgs& a, bool vec_c, int tiles, int tile_m, int bn,
@@ -433,13 +447,6 @@ inline Epilogue make_epilogue(const GemmArgs& a, bool vec_c, int tiles, int tile
   return ep;
 }
 
-// Each epilogue warp's 32 x 32 staging square in shared memory: with a row
-// stride of 33 words a warp's row-wise writes (lane l writes row l) and its
-// column-wise reads (lane l reads column l) each fall on 32 distinct banks.
-constexpr int EPI_STRIDE = 33;
-constexpr int EPI_WARP_FLOATS = 32 * EPI_STRIDE;
-// The squares of a CTA's four epilogue warps.
-constexpr int EPI_STAGE_BYTES = 4 * EPI_WARP_FLOATS * 4;
 
 // Drains this warp's 32 TMEM lanes -- rows q*32 .. q*32+31 of the BM x BN
 // accumulator whose first column of this warp's lanes is TMEM address
@@ -471,25 +478,35 @@ __device__ __forceinline__ void store_accumulator(uint32_t t_row, const Unit& w,
 #pragma unroll
       for (int i = 0; i < 32; ++i) stage[lane * EPI_STRIDE + i] = v[i];
       __syncwarp();
+      // Column `lane` of the chunk, all 32 reads in flight at once.
+#pragma unroll
+      for (int r = 0; r < 32; ++r) v[r] = stage[r * EPI_STRIDE + lane];
       const int col = w.tn * BN + ch * 32 + lane;  // this lane's column of C
       if (w.pidx >= 0) {
         float* p = partial + static_cast<int64_t>(w.pidx) * (TILE_M * BN) +
                    static_cast<int64_t>(r0) * BN + ch * 32 + lane;
-#pragma unroll 4
-        for (int r = 0; r < 32; ++r)
-          if (bounds_ok(ep.bounds, SITE_PARTIAL, (p - partial) + r * BN, 1, ep.partial_extent))
-            p[r * BN] = stage[r * EPI_STRIDE + lane];
+#pragma unroll
+        for (int r = 0; r < 32; ++r, p += BN)
+          if (bounds_ok(ep.bounds, SITE_PARTIAL, p - partial, 1, ep.partial_extent)) *p = v[r];
       } else if (col < ep.N && (!ep.bias || bounds_ok(ep.bounds, SITE_BIAS, col, 1, ep.N))) {
         const float bias_c = ep.bias ? ep.bias[col] : 0.0f;
         float* cp = ep.C + static_cast<int64_t>(row0) * ep.ldc + col;
         const int rows = min(32, ep.M - row0);
+        if (ep.beta == 0.0f) {
+#pragma unroll
+          for (int r = 0; r < 32; ++r, cp += ep.ldc)
+            if (r < rows && bounds_ok(ep.bounds, SITE_C_STORE, cp - ep.C, 1, ep.c_extent))
+              *cp = ep.bias ? ep.alpha * v[r] + bias_c : ep.alpha * v[r];
+        } else {
+          // C is read too: row by row from the square, which is rewritten
+          // only after the barrier below.
 #pragma unroll 4
-        for (int r = 0; r < rows; ++r, cp += ep.ldc) {
-          if (!bounds_ok(ep.bounds, SITE_C_STORE, cp - ep.C, 1, ep.c_extent)) continue;
-          float o = ep.alpha * stage[r * EPI_STRIDE + lane];
-          if (ep.beta != 0.0f) o = fmaf(ep.beta, *cp, o);
-          if (ep.bias) o += bias_c;
-          *cp = o;
+          for (int r = 0; r < rows; ++r, cp += ep.ldc) {
+            if (!bounds_ok(ep.bounds, SITE_C_STORE, cp - ep.C, 1, ep.c_extent)) continue;
+            float o = fmaf(ep.beta, *cp, ep.alpha * stage[r * EPI_STRIDE + lane]);
+            if (ep.bias) o += bias_c;
+            *cp = o;
+          }
         }
       }
       __syncwarp();  // the square is read before the next chunk is written
