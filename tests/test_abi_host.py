@@ -277,6 +277,30 @@ def test_ffma_kmajor_gather_unpadded_would_conflict():
     assert R.conflict_degree(addrs, 4) == 8
 
 
+def test_tensor_core_epilogue_square_is_conflict_free():
+    """The tensor-core epilogue's staging square (tcgen05.cuh): lane l
+    writes row l of a 32 x 32 chunk one element at a time, then reads
+    column l one row at a time.  With the row stride the kernels use both
+    patterns hit 32 banks; with 32 words (no padding) the row-wise writes
+    would all fall in one bank, as the pages' rule predicts for 32 rows
+    read at one column."""
+    text = open(os.path.join(ROOT, "tiled_fp32_gemm_gb300", "csrc", "tcgen05.cuh")).read()
+    stride = int(re.search(r"constexpr int EPI_STRIDE = (\d+);", text).group(1))
+    assert stride == 32 + R.row_padding(32, 32)
+
+    def writes(st, i):
+        return [4 * (lane * st + i) for lane in range(32)]
+
+    def reads(st, r):
+        return [4 * (r * st + lane) for lane in range(32)]
+
+    for k in range(32):
+        assert R.conflict_degree(writes(stride, k), 4) == 1
+        assert R.conflict_degree(reads(stride, k), 4) == 1
+        assert R.conflict_degree(writes(32, k), 4) == 32
+        assert R.conflict_degree(reads(32, k), 4) == 1
+
+
 @pytest.mark.parametrize("shape,trans_a,want", [
     ((4096, 4096, 4096), False, 5),   # large N: transposing copy of A
     ((65536, 128, 4096), False, 4),   # narrow N: gathered inside the kernel
